@@ -1,0 +1,275 @@
+/*
+ * attn_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * Plain, slow, fp64, two-pass CPU oracle for bottom-right-causal grouped-query
+ * attention.  Only the test suite, the smoke check and the benchmark's CPU
+ * baseline leg call it; the product library never links it, and it shares no
+ * code, header or table with the CUDA kernels.
+ *
+ * What it computes (restated from the pages, not copied):
+ *   "Attention execution mapping: 现状、缺口与有界实验" (LuisaCompute), §1:
+ *     the fixture is bottom-right-causal GQA; query head h reads KV head
+ *     kh = h / (Hq / Hkv); a key k is legal for query row q iff
+ *     k <= q + K - Q; one online-softmax program covers prefill and decode.
+ *   Same page, §2 (phase graph): QK contracts over d, a mask, then
+ *     max -> exp -> sum, then PV contracts over the key axis.
+ *   "快速後端" (Laya fast backends), "數值校驗": sliding window, per-sequence
+ *     (int32) lengths, empty sequences and finite padded output are covered.
+ *
+ * The online method (running max / sum / accumulator carried across KV
+ * blocks) reaches, in exact arithmetic, the plain softmax definition below, so
+ * the oracle is that definition written out -- no blocking, no online update:
+ *
+ *   for every sequence b, query head h, valid query row q < Qb:
+ *     kh  = h / (Hq / Hkv)
+ *     L   = { k : 0 <= k < Kb, k <= q + Kb - Qb,
+ *                 and (window <= 0 or k >= q + Kb - Qb - window + 1) }
+ *     if L is empty:   O[q,h,:] = +0,  LSE[q,h] = -inf
+ *     else:  s_k = scale * sum_d Q[q,h,d] * K[k,kh,d]        (fp64)
+ *            pass 1: m = max_{k in L} s_k
+ *            pass 2: l = sum_{k in L} exp(s_k - m)
+ *                    O[q,h,j] = sum_{k in L} exp(s_k - m) * V[k,kh,j] / l
+ *            LSE[q,h] = m + log(l)                         (natural log)
+ *   padded rows q >= Qb: O = +0, LSE = -inf.
+ *
+ * Readings where the pages are silent: a window w > 0 keeps the w most recent
+ * keys including the diagonal one; rows with no legal key give +0 / -inf; the
+ * LSE is in natural log.
+ *
+ * Inputs are float32 arrays holding exactly the values the device sees
+ * (bf16 / fp16 / fp32 values are all exact in float32); every product and sum
+ * is taken in double.  Layouts:
+ *   padded: q [B,Q,Hq,D]  k [B,K,Hkv,D]  v [B,K,Hkv,Dv]  o [B,Q,Hq,Dv]  lse [B,Q,Hq]
+ *   packed: q [Tq,Hq,D]   k [Tk,Hkv,D]   v [Tk,Hkv,Dv]   o [Tq,Hq,Dv]   lse [Tq,Hq]
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* One (sequence, head, query-row) of the definition above.  qrow points at
+ * Q[q,h,0]; kbase/vbase point at key row 0 of this sequence and KV head; the
+ * key stride is the element distance between consecutive key rows. */
+static void oracle_row(const float *qrow, const float *kbase, const float *vbase,
+                       long kstride, long vstride, int D, int Dv, int q, int Qb,
+                       int Kb, int window, double scale, double *s_scratch,
+                       double *orow, double *lse_out)
+{
+    const long diag = (long)q + Kb - Qb;              /* last legal key */
+    long lo = 0, hi = diag;                            /* inclusive bounds */
+    if (window > 0 && diag - window + 1 > lo) lo = diag - window + 1;
+    if (hi > (long)Kb - 1) hi = (long)Kb - 1;
+    for (int j = 0; j < Dv; ++j) orow[j] = 0.0;
+    if (hi < lo) { *lse_out = -INFINITY; return; }
+
+    /* scores of the legal keys, and pass 1: their maximum */
+    double m = -INFINITY;
+    for (long k = lo; k <= hi; ++k) {
+        const float *krow = kbase + k * kstride;
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d) acc += (double)qrow[d] * (double)krow[d];
+        const double s = scale * acc;
+        s_scratch[k - lo] = s;
+        if (s > m) m = s;
+    }
+    /* pass 2: normaliser and weighted sum of V rows */
+    double l = 0.0;
+    for (long k = lo; k <= hi; ++k) {
+        const double p = exp(s_scratch[k - lo] - m);
+        l += p;
+        const float *vrow = vbase + k * vstride;
+        for (int j = 0; j < Dv; ++j) orow[j] += p * (double)vrow[j];
+    }
+    for (int j = 0; j < Dv; ++j) orow[j] /= l;
+    *lse_out = m + log(l);
+}
+
+/* A per-sequence length outside [0, cap] is clamped into it (the padded
+ * layout holds at most cap rows per sequence). */
+static int clamp_len(int n, int cap)
+{
+    return n < 0 ? 0 : (n > cap ? cap : n);
+}
+
+static int check_dims(int B, int Hq, int Hkv, int D, int Dv)
+{
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Dv <= 0) return 1;
+    if (Hq % Hkv != 0) return 1;
+    return 0;
+}
+
+/* Padded layout.  seqlens_q / seqlens_k may be NULL (= all Q / all K). */
+int oracle_attn_padded(const float *q, const float *k, const float *v, double *o,
+                       double *lse, int B, int Hq, int Hkv, int Q, int K, int D,
+                       int Dv, const int32_t *seqlens_q, const int32_t *seqlens_k,
+                       int window, double scale, int nthreads)
+{
+    if (check_dims(B, Hq, Hkv, D, Dv) || Q < 0 || K < 0) return 1;
+    const int G = Hq / Hkv;
+    const long nrows = (long)B * Q * Hq;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+        if (!s) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (long r = 0; r < nrows; ++r) {
+            if (!s) continue;
+            const int h = (int)(r % Hq);
+            const int qi = (int)((r / Hq) % Q);
+            const int b = (int)(r / ((long)Hq * Q));
+            const int Qb = clamp_len(seqlens_q ? seqlens_q[b] : Q, Q);
+            const int Kb = clamp_len(seqlens_k ? seqlens_k[b] : K, K);
+            double *orow = o + r * Dv;
+            if (qi >= Qb) {
+                for (int j = 0; j < Dv; ++j) orow[j] = 0.0;
+                lse[r] = -INFINITY;
+                continue;
+            }
+            const int kh = h / G;
+            oracle_row(q + r * D, k + ((long)b * K * Hkv + kh) * D,
+                       v + ((long)b * K * Hkv + kh) * Dv, (long)Hkv * D,
+                       (long)Hkv * Dv, D, Dv, qi, Qb, Kb, window, scale, s, orow,
+                       &lse[r]);
+        }
+        free(s);
+    }
+    return bad ? 3 : 0;
+}
+
+/* Packed (varlen) layout: sequence b owns query rows [cu_q[b], cu_q[b+1]) and
+ * key rows [cu_k[b], cu_k[b+1]). */
+int oracle_attn_packed(const float *q, const float *k, const float *v, double *o,
+                       double *lse, int B, int Hq, int Hkv, int D, int Dv,
+                       const int32_t *cu_q, const int32_t *cu_k, int window,
+                       double scale, int nthreads)
+{
+    if (check_dims(B, Hq, Hkv, D, Dv) || !cu_q || !cu_k) return 1;
+    if (cu_q[0] != 0 || cu_k[0] != 0) return 1;
+    for (int b = 0; b < B; ++b)
+        if (cu_q[b + 1] < cu_q[b] || cu_k[b + 1] < cu_k[b]) return 1;
+    const int G = Hq / Hkv;
+    const long Tq = cu_q[B];
+    long maxK = 1;
+    for (int b = 0; b < B; ++b)
+        if (cu_k[b + 1] - cu_k[b] > maxK) maxK = cu_k[b + 1] - cu_k[b];
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)maxK);
+        if (!s) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (long r = 0; r < Tq * Hq; ++r) {
+            if (!s) continue;
+            const int h = (int)(r % Hq);
+            const long t = r / Hq;
+            int b = 0;
+            while (b + 1 < B && cu_q[b + 1] <= t) ++b;
+            const int Qb = cu_q[b + 1] - cu_q[b];
+            const int Kb = cu_k[b + 1] - cu_k[b];
+            const int qi = (int)(t - cu_q[b]);
+            const int kh = h / G;
+            oracle_row(q + r * D, k + ((long)cu_k[b] * Hkv + kh) * D,
+                       v + ((long)cu_k[b] * Hkv + kh) * Dv, (long)Hkv * D,
+                       (long)Hkv * Dv, D, Dv, qi, Qb, Kb, window, scale, s,
+                       o + r * Dv, &lse[r]);
+        }
+        free(s);
+    }
+    return bad ? 3 : 0;
+}
+
+/* Selected rows of the padded layout, for sampled checks at full size:
+ * row i is (rb[i], rq[i], rh[i]); o_rows is [n, Dv], lse_rows [n]. */
+int oracle_attn_padded_rows(const float *q, const float *k, const float *v,
+                            int B, int Hq, int Hkv, int Q, int K, int D, int Dv,
+                            const int32_t *seqlens_q, const int32_t *seqlens_k,
+                            int window, double scale, const int32_t *rb,
+                            const int32_t *rq, const int32_t *rh, long n,
+                            double *o_rows, double *lse_rows, int nthreads)
+{
+    if (check_dims(B, Hq, Hkv, D, Dv) || Q < 0 || K < 0) return 1;
+    for (long i = 0; i < n; ++i)
+        if (rb[i] < 0 || rb[i] >= B || rq[i] < 0 || rq[i] >= Q || rh[i] < 0 ||
+            rh[i] >= Hq)
+            return 1;
+    const int G = Hq / Hkv;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+        if (!s) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(dynamic, 4)
+        for (long i = 0; i < n; ++i) {
+            if (!s) continue;
+            const int b = rb[i], qi = rq[i], h = rh[i];
+            const int Qb = clamp_len(seqlens_q ? seqlens_q[b] : Q, Q);
+            const int Kb = clamp_len(seqlens_k ? seqlens_k[b] : K, K);
+            double *orow = o_rows + i * Dv;
+            if (qi >= Qb) {
+                for (int j = 0; j < Dv; ++j) orow[j] = 0.0;
+                lse_rows[i] = -INFINITY;
+                continue;
+            }
+            const long r = ((long)b * Q + qi) * Hq + h;
+            const int kh = h / G;
+            oracle_row(q + r * D, k + ((long)b * K * Hkv + kh) * D,
+                       v + ((long)b * K * Hkv + kh) * Dv, (long)Hkv * D,
+                       (long)Hkv * Dv, D, Dv, qi, Qb, Kb, window, scale, s, orow,
+                       &lse_rows[i]);
+        }
+        free(s);
+    }
+    return bad ? 3 : 0;
+}
+
+/* Number of legal (query, key) pairs of one sequence, per head: the unit the
+ * throughput figures count (FLOP = pairs * (2D + 2Dv) per head). */
+long long oracle_legal_pairs(int Qb, int Kb, int window)
+{
+    long long n = 0;
+    for (int q = 0; q < Qb; ++q) {
+        long diag = (long)q + Kb - Qb;
+        long lo = 0, hi = diag;
+        if (window > 0 && diag - window + 1 > lo) lo = diag - window + 1;
+        if (hi > (long)Kb - 1) hi = (long)Kb - 1;
+        if (hi >= lo) n += hi - lo + 1;
+    }
+    return n;
+}
+
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

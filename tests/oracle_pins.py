@@ -1,0 +1,310 @@
+"""Checks that pin the CPU oracle to facts outside itself.
+
+Each ``pin_*`` function takes an ``oracle.OracleLib`` and raises
+AssertionError when the oracle disagrees with:
+
+* hand-derived closed forms (``tests/golden/*.json``, each citing its passage);
+* ``torch.nn.functional.scaled_dot_product_attention`` in fp64 with a boolean
+  mask built by ``numpy.tril`` / ``numpy.triu`` (a library routine and a mask
+  construction independent of the oracle's explicit key enumeration);
+* invariants the definition fixes (constant V, a single legal key, identical
+  keys, probabilities summing to one, empty rows, window >= K, scale 0,
+  MHA/MQA equivalence, thread-count invariance).
+
+``tests/test_oracle.py`` runs them against the real oracle and
+``tests/test_oracle_mutants.py`` checks that every planted mistake in a copy
+of the oracle fails at least one of them.
+"""
+from __future__ import annotations
+
+import glob
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+GOLDEN_DIR = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ---------------------------------------------------------------------------
+# helpers
+
+def parse_value(s) -> float:
+    """A fixture scalar: a number, "a/b", "log(n)" or "-inf"."""
+    if isinstance(s, (int, float)):
+        return float(s)
+    s = s.strip()
+    if s == "-inf":
+        return -math.inf
+    if s.startswith("log(") and s.endswith(")"):
+        return math.log(float(Fraction(s[4:-1])))
+    return float(Fraction(s))
+
+
+def parse_array(a) -> np.ndarray:
+    return np.vectorize(parse_value, otypes=[np.float64])(np.array(a, dtype=object))
+
+
+def golden_files():
+    return sorted(glob.glob(os.path.join(GOLDEN_DIR, "*.json")))
+
+
+def mask_matrix(Qb: int, Kb: int, window: int) -> np.ndarray:
+    """Legal-key mask built from numpy's triangle routines: np.tril keeps
+    j - i <= Kb - Qb (bottom-right causal), np.triu keeps the window."""
+    m = np.tril(np.ones((Qb, Kb), dtype=bool), k=Kb - Qb)
+    if window > 0:
+        m &= np.triu(np.ones((Qb, Kb), dtype=bool), k=Kb - Qb - window + 1)
+    return m
+
+
+def sdpa_reference(q, k, v, Qb, Kb, Hq, Hkv, window, scale):
+    """fp64 torch SDPA with an explicit boolean mask for one sequence.
+
+    q [Qb,Hq,D], k [Kb,Hkv,D], v [Kb,Hkv,Dv] float arrays.  Returns
+    (o [Qb,Hq,Dv], lse [Qb,Hq], has_key [Qb]) with o/lse only meaningful where
+    the row has a legal key.  KV heads are expanded with repeat_interleave,
+    which maps query head h to KV head h // (Hq/Hkv)."""
+    G = Hq // Hkv
+    qt = torch.from_numpy(np.asarray(q, np.float64)).permute(1, 0, 2)       # [Hq,Qb,D]
+    kt = torch.from_numpy(np.asarray(k, np.float64)).permute(1, 0, 2).repeat_interleave(G, 0)
+    vt = torch.from_numpy(np.asarray(v, np.float64)).permute(1, 0, 2).repeat_interleave(G, 0)
+    m = mask_matrix(Qb, Kb, window)
+    has = m.any(axis=1)
+    mt = torch.from_numpy(m)
+    safe = mt.clone()
+    safe[~torch.from_numpy(has)] = True      # keep SDPA finite on rows we ignore
+    o = torch.nn.functional.scaled_dot_product_attention(
+        qt.unsqueeze(0), kt.unsqueeze(0), vt.unsqueeze(0), attn_mask=safe, scale=scale)[0]
+    s = torch.matmul(qt, kt.transpose(1, 2)) * scale
+    s = s.masked_fill(~mt, -math.inf)
+    lse = torch.logsumexp(s, dim=-1)
+    return o.permute(1, 0, 2).numpy(), lse.permute(1, 0).numpy(), has
+
+
+def rng_inputs(seed, B, Hq, Hkv, Q, K, D, Dv):
+    g = np.random.default_rng(seed)
+    q = g.standard_normal((B, Q, Hq, D)).astype(np.float32)
+    k = g.standard_normal((B, K, Hkv, D)).astype(np.float32)
+    v = g.standard_normal((B, K, Hkv, Dv)).astype(np.float32)
+    return q, k, v
+
+
+# ---------------------------------------------------------------------------
+# pins
+
+def pin_golden(ol):
+    files = golden_files()
+    assert files, "no golden fixtures found"
+    for path in files:
+        with open(path) as f:
+            g = json.load(f)
+        q = parse_array(g["q"]).astype(np.float32)
+        k = parse_array(g["k"]).astype(np.float32)
+        v = parse_array(g["v"]).astype(np.float32)
+        scale = parse_value(g["scale"])
+        exp_o = parse_array(g["expected_o"])
+        exp_l = parse_array(g["expected_lse"])
+        if g["layout"] == "padded":
+            o, lse = ol.attn_padded(q, k, v, B=g["B"], Hq=g["Hq"], Hkv=g["Hkv"], Q=g["Q"],
+                                    K=g["K"], D=g["D"], Dv=g["Dv"],
+                                    seqlens_q=g.get("seqlens_q"), seqlens_k=g.get("seqlens_k"),
+                                    window=g["window"], scale=scale)
+        else:
+            o, lse = ol.attn_packed(q, k, v, B=g["B"], Hq=g["Hq"], Hkv=g["Hkv"], D=g["D"],
+                                    Dv=g["Dv"], cu_seqlens_q=g["cu_seqlens_q"],
+                                    cu_seqlens_k=g["cu_seqlens_k"], window=g["window"],
+                                    scale=scale)
+        lse = lse.reshape(exp_l.shape)
+        o = o.reshape(exp_o.shape)
+        assert np.allclose(o, exp_o, atol=g["atol"], rtol=0), (g["name"], o, exp_o)
+        fin = np.isfinite(exp_l)
+        assert np.array_equal(np.isfinite(lse), fin), (g["name"], lse, exp_l)
+        assert np.all(lse[~fin] == -math.inf), (g["name"], lse)
+        assert np.allclose(lse[fin], exp_l[fin], atol=g["atol"], rtol=0), (g["name"], lse, exp_l)
+        # rows with no legal key hold +0.0 exactly (sign bit clear)
+        zero_rows = ~fin
+        if zero_rows.any():
+            oz = o[zero_rows]
+            assert np.all(oz == 0.0) and not np.any(np.signbit(oz)), (g["name"], oz)
+
+
+SDPA_CASES = [
+    # B, Hq, Hkv, Q, K, D, Dv, window, seqlens_q, seqlens_k
+    (1, 4, 2, 16, 37, 8, 8, 0, None, None),
+    (2, 6, 3, 9, 9, 5, 7, 0, None, None),
+    (1, 8, 2, 1, 53, 16, 12, 0, None, None),        # decode
+    (2, 4, 1, 13, 40, 8, 8, 5, None, None),         # MQA + window
+    (1, 3, 3, 20, 20, 4, 4, 3, None, None),         # MHA + window
+    (3, 4, 2, 12, 16, 8, 6, 0, [12, 5, 0], [16, 3, 9]),
+    (2, 2, 1, 10, 4, 4, 4, 0, None, None),          # Q > K: leading rows empty
+    (2, 4, 2, 7, 30, 6, 6, 4, [7, 3], [30, 0]),
+]
+
+
+def pin_sdpa(ol):
+    for ci, (B, Hq, Hkv, Q, K, D, Dv, w, sq, sk) in enumerate(SDPA_CASES):
+        q, k, v = rng_inputs(100 + ci, B, Hq, Hkv, Q, K, D, Dv)
+        scale = 1.0 / math.sqrt(D) * (1.0 + 0.25 * ci)
+        o, lse = ol.attn_padded(q, k, v, B=B, Hq=Hq, Hkv=Hkv, Q=Q, K=K, D=D, Dv=Dv,
+                                seqlens_q=sq, seqlens_k=sk, window=w, scale=scale)
+        for b in range(B):
+            Qb = Q if sq is None else sq[b]
+            Kb = K if sk is None else sk[b]
+            # padded rows
+            assert np.all(o[b, Qb:] == 0.0) and np.all(lse[b, Qb:] == -math.inf), (ci, b)
+            if Qb == 0:
+                continue
+            if Kb == 0:
+                assert np.all(o[b, :Qb] == 0.0) and np.all(lse[b, :Qb] == -math.inf), (ci, b)
+                continue
+            ro, rl, has = sdpa_reference(q[b, :Qb], k[b, :Kb], v[b, :Kb], Qb, Kb, Hq, Hkv, w,
+                                         scale)
+            assert np.allclose(o[b, :Qb][has], ro[has], atol=1e-12, rtol=1e-10), (ci, b)
+            assert np.allclose(lse[b, :Qb][has], rl[has], atol=1e-12, rtol=1e-12), (ci, b)
+            assert np.all(o[b, :Qb][~has] == 0.0), (ci, b)
+            assert np.all(lse[b, :Qb][~has] == -math.inf), (ci, b)
+
+
+def pin_invariants(ol):
+    B, Hq, Hkv, Q, K, D, Dv = 2, 4, 2, 11, 19, 8, 5
+    q, k, v = rng_inputs(7, B, Hq, Hkv, Q, K, D, Dv)
+    kw = dict(B=B, Hq=Hq, Hkv=Hkv, Q=Q, K=K, D=D, Dv=Dv)
+    G = Hq // Hkv
+
+    # constant V -> that constant on every row
+    vc = np.full_like(v, 0.375)
+    o, lse = ol.attn_padded(q, k, vc, **kw)
+    assert np.allclose(o, 0.375, atol=1e-14), "constant V"
+
+    # window 1 -> the diagonal key's V row, LSE = its score
+    o, lse = ol.attn_padded(q, k, v, window=1, **kw)
+    scale = 1.0 / math.sqrt(D)
+    for b in range(B):
+        for i in range(Q):
+            kd = i + K - Q
+            for h in range(Hq):
+                assert np.allclose(o[b, i, h], v[b, kd, h // G], atol=1e-14), "single key"
+                s = scale * float(np.dot(q[b, i, h].astype(np.float64), k[b, kd, h // G]))
+                assert abs(lse[b, i, h] - s) < 1e-12, "single key lse"
+
+    # identical keys -> mean of the legal V rows
+    ks = np.broadcast_to(k[:, :1], k.shape).copy()
+    for w in (0, 4):
+        o, lse = ol.attn_padded(q, ks, v, window=w, **kw)
+        m = mask_matrix(Q, K, w)
+        for b in range(B):
+            for i in range(Q):
+                for h in range(Hq):
+                    mean = v[b][m[i], h // G].astype(np.float64).mean(axis=0)
+                    assert np.allclose(o[b, i, h], mean, atol=1e-12), "identical keys"
+
+    # probabilities sum to one: sum_{legal k} exp(s_k - LSE) == 1
+    for w in (0, 6):
+        o, lse = ol.attn_padded(q, k, v, window=w, **kw)
+        m = mask_matrix(Q, K, w)
+        for b in range(B):
+            for h in range(Hq):
+                s = scale * (q[b, :, h].astype(np.float64) @ k[b, :, h // G].astype(np.float64).T)
+                tot = np.where(m, np.exp(s - lse[b, :, h][:, None]), 0.0).sum(axis=1)
+                assert np.allclose(tot, 1.0, atol=1e-12), "sum p = 1"
+
+    # scale 0 -> uniform weights -> mean of legal V rows, LSE = ln(#legal)
+    o, lse = ol.attn_padded(q, k, v, scale=0.0, window=3, **kw)
+    m = mask_matrix(Q, K, 3)
+    for b in range(B):
+        for i in range(Q):
+            for h in range(Hq):
+                mean = v[b][m[i], h // G].astype(np.float64).mean(axis=0)
+                assert np.allclose(o[b, i, h], mean, atol=1e-12), "scale 0"
+                assert abs(lse[b, i, h] - math.log(m[i].sum())) < 1e-12, "scale 0 lse"
+
+    # window >= K is the same as no window
+    o0, l0 = ol.attn_padded(q, k, v, window=0, **kw)
+    o1, l1 = ol.attn_padded(q, k, v, window=K, **kw)
+    o2, l2 = ol.attn_padded(q, k, v, window=K + 100, **kw)
+    assert np.array_equal(o0, o1) and np.array_equal(o0, o2), "window >= K"
+    assert np.array_equal(l0, l1) and np.array_equal(l0, l2), "window >= K lse"
+
+    # GQA == MHA with every KV head repeated G times (numpy.repeat)
+    kr = np.repeat(k, G, axis=2)
+    vr = np.repeat(v, G, axis=2)
+    om, lm = ol.attn_padded(q, kr, vr, B=B, Hq=Hq, Hkv=Hq, Q=Q, K=K, D=D, Dv=Dv)
+    assert np.array_equal(o0, om) and np.array_equal(l0, lm), "GQA == MHA"
+    # MQA: a single KV head
+    o_mqa, _ = ol.attn_padded(q, k[:, :, :1].copy(), v[:, :, :1].copy(), B=B, Hq=Hq, Hkv=1,
+                              Q=Q, K=K, D=D, Dv=Dv)
+    om2, _ = ol.attn_padded(q, np.repeat(k[:, :, :1], Hq, axis=2), np.repeat(v[:, :, :1], Hq, axis=2),
+                            B=B, Hq=Hq, Hkv=Hq, Q=Q, K=K, D=D, Dv=Dv)
+    assert np.array_equal(o_mqa, om2), "MQA == MHA"
+
+    # empty KV (Kb = 0) and Q > K leading rows: +0 and -inf exactly
+    o, lse = ol.attn_padded(q, k, v, seqlens_k=[0, 3], **kw)
+    assert np.all(o[0] == 0.0) and not np.any(np.signbit(o[0])) and np.all(lse[0] == -math.inf)
+    # sequence 1 has Qb = 11 > Kb = 3: rows 0..7 have no legal key
+    assert np.all(o[1, :8] == 0.0) and np.all(lse[1, :8] == -math.inf), "Q > K rows"
+    assert np.all(np.isfinite(lse[1, 8:])), "Q > K rows with keys"
+
+    # thread count does not change a single bit
+    oa, la = ol.attn_padded(q, k, v, window=5, nthreads=1, **kw)
+    ob, lb = ol.attn_padded(q, k, v, window=5, nthreads=4, **kw)
+    assert np.array_equal(oa, ob) and np.array_equal(la, lb), "thread invariance"
+
+
+def pin_packed_matches_padded(ol):
+    Hq, Hkv, D, Dv = 4, 2, 8, 6
+    sq = np.array([5, 0, 3, 9, 1], np.int32)
+    sk = np.array([5, 4, 0, 12, 7], np.int32)
+    cq = np.concatenate([[0], np.cumsum(sq)]).astype(np.int32)
+    ck = np.concatenate([[0], np.cumsum(sk)]).astype(np.int32)
+    g = np.random.default_rng(11)
+    q = g.standard_normal((cq[-1], Hq, D)).astype(np.float32)
+    k = g.standard_normal((ck[-1], Hkv, D)).astype(np.float32)
+    v = g.standard_normal((ck[-1], Hkv, Dv)).astype(np.float32)
+    for w in (0, 3):
+        o, lse = ol.attn_packed(q, k, v, B=sq.size, Hq=Hq, Hkv=Hkv, D=D, Dv=Dv,
+                                cu_seqlens_q=cq, cu_seqlens_k=ck, window=w)
+        for b in range(sq.size):
+            Qb, Kb = int(sq[b]), int(sk[b])
+            if Qb == 0:
+                continue
+            if Kb == 0:
+                assert np.all(o[cq[b]:cq[b + 1]] == 0.0)
+                assert np.all(lse[cq[b]:cq[b + 1]] == -math.inf)
+                continue
+            ro, rl, has = sdpa_reference(q[cq[b]:cq[b + 1]], k[ck[b]:ck[b + 1]],
+                                         v[ck[b]:ck[b + 1]], Qb, Kb, Hq, Hkv, w,
+                                         1.0 / math.sqrt(D))
+            ob, lb = o[cq[b]:cq[b + 1]], lse[cq[b]:cq[b + 1]]
+            assert np.allclose(ob[has], ro[has], atol=1e-12), ("packed", b)
+            assert np.allclose(lb[has], rl[has], atol=1e-12), ("packed lse", b)
+            assert np.all(ob[~has] == 0.0) and np.all(lb[~has] == -math.inf)
+
+
+def pin_rows_match_full(ol):
+    B, Hq, Hkv, Q, K, D, Dv = 2, 4, 2, 9, 14, 8, 8
+    q, k, v = rng_inputs(5, B, Hq, Hkv, Q, K, D, Dv)
+    kw = dict(B=B, Hq=Hq, Hkv=Hkv, Q=Q, K=K, D=D, Dv=Dv, seqlens_q=[9, 4], seqlens_k=[14, 2],
+              window=5)
+    o, lse = ol.attn_padded(q, k, v, **kw)
+    rows = np.array([[0, 0, 0], [0, 8, 3], [1, 3, 1], [1, 6, 2], [0, 4, 2]], np.int32)
+    ro, rl = ol.attn_padded_rows(q, k, v, rows, **kw)
+    for i, (b, qi, h) in enumerate(rows):
+        assert np.array_equal(ro[i], o[b, qi, h]) and rl[i] == lse[b, qi, h], ("rows", i)
+
+
+def pin_legal_pairs(ol):
+    for (Qb, Kb, w) in [(4096, 4096, 0), (1, 8192, 0), (512, 4000, 1024), (3, 1, 0),
+                        (0, 5, 0), (7, 0, 0), (10, 20, 3), (64, 128, 0)]:
+        n = int(mask_matrix(Qb, Kb, w).sum()) if Qb * Kb <= 4096 * 4096 else None
+        got = ol.legal_pairs(Qb, Kb, w)
+        if n is not None:
+            assert got == n, ("pairs", Qb, Kb, w, got, n)
+    assert ol.legal_pairs(4096, 4096, 0) == 4096 * 4097 // 2
+
+
+ALL_PINS = [pin_golden, pin_sdpa, pin_invariants, pin_packed_matches_padded,
+            pin_rows_match_full, pin_legal_pairs]

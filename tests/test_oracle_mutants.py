@@ -1,0 +1,53 @@
+"""Plant plausible mistakes in a copy of the oracle and check that the pins
+catch every one.  The mutants are compiled from text substitutions of
+``oracle/attn_oracle.c`` into a temporary directory; the real oracle is not
+touched.  CPU only."""
+import os
+
+import pytest
+
+import oracle
+from tests import oracle_pins as pins
+
+# (name, original text, mutated text)
+MUTANTS = [
+    ("causal_off_by_one", "const long diag = (long)q + Kb - Qb;",
+     "const long diag = (long)q + Kb - Qb - 1;"),
+    ("top_left_causal", "const long diag = (long)q + Kb - Qb;", "const long diag = (long)q;"),
+    ("head_map_modulo", "const int kh = h / G;", "const int kh = h % Hkv;"),
+    ("window_one_wider", "diag - window + 1 > lo) lo = diag - window + 1;",
+     "diag - window > lo) lo = diag - window;"),
+    ("scale_dropped", "const double s = scale * acc;", "const double s = acc;"),
+    ("lse_without_max", "*lse_out = m + log(l);", "*lse_out = log(l);"),
+    ("lse_base2", "*lse_out = m + log(l);", "*lse_out = m + log2(l);"),
+    ("no_normalisation", "orow[j] /= l;", "orow[j] /= 1.0;"),
+    ("empty_row_lse_zero", "if (hi < lo) { *lse_out = -INFINITY; return; }",
+     "if (hi < lo) { *lse_out = 0.0; return; }"),
+    ("v_uses_k_stride", "const float *vrow = vbase + k * vstride;",
+     "const float *vrow = vbase + k * kstride;"),
+    ("padded_row_kept", "            if (qi >= Qb) {", "            if (qi > Qb) {"),
+    ("kv_ignores_batch", "oracle_row(q + r * D, k + ((long)b * K * Hkv + kh) * D,",
+     "oracle_row(q + r * D, k + ((long)kh) * D,"),
+    ("exp_not_shifted", "const double p = exp(s_scratch[k - lo] - m);",
+     "const double p = exp(s_scratch[k - lo]) * 1.0000001;"),
+    ("q_transposed_index", "oracle_row(q + r * D, k + ((long)b * K * Hkv + kh) * D,",
+     "oracle_row(q + ((r % Hq) * Q + (r / Hq) % Q + (r / ((long)Hq * Q)) * Q * Hq) * D, k + ((long)b * K * Hkv + kh) * D,"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(tmp_path, name, old, new):
+    src = open(oracle.SOURCE).read()
+    assert old in src, f"mutation site for {name} not found"
+    path = os.path.join(tmp_path, f"mut_{name}.c")
+    with open(path, "w") as f:
+        f.write(src.replace(old, new, 1))
+    lib = oracle.OracleLib(oracle.build(force=True, src=path,
+                                        out=os.path.join(tmp_path, f"mut_{name}.so")))
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(lib)
+        except (AssertionError, ValueError):
+            caught.append(pin.__name__)
+    assert caught, f"mutant {name} passed every pin"
