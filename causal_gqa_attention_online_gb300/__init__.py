@@ -1,0 +1,16 @@
+"""GB300 (sm_103a) causal grouped-query attention forward.
+
+The compute lives in libattn_gqa.so (hand-written CUDA kernels behind the C
+ABI of include/attn_gqa.h); this package is its thin Python binding plus the
+seeded synthetic-input generators (``synth``).  Build the library with
+``build_ext.build()``.
+"""
+from .binding import (ALGOS, ATTN_ALGO_AUTO, ATTN_ALGO_DECODE, ATTN_ALGO_GENERIC,
+                      ATTN_ALGO_TCGEN05, ATTN_BF16, ATTN_F16, ATTN_F32, EXPORTED, AttnError,
+                      attn_fwd, attn_fwd_varlen, attn_lse_combine, device_status, last_error,
+                      library_path, load_library)
+
+__all__ = ["ALGOS", "ATTN_ALGO_AUTO", "ATTN_ALGO_DECODE", "ATTN_ALGO_GENERIC",
+           "ATTN_ALGO_TCGEN05", "ATTN_BF16", "ATTN_F16", "ATTN_F32", "EXPORTED", "AttnError",
+           "attn_fwd", "attn_fwd_varlen", "attn_lse_combine", "device_status", "last_error",
+           "library_path", "load_library"]

@@ -1,0 +1,189 @@
+"""Thin ctypes binding of libattn_gqa (the C ABI in include/attn_gqa.h).
+
+Argument marshalling only: torch tensors are used as device memory and
+streams, their data pointers are handed to the C entry points, and every step
+of the attention runs in the library's CUDA kernels.  There is no CPU path:
+if the library or a CUDA device is missing, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import build_ext
+
+ATTN_F32, ATTN_F16, ATTN_BF16 = 0, 1, 2
+ATTN_ALGO_AUTO, ATTN_ALGO_GENERIC, ATTN_ALGO_TCGEN05, ATTN_ALGO_DECODE = 0, 1, 2, 3
+ALGOS = {"auto": 0, "generic": 1, "tcgen05": 2, "decode": 3}
+_DTYPE_CODE = {torch.float32: ATTN_F32, torch.float16: ATTN_F16, torch.bfloat16: ATTN_BF16}
+
+EXPORTED = ("attn_fwd", "attn_fwd_varlen", "attn_fwd_algo", "attn_fwd_varlen_algo",
+            "attn_lse_combine", "attn_last_error", "attn_device_status", "attn_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    """A non-zero status from the library."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"attn status {status}: {message}")
+        self.status = status
+
+
+def library_path() -> str:
+    return build_ext.LIB_PATH
+
+
+def load_library(path: str | None = None):
+    """Load libattn_gqa.so (built in-tree by ``build_ext.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = path or build_ext.LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with causal_gqa_attention_online_gb300.build_ext."
+                "build() (no CPU fallback exists)")
+        lib = ctypes.CDLL(path)
+        vp, ip, fp = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        common = [vp, vp, vp, vp, vp] + [ip] * 7 + [vp, vp, ip, fp, ip]
+        lib.attn_fwd.argtypes = common + [vp]
+        lib.attn_fwd_varlen.argtypes = common + [vp]
+        lib.attn_fwd_algo.argtypes = common + [ip, vp]
+        lib.attn_fwd_varlen_algo.argtypes = common + [ip, vp]
+        for f in (lib.attn_fwd, lib.attn_fwd_varlen, lib.attn_fwd_algo, lib.attn_fwd_varlen_algo):
+            f.restype = ip
+        lib.attn_lse_combine.argtypes = [vp, vp, vp, vp, ip, ctypes.c_longlong, ip, ip, vp]
+        lib.attn_lse_combine.restype = ip
+        lib.attn_last_error.argtypes = []
+        lib.attn_last_error.restype = ctypes.c_char_p
+        lib.attn_device_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
+        lib.attn_device_status.restype = ip
+        lib.attn_version.argtypes = []
+        lib.attn_version.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def last_error() -> str:
+    return load_library().attn_last_error().decode()
+
+
+def device_status() -> tuple[int, int]:
+    """(status, detail) of the current device's status word (synchronises)."""
+    d = ctypes.c_int(0)
+    st = load_library().attn_device_status(ctypes.byref(d))
+    return st, d.value
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise AttnError(rc, last_error())
+
+
+def _check_tensor(name, t, dtype, numel, device):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() != numel:
+        raise ValueError(f"{name}: {t.numel()} elements, expected {numel}")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def attn_fwd(q, k, v, o=None, lse=None, *, seqlens_q=None, seqlens_k=None, window=0,
+             scale=None, algo="auto", stream=None, want_lse=True):
+    """Padded layout: q [B,Q,Hq,D], k [B,K,Hkv,D], v [B,K,Hkv,Dv] CUDA tensors.
+
+    Returns (o [B,Q,Hq,Dv], lse [B,Q,Hq] float32 or None)."""
+    lib = load_library()
+    B, Q, Hq, D = q.shape
+    K, Hkv = k.shape[1], k.shape[2]
+    Dv = v.shape[3]
+    dev = q.device
+    if o is None:
+        o = torch.empty((B, Q, Hq, Dv), dtype=q.dtype, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Q, Hq), dtype=torch.float32, device=dev)
+    for name, t, n in (("q", q, B * Q * Hq * D), ("k", k, B * K * Hkv * D),
+                       ("v", v, B * K * Hkv * Dv), ("o", o, B * Q * Hq * Dv)):
+        _check_tensor(name, t, q.dtype, n, dev)
+    if lse is not None:
+        _check_tensor("lse", lse, torch.float32, B * Q * Hq, dev)
+    for name, t in (("seqlens_q", seqlens_q), ("seqlens_k", seqlens_k)):
+        if t is not None:
+            _check_tensor(name, t, torch.int32, B, dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = lib.attn_fwd_algo(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Q, K, D, Dv,
+                           _ptr(seqlens_q), _ptr(seqlens_k), int(window), float(scale),
+                           _DTYPE_CODE[q.dtype], ALGOS[algo], _stream_ptr(stream))
+    _check(rc)
+    return o, lse
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_q, max_k, o=None, lse=None, *,
+                    window=0, scale=None, algo="auto", stream=None, want_lse=True):
+    """Packed layout: q [Tq,Hq,D], k [Tk,Hkv,D], v [Tk,Hkv,Dv], int32
+    cumulative lengths [B+1] on the device.  Returns (o [Tq,Hq,Dv], lse [Tq,Hq])."""
+    lib = load_library()
+    Tq, Hq, D = q.shape
+    Tk, Hkv = k.shape[0], k.shape[1]
+    Dv = v.shape[2]
+    B = cu_seqlens_q.numel() - 1
+    dev = q.device
+    if o is None:
+        o = torch.empty((Tq, Hq, Dv), dtype=q.dtype, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty((Tq, Hq), dtype=torch.float32, device=dev)
+    for name, t, n in (("q", q, Tq * Hq * D), ("k", k, Tk * Hkv * D), ("v", v, Tk * Hkv * Dv),
+                       ("o", o, Tq * Hq * Dv)):
+        _check_tensor(name, t, q.dtype, n, dev)
+    if lse is not None:
+        _check_tensor("lse", lse, torch.float32, Tq * Hq, dev)
+    _check_tensor("cu_seqlens_q", cu_seqlens_q, torch.int32, B + 1, dev)
+    _check_tensor("cu_seqlens_k", cu_seqlens_k, torch.int32, B + 1, dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = lib.attn_fwd_varlen_algo(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv,
+                                  int(max_q), int(max_k), D, Dv, _ptr(cu_seqlens_q),
+                                  _ptr(cu_seqlens_k), int(window), float(scale),
+                                  _DTYPE_CODE[q.dtype], ALGOS[algo], _stream_ptr(stream))
+    _check(rc)
+    return o, lse
+
+
+def attn_lse_combine(o_parts, lse_parts, o=None, lse=None, *, dtype=torch.float32, stream=None):
+    """Merge split-KV partials: o_parts [S,rows,Dv] fp32, lse_parts [S,rows] fp32."""
+    lib = load_library()
+    S, rows, Dv = o_parts.shape
+    dev = o_parts.device
+    if o is None:
+        o = torch.empty((rows, Dv), dtype=dtype, device=dev)
+    if lse is None:
+        lse = torch.empty((rows,), dtype=torch.float32, device=dev)
+    _check_tensor("o_parts", o_parts, torch.float32, S * rows * Dv, dev)
+    _check_tensor("lse_parts", lse_parts, torch.float32, S * rows, dev)
+    _check_tensor("o", o, o.dtype, rows * Dv, dev)
+    rc = lib.attn_lse_combine(_ptr(o_parts), _ptr(lse_parts), _ptr(o), _ptr(lse), S, rows, Dv,
+                              _DTYPE_CODE[o.dtype], _stream_ptr(stream))
+    _check(rc)
+    return o, lse

@@ -1,0 +1,354 @@
+// attn_api.cu -- the C ABI of libattn_gqa: argument validation, kernel choice,
+// split-KV workspace from a library-owned stream-ordered pool, error strings
+// and the device status word.  Declarations and contracts: include/attn_gqa.h.
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/attn_gqa.h"
+#include "common.cuh"
+#include "launch.h"
+
+namespace attn {
+
+namespace {
+thread_local char g_last_error[512] = "";
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+cudaMemPool_t g_pools[kMaxDevices] = {};
+int *g_status_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+}  // namespace
+
+// The device status word (one per device, in this module's device image).
+__device__ int g_device_status;
+
+void set_error(const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+}
+
+int sm_count(int device) {
+    if (device < 0 || device >= kMaxDevices) return 0;
+    std::lock_guard<std::mutex> lk(g_dev_mutex);
+    if (g_sm_count[device] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+            return 0;
+        g_sm_count[device] = n;
+    }
+    return g_sm_count[device];
+}
+
+namespace {
+
+int current_device(int *dev) {
+    const cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess || *dev < 0 || *dev >= kMaxDevices) {
+        set_error("cudaGetDevice: %s", cudaGetErrorString(e));
+        return ATTN_ERR_CUDA;
+    }
+    return ATTN_OK;
+}
+
+// Address of the status word on `dev` (the current device).
+int status_ptr(int dev, int **out) {
+    std::lock_guard<std::mutex> lk(g_dev_mutex);
+    if (g_status_ptr[dev] == nullptr) {
+        void *ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_device_status);
+        if (e != cudaSuccess) {
+            set_error("cudaGetSymbolAddress(status): %s", cudaGetErrorString(e));
+            return ATTN_ERR_CUDA;
+        }
+        g_status_ptr[dev] = static_cast<int *>(ptr);
+    }
+    *out = g_status_ptr[dev];
+    return ATTN_OK;
+}
+
+// Library-owned pool: freed blocks stay cached, so steady-state split-KV
+// calls do not reach the driver allocator.
+int pool_for(int dev, cudaMemPool_t *out) {
+    std::lock_guard<std::mutex> lk(g_dev_mutex);
+    if (g_pools[dev] == nullptr) {
+        cudaMemPoolProps props;
+        memset(&props, 0, sizeof(props));
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool;
+        cudaError_t e = cudaMemPoolCreate(&pool, &props);
+        if (e != cudaSuccess) {
+            set_error("cudaMemPoolCreate: %s", cudaGetErrorString(e));
+            return ATTN_ERR_CUDA;
+        }
+        uint64_t threshold = UINT64_MAX;
+        e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &threshold);
+        if (e != cudaSuccess) {
+            set_error("cudaMemPoolSetAttribute: %s", cudaGetErrorString(e));
+            return ATTN_ERR_CUDA;
+        }
+        g_pools[dev] = pool;
+    }
+    *out = g_pools[dev];
+    return ATTN_OK;
+}
+
+bool ptr_aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Host-side validation shared by both layouts.
+int validate(const void *q, const void *k, const void *v, const void *o, const float *lse,
+             int B, int Hq, int Hkv, int Q, int K, int D, int Dv, int dtype, int algo) {
+    if (B < 0 || Hq < 0 || Hkv < 0 || Q < 0 || K < 0) {
+        set_error("negative size (B=%d Hq=%d Hkv=%d Q=%d K=%d)", B, Hq, Hkv, Q, K);
+        return ATTN_ERR_INVALID;
+    }
+    if (Hq > 0 && (Hkv == 0 || Hq % Hkv != 0)) {
+        set_error("Hq (%d) must be a positive multiple of Hkv (%d)", Hq, Hkv);
+        return ATTN_ERR_INVALID;
+    }
+    if (D < 1 || D > 256 || Dv < 1 || Dv > 256) {
+        set_error("head widths must be in [1, 256] (D=%d Dv=%d)", D, Dv);
+        return ATTN_ERR_INVALID;
+    }
+    if (dtype < ATTN_F32 || dtype > ATTN_BF16) {
+        set_error("unknown dtype %d", dtype);
+        return ATTN_ERR_INVALID;
+    }
+    if (algo < ATTN_ALGO_AUTO || algo > ATTN_ALGO_DECODE) {
+        set_error("unknown algo %d", algo);
+        return ATTN_ERR_INVALID;
+    }
+    const bool any_q = (long long)B * Q * Hq > 0;
+    if (any_q && (q == nullptr || o == nullptr)) {
+        set_error("q and o must be non-null");
+        return ATTN_ERR_INVALID;
+    }
+    if (any_q && K > 0 && (k == nullptr || v == nullptr)) {
+        set_error("k and v must be non-null");
+        return ATTN_ERR_INVALID;
+    }
+    if (!ptr_aligned16(q) || !ptr_aligned16(k) || !ptr_aligned16(v) || !ptr_aligned16(o) ||
+        !ptr_aligned16(lse)) {
+        set_error("tensor pointers must be 16-byte aligned");
+        return ATTN_ERR_INVALID;
+    }
+    return ATTN_OK;
+}
+
+int run(AttnParams &p, int dtype, int algo, cudaStream_t stream) {
+    int dev = 0;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    rc = status_ptr(dev, &p.status);
+    if (rc) return rc;
+    const int nsm = sm_count(dev);
+
+    // Kernel choice.
+    int chosen = algo;
+    if (algo == ATTN_ALGO_AUTO) {
+        chosen = ATTN_ALGO_GENERIC;
+        if (dtype != ATTN_F32) {
+            if (decode_supported(p, dtype))
+                chosen = ATTN_ALGO_DECODE;
+            else if (prefill_tc_supported(p, dtype))
+                chosen = ATTN_ALGO_TCGEN05;
+        }
+    } else if (algo == ATTN_ALGO_DECODE && !decode_supported(p, dtype)) {
+        set_error("decode kernel does not take this shape/dtype");
+        return ATTN_ERR_UNSUPPORTED;
+    } else if (algo == ATTN_ALGO_TCGEN05 && !prefill_tc_supported(p, dtype)) {
+        set_error("tcgen05 prefill kernel does not take this shape/dtype");
+        return ATTN_ERR_UNSUPPORTED;
+    }
+
+    if (chosen == ATTN_ALGO_TCGEN05) return launch_prefill_tc(p, dtype, stream);
+
+    // Split the key axis when the (sequence, KV head, row-block) units alone
+    // would leave SMs idle.  A row whose legal keys fall in one split is
+    // written directly; the others are merged by the combine kernel.
+    if (chosen == ATTN_ALGO_DECODE) {
+        p.split_len = decode_split_len(p, nsm);
+    } else {
+        p.split_len = p.K > 0 ? p.K : 1;
+        const long long units = (long long)p.B * p.Hkv * (((long long)p.Q * p.G + 31) / 32);
+        const int min_split = 128;
+        if (p.K > 2 * min_split && units < 2LL * nsm) {
+            const long long want = (2LL * nsm + units - 1) / units;
+            const long long most = (p.K + min_split - 1) / min_split;
+            const long long ns = want < most ? want : most;
+            if (ns > 1) {
+                long long len = (p.K + ns - 1) / ns;
+                p.split_len = (int)((len + 63) / 64 * 64);
+            }
+        }
+    }
+    if (p.split_len < 1) p.split_len = 1;
+    p.nsplit = p.K > 0 ? (int)(((long long)p.K + p.split_len - 1) / p.split_len) : 1;
+
+    void *ws = nullptr;
+    if (p.nsplit > 1) {
+        const long long rows = (long long)p.nsplit * p.B * p.Q * p.Hq;
+        const size_t bytes = sizeof(float) * (size_t)rows * (size_t)(p.Dv + 1);
+        cudaMemPool_t pool = nullptr;
+        rc = pool_for(dev, &pool);
+        if (rc) return rc;
+        const cudaError_t e = cudaMallocFromPoolAsync(&ws, bytes, pool, stream);
+        if (e != cudaSuccess) {
+            set_error("workspace cudaMallocFromPoolAsync(%zu): %s", bytes, cudaGetErrorString(e));
+            return ATTN_ERR_CUDA;
+        }
+        p.part_o = static_cast<float *>(ws);
+        p.part_lse = p.part_o + rows * p.Dv;
+    }
+    rc = chosen == ATTN_ALGO_DECODE ? launch_decode(p, dtype, stream)
+                                    : launch_generic(p, dtype, stream);
+    if (rc == 0 && p.nsplit > 1) rc = launch_combine_rows(p, dtype, stream);
+    if (ws != nullptr) {
+        const cudaError_t e = cudaFreeAsync(ws, stream);
+        if (e != cudaSuccess && rc == 0) {
+            set_error("workspace cudaFreeAsync: %s", cudaGetErrorString(e));
+            rc = ATTN_ERR_CUDA;
+        }
+    }
+    return rc;
+}
+
+int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+               int Hkv, int Q, int K, int D, int Dv, const int32_t *seqlens_q,
+               const int32_t *seqlens_k, const int32_t *cu_q, const int32_t *cu_k, int window,
+               float scale, int dtype, int algo, cudaStream_t stream) {
+    g_last_error[0] = '\0';
+    int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Q, K, D, Dv, dtype, algo);
+    if (rc) return rc;
+    if ((long long)B * Q * Hq == 0) return ATTN_OK;
+    AttnParams p;
+    memset(&p, 0, sizeof(p));
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.o = o;
+    p.lse = lse;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = Hq / Hkv;
+    p.Q = Q;
+    p.K = K;
+    p.D = D;
+    p.Dv = Dv;
+    p.seqlens_q = seqlens_q;
+    p.seqlens_k = seqlens_k;
+    p.cu_q = cu_q;
+    p.cu_k = cu_k;
+    // A window of at least K keys keeps every causal key: same as no window
+    // (this also keeps the kernels' window arithmetic far from overflow).
+    p.window = (window <= 0 || window >= K) ? 0 : window;
+    p.scale = scale;
+    p.scale_log2 = scale * kLog2e;
+    p.nsplit = 1;
+    p.split_len = K > 0 ? K : 1;
+    return run(p, dtype, algo, stream);
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+int attn_fwd_algo(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                  int Hq, int Hkv, int Q, int K, int D, int Dv, const int32_t *seqlens_q,
+                  const int32_t *seqlens_k, int window, float scale, int dtype, int algo,
+                  attn_stream_t stream) {
+    return fwd_common(q, k, v, o, lse, B, Hq, Hkv, Q, K, D, Dv, seqlens_q, seqlens_k, nullptr,
+                      nullptr, window, scale, dtype, algo, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+             int Hkv, int Q, int K, int D, int Dv, const int32_t *seqlens_q,
+             const int32_t *seqlens_k, int window, float scale, int dtype,
+             attn_stream_t stream) {
+    return attn_fwd_algo(q, k, v, o, lse, B, Hq, Hkv, Q, K, D, Dv, seqlens_q, seqlens_k, window,
+                         scale, dtype, ATTN_ALGO_AUTO, stream);
+}
+
+int attn_fwd_varlen_algo(const void *q, const void *k, const void *v, void *o, float *lse,
+                         int B, int Hq, int Hkv, int max_Q, int max_K, int D, int Dv,
+                         const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int window,
+                         float scale, int dtype, int algo, attn_stream_t stream) {
+    if (B > 0 && (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr)) {
+        attn::set_error("cu_seqlens_q and cu_seqlens_k must be non-null");
+        return ATTN_ERR_INVALID;
+    }
+    return fwd_common(q, k, v, o, lse, B, Hq, Hkv, max_Q, max_K, D, Dv, nullptr, nullptr,
+                      cu_seqlens_q, cu_seqlens_k, window, scale, dtype, algo,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                    int Hq, int Hkv, int max_Q, int max_K, int D, int Dv,
+                    const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int window,
+                    float scale, int dtype, attn_stream_t stream) {
+    return attn_fwd_varlen_algo(q, k, v, o, lse, B, Hq, Hkv, max_Q, max_K, D, Dv, cu_seqlens_q,
+                                cu_seqlens_k, window, scale, dtype, ATTN_ALGO_AUTO, stream);
+}
+
+int attn_lse_combine(const float *o_parts, const float *lse_parts, void *o, float *lse,
+                     int nsplit, long long rows, int Dv, int dtype, attn_stream_t stream) {
+    g_last_error[0] = '\0';
+    if (nsplit < 1 || rows < 0 || Dv < 1 || Dv > 4096 || dtype < ATTN_F32 || dtype > ATTN_BF16) {
+        attn::set_error("attn_lse_combine: bad size or dtype (nsplit=%d rows=%lld Dv=%d)",
+                        nsplit, rows, Dv);
+        return ATTN_ERR_INVALID;
+    }
+    if (rows > 0 && (o_parts == nullptr || lse_parts == nullptr || o == nullptr)) {
+        attn::set_error("attn_lse_combine: null pointer");
+        return ATTN_ERR_INVALID;
+    }
+    if (rows > (1LL << 40)) {
+        attn::set_error("attn_lse_combine: too many rows");
+        return ATTN_ERR_UNSUPPORTED;
+    }
+    return launch_combine_flat(o_parts, lse_parts, o, lse, nsplit, rows, Dv, dtype,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char *attn_last_error(void) { return g_last_error; }
+
+int attn_device_status(int *detail) {
+    if (detail) *detail = 0;
+    int dev = 0;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        attn::set_error("cudaDeviceSynchronize: %s", cudaGetErrorString(e));
+        return ATTN_ERR_CUDA;
+    }
+    int value = 0;
+    e = cudaMemcpyFromSymbol(&value, g_device_status, sizeof(int));
+    if (e != cudaSuccess) {
+        attn::set_error("reading the status word: %s", cudaGetErrorString(e));
+        return ATTN_ERR_CUDA;
+    }
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int));
+    if (e != cudaSuccess) {
+        attn::set_error("clearing the status word: %s", cudaGetErrorString(e));
+        return ATTN_ERR_CUDA;
+    }
+    if (detail) *detail = value;
+    return value == 0 ? ATTN_OK : ATTN_ERR_TIMEOUT;
+}
+
+const char *attn_version(void) { return "0.1.0"; }
+
+}  // extern "C"

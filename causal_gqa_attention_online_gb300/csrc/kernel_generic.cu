@@ -1,0 +1,330 @@
+// kernel_generic.cu -- CUDA-core online-softmax attention forward (any storage
+// dtype, head widths up to 256) and the split-KV combine kernels.
+//
+// This is the fp32 path ("Accelerating PyTorch on AMD GPUs with FlyDSL",
+// section on FMHA through AOTriton: that attention kernel family has no FP32
+// variant, so fp32 needs its own kernel) and the fallback for bf16/fp16 head
+// widths the tensor-core kernels do not take.  It follows the phase graph of
+// "Attention execution mapping" (LuisaCompute), section 2: per KV tile,
+// QK -> mask -> max -> exp -> sum -> alpha-rescale -> PV, with the row max,
+// row sum and accumulator carried across tiles (section 1).
+//
+// Work decomposition: a block owns 32 consecutive rows of the flattened
+// (query position, head-in-group) space of one (sequence, KV head), so every
+// K/V tile it stages serves all query heads of the group; it walks the union
+// of its rows' legal key ranges in tiles of 32 keys (one key per lane for QK,
+// output columns spread over lanes for PV).  Blocks may also own one split
+// of the key axis (split-KV), writing normalised partials and their LSE for
+// the combine kernel (the legal (max, sum, acc) merge of section 5).
+#include <climits>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace attn {
+namespace {
+
+constexpr int kRows = 32;            // flattened rows per block
+constexpr int kTK = 32;              // keys per tile (one per lane)
+constexpr int kWarps = 4;
+constexpr int kRPW = kRows / kWarps;  // rows per warp
+
+template <typename T, int DVL>
+__global__ void __launch_bounds__(128) generic_fwd_kernel(const AttnParams p) {
+    extern __shared__ float smem[];
+    const int D = p.D, Dv = p.Dv, G = p.G;
+    const int Dp = D | 1;  // odd row pitch: lane-per-key reads hit distinct banks
+    float *qs = smem;                // [kRows][D], pre-scaled by scale*log2(e)
+    float *ks = qs + kRows * D;      // [kTK][Dp]
+    float *vs = ks + kTK * Dp;       // [kTK][Dv]
+
+    const int b = blockIdx.y / p.Hkv, kvh = blockIdx.y % p.Hkv;
+    const int split = blockIdx.z;
+    const SeqInfo si = seq_info(p, b);
+    const bool packed = p.cu_q != nullptr;
+    const int r0 = blockIdx.x * kRows;
+    const int nvalid = si.Qb * G;                    // rows holding real queries
+    const int ncap = (packed ? si.Qb : p.Q) * G;     // rows this block must write
+    if (r0 >= ncap) return;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const T *qg = static_cast<const T *>(p.q);
+    const T *kg = static_cast<const T *>(p.k);
+    const T *vg = static_cast<const T *>(p.v);
+
+    for (int i = tid; i < kRows * D; i += blockDim.x) {
+        const int r = r0 + i / D, d = i % D;
+        float x = 0.f;
+        if (r < nvalid) {
+            const int qi = r / G, h = kvh * G + r % G;
+            x = to_f32(qg[((si.q_off + qi) * p.Hq + h) * (long long)D + d]) * p.scale_log2;
+        }
+        qs[i] = x;
+    }
+
+    // Key range of the block: legal ranges are monotone in the query index.
+    int key_lo = 0, key_hi = 0;
+    if (r0 < nvalid) {
+        int lo_a, hi_a, lo_b, hi_b;
+        legal_range(r0 / G, si.Qb, si.Kb, p.window, lo_a, hi_a);
+        legal_range((min(r0 + kRows, nvalid) - 1) / G, si.Qb, si.Kb, p.window, lo_b, hi_b);
+        key_lo = lo_a;
+        key_hi = hi_b;
+    }
+    const int s_lo = split * p.split_len;
+    key_lo = max(key_lo, s_lo);
+    key_hi = min(key_hi, s_lo + p.split_len);
+
+    float m[kRPW], l[kRPW], acc[kRPW][DVL];
+    int rlo[kRPW], rhi[kRPW];
+    SplitSpan span[kRPW];
+#pragma unroll
+    for (int i = 0; i < kRPW; ++i) {
+        const int r = r0 + warp + kWarps * i;
+        rlo[i] = 0;
+        rhi[i] = 0;
+        if (r < nvalid) legal_range(r / G, si.Qb, si.Kb, p.window, rlo[i], rhi[i]);
+        span[i] = split_span(rlo[i], rhi[i], p.split_len);
+        rlo[i] = max(rlo[i], key_lo);
+        rhi[i] = min(rhi[i], key_hi);
+        m[i] = -INFINITY;
+        l[i] = 0.f;
+#pragma unroll
+        for (int c = 0; c < DVL; ++c) acc[i][c] = 0.f;
+    }
+
+    for (int t0 = key_lo; t0 < key_hi; t0 += kTK) {
+        __syncthreads();  // previous tile consumed; q staged
+        for (int i = tid; i < kTK * D; i += blockDim.x) {
+            const int j = i / D, d = i % D, key = t0 + j;
+            ks[j * Dp + d] = key < key_hi
+                ? to_f32(kg[((si.k_off + key) * p.Hkv + kvh) * (long long)D + d]) : 0.f;
+        }
+        for (int i = tid; i < kTK * Dv; i += blockDim.x) {
+            const int j = i / Dv, c = i % Dv, key = t0 + j;
+            vs[i] = key < key_hi
+                ? to_f32(vg[((si.k_off + key) * p.Hkv + kvh) * (long long)Dv + c]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kRPW; ++i) {
+            // warp-uniform: the row's legal range misses this tile
+            if (rhi[i] <= t0 || rlo[i] >= t0 + kTK) continue;
+            const int rr = warp + kWarps * i;
+            const int key = t0 + lane;
+            float s = -INFINITY;
+            if (key >= rlo[i] && key < rhi[i]) {
+                const float *qr = qs + rr * D;
+                const float *kr = ks + lane * Dp;
+                float a = 0.f;
+                for (int d = 0; d < D; ++d) a = fmaf(qr[d], kr[d], a);
+                s = a;
+            }
+            const float mnew = fmaxf(m[i], warp_max(s));  // finite: a legal key is in the tile
+            const float pj = exp2f(s - mnew);
+            const float alpha = exp2f(m[i] - mnew);
+            l[i] = l[i] * alpha + warp_sum(pj);
+#pragma unroll
+            for (int c = 0; c < DVL; ++c) acc[i][c] *= alpha;
+            for (int j = 0; j < kTK; ++j) {
+                const float pb = __shfl_sync(0xffffffffu, pj, j);
+                const float *vr = vs + j * Dv;
+#pragma unroll
+                for (int c = 0; c < DVL; ++c) {
+                    const int col = lane + 32 * c;
+                    if (col < Dv) acc[i][c] = fmaf(pb, vr[col], acc[i][c]);
+                }
+            }
+            m[i] = mnew;
+        }
+    }
+
+    T *og = static_cast<T *>(p.o);
+#pragma unroll
+    for (int i = 0; i < kRPW; ++i) {
+        const int r = r0 + warp + kWarps * i;
+        if (r >= ncap) continue;
+        const int qi = r / G, h = kvh * G + r % G;
+        // padded rows (r >= nvalid) and empty rows are direct with first == 0
+        if (span[i].direct ? split != span[i].first
+                           : (split < span[i].first || split > span[i].last))
+            continue;
+        const float inv = l[i] > 0.f ? 1.f / l[i] : 0.f;
+        const float lse = l[i] > 0.f ? (m[i] + __log2f(l[i])) * kLn2 : -INFINITY;
+        if (span[i].direct) {
+            T *orow = og + ((si.q_off + qi) * p.Hq + h) * (long long)Dv;
+#pragma unroll
+            for (int c = 0; c < DVL; ++c) {
+                const int col = lane + 32 * c;
+                if (col < Dv) orow[col] = from_f32<T>(acc[i][c] * inv);
+            }
+            if (lane == 0 && p.lse) p.lse[(si.q_off + qi) * p.Hq + h] = lse;
+        } else {
+            const long long prow = (((long long)split * p.B + b) * p.Q + qi) * p.Hq + h;
+            float *po = p.part_o + prow * Dv;
+#pragma unroll
+            for (int c = 0; c < DVL; ++c) {
+                const int col = lane + 32 * c;
+                if (col < Dv) po[col] = acc[i][c] * inv;
+            }
+            if (lane == 0) p.part_lse[prow] = lse;
+        }
+    }
+}
+
+// One warp per output row: merge nsplit normalised partials by their LSE.
+template <typename T>
+__device__ __forceinline__ void combine_one_row(const float *o_parts, const float *lse_parts,
+                                                long long part_stride_rows, long long prow,
+                                                int nsplit, int Dv, T *orow, float *lse_out,
+                                                int lane) {
+    float mx = -INFINITY;
+    for (int s = 0; s < nsplit; ++s) mx = fmaxf(mx, lse_parts[s * part_stride_rows + prow]);
+    if (mx == -INFINITY) {
+        for (int c = lane; c < Dv; c += 32) orow[c] = from_f32<T>(0.f);
+        if (lane == 0 && lse_out) *lse_out = -INFINITY;
+        return;
+    }
+    float wsum = 0.f;
+    for (int s = 0; s < nsplit; ++s)
+        wsum += exp2f((lse_parts[s * part_stride_rows + prow] - mx) * kLog2e);
+    const float inv = 1.f / wsum;
+    for (int c = lane; c < Dv; c += 32) {
+        float a = 0.f;
+        for (int s = 0; s < nsplit; ++s) {
+            const float w = exp2f((lse_parts[s * part_stride_rows + prow] - mx) * kLog2e);
+            a = fmaf(w, o_parts[(s * part_stride_rows + prow) * Dv + c], a);
+        }
+        orow[c] = from_f32<T>(a * inv);
+    }
+    if (lane == 0 && lse_out) *lse_out = mx + __logf(wsum);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(128) combine_rows_kernel(const AttnParams p) {
+    const int lane = threadIdx.x & 31;
+    const long long row = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (row >= (long long)p.B * p.Q * p.Hq) return;
+    const int h = (int)(row % p.Hq);
+    const int qi = (int)((row / p.Hq) % p.Q);
+    const int b = (int)(row / ((long long)p.Hq * p.Q));
+    const SeqInfo si = seq_info(p, b);
+    T *orow = static_cast<T *>(p.o) + ((si.q_off + qi) * p.Hq + h) * (long long)p.Dv;
+    float *lse_out = p.lse ? p.lse + (si.q_off + qi) * p.Hq + h : nullptr;
+    if (qi >= si.Qb) return;  // padded rows are written by the forward kernel
+    int lo, hi;
+    legal_range(qi, si.Qb, si.Kb, p.window, lo, hi);
+    const SplitSpan span = split_span(lo, hi, p.split_len);
+    if (span.direct) return;  // written by the forward kernel
+    const long long stride = (long long)p.B * p.Q * p.Hq;
+    const long long first = (long long)span.first * stride + row;
+    combine_one_row<T>(p.part_o + first * p.Dv, p.part_lse + first, stride, 0,
+                       span.last - span.first + 1, p.Dv, orow, lse_out, lane);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(128) combine_flat_kernel(const float *o_parts,
+                                                           const float *lse_parts, T *o,
+                                                           float *lse, int nsplit,
+                                                           long long rows, int Dv) {
+    const int lane = threadIdx.x & 31;
+    const long long row = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    combine_one_row<T>(o_parts, lse_parts, rows, row, nsplit, Dv, o + row * Dv,
+                       lse ? lse + row : nullptr, lane);
+}
+
+template <typename T, int DVL>
+int launch_generic_t(const AttnParams &p, cudaStream_t stream) {
+    const int Dp = p.D | 1;
+    const size_t smem = sizeof(float) * ((size_t)kRows * p.D + (size_t)kTK * Dp +
+                                         (size_t)kTK * p.Dv);
+    auto kern = generic_fwd_kernel<T, DVL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) {
+        set_error("generic kernel: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        return 3;
+    }
+    const long long rows = (long long)p.Q * p.G;
+    dim3 grid((unsigned)((rows + kRows - 1) / kRows), (unsigned)(p.B * p.Hkv),
+              (unsigned)p.nsplit);
+    kern<<<grid, 128, smem, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("generic kernel launch: %s", cudaGetErrorString(e));
+        return 3;
+    }
+    return 0;
+}
+
+template <typename T>
+int launch_generic_dtype(const AttnParams &p, cudaStream_t stream) {
+    if (p.Dv <= 32) return launch_generic_t<T, 1>(p, stream);
+    if (p.Dv <= 64) return launch_generic_t<T, 2>(p, stream);
+    if (p.Dv <= 128) return launch_generic_t<T, 4>(p, stream);
+    return launch_generic_t<T, 8>(p, stream);
+}
+
+}  // namespace
+
+int launch_generic(const AttnParams &p, int dtype, cudaStream_t stream) {
+    if (p.Q * (long long)p.G / kRows + 1 > 0x7fffffffLL || p.B * (long long)p.Hkv > 65535 ||
+        p.nsplit > 65535) {
+        set_error("generic kernel: grid too large");
+        return 2;
+    }
+    switch (dtype) {
+        case 0: return launch_generic_dtype<float>(p, stream);
+        case 1: return launch_generic_dtype<__half>(p, stream);
+        case 2: return launch_generic_dtype<__nv_bfloat16>(p, stream);
+    }
+    set_error("generic kernel: bad dtype %d", dtype);
+    return 1;
+}
+
+int launch_combine_rows(const AttnParams &p, int dtype, cudaStream_t stream) {
+    const long long rows = (long long)p.B * p.Q * p.Hq;
+    if (rows == 0) return 0;
+    const unsigned blocks = (unsigned)((rows + 3) / 4);
+    switch (dtype) {
+        case 0: combine_rows_kernel<float><<<blocks, 128, 0, stream>>>(p); break;
+        case 1: combine_rows_kernel<__half><<<blocks, 128, 0, stream>>>(p); break;
+        case 2: combine_rows_kernel<__nv_bfloat16><<<blocks, 128, 0, stream>>>(p); break;
+        default: set_error("combine: bad dtype %d", dtype); return 1;
+    }
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("combine kernel launch: %s", cudaGetErrorString(e));
+        return 3;
+    }
+    return 0;
+}
+
+int launch_combine_flat(const float *o_parts, const float *lse_parts, void *o, float *lse,
+                        int nsplit, long long rows, int Dv, int dtype, cudaStream_t stream) {
+    if (rows == 0) return 0;
+    const unsigned blocks = (unsigned)((rows + 3) / 4);
+    switch (dtype) {
+        case 0:
+            combine_flat_kernel<float><<<blocks, 128, 0, stream>>>(
+                o_parts, lse_parts, static_cast<float *>(o), lse, nsplit, rows, Dv);
+            break;
+        case 1:
+            combine_flat_kernel<__half><<<blocks, 128, 0, stream>>>(
+                o_parts, lse_parts, static_cast<__half *>(o), lse, nsplit, rows, Dv);
+            break;
+        case 2:
+            combine_flat_kernel<__nv_bfloat16><<<blocks, 128, 0, stream>>>(
+                o_parts, lse_parts, static_cast<__nv_bfloat16 *>(o), lse, nsplit, rows, Dv);
+            break;
+        default: set_error("combine: bad dtype %d", dtype); return 1;
+    }
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("combine kernel launch: %s", cudaGetErrorString(e));
+        return 3;
+    }
+    return 0;
+}
+
+}  // namespace attn

@@ -1,0 +1,30 @@
+// launch.h -- host-side launchers of the kernels (internal to libattn_gqa).
+// Each returns 0 on success, otherwise an attn_status code, and writes a
+// message through set_error().
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace attn {
+
+void set_error(const char *fmt, ...);
+int sm_count(int device);
+
+// CUDA-core online softmax (any dtype; D, Dv <= 256).  Honours p.nsplit.
+int launch_generic(const AttnParams &p, int dtype, cudaStream_t stream);
+// Split-KV partial merge, driven by the problem's layout.
+int launch_combine_rows(const AttnParams &p, int dtype, cudaStream_t stream);
+// Plain [nsplit, rows, Dv] merge for attn_lse_combine.
+int launch_combine_flat(const float *o_parts, const float *lse_parts, void *o, float *lse,
+                        int nsplit, long long rows, int Dv, int dtype, cudaStream_t stream);
+// Tensor-core split-KV decode (bf16/fp16, Q*G <= 16).  Honours p.nsplit.
+bool decode_supported(const AttnParams &p, int dtype);
+int decode_split_len(const AttnParams &p, int nsm);
+int launch_decode(const AttnParams &p, int dtype, cudaStream_t stream);
+// tcgen05/TMEM prefill (bf16/fp16, D, Dv in {64, 128}).
+bool prefill_tc_supported(const AttnParams &p, int dtype);
+int launch_prefill_tc(const AttnParams &p, int dtype, cudaStream_t stream);
+
+}  // namespace attn

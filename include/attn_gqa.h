@@ -1,0 +1,166 @@
+/*
+ * attn_gqa.h -- C ABI of the GB300 (sm_103a) causal grouped-query attention
+ * forward library (libattn_gqa.so).
+ *
+ * Operation.  Every entry point computes, for each sequence b, query head h and
+ * valid query row q, the softmax attention
+ *
+ *     O[q,h,:] = sum_k p_k V[k,kh,:],   p_k = exp(s_k - LSE[q,h]),
+ *     s_k      = scale * <Q[q,h,:], K[k,kh,:]>,
+ *     LSE[q,h] = log sum_{k legal} exp(s_k)            (natural log)
+ *
+ * over the legal keys of the row, with kh = h / (Hq / Hkv):
+ *
+ *     0 <= k < Kb,   k <= q + Kb - Qb,
+ *     and, when window > 0,   k >= q + Kb - Qb - window + 1.
+ *
+ * Sources: "Attention execution mapping: 现状、缺口与有界实验"
+ * (LuisaCompute), section 1 (bottom-right causal GQA, kh = h / (Hq/Hkv),
+ * legal keys k <= q + K - Q, one online-softmax program for prefill and
+ * decode with row max / row sum / accumulator carried across KV blocks) and
+ * section 5 (split-KV needs a legal merge of the (max, sum, acc) state);
+ * "快速後端" (Laya fast backends), numerical verification (sliding window,
+ * int32 per-sequence lengths, empty sequences, finite padded output).
+ * The window reading (the w most recent keys including the diagonal one),
+ * the empty-row convention and the natural-log LSE are this library's
+ * readings where the pages are silent.
+ *
+ * Rows with no legal key (Kb = 0, leading rows when Qb > Kb, or a window
+ * that excludes every key) return O = +0.0 and LSE = -inf.  Padded query rows
+ * q >= Qb of the padded layout are written as O = +0.0 and LSE = -inf.
+ *
+ * Memory and ownership.  All tensor and length pointers are DEVICE pointers
+ * owned by the caller; the library never frees or retains them.  Tensors are
+ * dense and contiguous (row-major in the order given), 16-byte aligned.
+ * Key / value rows past a sequence's length are never used as values: they
+ * may hold anything, NaN included.
+ *
+ * Asynchrony.  Every call validates its host-side arguments, enqueues its
+ * kernels on `stream` and returns; nothing synchronises.  Split-KV calls take
+ * their temporary workspace from a library-owned stream-ordered pool
+ * (cudaMallocAsync / cudaFreeAsync on `stream`).
+ *
+ * Errors.  Calls return ATTN_OK or a status below; no exception crosses the
+ * ABI.  attn_last_error() gives a message for the calling thread's last
+ * failure.  Device-side contract violations found by the kernels (a bounded
+ * wait that ran out) are recorded in a device status word read by
+ * attn_device_status().
+ */
+#ifndef ATTN_GQA_H
+#define ATTN_GQA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *attn_stream_t;
+
+/* Element types of q, k, v and o.  lse is always float32. */
+enum attn_dtype { ATTN_F32 = 0, ATTN_F16 = 1, ATTN_BF16 = 2 };
+
+/* Status codes. */
+enum attn_status {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID = 1,     /* null pointer, negative size, Hq % Hkv != 0 ... */
+    ATTN_ERR_UNSUPPORTED = 2, /* dtype / head-width / algorithm combination */
+    ATTN_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+    ATTN_ERR_TIMEOUT = 4      /* a kernel's bounded wait ran out (device status) */
+};
+
+/* Kernel selection for the *_algo entry points. */
+enum attn_algo {
+    ATTN_ALGO_AUTO = 0,     /* choose by dtype, head widths and query length */
+    ATTN_ALGO_GENERIC = 1,  /* CUDA-core online softmax: any dtype, D, Dv <= 256 */
+    ATTN_ALGO_TCGEN05 = 2,  /* tcgen05/TMEM prefill: bf16/fp16, D, Dv in {64, 128} */
+    ATTN_ALGO_DECODE = 3    /* split-KV tensor-core decode: bf16/fp16, Q*G <= 16 */
+};
+
+/*
+ * attn_fwd -- padded layout.
+ *   q   [B, Q, Hq, D]    o   [B, Q, Hq, Dv]    lse [B, Q, Hq] (float32, may be NULL)
+ *   k   [B, K, Hkv, D]   v   [B, K, Hkv, Dv]
+ *   Q, K        padded capacities (query rows / key rows per sequence).
+ *   seqlens_q   int32 [B] valid query rows per sequence, or NULL for all Q.
+ *   seqlens_k   int32 [B] valid key rows per sequence, or NULL for all K.
+ *               Values outside [0, Q] / [0, K] are clamped into range.
+ *   window      > 0: keep the `window` most recent keys (diagonal included);
+ *               <= 0: no window.
+ *   scale       multiplies Q.K (pass 1/sqrt(D) for the usual scaling).
+ *   dtype       attn_dtype of q, k, v and o.
+ * Returns ATTN_OK, ATTN_ERR_INVALID (bad pointer or size, Hq % Hkv != 0,
+ * D or Dv outside [1, 256]), ATTN_ERR_UNSUPPORTED or ATTN_ERR_CUDA.
+ * B = 0, Q = 0 or Hq = 0 work is a successful no-op.
+ */
+ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+             int Hkv, int Q, int K, int D, int Dv, const int32_t *seqlens_q,
+             const int32_t *seqlens_k, int window, float scale, int dtype,
+             attn_stream_t stream);
+
+/*
+ * attn_fwd_varlen -- packed layout.
+ *   q [Tq, Hq, D]  k [Tk, Hkv, D]  v [Tk, Hkv, Dv]  o [Tq, Hq, Dv]  lse [Tq, Hq] (may be NULL)
+ *   cu_seqlens_q, cu_seqlens_k   int32 [B+1], cu[0] = 0, non-decreasing:
+ *               sequence b owns query rows [cu_q[b], cu_q[b+1]) and key rows
+ *               [cu_k[b], cu_k[b+1]); an empty sequence owns none.
+ *   max_Q, max_K   upper bounds of the per-sequence lengths (sizes the grid;
+ *               rows beyond them are not computed).
+ * Other arguments and return codes as attn_fwd.  Rows outside every
+ * sequence are not written.
+ */
+ATTN_API int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                    int Hq, int Hkv, int max_Q, int max_K, int D, int Dv,
+                    const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int window,
+                    float scale, int dtype, attn_stream_t stream);
+
+/* The same two operations with an explicit kernel choice (attn_algo).  A
+ * choice that cannot run the given shape returns ATTN_ERR_UNSUPPORTED. */
+ATTN_API int attn_fwd_algo(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                  int Hq, int Hkv, int Q, int K, int D, int Dv, const int32_t *seqlens_q,
+                  const int32_t *seqlens_k, int window, float scale, int dtype, int algo,
+                  attn_stream_t stream);
+ATTN_API int attn_fwd_varlen_algo(const void *q, const void *k, const void *v, void *o, float *lse,
+                         int B, int Hq, int Hkv, int max_Q, int max_K, int D, int Dv,
+                         const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int window,
+                         float scale, int dtype, int algo, attn_stream_t stream);
+
+/*
+ * attn_lse_combine -- the legal merge of split-KV partial states (the
+ * "(max, sum, acc)" merge of the LuisaCompute page, section 5), written as a
+ * merge of normalised partials:
+ *   o_parts   float32 [nsplit, rows, Dv]   each partial normalised by its own sum
+ *   lse_parts float32 [nsplit, rows]       natural-log LSE of each partial;
+ *                                          -inf marks a partial with no key
+ *   o         [rows, Dv] in `dtype`;  lse [rows] float32 (may be NULL)
+ *   L = log sum_s exp(lse_s);   o = sum_s exp(lse_s - L) o_s.
+ * A row whose partials are all -inf gives o = +0 and lse = -inf.
+ */
+ATTN_API int attn_lse_combine(const float *o_parts, const float *lse_parts, void *o, float *lse,
+                     int nsplit, long long rows, int Dv, int dtype, attn_stream_t stream);
+
+/* Message for the calling thread's most recent failed call ("" if none). */
+ATTN_API const char *attn_last_error(void);
+
+/* Reads and clears the device status word of the current device
+ * (synchronises the device).  Returns ATTN_OK, ATTN_ERR_TIMEOUT, or
+ * ATTN_ERR_CUDA if the read itself failed; *detail (may be NULL) receives the
+ * kernel-specific detail code. */
+ATTN_API int attn_device_status(int *detail);
+
+/* Library version, e.g. "0.1.0". */
+ATTN_API const char *attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GQA_H */

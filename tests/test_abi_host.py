@@ -1,0 +1,93 @@
+"""The C-ABI library on the host: it builds, loads, exports every symbol
+include/attn_gqa.h declares, and rejects bad arguments before touching a GPU
+(no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import causal_gqa_attention_online_gb300 as attn
+from causal_gqa_attention_online_gb300 import build_ext
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn_gqa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_ext.build()
+    return attn.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"ATTN_API\s+[\w\s\*]*?\b(attn_\w+)\s*\(", text)
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    assert {"attn_fwd", "attn_fwd_varlen", "attn_lse_combine", "attn_last_error"} <= set(names)
+
+
+def test_every_declared_symbol_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) == set(attn.EXPORTED)
+
+
+def test_version(lib):
+    assert lib.attn_version().decode().count(".") == 2
+
+
+def _call_fwd(lib, q=1 << 20, k=1 << 21, v=1 << 22, o=1 << 23, lse=None, B=1, Hq=4, Hkv=2, Q=8,
+              K=8, D=64, Dv=64, window=0, scale=0.125, dtype=2, algo=0):
+    vp = ctypes.c_void_p
+    return lib.attn_fwd_algo(vp(q), vp(k), vp(v), vp(o), vp(lse), B, Hq, Hkv, Q, K, D, Dv, None,
+                             None, window, scale, dtype, algo, None)
+
+
+@pytest.mark.parametrize("kw,needle", [
+    (dict(B=-1), "negative"),
+    (dict(Hq=6, Hkv=4), "multiple"),
+    (dict(Hkv=0), "multiple"),
+    (dict(D=0), "head widths"),
+    (dict(Dv=257), "head widths"),
+    (dict(dtype=7), "dtype"),
+    (dict(algo=9), "algo"),
+    (dict(q=0), "non-null"),
+    (dict(k=0), "non-null"),
+    (dict(o=(1 << 23) + 2), "aligned"),
+])
+def test_invalid_arguments_rejected_on_host(lib, kw, needle):
+    rc = _call_fwd(lib, **kw)
+    assert rc == 1
+    assert needle in lib.attn_last_error().decode()
+
+
+def test_empty_problem_is_noop(lib):
+    # B = 0 or Q = 0: nothing to do, no CUDA call is made
+    assert _call_fwd(lib, B=0, q=0, k=0, v=0, o=0) == 0
+    assert _call_fwd(lib, Q=0, q=0, o=0) == 0
+
+
+def test_varlen_requires_cu_seqlens(lib):
+    vp = ctypes.c_void_p
+    rc = lib.attn_fwd_varlen(vp(1 << 20), vp(1 << 21), vp(1 << 22), vp(1 << 23), None, 2, 4, 2,
+                             8, 8, 64, 64, None, None, 0, 0.125, 2, None)
+    assert rc == 1 and "cu_seqlens" in lib.attn_last_error().decode()
+
+
+def test_combine_rejects_bad_sizes(lib):
+    vp = ctypes.c_void_p
+    assert lib.attn_lse_combine(vp(16), vp(32), vp(64), None, 0, 4, 8, 0, None) == 1
+    assert lib.attn_lse_combine(None, vp(32), vp(64), None, 2, 4, 8, 0, None) == 1
+
+
+def test_binding_has_no_cpu_path():
+    src = open(os.path.join(ROOT, "causal_gqa_attention_online_gb300", "binding.py")).read()
+    assert "oracle" not in src
+    for f in os.listdir(os.path.join(ROOT, "causal_gqa_attention_online_gb300")):
+        if f.endswith(".py"):
+            text = open(os.path.join(ROOT, "causal_gqa_attention_online_gb300", f)).read()
+            assert "import oracle" not in text and "from oracle" not in text, f

@@ -1,0 +1,134 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the
+same seeded inputs, element by element (tolerances in tests/parity.py).
+
+Shapes: the named synthetic workloads, the held-out matrix of the
+LuisaCompute attention-mapping page (section 7: Q/K tails, small Q with a
+bottom-right offset, MQA/MHA/batch, long KV), reduction lengths
+0/1/7/16/31/32/33/65 around tile edges (same page, section 21.4), windows,
+Q > K, all-empty and K = 0 problems, and the packed layout with empty
+sequences (Laya fast backends, numerical verification)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from causal_gqa_attention_online_gb300 import AttnError, attn_fwd, attn_lse_combine, build_ext, synth
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+NAN = float("nan")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    build_ext.build()
+
+
+HELD_OUT = [
+    # B, Hq, Hkv, Q, K, D, Dv
+    (1, 4, 2, 65, 131, 64, 64),
+    (1, 8, 2, 256, 1024, 64, 64),
+    (1, 8, 2, 3, 67, 80, 96),
+    (1, 4, 2, 65, 65, 64, 64),
+    (2, 8, 1, 1, 2053, 80, 96),
+    (1, 8, 8, 1, 2048, 64, 64),
+    (1, 16, 4, 1, 8193, 128, 128),
+    (1, 8, 2, 1, 32768, 64, 96),
+    (1, 8, 2, 1, 2048, 64, 64),
+    (1, 16, 4, 1, 4096, 128, 128),
+]
+
+
+def test_named_fp32_prefill():
+    parity.check(synth.prefill_f32_b1_h4x2_q64_k128_d64(), "auto", "fp32 prefill 1,4,2,64,128")
+
+
+def test_named_fp32_decode():
+    parity.check(synth.decode_f32_b1_h8x2_k2053_d80x96(), "auto", "fp32 decode 1,8,2,1,2053")
+
+
+@pytest.mark.parametrize("shape", HELD_OUT, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_generic_held_out(shape, dtype):
+    B, Hq, Hkv, Q, K, D, Dv = shape
+    inp = synth.make_padded(B, Hq, Hkv, Q, K, D, Dv, dtype, seed=11)
+    parity.check(inp, "generic", f"generic {dtype} {shape}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_generic_reduction_lengths(dtype):
+    # lengths around the 32-key tile: 0/1/7/16/31/32/33/65; NaN in padded rows
+    sk = np.array([0, 1, 7, 16, 31, 32, 33, 65], np.int32)
+    sq = np.array([5, 1, 7, 3, 31, 32, 33, 65], np.int32)
+    inp = synth.make_padded(8, 4, 2, 65, 65, 64, 48, dtype, seed=3, seqlens_q=sq, seqlens_k=sk,
+                            pad_value=NAN)
+    parity.check(inp, "generic", f"lengths {dtype}")
+
+
+@pytest.mark.parametrize("window", [1, 7, 64, 199])
+def test_generic_window(window):
+    inp = synth.make_padded(2, 6, 2, 200, 200, 32, 32, "f32", seed=5, window=window)
+    parity.check(inp, "generic", f"window {window}")
+
+
+def test_generic_q_longer_than_k():
+    # rows q < Qb - Kb have no legal key: +0 / -inf
+    inp = synth.make_padded(2, 4, 2, 40, 10, 16, 16, "f32", seed=6)
+    parity.check(inp, "generic", "Q > K")
+
+
+def test_generic_all_empty_and_k_zero():
+    inp = synth.make_padded(3, 4, 1, 9, 12, 16, 16, "bf16", seed=7,
+                            seqlens_k=np.zeros(3, np.int32), pad_value=NAN)
+    parity.check(inp, "generic", "all empty")
+    inp = synth.make_padded(1, 4, 2, 5, 0, 16, 16, "f32", seed=8)
+    parity.check(inp, "auto", "K = 0")
+
+
+def test_generic_varlen_packed():
+    sk = np.array([0, 5, 33, 130, 1, 64, 0, 300], np.int32)
+    sq = np.minimum(sk, np.array([0, 5, 7, 64, 1, 64, 0, 100]))
+    for dtype, w in (("f32", 0), ("bf16", 40), ("f16", 0)):
+        inp = synth.make_packed(sq, sk, 8, 2, 64, 64, dtype, seed=9, window=w)
+        parity.check(inp, "generic", f"varlen {dtype} w={w}")
+
+
+def test_generic_split_kv_long_decode_with_lengths():
+    # few units and long keys: the key axis is split and merged
+    sk = np.array([0, 1, 511, 512, 513, 4000], np.int32)
+    inp = synth.make_padded(6, 8, 2, 1, 4096, 64, 64, "bf16", seed=10, seqlens_k=sk,
+                            pad_value=NAN)
+    parity.check(inp, "generic", "split-KV lengths")
+
+
+def test_lse_combine_entry_point():
+    # two partials of a decode row: keys [0, c) (seqlens_k = c) and [c, Kb)
+    # (window = Kb - c); their merge must equal the full row.
+    B, Hq, Hkv, K, D, Dv = 2, 8, 2, 700, 64, 64
+    inp = synth.make_padded(B, Hq, Hkv, 1, K, D, Dv, "f32", seed=12)
+    c = 300
+    q, k, v = inp.q.cuda(), inp.k.cuda(), inp.v.cuda()
+    o1, l1 = attn_fwd(q, k, v, seqlens_k=torch.full((B,), c, dtype=torch.int32, device="cuda"),
+                      algo="generic")
+    o2, l2 = attn_fwd(q, k, v, window=K - c, algo="generic")
+    parts_o = torch.stack([o1.reshape(-1, Dv), o2.reshape(-1, Dv)]).contiguous()
+    parts_l = torch.stack([l1.reshape(-1), l2.reshape(-1)]).contiguous()
+    o, lse = attn_lse_combine(parts_o, parts_l, dtype=torch.float32)
+    ro, rl = parity.run_oracle(inp)
+    parity.compare("f32", o.cpu().numpy(), lse.cpu().numpy(), ro.reshape(-1, Dv),
+                   rl.reshape(-1), "combine")
+    # all partials empty -> +0 / -inf
+    e_o = torch.zeros((3, 4, 16), device="cuda")
+    e_l = torch.full((3, 4), -math.inf, device="cuda")
+    o, lse = attn_lse_combine(e_o, e_l, dtype=torch.bfloat16)
+    assert torch.all(o.float() == 0) and not torch.any(torch.signbit(o.float()))
+    assert torch.all(lse == -math.inf)
+
+
+def test_unsupported_algo_reports():
+    inp = synth.make_padded(1, 4, 2, 8, 8, 16, 16, "f32", seed=1)
+    with pytest.raises(AttnError) as ei:
+        attn_fwd(inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), algo="tcgen05")
+    assert ei.value.status == 2
