@@ -54,10 +54,11 @@ def load_library(path: str | None = None):
         lib = ctypes.CDLL(path)
         vp, ip, fp = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         common = [vp, vp, vp, vp, vp] + [ip] * 7 + [vp, vp, ip, fp, ip]
+        varlen = [vp, vp, vp, vp, vp] + [ip] * 9 + [vp, vp, ip, fp, ip]
         lib.attn_fwd.argtypes = common + [vp]
-        lib.attn_fwd_varlen.argtypes = common + [vp]
+        lib.attn_fwd_varlen.argtypes = varlen + [vp]
         lib.attn_fwd_algo.argtypes = common + [ip, vp]
-        lib.attn_fwd_varlen_algo.argtypes = common + [ip, vp]
+        lib.attn_fwd_varlen_algo.argtypes = varlen + [ip, vp]
         for f in (lib.attn_fwd, lib.attn_fwd_varlen, lib.attn_fwd_algo, lib.attn_fwd_varlen_algo):
             f.restype = ip
         lib.attn_lse_combine.argtypes = [vp, vp, vp, vp, ip, ctypes.c_longlong, ip, ip, vp]
@@ -164,7 +165,7 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_q, max_k, o=None, l
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     rc = lib.attn_fwd_varlen_algo(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv,
-                                  int(max_q), int(max_k), D, Dv, _ptr(cu_seqlens_q),
+                                  Tq, Tk, int(max_q), int(max_k), D, Dv, _ptr(cu_seqlens_q),
                                   _ptr(cu_seqlens_k), int(window), float(scale),
                                   _DTYPE_CODE[q.dtype], ALGOS[algo], _stream_ptr(stream))
     _check(rc)

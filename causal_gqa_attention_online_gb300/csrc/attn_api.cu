@@ -221,7 +221,8 @@ int run(AttnParams &p, int dtype, int algo, cudaStream_t stream) {
 }
 
 int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
-               int Hkv, int Q, int K, int D, int Dv, const int32_t *seqlens_q,
+               int Hkv, long long Tq, long long Tk, int Q, int K, int D, int Dv,
+               const int32_t *seqlens_q,
                const int32_t *seqlens_k, const int32_t *cu_q, const int32_t *cu_k, int window,
                float scale, int dtype, int algo, cudaStream_t stream) {
     g_last_error[0] = '\0';
@@ -241,6 +242,8 @@ int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
     p.G = Hq / Hkv;
     p.Q = Q;
     p.K = K;
+    p.Tq = Tq;
+    p.Tk = Tk;
     p.D = D;
     p.Dv = Dv;
     p.seqlens_q = seqlens_q;
@@ -268,7 +271,8 @@ int attn_fwd_algo(const void *q, const void *k, const void *v, void *o, float *l
                   int Hq, int Hkv, int Q, int K, int D, int Dv, const int32_t *seqlens_q,
                   const int32_t *seqlens_k, int window, float scale, int dtype, int algo,
                   attn_stream_t stream) {
-    return fwd_common(q, k, v, o, lse, B, Hq, Hkv, Q, K, D, Dv, seqlens_q, seqlens_k, nullptr,
+    return fwd_common(q, k, v, o, lse, B, Hq, Hkv, (long long)B * Q, (long long)B * K, Q, K, D, Dv,
+                      seqlens_q, seqlens_k, nullptr,
                       nullptr, window, scale, dtype, algo, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -281,23 +285,31 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
 }
 
 int attn_fwd_varlen_algo(const void *q, const void *k, const void *v, void *o, float *lse,
-                         int B, int Hq, int Hkv, int max_Q, int max_K, int D, int Dv,
-                         const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int window,
-                         float scale, int dtype, int algo, attn_stream_t stream) {
+                         int B, int Hq, int Hkv, int total_q, int total_k, int max_Q, int max_K,
+                         int D, int Dv, const int32_t *cu_seqlens_q,
+                         const int32_t *cu_seqlens_k, int window, float scale, int dtype,
+                         int algo, attn_stream_t stream) {
     if (B > 0 && (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr)) {
         attn::set_error("cu_seqlens_q and cu_seqlens_k must be non-null");
         return ATTN_ERR_INVALID;
     }
-    return fwd_common(q, k, v, o, lse, B, Hq, Hkv, max_Q, max_K, D, Dv, nullptr, nullptr,
+    if (total_q < 0 || total_k < 0) {
+        attn::set_error("negative size (total_q=%d total_k=%d)", total_q, total_k);
+        return ATTN_ERR_INVALID;
+    }
+    if (total_q == 0) return ATTN_OK;
+    return fwd_common(q, k, v, o, lse, B, Hq, Hkv, total_q, total_k, max_Q, max_K, D, Dv,
+                      nullptr, nullptr,
                       cu_seqlens_q, cu_seqlens_k, window, scale, dtype, algo,
                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse, int B,
-                    int Hq, int Hkv, int max_Q, int max_K, int D, int Dv,
-                    const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int window,
-                    float scale, int dtype, attn_stream_t stream) {
-    return attn_fwd_varlen_algo(q, k, v, o, lse, B, Hq, Hkv, max_Q, max_K, D, Dv, cu_seqlens_q,
+                    int Hq, int Hkv, int total_q, int total_k, int max_Q, int max_K, int D,
+                    int Dv, const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                    int window, float scale, int dtype, attn_stream_t stream) {
+    return attn_fwd_varlen_algo(q, k, v, o, lse, B, Hq, Hkv, total_q, total_k, max_Q, max_K, D,
+                                Dv, cu_seqlens_q,
                                 cu_seqlens_k, window, scale, dtype, ATTN_ALGO_AUTO, stream);
 }
 

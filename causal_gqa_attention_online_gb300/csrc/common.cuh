@@ -32,6 +32,7 @@ struct AttnParams {
     float *lse;              // may be null
     int B, Hq, Hkv, G;       // G = Hq / Hkv
     int Q, K;                // padded capacities, or max lengths (packed)
+    long long Tq, Tk;        // rows of the q/o and k/v buffers (B*Q, B*K when padded)
     int D, Dv;
     const int32_t *seqlens_q;  // padded layout, may be null
     const int32_t *seqlens_k;  // padded layout, may be null
@@ -65,8 +66,9 @@ __device__ __forceinline__ SeqInfo seq_info(const AttnParams &p, int b) {
         const int k0 = __ldg(p.cu_k + b), k1 = __ldg(p.cu_k + b + 1);
         s.q_off = q0;
         s.k_off = k0;
-        s.Qb = clamp_len(q1 - q0, p.Q);
-        s.Kb = clamp_len(k1 - k0, p.K);
+        // a sequence never reaches past the buffers, whatever cu_seqlens holds
+        s.Qb = clamp_len(min((long long)(q1 - q0), p.Tq - q0), p.Q);
+        s.Kb = clamp_len(min((long long)(k1 - k0), p.Tk - k0), p.K);
     } else {
         s.q_off = (long long)b * p.Q;
         s.k_off = (long long)b * p.K;

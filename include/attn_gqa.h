@@ -109,16 +109,19 @@ ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *o, floa
 /*
  * attn_fwd_varlen -- packed layout.
  *   q [Tq, Hq, D]  k [Tk, Hkv, D]  v [Tk, Hkv, Dv]  o [Tq, Hq, Dv]  lse [Tq, Hq] (may be NULL)
+ *   total_q, total_k   rows of the packed buffers (Tq, Tk): bounds every read
+ *               and write; cu_seqlens_q[B] <= total_q, cu_seqlens_k[B] <= total_k.
  *   cu_seqlens_q, cu_seqlens_k   int32 [B+1], cu[0] = 0, non-decreasing:
  *               sequence b owns query rows [cu_q[b], cu_q[b+1]) and key rows
  *               [cu_k[b], cu_k[b+1]); an empty sequence owns none.
  *   max_Q, max_K   upper bounds of the per-sequence lengths (sizes the grid;
- *               rows beyond them are not computed).
+ *               a sequence longer than them is cut to its first max_Q query
+ *               rows / max_K key rows).
  * Other arguments and return codes as attn_fwd.  Rows outside every
  * sequence are not written.
  */
 ATTN_API int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse, int B,
-                    int Hq, int Hkv, int max_Q, int max_K, int D, int Dv,
+                    int Hq, int Hkv, int total_q, int total_k, int max_Q, int max_K, int D, int Dv,
                     const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int window,
                     float scale, int dtype, attn_stream_t stream);
 
@@ -129,7 +132,8 @@ ATTN_API int attn_fwd_algo(const void *q, const void *k, const void *v, void *o,
                   const int32_t *seqlens_k, int window, float scale, int dtype, int algo,
                   attn_stream_t stream);
 ATTN_API int attn_fwd_varlen_algo(const void *q, const void *k, const void *v, void *o, float *lse,
-                         int B, int Hq, int Hkv, int max_Q, int max_K, int D, int Dv,
+                         int B, int Hq, int Hkv, int total_q, int total_k, int max_Q, int max_K,
+                         int D, int Dv,
                          const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int window,
                          float scale, int dtype, int algo, attn_stream_t stream);
 

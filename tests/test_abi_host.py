@@ -74,7 +74,7 @@ def test_empty_problem_is_noop(lib):
 def test_varlen_requires_cu_seqlens(lib):
     vp = ctypes.c_void_p
     rc = lib.attn_fwd_varlen(vp(1 << 20), vp(1 << 21), vp(1 << 22), vp(1 << 23), None, 2, 4, 2,
-                             8, 8, 64, 64, None, None, 0, 0.125, 2, None)
+                             16, 16, 8, 8, 64, 64, None, None, 0, 0.125, 2, None)
     assert rc == 1 and "cu_seqlens" in lib.attn_last_error().decode()
 
 

@@ -132,3 +132,68 @@ def test_unsupported_algo_reports():
     with pytest.raises(AttnError) as ei:
         attn_fwd(inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), algo="tcgen05")
     assert ei.value.status == 2
+
+
+# ---------------------------------------------------------------------------
+# split-KV tensor-core decode
+
+DECODE_SHAPES = [
+    # B, Hq, Hkv, Q, K, D, Dv
+    (8, 32, 8, 1, 1024, 128, 128),
+    (3, 16, 2, 1, 700, 64, 64),      # G = 8
+    (2, 16, 1, 1, 333, 128, 64),     # MQA, G = 16 (two n-tiles)
+    (2, 8, 8, 1, 257, 64, 128),      # MHA
+    (2, 8, 2, 2, 300, 128, 128),     # two query rows per sequence (causal offset)
+    (1, 16, 4, 4, 129, 128, 128),    # Q*G = 16
+    (1, 8, 2, 1, 32768, 64, 64),     # long KV: many splits
+    (1, 16, 4, 1, 8193, 128, 128),
+]
+
+
+@pytest.mark.parametrize("shape", DECODE_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_decode_shapes(shape, dtype):
+    B, Hq, Hkv, Q, K, D, Dv = shape
+    g = np.random.default_rng(B * 131 + K)
+    sk = g.integers(0, K + 1, size=B).astype(np.int32)
+    sk[0] = K
+    inp = synth.make_padded(B, Hq, Hkv, Q, K, D, Dv, dtype, seed=21, seqlens_k=sk, pad_value=NAN)
+    parity.check(inp, "decode", f"decode {dtype} {shape}")
+
+
+@pytest.mark.parametrize("window", [1, 100, 1000])
+def test_decode_window(window):
+    sk = np.array([0, 5, 999, 1000, 2500], np.int32)
+    inp = synth.make_padded(5, 32, 8, 1, 2500, 128, 128, "bf16", seed=22, seqlens_k=sk,
+                            window=window, pad_value=NAN)
+    parity.check(inp, "decode", f"decode window {window}")
+
+
+def test_decode_reduction_lengths():
+    sk = np.array([0, 1, 7, 16, 31, 32, 33, 63, 64, 65, 127, 128, 129, 511, 512, 513], np.int32)
+    inp = synth.make_padded(16, 8, 2, 1, 600, 128, 128, "bf16", seed=23, seqlens_k=sk,
+                            pad_value=NAN)
+    parity.check(inp, "decode", "decode lengths")
+
+
+def test_decode_padded_query_rows():
+    # Q capacity 2 with Qb = 1 or 0: padded rows must be +0 / -inf
+    inp = synth.make_padded(3, 8, 2, 2, 200, 64, 64, "bf16", seed=24, seqlens_q=[1, 0, 2],
+                            seqlens_k=[200, 50, 0], pad_value=NAN)
+    parity.check(inp, "decode", "decode padded rows")
+
+
+def test_decode_varlen_packed():
+    sk = np.array([0, 1, 300, 4097, 64], np.int32)
+    sq = np.array([0, 1, 1, 1, 1], np.int32)
+    inp = synth.make_packed(sq, sk, 32, 8, 128, 128, "bf16", seed=25)
+    parity.check(inp, "decode", "decode packed")
+
+
+def test_decode_full_size_batched():
+    """bf16 batched decode B=64 Hq=32 Hkv=8 D=Dv=128, key lengths uniform on
+    [0, 8192], KV padded to 8192 (NaN in the padding): every row checked."""
+    inp = synth.decode_bf16_b64_h32x8_k8192_d128(pad_value=NAN)
+    o, lse = parity.run_gpu(inp, "auto")
+    rows = np.array([(b, 0, h) for b in range(inp.B) for h in range(inp.Hq)], np.int32)
+    parity.check_sampled_padded(inp, o, lse, rows, "decode full size")
