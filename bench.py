@@ -1,0 +1,403 @@
+"""Benchmark of the causal GQA attention forward on one GB300 (or N, one
+process per GPU under torchrun: weak scaling, each rank runs its own copy of
+the workload, no data-path collective).
+
+Headline workload (value): bf16 causal prefill B=4 Hq=32 Hkv=8 Q=K=4096
+D=Dv=128, TFLOP/s counted over legal (query, key) pairs only:
+FLOP = B * Hq * pairs * (2*D + 2*Dv).
+Second workload (the "decode" object): bf16 batched decode B=64 Hq=32 Hkv=8
+Q=1 D=Dv=128, key lengths uniform on [0, 8192] (0 included), KV padded to
+8192, KV GB/s counted over valid key rows: bytes = sum_b Kb * Hkv * (D+Dv) * 2.
+
+Timing: W warm-up steps, then K timed steps; before every step a 512 MiB
+buffer is written to flush L2, and each step is bracketed by CUDA events on
+the launching stream (device time of the attention call only); a barrier and
+a device synchronize bracket the timed region; the max over ranks is taken.
+The e2e figures time the same call through the public API with the inputs
+copied in from pinned host memory and O / LSE copied back, every step.
+
+``--impl reference`` times the CPU oracle (fp64, all host cores) on a bounded
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal GQA attention TFLOP/s (prefill) and KV GB/s (decode) on 1 GB300"
+PREFILL = dict(B=4, Hq=32, Hkv=8, Q=4096, K=4096, D=128, Dv=128)
+DECODE = dict(B=64, Hq=32, Hkv=8, Q=1, K=8192, D=128, Dv=128)
+PREFILL_NAME = "bf16 causal prefill B=4 Hq=32 Hkv=8 Q=K=4096 D=Dv=128"
+DECODE_NAME = ("bf16 batched decode B=64 Hq=32 Hkv=8 Q=1 D=Dv=128, key lengths U[0,8192], "
+               "KV padded to 8192")
+FLUSH_BYTES = 512 << 20
+
+
+def legal_pairs(Qb: int, Kb: int, window: int = 0) -> int:
+    """Legal (query, key) pairs of one sequence and head (closed form)."""
+    total = 0
+    if Qb <= 0 or Kb <= 0:
+        return 0
+    # row q sees keys [lo, hi) with hi = min(q + Kb - Qb + 1, Kb), lo = max(0, hi' - window)
+    for q in range(Qb):
+        diag = q + Kb - Qb
+        hi = min(diag + 1, Kb)
+        lo = max(0, diag - window + 1) if window > 0 else 0
+        total += max(0, hi - lo)
+    return total
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_steps(fn, steps, warmup, flush, stream):
+    """Per-step device time (ms) of fn() with an L2 flush before each step."""
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def run_gpu(args, world, rank, local):
+    import causal_gqa_attention_online_gb300 as attn
+    from causal_gqa_attention_online_gb300 import build_ext, synth
+
+    build_ext.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    hbm_peak, tf_peak, peak_src = measured_peaks()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    # ---------------- prefill (headline) ----------------
+    P = PREFILL
+    pin = synth.prefill_bf16_b4_h32x8_s4096_d128(seed=1234 + rank)
+    q, k, v = pin.q.to(dev), pin.k.to(dev), pin.v.to(dev)
+    o = torch.empty((P["B"], P["Q"], P["Hq"], P["Dv"]), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((P["B"], P["Q"], P["Hq"]), dtype=torch.float32, device=dev)
+    flop = P["B"] * P["Hq"] * legal_pairs(P["Q"], P["K"]) * (2 * P["D"] + 2 * P["Dv"])
+
+    def prefill():
+        attn.attn_fwd(q, k, v, o, lse, stream=stream)
+
+    prefill()
+    torch.cuda.synchronize()
+    n0 = attn.kernel_launches()
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        times = time_steps(prefill, args.steps, args.warmup, flush, stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    launches_prefill = (attn.kernel_launches() - n0) // (args.steps + args.warmup)
+    ms = max_over_ranks(sum(times) / len(times), world)
+    value = world * flop / (ms * 1e-3) / 1e12
+
+    # e2e: pinned host inputs copied in, O / LSE copied back, every step
+    hq, hk, hv = pin.q.pin_memory(), pin.k.pin_memory(), pin.v.pin_memory()
+    ho, hl = torch.empty_like(o, device="cpu").pin_memory(), torch.empty_like(lse, device="cpu").pin_memory()
+
+    def prefill_e2e():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        attn.attn_fwd(q, k, v, o, lse, stream=stream)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    e2e_times = time_steps(prefill_e2e, max(3, args.steps // 2), 2, flush, stream)
+    e2e_ms = max_over_ranks(sum(e2e_times) / len(e2e_times), world)
+    h2d = (q.numel() + k.numel() + v.numel()) * 2
+    d2h = o.numel() * 2 + lse.numel() * 4
+
+    # ---------------- decode ----------------
+    Dd = DECODE
+    din = synth.decode_bf16_b64_h32x8_k8192_d128(seed=1234 + rank)
+    dq, dk, dv = din.q.to(dev), din.k.to(dev), din.v.to(dev)
+    dsk = torch.from_numpy(din.seqlens_k).to(dev)
+    do = torch.empty((Dd["B"], 1, Dd["Hq"], Dd["Dv"]), dtype=torch.bfloat16, device=dev)
+    dl = torch.empty((Dd["B"], 1, Dd["Hq"]), dtype=torch.float32, device=dev)
+    kv_bytes = int(din.seqlens_k.astype(np.int64).sum()) * Dd["Hkv"] * (Dd["D"] + Dd["Dv"]) * 2
+
+    def decode():
+        attn.attn_fwd(dq, dk, dv, do, dl, seqlens_k=dsk, stream=stream)
+
+    decode()
+    torch.cuda.synchronize()
+    n1 = attn.kernel_launches()
+    barrier(world)
+    dtimes = time_steps(decode, args.steps, args.warmup, flush, stream)
+    barrier(world)
+    launches_decode = (attn.kernel_launches() - n1) // (args.steps + args.warmup)
+    dms = max_over_ranks(sum(dtimes) / len(dtimes), world)
+    dvalue = world * kv_bytes / (dms * 1e-3) / 1e9
+    hdq, hdk, hdv = din.q.pin_memory(), din.k.pin_memory(), din.v.pin_memory()
+    hdo = torch.empty_like(do, device="cpu").pin_memory()
+    hdl = torch.empty_like(dl, device="cpu").pin_memory()
+
+    def decode_e2e():
+        dq.copy_(hdq, non_blocking=True)
+        dk.copy_(hdk, non_blocking=True)
+        dv.copy_(hdv, non_blocking=True)
+        attn.attn_fwd(dq, dk, dv, do, dl, seqlens_k=dsk, stream=stream)
+        hdo.copy_(do, non_blocking=True)
+        hdl.copy_(dl, non_blocking=True)
+
+    de2e = time_steps(decode_e2e, max(3, args.steps // 2), 2, flush, stream)
+    de2e_ms = max_over_ranks(sum(de2e) / len(de2e), world)
+    dh2d = (dq.numel() + dk.numel() + dv.numel()) * 2
+    dd2h = do.numel() * 2 + dl.numel() * 4
+
+    traffic = load_traffic()
+    result = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: N(0,1) seeded (PCG64), bf16 round-to-nearest",
+        "config": {"workload": PREFILL_NAME, "B": P["B"], "Hq": P["Hq"], "Hkv": P["Hkv"],
+                   "seq_len": P["Q"], "D": P["D"], "Dv": P["Dv"], "global_batch": P["B"] * world,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "512 MiB buffer written before every timed step",
+                   "flop_per_step": flop},
+        "roofline": {"bound": "tensor", "achieved": round(flop / (ms * 1e-3) / 1e12, 3),
+                     "peak": tf_peak, "unit": "TFLOP/s",
+                     "frac": round(flop / (ms * 1e-3) / 1e12 / tf_peak, 4),
+                     "traffic": traffic.get("prefill"),
+                     "peak_source": f"{peak_src} bf16 dense (cuBLAS burst)"},
+        "e2e": {"value": round(world * flop / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches_prefill * args.steps),
+        "clocks": clk.summary(),
+        "decode": {
+            "workload": DECODE_NAME, "metric": "KV GB/s", "value": round(dvalue, 2),
+            "unit": "GB/s", "ms_per_step": round(dms, 5), "kv_bytes_per_step": kv_bytes,
+            "gpu_launches": int(launches_decode * args.steps),
+            "roofline": {"bound": "hbm", "achieved": round(kv_bytes / (dms * 1e-3) / 1e9, 2),
+                         "peak": hbm_peak, "unit": "GB/s",
+                         "frac": round(kv_bytes / (dms * 1e-3) / 1e9 / hbm_peak, 4),
+                         "traffic": traffic.get("decode"),
+                         "peak_source": f"{peak_src} HBM copy"},
+            "e2e": {"value": round(world * kv_bytes / (de2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "ms_per_step": round(de2e_ms, 4), "h2d_bytes_per_step": dh2d,
+                    "d2h_bytes_per_step": dd2h},
+        },
+    }
+    return result, pin
+
+
+def load_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, if current."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return {}
+    with open(path) as f:
+        return json.load(f)
+
+
+def oracle_sample_rate(inp, rows_budget_s=12.0, nthreads=0, seed=0):
+    """Time the CPU oracle on random query rows of the prefill workload until
+    about ``rows_budget_s`` seconds of work; returns (TFLOP/s, rows, secs, threads)."""
+    import oracle
+    from causal_gqa_attention_online_gb300 import synth
+
+    q32 = synth.exact_f32(inp.q)
+    k32 = synth.exact_f32(inp.k)
+    v32 = synth.exact_f32(inp.v)
+    g = np.random.default_rng(seed)
+    P = PREFILL
+    total_flop, total_s, nrows = 0, 0.0, 0
+    batch = 2048
+    while total_s < rows_budget_s:
+        rows = np.stack([g.integers(0, P["B"], batch), g.integers(0, P["Q"], batch),
+                         g.integers(0, P["Hq"], batch)], axis=1).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.attn_padded_rows(q32, k32, v32, rows, B=P["B"], Hq=P["Hq"], Hkv=P["Hkv"],
+                                Q=P["Q"], K=P["K"], D=P["D"], Dv=P["Dv"], nthreads=nthreads)
+        total_s += time.perf_counter() - t0
+        # row q of a Q=K problem sees q+1 keys
+        total_flop += int((rows[:, 1].astype(np.int64) + 1).sum()) * (2 * P["D"] + 2 * P["Dv"])
+        nrows += batch
+    threads = nthreads if nthreads > 0 else oracle.max_threads()
+    return total_flop / total_s / 1e12, nrows, total_s, threads
+
+
+def run_reference(args, world, rank):
+    from causal_gqa_attention_online_gb300 import synth
+    if rank != 0:
+        return None
+    inp = synth.prefill_bf16_b4_h32x8_s4096_d128(seed=1234)
+    P = PREFILL
+    per_step_s = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    rates = []
+    for i in range(args.warmup + args.steps):
+        r, nrows, secs, threads = oracle_sample_rate(inp, per_step_s, seed=i)
+        if i >= args.warmup:
+            rates.append(r)
+    value = statistics.mean(rates)
+    flop = P["B"] * P["Hq"] * legal_pairs(P["Q"], P["K"]) * (2 * P["D"] + 2 * P["Dv"])
+    sample = (f"random (b, q, h) rows of the prefill workload, batches of 2048 rows, "
+              f"~{per_step_s:.1f} s of oracle work per step")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": flop / (value * 1e12) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": PREFILL_NAME},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+        if res is not None:
+            print(json.dumps(res))
+        return
+    res, pin = run_gpu(args, world, rank, local)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            r, nrows, secs, threads = oracle_sample_rate(pin, 12.0)
+            res["cpu_baseline"] = {
+                "value": r, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                "sample": f"{nrows} random (b, q, h) rows of the prefill workload, {secs:.1f} s"}
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

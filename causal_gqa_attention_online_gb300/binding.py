@@ -22,7 +22,8 @@ ALGOS = {"auto": 0, "generic": 1, "tcgen05": 2, "decode": 3}
 _DTYPE_CODE = {torch.float32: ATTN_F32, torch.float16: ATTN_F16, torch.bfloat16: ATTN_BF16}
 
 EXPORTED = ("attn_fwd", "attn_fwd_varlen", "attn_fwd_algo", "attn_fwd_varlen_algo",
-            "attn_lse_combine", "attn_last_error", "attn_device_status", "attn_version")
+            "attn_lse_combine", "attn_last_error", "attn_device_status", "attn_kernel_launches",
+            "attn_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -67,6 +68,8 @@ def load_library(path: str | None = None):
         lib.attn_last_error.restype = ctypes.c_char_p
         lib.attn_device_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
         lib.attn_device_status.restype = ip
+        lib.attn_kernel_launches.argtypes = []
+        lib.attn_kernel_launches.restype = ctypes.c_ulonglong
         lib.attn_version.argtypes = []
         lib.attn_version.restype = ctypes.c_char_p
         _lib = lib
@@ -75,6 +78,11 @@ def load_library(path: str | None = None):
 
 def last_error() -> str:
     return load_library().attn_last_error().decode()
+
+
+def kernel_launches() -> int:
+    """Kernels the library has launched in this process so far."""
+    return int(load_library().attn_kernel_launches())
 
 
 def device_status() -> tuple[int, int]:

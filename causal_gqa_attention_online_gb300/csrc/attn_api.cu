@@ -1,6 +1,7 @@
 // attn_api.cu -- the C ABI of libattn_gqa: argument validation, kernel choice,
 // split-KV workspace from a library-owned stream-ordered pool, error strings
 // and the device status word.  Declarations and contracts: include/attn_gqa.h.
+#include <atomic>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -22,6 +23,10 @@ cudaMemPool_t g_pools[kMaxDevices] = {};
 int *g_status_ptr[kMaxDevices] = {};
 int g_sm_count[kMaxDevices] = {};
 }  // namespace
+
+std::atomic<unsigned long long> g_launches{0};
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 // The device status word (one per device, in this module's device image).
 __device__ int g_device_status;
@@ -359,6 +364,10 @@ int attn_device_status(int *detail) {
     }
     if (detail) *detail = value;
     return value == 0 ? ATTN_OK : ATTN_ERR_TIMEOUT;
+}
+
+unsigned long long attn_kernel_launches(void) {
+    return g_launches.load(std::memory_order_relaxed);
 }
 
 const char *attn_version(void) { return "0.1.0"; }

@@ -376,6 +376,7 @@ int launch_decode_t(const AttnParams &p, cudaStream_t stream) {
         set_error("decode kernel launch: %s", cudaGetErrorString(e));
         return 3;
     }
+    count_launch();
     return 0;
 }
 

@@ -254,6 +254,7 @@ int launch_generic_t(const AttnParams &p, cudaStream_t stream) {
         set_error("generic kernel launch: %s", cudaGetErrorString(e));
         return 3;
     }
+    count_launch();
     return 0;
 }
 
@@ -297,6 +298,7 @@ int launch_combine_rows(const AttnParams &p, int dtype, cudaStream_t stream) {
         set_error("combine kernel launch: %s", cudaGetErrorString(e));
         return 3;
     }
+    count_launch();
     return 0;
 }
 
@@ -324,6 +326,7 @@ int launch_combine_flat(const float *o_parts, const float *lse_parts, void *o, f
         set_error("combine kernel launch: %s", cudaGetErrorString(e));
         return 3;
     }
+    count_launch();
     return 0;
 }
 

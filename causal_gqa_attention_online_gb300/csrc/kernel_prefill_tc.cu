@@ -1,12 +1,677 @@
-// kernel_prefill_tc.cu -- tcgen05/TMEM prefill (placeholder until the kernel
-// lands; the generic kernel serves every shape meanwhile).
+// kernel_prefill_tc.cu -- bf16 / fp16 causal GQA prefill on the 5th-generation
+// tensor cores (tcgen05, TMEM accumulators, TMA-fed shared memory), sm_103a.
+//
+// What it computes is the online-softmax program of "Attention execution
+// mapping" (LuisaCompute), sections 1-2: per KV block QK^T -> mask -> max ->
+// exp -> sum -> alpha-rescale -> PV, with the row max / row sum / accumulator
+// carried across blocks.  How it runs it is GB300-specific:
+//
+// * Persistent CTAs, one per SM, walk work units (sequence, KV head, head
+//   subgroup, query block) in longest-first order (bottom-right causal: the
+//   last query blocks see the most keys).
+// * A unit holds two Q tiles of 128 rows.  The rows of a tile are
+//   (query position, head) pairs with up to 16 heads of one KV group packed
+//   together, so every K/V tile brought in by TMA serves all of those heads
+//   (the cross-head KV reuse of the same page, section 5).
+// * Warp roles: warps 0-3 and 4-7 are the softmax warpgroups of Q tile 0 and
+//   Q tile 1 (TMEM lane = row = thread); warp 8 issues tcgen05.mma from one
+//   thread; warp 9 issues TMA loads from one thread.
+// * TMEM (512 columns): S0 | S1 | O0 | O1.  S_t = Q_t K^T accumulates in fp32;
+//   the softmax writes P_t as bf16/fp16 pairs over the first half of S_t and
+//   the PV MMA reads P_t straight from TMEM (A operand in TMEM, V from shared
+//   memory as an MN-major operand).  While one warpgroup runs its softmax the
+//   tensor core works on the other tile (the dual-pipeline idea of the FlyDSL
+//   FMHA forward on the "Accelerating PyTorch on AMD GPUs with FlyDSL" page,
+//   rebuilt around TMEM and an MMA-issuing warp).
+// * K/V tiles stream through a ring of shared-memory stages with
+//   full/empty mbarriers; Q tiles are reloaded per unit.
+// * The O rescale by alpha = exp2(m_old - m_new) is skipped unless the row
+//   max grows by more than 2^8: the stale max is kept and the final
+//   normalisation uses the same reference, so the result is unchanged.
+// * Every mbarrier wait is bounded; a wait that runs out records a status,
+//   raises an abort flag, and the CTA drains its copies and frees TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+
 #include "common.cuh"
 #include "launch.h"
+#include "sm100_ptx.cuh"
 
 namespace attn {
-bool prefill_tc_supported(const AttnParams &, int) { return false; }
-int launch_prefill_tc(const AttnParams &, int, cudaStream_t) {
-    set_error("tcgen05 prefill kernel not built");
-    return 2;
+namespace {
+
+using namespace sm100;
+
+constexpr int kBM = 128;  // rows per Q tile (MMA M)
+constexpr int kBN = 128;  // keys per KV tile
+constexpr int kThreads = 320;
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint32_t kChunkBytes = 128 * 128;       // one 128-row x 128-byte swizzled chunk
+
+struct PrefillArgs {
+    AttnParams p;
+    int Gp;            // heads packed into the rows of a Q tile
+    int QP;            // query positions per Q tile (kBM / Gp)
+    int nsub;          // head subgroups per KV head (G / Gp)
+    int nqblk;         // query blocks (2 * QP positions) per sequence
+    long long nunits;
+    float c_scale;     // |scale| * log2(e)  (> 0)
+    uint32_t idesc_s;  // S = Q K^T
+    uint32_t idesc_o;  // O += P V
+};
+
+template <int D, int DV> struct Layout {
+    static constexpr int QTILE = kBM * D * 2;
+    static constexpr int KTILE = kBN * D * 2;
+    static constexpr int VTILE = kBN * DV * 2;
+    static constexpr int STAGE = KTILE > VTILE ? KTILE : VTILE;
+    static constexpr int BUDGET = 225 * 1024;
+    static constexpr int NS_FIT = (BUDGET - 2 * QTILE - 1024 - 512) / STAGE;
+    static constexpr int NS = NS_FIT > 8 ? 8 : NS_FIT;
+    static constexpr int Q_OFF = 0;
+    static constexpr int KV_OFF = 2 * QTILE;
+    static constexpr int BAR_OFF = KV_OFF + NS * STAGE;
+    static constexpr int SMEM = 1024 + BAR_OFF + 512;  // + alignment slack
+    static constexpr int O_COL = 256;                  // TMEM columns: S0 S1 | O0 O1
+    static_assert(NS >= 2, "K/V ring needs two stages");
+    static_assert(O_COL + 2 * DV <= 512, "TMEM budget");
+};
+
+// Barrier slots (8 bytes each) after the K/V ring.
+enum : int {
+    B_Q_FULL = 0,
+    B_Q_EMPTY = 1,
+    B_S_FULL = 2,    // [2]
+    B_P_READY = 4,   // [2]
+    B_O_FULL = 6,    // [2]
+    B_O_EMPTY = 8,   // [2]
+    B_TEARDOWN = 10,
+    B_KV_FULL = 11,  // [NS]
+};
+
+struct UnitInfo {
+    int b, kvh, h0, q0;  // first head of the packed subgroup, first query position
+    SeqInfo si;
+    int n_kv;            // KV tiles
+    int kv_start;        // first key of tile 0
+    int lo_last, hi_first;  // interior test: all rows legal on [lo_last, hi_first)
+    int hi_unit;         // one past the last key any row uses
+    bool all_valid;      // every row of both tiles holds a real query
+};
+
+__device__ __forceinline__ UnitInfo unit_info(const PrefillArgs &a, long long u) {
+    const AttnParams &p = a.p;
+    const long long per = (long long)p.B * p.Hkv * a.nsub;
+    const int qblk = a.nqblk - 1 - (int)(u / per);
+    const int rest = (int)(u % per);
+    UnitInfo x;
+    x.b = rest / (p.Hkv * a.nsub);
+    x.kvh = (rest / a.nsub) % p.Hkv;
+    x.h0 = x.kvh * p.G + (rest % a.nsub) * a.Gp;
+    x.q0 = qblk * 2 * a.QP;
+    x.si = seq_info(p, x.b);
+    x.n_kv = 0;
+    x.kv_start = 0;
+    x.lo_last = INT_MAX;
+    x.hi_first = INT_MIN;
+    x.hi_unit = 0;
+    x.all_valid = false;
+    if (x.q0 >= x.si.Qb) return x;
+    const int q_last = min(x.q0 + 2 * a.QP, x.si.Qb) - 1;
+    int lo_f, hi_f, lo_l, hi_l;
+    legal_range(x.q0, x.si.Qb, x.si.Kb, p.window, lo_f, hi_f);
+    legal_range(q_last, x.si.Qb, x.si.Kb, p.window, lo_l, hi_l);
+    if (hi_l <= lo_f) return x;
+    x.kv_start = lo_f;
+    x.hi_unit = hi_l;
+    x.n_kv = (hi_l - lo_f + kBN - 1) / kBN;
+    x.lo_last = lo_l;
+    x.hi_first = hi_f;
+    x.all_valid = x.q0 + 2 * a.QP <= x.si.Qb;
+    return x;
 }
+
+template <typename T> __device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+template <> __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    const bool ok = mbar_wait(bar, parity, abort_flag, kWaitLimitNs);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void raise_abort(volatile int *abort_flag, int *status, int code) {
+    *abort_flag = 1;
+    report_status(status, code);
+}
+
+template <typename T, int D, int DV>
+__global__ void __maxnreg__(200)
+    prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tmQ,
+                      const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV) {
+    using L = Layout<D, DV>;
+    constexpr int NS = L::NS;
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment for the 128-byte-swizzle atoms
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    const uint32_t q_smem = base + L::Q_OFF;
+    const uint32_t kv_smem = base + L::KV_OFF;
+    const uint32_t bars = base + L::BAR_OFF;
+    auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + L::BAR_OFF + 8 * (B_KV_FULL + 2 * NS));
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const AttnParams &p = a.p;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(B_Q_FULL), 1);
+        mbar_init(bar(B_Q_EMPTY), 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(B_S_FULL + t), 1);
+            mbar_init(bar(B_P_READY + t), 128);
+            mbar_init(bar(B_O_FULL + t), 1);
+            mbar_init(bar(B_O_EMPTY + t), 128);
+        }
+        mbar_init(bar(B_TEARDOWN), 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(bar(B_KV_FULL + s), 1);
+            mbar_init(bar(B_KV_FULL + NS + s), 1);  // kv_empty
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_addr(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    if (warp == kLoadWarp && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    auto kv_full = [&](int s) { return bar(B_KV_FULL + s); };
+    auto kv_empty = [&](int s) { return bar(B_KV_FULL + NS + s); };
+    auto stage = [&](int s) { return kv_smem + (uint32_t)s * L::STAGE; };
+    const bool padded = p.cu_q == nullptr;
+
+    if (warp == kLoadWarp) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t kv_it = 0, q_ph = 0;
+            int last_q_parity = -1;
+            int last_kv_parity[8];
+            for (int s = 0; s < 8; ++s) last_kv_parity[s] = -1;
+            bool ok = true;
+            for (long long u = blockIdx.x; u < a.nunits && ok; u += gridDim.x) {
+                const UnitInfo x = unit_info(a, u);
+                if (x.n_kv == 0) continue;
+                const int qrow = (padded ? 0 : (int)x.si.q_off) + x.q0;
+                const int krow = padded ? 0 : (int)x.si.k_off;
+                const int bc = padded ? x.b : 0;
+                if (!mbar_wait(bar(B_Q_EMPTY), q_ph ^ 1u, abort_flag, kWaitLimitNs)) {
+                    raise_abort(abort_flag, p.status, kStatusTimeoutQ);
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(bar(B_Q_FULL), 2 * L::QTILE);
+                last_q_parity = (int)q_ph;
+                q_ph ^= 1u;
+                for (int t = 0; t < 2; ++t)
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_load_4d(q_smem + t * L::QTILE + c * kChunkBytes, &tmQ, bar(B_Q_FULL),
+                                    c * 64, x.h0, qrow + t * a.QP, bc);
+                for (int j = 0; j < x.n_kv && ok; ++j) {
+                    const int k0 = x.kv_start + j * kBN;
+#pragma unroll
+                    for (int which = 0; which < 2; ++which) {
+                        const uint32_t it = kv_it++;
+                        const int s = (int)(it % NS);
+                        const uint32_t ph = (it / NS) & 1u;
+                        if (!mbar_wait(kv_empty(s), ph ^ 1u, abort_flag, kWaitLimitNs)) {
+                            raise_abort(abort_flag, p.status, kStatusTimeoutKvEmpty);
+                            ok = false;
+                            break;
+                        }
+                        if (which == 0) {
+                            mbar_arrive_expect_tx(kv_full(s), L::KTILE);
+                            for (int c = 0; c < D / 64; ++c)
+                                tma_load_4d(stage(s) + c * kChunkBytes, &tmK, kv_full(s), c * 64,
+                                            x.kvh, krow + k0, bc);
+                        } else {
+                            mbar_arrive_expect_tx(kv_full(s), L::VTILE);
+                            for (int c = 0; c < DV / 64; ++c)
+                                tma_load_4d(stage(s) + c * kChunkBytes, &tmV, kv_full(s), c * 64,
+                                            x.kvh, krow + k0, bc);
+                        }
+                        last_kv_parity[s] = (int)ph;
+                    }
+                }
+            }
+            // Drain: every copy this thread issued has landed before the CTA exits.
+            if (last_q_parity >= 0)
+                mbar_wait(bar(B_Q_FULL), (uint32_t)last_q_parity, abort_flag, kWaitLimitNs);
+            for (int s = 0; s < NS; ++s)
+                if (last_kv_parity[s] >= 0)
+                    mbar_wait(kv_full(s), (uint32_t)last_kv_parity[s], abort_flag, kWaitLimitNs);
+        }
+    } else if (warp == kMmaWarp) {
+        // --------------------------------------------------- MMA issuer
+        uint32_t kv_it = 0, q_ph = 0;
+        uint32_t p_ph[2] = {0u, 0u}, oe_ph[2] = {0u, 0u};
+        bool ok = true;
+        const uint32_t s_col[2] = {0u, 128u};
+        const uint32_t o_col[2] = {(uint32_t)L::O_COL, (uint32_t)(L::O_COL + DV)};
+        for (long long u = blockIdx.x; u < a.nunits && ok; u += gridDim.x) {
+            const UnitInfo x = unit_info(a, u);
+            if (x.n_kv == 0) continue;
+            if (!warp_wait(bar(B_Q_FULL), q_ph, abort_flag)) {
+                if (lane == 0) raise_abort(abort_flag, p.status, kStatusTimeoutMma);
+                ok = false;
+                break;
+            }
+            q_ph ^= 1u;
+            const uint32_t kb = kv_it;
+
+            auto issue_s = [&](int t, int kslot) {
+                if (lane == 0) {
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk / 4) * kChunkBytes + (kk % 4) * 32;
+                        mma_ss(tmem + s_col[t], sw128_desc(q_smem + t * L::QTILE + off, 16, 1024),
+                               sw128_desc(stage(kslot) + off, 16, 1024), a.idesc_s, kk > 0);
+                    }
+                    mma_commit(bar(B_S_FULL + t));
+                }
+                __syncwarp();
+            };
+            // O_t += P_t V_jj
+            auto issue_pv = [&](int t, int jj) -> bool {
+                if (!warp_wait(bar(B_P_READY + t), p_ph[t], abort_flag)) return false;
+                p_ph[t] ^= 1u;
+                if (jj == 0) {  // the previous unit's epilogue has read O_t
+                    if (!warp_wait(bar(B_O_EMPTY + t), oe_ph[t] ^ 1u, abort_flag)) return false;
+                    oe_ph[t] ^= 1u;
+                }
+                const uint32_t it = kb + 2u * (uint32_t)jj + 1u;
+                const int vslot = (int)(it % NS);
+                if (t == 0) {
+                    if (!warp_wait(kv_full(vslot), (it / NS) & 1u, abort_flag)) return false;
+                    // rows past the last key any row uses may hold anything
+                    // (NaN included): zero them so 0 * V stays 0
+                    const int k0 = x.kv_start + jj * kBN;
+                    const int nzero = k0 + kBN - x.hi_unit;
+                    if (nzero > 0) {
+                        uint8_t *vt = gbase + (stage(vslot) - base);
+                        for (int i = lane; i < nzero * 8 * (DV / 64); i += 32) {
+                            const int c = i / (nzero * 8), rem = i % (nzero * 8);
+                            const int row = kBN - nzero + rem / 8;
+                            *reinterpret_cast<uint4 *>(vt + c * kChunkBytes + row * 128 +
+                                                       (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
+                }
+                tc_fence_after();
+                if (lane == 0) {
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        mma_ts(tmem + o_col[t], tmem + s_col[t] + kk * 8,
+                               sw128_desc(stage(vslot) + kk * 2048, kChunkBytes, 1024), a.idesc_o,
+                               (jj > 0 || kk > 0) ? 1u : 0u);
+                }
+                __syncwarp();
+                return true;
+            };
+
+            for (int j = 0; j < x.n_kv && ok; ++j) {
+                const uint32_t it = kb + 2u * (uint32_t)j;
+                const int kslot = (int)(it % NS);
+                if (!warp_wait(kv_full(kslot), (it / NS) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (j > 0 && !issue_pv(0, j - 1)) {
+                    ok = false;
+                    break;
+                }
+                issue_s(0, kslot);
+                if (j > 0) {
+                    if (!issue_pv(1, j - 1)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) mma_commit(kv_empty((int)((it - 1) % NS)));  // V_{j-1}
+                }
+                issue_s(1, kslot);
+                if (lane == 0) {
+                    mma_commit(kv_empty(kslot));                        // K_j
+                    if (j == x.n_kv - 1) mma_commit(bar(B_Q_EMPTY));   // Q tiles free
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (!issue_pv(0, x.n_kv - 1)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) mma_commit(bar(B_O_FULL + 0));
+            if (!issue_pv(1, x.n_kv - 1)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                mma_commit(bar(B_O_FULL + 1));
+                mma_commit(kv_empty((int)((kb + 2u * (uint32_t)x.n_kv - 1u) % NS)));
+            }
+            __syncwarp();
+            kv_it += 2u * (uint32_t)x.n_kv;
+        }
+        if (!ok && lane == 0) raise_abort(abort_flag, p.status, kStatusTimeoutMma);
+        // all MMAs issued by this warp complete before TMEM is released
+        if (lane == 0) {
+            mma_commit(bar(B_TEARDOWN));
+            mbar_wait(bar(B_TEARDOWN), 0, abort_flag, kWaitLimitNs);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------- softmax warpgroups
+        const int t = warp >> 2;                 // Q tile of this warpgroup
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;       // row of the tile = TMEM lane
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tS = tmem + lane_off + (uint32_t)(t * 128);
+        const uint32_t tO = tmem + lane_off + (uint32_t)(L::O_COL + t * DV);
+        const float c = a.c_scale;
+        uint32_t s_ph = 0, o_ph = 0;
+        bool ok = true;
+        T *og = static_cast<T *>(p.o);
+
+        for (long long u = blockIdx.x; u < a.nunits && ok; u += gridDim.x) {
+            const UnitInfo x = unit_info(a, u);
+            const int qpos = x.q0 + t * a.QP + r / a.Gp;
+            const int head = x.h0 + r % a.Gp;
+            const bool valid = qpos < x.si.Qb;
+            const bool writes = padded ? qpos < p.Q : valid;
+            int lo = 0, hi = 0;
+            if (valid) legal_range(qpos, x.si.Qb, x.si.Kb, p.window, lo, hi);
+            const long long orow = (x.si.q_off + qpos) * p.Hq + head;
+
+            if (x.n_kv == 0) {  // nothing to attend: +0 and -inf
+                if (writes) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(og + orow * DV);
+#pragma unroll
+                    for (int i = 0; i < DV * 2 / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+                    if (p.lse) p.lse[orow] = -INFINITY;
+                }
+                continue;
+            }
+
+            float m_run = -INFINITY, l_run = 0.f;
+            for (int j = 0; j < x.n_kv; ++j) {
+                if (!warp_wait(bar(B_S_FULL + t), s_ph, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                s_ph ^= 1u;
+                tc_fence_after();
+                uint32_t sr[4][32];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
+                tmem_ld_wait();
+                const int k0 = x.kv_start + j * kBN;
+                const bool interior = x.all_valid && k0 >= x.lo_last && k0 + kBN <= x.hi_first;
+                float mx = -INFINITY;
+                if (interior) {
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[cc][i]));
+                } else {
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int key = k0 + cc * 32 + i;
+                            const float v = (key >= lo && key < hi) ? __uint_as_float(sr[cc][i])
+                                                                    : -INFINITY;
+                            sr[cc][i] = __float_as_uint(v);
+                            mx = fmaxf(mx, v);
+                        }
+                }
+                const float m_tile = mx * c;
+                float alpha = 1.f;
+                bool rescale = false;
+                if (m_run == -INFINITY) {
+                    m_run = m_tile;  // first keys of this row (or still none)
+                } else if (m_tile > m_run + 8.f) {
+                    alpha = exp2f(m_run - m_tile);
+                    m_run = m_tile;
+                    rescale = true;
+                }
+                const float m_use = m_run == -INFINITY ? 0.f : m_run;
+                float sum = 0.f;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    // P columns [32*half, 32*half + 32) hold keys [64*half, 64*half + 64)
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int cc = 2 * half; cc < 2 * half + 2; ++cc)
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float p0 =
+                                exp2f(fmaf(__uint_as_float(sr[cc][2 * i]), c, -m_use));
+                            const float p1 =
+                                exp2f(fmaf(__uint_as_float(sr[cc][2 * i + 1]), c, -m_use));
+                            sum += p0 + p1;
+                            pk[(cc & 1) * 16 + i] = pack2<T>(p0, p1);
+                        }
+                    tmem_st32(tS + 32 * half, pk);
+                }
+                l_run = l_run * alpha + sum;
+                if (__any_sync(0xffffffffu, rescale)) {
+                    // O_t holds every PV up to tile j-1: the commit that
+                    // signalled S_t(j) was issued after them.
+#pragma unroll
+                    for (int cc = 0; cc < DV / 32; ++cc) {
+                        uint32_t ov[32];
+                        tmem_ld32(tO + cc * 32, ov);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                        tmem_st32(tO + cc * 32, ov);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(bar(B_P_READY + t));
+            }
+            if (!ok) break;
+
+            // epilogue: O / l, LSE
+            if (!warp_wait(bar(B_O_FULL + t), o_ph, abort_flag)) {
+                ok = false;
+                break;
+            }
+            o_ph ^= 1u;
+            tc_fence_after();
+            const bool has = valid && l_run > 0.f;
+            const float inv = has ? 1.f / l_run : 0.f;
+#pragma unroll
+            for (int cc = 0; cc < DV / 32; ++cc) {
+                uint32_t ov[32];
+                tmem_ld32(tO + cc * 32, ov);
+                tmem_ld_wait();
+                if (writes) {
+                    uint32_t pkd[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float o0 = has ? __uint_as_float(ov[2 * i]) * inv : 0.f;
+                        const float o1 = has ? __uint_as_float(ov[2 * i + 1]) * inv : 0.f;
+                        pkd[i] = pack2<T>(o0, o1);
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(og + orow * DV + cc * 32);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+                }
+            }
+            if (writes && p.lse) p.lse[orow] = has ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
+            tc_fence_before();
+            mbar_arrive(bar(B_O_EMPTY + t));
+        }
+        if (!ok && lane == 0) raise_abort(abort_flag, p.status, kStatusTimeoutSoftmax);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------ host
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 4-D map over [d3][d2][d1][d0] (d0 innermost) with a {64, b1, b2, 1} box and
+// 128-byte swizzle.
+int make_map(CUtensorMap *map, const void *ptr, CUtensorMapDataType dt, uint64_t d0, uint64_t d1,
+             uint64_t d2, uint64_t d3, uint32_t b1, uint32_t b2) {
+    auto fn = encode_fn();
+    if (fn == nullptr) {
+        set_error("cuTensorMapEncodeTiled is not available from the driver");
+        return 3;
+    }
+    const cuuint64_t dims[4] = {d0, d1, d2, d3};
+    const cuuint64_t strides[3] = {d0 * 2, d0 * d1 * 2, d0 * d1 * d2 * 2};
+    const cuuint32_t box[4] = {64, b1, b2, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = fn(map, dt, 4, const_cast<void *>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled failed (%d)", (int)r);
+        return 3;
+    }
+    return 0;
+}
+
+int pack_factor(int G) {
+    int gp = 1;
+    while (gp < 16 && G % (gp * 2) == 0) gp *= 2;
+    return gp;
+}
+
+template <typename T, int D, int DV>
+int launch_t(const AttnParams &p, bool bf16, cudaStream_t stream) {
+    using L = Layout<D, DV>;
+    PrefillArgs a;
+    a.p = p;
+    a.Gp = pack_factor(p.G);
+    a.QP = kBM / a.Gp;
+    a.nsub = p.G / a.Gp;
+    a.nqblk = (p.Q + 2 * a.QP - 1) / (2 * a.QP);
+    a.nunits = (long long)a.nqblk * p.B * p.Hkv * a.nsub;
+    const float sc = p.scale == 0.f ? 1e-30f : fabsf(p.scale);
+    a.c_scale = sc * kLog2e;
+    a.idesc_s = idesc_f16(bf16, kBM, kBN, false, p.scale < 0.f);
+    a.idesc_o = idesc_f16(bf16, kBM, DV, true, false);
+    if (a.nunits == 0) return 0;
+
+    const CUtensorMapDataType dt =
+        bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const bool padded = p.cu_q == nullptr;
+    const uint64_t qrows = padded ? (uint64_t)p.Q : (uint64_t)p.Tq;
+    const uint64_t krows = padded ? (uint64_t)p.K : (uint64_t)p.Tk;
+    const uint64_t nb = padded ? (uint64_t)p.B : 1;
+    CUtensorMap tq, tk, tv;
+    int rc = make_map(&tq, p.q, dt, D, p.Hq, qrows, nb, a.Gp, a.QP);
+    if (rc) return rc;
+    if (krows > 0) {
+        rc = make_map(&tk, p.k, dt, D, p.Hkv, krows, nb, 1, kBN);
+        if (rc) return rc;
+        rc = make_map(&tv, p.v, dt, DV, p.Hkv, krows, nb, 1, kBN);
+        if (rc) return rc;
+    } else {
+        tk = tq;  // never read: every unit has no key
+        tv = tq;
+    }
+    auto kern = prefill_tc_kernel<T, D, DV>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+    if (e != cudaSuccess) {
+        set_error("prefill kernel: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        return 3;
+    }
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int nsm = sm_count(dev);
+    const long long grid = a.nunits < nsm ? a.nunits : nsm;
+    kern<<<(unsigned)grid, kThreads, L::SMEM, stream>>>(a, tq, tk, tv);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("prefill kernel launch: %s", cudaGetErrorString(e));
+        return 3;
+    }
+    count_launch();
+    return 0;
+}
+
+template <typename T>
+int launch_dtype(const AttnParams &p, bool bf16, cudaStream_t stream) {
+    if (p.D == 128 && p.Dv == 128) return launch_t<T, 128, 128>(p, bf16, stream);
+    if (p.D == 64 && p.Dv == 64) return launch_t<T, 64, 64>(p, bf16, stream);
+    if (p.D == 128 && p.Dv == 64) return launch_t<T, 128, 64>(p, bf16, stream);
+    return launch_t<T, 64, 128>(p, bf16, stream);
+}
+
+}  // namespace
+
+bool prefill_tc_supported(const AttnParams &p, int dtype) {
+    if (dtype != 1 && dtype != 2) return false;
+    if ((p.D != 64 && p.D != 128) || (p.Dv != 64 && p.Dv != 128)) return false;
+    if (p.Q < 1) return false;
+    const long long rows = p.cu_q ? p.Tq : (long long)p.Q;
+    const long long keys = p.cu_q ? p.Tk : (long long)p.K;
+    return rows < (1LL << 31) && keys < (1LL << 31);
+}
+
+int launch_prefill_tc(const AttnParams &p, int dtype, cudaStream_t stream) {
+    if (dtype == 2) return launch_dtype<__nv_bfloat16>(p, true, stream);
+    return launch_dtype<__half>(p, false, stream);
+}
+
 }  // namespace attn

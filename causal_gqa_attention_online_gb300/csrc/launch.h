@@ -10,6 +10,7 @@
 namespace attn {
 
 void set_error(const char *fmt, ...);
+void count_launch();  // one successful kernel launch
 int sm_count(int device);
 
 // CUDA-core online softmax (any dtype; D, Dv <= 256).  Honours p.nsplit.

@@ -160,6 +160,11 @@ ATTN_API const char *attn_last_error(void);
  * kernel-specific detail code. */
 ATTN_API int attn_device_status(int *detail);
 
+/* Number of kernels this library has launched in the process so far (all
+ * devices, all threads).  A measurement aid: the difference around a region
+ * counts the library's launches inside it. */
+ATTN_API unsigned long long attn_kernel_launches(void);
+
 /* Library version, e.g. "0.1.0". */
 ATTN_API const char *attn_version(void);
 

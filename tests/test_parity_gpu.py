@@ -197,3 +197,88 @@ def test_decode_full_size_batched():
     o, lse = parity.run_gpu(inp, "auto")
     rows = np.array([(b, 0, h) for b in range(inp.B) for h in range(inp.Hq)], np.int32)
     parity.check_sampled_padded(inp, o, lse, rows, "decode full size")
+
+
+# ---------------------------------------------------------------------------
+# tcgen05 / TMEM prefill
+
+TC_SHAPES = [
+    # B, Hq, Hkv, Q, K, D, Dv
+    (1, 4, 2, 64, 128, 64, 64),       # the fp32 prefill shape, in bf16
+    (1, 4, 2, 65, 131, 64, 64),       # Q/K tails
+    (1, 8, 2, 256, 1024, 64, 64),
+    (2, 8, 2, 300, 300, 128, 128),
+    (1, 4, 1, 129, 129, 128, 64),     # MQA, G = 4
+    (1, 2, 2, 200, 200, 64, 128),     # MHA: one head per row block
+    (2, 32, 8, 512, 512, 128, 128),   # G = 4 as in the 4096^2 workload
+    (1, 16, 2, 100, 357, 128, 128),   # G = 8
+    (1, 32, 2, 70, 70, 64, 64),       # G = 16
+    (1, 6, 2, 90, 150, 128, 128),     # G = 3: three subgroups of one head
+    (1, 8, 2, 3, 67, 128, 128),       # short query chunk, bottom-right offset
+    (1, 4, 2, 300, 40, 64, 64),       # Q > K: leading rows without keys
+]
+
+
+@pytest.mark.parametrize("shape", TC_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_tcgen05_shapes(shape, dtype):
+    B, Hq, Hkv, Q, K, D, Dv = shape
+    inp = synth.make_padded(B, Hq, Hkv, Q, K, D, Dv, dtype, seed=31)
+    parity.check(inp, "tcgen05", f"tcgen05 {dtype} {shape}")
+
+
+@pytest.mark.parametrize("window", [1, 50, 128, 129, 1000])
+def test_tcgen05_window(window):
+    inp = synth.make_padded(2, 8, 2, 400, 700, 128, 128, "bf16", seed=32, window=window)
+    parity.check(inp, "tcgen05", f"tcgen05 window {window}")
+
+
+def test_tcgen05_lengths_nan_padding():
+    sq = np.array([0, 1, 7, 16, 31, 32, 33, 65, 200, 130], np.int32)
+    sk = np.array([0, 1, 7, 16, 31, 32, 33, 65, 250, 129], np.int32)
+    inp = synth.make_padded(10, 8, 2, 200, 250, 128, 128, "bf16", seed=33, seqlens_q=sq,
+                            seqlens_k=sk, pad_value=NAN)
+    parity.check(inp, "tcgen05", "tcgen05 lengths")
+
+
+def test_tcgen05_all_empty():
+    inp = synth.make_padded(2, 8, 2, 64, 64, 128, 128, "bf16", seed=34,
+                            seqlens_k=np.zeros(2, np.int32), pad_value=NAN)
+    parity.check(inp, "tcgen05", "tcgen05 all empty")
+
+
+def test_tcgen05_negative_scale():
+    inp = synth.make_padded(1, 4, 2, 130, 130, 64, 64, "bf16", seed=35, scale=-0.2)
+    parity.check(inp, "tcgen05", "tcgen05 negative scale")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_tcgen05_varlen_packed(dtype):
+    sk = np.array([0, 5, 33, 130, 1, 640, 0, 300, 1000], np.int32)
+    sq = np.minimum(sk, np.array([0, 5, 7, 64, 1, 512, 0, 100, 512]))
+    for w in (0, 100):
+        inp = synth.make_packed(sq, sk, 16, 4, 128, 128, dtype, seed=36, window=w)
+        parity.check(inp, "tcgen05", f"tcgen05 varlen {dtype} w={w}")
+
+
+def test_tcgen05_full_size_prefill_sampled():
+    """bf16 causal prefill B=4 Hq=32 Hkv=8 Q=K=4096 D=Dv=128 (the benchmark's
+    launch): sampled rows against the oracle, plus invariants on every row."""
+    inp = synth.prefill_bf16_b4_h32x8_s4096_d128()
+    o, lse = parity.run_gpu(inp, "auto")
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+    rows = parity.sample_rows(inp, 3000, seed=4)
+    parity.check_sampled_padded(inp, o, lse, rows, "prefill full size")
+    # row 0 of every (b, h) sees exactly key 0: O = V[0, kv head]
+    v0 = synth.exact_f32(inp.v[:, 0])            # [B, Hkv, Dv]
+    G = inp.Hq // inp.Hkv
+    want = np.repeat(v0, G, axis=1)             # [B, Hq, Dv]
+    assert np.max(np.abs(o[:, 0] - want)) <= 2e-2
+
+
+def test_tcgen05_full_size_varlen():
+    """bf16 varlen chunked prefill: 16 packed sequences, key lengths U[0,4096]
+    incl. empty, queries = last min(512, Kb) tokens, Hq=16 Hkv=4, window 1024:
+    every row against the oracle."""
+    inp = synth.varlen_bf16_16seq_h16x4_k4096_q512_w1024()
+    parity.check(inp, "auto", "varlen full size")
