@@ -46,9 +46,17 @@ using namespace sm100;
 
 constexpr int kBM = 128;  // rows per Q tile (MMA M)
 constexpr int kBN = 128;  // keys per KV tile
-constexpr int kThreads = 320;
+// Three warpgroups: two softmax warpgroups and one for the MMA warp, the TMA
+// warp and two idle warps.  Launched at 168 registers a thread (384 x 168 =
+// 64512); the softmax warpgroups take 200 and the third gives back down to
+// 104: 256 x 200 + 128 x 104 = 64512, and per SM sub-partition
+// 2 x 200 + 104 <= 512 register slots a lane.
+constexpr int kThreads = 384;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
+constexpr uint32_t kRegsSoftmax = 200;
+constexpr uint32_t kRegsOther = 104;
+static_assert(256 * kRegsSoftmax + 128 * kRegsOther <= kThreads * 168, "register split");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kChunkBytes = 128 * 128;       // one 128-row x 128-byte swizzled chunk
 
@@ -156,7 +164,7 @@ __device__ __forceinline__ void raise_abort(volatile int *abort_flag, int *statu
 }
 
 template <typename T, int D, int DV>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV) {
@@ -212,13 +220,13 @@ __global__ void __maxnreg__(200)
     auto stage = [&](int s) { return kv_smem + (uint32_t)s * L::STAGE; };
     const bool padded = p.cu_q == nullptr;
 
+    if (warp >= 8) regs_decrease<kRegsOther>();
     if (warp == kLoadWarp) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             uint32_t kv_it = 0, q_ph = 0;
             int last_q_parity = -1;
-            int last_kv_parity[8];
-            for (int s = 0; s < 8; ++s) last_kv_parity[s] = -1;
+            uint32_t armed = 0, armed_parity = 0;  // per ring slot: loaded at least once, last parity
             bool ok = true;
             for (long long u = blockIdx.x; u < a.nunits && ok; u += gridDim.x) {
                 const UnitInfo x = unit_info(a, u);
@@ -261,7 +269,8 @@ __global__ void __maxnreg__(200)
                                 tma_load_4d(stage(s) + c * kChunkBytes, &tmV, kv_full(s), c * 64,
                                             x.kvh, krow + k0, bc);
                         }
-                        last_kv_parity[s] = (int)ph;
+                        armed |= 1u << s;
+                        armed_parity = (armed_parity & ~(1u << s)) | (ph << s);
                     }
                 }
             }
@@ -269,8 +278,8 @@ __global__ void __maxnreg__(200)
             if (last_q_parity >= 0)
                 mbar_wait(bar(B_Q_FULL), (uint32_t)last_q_parity, abort_flag, kWaitLimitNs);
             for (int s = 0; s < NS; ++s)
-                if (last_kv_parity[s] >= 0)
-                    mbar_wait(kv_full(s), (uint32_t)last_kv_parity[s], abort_flag, kWaitLimitNs);
+                if (armed & (1u << s))
+                    mbar_wait(kv_full(s), (armed_parity >> s) & 1u, abort_flag, kWaitLimitNs);
         }
     } else if (warp == kMmaWarp) {
         // --------------------------------------------------- MMA issuer
@@ -292,11 +301,13 @@ __global__ void __maxnreg__(200)
 
             auto issue_s = [&](int t, int kslot) {
                 if (lane == 0) {
+                    // the start-address field is the low 14 bits (address >> 4)
+                    const uint64_t qd = sw128_desc(q_smem + t * L::QTILE, 16, 1024);
+                    const uint64_t kd = sw128_desc(stage(kslot), 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk / 4) * kChunkBytes + (kk % 4) * 32;
-                        mma_ss(tmem + s_col[t], sw128_desc(q_smem + t * L::QTILE + off, 16, 1024),
-                               sw128_desc(stage(kslot) + off, 16, 1024), a.idesc_s, kk > 0);
+                        const uint32_t off = ((kk / 4) * kChunkBytes + (kk % 4) * 32) >> 4;
+                        mma_ss(tmem + s_col[t], qd + off, kd + off, a.idesc_s, kk > 0);
                     }
                     mma_commit(bar(B_S_FULL + t));
                 }
@@ -332,11 +343,11 @@ __global__ void __maxnreg__(200)
                 }
                 tc_fence_after();
                 if (lane == 0) {
+                    const uint64_t vd = sw128_desc(stage(vslot), kChunkBytes, 1024);
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk)
-                        mma_ts(tmem + o_col[t], tmem + s_col[t] + kk * 8,
-                               sw128_desc(stage(vslot) + kk * 2048, kChunkBytes, 1024), a.idesc_o,
-                               (jj > 0 || kk > 0) ? 1u : 0u);
+                        mma_ts(tmem + o_col[t], tmem + s_col[t] + kk * 8, vd + (kk * 2048 >> 4),
+                               a.idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
                 }
                 __syncwarp();
                 return true;
@@ -393,8 +404,9 @@ __global__ void __maxnreg__(200)
             mbar_wait(bar(B_TEARDOWN), 0, abort_flag, kWaitLimitNs);
         }
         __syncwarp();
-    } else {
+    } else if (warp < 8) {
         // ------------------------------------------------- softmax warpgroups
+        regs_increase<kRegsSoftmax>();
         const int t = warp >> 2;                 // Q tile of this warpgroup
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;       // row of the tile = TMEM lane
