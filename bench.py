@@ -169,18 +169,7 @@ def time_steps(fn, steps, warmup, flush, stream):
     return [a.elapsed_time(b) for a, b in evs]
 
 
-def run_gpu(args, world, rank, local):
-    import causal_gqa_attention_online_gb300 as attn
-    from causal_gqa_attention_online_gb300 import build_ext, synth
-
-    build_ext.build()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    stream = torch.cuda.current_stream()
-    hbm_peak, tf_peak, peak_src = measured_peaks()
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-
-    # ---------------- prefill (headline) ----------------
+def measure_prefill(args, world, rank, dev, stream, flush, attn, synth):
     P = PREFILL
     pin = synth.prefill_bf16_b4_h32x8_s4096_d128(seed=1234 + rank)
     q, k, v = pin.q.to(dev), pin.k.to(dev), pin.v.to(dev)
@@ -196,17 +185,17 @@ def run_gpu(args, world, rank, local):
     n0 = attn.kernel_launches()
     barrier(world)
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    with ClockSampler(dev.index) as clk:
         times = time_steps(prefill, args.steps, args.warmup, flush, stream)
     torch.cuda.synchronize()
     barrier(world)
-    launches_prefill = (attn.kernel_launches() - n0) // (args.steps + args.warmup)
+    launches = (attn.kernel_launches() - n0) // (args.steps + args.warmup)
     ms = max_over_ranks(sum(times) / len(times), world)
-    value = world * flop / (ms * 1e-3) / 1e12
 
     # e2e: pinned host inputs copied in, O / LSE copied back, every step
     hq, hk, hv = pin.q.pin_memory(), pin.k.pin_memory(), pin.v.pin_memory()
-    ho, hl = torch.empty_like(o, device="cpu").pin_memory(), torch.empty_like(lse, device="cpu").pin_memory()
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
 
     def prefill_e2e():
         q.copy_(hq, non_blocking=True)
@@ -216,12 +205,14 @@ def run_gpu(args, world, rank, local):
         ho.copy_(o, non_blocking=True)
         hl.copy_(lse, non_blocking=True)
 
-    e2e_times = time_steps(prefill_e2e, max(3, args.steps // 2), 2, flush, stream)
+    e2e_times = time_steps(prefill_e2e, max(3, args.steps // 2), 3, flush, stream)
     e2e_ms = max_over_ranks(sum(e2e_times) / len(e2e_times), world)
-    h2d = (q.numel() + k.numel() + v.numel()) * 2
-    d2h = o.numel() * 2 + lse.numel() * 4
+    return dict(pin=pin, flop=flop, ms=ms, launches=launches, clocks=clk.summary(),
+                e2e_ms=e2e_ms, h2d=(q.numel() + k.numel() + v.numel()) * 2,
+                d2h=o.numel() * 2 + lse.numel() * 4)
 
-    # ---------------- decode ----------------
+
+def measure_decode(args, world, rank, dev, stream, flush, attn, synth):
     Dd = DECODE
     din = synth.decode_bf16_b64_h32x8_k8192_d128(seed=1234 + rank)
     dq, dk, dv = din.q.to(dev), din.k.to(dev), din.v.to(dev)
@@ -237,81 +228,124 @@ def run_gpu(args, world, rank, local):
     torch.cuda.synchronize()
     n1 = attn.kernel_launches()
     barrier(world)
-    dtimes = time_steps(decode, args.steps, args.warmup, flush, stream)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        times = time_steps(decode, args.steps, args.warmup, flush, stream)
     barrier(world)
-    launches_decode = (attn.kernel_launches() - n1) // (args.steps + args.warmup)
-    dms = max_over_ranks(sum(dtimes) / len(dtimes), world)
-    dvalue = world * kv_bytes / (dms * 1e-3) / 1e9
+    launches = (attn.kernel_launches() - n1) // (args.steps + args.warmup)
+    ms = max_over_ranks(sum(times) / len(times), world)
     hdq, hdk, hdv = din.q.pin_memory(), din.k.pin_memory(), din.v.pin_memory()
-    hdo = torch.empty_like(do, device="cpu").pin_memory()
-    hdl = torch.empty_like(dl, device="cpu").pin_memory()
+    hsk = torch.from_numpy(din.seqlens_k).pin_memory()
+    hdo = torch.empty(do.shape, dtype=do.dtype).pin_memory()
+    hdl = torch.empty(dl.shape, dtype=dl.dtype).pin_memory()
 
     def decode_e2e():
         dq.copy_(hdq, non_blocking=True)
         dk.copy_(hdk, non_blocking=True)
         dv.copy_(hdv, non_blocking=True)
+        dsk.copy_(hsk, non_blocking=True)
         attn.attn_fwd(dq, dk, dv, do, dl, seqlens_k=dsk, stream=stream)
         hdo.copy_(do, non_blocking=True)
         hdl.copy_(dl, non_blocking=True)
 
-    de2e = time_steps(decode_e2e, max(3, args.steps // 2), 2, flush, stream)
-    de2e_ms = max_over_ranks(sum(de2e) / len(de2e), world)
-    dh2d = (dq.numel() + dk.numel() + dv.numel()) * 2
-    dd2h = do.numel() * 2 + dl.numel() * 4
+    e2e_times = time_steps(decode_e2e, max(3, args.steps // 2), 3, flush, stream)
+    e2e_ms = max_over_ranks(sum(e2e_times) / len(e2e_times), world)
+    return dict(kv_bytes=kv_bytes, ms=ms, launches=launches, clocks=clk.summary(),
+                e2e_ms=e2e_ms,
+                h2d=(dq.numel() + dk.numel() + dv.numel()) * 2 + dsk.numel() * 4,
+                d2h=do.numel() * 2 + dl.numel() * 4)
 
+
+def run_gpu(args, world, rank, local):
+    import causal_gqa_attention_online_gb300 as attn
+    from causal_gqa_attention_online_gb300 import build_ext, synth
+
+    build_ext.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    hbm_peak, tf_peak, peak_src = measured_peaks()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     traffic = load_traffic()
-    result = {
-        "metric": METRIC,
-        "value": round(value, 3),
-        "unit": "TFLOP/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": round(ms, 5),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic: N(0,1) seeded (PCG64), bf16 round-to-nearest",
-        "config": {"workload": PREFILL_NAME, "B": P["B"], "Hq": P["Hq"], "Hkv": P["Hkv"],
-                   "seq_len": P["Q"], "D": P["D"], "Dv": P["Dv"], "global_batch": P["B"] * world,
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "512 MiB buffer written before every timed step",
-                   "flop_per_step": flop},
-        "roofline": {"bound": "tensor", "achieved": round(flop / (ms * 1e-3) / 1e12, 3),
-                     "peak": tf_peak, "unit": "TFLOP/s",
-                     "frac": round(flop / (ms * 1e-3) / 1e12 / tf_peak, 4),
-                     "traffic": traffic.get("prefill"),
-                     "peak_source": f"{peak_src} bf16 dense (cuBLAS burst)"},
-        "e2e": {"value": round(world * flop / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
-                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "gpu_launches": int(launches_prefill * args.steps),
-        "clocks": clk.summary(),
-        "decode": {
-            "workload": DECODE_NAME, "metric": "KV GB/s", "value": round(dvalue, 2),
-            "unit": "GB/s", "ms_per_step": round(dms, 5), "kv_bytes_per_step": kv_bytes,
-            "gpu_launches": int(launches_decode * args.steps),
-            "roofline": {"bound": "hbm", "achieved": round(kv_bytes / (dms * 1e-3) / 1e9, 2),
-                         "peak": hbm_peak, "unit": "GB/s",
-                         "frac": round(kv_bytes / (dms * 1e-3) / 1e9 / hbm_peak, 4),
+    P = PREFILL
+    result = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+              "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+              "data": "synthetic: N(0,1) seeded (PCG64), bf16 round-to-nearest"}
+    pin = None
+    if args.only in ("all", "prefill"):
+        r = measure_prefill(args, world, rank, dev, stream, flush, attn, synth)
+        pin = r["pin"]
+        tf = r["flop"] / (r["ms"] * 1e-3) / 1e12
+        result.update({
+            "value": round(world * tf, 3), "unit": "TFLOP/s", "ms_per_step": round(r["ms"], 5),
+            "config": {"workload": PREFILL_NAME, "B": P["B"], "Hq": P["Hq"], "Hkv": P["Hkv"],
+                       "seq_len": P["Q"], "D": P["D"], "Dv": P["Dv"],
+                       "global_batch": P["B"] * world,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "512 MiB buffer written before every timed step",
+                       "flop_per_step": r["flop"]},
+            "roofline": {"bound": "tensor", "achieved": round(tf, 3), "peak": tf_peak,
+                         "unit": "TFLOP/s", "frac": round(tf / tf_peak, 4),
+                         "traffic": traffic.get("prefill"),
+                         "peak_source": f"{peak_src} bf16 dense (cuBLAS burst)"},
+            "e2e": {"value": round(world * r["flop"] / (r["e2e_ms"] * 1e-3) / 1e12, 3),
+                    "unit": "TFLOP/s", "ms_per_step": round(r["e2e_ms"], 4),
+                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+            "gpu_launches": int(r["launches"] * args.steps),
+            "clocks": r["clocks"],
+        })
+    if args.only in ("all", "decode"):
+        d = measure_decode(args, world, rank, dev, stream, flush, attn, synth)
+        gbs = d["kv_bytes"] / (d["ms"] * 1e-3) / 1e9
+        dec = {
+            "workload": DECODE_NAME, "metric": "KV GB/s", "value": round(world * gbs, 2),
+            "unit": "GB/s", "ms_per_step": round(d["ms"], 5), "kv_bytes_per_step": d["kv_bytes"],
+            "gpu_launches": int(d["launches"] * args.steps), "clocks": d["clocks"],
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
                          "traffic": traffic.get("decode"),
                          "peak_source": f"{peak_src} HBM copy"},
-            "e2e": {"value": round(world * kv_bytes / (de2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-                    "ms_per_step": round(de2e_ms, 4), "h2d_bytes_per_step": dh2d,
-                    "d2h_bytes_per_step": dd2h},
-        },
-    }
+            "e2e": {"value": round(world * d["kv_bytes"] / (d["e2e_ms"] * 1e-3) / 1e9, 2),
+                    "unit": "GB/s", "ms_per_step": round(d["e2e_ms"], 4),
+                    "h2d_bytes_per_step": d["h2d"], "d2h_bytes_per_step": d["d2h"]},
+        }
+        if args.only == "decode":
+            result.update({"value": dec["value"], "unit": "GB/s", "ms_per_step": dec["ms_per_step"],
+                           "config": {"workload": DECODE_NAME}, "roofline": dec["roofline"],
+                           "e2e": dec["e2e"], "gpu_launches": dec["gpu_launches"],
+                           "clocks": dec["clocks"]})
+        else:
+            result["decode"] = dec
     return result, pin
 
 
+KERNEL_SOURCES = {
+    "prefill": "causal_gqa_attention_online_gb300/csrc/kernel_prefill_tc.cu",
+    "decode": "causal_gqa_attention_online_gb300/csrc/kernel_decode.cu",
+}
+
+
+def source_sha(rel: str) -> str:
+    import hashlib
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
 def load_traffic():
-    """Per-launch DRAM bytes from the committed ncu summary, if current."""
+    """Per-launch DRAM bytes (read + write) from the committed ncu summary
+    profiles/traffic.json, kept only while the kernel source is unchanged
+    since the capture (its sha256 prefix is stored beside the figure)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return {}
     with open(path) as f:
-        return json.load(f)
+        d = json.load(f)
+    out = {}
+    for name, rel in KERNEL_SOURCES.items():
+        e = d.get(name)
+        if e and e.get("source_sha") == source_sha(rel):
+            out[name] = e.get("bytes_per_launch")
+    return out
 
 
 def oracle_sample_rate(inp, rows_budget_s=12.0, nthreads=0, seed=0):
@@ -377,6 +411,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode"],
+                    help="profiling aid: run one workload (the JSON line then lacks the other)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -388,7 +424,7 @@ def main():
         return
     res, pin = run_gpu(args, world, rank, local)
     if rank == 0:
-        if world == 1 and not args.no_cpu_baseline:
+        if world == 1 and not args.no_cpu_baseline and pin is not None:
             r, nrows, secs, threads = oracle_sample_rate(pin, 12.0)
             res["cpu_baseline"] = {
                 "value": r, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
