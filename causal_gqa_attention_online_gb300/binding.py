@@ -22,8 +22,8 @@ ALGOS = {"auto": 0, "generic": 1, "tcgen05": 2, "decode": 3}
 _DTYPE_CODE = {torch.float32: ATTN_F32, torch.float16: ATTN_F16, torch.bfloat16: ATTN_BF16}
 
 EXPORTED = ("attn_fwd", "attn_fwd_varlen", "attn_fwd_algo", "attn_fwd_varlen_algo",
-            "attn_lse_combine", "attn_last_error", "attn_device_status", "attn_kernel_launches",
-            "attn_version")
+            "attn_lse_combine", "attn_fwd_decode_noalloc", "attn_last_error",
+            "attn_device_status", "attn_kernel_launches", "attn_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -60,6 +60,8 @@ def load_library(path: str | None = None):
         lib.attn_fwd_varlen.argtypes = varlen + [vp]
         lib.attn_fwd_algo.argtypes = common + [ip, vp]
         lib.attn_fwd_varlen_algo.argtypes = varlen + [ip, vp]
+        lib.attn_fwd_decode_noalloc.argtypes = common + [vp]
+        lib.attn_fwd_decode_noalloc.restype = ip
         for f in (lib.attn_fwd, lib.attn_fwd_varlen, lib.attn_fwd_algo, lib.attn_fwd_varlen_algo):
             f.restype = ip
         lib.attn_lse_combine.argtypes = [vp, vp, vp, vp, ip, ctypes.c_longlong, ip, ip, vp]
@@ -176,6 +178,34 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_q, max_k, o=None, l
                                   Tq, Tk, int(max_q), int(max_k), D, Dv, _ptr(cu_seqlens_q),
                                   _ptr(cu_seqlens_k), int(window), float(scale),
                                   _DTYPE_CODE[q.dtype], ALGOS[algo], _stream_ptr(stream))
+    _check(rc)
+    return o, lse
+
+
+def attn_fwd_decode_noalloc(q, k, v, o, lse=None, *, seqlens_q=None, seqlens_k=None, window=0,
+                            scale=None, stream=None):
+    """attn_fwd's split-KV decode with its scratch in the library's fixed
+    device array: the call allocates nothing (``o`` and ``lse`` are the
+    caller's).  For callers that may not allocate device memory while
+    attention runs.  Calls that overlap on one GPU race on the shared array."""
+    lib = load_library()
+    B, Q, Hq, D = q.shape
+    K, Hkv = k.shape[1], k.shape[2]
+    Dv = v.shape[3]
+    dev = q.device
+    for name, t, n in (("q", q, B * Q * Hq * D), ("k", k, B * K * Hkv * D),
+                       ("v", v, B * K * Hkv * Dv), ("o", o, B * Q * Hq * Dv)):
+        _check_tensor(name, t, q.dtype, n, dev)
+    if lse is not None:
+        _check_tensor("lse", lse, torch.float32, B * Q * Hq, dev)
+    for name, t in (("seqlens_q", seqlens_q), ("seqlens_k", seqlens_k)):
+        if t is not None:
+            _check_tensor(name, t, torch.int32, B, dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = lib.attn_fwd_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv,
+                                     Q, K, D, Dv, _ptr(seqlens_q), _ptr(seqlens_k), int(window),
+                                     float(scale), _DTYPE_CODE[q.dtype], _stream_ptr(stream))
     _check(rc)
     return o, lse
 

@@ -151,6 +151,30 @@ ATTN_API int attn_fwd_varlen_algo(const void *q, const void *k, const void *v, v
 ATTN_API int attn_lse_combine(const float *o_parts, const float *lse_parts, void *o, float *lse,
                      int nsplit, long long rows, int Dv, int dtype, attn_stream_t stream);
 
+/*
+ * attn_fwd_decode_noalloc -- attn_fwd's split-KV decode for callers that may
+ * not allocate device memory while attention runs: for example a serving
+ * process whose device memory is owned by another runtime's allocator or held
+ * under a hard cap, or a latency-critical decode loop where an allocation (or
+ * a synchronisation it may bring) is not allowed.  The pages have no
+ * counterpart to this entry point; it is a deployment aid of this library.
+ *
+ * Same arguments, layout and result as attn_fwd, restricted to the shapes the
+ * decode kernel takes (bf16/fp16, D and Dv in {64, 128}, Q * Hq / Hkv <= 16).
+ * The split-KV partials live in a fixed 32 MiB __device__ array that every
+ * GPU using the library keeps until the process exits; the call makes no
+ * allocation of any kind.  A problem whose partials would not fit returns
+ * ATTN_ERR_UNSUPPORTED with a message giving the bytes needed.  The first
+ * call on a device looks up the array's device address (make that call before
+ * any stream capture).  All calls share the array: calls that overlap on the
+ * GPU (other streams or host threads on the same device) race on it and must
+ * be serialised by the caller.  Nothing in the array needs to start at zero.
+ */
+ATTN_API int attn_fwd_decode_noalloc(const void *q, const void *k, const void *v, void *o,
+                                     float *lse, int B, int Hq, int Hkv, int Q, int K, int D,
+                                     int Dv, const int32_t *seqlens_q, const int32_t *seqlens_k,
+                                     int window, float scale, int dtype, attn_stream_t stream);
+
 /* Message for the calling thread's most recent failed call ("" if none). */
 ATTN_API const char *attn_last_error(void);
 
