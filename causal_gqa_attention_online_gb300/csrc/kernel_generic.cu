@@ -172,29 +172,65 @@ __global__ void __launch_bounds__(128) generic_fwd_kernel(const AttnParams p) {
 }
 
 // One warp per output row: merge nsplit normalised partials by their LSE.
+// Lane s holds the weight of split s (of each group of 32 splits), so every
+// weight is computed once; the column loop then issues independent loads.
 template <typename T>
 __device__ __forceinline__ void combine_one_row(const float *o_parts, const float *lse_parts,
                                                 long long part_stride_rows, long long prow,
                                                 int nsplit, int Dv, T *orow, float *lse_out,
                                                 int lane) {
     float mx = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) mx = fmaxf(mx, lse_parts[s * part_stride_rows + prow]);
+    for (int s = lane; s < nsplit; s += 32) mx = fmaxf(mx, lse_parts[s * part_stride_rows + prow]);
+    mx = warp_max(mx);
     if (mx == -INFINITY) {
         for (int c = lane; c < Dv; c += 32) orow[c] = from_f32<T>(0.f);
         if (lane == 0 && lse_out) *lse_out = -INFINITY;
         return;
     }
     float wsum = 0.f;
-    for (int s = 0; s < nsplit; ++s)
+    for (int s = lane; s < nsplit; s += 32)
         wsum += exp2f((lse_parts[s * part_stride_rows + prow] - mx) * kLog2e);
+    wsum = warp_sum(wsum);
     const float inv = 1.f / wsum;
-    for (int c = lane; c < Dv; c += 32) {
-        float a = 0.f;
-        for (int s = 0; s < nsplit; ++s) {
-            const float w = exp2f((lse_parts[s * part_stride_rows + prow] - mx) * kLog2e);
-            a = fmaf(w, o_parts[(s * part_stride_rows + prow) * Dv + c], a);
+    if ((Dv & 3) == 0) {
+        // uniform trip count: every lane takes part in the shuffles
+        for (int c0 = 0; c0 < Dv; c0 += 128) {
+            const int c = c0 + lane * 4;
+            const bool act = c < Dv;
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s0 = 0; s0 < nsplit; s0 += 32) {
+                const int sl = s0 + lane;
+                const float wl =
+                    sl < nsplit ? exp2f((lse_parts[sl * part_stride_rows + prow] - mx) * kLog2e) : 0.f;
+                const int n = min(32, nsplit - s0);
+#pragma unroll 4
+                for (int j = 0; j < n; ++j) {
+                    const float w = __shfl_sync(0xffffffffu, wl, j);
+                    const float4 v = act ? *reinterpret_cast<const float4 *>(
+                                               o_parts + ((s0 + j) * part_stride_rows + prow) * Dv + c)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                    a.x = fmaf(w, v.x, a.x);
+                    a.y = fmaf(w, v.y, a.y);
+                    a.z = fmaf(w, v.z, a.z);
+                    a.w = fmaf(w, v.w, a.w);
+                }
+            }
+            if (act) {
+                orow[c] = from_f32<T>(a.x * inv);
+                orow[c + 1] = from_f32<T>(a.y * inv);
+                orow[c + 2] = from_f32<T>(a.z * inv);
+                orow[c + 3] = from_f32<T>(a.w * inv);
+            }
         }
-        orow[c] = from_f32<T>(a * inv);
+    } else {
+        for (int c = lane; c < Dv; c += 32) {
+            float a = 0.f;
+            for (int s = 0; s < nsplit; ++s) {
+                const float w = exp2f((lse_parts[s * part_stride_rows + prow] - mx) * kLog2e);
+                a = fmaf(w, o_parts[(s * part_stride_rows + prow) * Dv + c], a);
+            }
+            orow[c] = from_f32<T>(a * inv);
+        }
     }
     if (lane == 0 && lse_out) *lse_out = mx + __logf(wsum);
 }

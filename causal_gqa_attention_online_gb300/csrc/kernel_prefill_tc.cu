@@ -153,6 +153,19 @@ template <> __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;\n" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// 2^x on the MUFU unit (flushes subnormal results to zero; 2^-inf = +0)
+__device__ __forceinline__ float ex2(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(r) : "f"(x));
+    return r;
+}
+
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
     const bool ok = mbar_wait(bar, parity, abort_flag, kWaitLimitNs);
     return __all_sync(0xffffffffu, ok);
@@ -452,36 +465,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_wait();
                 const int k0 = x.kv_start + j * kBN;
                 const bool interior = x.all_valid && k0 >= x.lo_last && k0 + kBN <= x.hi_first;
-                float mx = -INFINITY;
-                if (interior) {
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[cc][i]));
-                } else {
+                if (!interior) {
+                    // keys outside [lo, hi) -> -inf (also replaces NaN from padding)
+                    const int lo_rel = lo - k0, hi_rel = hi - k0;
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
-                            const int key = k0 + cc * 32 + i;
-                            const float v = (key >= lo && key < hi) ? __uint_as_float(sr[cc][i])
-                                                                    : -INFINITY;
-                            sr[cc][i] = __float_as_uint(v);
-                            mx = fmaxf(mx, v);
+                            const int kr = cc * 32 + i;
+                            if (kr < lo_rel || kr >= hi_rel) sr[cc][i] = __float_as_uint(-INFINITY);
                         }
                 }
+                // row max: four independent chains of 3-input max
+                float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        mc[i & 3] = fmax3(mc[i & 3], __uint_as_float(sr[cc][2 * i]),
+                                          __uint_as_float(sr[cc][2 * i + 1]));
+                const float mx = fmax3(fmaxf(mc[0], mc[1]), mc[2], mc[3]);
                 const float m_tile = mx * c;
                 float alpha = 1.f;
                 bool rescale = false;
                 if (m_run == -INFINITY) {
                     m_run = m_tile;  // first keys of this row (or still none)
                 } else if (m_tile > m_run + 8.f) {
-                    alpha = exp2f(m_run - m_tile);
+                    alpha = ex2(m_run - m_tile);
                     m_run = m_tile;
                     rescale = true;
                 }
-                const float m_use = m_run == -INFINITY ? 0.f : m_run;
-                float sum = 0.f;
+                const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
+                float sc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     // P columns [32*half, 32*half + 32) hold keys [64*half, 64*half + 64)
@@ -490,15 +505,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int cc = 2 * half; cc < 2 * half + 2; ++cc)
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const float p0 =
-                                exp2f(fmaf(__uint_as_float(sr[cc][2 * i]), c, -m_use));
+                            const float p0 = ex2(fmaf(__uint_as_float(sr[cc][2 * i]), c, neg_m));
                             const float p1 =
-                                exp2f(fmaf(__uint_as_float(sr[cc][2 * i + 1]), c, -m_use));
-                            sum += p0 + p1;
+                                ex2(fmaf(__uint_as_float(sr[cc][2 * i + 1]), c, neg_m));
+                            sc[(2 * i) & 7] += p0;
+                            sc[(2 * i + 1) & 7] += p1;
                             pk[(cc & 1) * 16 + i] = pack2<T>(p0, p1);
                         }
                     tmem_st32(tS + 32 * half, pk);
                 }
+                const float sum = ((sc[0] + sc[1]) + (sc[2] + sc[3])) + ((sc[4] + sc[5]) + (sc[6] + sc[7]));
                 l_run = l_run * alpha + sum;
                 if (__any_sync(0xffffffffu, rescale)) {
                     // O_t holds every PV up to tile j-1: the commit that
