@@ -9,7 +9,7 @@
 #include <mutex>
 #include <string>
 
-#include "../../include/attn_gqa.h"
+#include "attn_gqa.h"
 #include "common.cuh"
 #include "launch.h"
 

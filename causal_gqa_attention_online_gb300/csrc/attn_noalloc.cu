@@ -24,7 +24,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/attn_gqa.h"
+#include "attn_gqa.h"
 #include "common.cuh"
 #include "launch.h"
 
