@@ -77,7 +77,7 @@ template <int D, int DV> struct Layout {
     static constexpr int KTILE = kBN * D * 2;
     static constexpr int VTILE = kBN * DV * 2;
     static constexpr int STAGE = KTILE > VTILE ? KTILE : VTILE;
-    static constexpr int BUDGET = 225 * 1024;
+    static constexpr int BUDGET = 227 * 1024;  // opt-in shared memory per block
     static constexpr int NS_FIT = (BUDGET - 2 * QTILE - 1024 - 512) / STAGE;
     static constexpr int NS = NS_FIT > 8 ? 8 : NS_FIT;
     static constexpr int Q_OFF = 0;
@@ -369,15 +369,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < x.n_kv && ok; ++j) {
                 const uint32_t it = kb + 2u * (uint32_t)j;
                 const int kslot = (int)(it % NS);
+                // PV0 of the previous tile does not need K_j: issue it first
+                if (j > 0 && !issue_pv(0, j - 1)) {
+                    ok = false;
+                    break;
+                }
                 if (!warp_wait(kv_full(kslot), (it / NS) & 1u, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (j > 0 && !issue_pv(0, j - 1)) {
-                    ok = false;
-                    break;
-                }
                 issue_s(0, kslot);
                 if (j > 0) {
                     if (!issue_pv(1, j - 1)) {
