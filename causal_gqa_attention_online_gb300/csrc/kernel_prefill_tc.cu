@@ -59,6 +59,7 @@ constexpr uint32_t kRegsOther = 104;
 static_assert(256 * kRegsSoftmax + 128 * kRegsOther <= kThreads * 168, "register split");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kChunkBytes = 128 * 128;       // one 128-row x 128-byte swizzled chunk
+constexpr int kPrefetchTiles = 4;                 // K/V tiles pulled into L2 ahead of use
 
 struct PrefillArgs {
     AttnParams p;
@@ -259,8 +260,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < D / 64; ++c)
                         tma_load_4d(q_smem + t * L::QTILE + c * kChunkBytes, &tmQ, bar(B_Q_FULL),
                                     c * 64, x.h0, qrow + t * a.QP, bc);
+                // L2 prefetch: the first K/V tiles of this unit and the next unit's Q
+                auto prefetch_kv = [&](int jj) {
+                    const int kk0 = x.kv_start + jj * kBN;
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_prefetch_l2_4d(&tmK, c * 64, x.kvh, krow + kk0, bc);
+                    for (int c = 0; c < DV / 64; ++c)
+                        tma_prefetch_l2_4d(&tmV, c * 64, x.kvh, krow + kk0, bc);
+                };
+                for (int jj = 1; jj < kPrefetchTiles && jj < x.n_kv; ++jj) prefetch_kv(jj);
+                if (u + gridDim.x < a.nunits) {
+                    const UnitInfo nx = unit_info(a, u + gridDim.x);
+                    if (nx.n_kv > 0) {
+                        const int nq = (padded ? 0 : (int)nx.si.q_off) + nx.q0;
+                        const int nbc = padded ? nx.b : 0;
+                        for (int t = 0; t < 2; ++t)
+                            for (int c = 0; c < D / 64; ++c)
+                                tma_prefetch_l2_4d(&tmQ, c * 64, nx.h0, nq + t * a.QP, nbc);
+                    }
+                }
                 for (int j = 0; j < x.n_kv && ok; ++j) {
                     const int k0 = x.kv_start + j * kBN;
+                    if (j + kPrefetchTiles < x.n_kv) prefetch_kv(j + kPrefetchTiles);
 #pragma unroll
                     for (int which = 0; which < 2; ++which) {
                         const uint32_t it = kv_it++;
