@@ -14,8 +14,10 @@
 //   together, so every K/V tile brought in by TMA serves all of those heads
 //   (the cross-head KV reuse of the same page, section 5).
 // * Warp roles: warps 0-3 and 4-7 are the softmax warpgroups of Q tile 0 and
-//   Q tile 1 (TMEM lane = row = thread); warp 8 issues tcgen05.mma from one
-//   thread; warp 9 issues TMA loads from one thread.
+//   Q tile 1 (TMEM lane = row = thread); warps 8 and 9 issue the tcgen05.mma
+//   of Q tile 0 and Q tile 1 (one thread each: a single issuing thread leaves
+//   the tensor core idle whenever it waits on a dependency, two keep it fed);
+//   warp 10 issues TMA loads from one thread; warp 11 idles.
 // * TMEM (512 columns): S0 | S1 | O0 | O1.  S_t = Q_t K^T accumulates in fp32;
 //   the softmax writes P_t as bf16/fp16 pairs over the first half of S_t and
 //   the PV MMA reads P_t straight from TMEM (A operand in TMEM, V from shared
@@ -52,8 +54,9 @@ constexpr int kBN = 128;  // keys per KV tile
 // 104: 256 x 200 + 128 x 104 = 64512, and per SM sub-partition
 // 2 x 200 + 104 <= 512 register slots a lane.
 constexpr int kThreads = 384;
-constexpr int kMmaWarp = 8;
-constexpr int kLoadWarp = 9;
+constexpr int kMmaWarp0 = 8;  // issues the MMAs of Q tile 0; owns the TMEM allocation
+constexpr int kMmaWarp1 = 9;  // issues the MMAs of Q tile 1
+constexpr int kLoadWarp = 10;
 constexpr uint32_t kRegsSoftmax = 200;
 constexpr uint32_t kRegsOther = 104;
 static_assert(256 * kRegsSoftmax + 128 * kRegsOther <= kThreads * 168, "register split");
@@ -98,8 +101,11 @@ enum : int {
     B_P_READY = 4,   // [2]
     B_O_FULL = 6,    // [2]
     B_O_EMPTY = 8,   // [2]
-    B_TEARDOWN = 10,
-    B_KV_FULL = 11,  // [NS]
+    B_TEARDOWN = 10,  // [2]
+    B_KV_FULL = 12,   // [NS] kv_full, [NS] kv_empty, [NS] v_tail: the zeroed tail V
+                      // tile of a ring slot, handed from MMA warp 0 to MMA warp 1
+                      // (a slot is refilled only after both warps released it, so
+                      // its v_tail barrier is never more than one phase ahead)
 };
 
 struct UnitInfo {
@@ -193,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t kv_smem = base + L::KV_OFF;
     const uint32_t bars = base + L::BAR_OFF;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + L::BAR_OFF + 8 * (B_KV_FULL + 2 * NS));
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + L::BAR_OFF + 8 * (B_KV_FULL + 3 * NS));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const AttnParams &p = a.p;
@@ -201,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(B_Q_FULL), 1);
-        mbar_init(bar(B_Q_EMPTY), 1);
+        mbar_init(bar(B_Q_EMPTY), 2);  // one commit from each MMA warp
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(B_S_FULL + t), 1);
             mbar_init(bar(B_P_READY + t), 128);
@@ -209,14 +215,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(B_O_EMPTY + t), 128);
         }
         mbar_init(bar(B_TEARDOWN), 1);
+        mbar_init(bar(B_TEARDOWN + 1), 1);
         for (int s = 0; s < NS; ++s) {
             mbar_init(bar(B_KV_FULL + s), 1);
-            mbar_init(bar(B_KV_FULL + NS + s), 1);  // kv_empty
+            mbar_init(bar(B_KV_FULL + NS + s), 2);  // kv_empty: one commit per MMA warp
+            mbar_init(bar(B_KV_FULL + 2 * NS + s), 1);  // v_tail
         }
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == kMmaWarp) {
+    if (warp == kMmaWarp0) {
         tmem_alloc(smem_addr(tmem_slot), 512);
         tmem_relinquish();
     }
@@ -231,6 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     auto kv_full = [&](int s) { return bar(B_KV_FULL + s); };
     auto kv_empty = [&](int s) { return bar(B_KV_FULL + NS + s); };
+    auto v_tail = [&](int s) { return bar(B_KV_FULL + 2 * NS + s); };
     auto stage = [&](int s) { return kv_smem + (uint32_t)s * L::STAGE; };
     const bool padded = p.cu_q == nullptr;
 
@@ -315,55 +324,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (armed & (1u << s))
                     mbar_wait(kv_full(s), (armed_parity >> s) & 1u, abort_flag, kWaitLimitNs);
         }
-    } else if (warp == kMmaWarp) {
-        // --------------------------------------------------- MMA issuer
-        uint32_t kv_it = 0, q_ph = 0;
-        uint32_t p_ph[2] = {0u, 0u}, oe_ph[2] = {0u, 0u};
+    } else if (warp == kMmaWarp0 || warp == kMmaWarp1) {
+        // -------------------------------------- MMA issuers, one per Q tile
+        // Each warp runs the chain S_t(j) -> [softmax_t] -> PV_t(j) -> S_t(j+1)
+        // of its own tile; two issuing warps keep the tensor core fed while
+        // either one waits.  P_t aliases S_t in TMEM, so S_t(j+1) is issued
+        // after PV_t(j) by the same thread (tcgen05.mma executes in order).
+        const int t = warp - kMmaWarp0;
+        uint32_t kv_it = 0, q_ph = 0, p_ph = 0, oe_ph = 0;
+        uint32_t vt_ph = 0;  // per ring slot: parity of its next v_tail phase (bit s)
         bool ok = true;
-        const uint32_t s_col[2] = {0u, 128u};
-        const uint32_t o_col[2] = {(uint32_t)L::O_COL, (uint32_t)(L::O_COL + DV)};
+        const uint32_t s_tm = tmem + (uint32_t)t * 128u;
+        const uint32_t o_tm = tmem + (uint32_t)(L::O_COL + t * DV);
+        const uint64_t qd = sw128_desc(q_smem + t * L::QTILE, 16, 1024);
         for (long long u = blockIdx.x; u < a.nunits && ok; u += gridDim.x) {
             const UnitInfo x = unit_info(a, u);
             if (x.n_kv == 0) continue;
             if (!warp_wait(bar(B_Q_FULL), q_ph, abort_flag)) {
-                if (lane == 0) raise_abort(abort_flag, p.status, kStatusTimeoutMma);
                 ok = false;
                 break;
             }
             q_ph ^= 1u;
             const uint32_t kb = kv_it;
 
-            auto issue_s = [&](int t, int kslot) {
-                if (lane == 0) {
-                    // the start-address field is the low 14 bits (address >> 4)
-                    const uint64_t qd = sw128_desc(q_smem + t * L::QTILE, 16, 1024);
-                    const uint64_t kd = sw128_desc(stage(kslot), 16, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = ((kk / 4) * kChunkBytes + (kk % 4) * 32) >> 4;
-                        mma_ss(tmem + s_col[t], qd + off, kd + off, a.idesc_s, kk > 0);
-                    }
-                    mma_commit(bar(B_S_FULL + t));
-                }
-                __syncwarp();
-            };
-            // O_t += P_t V_jj
-            auto issue_pv = [&](int t, int jj) -> bool {
-                if (!warp_wait(bar(B_P_READY + t), p_ph[t], abort_flag)) return false;
-                p_ph[t] ^= 1u;
+            // O_t (+)= P_t V_jj, then release V_jj
+            auto issue_pv = [&](int jj) -> bool {
+                if (!warp_wait(bar(B_P_READY + t), p_ph, abort_flag)) return false;
+                p_ph ^= 1u;
                 if (jj == 0) {  // the previous unit's epilogue has read O_t
-                    if (!warp_wait(bar(B_O_EMPTY + t), oe_ph[t] ^ 1u, abort_flag)) return false;
-                    oe_ph[t] ^= 1u;
+                    if (!warp_wait(bar(B_O_EMPTY + t), oe_ph ^ 1u, abort_flag)) return false;
+                    oe_ph ^= 1u;
                 }
                 const uint32_t it = kb + 2u * (uint32_t)jj + 1u;
                 const int vslot = (int)(it % NS);
-                if (t == 0) {
+                const int k0 = x.kv_start + jj * kBN;
+                const int nzero = k0 + kBN - x.hi_unit;  // rows past the last key in use
+                if (t == 0 || nzero <= 0) {
                     if (!warp_wait(kv_full(vslot), (it / NS) & 1u, abort_flag)) return false;
-                    // rows past the last key any row uses may hold anything
-                    // (NaN included): zero them so 0 * V stays 0
-                    const int k0 = x.kv_start + jj * kBN;
-                    const int nzero = k0 + kBN - x.hi_unit;
-                    if (nzero > 0) {
+                }
+                if (nzero > 0) {
+                    if (t == 0) {
+                        // those rows may hold anything (NaN included): zero them so
+                        // that 0 * V stays 0, then hand the tile to the other warp
                         uint8_t *vt = gbase + (stage(vslot) - base);
                         for (int i = lane; i < nzero * 8 * (DV / 64); i += 32) {
                             const int c = i / (nzero * 8), rem = i % (nzero * 8);
@@ -373,6 +375,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         fence_proxy_async_smem();
                         __syncwarp();
+                        if (lane == 0) mbar_arrive(v_tail(vslot));
+                    } else {
+                        if (!warp_wait(v_tail(vslot), (vt_ph >> vslot) & 1u, abort_flag))
+                            return false;
+                        vt_ph ^= 1u << vslot;
                     }
                 }
                 tc_fence_after();
@@ -380,63 +387,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t vd = sw128_desc(stage(vslot), kChunkBytes, 1024);
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk)
-                        mma_ts(tmem + o_col[t], tmem + s_col[t] + kk * 8, vd + (kk * 2048 >> 4),
-                               a.idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+                        mma_ts(o_tm, s_tm + kk * 8, vd + (kk * 2048 >> 4), a.idesc_o,
+                               (jj > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(kv_empty(vslot));
                 }
                 __syncwarp();
                 return true;
             };
 
             for (int j = 0; j < x.n_kv && ok; ++j) {
-                const uint32_t it = kb + 2u * (uint32_t)j;
-                const int kslot = (int)(it % NS);
-                // PV0 of the previous tile does not need K_j: issue it first
-                if (j > 0 && !issue_pv(0, j - 1)) {
+                if (j > 0 && !issue_pv(j - 1)) {
                     ok = false;
                     break;
                 }
+                const uint32_t it = kb + 2u * (uint32_t)j;
+                const int kslot = (int)(it % NS);
                 if (!warp_wait(kv_full(kslot), (it / NS) & 1u, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                issue_s(0, kslot);
-                if (j > 0) {
-                    if (!issue_pv(1, j - 1)) {
-                        ok = false;
-                        break;
-                    }
-                    if (lane == 0) mma_commit(kv_empty((int)((it - 1) % NS)));  // V_{j-1}
-                }
-                issue_s(1, kslot);
                 if (lane == 0) {
-                    mma_commit(kv_empty(kslot));                        // K_j
-                    if (j == x.n_kv - 1) mma_commit(bar(B_Q_EMPTY));   // Q tiles free
+                    // the start-address field is the low 14 bits (address >> 4)
+                    const uint64_t kd = sw128_desc(stage(kslot), 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = ((kk / 4) * kChunkBytes + (kk % 4) * 32) >> 4;
+                        mma_ss(s_tm, qd + off, kd + off, a.idesc_s, kk > 0);
+                    }
+                    mma_commit(bar(B_S_FULL + t));
+                    mma_commit(kv_empty(kslot));
+                    if (j == x.n_kv - 1) mma_commit(bar(B_Q_EMPTY));
                 }
                 __syncwarp();
             }
             if (!ok) break;
-            if (!issue_pv(0, x.n_kv - 1)) {
+            if (!issue_pv(x.n_kv - 1)) {
                 ok = false;
                 break;
             }
-            if (lane == 0) mma_commit(bar(B_O_FULL + 0));
-            if (!issue_pv(1, x.n_kv - 1)) {
-                ok = false;
-                break;
-            }
-            if (lane == 0) {
-                mma_commit(bar(B_O_FULL + 1));
-                mma_commit(kv_empty((int)((kb + 2u * (uint32_t)x.n_kv - 1u) % NS)));
-            }
+            if (lane == 0) mma_commit(bar(B_O_FULL + t));
             __syncwarp();
             kv_it += 2u * (uint32_t)x.n_kv;
         }
         if (!ok && lane == 0) raise_abort(abort_flag, p.status, kStatusTimeoutMma);
         // all MMAs issued by this warp complete before TMEM is released
         if (lane == 0) {
-            mma_commit(bar(B_TEARDOWN));
-            mbar_wait(bar(B_TEARDOWN), 0, abort_flag, kWaitLimitNs);
+            mma_commit(bar(B_TEARDOWN + t));
+            mbar_wait(bar(B_TEARDOWN + t), 0, abort_flag, kWaitLimitNs);
         }
         __syncwarp();
     } else if (warp < 8) {
@@ -595,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == kMmaWarp0) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
