@@ -448,6 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tmem + lane_off + (uint32_t)(L::O_COL + t * DV);
         const float c = a.c_scale;
         uint32_t s_ph = 0, o_ph = 0;
+        uint32_t ntile = 0;  // tiles this warpgroup has processed (all units)
         bool ok = true;
         T *og = static_cast<T *>(p.o);
 
@@ -473,6 +474,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             float m_run = -INFINITY, l_run = 0.f;
             for (int j = 0; j < x.n_kv; ++j) {
+                // The two warpgroups take turns (tile k of group 0, tile k of
+                // group 1, tile k+1 of group 0, ...): while one runs its softmax
+                // the tensor core works on the other's tile.  Left free, the two
+                // drift into step and then both wait on the tensor core together.
+                // Each p_ready barrier is thus never more than one phase ahead.
+                if (t == 1) {
+                    if (!warp_wait(bar(B_P_READY + 0), ntile & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                } else if (ntile > 0) {
+                    if (!warp_wait(bar(B_P_READY + 1), (ntile - 1) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                ++ntile;
                 if (!warp_wait(bar(B_S_FULL + t), s_ph, abort_flag)) {
                     ok = false;
                     break;
