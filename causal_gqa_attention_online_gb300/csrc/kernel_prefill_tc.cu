@@ -474,23 +474,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             float m_run = -INFINITY, l_run = 0.f;
             for (int j = 0; j < x.n_kv; ++j) {
-                // The two warpgroups take turns (tile k of group 0, tile k of
-                // group 1, tile k+1 of group 0, ...): while one runs its softmax
-                // the tensor core works on the other's tile.  Left free, the two
-                // drift into step and then both wait on the tensor core together.
-                // Each p_ready barrier is thus never more than one phase ahead.
-                if (t == 1) {
-                    if (!warp_wait(bar(B_P_READY + 0), ntile & 1u, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                } else if (ntile > 0) {
-                    if (!warp_wait(bar(B_P_READY + 1), (ntile - 1) & 1u, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                }
-                ++ntile;
                 if (!warp_wait(bar(B_S_FULL + t), s_ph, abort_flag)) {
                     ok = false;
                     break;
@@ -514,15 +497,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (kr < lo_rel || kr >= hi_rel) sr[cc][i] = __float_as_uint(-INFINITY);
                         }
                 }
-                // row max: four independent chains of 3-input max
-                float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                // row max: eight independent chains of 3-input max
+                float mc[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mc[i] = -INFINITY;
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        mc[i & 3] = fmax3(mc[i & 3], __uint_as_float(sr[cc][2 * i]),
+                        mc[i & 7] = fmax3(mc[i & 7], __uint_as_float(sr[cc][2 * i]),
                                           __uint_as_float(sr[cc][2 * i + 1]));
-                const float mx = fmax3(fmaxf(mc[0], mc[1]), mc[2], mc[3]);
+                const float mx = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]),
+                                       fmaxf(mc[6], mc[7]));
                 const float m_tile = mx * c;
                 float alpha = 1.f;
                 bool rescale = false;
@@ -534,6 +520,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     rescale = true;
                 }
                 const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
+                // The two warpgroups take turns on the exp phase (tile k of group
+                // 0, tile k of group 1, tile k+1 of group 0, ...): the exps of one
+                // group overlap the other group's TMEM load and row max, and the
+                // tensor core works on one tile while the other is in softmax.
+                // Left free, the two drift into step and then wait on the tensor
+                // core together.  Each p_ready barrier is thus never more than one
+                // phase ahead of the group that waits on it.
+                if (t == 1) {
+                    if (!warp_wait(bar(B_P_READY + 0), ntile & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                } else if (ntile > 0) {
+                    if (!warp_wait(bar(B_P_READY + 1), (ntile - 1) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                ++ntile;
                 float sc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
