@@ -63,6 +63,9 @@ static_assert(256 * kRegsSoftmax + 128 * kRegsOther <= kThreads * 168, "register
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kChunkBytes = 128 * 128;       // one 128-row x 128-byte swizzled chunk
 constexpr int kPrefetchTiles = 4;                 // K/V tiles pulled into L2 ahead of use
+// Where the two softmax warpgroups take turns: 0 = never, 1 = the whole
+// softmax of a tile, 2 = only its exp phase.
+constexpr int kTurnMode = 1;
 
 struct PrefillArgs {
     AttnParams p;
@@ -163,6 +166,26 @@ template <> __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float r;
     asm("max.f32 %0, %1, %2, %3;\n" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Packed fp32 pairs (two lanes of work per instruction on sm_100+).
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};\n" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;\n" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;\n" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
 
@@ -474,6 +497,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             float m_run = -INFINITY, l_run = 0.f;
             for (int j = 0; j < x.n_kv; ++j) {
+                // The two warpgroups take turns (tile k of group 0, tile k of
+                // group 1, tile k+1 of group 0, ...): while one runs its softmax
+                // the tensor core works on the other's tile.  Left free, the two
+                // drift into step and then both wait on the tensor core together.
+                // Each p_ready barrier is thus never more than one phase ahead
+                // of the group that waits on it.
+                auto take_turn = [&]() -> bool {
+                    bool w = true;
+                    if (t == 1)
+                        w = warp_wait(bar(B_P_READY + 0), ntile & 1u, abort_flag);
+                    else if (ntile > 0)
+                        w = warp_wait(bar(B_P_READY + 1), (ntile - 1) & 1u, abort_flag);
+                    ++ntile;
+                    return w;
+                };
+                if (kTurnMode == 1 && !take_turn()) {
+                    ok = false;
+                    break;
+                }
                 if (!warp_wait(bar(B_S_FULL + t), s_ph, abort_flag)) {
                     ok = false;
                     break;
@@ -520,26 +562,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     rescale = true;
                 }
                 const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
-                // The two warpgroups take turns on the exp phase (tile k of group
-                // 0, tile k of group 1, tile k+1 of group 0, ...): the exps of one
-                // group overlap the other group's TMEM load and row max, and the
-                // tensor core works on one tile while the other is in softmax.
-                // Left free, the two drift into step and then wait on the tensor
-                // core together.  Each p_ready barrier is thus never more than one
-                // phase ahead of the group that waits on it.
-                if (t == 1) {
-                    if (!warp_wait(bar(B_P_READY + 0), ntile & 1u, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                } else if (ntile > 0) {
-                    if (!warp_wait(bar(B_P_READY + 1), (ntile - 1) & 1u, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
+                if (kTurnMode == 2 && !take_turn()) {
+                    ok = false;
+                    break;
                 }
-                ++ntile;
-                float sc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                // p = 2^(s*c - m) two keys at a time: one packed FMA, two MUFU
+                // exps, one packed add into the row sum, one pack to P
+                const uint64_t c2 = f2pack(c, c), nm2 = f2pack(neg_m, neg_m);
+                uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     // P columns [32*half, 32*half + 32) hold keys [64*half, 64*half + 64)
@@ -548,16 +578,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int cc = 2 * half; cc < 2 * half + 2; ++cc)
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const float p0 = ex2(fmaf(__uint_as_float(sr[cc][2 * i]), c, neg_m));
-                            const float p1 =
-                                ex2(fmaf(__uint_as_float(sr[cc][2 * i + 1]), c, neg_m));
-                            sc[(2 * i) & 7] += p0;
-                            sc[(2 * i + 1) & 7] += p1;
+                            const uint64_t x2 = ffma2(
+                                f2pack(__uint_as_float(sr[cc][2 * i]), __uint_as_float(sr[cc][2 * i + 1])),
+                                c2, nm2);
+                            float x0, x1;
+                            f2unpack(x2, x0, x1);
+                            const float p0 = ex2(x0), p1 = ex2(x1);
+                            acc2[i & 3] = fadd2(acc2[i & 3], f2pack(p0, p1));
                             pk[(cc & 1) * 16 + i] = pack2<T>(p0, p1);
                         }
                     tmem_st32(tS + 32 * half, pk);
                 }
-                const float sum = ((sc[0] + sc[1]) + (sc[2] + sc[3])) + ((sc[4] + sc[5]) + (sc[6] + sc[7]));
+                float sa[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) f2unpack(acc2[i], sa[2 * i], sa[2 * i + 1]);
+                const float sum = ((sa[0] + sa[1]) + (sa[2] + sa[3])) + ((sa[4] + sa[5]) + (sa[6] + sa[7]));
                 l_run = l_run * alpha + sum;
                 if (__any_sync(0xffffffffu, rescale)) {
                     // O_t holds every PV up to tile j-1: the commit that
