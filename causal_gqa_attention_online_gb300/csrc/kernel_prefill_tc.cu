@@ -8,7 +8,8 @@
 //
 // * Persistent CTAs, one per SM, walk work units (sequence, KV head, head
 //   subgroup, query block) in longest-first order (bottom-right causal: the
-//   last query blocks see the most keys).
+//   last query blocks see the most keys), in rounds that alternate direction
+//   across the CTAs so that the total work per CTA evens out.
 // * A unit holds two Q tiles of 128 rows.  The rows of a tile are
 //   (query position, head) pairs with up to 16 heads of one KV group packed
 //   together, so every K/V tile brought in by TMA serves all of those heads
@@ -153,6 +154,14 @@ __device__ __forceinline__ UnitInfo unit_info(const PrefillArgs &a, long long u)
     return x;
 }
 
+// Unit processed by CTA c in round r: rounds alternate direction over the
+// longest-first unit order (c, then G-1-c, ...), so every CTA gets a mix of
+// long and short units (a plain stride leaves CTA 0 with the longest of every
+// round).
+__device__ __forceinline__ long long snake_unit(long long r, int c, int G) {
+    return r * G + ((r & 1) ? (G - 1 - c) : c);
+}
+
 template <typename T> __device__ __forceinline__ uint32_t pack2(float lo, float hi);
 template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -274,7 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int last_q_parity = -1;
             uint32_t armed = 0, armed_parity = 0;  // per ring slot: loaded at least once, last parity
             bool ok = true;
-            for (long long u = blockIdx.x; u < a.nunits && ok; u += gridDim.x) {
+            for (long long rnd = 0; rnd * gridDim.x < a.nunits && ok; ++rnd) {
+                const long long u = snake_unit(rnd, blockIdx.x, gridDim.x);
+                if (u >= a.nunits) continue;
                 const UnitInfo x = unit_info(a, u);
                 if (x.n_kv == 0) continue;
                 const int qrow = (padded ? 0 : (int)x.si.q_off) + x.q0;
@@ -301,8 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_prefetch_l2_4d(&tmV, c * 64, x.kvh, krow + kk0, bc);
                 };
                 for (int jj = 1; jj < kPrefetchTiles && jj < x.n_kv; ++jj) prefetch_kv(jj);
-                if (u + gridDim.x < a.nunits) {
-                    const UnitInfo nx = unit_info(a, u + gridDim.x);
+                const long long un = snake_unit(rnd + 1, blockIdx.x, gridDim.x);
+                if (un < a.nunits) {
+                    const UnitInfo nx = unit_info(a, un);
                     if (nx.n_kv > 0) {
                         const int nq = (padded ? 0 : (int)nx.si.q_off) + nx.q0;
                         const int nbc = padded ? nx.b : 0;
@@ -360,7 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t s_tm = tmem + (uint32_t)t * 128u;
         const uint32_t o_tm = tmem + (uint32_t)(L::O_COL + t * DV);
         const uint64_t qd = sw128_desc(q_smem + t * L::QTILE, 16, 1024);
-        for (long long u = blockIdx.x; u < a.nunits && ok; u += gridDim.x) {
+        for (long long rnd = 0; rnd * gridDim.x < a.nunits && ok; ++rnd) {
+            const long long u = snake_unit(rnd, blockIdx.x, gridDim.x);
+            if (u >= a.nunits) continue;
             const UnitInfo x = unit_info(a, u);
             if (x.n_kv == 0) continue;
             if (!warp_wait(bar(B_Q_FULL), q_ph, abort_flag)) {
@@ -475,7 +489,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         T *og = static_cast<T *>(p.o);
 
-        for (long long u = blockIdx.x; u < a.nunits && ok; u += gridDim.x) {
+        for (long long rnd = 0; rnd * gridDim.x < a.nunits && ok; ++rnd) {
+            const long long u = snake_unit(rnd, blockIdx.x, gridDim.x);
+            if (u >= a.nunits) continue;
             const UnitInfo x = unit_info(a, u);
             const int qpos = x.q0 + t * a.QP + r / a.Gp;
             const int head = x.h0 + r % a.Gp;
