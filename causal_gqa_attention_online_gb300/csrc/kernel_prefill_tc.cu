@@ -86,11 +86,13 @@ template <int D, int DV> struct Layout {
     static constexpr int VTILE = kBN * DV * 2;
     static constexpr int STAGE = KTILE > VTILE ? KTILE : VTILE;
     static constexpr int BUDGET = 227 * 1024;  // opt-in shared memory per block
-    static constexpr int NS_FIT = (BUDGET - 2 * QTILE - 1024 - 512) / STAGE;
+    static constexpr int STG_BYTES = 8 * 4096;  // epilogue staging: 4 KB per softmax warp
+    static constexpr int NS_FIT = (BUDGET - 2 * QTILE - STG_BYTES - 1024 - 512) / STAGE;
     static constexpr int NS = NS_FIT > 8 ? 8 : NS_FIT;
     static constexpr int Q_OFF = 0;
     static constexpr int KV_OFF = 2 * QTILE;
-    static constexpr int BAR_OFF = KV_OFF + NS * STAGE;
+    static constexpr int STG_OFF = KV_OFF + NS * STAGE;
+    static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
     static constexpr int SMEM = 1024 + BAR_OFF + 512;  // + alignment slack
     static constexpr int O_COL = 256;                  // TMEM columns: S0 S1 | O0 O1
     static_assert(NS >= 2, "K/V ring needs two stages");
@@ -639,24 +641,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const bool has = valid && l_run > 0.f;
             const float inv = has ? 1.f / l_run : 0.f;
+            // O rows go out through a per-warp staging area so that every store
+            // instruction writes four 128-byte row segments instead of 32
+            // scattered 16-byte pieces.  Staging rows hold 64 columns (128 B);
+            // their 16-byte chunks are XOR-swizzled by the row's low 3 bits.
+            const uint32_t wmask = __ballot_sync(0xffffffffu, writes);
+            uint8_t *stg = gbase + L::STG_OFF + warp * 4096;
 #pragma unroll
-            for (int cc = 0; cc < DV / 32; ++cc) {
-                uint32_t ov[32];
-                tmem_ld32(tO + cc * 32, ov);
-                tmem_ld_wait();
-                if (writes) {
-                    uint32_t pkd[16];
+            for (int cp = 0; cp < DV / 64; ++cp) {
+                uint32_t pkd[32];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t ov[32];
+                    tmem_ld32(tO + cp * 64 + h * 32, ov);
+                    tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const float o0 = has ? __uint_as_float(ov[2 * i]) * inv : 0.f;
                         const float o1 = has ? __uint_as_float(ov[2 * i + 1]) * inv : 0.f;
-                        pkd[i] = pack2<T>(o0, o1);
+                        pkd[h * 16 + i] = pack2<T>(o0, o1);
                     }
-                    uint4 *dst = reinterpret_cast<uint4 *>(og + orow * DV + cc * 32);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
                 }
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4 *>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                        make_uint4(pkd[4 * c], pkd[4 * c + 1], pkd[4 * c + 2], pkd[4 * c + 3]);
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int e = i * 32 + lane;      // 16-byte piece of the warp's 32 x 128 B
+                    const int row = e >> 3, c = e & 7;  // row of this warp, chunk within it
+                    const uint4 v =
+                        *reinterpret_cast<const uint4 *>(stg + row * 128 + ((c ^ (row & 7)) << 4));
+                    if ((wmask >> row) & 1u) {
+                        const int rr = quarter * 32 + row;
+                        const int qp = x.q0 + t * a.QP + rr / a.Gp;
+                        const long long orr = (x.si.q_off + qp) * p.Hq + x.h0 + rr % a.Gp;
+                        *reinterpret_cast<uint4 *>(og + orr * DV + cp * 64 + c * 8) = v;
+                    }
+                }
+                __syncwarp();
             }
             if (writes && p.lse) p.lse[orow] = has ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
             tc_fence_before();
