@@ -541,31 +541,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 s_ph ^= 1u;
                 tc_fence_after();
                 uint32_t sr[4][32];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
+                tmem_ld_wait();
                 const int k0 = x.kv_start + j * kBN;
                 const bool interior = x.all_valid && k0 >= x.lo_last && k0 + kBN <= x.hi_first;
-                // S_t row of this thread into registers; keys outside [lo, hi)
-                // become -inf (which also replaces NaN from padding rows)
-                auto load_s = [&]() {
+                if (!interior) {
+                    // keys outside [lo, hi) -> -inf (also replaces NaN from padding)
+                    const int lo_rel = lo - k0, hi_rel = hi - k0;
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
-                    tmem_ld_wait();
-                    if (!interior) {
-                        const int lo_rel = lo - k0, hi_rel = hi - k0;
+                    for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-                        for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) {
-                                const int kr = cc * 32 + i;
-                                if (kr < lo_rel || kr >= hi_rel) sr[cc][i] = __float_as_uint(-INFINITY);
-                            }
-                    }
-                };
-                load_s();
+                        for (int i = 0; i < 32; ++i) {
+                            const int kr = cc * 32 + i;
+                            if (kr < lo_rel || kr >= hi_rel) sr[cc][i] = __float_as_uint(-INFINITY);
+                        }
+                }
                 // p = 2^(s*c - m) two keys at a time (one packed FMA, two MUFU exps,
                 // one packed add into the row sum, one pack to P), tracking the
                 // largest exponent x = s*c - m on the side (ALU work that hides
                 // under the MUFU-bound exps).
-                uint32_t pk[64];  // P of the row as 64 packed pairs (stored after the check)
                 auto exp_pass = [&](float neg_m, float &sum, float &xmax) {
                     const uint64_t c2 = f2pack(c, c), nm2 = f2pack(neg_m, neg_m);
                     uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
@@ -573,19 +568,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 8; ++i) xm[i] = -INFINITY;
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc)
+                    for (int half = 0; half < 2; ++half) {
+                        // P columns [32*half, 32*half + 32) hold keys [64*half, 64*half + 64)
+                        uint32_t pk[32];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const uint64_t x2 = ffma2(f2pack(__uint_as_float(sr[cc][2 * i]),
-                                                             __uint_as_float(sr[cc][2 * i + 1])),
-                                                      c2, nm2);
-                            float x0, x1;
-                            f2unpack(x2, x0, x1);
-                            xm[i & 7] = fmax3(xm[i & 7], x0, x1);
-                            const float p0 = ex2(x0), p1 = ex2(x1);
-                            acc2[i & 3] = fadd2(acc2[i & 3], f2pack(p0, p1));
-                            pk[cc * 16 + i] = pack2<T>(p0, p1);
-                        }
+                        for (int cc = 2 * half; cc < 2 * half + 2; ++cc)
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const uint64_t x2 = ffma2(f2pack(__uint_as_float(sr[cc][2 * i]),
+                                                                 __uint_as_float(sr[cc][2 * i + 1])),
+                                                          c2, nm2);
+                                float x0, x1;
+                                f2unpack(x2, x0, x1);
+                                xm[i & 7] = fmax3(xm[i & 7], x0, x1);
+                                const float p0 = ex2(x0), p1 = ex2(x1);
+                                acc2[i & 3] = fadd2(acc2[i & 3], f2pack(p0, p1));
+                                pk[(cc & 1) * 16 + i] = pack2<T>(p0, p1);
+                            }
+                        tmem_st32(tS + 32 * half, pk);
+                    }
                     float sa[8];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) f2unpack(acc2[i], sa[2 * i], sa[2 * i + 1]);
@@ -597,9 +598,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // than 2^8 (p <= 2^8 stays exact in fp32 and in P's 8-bit
                 // significand).  A row that has seen no key yet takes this tile's
                 // max first (two passes); every other row computes P straight
-                // against m_run, and the rare row whose max grew too far sends its
-                // warp through the tile again with the new reference (S is still
-                // intact in TMEM: P is stored only after the check).
+                // against m_run and the rare row whose max grew too far sends its
+                // warp through the tile again with the new reference.
                 if (m_run == -INFINITY) {
                     float mc[8];
 #pragma unroll
@@ -617,30 +617,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                float alpha = 1.f, sum;
+                float alpha = 1.f, sum, xmax;
                 bool rescale = false;
-#pragma unroll 1
-                for (int attempt = 0;; ++attempt) {
-                    float xmax;
-                    exp_pass(m_run == -INFINITY ? 0.f : -m_run, sum, xmax);
-                    const bool grow = attempt == 0 && xmax > 8.f;
-                    if (!__any_sync(0xffffffffu, grow)) break;
+                exp_pass(m_run == -INFINITY ? 0.f : -m_run, sum, xmax);
+                const bool grow = xmax > 8.f;
+                if (__any_sync(0xffffffffu, grow)) {
                     if (grow) {
                         alpha = ex2(-xmax);  // 2^(m_old - m_new)
                         m_run += xmax;
                         rescale = true;
                     }
-                    load_s();
-                }
-                {
-                    uint32_t lo32[32], hi32[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        lo32[i] = pk[i];
-                        hi32[i] = pk[32 + i];
-                    }
-                    tmem_st32(tS, lo32);       // keys 0-63
-                    tmem_st32(tS + 32, hi32);  // keys 64-127
+                    float unused;
+                    exp_pass(m_run == -INFINITY ? 0.f : -m_run, sum, unused);
                 }
                 l_run = l_run * alpha + sum;
                 if (__any_sync(0xffffffffu, rescale)) {
