@@ -557,79 +557,60 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (kr < lo_rel || kr >= hi_rel) sr[cc][i] = __float_as_uint(-INFINITY);
                         }
                 }
-                // p = 2^(s*c - m) two keys at a time (one packed FMA, two MUFU exps,
-                // one packed add into the row sum, one pack to P), tracking the
-                // largest exponent x = s*c - m on the side (ALU work that hides
-                // under the MUFU-bound exps).
-                auto exp_pass = [&](float neg_m, float &sum, float &xmax) {
-                    const uint64_t c2 = f2pack(c, c), nm2 = f2pack(neg_m, neg_m);
-                    uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
-                    float xm[8];
+                // row max: eight independent chains of 3-input max
+                float mc[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) xm[i] = -INFINITY;
+                for (int i = 0; i < 8; ++i) mc[i] = -INFINITY;
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        // P columns [32*half, 32*half + 32) hold keys [64*half, 64*half + 64)
-                        uint32_t pk[32];
+                for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-                        for (int cc = 2 * half; cc < 2 * half + 2; ++cc)
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const uint64_t x2 = ffma2(f2pack(__uint_as_float(sr[cc][2 * i]),
-                                                                 __uint_as_float(sr[cc][2 * i + 1])),
-                                                          c2, nm2);
-                                float x0, x1;
-                                f2unpack(x2, x0, x1);
-                                xm[i & 7] = fmax3(xm[i & 7], x0, x1);
-                                const float p0 = ex2(x0), p1 = ex2(x1);
-                                acc2[i & 3] = fadd2(acc2[i & 3], f2pack(p0, p1));
-                                pk[(cc & 1) * 16 + i] = pack2<T>(p0, p1);
-                            }
-                        tmem_st32(tS + 32 * half, pk);
-                    }
-                    float sa[8];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) f2unpack(acc2[i], sa[2 * i], sa[2 * i + 1]);
-                    sum = ((sa[0] + sa[1]) + (sa[2] + sa[3])) + ((sa[4] + sa[5]) + (sa[6] + sa[7]));
-                    xmax = fmax3(fmax3(xm[0], xm[1], xm[2]), fmax3(xm[3], xm[4], xm[5]),
-                                 fmaxf(xm[6], xm[7]));
-                };
-                // The reference max m_run only moves when a row's max grows by more
-                // than 2^8 (p <= 2^8 stays exact in fp32 and in P's 8-bit
-                // significand).  A row that has seen no key yet takes this tile's
-                // max first (two passes); every other row computes P straight
-                // against m_run and the rare row whose max grew too far sends its
-                // warp through the tile again with the new reference.
+                    for (int i = 0; i < 16; ++i)
+                        mc[i & 7] = fmax3(mc[i & 7], __uint_as_float(sr[cc][2 * i]),
+                                          __uint_as_float(sr[cc][2 * i + 1]));
+                const float mx = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]),
+                                       fmaxf(mc[6], mc[7]));
+                const float m_tile = mx * c;
+                float alpha = 1.f;
+                bool rescale = false;
                 if (m_run == -INFINITY) {
-                    float mc[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) mc[i] = -INFINITY;
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            mc[i & 7] = fmax3(mc[i & 7], __uint_as_float(sr[cc][2 * i]),
-                                              __uint_as_float(sr[cc][2 * i + 1]));
-                    m_run = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]),
-                                  fmaxf(mc[6], mc[7])) * c;  // stays -inf if no key yet
+                    m_run = m_tile;  // first keys of this row (or still none)
+                } else if (m_tile > m_run + 8.f) {
+                    alpha = ex2(m_run - m_tile);
+                    m_run = m_tile;
+                    rescale = true;
                 }
+                const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
                 if (kTurnMode == 2 && !take_turn()) {
                     ok = false;
                     break;
                 }
-                float alpha = 1.f, sum, xmax;
-                bool rescale = false;
-                exp_pass(m_run == -INFINITY ? 0.f : -m_run, sum, xmax);
-                const bool grow = xmax > 8.f;
-                if (__any_sync(0xffffffffu, grow)) {
-                    if (grow) {
-                        alpha = ex2(-xmax);  // 2^(m_old - m_new)
-                        m_run += xmax;
-                        rescale = true;
-                    }
-                    float unused;
-                    exp_pass(m_run == -INFINITY ? 0.f : -m_run, sum, unused);
+                // p = 2^(s*c - m) two keys at a time: one packed FMA, two MUFU
+                // exps, one packed add into the row sum, one pack to P
+                const uint64_t c2 = f2pack(c, c), nm2 = f2pack(neg_m, neg_m);
+                uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    // P columns [32*half, 32*half + 32) hold keys [64*half, 64*half + 64)
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int cc = 2 * half; cc < 2 * half + 2; ++cc)
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const uint64_t x2 = ffma2(
+                                f2pack(__uint_as_float(sr[cc][2 * i]), __uint_as_float(sr[cc][2 * i + 1])),
+                                c2, nm2);
+                            float x0, x1;
+                            f2unpack(x2, x0, x1);
+                            const float p0 = ex2(x0), p1 = ex2(x1);
+                            acc2[i & 3] = fadd2(acc2[i & 3], f2pack(p0, p1));
+                            pk[(cc & 1) * 16 + i] = pack2<T>(p0, p1);
+                        }
+                    tmem_st32(tS + 32 * half, pk);
                 }
+                float sa[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) f2unpack(acc2[i], sa[2 * i], sa[2 * i + 1]);
+                const float sum = ((sa[0] + sa[1]) + (sa[2] + sa[3])) + ((sa[4] + sa[5]) + (sa[6] + sa[7]));
                 l_run = l_run * alpha + sum;
                 if (__any_sync(0xffffffffu, rescale)) {
                     // O_t holds every PV up to tile j-1: the commit that
