@@ -70,7 +70,10 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples every 200 ms while running."""
+    """nvidia-smi clock / throttle samples every 20 ms, each stamped with the
+    host time it arrived; summary() keeps the samples inside the timed windows
+    recorded with mark() (or, if a window is shorter than the sampling
+    interval, the samples within 50 ms of it)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -79,50 +82,69 @@ class ClockSampler:
     def __init__(self, device_index: int):
         self.dev = device_index
         self.proc = None
-        self.path = None
+        self.lines = []
+        self.windows = []
+        self.thread = None
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line))
 
     def __enter__(self):
-        fd, self.path = tempfile.mkstemp(suffix=".csv")
-        os.close(fd)
+        import threading
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._reader, daemon=True)
+            self.thread.start()
         except (OSError, FileNotFoundError):
             self.proc = None
-        time.sleep(0.3)
+        time.sleep(0.2)
         return self
 
+    def mark(self, t0: float, t1: float):
+        self.windows.append((t0, t1))
+
     def __exit__(self, *exc):
+        time.sleep(0.1)
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+            if self.thread is not None:
+                self.thread.join(timeout=2)
 
     def summary(self):
-        if self.proc is None or not self.path:
+        if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        with open(self.path) as f:
-            for line in f:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sm.append(float(parts[1]))
-                    smax = float(parts[2])
-                except ValueError:
-                    continue
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower().startswith("active"):
-                        reasons.add(n)
-        os.unlink(self.path)
+
+        def pick(margin):
+            return [(t, l) for t, l in self.lines
+                    if any(a - margin <= t <= b + margin for a, b in self.windows)]
+
+        chosen, where = pick(0.0), "inside the timed region"
+        if not chosen:
+            chosen, where = pick(0.05), "within 50 ms of the timed region"
+        sm, smax, reasons = [], None, set()
+        for _, line in chosen:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "samples_from": where}
 
 
 def dist_setup():
@@ -152,20 +174,24 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
-def time_steps(fn, steps, warmup, flush, stream):
-    """Per-step device time (ms) of fn() with an L2 flush before each step."""
+def time_steps(fn, steps, warmup, flush, stream, clk=None):
+    """Per-step device time (ms) of fn() with an L2 flush before each step.
+    The host-side window of the timed steps is recorded on ``clk``."""
     for _ in range(warmup):
         flush.zero_()
         fn()
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
+    t0 = time.time()
     for a, b in evs:
         flush.zero_()
         a.record(stream)
         fn()
         b.record(stream)
     torch.cuda.synchronize()
+    if clk is not None:
+        clk.mark(t0, time.time())
     return [a.elapsed_time(b) for a, b in evs]
 
 
@@ -186,7 +212,7 @@ def measure_prefill(args, world, rank, dev, stream, flush, attn, synth):
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
-        times = time_steps(prefill, args.steps, args.warmup, flush, stream)
+        times = time_steps(prefill, args.steps, args.warmup, flush, stream, clk)
     torch.cuda.synchronize()
     barrier(world)
     launches = (attn.kernel_launches() - n0) // (args.steps + args.warmup)
@@ -230,7 +256,7 @@ def measure_decode(args, world, rank, dev, stream, flush, attn, synth):
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
-        times = time_steps(decode, args.steps, args.warmup, flush, stream)
+        times = time_steps(decode, args.steps, args.warmup, flush, stream, clk)
     barrier(world)
     launches = (attn.kernel_launches() - n1) // (args.steps + args.warmup)
     ms = max_over_ranks(sum(times) / len(times), world)
@@ -360,7 +386,7 @@ def oracle_sample_rate(inp, rows_budget_s=12.0, nthreads=0, seed=0):
     g = np.random.default_rng(seed)
     P = PREFILL
     total_flop, total_s, nrows = 0, 0.0, 0
-    batch = 2048
+    batch = 2048 if rows_budget_s >= 1.0 else 64
     while total_s < rows_budget_s:
         rows = np.stack([g.integers(0, P["B"], batch), g.integers(0, P["Q"], batch),
                          g.integers(0, P["Hq"], batch)], axis=1).astype(np.int32)
@@ -381,7 +407,7 @@ def run_reference(args, world, rank):
         return None
     inp = synth.prefill_bf16_b4_h32x8_s4096_d128(seed=1234)
     P = PREFILL
-    per_step_s = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    per_step_s = max(0.05, args.ref_seconds / max(1, args.steps + args.warmup))
     rates = []
     for i in range(args.warmup + args.steps):
         r, nrows, secs, threads = oracle_sample_rate(inp, per_step_s, seed=i)
@@ -407,10 +433,12 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="--impl reference: total seconds of oracle work over all steps")
     ap.add_argument("--only", default="all", choices=["all", "prefill", "decode"],
                     help="profiling aid: run one workload (the JSON line then lacks the other)")
     args = ap.parse_args()
