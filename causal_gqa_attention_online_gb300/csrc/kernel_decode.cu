@@ -139,6 +139,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p)
             hi_max = max(hi_max, hi);
         }
     }
+    // let the combine grid (a programmatic dependent launch) be scheduled
+    // while this grid's last blocks run; it waits for our completion itself
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     if (!mine) return;
     const int kbeg = max(lo_min, split * p.split_len);
     const int kend = min(hi_max, (split + 1) * p.split_len);

@@ -192,7 +192,35 @@ __device__ __forceinline__ void combine_one_row(const float *o_parts, const floa
         wsum += exp2f((lse_parts[s * part_stride_rows + prow] - mx) * kLog2e);
     wsum = warp_sum(wsum);
     const float inv = 1.f / wsum;
-    if ((Dv & 3) == 0) {
+    if ((Dv & 3) == 0 && Dv <= 128 && nsplit <= 16) {
+        // common case: one 4-column block per lane, every split's partial
+        // loaded before any is used (16 independent loads in flight a lane)
+        const int c = lane * 4;
+        const bool act = c < Dv;
+        const float wl = lane < nsplit
+            ? exp2f((lse_parts[lane * part_stride_rows + prow] - mx) * kLog2e) : 0.f;
+        float4 v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            v[j] = (act && j < nsplit)
+                ? *reinterpret_cast<const float4 *>(o_parts + (j * part_stride_rows + prow) * Dv + c)
+                : make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float w = __shfl_sync(0xffffffffu, wl, j);
+            a.x = fmaf(w, v[j].x, a.x);
+            a.y = fmaf(w, v[j].y, a.y);
+            a.z = fmaf(w, v[j].z, a.z);
+            a.w = fmaf(w, v[j].w, a.w);
+        }
+        if (act) {
+            orow[c] = from_f32<T>(a.x * inv);
+            orow[c + 1] = from_f32<T>(a.y * inv);
+            orow[c + 2] = from_f32<T>(a.z * inv);
+            orow[c + 3] = from_f32<T>(a.w * inv);
+        }
+    } else if ((Dv & 3) == 0) {
         // uniform trip count: every lane takes part in the shuffles
         for (int c0 = 0; c0 < Dv; c0 += 128) {
             const int c = c0 + lane * 4;
@@ -237,6 +265,9 @@ __device__ __forceinline__ void combine_one_row(const float *o_parts, const floa
 
 template <typename T>
 __global__ void __launch_bounds__(128) combine_rows_kernel(const AttnParams p) {
+    // launched as a programmatic dependent of the forward kernel: wait here
+    // until that grid has completed and its partials are visible
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     const int lane = threadIdx.x & 31;
     const long long row = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
     if (row >= (long long)p.B * p.Q * p.Hq) return;
@@ -322,12 +353,28 @@ int launch_generic(const AttnParams &p, int dtype, cudaStream_t stream) {
 int launch_combine_rows(const AttnParams &p, int dtype, cudaStream_t stream) {
     const long long rows = (long long)p.B * p.Q * p.Hq;
     if (rows == 0) return 0;
-    const unsigned blocks = (unsigned)((rows + 3) / 4);
+    // programmatic dependent launch: the combine grid is scheduled while the
+    // forward grid drains and waits in griddepcontrol.wait for its results
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((rows + 3) / 4));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t le = cudaSuccess;
     switch (dtype) {
-        case 0: combine_rows_kernel<float><<<blocks, 128, 0, stream>>>(p); break;
-        case 1: combine_rows_kernel<__half><<<blocks, 128, 0, stream>>>(p); break;
-        case 2: combine_rows_kernel<__nv_bfloat16><<<blocks, 128, 0, stream>>>(p); break;
+        case 0: le = cudaLaunchKernelEx(&cfg, combine_rows_kernel<float>, p); break;
+        case 1: le = cudaLaunchKernelEx(&cfg, combine_rows_kernel<__half>, p); break;
+        case 2: le = cudaLaunchKernelEx(&cfg, combine_rows_kernel<__nv_bfloat16>, p); break;
         default: set_error("combine: bad dtype %d", dtype); return 1;
+    }
+    if (le != cudaSuccess) {
+        set_error("combine kernel launch: %s", cudaGetErrorString(le));
+        return 3;
     }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
