@@ -65,7 +65,9 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kChunkBytes = 128 * 128;       // one 128-row x 128-byte swizzled chunk
 constexpr int kPrefetchTiles = 4;                 // K/V tiles pulled into L2 ahead of use
 // Where the two softmax warpgroups take turns: 0 = never, 1 = the whole
-// softmax of a tile, 2 = only its exp phase.
+// softmax of a tile (the turn passes when P is stored), 2 = only its exp
+// phase, 3 = the whole softmax, the turn passing as soon as the exps of the
+// tile are issued (the P store wait and arrival overlap the next group).
 constexpr int kTurnMode = 1;
 
 struct PrefillArgs {
@@ -108,7 +110,8 @@ enum : int {
     B_O_FULL = 6,    // [2]
     B_O_EMPTY = 8,   // [2]
     B_TEARDOWN = 10,  // [2]
-    B_KV_FULL = 12,   // [NS] kv_full, [NS] kv_empty, [NS] v_tail: the zeroed tail V
+    B_TURN = 12,      // [2] softmax group t has issued the exps of its tile
+    B_KV_FULL = 14,   // [NS] kv_full, [NS] kv_empty, [NS] v_tail: the zeroed tail V
                       // tile of a ring slot, handed from MMA warp 0 to MMA warp 1
                       // (a slot is refilled only after both warps released it, so
                       // its v_tail barrier is never more than one phase ahead)
@@ -247,6 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(B_P_READY + t), 128);
             mbar_init(bar(B_O_FULL + t), 1);
             mbar_init(bar(B_O_EMPTY + t), 128);
+            mbar_init(bar(B_TURN + t), 128);
         }
         mbar_init(bar(B_TEARDOWN), 1);
         mbar_init(bar(B_TEARDOWN + 1), 1);
@@ -522,15 +526,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Each p_ready barrier is thus never more than one phase ahead
                 // of the group that waits on it.
                 auto take_turn = [&]() -> bool {
+                    const int tb = kTurnMode == 3 ? B_TURN : B_P_READY;
                     bool w = true;
                     if (t == 1)
-                        w = warp_wait(bar(B_P_READY + 0), ntile & 1u, abort_flag);
+                        w = warp_wait(bar(tb + 0), ntile & 1u, abort_flag);
                     else if (ntile > 0)
-                        w = warp_wait(bar(B_P_READY + 1), (ntile - 1) & 1u, abort_flag);
+                        w = warp_wait(bar(tb + 1), (ntile - 1) & 1u, abort_flag);
                     ++ntile;
                     return w;
                 };
-                if (kTurnMode == 1 && !take_turn()) {
+                if ((kTurnMode == 1 || kTurnMode == 3) && !take_turn()) {
                     ok = false;
                     break;
                 }
@@ -607,6 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     tmem_st32(tS + 32 * half, pk);
                 }
+                if (kTurnMode == 3) mbar_arrive(bar(B_TURN + t));
                 float sa[8];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) f2unpack(acc2[i], sa[2 * i], sa[2 * i + 1]);
