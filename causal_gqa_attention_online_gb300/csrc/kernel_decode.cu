@@ -413,7 +413,7 @@ int decode_split_len(const AttnParams &p, int nsm) {
     long long len = ((long long)p.K * units + 4LL * nsm - 1) / (4LL * nsm);
     len = (len + kTK - 1) / kTK * kTK;
     if (len < 128) len = 128;
-    if (len > 512) len = 512;
+    if (len > 1024) len = 1024;
     return (int)len;
 }
 
