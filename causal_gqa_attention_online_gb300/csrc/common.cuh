@@ -17,7 +17,7 @@ enum : int {
     kStatusTimeoutKvEmpty = 0x102,
     kStatusTimeoutMma = 0x103,
     kStatusTimeoutSoftmax = 0x104,
-    kStatusTimeoutCorrection = 0x105,
+    kStatusTimeoutEpilogue = 0x105,
     kStatusTimeoutQ = 0x106,
     kStatusTimeoutDecode = 0x201,
 };

@@ -18,7 +18,12 @@
 //   Q tile 1 (TMEM lane = row = thread); warps 8 and 9 issue the tcgen05.mma
 //   of Q tile 0 and Q tile 1 (one thread each: a single issuing thread leaves
 //   the tensor core idle whenever it waits on a dependency, two keep it fed);
-//   warp 10 issues TMA loads from one thread; warp 11 idles.
+//   warp 10 issues TMA loads from one thread; warp 11 idles; warps 12-15
+//   are the epilogue warpgroup, which takes each finished O_t out of TMEM,
+//   normalises it by the row sums the softmax warpgroup handed over through
+//   shared memory, frees O_t for the next unit as soon as it is read, and
+//   writes it out with TMA stores -- so the softmax warpgroups go straight on
+//   to the next unit and the tensor core to its first PV.
 // * TMEM (512 columns): S0 | S1 | O0 | O1.  S_t = Q_t K^T accumulates in fp32;
 //   the softmax writes P_t as bf16/fp16 pairs over the first half of S_t and
 //   the PV MMA reads P_t straight from TMEM (A operand in TMEM, V from shared
@@ -49,18 +54,24 @@ using namespace sm100;
 
 constexpr int kBM = 128;  // rows per Q tile (MMA M)
 constexpr int kBN = 128;  // keys per KV tile
-// Three warpgroups: two softmax warpgroups and one for the MMA warp, the TMA
-// warp and two idle warps.  Launched at 168 registers a thread (384 x 168 =
-// 64512); the softmax warpgroups take 200 and the third gives back down to
-// 104: 256 x 200 + 128 x 104 = 64512, and per SM sub-partition
-// 2 x 200 + 104 <= 512 register slots a lane.
-constexpr int kThreads = 384;
+// Four warpgroups: two softmax warpgroups, one for the MMA warps, the TMA
+// warp and an idle warp, and the epilogue warpgroup.  Launched at 128
+// registers a thread (512 x 128 = 65536, the whole register file); the
+// softmax warpgroups take 192 and the other two give back down to 64:
+// 256 x 192 + 256 x 64 = 65536, and per SM sub-partition (one warp of each
+// warpgroup) 2 x 192 + 2 x 64 = 512 register slots a lane.
+constexpr int kThreads = 512;
 constexpr int kMmaWarp0 = 8;  // issues the MMAs of Q tile 0; owns the TMEM allocation
 constexpr int kMmaWarp1 = 9;  // issues the MMAs of Q tile 1
 constexpr int kLoadWarp = 10;
-constexpr uint32_t kRegsSoftmax = 200;
-constexpr uint32_t kRegsOther = 104;
-static_assert(256 * kRegsSoftmax + 128 * kRegsOther <= kThreads * 168, "register split");
+constexpr int kEpiWarp0 = 12;  // warps 12-15: epilogue
+constexpr uint32_t kRegsLaunch = 65536 / kThreads;
+constexpr uint32_t kRegsSoftmax = 192;
+constexpr uint32_t kRegsOther = 56;  // MMA, TMA and idle warps
+constexpr uint32_t kRegsEpi = 72;    // epilogue warpgroup
+static_assert(256 * kRegsSoftmax + 128 * (kRegsOther + kRegsEpi) <= kThreads * kRegsLaunch,
+              "register split");
+static_assert(2 * kRegsSoftmax + kRegsOther + kRegsEpi <= 512, "register split per sub-partition");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kChunkBytes = 128 * 128;       // one 128-row x 128-byte swizzled chunk
 constexpr int kPrefetchTiles = 4;                 // K/V tiles pulled into L2 ahead of use
@@ -88,13 +99,15 @@ template <int D, int DV> struct Layout {
     static constexpr int VTILE = kBN * DV * 2;
     static constexpr int STAGE = KTILE > VTILE ? KTILE : VTILE;
     static constexpr int BUDGET = 227 * 1024;  // opt-in shared memory per block
-    static constexpr int STG_BYTES = 8 * 4096;  // epilogue staging: 4 KB per softmax warp
-    static constexpr int NS_FIT = (BUDGET - 2 * QTILE - STG_BYTES - 1024 - 512) / STAGE;
+    static constexpr int STG_BYTES = kBM * 128;  // epilogue staging: 64 columns of a Q tile
+    static constexpr int STATS_BYTES = 2 * 2 * kBM * 4;  // 1 / l per row: [unit parity][tile]
+    static constexpr int NS_FIT = (BUDGET - 2 * QTILE - STG_BYTES - STATS_BYTES - 1024 - 512) / STAGE;
     static constexpr int NS = NS_FIT > 8 ? 8 : NS_FIT;
     static constexpr int Q_OFF = 0;
     static constexpr int KV_OFF = 2 * QTILE;
     static constexpr int STG_OFF = KV_OFF + NS * STAGE;
-    static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
+    static constexpr int STATS_OFF = STG_OFF + STG_BYTES;
+    static constexpr int BAR_OFF = STATS_OFF + STATS_BYTES;
     static constexpr int SMEM = 1024 + BAR_OFF + 512;  // + alignment slack
     static constexpr int O_COL = 256;                  // TMEM columns: S0 S1 | O0 O1
     static_assert(NS >= 2, "K/V ring needs two stages");
@@ -111,7 +124,12 @@ enum : int {
     B_O_EMPTY = 8,   // [2]
     B_TEARDOWN = 10,  // [2]
     B_TURN = 12,      // [2] softmax group t has issued the exps of its tile
-    B_KV_FULL = 14,   // [NS] kv_full, [NS] kv_empty, [NS] v_tail: the zeroed tail V
+    B_STATS = 14,     // [2 tiles][2 unit parities]: the 1 / l of tile t's rows are in
+                      // shared memory.  One barrier per unit parity, so that none runs
+                      // more than one phase ahead of the epilogue (a unit's stats can
+                      // only be written once the epilogue has freed O of the unit two
+                      // back)
+    B_KV_FULL = 18,   // [NS] kv_full, [NS] kv_empty, [NS] v_tail: the zeroed tail V
                       // tile of a ring slot, handed from MMA warp 0 to MMA warp 1
                       // (a slot is refilled only after both warps released it, so
                       // its v_tail barrier is never more than one phase ahead)
@@ -224,7 +242,8 @@ template <typename T, int D, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV) {
+                      const __grid_constant__ CUtensorMap tmV,
+                      const __grid_constant__ CUtensorMap tmO) {
     using L = Layout<D, DV>;
     constexpr int NS = L::NS;
     extern __shared__ uint8_t smem_raw[];
@@ -251,6 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(B_O_FULL + t), 1);
             mbar_init(bar(B_O_EMPTY + t), 128);
             mbar_init(bar(B_TURN + t), 128);
+            mbar_init(bar(B_STATS + 2 * t), 128);
+            mbar_init(bar(B_STATS + 2 * t + 1), 128);
         }
         mbar_init(bar(B_TEARDOWN), 1);
         mbar_init(bar(B_TEARDOWN + 1), 1);
@@ -270,6 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmO);
     }
     tc_fence_before();
     __syncthreads();
@@ -281,205 +303,209 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto stage = [&](int s) { return kv_smem + (uint32_t)s * L::STAGE; };
     const bool padded = p.cu_q == nullptr;
 
-    if (warp >= 8) regs_decrease<kRegsOther>();
-    if (warp == kLoadWarp) {
-        // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            uint32_t kv_it = 0, q_ph = 0;
-            int last_q_parity = -1;
-            uint32_t armed = 0, armed_parity = 0;  // per ring slot: loaded at least once, last parity
+    if (warp >= 8 && warp < kEpiWarp0) {
+        // the setmaxnreg of each role dominates that role's code, so that the
+        // compiler allocates the role's registers against its own limit
+        regs_decrease<kRegsOther>();
+        if (warp == kLoadWarp) {
+            // ------------------------------------------------------ TMA producer
+            if (lane == 0) {
+                uint32_t kv_it = 0, q_ph = 0;
+                int last_q_parity = -1;
+                uint32_t armed = 0, armed_parity = 0;  // per ring slot: loaded at least once, last parity
+                bool ok = true;
+                for (long long rnd = 0; rnd * gridDim.x < a.nunits && ok; ++rnd) {
+                    const long long u = snake_unit(rnd, blockIdx.x, gridDim.x);
+                    if (u >= a.nunits) continue;
+                    const UnitInfo x = unit_info(a, u);
+                    if (x.n_kv == 0) continue;
+                    const int qrow = (padded ? 0 : (int)x.si.q_off) + x.q0;
+                    const int krow = padded ? 0 : (int)x.si.k_off;
+                    const int bc = padded ? x.b : 0;
+                    if (!mbar_wait(bar(B_Q_EMPTY), q_ph ^ 1u, abort_flag, kWaitLimitNs)) {
+                        raise_abort(abort_flag, p.status, kStatusTimeoutQ);
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(B_Q_FULL), 2 * L::QTILE);
+                    last_q_parity = (int)q_ph;
+                    q_ph ^= 1u;
+                    for (int t = 0; t < 2; ++t)
+                        for (int c = 0; c < D / 64; ++c)
+                            tma_load_4d(q_smem + t * L::QTILE + c * kChunkBytes, &tmQ, bar(B_Q_FULL),
+                                        c * 64, x.h0, qrow + t * a.QP, bc);
+                    // L2 prefetch: the first K/V tiles of this unit and the next unit's Q
+                    auto prefetch_kv = [&](int jj) {
+                        const int kk0 = x.kv_start + jj * kBN;
+                        for (int c = 0; c < D / 64; ++c)
+                            tma_prefetch_l2_4d(&tmK, c * 64, x.kvh, krow + kk0, bc);
+                        for (int c = 0; c < DV / 64; ++c)
+                            tma_prefetch_l2_4d(&tmV, c * 64, x.kvh, krow + kk0, bc);
+                    };
+                    for (int jj = 1; jj < kPrefetchTiles && jj < x.n_kv; ++jj) prefetch_kv(jj);
+                    const long long un = snake_unit(rnd + 1, blockIdx.x, gridDim.x);
+                    if (un < a.nunits) {
+                        const UnitInfo nx = unit_info(a, un);
+                        if (nx.n_kv > 0) {
+                            const int nq = (padded ? 0 : (int)nx.si.q_off) + nx.q0;
+                            const int nbc = padded ? nx.b : 0;
+                            for (int t = 0; t < 2; ++t)
+                                for (int c = 0; c < D / 64; ++c)
+                                    tma_prefetch_l2_4d(&tmQ, c * 64, nx.h0, nq + t * a.QP, nbc);
+                        }
+                    }
+                    for (int j = 0; j < x.n_kv && ok; ++j) {
+                        const int k0 = x.kv_start + j * kBN;
+                        if (j + kPrefetchTiles < x.n_kv) prefetch_kv(j + kPrefetchTiles);
+    #pragma unroll
+                        for (int which = 0; which < 2; ++which) {
+                            const uint32_t it = kv_it++;
+                            const int s = (int)(it % NS);
+                            const uint32_t ph = (it / NS) & 1u;
+                            if (!mbar_wait(kv_empty(s), ph ^ 1u, abort_flag, kWaitLimitNs)) {
+                                raise_abort(abort_flag, p.status, kStatusTimeoutKvEmpty);
+                                ok = false;
+                                break;
+                            }
+                            if (which == 0) {
+                                mbar_arrive_expect_tx(kv_full(s), L::KTILE);
+                                for (int c = 0; c < D / 64; ++c)
+                                    tma_load_4d(stage(s) + c * kChunkBytes, &tmK, kv_full(s), c * 64,
+                                                x.kvh, krow + k0, bc);
+                            } else {
+                                mbar_arrive_expect_tx(kv_full(s), L::VTILE);
+                                for (int c = 0; c < DV / 64; ++c)
+                                    tma_load_4d(stage(s) + c * kChunkBytes, &tmV, kv_full(s), c * 64,
+                                                x.kvh, krow + k0, bc);
+                            }
+                            armed |= 1u << s;
+                            armed_parity = (armed_parity & ~(1u << s)) | (ph << s);
+                        }
+                    }
+                }
+                // Drain: every copy this thread issued has landed before the CTA exits.
+                if (last_q_parity >= 0)
+                    mbar_wait(bar(B_Q_FULL), (uint32_t)last_q_parity, abort_flag, kWaitLimitNs);
+                for (int s = 0; s < NS; ++s)
+                    if (armed & (1u << s))
+                        mbar_wait(kv_full(s), (armed_parity >> s) & 1u, abort_flag, kWaitLimitNs);
+            }
+        } else if (warp == kMmaWarp0 || warp == kMmaWarp1) {
+            // -------------------------------------- MMA issuers, one per Q tile
+            // Each warp runs the chain S_t(j) -> [softmax_t] -> PV_t(j) -> S_t(j+1)
+            // of its own tile; two issuing warps keep the tensor core fed while
+            // either one waits.  P_t aliases S_t in TMEM, so S_t(j+1) is issued
+            // after PV_t(j) by the same thread (tcgen05.mma executes in order).
+            const int t = warp - kMmaWarp0;
+            uint32_t kv_it = 0, q_ph = 0, p_ph = 0, oe_ph = 0;
+            uint32_t vt_ph = 0;  // per ring slot: parity of its next v_tail phase (bit s)
             bool ok = true;
+            const uint32_t s_tm = tmem + (uint32_t)t * 128u;
+            const uint32_t o_tm = tmem + (uint32_t)(L::O_COL + t * DV);
+            const uint64_t qd = sw128_desc(q_smem + t * L::QTILE, 16, 1024);
             for (long long rnd = 0; rnd * gridDim.x < a.nunits && ok; ++rnd) {
                 const long long u = snake_unit(rnd, blockIdx.x, gridDim.x);
                 if (u >= a.nunits) continue;
                 const UnitInfo x = unit_info(a, u);
                 if (x.n_kv == 0) continue;
-                const int qrow = (padded ? 0 : (int)x.si.q_off) + x.q0;
-                const int krow = padded ? 0 : (int)x.si.k_off;
-                const int bc = padded ? x.b : 0;
-                if (!mbar_wait(bar(B_Q_EMPTY), q_ph ^ 1u, abort_flag, kWaitLimitNs)) {
-                    raise_abort(abort_flag, p.status, kStatusTimeoutQ);
+                if (!warp_wait(bar(B_Q_FULL), q_ph, abort_flag)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(bar(B_Q_FULL), 2 * L::QTILE);
-                last_q_parity = (int)q_ph;
                 q_ph ^= 1u;
-                for (int t = 0; t < 2; ++t)
-                    for (int c = 0; c < D / 64; ++c)
-                        tma_load_4d(q_smem + t * L::QTILE + c * kChunkBytes, &tmQ, bar(B_Q_FULL),
-                                    c * 64, x.h0, qrow + t * a.QP, bc);
-                // L2 prefetch: the first K/V tiles of this unit and the next unit's Q
-                auto prefetch_kv = [&](int jj) {
-                    const int kk0 = x.kv_start + jj * kBN;
-                    for (int c = 0; c < D / 64; ++c)
-                        tma_prefetch_l2_4d(&tmK, c * 64, x.kvh, krow + kk0, bc);
-                    for (int c = 0; c < DV / 64; ++c)
-                        tma_prefetch_l2_4d(&tmV, c * 64, x.kvh, krow + kk0, bc);
-                };
-                for (int jj = 1; jj < kPrefetchTiles && jj < x.n_kv; ++jj) prefetch_kv(jj);
-                const long long un = snake_unit(rnd + 1, blockIdx.x, gridDim.x);
-                if (un < a.nunits) {
-                    const UnitInfo nx = unit_info(a, un);
-                    if (nx.n_kv > 0) {
-                        const int nq = (padded ? 0 : (int)nx.si.q_off) + nx.q0;
-                        const int nbc = padded ? nx.b : 0;
-                        for (int t = 0; t < 2; ++t)
-                            for (int c = 0; c < D / 64; ++c)
-                                tma_prefetch_l2_4d(&tmQ, c * 64, nx.h0, nq + t * a.QP, nbc);
+                const uint32_t kb = kv_it;
+
+                // O_t (+)= P_t V_jj, then release V_jj
+                auto issue_pv = [&](int jj) -> bool {
+                    if (!warp_wait(bar(B_P_READY + t), p_ph, abort_flag)) return false;
+                    p_ph ^= 1u;
+                    if (jj == 0) {  // the previous unit's epilogue has read O_t
+                        if (!warp_wait(bar(B_O_EMPTY + t), oe_ph ^ 1u, abort_flag)) return false;
+                        oe_ph ^= 1u;
                     }
-                }
-                for (int j = 0; j < x.n_kv && ok; ++j) {
-                    const int k0 = x.kv_start + j * kBN;
-                    if (j + kPrefetchTiles < x.n_kv) prefetch_kv(j + kPrefetchTiles);
-#pragma unroll
-                    for (int which = 0; which < 2; ++which) {
-                        const uint32_t it = kv_it++;
-                        const int s = (int)(it % NS);
-                        const uint32_t ph = (it / NS) & 1u;
-                        if (!mbar_wait(kv_empty(s), ph ^ 1u, abort_flag, kWaitLimitNs)) {
-                            raise_abort(abort_flag, p.status, kStatusTimeoutKvEmpty);
-                            ok = false;
-                            break;
-                        }
-                        if (which == 0) {
-                            mbar_arrive_expect_tx(kv_full(s), L::KTILE);
-                            for (int c = 0; c < D / 64; ++c)
-                                tma_load_4d(stage(s) + c * kChunkBytes, &tmK, kv_full(s), c * 64,
-                                            x.kvh, krow + k0, bc);
+                    const uint32_t it = kb + 2u * (uint32_t)jj + 1u;
+                    const int vslot = (int)(it % NS);
+                    const int k0 = x.kv_start + jj * kBN;
+                    const int nzero = k0 + kBN - x.hi_unit;  // rows past the last key in use
+                    if (t == 0 || nzero <= 0) {
+                        if (!warp_wait(kv_full(vslot), (it / NS) & 1u, abort_flag)) return false;
+                    }
+                    if (nzero > 0) {
+                        if (t == 0) {
+                            // those rows may hold anything (NaN included): zero them so
+                            // that 0 * V stays 0, then hand the tile to the other warp
+                            uint8_t *vt = gbase + (stage(vslot) - base);
+                            for (int i = lane; i < nzero * 8 * (DV / 64); i += 32) {
+                                const int c = i / (nzero * 8), rem = i % (nzero * 8);
+                                const int row = kBN - nzero + rem / 8;
+                                *reinterpret_cast<uint4 *>(vt + c * kChunkBytes + row * 128 +
+                                                           (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+                            }
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(v_tail(vslot));
                         } else {
-                            mbar_arrive_expect_tx(kv_full(s), L::VTILE);
-                            for (int c = 0; c < DV / 64; ++c)
-                                tma_load_4d(stage(s) + c * kChunkBytes, &tmV, kv_full(s), c * 64,
-                                            x.kvh, krow + k0, bc);
+                            if (!warp_wait(v_tail(vslot), (vt_ph >> vslot) & 1u, abort_flag))
+                                return false;
+                            vt_ph ^= 1u << vslot;
                         }
-                        armed |= 1u << s;
-                        armed_parity = (armed_parity & ~(1u << s)) | (ph << s);
                     }
-                }
-            }
-            // Drain: every copy this thread issued has landed before the CTA exits.
-            if (last_q_parity >= 0)
-                mbar_wait(bar(B_Q_FULL), (uint32_t)last_q_parity, abort_flag, kWaitLimitNs);
-            for (int s = 0; s < NS; ++s)
-                if (armed & (1u << s))
-                    mbar_wait(kv_full(s), (armed_parity >> s) & 1u, abort_flag, kWaitLimitNs);
-        }
-    } else if (warp == kMmaWarp0 || warp == kMmaWarp1) {
-        // -------------------------------------- MMA issuers, one per Q tile
-        // Each warp runs the chain S_t(j) -> [softmax_t] -> PV_t(j) -> S_t(j+1)
-        // of its own tile; two issuing warps keep the tensor core fed while
-        // either one waits.  P_t aliases S_t in TMEM, so S_t(j+1) is issued
-        // after PV_t(j) by the same thread (tcgen05.mma executes in order).
-        const int t = warp - kMmaWarp0;
-        uint32_t kv_it = 0, q_ph = 0, p_ph = 0, oe_ph = 0;
-        uint32_t vt_ph = 0;  // per ring slot: parity of its next v_tail phase (bit s)
-        bool ok = true;
-        const uint32_t s_tm = tmem + (uint32_t)t * 128u;
-        const uint32_t o_tm = tmem + (uint32_t)(L::O_COL + t * DV);
-        const uint64_t qd = sw128_desc(q_smem + t * L::QTILE, 16, 1024);
-        for (long long rnd = 0; rnd * gridDim.x < a.nunits && ok; ++rnd) {
-            const long long u = snake_unit(rnd, blockIdx.x, gridDim.x);
-            if (u >= a.nunits) continue;
-            const UnitInfo x = unit_info(a, u);
-            if (x.n_kv == 0) continue;
-            if (!warp_wait(bar(B_Q_FULL), q_ph, abort_flag)) {
-                ok = false;
-                break;
-            }
-            q_ph ^= 1u;
-            const uint32_t kb = kv_it;
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint64_t vd = sw128_desc(stage(vslot), kChunkBytes, 1024);
+    #pragma unroll
+                        for (int kk = 0; kk < kBN / 16; ++kk)
+                            mma_ts(o_tm, s_tm + kk * 8, vd + (kk * 2048 >> 4), a.idesc_o,
+                                   (jj > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(kv_empty(vslot));
+                    }
+                    __syncwarp();
+                    return true;
+                };
 
-            // O_t (+)= P_t V_jj, then release V_jj
-            auto issue_pv = [&](int jj) -> bool {
-                if (!warp_wait(bar(B_P_READY + t), p_ph, abort_flag)) return false;
-                p_ph ^= 1u;
-                if (jj == 0) {  // the previous unit's epilogue has read O_t
-                    if (!warp_wait(bar(B_O_EMPTY + t), oe_ph ^ 1u, abort_flag)) return false;
-                    oe_ph ^= 1u;
-                }
-                const uint32_t it = kb + 2u * (uint32_t)jj + 1u;
-                const int vslot = (int)(it % NS);
-                const int k0 = x.kv_start + jj * kBN;
-                const int nzero = k0 + kBN - x.hi_unit;  // rows past the last key in use
-                if (t == 0 || nzero <= 0) {
-                    if (!warp_wait(kv_full(vslot), (it / NS) & 1u, abort_flag)) return false;
-                }
-                if (nzero > 0) {
-                    if (t == 0) {
-                        // those rows may hold anything (NaN included): zero them so
-                        // that 0 * V stays 0, then hand the tile to the other warp
-                        uint8_t *vt = gbase + (stage(vslot) - base);
-                        for (int i = lane; i < nzero * 8 * (DV / 64); i += 32) {
-                            const int c = i / (nzero * 8), rem = i % (nzero * 8);
-                            const int row = kBN - nzero + rem / 8;
-                            *reinterpret_cast<uint4 *>(vt + c * kChunkBytes + row * 128 +
-                                                       (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+                for (int j = 0; j < x.n_kv && ok; ++j) {
+                    if (j > 0 && !issue_pv(j - 1)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t it = kb + 2u * (uint32_t)j;
+                    const int kslot = (int)(it % NS);
+                    if (!warp_wait(kv_full(kslot), (it / NS) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (lane == 0) {
+                        // the start-address field is the low 14 bits (address >> 4)
+                        const uint64_t kd = sw128_desc(stage(kslot), 16, 1024);
+    #pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = ((kk / 4) * kChunkBytes + (kk % 4) * 32) >> 4;
+                            mma_ss(s_tm, qd + off, kd + off, a.idesc_s, kk > 0);
                         }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(v_tail(vslot));
-                    } else {
-                        if (!warp_wait(v_tail(vslot), (vt_ph >> vslot) & 1u, abort_flag))
-                            return false;
-                        vt_ph ^= 1u << vslot;
+                        mma_commit(bar(B_S_FULL + t));
+                        mma_commit(kv_empty(kslot));
+                        if (j == x.n_kv - 1) mma_commit(bar(B_Q_EMPTY));
                     }
+                    __syncwarp();
                 }
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint64_t vd = sw128_desc(stage(vslot), kChunkBytes, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk)
-                        mma_ts(o_tm, s_tm + kk * 8, vd + (kk * 2048 >> 4), a.idesc_o,
-                               (jj > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(kv_empty(vslot));
-                }
-                __syncwarp();
-                return true;
-            };
-
-            for (int j = 0; j < x.n_kv && ok; ++j) {
-                if (j > 0 && !issue_pv(j - 1)) {
+                if (!ok) break;
+                if (!issue_pv(x.n_kv - 1)) {
                     ok = false;
                     break;
                 }
-                const uint32_t it = kb + 2u * (uint32_t)j;
-                const int kslot = (int)(it % NS);
-                if (!warp_wait(kv_full(kslot), (it / NS) & 1u, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (lane == 0) {
-                    // the start-address field is the low 14 bits (address >> 4)
-                    const uint64_t kd = sw128_desc(stage(kslot), 16, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = ((kk / 4) * kChunkBytes + (kk % 4) * 32) >> 4;
-                        mma_ss(s_tm, qd + off, kd + off, a.idesc_s, kk > 0);
-                    }
-                    mma_commit(bar(B_S_FULL + t));
-                    mma_commit(kv_empty(kslot));
-                    if (j == x.n_kv - 1) mma_commit(bar(B_Q_EMPTY));
-                }
+                if (lane == 0) mma_commit(bar(B_O_FULL + t));
                 __syncwarp();
+                kv_it += 2u * (uint32_t)x.n_kv;
             }
-            if (!ok) break;
-            if (!issue_pv(x.n_kv - 1)) {
-                ok = false;
-                break;
+            if (!ok && lane == 0) raise_abort(abort_flag, p.status, kStatusTimeoutMma);
+            // all MMAs issued by this warp complete before TMEM is released
+            if (lane == 0) {
+                mma_commit(bar(B_TEARDOWN + t));
+                mbar_wait(bar(B_TEARDOWN + t), 0, abort_flag, kWaitLimitNs);
             }
-            if (lane == 0) mma_commit(bar(B_O_FULL + t));
             __syncwarp();
-            kv_it += 2u * (uint32_t)x.n_kv;
         }
-        if (!ok && lane == 0) raise_abort(abort_flag, p.status, kStatusTimeoutMma);
-        // all MMAs issued by this warp complete before TMEM is released
-        if (lane == 0) {
-            mma_commit(bar(B_TEARDOWN + t));
-            mbar_wait(bar(B_TEARDOWN + t), 0, abort_flag, kWaitLimitNs);
-        }
-        __syncwarp();
     } else if (warp < 8) {
         // ------------------------------------------------- softmax warpgroups
         regs_increase<kRegsSoftmax>();
@@ -490,10 +516,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tS = tmem + lane_off + (uint32_t)(t * 128);
         const uint32_t tO = tmem + lane_off + (uint32_t)(L::O_COL + t * DV);
         const float c = a.c_scale;
-        uint32_t s_ph = 0, o_ph = 0;
+        uint32_t s_ph = 0;
         uint32_t ntile = 0;  // tiles this warpgroup has processed (all units)
+        uint32_t nunit = 0;  // units with keys this warpgroup has processed
         bool ok = true;
         T *og = static_cast<T *>(p.o);
+        float *inv_l = reinterpret_cast<float *>(gbase + L::STATS_OFF);
 
         for (long long rnd = 0; rnd * gridDim.x < a.nunits && ok; ++rnd) {
             const long long u = snake_unit(rnd, blockIdx.x, gridDim.x);
@@ -638,61 +666,116 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
 
-            // epilogue: O / l, LSE
-            if (!warp_wait(bar(B_O_FULL + t), o_ph, abort_flag)) {
-                ok = false;
-                break;
-            }
-            o_ph ^= 1u;
-            tc_fence_after();
+            // LSE here; 1 / l (0 for a row without keys) to the epilogue warpgroup
             const bool has = valid && l_run > 0.f;
-            const float inv = has ? 1.f / l_run : 0.f;
-            // O rows go out through a per-warp staging area so that every store
-            // instruction writes four 128-byte row segments instead of 32
-            // scattered 16-byte pieces.  Staging rows hold 64 columns (128 B);
-            // their 16-byte chunks are XOR-swizzled by the row's low 3 bits.
-            const uint32_t wmask = __ballot_sync(0xffffffffu, writes);
-            uint8_t *stg = gbase + L::STG_OFF + warp * 4096;
-#pragma unroll
-            for (int cp = 0; cp < DV / 64; ++cp) {
-                uint32_t pkd[32];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t ov[32];
-                    tmem_ld32(tO + cp * 64 + h * 32, ov);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float o0 = has ? __uint_as_float(ov[2 * i]) * inv : 0.f;
-                        const float o1 = has ? __uint_as_float(ov[2 * i + 1]) * inv : 0.f;
-                        pkd[h * 16 + i] = pack2<T>(o0, o1);
-                    }
-                }
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<uint4 *>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
-                        make_uint4(pkd[4 * c], pkd[4 * c + 1], pkd[4 * c + 2], pkd[4 * c + 3]);
-                __syncwarp();
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int e = i * 32 + lane;      // 16-byte piece of the warp's 32 x 128 B
-                    const int row = e >> 3, c = e & 7;  // row of this warp, chunk within it
-                    const uint4 v =
-                        *reinterpret_cast<const uint4 *>(stg + row * 128 + ((c ^ (row & 7)) << 4));
-                    if ((wmask >> row) & 1u) {
-                        const int rr = quarter * 32 + row;
-                        const int qp = x.q0 + t * a.QP + rr / a.Gp;
-                        const long long orr = (x.si.q_off + qp) * p.Hq + x.h0 + rr % a.Gp;
-                        *reinterpret_cast<uint4 *>(og + orr * DV + cp * 64 + c * 8) = v;
-                    }
-                }
-                __syncwarp();
-            }
             if (writes && p.lse) p.lse[orow] = has ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
-            tc_fence_before();
-            mbar_arrive(bar(B_O_EMPTY + t));
+            inv_l[(nunit & 1u) * 2 * kBM + t * kBM + r] = has ? 1.f / l_run : 0.f;
+            mbar_arrive(bar(B_STATS + 2 * t + (int)(nunit & 1u)));
+            ++nunit;
         }
         if (!ok && lane == 0) raise_abort(abort_flag, p.status, kStatusTimeoutSoftmax);
+    } else {
+        // ------------------------------------------------ epilogue warpgroup
+        // Per unit, tile 0 then tile 1: wait for O_t and the rows' 1 / l, read
+        // O_t out of TMEM 64 columns at a time into a staging tile (the TMA
+        // box layout: 128 rows of 128 bytes, 16-byte chunks XOR-swizzled by the
+        // row's low 3 bits), free O_t once the last columns are read, and store
+        // each staged box with one TMA store.  The next unit's first PV into
+        // O_t waits only for the TMEM reads.  A tile whose rows run into the
+        // next sequence of a packed batch goes out row by row instead.
+        regs_decrease<kRegsEpi>();
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;  // row of the tile = TMEM lane
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const bool leader = warp == kEpiWarp0 && lane == 0;  // issues the TMA stores
+        uint32_t o_ph = 0;   // bit t: parity of O_t's next phase
+        uint32_t st_ph = 0;  // bit 2t+b: parity of stats barrier (t, b)
+        uint32_t nunit = 0;
+        bool ok = true;
+        T *og = static_cast<T *>(p.o);
+        const float *inv_l = reinterpret_cast<const float *>(gbase + L::STATS_OFF);
+        uint8_t *stg = gbase + L::STG_OFF;
+        const uint32_t stg_s = base + L::STG_OFF;
+
+        for (long long rnd = 0; rnd * gridDim.x < a.nunits && ok; ++rnd) {
+            const long long u = snake_unit(rnd, blockIdx.x, gridDim.x);
+            if (u >= a.nunits) continue;
+            const UnitInfo x = unit_info(a, u);
+            if (x.n_kv == 0) continue;  // the softmax warpgroups wrote those rows
+            const int b = (int)(nunit & 1u);
+            ++nunit;
+            for (int t = 0; t < 2; ++t) {
+                const int sb = 2 * t + b;
+                if (!warp_wait(bar(B_O_FULL + t), (o_ph >> t) & 1u, abort_flag) ||
+                    !warp_wait(bar(B_STATS + sb), (st_ph >> sb) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                o_ph ^= 1u << t;
+                st_ph ^= 1u << sb;
+                tc_fence_after();
+                const float inv = inv_l[b * 2 * kBM + t * kBM + r];
+                const int qt0 = x.q0 + t * a.QP;  // first query position of the tile
+                // padded rows past Q fall outside the tensor map and are dropped
+                // by the TMA store; rows in [Qb, Q) are written as zeros
+                const bool by_tma = padded || qt0 + a.QP <= x.si.Qb;
+                const uint32_t tO = tmem + lane_off + (uint32_t)(L::O_COL + t * DV);
+#pragma unroll
+                for (int cp = 0; cp < DV / 64; ++cp) {
+                    if (leader) bulk_wait_read0();  // the staging tile is free again
+                    named_bar_sync(1, 128);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t ov[32];
+                        tmem_ld32(tO + cp * 64 + h * 32, ov);
+                        tmem_ld_wait();
+                        if (cp == DV / 64 - 1 && h == 1) {  // O_t is read: free it
+                            tc_fence_before();
+                            mbar_arrive(bar(B_O_EMPTY + t));
+                        }
+#pragma unroll
+                        for (int c4 = 0; c4 < 4; ++c4) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int e = 8 * c4 + 2 * i;
+                                w[i] = pack2<T>(inv > 0.f ? __uint_as_float(ov[e]) * inv : 0.f,
+                                                inv > 0.f ? __uint_as_float(ov[e + 1]) * inv : 0.f);
+                            }
+                            const int ch = 4 * h + c4;
+                            *reinterpret_cast<uint4 *>(stg + r * 128 + ((ch ^ (r & 7)) << 4)) =
+                                make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                    if (by_tma) {
+                        fence_proxy_async_smem();
+                        named_bar_sync(1, 128);
+                        if (leader) {
+                            const int qrow = (padded ? 0 : (int)x.si.q_off) + qt0;
+                            tma_store_4d(&tmO, stg_s, cp * 64, x.h0, qrow, padded ? x.b : 0);
+                            bulk_commit();
+                        }
+                    } else {
+                        // this warp's 32 rows, 16 bytes a lane per step
+                        __syncwarp();
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int e = i * 32 + lane;
+                            const int rr = quarter * 32 + (e >> 3), ch = e & 7;
+                            const int qp = qt0 + rr / a.Gp;
+                            if (qp < x.si.Qb) {
+                                const uint4 v = *reinterpret_cast<const uint4 *>(
+                                    stg + rr * 128 + ((ch ^ (rr & 7)) << 4));
+                                const long long orr = (x.si.q_off + qp) * p.Hq + x.h0 + rr % a.Gp;
+                                *reinterpret_cast<uint4 *>(og + orr * DV + cp * 64 + ch * 8) = v;
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        if (leader) bulk_wait0();
+        if (!ok && lane == 0) raise_abort(abort_flag, p.status, kStatusTimeoutEpilogue);
     }
 
     tc_fence_before();
@@ -769,8 +852,10 @@ int launch_t(const AttnParams &p, bool bf16, cudaStream_t stream) {
     const uint64_t qrows = padded ? (uint64_t)p.Q : (uint64_t)p.Tq;
     const uint64_t krows = padded ? (uint64_t)p.K : (uint64_t)p.Tk;
     const uint64_t nb = padded ? (uint64_t)p.B : 1;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     int rc = make_map(&tq, p.q, dt, D, p.Hq, qrows, nb, a.Gp, a.QP);
+    if (rc) return rc;
+    rc = make_map(&to, p.o, dt, DV, p.Hq, qrows, nb, a.Gp, a.QP);
     if (rc) return rc;
     if (krows > 0) {
         rc = make_map(&tk, p.k, dt, D, p.Hkv, krows, nb, 1, kBN);
@@ -792,7 +877,7 @@ int launch_t(const AttnParams &p, bool bf16, cudaStream_t stream) {
     cudaGetDevice(&dev);
     const int nsm = sm_count(dev);
     const long long grid = a.nunits < nsm ? a.nunits : nsm;
-    kern<<<(unsigned)grid, kThreads, L::SMEM, stream>>>(a, tq, tk, tv);
+    kern<<<(unsigned)grid, kThreads, L::SMEM, stream>>>(a, tq, tk, tv, to);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("prefill kernel launch: %s", cudaGetErrorString(e));
