@@ -42,6 +42,7 @@
 #include <cudaTypedefs.h>
 
 #include <climits>
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
@@ -87,7 +88,9 @@ struct PrefillArgs {
     int QP;            // query positions per Q tile (kBM / Gp)
     int nsub;          // head subgroups per KV head (G / Gp)
     int nqblk;         // query blocks (2 * QP positions) per sequence
-    long long nunits;
+    uint32_t per;      // units per query block: B * Hkv * nsub
+    uint32_t hs;       // Hkv * nsub
+    long long nunits;  // < 2^31
     float c_scale;     // |scale| * log2(e)  (> 0)
     uint32_t idesc_s;  // S = Q K^T
     uint32_t idesc_o;  // O += P V
@@ -145,15 +148,18 @@ struct UnitInfo {
     bool all_valid;      // every row of both tiles holds a real query
 };
 
-__device__ __forceinline__ UnitInfo unit_info(const PrefillArgs &a, long long u) {
+__device__ __forceinline__ UnitInfo unit_info(const PrefillArgs &a, long long u64) {
     const AttnParams &p = a.p;
-    const long long per = (long long)p.B * p.Hkv * a.nsub;
-    const int qblk = a.nqblk - 1 - (int)(u / per);
-    const int rest = (int)(u % per);
+    // 32-bit index arithmetic (the unit count is below 2^31)
+    const uint32_t u = (uint32_t)u64;
+    const uint32_t qi = u / a.per, rest = u - qi * a.per;
+    const uint32_t b = rest / a.hs, r2 = rest - b * a.hs;
+    const uint32_t kvh = r2 / (uint32_t)a.nsub, sub = r2 - kvh * (uint32_t)a.nsub;
+    const int qblk = a.nqblk - 1 - (int)qi;
     UnitInfo x;
-    x.b = rest / (p.Hkv * a.nsub);
-    x.kvh = (rest / a.nsub) % p.Hkv;
-    x.h0 = x.kvh * p.G + (rest % a.nsub) * a.Gp;
+    x.b = (int)b;
+    x.kvh = (int)kvh;
+    x.h0 = x.kvh * p.G + (int)sub * a.Gp;
     x.q0 = qblk * 2 * a.QP;
     x.si = seq_info(p, x.b);
     x.n_kv = 0;
@@ -257,6 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + L::BAR_OFF + 8 * (B_KV_FULL + 3 * NS));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    // per Q load, for the MMA warps: {KV tiles, first key, end of keys in use}
+    // of the unit (two slots by load parity; KV tiles 0 = no more units)
+    int *unit_desc = reinterpret_cast<int *>(tmem_slot + 2);
 
     const AttnParams &p = a.p;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -327,6 +336,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
+                    int *d = unit_desc + q_ph * 4;  // slot by the parity of this Q_FULL phase
+                    d[0] = x.n_kv;
+                    d[1] = x.kv_start;
+                    d[2] = x.hi_unit;
                     mbar_arrive_expect_tx(bar(B_Q_FULL), 2 * L::QTILE);
                     last_q_parity = (int)q_ph;
                     q_ph ^= 1u;
@@ -357,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < x.n_kv && ok; ++j) {
                         const int k0 = x.kv_start + j * kBN;
                         if (j + kPrefetchTiles < x.n_kv) prefetch_kv(j + kPrefetchTiles);
-    #pragma unroll
+#pragma unroll
                         for (int which = 0; which < 2; ++which) {
                             const uint32_t it = kv_it++;
                             const int s = (int)(it % NS);
@@ -383,6 +396,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
+                // End marker for the MMA warps, once the last Q tile has been
+                // consumed (so no Q load is left in flight either).
+                if (ok) {
+                    if (mbar_wait(bar(B_Q_EMPTY), q_ph ^ 1u, abort_flag, kWaitLimitNs)) {
+                        unit_desc[q_ph * 4] = 0;
+                        mbar_arrive(bar(B_Q_FULL));
+                        last_q_parity = -1;
+                    } else {
+                        raise_abort(abort_flag, p.status, kStatusTimeoutQ);
+                    }
+                }
                 // Drain: every copy this thread issued has landed before the CTA exits.
                 if (last_q_parity >= 0)
                     mbar_wait(bar(B_Q_FULL), (uint32_t)last_q_parity, abort_flag, kWaitLimitNs);
@@ -403,16 +427,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t s_tm = tmem + (uint32_t)t * 128u;
             const uint32_t o_tm = tmem + (uint32_t)(L::O_COL + t * DV);
             const uint64_t qd = sw128_desc(q_smem + t * L::QTILE, 16, 1024);
-            for (long long rnd = 0; rnd * gridDim.x < a.nunits && ok; ++rnd) {
-                const long long u = snake_unit(rnd, blockIdx.x, gridDim.x);
-                if (u >= a.nunits) continue;
-                const UnitInfo x = unit_info(a, u);
-                if (x.n_kv == 0) continue;
+            // The units come from the TMA warp with each Q tile: no index
+            // arithmetic on this warp's path from one unit to the next.
+            while (ok) {
                 if (!warp_wait(bar(B_Q_FULL), q_ph, abort_flag)) {
                     ok = false;
                     break;
                 }
+                const volatile int *d = unit_desc + q_ph * 4;
                 q_ph ^= 1u;
+                struct {
+                    int n_kv, kv_start, hi_unit;
+                } x;
+                x.n_kv = d[0];
+                x.kv_start = d[1];
+                x.hi_unit = d[2];
+                if (x.n_kv == 0) break;  // end marker
                 const uint32_t kb = kv_it;
 
                 // O_t (+)= P_t V_jj, then release V_jj
@@ -425,22 +455,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint32_t it = kb + 2u * (uint32_t)jj + 1u;
                     const int vslot = (int)(it % NS);
-                    const int k0 = x.kv_start + jj * kBN;
-                    const int nzero = k0 + kBN - x.hi_unit;  // rows past the last key in use
-                    if (t == 0 || nzero <= 0) {
+                    // Keys past the last one any row of the unit uses (only in the
+                    // last tile) are left out 16 at a time; the V rows of the
+                    // last 16-key step that lie past it may hold anything (NaN
+                    // included), so they are zeroed to keep 0 * V at 0.
+                    const int nvalid = min(kBN, x.hi_unit - (x.kv_start + jj * kBN));
+                    const int ksteps = (nvalid + 15) / 16;
+                    const int nzero = ksteps * 16 - nvalid;
+                    if (t == 0 || nzero == 0) {
                         if (!warp_wait(kv_full(vslot), (it / NS) & 1u, abort_flag)) return false;
                     }
                     if (nzero > 0) {
                         if (t == 0) {
-                            // those rows may hold anything (NaN included): zero them so
-                            // that 0 * V stays 0, then hand the tile to the other warp
-                            uint8_t *vt = gbase + (stage(vslot) - base);
-                            for (int i = lane; i < nzero * 8 * (DV / 64); i += 32) {
-                                const int c = i / (nzero * 8), rem = i % (nzero * 8);
-                                const int row = kBN - nzero + rem / 8;
-                                *reinterpret_cast<uint4 *>(vt + c * kChunkBytes + row * 128 +
-                                                           (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
-                            }
+                            // zero the rows (whole 128-byte rows: the swizzle does not
+                            // matter), then hand the tile to the other MMA warp
+                            uint8_t *vt = gbase + (stage(vslot) - base) + nvalid * 128;
+#pragma unroll
+                            for (int c = 0; c < DV / 64; ++c)
+                                for (int i = lane; i < nzero * 8; i += 32)
+                                    *reinterpret_cast<uint4 *>(vt + c * kChunkBytes + i * 16) =
+                                        make_uint4(0, 0, 0, 0);
                             fence_proxy_async_smem();
                             __syncwarp();
                             if (lane == 0) mbar_arrive(v_tail(vslot));
@@ -453,10 +487,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     if (lane == 0) {
                         const uint64_t vd = sw128_desc(stage(vslot), kChunkBytes, 1024);
-    #pragma unroll
+                        // unrolled with a guard: a loop with a run-time trip count
+                        // issues markedly slower
+#pragma unroll
                         for (int kk = 0; kk < kBN / 16; ++kk)
-                            mma_ts(o_tm, s_tm + kk * 8, vd + (kk * 2048 >> 4), a.idesc_o,
-                                   (jj > 0 || kk > 0) ? 1u : 0u);
+                            if (kk < ksteps)
+                                mma_ts(o_tm, s_tm + kk * 8, vd + (kk * 2048 >> 4), a.idesc_o,
+                                       (jj > 0 || kk > 0) ? 1u : 0u);
                         mma_commit(kv_empty(vslot));
                     }
                     __syncwarp();
@@ -478,10 +515,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) {
                         // the start-address field is the low 14 bits (address >> 4)
                         const uint64_t kd = sw128_desc(stage(kslot), 16, 1024);
-    #pragma unroll
+                        // the last tile computes only the key columns in use (rounded
+                        // up to 16); the softmax masks the stale columns past them
+                        const int nvalid = min(kBN, x.hi_unit - (x.kv_start + j * kBN));
+                        const uint32_t ncols = (uint32_t)((nvalid + 15) & ~15);
+                        const uint32_t idesc =
+                            (a.idesc_s & ~(0x3Fu << 17)) | ((ncols >> 3) << 17);
+#pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = ((kk / 4) * kChunkBytes + (kk % 4) * 32) >> 4;
-                            mma_ss(s_tm, qd + off, kd + off, a.idesc_s, kk > 0);
+                            mma_ss(s_tm, qd + off, kd + off, idesc, kk > 0);
                         }
                         mma_commit(bar(B_S_FULL + t));
                         mma_commit(kv_empty(kslot));
@@ -546,7 +589,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 
             float m_run = -INFINITY, l_run = 0.f;
-            for (int j = 0; j < x.n_kv; ++j) {
+            // One KV tile of this warpgroup's softmax.  Two copies are compiled:
+            // with the key mask (the tiles that cross the causal diagonal, the
+            // window edge or the end of the keys) and without it (all others),
+            // so that the common path carries no masking code.
+            auto tile_step = [&](int j, auto masked) -> bool {
                 // The two warpgroups take turns (tile k of group 0, tile k of
                 // group 1, tile k+1 of group 0, ...): while one runs its softmax
                 // the tensor core works on the other's tile.  Left free, the two
@@ -563,32 +610,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++ntile;
                     return w;
                 };
-                if ((kTurnMode == 1 || kTurnMode == 3) && !take_turn()) {
-                    ok = false;
-                    break;
-                }
-                if (!warp_wait(bar(B_S_FULL + t), s_ph, abort_flag)) {
-                    ok = false;
-                    break;
-                }
+                if ((kTurnMode == 1 || kTurnMode == 3) && !take_turn()) return false;
+                if (!warp_wait(bar(B_S_FULL + t), s_ph, abort_flag)) return false;
                 s_ph ^= 1u;
                 tc_fence_after();
                 uint32_t sr[4][32];
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
                 tmem_ld_wait();
-                const int k0 = x.kv_start + j * kBN;
-                const bool interior = x.all_valid && k0 >= x.lo_last && k0 + kBN <= x.hi_first;
-                if (!interior) {
-                    // keys outside [lo, hi) -> -inf (also replaces NaN from padding)
-                    const int lo_rel = lo - k0, hi_rel = hi - k0;
+                if constexpr (decltype(masked)::value) {
+                    // keys outside [lo, hi) -> -inf (also replaces NaN from padding).
+                    // Per 32-key chunk: the row's legal keys as a bit mask; a chunk
+                    // that every row of the warp keeps whole is left alone.
+                    const int k0 = x.kv_start + j * kBN;
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc)
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int a0 = min(max(lo - k0 - cc * 32, 0), 32);
+                        const int b0 = min(max(hi - k0 - cc * 32, 0), 32);
+                        const uint32_t below_b = b0 >= 32 ? 0xffffffffu : (1u << b0) - 1u;
+                        const uint32_t below_a = a0 >= 32 ? 0xffffffffu : (1u << a0) - 1u;
+                        const uint32_t keep = below_b & ~below_a;
+                        if (__all_sync(0xffffffffu, keep == 0xffffffffu)) continue;
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int kr = cc * 32 + i;
-                            if (kr < lo_rel || kr >= hi_rel) sr[cc][i] = __float_as_uint(-INFINITY);
-                        }
+                        for (int i = 0; i < 32; ++i)
+                            if (!((keep >> i) & 1u)) sr[cc][i] = __float_as_uint(-INFINITY);
+                    }
                 }
                 // row max: eight independent chains of 3-input max
                 float mc[8];
@@ -613,10 +659,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     rescale = true;
                 }
                 const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
-                if (kTurnMode == 2 && !take_turn()) {
-                    ok = false;
-                    break;
+                if (__any_sync(0xffffffffu, rescale)) {
+                    // O_t holds every PV up to tile j-1 (the commit that signalled
+                    // S_t(j) was issued after them) and none of tile j yet
+#pragma unroll
+                    for (int cc = 0; cc < DV / 16; ++cc) {
+                        uint32_t ov[16];
+                        tmem_ld16(tO + cc * 16, ov);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                        tmem_st16(tO + cc * 16, ov);
+                    }
                 }
+                if (kTurnMode == 2 && !take_turn()) return false;
                 // p = 2^(s*c - m) two keys at a time: one packed FMA, two MUFU
                 // exps, one packed add into the row sum, one pack to P
                 const uint64_t c2 = f2pack(c, c), nm2 = f2pack(neg_m, neg_m);
@@ -646,23 +703,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 4; ++i) f2unpack(acc2[i], sa[2 * i], sa[2 * i + 1]);
                 const float sum = ((sa[0] + sa[1]) + (sa[2] + sa[3])) + ((sa[4] + sa[5]) + (sa[6] + sa[7]));
                 l_run = l_run * alpha + sum;
-                if (__any_sync(0xffffffffu, rescale)) {
-                    // O_t holds every PV up to tile j-1: the commit that
-                    // signalled S_t(j) was issued after them.
-#pragma unroll
-                    for (int cc = 0; cc < DV / 32; ++cc) {
-                        uint32_t ov[32];
-                        tmem_ld32(tO + cc * 32, ov);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                        tmem_st32(tO + cc * 32, ov);
-                    }
-                }
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(bar(B_P_READY + t));
+                return true;
+            };
+            for (int j = 0; j < x.n_kv && ok; ++j) {
+                const int k0 = x.kv_start + j * kBN;
+                const bool interior = x.all_valid && k0 >= x.lo_last && k0 + kBN <= x.hi_first;
+                ok = interior ? tile_step(j, std::false_type{}) : tile_step(j, std::true_type{});
             }
             if (!ok) break;
 
@@ -840,6 +889,8 @@ int launch_t(const AttnParams &p, bool bf16, cudaStream_t stream) {
     a.nsub = p.G / a.Gp;
     a.nqblk = (p.Q + 2 * a.QP - 1) / (2 * a.QP);
     a.nunits = (long long)a.nqblk * p.B * p.Hkv * a.nsub;
+    a.per = (uint32_t)((long long)p.B * p.Hkv * a.nsub);
+    a.hs = (uint32_t)(p.Hkv * a.nsub);
     const float sc = p.scale == 0.f ? 1e-30f : fabsf(p.scale);
     a.c_scale = sc * kLog2e;
     a.idesc_s = idesc_f16(bf16, kBM, kBN, false, p.scale < 0.f);
@@ -903,7 +954,10 @@ bool prefill_tc_supported(const AttnParams &p, int dtype) {
     if (p.Q < 1) return false;
     const long long rows = p.cu_q ? p.Tq : (long long)p.Q;
     const long long keys = p.cu_q ? p.Tk : (long long)p.K;
-    return rows < (1LL << 31) && keys < (1LL << 31);
+    // work units are indexed in 32 bits
+    const int gp = pack_factor(p.G), qp = kBM / gp;
+    const long long nunits = (long long)((p.Q + 2 * qp - 1) / (2 * qp)) * p.B * p.Hkv * (p.G / gp);
+    return rows < (1LL << 31) && keys < (1LL << 31) && nunits < (1LL << 31);
 }
 
 int launch_prefill_tc(const AttnParams &p, int dtype, cudaStream_t stream) {
