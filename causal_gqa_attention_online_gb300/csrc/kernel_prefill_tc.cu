@@ -42,7 +42,6 @@
 #include <cudaTypedefs.h>
 
 #include <climits>
-#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
@@ -589,11 +588,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 
             float m_run = -INFINITY, l_run = 0.f;
-            // One KV tile of this warpgroup's softmax.  Two copies are compiled:
-            // with the key mask (the tiles that cross the causal diagonal, the
-            // window edge or the end of the keys) and without it (all others),
-            // so that the common path carries no masking code.
-            auto tile_step = [&](int j, auto masked) -> bool {
+            // One KV tile of this warpgroup's softmax.
+            auto tile_step = [&](int j, bool interior) -> bool {
                 // The two warpgroups take turns (tile k of group 0, tile k of
                 // group 1, tile k+1 of group 0, ...): while one runs its softmax
                 // the tensor core works on the other's tile.  Left free, the two
@@ -614,16 +610,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!warp_wait(bar(B_S_FULL + t), s_ph, abort_flag)) return false;
                 s_ph ^= 1u;
                 tc_fence_after();
-                uint32_t sr[4][32];
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
-                tmem_ld_wait();
-                if constexpr (decltype(masked)::value) {
-                    // keys outside [lo, hi) -> -inf (also replaces NaN from padding).
-                    // Per 32-key chunk: the row's legal keys as a bit mask; a chunk
-                    // that every row of the warp keeps whole is left alone.
+                if (!interior) {
+                    // A tile that crosses the causal diagonal, the window edge or the
+                    // end of the keys: keys outside [lo, hi) are set to -inf in TMEM
+                    // (which also keeps NaN from padding out) before the softmax
+                    // below reads S, so that there is one copy of that code for all
+                    // tiles.  Per 32-key chunk: the row's legal keys as a bit mask;
+                    // a chunk that every row of the warp keeps whole is left alone.
                     const int k0 = x.kv_start + j * kBN;
-#pragma unroll
+#pragma unroll 1
                     for (int cc = 0; cc < 4; ++cc) {
                         const int a0 = min(max(lo - k0 - cc * 32, 0), 32);
                         const int b0 = min(max(hi - k0 - cc * 32, 0), 32);
@@ -631,11 +626,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t below_a = a0 >= 32 ? 0xffffffffu : (1u << a0) - 1u;
                         const uint32_t keep = below_b & ~below_a;
                         if (__all_sync(0xffffffffu, keep == 0xffffffffu)) continue;
+                        uint32_t v[32];
+                        tmem_ld32(tS + cc * 32, v);
+                        tmem_ld_wait();
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
-                            if (!((keep >> i) & 1u)) sr[cc][i] = __float_as_uint(-INFINITY);
+                            v[i] = ((keep >> i) & 1u) ? v[i] : 0xff800000u;
+                        tmem_st32(tS + cc * 32, v);
                     }
+                    tmem_st_wait();
                 }
+                uint32_t sr[4][32];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
+                tmem_ld_wait();
                 // row max: eight independent chains of 3-input max
                 float mc[8];
 #pragma unroll
@@ -711,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < x.n_kv && ok; ++j) {
                 const int k0 = x.kv_start + j * kBN;
                 const bool interior = x.all_valid && k0 >= x.lo_last && k0 + kBN <= x.hi_first;
-                ok = interior ? tile_step(j, std::false_type{}) : tile_step(j, std::true_type{});
+                ok = tile_step(j, interior);
             }
             if (!ok) break;
 
