@@ -147,6 +147,12 @@ DECODE_SHAPES = [
     (1, 16, 4, 4, 129, 128, 128),    # Q*G = 16
     (1, 8, 2, 1, 32768, 64, 64),     # long KV: many splits
     (1, 16, 4, 1, 8193, 128, 128),
+    # many (sequence, KV head) units, as in batched serving
+    (40, 16, 1, 1, 333, 128, 64),
+    (20, 8, 2, 2, 300, 128, 128),
+    (10, 16, 4, 4, 129, 64, 128),
+    (48, 16, 2, 1, 700, 64, 64),
+    (38, 8, 1, 1, 5000, 128, 128),
 ]
 
 
