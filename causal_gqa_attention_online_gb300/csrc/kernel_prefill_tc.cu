@@ -243,6 +243,8 @@ __device__ __forceinline__ void raise_abort(volatile int *abort_flag, int *statu
     report_status(status, code);
 }
 
+// D, DV: the tile widths (64 or 128 columns); the real head dims p.D <= D and
+// p.Dv <= DV are multiples of 16, the rest of the tile columns zero-filled.
 template <typename T, int D, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tmQ,
@@ -579,9 +581,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             if (x.n_kv == 0) {  // nothing to attend: +0 and -inf
                 if (writes) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(og + orow * DV);
-#pragma unroll
-                    for (int i = 0; i < DV * 2 / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+                    uint4 *dst = reinterpret_cast<uint4 *>(og + orow * p.Dv);
+                    for (int i = 0; i < p.Dv * 2 / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
                     if (p.lse) p.lse[orow] = -INFINITY;
                 }
                 continue;
@@ -816,11 +817,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int e = i * 32 + lane;
                             const int rr = quarter * 32 + (e >> 3), ch = e & 7;
                             const int qp = qt0 + rr / a.Gp;
-                            if (qp < x.si.Qb) {
+                            if (qp < x.si.Qb && cp * 64 + ch * 8 < p.Dv) {
                                 const uint4 v = *reinterpret_cast<const uint4 *>(
                                     stg + rr * 128 + ((ch ^ (rr & 7)) << 4));
                                 const long long orr = (x.si.q_off + qp) * p.Hq + x.h0 + rr % a.Gp;
-                                *reinterpret_cast<uint4 *>(og + orr * DV + cp * 64 + ch * 8) = v;
+                                *reinterpret_cast<uint4 *>(og + orr * p.Dv + cp * 64 + ch * 8) = v;
                             }
                         }
                     }
@@ -908,14 +909,17 @@ int launch_t(const AttnParams &p, bool bf16, cudaStream_t stream) {
     const uint64_t krows = padded ? (uint64_t)p.K : (uint64_t)p.Tk;
     const uint64_t nb = padded ? (uint64_t)p.B : 1;
     CUtensorMap tq, tk, tv, to;
-    int rc = make_map(&tq, p.q, dt, D, p.Hq, qrows, nb, a.Gp, a.QP);
+    // maps over the real head dims: the columns up to the padded D / DV of the
+    // tiles are zero-filled by the loads (so they add nothing to S or O) and
+    // dropped by the O stores
+    int rc = make_map(&tq, p.q, dt, (uint64_t)p.D, p.Hq, qrows, nb, a.Gp, a.QP);
     if (rc) return rc;
-    rc = make_map(&to, p.o, dt, DV, p.Hq, qrows, nb, a.Gp, a.QP);
+    rc = make_map(&to, p.o, dt, (uint64_t)p.Dv, p.Hq, qrows, nb, a.Gp, a.QP);
     if (rc) return rc;
     if (krows > 0) {
-        rc = make_map(&tk, p.k, dt, D, p.Hkv, krows, nb, 1, kBN);
+        rc = make_map(&tk, p.k, dt, (uint64_t)p.D, p.Hkv, krows, nb, 1, kBN);
         if (rc) return rc;
-        rc = make_map(&tv, p.v, dt, DV, p.Hkv, krows, nb, 1, kBN);
+        rc = make_map(&tv, p.v, dt, (uint64_t)p.Dv, p.Hkv, krows, nb, 1, kBN);
         if (rc) return rc;
     } else {
         tk = tq;  // never read: every unit has no key
@@ -944,9 +948,11 @@ int launch_t(const AttnParams &p, bool bf16, cudaStream_t stream) {
 
 template <typename T>
 int launch_dtype(const AttnParams &p, bool bf16, cudaStream_t stream) {
-    if (p.D == 128 && p.Dv == 128) return launch_t<T, 128, 128>(p, bf16, stream);
-    if (p.D == 64 && p.Dv == 64) return launch_t<T, 64, 64>(p, bf16, stream);
-    if (p.D == 128 && p.Dv == 64) return launch_t<T, 128, 64>(p, bf16, stream);
+    // tiles padded to 64 or 128 columns
+    const bool d128 = p.D > 64, dv128 = p.Dv > 64;
+    if (d128 && dv128) return launch_t<T, 128, 128>(p, bf16, stream);
+    if (!d128 && !dv128) return launch_t<T, 64, 64>(p, bf16, stream);
+    if (d128) return launch_t<T, 128, 64>(p, bf16, stream);
     return launch_t<T, 64, 128>(p, bf16, stream);
 }
 
@@ -954,7 +960,8 @@ int launch_dtype(const AttnParams &p, bool bf16, cudaStream_t stream) {
 
 bool prefill_tc_supported(const AttnParams &p, int dtype) {
     if (dtype != 1 && dtype != 2) return false;
-    if ((p.D != 64 && p.D != 128) || (p.Dv != 64 && p.Dv != 128)) return false;
+    // head dims: multiples of 16 in [64, 128] (tiles padded to 64 or 128 columns)
+    if (p.D < 64 || p.D > 128 || p.D % 16 || p.Dv < 64 || p.Dv > 128 || p.Dv % 16) return false;
     if (p.Q < 1) return false;
     const long long rows = p.cu_q ? p.Tq : (long long)p.Q;
     const long long keys = p.cu_q ? p.Tk : (long long)p.K;

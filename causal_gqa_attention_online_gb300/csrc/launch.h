@@ -24,7 +24,7 @@ int launch_combine_flat(const float *o_parts, const float *lse_parts, void *o, f
 bool decode_supported(const AttnParams &p, int dtype);
 int decode_split_len(const AttnParams &p, int nsm);
 int launch_decode(const AttnParams &p, int dtype, cudaStream_t stream);
-// tcgen05/TMEM prefill (bf16/fp16, D, Dv in {64, 128}).
+// tcgen05/TMEM prefill (bf16/fp16, D and Dv multiples of 16 in [64, 128]).
 bool prefill_tc_supported(const AttnParams &p, int dtype);
 int launch_prefill_tc(const AttnParams &p, int dtype, cudaStream_t stream);
 

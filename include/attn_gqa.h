@@ -81,7 +81,7 @@ enum attn_status {
 enum attn_algo {
     ATTN_ALGO_AUTO = 0,     /* choose by dtype, head widths and query length */
     ATTN_ALGO_GENERIC = 1,  /* CUDA-core online softmax: any dtype, D, Dv <= 256 */
-    ATTN_ALGO_TCGEN05 = 2,  /* tcgen05/TMEM prefill: bf16/fp16, D, Dv in {64, 128} */
+    ATTN_ALGO_TCGEN05 = 2,  /* tcgen05/TMEM prefill: bf16/fp16, D, Dv multiples of 16 in [64, 128] */
     ATTN_ALGO_DECODE = 3    /* split-KV tensor-core decode: bf16/fp16, Q*G <= 16 */
 };
 

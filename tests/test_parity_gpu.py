@@ -222,6 +222,12 @@ TC_SHAPES = [
     (1, 6, 2, 90, 150, 128, 128),     # G = 3: three subgroups of one head
     (1, 8, 2, 3, 67, 128, 128),       # short query chunk, bottom-right offset
     (1, 4, 2, 300, 40, 64, 64),       # Q > K: leading rows without keys
+    # head dims between the tile widths: zero-filled tile columns
+    (1, 8, 2, 200, 260, 80, 80),
+    (1, 8, 2, 130, 130, 96, 96),
+    (2, 8, 4, 100, 300, 112, 64),     # G = 2
+    (1, 4, 2, 150, 150, 64, 96),
+    (1, 4, 1, 77, 200, 96, 128),
 ]
 
 
@@ -259,12 +265,13 @@ def test_tcgen05_negative_scale():
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-def test_tcgen05_varlen_packed(dtype):
+@pytest.mark.parametrize("dims", [(128, 128), (96, 80)], ids=lambda d: f"d{d[0]}x{d[1]}")
+def test_tcgen05_varlen_packed(dtype, dims):
     sk = np.array([0, 5, 33, 130, 1, 640, 0, 300, 1000], np.int32)
     sq = np.minimum(sk, np.array([0, 5, 7, 64, 1, 512, 0, 100, 512]))
     for w in (0, 100):
-        inp = synth.make_packed(sq, sk, 16, 4, 128, 128, dtype, seed=36, window=w)
-        parity.check(inp, "tcgen05", f"tcgen05 varlen {dtype} w={w}")
+        inp = synth.make_packed(sq, sk, 16, 4, dims[0], dims[1], dtype, seed=36, window=w)
+        parity.check(inp, "tcgen05", f"tcgen05 varlen {dtype} {dims} w={w}")
 
 
 def test_tcgen05_full_size_prefill_sampled():
