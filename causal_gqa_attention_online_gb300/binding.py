@@ -22,7 +22,7 @@ ALGOS = {"auto": 0, "generic": 1, "tcgen05": 2, "decode": 3}
 _DTYPE_CODE = {torch.float32: ATTN_F32, torch.float16: ATTN_F16, torch.bfloat16: ATTN_BF16}
 
 EXPORTED = ("attn_fwd", "attn_fwd_varlen", "attn_fwd_algo", "attn_fwd_varlen_algo",
-            "attn_lse_combine", "attn_fwd_decode_noalloc", "attn_last_error",
+            "attn_lse_combine", "attn_fwd_decode_noalloc", "attn_fwd_staged", "attn_last_error",
             "attn_device_status", "attn_kernel_launches", "attn_version")
 
 _lock = threading.Lock()
@@ -64,6 +64,10 @@ def load_library(path: str | None = None):
         lib.attn_fwd_decode_noalloc.restype = ip
         for f in (lib.attn_fwd, lib.attn_fwd_varlen, lib.attn_fwd_algo, lib.attn_fwd_varlen_algo):
             f.restype = ip
+        ullp = ctypes.POINTER(ctypes.c_ulonglong)
+        lib.attn_fwd_staged.argtypes = ([vp] * 10 + [ip] * 7 + [vp] * 4 + [ip, fp, ip, ip] +
+                                        [ullp, ullp, vp])
+        lib.attn_fwd_staged.restype = ip
         lib.attn_lse_combine.argtypes = [vp, vp, vp, vp, ip, ctypes.c_longlong, ip, ip, vp]
         lib.attn_lse_combine.restype = ip
         lib.attn_last_error.argtypes = []
@@ -226,3 +230,59 @@ def attn_lse_combine(o_parts, lse_parts, o=None, lse=None, *, dtype=torch.float3
                               _DTYPE_CODE[o.dtype], _stream_ptr(stream))
     _check(rc)
     return o, lse
+
+
+def attn_fwd_staged(hq, hk, hv, q, k, v, o, lse=None, ho=None, hlse=None, *, seqlens_q=None,
+                    seqlens_k=None, seqlens_q_dev=None, seqlens_k_dev=None, window=0, scale=None,
+                    chunks=0, stream=None):
+    """attn_fwd on host tensors (padded layout; page-locked for overlap): per
+    group of sequences, copy in the valid rows, run attention, copy the
+    outputs back, the copies of one group overlapping the attention of the
+    next.  ``q, k, v, o, lse`` are device staging buffers of the same shapes.
+    ``seqlens_q/k`` are int32 CPU tensors; their device copies may be given
+    as ``seqlens_q_dev/k_dev`` (else they are copied here, on ``stream``).
+    Returns (ho, hlse, bytes_in, bytes_out); the host outputs are complete
+    once ``stream`` reaches this point."""
+    lib = load_library()
+    B, Q, Hq, D = hq.shape
+    K, Hkv = hk.shape[1], hk.shape[2]
+    Dv = hv.shape[3]
+    dev = q.device
+    if ho is None:
+        ho = torch.empty((B, Q, Hq, Dv), dtype=hq.dtype).pin_memory()
+    if hlse is None and lse is not None:
+        hlse = torch.empty((B, Q, Hq), dtype=torch.float32).pin_memory()
+    cpu = torch.device("cpu")
+    for name, t, n in (("hq", hq, B * Q * Hq * D), ("hk", hk, B * K * Hkv * D),
+                       ("hv", hv, B * K * Hkv * Dv), ("ho", ho, B * Q * Hq * Dv)):
+        _check_tensor(name, t, hq.dtype, n, cpu)
+    for name, t, n in (("q", q, B * Q * Hq * D), ("k", k, B * K * Hkv * D),
+                       ("v", v, B * K * Hkv * Dv), ("o", o, B * Q * Hq * Dv)):
+        _check_tensor(name, t, hq.dtype, n, dev)
+    if lse is not None:
+        _check_tensor("lse", lse, torch.float32, B * Q * Hq, dev)
+        _check_tensor("hlse", hlse, torch.float32, B * Q * Hq, cpu)
+    dsq, dsk = seqlens_q_dev, seqlens_k_dev
+    st = stream if stream is not None else torch.cuda.current_stream()
+    if seqlens_q is not None:
+        _check_tensor("seqlens_q", seqlens_q, torch.int32, B, cpu)
+        if dsq is None:
+            with torch.cuda.stream(st):
+                dsq = seqlens_q.to(dev, non_blocking=True)
+        _check_tensor("seqlens_q_dev", dsq, torch.int32, B, dev)
+    if seqlens_k is not None:
+        _check_tensor("seqlens_k", seqlens_k, torch.int32, B, cpu)
+        if dsk is None:
+            with torch.cuda.stream(st):
+                dsk = seqlens_k.to(dev, non_blocking=True)
+        _check_tensor("seqlens_k_dev", dsk, torch.int32, B, dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    bin_, bout = ctypes.c_ulonglong(0), ctypes.c_ulonglong(0)
+    rc = lib.attn_fwd_staged(_ptr(hq), _ptr(hk), _ptr(hv), _ptr(ho), _ptr(hlse), _ptr(q), _ptr(k),
+                             _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Q, K, D, Dv, _ptr(dsq),
+                             _ptr(dsk), _ptr(seqlens_q), _ptr(seqlens_k), int(window),
+                             float(scale), _DTYPE_CODE[hq.dtype], int(chunks),
+                             ctypes.byref(bin_), ctypes.byref(bout), _stream_ptr(st))
+    _check(rc)
+    return ho, hlse, bin_.value, bout.value

@@ -175,6 +175,37 @@ ATTN_API int attn_fwd_decode_noalloc(const void *q, const void *k, const void *v
                                      int Dv, const int32_t *seqlens_q, const int32_t *seqlens_k,
                                      int window, float scale, int dtype, attn_stream_t stream);
 
+/*
+ * attn_fwd_staged -- attn_fwd on tensors that live in host memory.  A
+ * serving aid of this library (the pages have no counterpart): the batch is
+ * cut into `chunks` groups of sequences (<= 0: 4; at most B and 32), and for
+ * each group the host->device copy of its inputs, its attention launch (on
+ * `stream`, exactly as attn_fwd) and the device->host copy of its outputs are
+ * ordered by events across three streams, so the copies of one group overlap
+ * the attention of another.
+ *   hq, hk, hv, ho, hlse   host tensors, padded layout as in attn_fwd (hlse
+ *                          may be NULL); page-locked memory is needed for the
+ *                          copies to overlap anything
+ *   q, k, v, o, lse        caller-owned device buffers of the same shapes,
+ *                          used as staging (lse may be NULL only with hlse)
+ *   seqlens_q, seqlens_k   as in attn_fwd (device int32 [B] or NULL), and
+ *   seqlens_q_host, seqlens_k_host  the same values in host memory (NULL
+ *                          exactly when the device array is NULL): only rows
+ *                          [0, Qb) of q and [0, Kb) of k and v are copied in;
+ *                          every row of o and lse is copied out
+ *   bytes_in, bytes_out    (may be NULL) receive the bytes copied each way
+ * Asynchronous like attn_fwd: `stream` is ordered after the last copy out.
+ * Calls on one device are serialised inside the library (they share its two
+ * copy streams).  Return codes as attn_fwd.
+ */
+ATTN_API int attn_fwd_staged(const void *hq, const void *hk, const void *hv, void *ho, float *hlse,
+                             void *q, void *k, void *v, void *o, float *lse, int B, int Hq,
+                             int Hkv, int Q, int K, int D, int Dv, const int32_t *seqlens_q,
+                             const int32_t *seqlens_k, const int32_t *seqlens_q_host,
+                             const int32_t *seqlens_k_host, int window, float scale, int dtype,
+                             int chunks, unsigned long long *bytes_in,
+                             unsigned long long *bytes_out, attn_stream_t stream);
+
 /* Message for the calling thread's most recent failed call ("" if none). */
 ATTN_API const char *attn_last_error(void);
 
