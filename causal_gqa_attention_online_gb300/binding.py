@@ -19,9 +19,12 @@ from . import build_ext
 ATTN_F32, ATTN_F16, ATTN_BF16 = 0, 1, 2
 ATTN_ALGO_AUTO, ATTN_ALGO_GENERIC, ATTN_ALGO_TCGEN05, ATTN_ALGO_DECODE = 0, 1, 2, 3
 ALGOS = {"auto": 0, "generic": 1, "tcgen05": 2, "decode": 3}
+# bottom-right causal (the pages' rule), top-left causal, none
+MASKS = {"causal": 0, "causal_top_left": 1, "none": 2}
 _DTYPE_CODE = {torch.float32: ATTN_F32, torch.float16: ATTN_F16, torch.bfloat16: ATTN_BF16}
 
 EXPORTED = ("attn_fwd", "attn_fwd_varlen", "attn_fwd_algo", "attn_fwd_varlen_algo",
+            "attn_fwd_ex", "attn_fwd_varlen_ex",
             "attn_lse_combine", "attn_fwd_decode_noalloc", "attn_fwd_staged", "attn_last_error",
             "attn_device_status", "attn_kernel_launches", "attn_version")
 
@@ -60,6 +63,10 @@ def load_library(path: str | None = None):
         lib.attn_fwd_varlen.argtypes = varlen + [vp]
         lib.attn_fwd_algo.argtypes = common + [ip, vp]
         lib.attn_fwd_varlen_algo.argtypes = varlen + [ip, vp]
+        lib.attn_fwd_ex.argtypes = common[:-1] + [ip, ip, ip, vp]
+        lib.attn_fwd_varlen_ex.argtypes = varlen[:-1] + [ip, ip, ip, vp]
+        lib.attn_fwd_ex.restype = ip
+        lib.attn_fwd_varlen_ex.restype = ip
         lib.attn_fwd_decode_noalloc.argtypes = common + [vp]
         lib.attn_fwd_decode_noalloc.restype = ip
         for f in (lib.attn_fwd, lib.attn_fwd_varlen, lib.attn_fwd_algo, lib.attn_fwd_varlen_algo):
@@ -125,8 +132,9 @@ def _check_tensor(name, t, dtype, numel, device):
 
 
 def attn_fwd(q, k, v, o=None, lse=None, *, seqlens_q=None, seqlens_k=None, window=0,
-             scale=None, algo="auto", stream=None, want_lse=True):
+             scale=None, algo="auto", mask="causal", stream=None, want_lse=True):
     """Padded layout: q [B,Q,Hq,D], k [B,K,Hkv,D], v [B,K,Hkv,Dv] CUDA tensors.
+    ``mask``: "causal" (bottom-right, the default), "causal_top_left" or "none".
 
     Returns (o [B,Q,Hq,Dv], lse [B,Q,Hq] float32 or None)."""
     lib = load_library()
@@ -148,17 +156,19 @@ def attn_fwd(q, k, v, o=None, lse=None, *, seqlens_q=None, seqlens_k=None, windo
             _check_tensor(name, t, torch.int32, B, dev)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    rc = lib.attn_fwd_algo(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Q, K, D, Dv,
-                           _ptr(seqlens_q), _ptr(seqlens_k), int(window), float(scale),
-                           _DTYPE_CODE[q.dtype], ALGOS[algo], _stream_ptr(stream))
+    rc = lib.attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Q, K, D, Dv,
+                         _ptr(seqlens_q), _ptr(seqlens_k), int(window), float(scale), MASKS[mask],
+                         _DTYPE_CODE[q.dtype], ALGOS[algo], _stream_ptr(stream))
     _check(rc)
     return o, lse
 
 
 def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_q, max_k, o=None, lse=None, *,
-                    window=0, scale=None, algo="auto", stream=None, want_lse=True):
+                    window=0, scale=None, algo="auto", mask="causal", stream=None,
+                    want_lse=True):
     """Packed layout: q [Tq,Hq,D], k [Tk,Hkv,D], v [Tk,Hkv,Dv], int32
-    cumulative lengths [B+1] on the device.  Returns (o [Tq,Hq,Dv], lse [Tq,Hq])."""
+    cumulative lengths [B+1] on the device.  ``mask`` as in attn_fwd.
+    Returns (o [Tq,Hq,Dv], lse [Tq,Hq])."""
     lib = load_library()
     Tq, Hq, D = q.shape
     Tk, Hkv = k.shape[0], k.shape[1]
@@ -178,10 +188,10 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_q, max_k, o=None, l
     _check_tensor("cu_seqlens_k", cu_seqlens_k, torch.int32, B + 1, dev)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    rc = lib.attn_fwd_varlen_algo(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv,
-                                  Tq, Tk, int(max_q), int(max_k), D, Dv, _ptr(cu_seqlens_q),
-                                  _ptr(cu_seqlens_k), int(window), float(scale),
-                                  _DTYPE_CODE[q.dtype], ALGOS[algo], _stream_ptr(stream))
+    rc = lib.attn_fwd_varlen_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv,
+                                Tq, Tk, int(max_q), int(max_k), D, Dv, _ptr(cu_seqlens_q),
+                                _ptr(cu_seqlens_k), int(window), float(scale), MASKS[mask],
+                                _DTYPE_CODE[q.dtype], ALGOS[algo], _stream_ptr(stream))
     _check(rc)
     return o, lse
 

@@ -229,10 +229,18 @@ int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
                int Hkv, long long Tq, long long Tk, int Q, int K, int D, int Dv,
                const int32_t *seqlens_q,
                const int32_t *seqlens_k, const int32_t *cu_q, const int32_t *cu_k, int window,
-               float scale, int dtype, int algo, cudaStream_t stream) {
+               float scale, int mask, int dtype, int algo, cudaStream_t stream) {
     g_last_error[0] = '\0';
     int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Q, K, D, Dv, dtype, algo);
     if (rc) return rc;
+    if (mask < ATTN_MASK_CAUSAL || mask > ATTN_MASK_NONE) {
+        set_error("unknown mask %d", mask);
+        return ATTN_ERR_INVALID;
+    }
+    if (mask == ATTN_MASK_NONE && window > 0) {
+        set_error("a window needs a causal mask (window=%d with ATTN_MASK_NONE)", window);
+        return ATTN_ERR_INVALID;
+    }
     if ((long long)B * Q * Hq == 0) return ATTN_OK;
     AttnParams p;
     memset(&p, 0, sizeof(p));
@@ -258,6 +266,7 @@ int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
     // A window of at least K keys keeps every causal key: same as no window
     // (this also keeps the kernels' window arithmetic far from overflow).
     p.window = (window <= 0 || window >= K) ? 0 : window;
+    p.mask = mask;
     p.scale = scale;
     p.scale_log2 = scale * kLog2e;
     p.nsplit = 1;
@@ -272,13 +281,21 @@ using namespace attn;
 
 extern "C" {
 
+int attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+                int Hkv, int Q, int K, int D, int Dv, const int32_t *seqlens_q,
+                const int32_t *seqlens_k, int window, float scale, int mask, int dtype, int algo,
+                attn_stream_t stream) {
+    return fwd_common(q, k, v, o, lse, B, Hq, Hkv, (long long)B * Q, (long long)B * K, Q, K, D, Dv,
+                      seqlens_q, seqlens_k, nullptr, nullptr, window, scale, mask, dtype, algo,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
 int attn_fwd_algo(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                   int Hq, int Hkv, int Q, int K, int D, int Dv, const int32_t *seqlens_q,
                   const int32_t *seqlens_k, int window, float scale, int dtype, int algo,
                   attn_stream_t stream) {
-    return fwd_common(q, k, v, o, lse, B, Hq, Hkv, (long long)B * Q, (long long)B * K, Q, K, D, Dv,
-                      seqlens_q, seqlens_k, nullptr,
-                      nullptr, window, scale, dtype, algo, reinterpret_cast<cudaStream_t>(stream));
+    return attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, Q, K, D, Dv, seqlens_q, seqlens_k, window,
+                       scale, ATTN_MASK_CAUSAL, dtype, algo, stream);
 }
 
 int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
@@ -289,11 +306,11 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
                          scale, dtype, ATTN_ALGO_AUTO, stream);
 }
 
-int attn_fwd_varlen_algo(const void *q, const void *k, const void *v, void *o, float *lse,
-                         int B, int Hq, int Hkv, int total_q, int total_k, int max_Q, int max_K,
-                         int D, int Dv, const int32_t *cu_seqlens_q,
-                         const int32_t *cu_seqlens_k, int window, float scale, int dtype,
-                         int algo, attn_stream_t stream) {
+int attn_fwd_varlen_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                       int Hq, int Hkv, int total_q, int total_k, int max_Q, int max_K, int D,
+                       int Dv, const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                       int window, float scale, int mask, int dtype, int algo,
+                       attn_stream_t stream) {
     if (B > 0 && (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr)) {
         attn::set_error("cu_seqlens_q and cu_seqlens_k must be non-null");
         return ATTN_ERR_INVALID;
@@ -304,9 +321,18 @@ int attn_fwd_varlen_algo(const void *q, const void *k, const void *v, void *o, f
     }
     if (total_q == 0) return ATTN_OK;
     return fwd_common(q, k, v, o, lse, B, Hq, Hkv, total_q, total_k, max_Q, max_K, D, Dv,
-                      nullptr, nullptr,
-                      cu_seqlens_q, cu_seqlens_k, window, scale, dtype, algo,
-                      reinterpret_cast<cudaStream_t>(stream));
+                      nullptr, nullptr, cu_seqlens_q, cu_seqlens_k, window, scale, mask, dtype,
+                      algo, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_fwd_varlen_algo(const void *q, const void *k, const void *v, void *o, float *lse,
+                         int B, int Hq, int Hkv, int total_q, int total_k, int max_Q, int max_K,
+                         int D, int Dv, const int32_t *cu_seqlens_q,
+                         const int32_t *cu_seqlens_k, int window, float scale, int dtype,
+                         int algo, attn_stream_t stream) {
+    return attn_fwd_varlen_ex(q, k, v, o, lse, B, Hq, Hkv, total_q, total_k, max_Q, max_K, D, Dv,
+                              cu_seqlens_q, cu_seqlens_k, window, scale, ATTN_MASK_CAUSAL, dtype,
+                              algo, stream);
 }
 
 int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse, int B,

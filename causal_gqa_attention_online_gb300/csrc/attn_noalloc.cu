@@ -111,6 +111,7 @@ extern "C" int attn_fwd_decode_noalloc(const void *q, const void *k, const void 
     p.seqlens_q = seqlens_q;
     p.seqlens_k = seqlens_k;
     p.window = (window <= 0 || window >= K) ? 0 : window;
+    p.mask = 0;  // bottom-right causal, as attn_fwd
     p.scale = scale;
     p.scale_log2 = scale * kLog2e;
     if (!decode_supported(p, dtype)) {

@@ -39,6 +39,7 @@ struct AttnParams {
     const int32_t *cu_q;       // packed layout
     const int32_t *cu_k;       // packed layout
     int window;              // <= 0: off
+    int mask;                // attn_mask: 0 bottom-right causal, 1 top-left causal, 2 none
     float scale;             // multiplies Q.K
     float scale_log2;        // scale * log2(e)
     // split-KV
@@ -78,10 +79,18 @@ __device__ __forceinline__ SeqInfo seq_info(const AttnParams &p, int b) {
     return s;
 }
 
-// Legal keys of query row qi: [lo, hi) (empty when hi <= lo).
-__device__ __forceinline__ void legal_range(int qi, int Qb, int Kb, int window, int &lo,
+// Legal keys of query row qi: [lo, hi) (empty when hi <= lo).  Causal masks
+// keep the keys up to the row's diagonal -- aligned to the end of the keys
+// (bottom-right, the default) or to their start (top-left) -- and a window
+// keeps the last `window` of those; no mask keeps every key of the sequence.
+__device__ __forceinline__ void legal_range(int qi, int Qb, int Kb, int window, int mask, int &lo,
                                             int &hi) {
-    const int diag = qi + Kb - Qb;  // last legal key
+    if (mask == 2) {
+        lo = 0;
+        hi = Kb;
+        return;
+    }
+    const int diag = mask == 1 ? qi : qi + Kb - Qb;  // last legal key
     hi = min(diag + 1, Kb);
     lo = 0;
     if (window > 0) lo = max(0, diag - window + 1);

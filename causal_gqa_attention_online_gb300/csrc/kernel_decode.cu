@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p)
     bool mine = false;
     for (int r = 0; r < nrows; ++r) {
         int lo = 0, hi = 0;
-        if (r < nvalid) legal_range(r / G, si.Qb, si.Kb, p.window, lo, hi);
+        if (r < nvalid) legal_range(r / G, si.Qb, si.Kb, p.window, p.mask, lo, hi);
         const SplitSpan sp = split_span(lo, hi, p.split_len);
         if (sp.direct ? sp.first == split : (split >= sp.first && split <= sp.last)) mine = true;
         if (hi > lo) {
@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p)
         for (int e = 0; e < 2; ++e) {
             const int row = nt * 8 + 2 * tig + e;
             int lo = 0, hi = 0;
-            if (row < nvalid) legal_range(row / G, si.Qb, si.Kb, p.window, lo, hi);
+            if (row < nvalid) legal_range(row / G, si.Qb, si.Kb, p.window, p.mask, lo, hi);
             rlo[nt][e] = max(lo, kbeg);
             rhi[nt][e] = min(hi, kend);
         }
@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p)
     for (int idx = tid; idx < nrows * C4; idx += kThreads) {
         const int row = idx / C4, c = (idx % C4) * 4;
         int lo = 0, hi = 0;
-        if (row < nvalid) legal_range(row / G, si.Qb, si.Kb, p.window, lo, hi);
+        if (row < nvalid) legal_range(row / G, si.Qb, si.Kb, p.window, p.mask, lo, hi);
         const SplitSpan sp = split_span(lo, hi, p.split_len);
         const bool direct = sp.direct;
         if (direct ? sp.first != split : (split < sp.first || split > sp.last)) continue;

@@ -65,8 +65,8 @@ __global__ void __launch_bounds__(128) generic_fwd_kernel(const AttnParams p) {
     int key_lo = 0, key_hi = 0;
     if (r0 < nvalid) {
         int lo_a, hi_a, lo_b, hi_b;
-        legal_range(r0 / G, si.Qb, si.Kb, p.window, lo_a, hi_a);
-        legal_range((min(r0 + kRows, nvalid) - 1) / G, si.Qb, si.Kb, p.window, lo_b, hi_b);
+        legal_range(r0 / G, si.Qb, si.Kb, p.window, p.mask, lo_a, hi_a);
+        legal_range((min(r0 + kRows, nvalid) - 1) / G, si.Qb, si.Kb, p.window, p.mask, lo_b, hi_b);
         key_lo = lo_a;
         key_hi = hi_b;
     }
@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(128) generic_fwd_kernel(const AttnParams p) {
         const int r = r0 + warp + kWarps * i;
         rlo[i] = 0;
         rhi[i] = 0;
-        if (r < nvalid) legal_range(r / G, si.Qb, si.Kb, p.window, rlo[i], rhi[i]);
+        if (r < nvalid) legal_range(r / G, si.Qb, si.Kb, p.window, p.mask, rlo[i], rhi[i]);
         span[i] = split_span(rlo[i], rhi[i], p.split_len);
         rlo[i] = max(rlo[i], key_lo);
         rhi[i] = min(rhi[i], key_hi);
@@ -107,8 +107,9 @@ __global__ void __launch_bounds__(128) generic_fwd_kernel(const AttnParams p) {
         __syncthreads();
 #pragma unroll
         for (int i = 0; i < kRPW; ++i) {
-            // warp-uniform: the row's legal range misses this tile
-            if (rhi[i] <= t0 || rlo[i] >= t0 + kTK) continue;
+            // warp-uniform: the row's legal range misses this tile (or is empty:
+            // with the top-left mask and a window, lo can pass the last key)
+            if (rhi[i] <= rlo[i] || rhi[i] <= t0 || rlo[i] >= t0 + kTK) continue;
             const int rr = warp + kWarps * i;
             const int key = t0 + lane;
             float s = -INFINITY;
@@ -279,7 +280,7 @@ __global__ void __launch_bounds__(128) combine_rows_kernel(const AttnParams p) {
     float *lse_out = p.lse ? p.lse + (si.q_off + qi) * p.Hq + h : nullptr;
     if (qi >= si.Qb) return;  // padded rows are written by the forward kernel
     int lo, hi;
-    legal_range(qi, si.Qb, si.Kb, p.window, lo, hi);
+    legal_range(qi, si.Qb, si.Kb, p.window, p.mask, lo, hi);
     const SplitSpan span = split_span(lo, hi, p.split_len);
     if (span.direct) return;  // written by the forward kernel
     const long long stride = (long long)p.B * p.Q * p.Hq;

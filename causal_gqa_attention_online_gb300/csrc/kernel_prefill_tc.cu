@@ -170,8 +170,8 @@ __device__ __forceinline__ UnitInfo unit_info(const PrefillArgs &a, long long u6
     if (x.q0 >= x.si.Qb) return x;
     const int q_last = min(x.q0 + 2 * a.QP, x.si.Qb) - 1;
     int lo_f, hi_f, lo_l, hi_l;
-    legal_range(x.q0, x.si.Qb, x.si.Kb, p.window, lo_f, hi_f);
-    legal_range(q_last, x.si.Qb, x.si.Kb, p.window, lo_l, hi_l);
+    legal_range(x.q0, x.si.Qb, x.si.Kb, p.window, p.mask, lo_f, hi_f);
+    legal_range(q_last, x.si.Qb, x.si.Kb, p.window, p.mask, lo_l, hi_l);
     if (hi_l <= lo_f) return x;
     x.kv_start = lo_f;
     x.hi_unit = hi_l;
@@ -576,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool valid = qpos < x.si.Qb;
             const bool writes = padded ? qpos < p.Q : valid;
             int lo = 0, hi = 0;
-            if (valid) legal_range(qpos, x.si.Qb, x.si.Kb, p.window, lo, hi);
+            if (valid) legal_range(qpos, x.si.Qb, x.si.Kb, p.window, p.mask, lo, hi);
             const long long orow = (x.si.q_off + qpos) * p.Hq + head;
 
             if (x.n_kv == 0) {  // nothing to attend: +0 and -inf

@@ -85,6 +85,13 @@ enum attn_algo {
     ATTN_ALGO_DECODE = 3    /* split-KV tensor-core decode: bf16/fp16, Q*G <= 16 */
 };
 
+/* Which keys a query row may attend to (attn_fwd_ex, attn_fwd_varlen_ex). */
+enum attn_mask {
+    ATTN_MASK_CAUSAL = 0,          /* bottom-right causal: key k <= q + Kb - Qb (attn_fwd's) */
+    ATTN_MASK_CAUSAL_TOP_LEFT = 1, /* top-left causal: key k <= q */
+    ATTN_MASK_NONE = 2             /* every key k < Kb (no window allowed) */
+};
+
 /*
  * attn_fwd -- padded layout.
  *   q   [B, Q, Hq, D]    o   [B, Q, Hq, Dv]    lse [B, Q, Hq] (float32, may be NULL)
@@ -136,6 +143,24 @@ ATTN_API int attn_fwd_varlen_algo(const void *q, const void *k, const void *v, v
                          int D, int Dv,
                          const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int window,
                          float scale, int dtype, int algo, attn_stream_t stream);
+
+/*
+ * attn_fwd_ex / attn_fwd_varlen_ex -- the two operations with an explicit
+ * mask (attn_mask) and kernel choice (attn_algo).  The pages define the
+ * bottom-right causal mask only; the top-left causal mask and no mask are
+ * extensions of this library: the same online-softmax recurrence over a
+ * different set of legal keys (a window applies to the causal masks only:
+ * ATTN_MASK_NONE with window > 0 is ATTN_ERR_INVALID).
+ */
+ATTN_API int attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                         int Hq, int Hkv, int Q, int K, int D, int Dv, const int32_t *seqlens_q,
+                         const int32_t *seqlens_k, int window, float scale, int mask, int dtype,
+                         int algo, attn_stream_t stream);
+ATTN_API int attn_fwd_varlen_ex(const void *q, const void *k, const void *v, void *o, float *lse,
+                                int B, int Hq, int Hkv, int total_q, int total_k, int max_Q,
+                                int max_K, int D, int Dv, const int32_t *cu_seqlens_q,
+                                const int32_t *cu_seqlens_k, int window, float scale, int mask,
+                                int dtype, int algo, attn_stream_t stream);
 
 /*
  * attn_lse_combine -- the legal merge of split-KV partial states (the

@@ -75,15 +75,15 @@ class OracleLib:
         i32p = ctypes.POINTER(ctypes.c_int32)
         ci, cd, cl = ctypes.c_int, ctypes.c_double, ctypes.c_long
         lib.oracle_attn_padded.argtypes = [f32p, f32p, f32p, f64p, f64p] + [ci] * 7 + [
-            i32p, i32p, ci, cd, ci]
+            i32p, i32p, ci, ci, cd, ci]
         lib.oracle_attn_padded.restype = ci
         lib.oracle_attn_packed.argtypes = [f32p, f32p, f32p, f64p, f64p] + [ci] * 5 + [
-            i32p, i32p, ci, cd, ci]
+            i32p, i32p, ci, ci, cd, ci]
         lib.oracle_attn_packed.restype = ci
         lib.oracle_attn_padded_rows.argtypes = [f32p, f32p, f32p] + [ci] * 7 + [
-            i32p, i32p, ci, cd, i32p, i32p, i32p, cl, f64p, f64p, ci]
+            i32p, i32p, ci, ci, cd, i32p, i32p, i32p, cl, f64p, f64p, ci]
         lib.oracle_attn_padded_rows.restype = ci
-        lib.oracle_legal_pairs.argtypes = [ci, ci, ci]
+        lib.oracle_legal_pairs.argtypes = [ci, ci, ci, ci]
         lib.oracle_legal_pairs.restype = ctypes.c_longlong
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ci
@@ -91,8 +91,10 @@ class OracleLib:
         self.path = path
 
     def attn_padded(self, q, k, v, *, B, Hq, Hkv, Q, K, D, Dv, seqlens_q=None,
-                    seqlens_k=None, window=0, scale=None, nthreads=0):
+                    seqlens_k=None, window=0, scale=None, nthreads=0, mask=0):
         """Padded layout q [B,Q,Hq,D], k [B,K,Hkv,D], v [B,K,Hkv,Dv].
+        ``mask``: 0 bottom-right causal (the pages' rule), 1 top-left causal,
+        2 none.
 
         Returns (o [B,Q,Hq,Dv] float64, lse [B,Q,Hq] float64)."""
         if scale is None:
@@ -107,14 +109,14 @@ class OracleLib:
         o = np.empty((B, Q, Hq, Dv), np.float64)
         lse = np.empty((B, Q, Hq), np.float64)
         rc = self.lib.oracle_attn_padded(qp, kp, vp, _f64p(o), _f64p(lse), B, Hq, Hkv, Q, K,
-                                         D, Dv, sqp, skp, int(window), float(scale),
+                                         D, Dv, sqp, skp, int(window), int(mask), float(scale),
                                          int(nthreads))
         if rc != 0:
             raise ValueError(f"oracle_attn_padded failed with status {rc}")
         return o, lse
 
     def attn_packed(self, q, k, v, *, B, Hq, Hkv, D, Dv, cu_seqlens_q, cu_seqlens_k,
-                    window=0, scale=None, nthreads=0):
+                    window=0, scale=None, nthreads=0, mask=0):
         """Packed layout q [Tq,Hq,D], k [Tk,Hkv,D], v [Tk,Hkv,Dv] with int32
         cumulative lengths [B+1].  Returns (o [Tq,Hq,Dv], lse [Tq,Hq]) float64."""
         if scale is None:
@@ -130,13 +132,14 @@ class OracleLib:
         o = np.empty((Tq, Hq, Dv), np.float64)
         lse = np.empty((Tq, Hq), np.float64)
         rc = self.lib.oracle_attn_packed(qp, kp, vp, _f64p(o), _f64p(lse), B, Hq, Hkv, D, Dv,
-                                         cqp, ckp, int(window), float(scale), int(nthreads))
+                                         cqp, ckp, int(window), int(mask), float(scale),
+                                         int(nthreads))
         if rc != 0:
             raise ValueError(f"oracle_attn_packed failed with status {rc}")
         return o, lse
 
     def attn_padded_rows(self, q, k, v, rows, *, B, Hq, Hkv, Q, K, D, Dv, seqlens_q=None,
-                         seqlens_k=None, window=0, scale=None, nthreads=0):
+                         seqlens_k=None, window=0, scale=None, nthreads=0, mask=0):
         """Selected rows of the padded layout.  ``rows`` is an int array [n,3]
         of (b, q, h).  Returns (o [n,Dv], lse [n]) float64."""
         if scale is None:
@@ -156,15 +159,16 @@ class OracleLib:
         o = np.empty((n, Dv), np.float64)
         lse = np.empty((n,), np.float64)
         rc = self.lib.oracle_attn_padded_rows(qp, kp, vp, B, Hq, Hkv, Q, K, D, Dv, sqp, skp,
-                                              int(window), float(scale), rbp, rqp, rhp, n,
+                                              int(window), int(mask), float(scale), rbp, rqp,
+                                              rhp, n,
                                               _f64p(o), _f64p(lse), int(nthreads))
         if rc != 0:
             raise ValueError(f"oracle_attn_padded_rows failed with status {rc}")
         return o, lse
 
-    def legal_pairs(self, Qb: int, Kb: int, window: int = 0) -> int:
+    def legal_pairs(self, Qb: int, Kb: int, window: int = 0, mask: int = 0) -> int:
         """Legal (query, key) pairs of one sequence and head, by enumeration."""
-        return int(self.lib.oracle_legal_pairs(int(Qb), int(Kb), int(window)))
+        return int(self.lib.oracle_legal_pairs(int(Qb), int(Kb), int(window), int(mask)))
 
     def max_threads(self) -> int:
         return int(self.lib.oracle_max_threads())
@@ -190,8 +194,8 @@ def attn_padded_rows(*args, **kw):
     return _default().attn_padded_rows(*args, **kw)
 
 
-def legal_pairs(Qb: int, Kb: int, window: int = 0) -> int:
-    return _default().legal_pairs(Qb, Kb, window)
+def legal_pairs(Qb: int, Kb: int, window: int = 0, mask: int = 0) -> int:
+    return _default().legal_pairs(Qb, Kb, window, mask)
 
 
 def max_threads() -> int:

@@ -36,6 +36,13 @@
  * keys including the diagonal one; rows with no legal key give +0 / -inf; the
  * LSE is in natural log.
  *
+ * Two masks beyond the pages' bottom-right rule, selected by `mask` (the
+ * library's extensions; the definition above is otherwise unchanged):
+ *   mask 1, top-left causal: the diagonal is k = q (L = { k < Kb : k <= q },
+ *           with the window counted back from that diagonal);
+ *   mask 2, no mask: L = { k : 0 <= k < Kb } (no window).
+ * mask 0 is the pages' bottom-right causal rule.
+ *
  * Inputs are float32 arrays holding exactly the values the device sees
  * (bf16 / fp16 / fp32 values are all exact in float32); every product and sum
  * is taken in double.  Layouts:
@@ -53,15 +60,27 @@
 /* One (sequence, head, query-row) of the definition above.  qrow points at
  * Q[q,h,0]; kbase/vbase point at key row 0 of this sequence and KV head; the
  * key stride is the element distance between consecutive key rows. */
+/* The legal keys of query row q as inclusive bounds [*lo, *hi]. */
+static void legal_keys(int q, int Qb, int Kb, int window, int mask, long *lo, long *hi)
+{
+    *lo = 0;
+    if (mask == 2) {                                   /* no mask: every key */
+        *hi = (long)Kb - 1;
+        return;
+    }
+    const long diag = mask == 1 ? (long)q : (long)q + Kb - Qb;   /* last legal key */
+    *hi = diag;
+    if (window > 0 && diag - window + 1 > *lo) *lo = diag - window + 1;
+    if (*hi > (long)Kb - 1) *hi = (long)Kb - 1;
+}
+
 static void oracle_row(const float *qrow, const float *kbase, const float *vbase,
                        long kstride, long vstride, int D, int Dv, int q, int Qb,
-                       int Kb, int window, double scale, double *s_scratch,
+                       int Kb, int window, int mask, double scale, double *s_scratch,
                        double *orow, double *lse_out)
 {
-    const long diag = (long)q + Kb - Qb;              /* last legal key */
-    long lo = 0, hi = diag;                            /* inclusive bounds */
-    if (window > 0 && diag - window + 1 > lo) lo = diag - window + 1;
-    if (hi > (long)Kb - 1) hi = (long)Kb - 1;
+    long lo, hi;                                       /* inclusive bounds */
+    legal_keys(q, Qb, Kb, window, mask, &lo, &hi);
     for (int j = 0; j < Dv; ++j) orow[j] = 0.0;
     if (hi < lo) { *lse_out = -INFINITY; return; }
 
@@ -105,9 +124,10 @@ static int check_dims(int B, int Hq, int Hkv, int D, int Dv)
 int oracle_attn_padded(const float *q, const float *k, const float *v, double *o,
                        double *lse, int B, int Hq, int Hkv, int Q, int K, int D,
                        int Dv, const int32_t *seqlens_q, const int32_t *seqlens_k,
-                       int window, double scale, int nthreads)
+                       int window, int mask, double scale, int nthreads)
 {
     if (check_dims(B, Hq, Hkv, D, Dv) || Q < 0 || K < 0) return 1;
+    if (mask < 0 || mask > 2 || (mask == 2 && window > 0)) return 1;
     const int G = Hq / Hkv;
     const long nrows = (long)B * Q * Hq;
 #ifdef _OPENMP
@@ -140,7 +160,7 @@ int oracle_attn_padded(const float *q, const float *k, const float *v, double *o
             const int kh = h / G;
             oracle_row(q + r * D, k + ((long)b * K * Hkv + kh) * D,
                        v + ((long)b * K * Hkv + kh) * Dv, (long)Hkv * D,
-                       (long)Hkv * Dv, D, Dv, qi, Qb, Kb, window, scale, s, orow,
+                       (long)Hkv * Dv, D, Dv, qi, Qb, Kb, window, mask, scale, s, orow,
                        &lse[r]);
         }
         free(s);
@@ -153,9 +173,10 @@ int oracle_attn_padded(const float *q, const float *k, const float *v, double *o
 int oracle_attn_packed(const float *q, const float *k, const float *v, double *o,
                        double *lse, int B, int Hq, int Hkv, int D, int Dv,
                        const int32_t *cu_q, const int32_t *cu_k, int window,
-                       double scale, int nthreads)
+                       int mask, double scale, int nthreads)
 {
     if (check_dims(B, Hq, Hkv, D, Dv) || !cu_q || !cu_k) return 1;
+    if (mask < 0 || mask > 2 || (mask == 2 && window > 0)) return 1;
     if (cu_q[0] != 0 || cu_k[0] != 0) return 1;
     for (int b = 0; b < B; ++b)
         if (cu_q[b + 1] < cu_q[b] || cu_k[b + 1] < cu_k[b]) return 1;
@@ -190,7 +211,7 @@ int oracle_attn_packed(const float *q, const float *k, const float *v, double *o
             const int kh = h / G;
             oracle_row(q + r * D, k + ((long)cu_k[b] * Hkv + kh) * D,
                        v + ((long)cu_k[b] * Hkv + kh) * Dv, (long)Hkv * D,
-                       (long)Hkv * Dv, D, Dv, qi, Qb, Kb, window, scale, s,
+                       (long)Hkv * Dv, D, Dv, qi, Qb, Kb, window, mask, scale, s,
                        o + r * Dv, &lse[r]);
         }
         free(s);
@@ -203,11 +224,12 @@ int oracle_attn_packed(const float *q, const float *k, const float *v, double *o
 int oracle_attn_padded_rows(const float *q, const float *k, const float *v,
                             int B, int Hq, int Hkv, int Q, int K, int D, int Dv,
                             const int32_t *seqlens_q, const int32_t *seqlens_k,
-                            int window, double scale, const int32_t *rb,
+                            int window, int mask, double scale, const int32_t *rb,
                             const int32_t *rq, const int32_t *rh, long n,
                             double *o_rows, double *lse_rows, int nthreads)
 {
     if (check_dims(B, Hq, Hkv, D, Dv) || Q < 0 || K < 0) return 1;
+    if (mask < 0 || mask > 2 || (mask == 2 && window > 0)) return 1;
     for (long i = 0; i < n; ++i)
         if (rb[i] < 0 || rb[i] >= B || rq[i] < 0 || rq[i] >= Q || rh[i] < 0 ||
             rh[i] >= Hq)
@@ -242,7 +264,7 @@ int oracle_attn_padded_rows(const float *q, const float *k, const float *v,
             const int kh = h / G;
             oracle_row(q + r * D, k + ((long)b * K * Hkv + kh) * D,
                        v + ((long)b * K * Hkv + kh) * Dv, (long)Hkv * D,
-                       (long)Hkv * Dv, D, Dv, qi, Qb, Kb, window, scale, s, orow,
+                       (long)Hkv * Dv, D, Dv, qi, Qb, Kb, window, mask, scale, s, orow,
                        &lse_rows[i]);
         }
         free(s);
@@ -252,14 +274,12 @@ int oracle_attn_padded_rows(const float *q, const float *k, const float *v,
 
 /* Number of legal (query, key) pairs of one sequence, per head: the unit the
  * throughput figures count (FLOP = pairs * (2D + 2Dv) per head). */
-long long oracle_legal_pairs(int Qb, int Kb, int window)
+long long oracle_legal_pairs(int Qb, int Kb, int window, int mask)
 {
     long long n = 0;
     for (int q = 0; q < Qb; ++q) {
-        long diag = (long)q + Kb - Qb;
-        long lo = 0, hi = diag;
-        if (window > 0 && diag - window + 1 > lo) lo = diag - window + 1;
-        if (hi > (long)Kb - 1) hi = (long)Kb - 1;
+        long lo, hi;
+        legal_keys(q, Qb, Kb, window, mask, &lo, &hi);
         if (hi >= lo) n += hi - lo + 1;
     }
     return n;

@@ -52,16 +52,20 @@ def golden_files():
     return sorted(glob.glob(os.path.join(GOLDEN_DIR, "*.json")))
 
 
-def mask_matrix(Qb: int, Kb: int, window: int) -> np.ndarray:
+def mask_matrix(Qb: int, Kb: int, window: int, mask: int = 0) -> np.ndarray:
     """Legal-key mask built from numpy's triangle routines: np.tril keeps
-    j - i <= Kb - Qb (bottom-right causal), np.triu keeps the window."""
-    m = np.tril(np.ones((Qb, Kb), dtype=bool), k=Kb - Qb)
+    j - i <= Kb - Qb (bottom-right causal; j - i <= 0 for the top-left mask),
+    np.triu keeps the window; mask 2 keeps every key."""
+    if mask == 2:
+        return np.ones((Qb, Kb), dtype=bool)
+    off = Kb - Qb if mask == 0 else 0
+    m = np.tril(np.ones((Qb, Kb), dtype=bool), k=off)
     if window > 0:
-        m &= np.triu(np.ones((Qb, Kb), dtype=bool), k=Kb - Qb - window + 1)
+        m &= np.triu(np.ones((Qb, Kb), dtype=bool), k=off - window + 1)
     return m
 
 
-def sdpa_reference(q, k, v, Qb, Kb, Hq, Hkv, window, scale):
+def sdpa_reference(q, k, v, Qb, Kb, Hq, Hkv, window, scale, mask=0):
     """fp64 torch SDPA with an explicit boolean mask for one sequence.
 
     q [Qb,Hq,D], k [Kb,Hkv,D], v [Kb,Hkv,Dv] float arrays.  Returns
@@ -72,7 +76,7 @@ def sdpa_reference(q, k, v, Qb, Kb, Hq, Hkv, window, scale):
     qt = torch.from_numpy(np.asarray(q, np.float64)).permute(1, 0, 2)       # [Hq,Qb,D]
     kt = torch.from_numpy(np.asarray(k, np.float64)).permute(1, 0, 2).repeat_interleave(G, 0)
     vt = torch.from_numpy(np.asarray(v, np.float64)).permute(1, 0, 2).repeat_interleave(G, 0)
-    m = mask_matrix(Qb, Kb, window)
+    m = mask_matrix(Qb, Kb, window, mask)
     has = m.any(axis=1)
     mt = torch.from_numpy(m)
     safe = mt.clone()
@@ -299,12 +303,71 @@ def pin_rows_match_full(ol):
 def pin_legal_pairs(ol):
     for (Qb, Kb, w) in [(4096, 4096, 0), (1, 8192, 0), (512, 4000, 1024), (3, 1, 0),
                         (0, 5, 0), (7, 0, 0), (10, 20, 3), (64, 128, 0)]:
-        n = int(mask_matrix(Qb, Kb, w).sum()) if Qb * Kb <= 4096 * 4096 else None
-        got = ol.legal_pairs(Qb, Kb, w)
-        if n is not None:
-            assert got == n, ("pairs", Qb, Kb, w, got, n)
+        for mask in (0, 1, 2):
+            ww = 0 if mask == 2 else w
+            n = int(mask_matrix(Qb, Kb, ww, mask).sum())
+            got = ol.legal_pairs(Qb, Kb, ww, mask)
+            assert got == n, ("pairs", Qb, Kb, ww, mask, got, n)
     assert ol.legal_pairs(4096, 4096, 0) == 4096 * 4097 // 2
+    # closed forms of the two extension masks
+    assert ol.legal_pairs(300, 700, 0, 2) == 300 * 700
+    assert ol.legal_pairs(700, 300, 0, 1) == 300 * 301 // 2 + 400 * 300
+
+
+# (B, Hq, Hkv, Q, K, D, Dv, window, seqlens_q, seqlens_k, mask) for the two
+# masks beyond the pages' bottom-right rule
+MASK_CASES = [
+    (1, 4, 2, 16, 37, 8, 8, 0, None, None, 1),        # top-left, Q < K
+    (2, 4, 1, 30, 12, 8, 6, 0, None, None, 1),        # top-left, Q > K
+    (1, 6, 3, 20, 25, 5, 7, 4, None, None, 1),        # top-left + window
+    (3, 4, 2, 12, 16, 8, 6, 0, [12, 5, 0], [16, 3, 9], 1),
+    (1, 4, 2, 16, 37, 8, 8, 0, None, None, 2),        # no mask
+    (2, 8, 2, 1, 53, 16, 12, 0, None, None, 2),       # no mask, decode
+    (3, 4, 2, 12, 16, 8, 6, 0, [12, 5, 3], [16, 0, 9], 2),
+]
+
+
+def pin_sdpa_masks(ol):
+    for ci, (B, Hq, Hkv, Q, K, D, Dv, w, sq, sk, mask) in enumerate(MASK_CASES):
+        q, k, v = rng_inputs(300 + ci, B, Hq, Hkv, Q, K, D, Dv)
+        scale = 1.0 / math.sqrt(D) * (1.0 + 0.25 * ci)
+        o, lse = ol.attn_padded(q, k, v, B=B, Hq=Hq, Hkv=Hkv, Q=Q, K=K, D=D, Dv=Dv,
+                                seqlens_q=sq, seqlens_k=sk, window=w, scale=scale, mask=mask)
+        for b in range(B):
+            Qb = Q if sq is None else sq[b]
+            Kb = K if sk is None else sk[b]
+            assert np.all(o[b, Qb:] == 0.0) and np.all(lse[b, Qb:] == -math.inf), (ci, b)
+            if Qb == 0:
+                continue
+            if Kb == 0:
+                assert np.all(o[b, :Qb] == 0.0) and np.all(lse[b, :Qb] == -math.inf), (ci, b)
+                continue
+            ro, rl, has = sdpa_reference(q[b, :Qb], k[b, :Kb], v[b, :Kb], Qb, Kb, Hq, Hkv, w,
+                                         scale, mask)
+            assert np.allclose(o[b, :Qb][has], ro[has], atol=1e-12, rtol=1e-10), (ci, b)
+            assert np.allclose(lse[b, :Qb][has], rl[has], atol=1e-12, rtol=1e-12), (ci, b)
+            assert np.all(o[b, :Qb][~has] == 0.0), (ci, b)
+            assert np.all(lse[b, :Qb][~has] == -math.inf), (ci, b)
+    # relations between the masks: with Q = K the two causal masks agree; a
+    # causal row that sees every key is the unmasked row
+    B, Hq, Hkv, Q, K, D, Dv = 2, 4, 2, 9, 9, 8, 8
+    q, k, v = rng_inputs(400, B, Hq, Hkv, Q, K, D, Dv)
+    kw = dict(B=B, Hq=Hq, Hkv=Hkv, Q=Q, K=K, D=D, Dv=Dv)
+    o0, l0 = ol.attn_padded(q, k, v, mask=0, **kw)
+    o1, l1 = ol.attn_padded(q, k, v, mask=1, **kw)
+    o2, l2 = ol.attn_padded(q, k, v, mask=2, **kw)
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1), "Q = K: causal masks differ"
+    assert np.array_equal(o0[:, -1], o2[:, -1]) and np.array_equal(l0[:, -1], l2[:, -1]), \
+        "last causal row != unmasked row"
+    assert not np.allclose(o0[:, 0], o2[:, 0]), "unmasked first row sees only key 0"
+    # a window is rejected without a causal mask
+    try:
+        ol.attn_padded(q, k, v, mask=2, window=3, **kw)
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("window accepted with no mask")
 
 
 ALL_PINS = [pin_golden, pin_sdpa, pin_invariants, pin_packed_matches_padded,
-            pin_rows_match_full, pin_legal_pairs]
+            pin_rows_match_full, pin_legal_pairs, pin_sdpa_masks]

@@ -31,7 +31,10 @@ def _bits(t):
     return t.view(torch.int32 if t.element_size() == 4 else torch.int16)
 
 
-def run_gpu(inp: synth.Inputs, algo="auto", device="cuda"):
+MASK_NAMES = {0: "causal", 1: "causal_top_left", 2: "none"}
+
+
+def run_gpu(inp: synth.Inputs, algo="auto", device="cuda", mask=0):
     """Run the library on ``inp``.  Outputs start as NaN canaries and are
     followed by guard regions; both are checked.  Returns numpy (o, lse)."""
     q = inp.q.to(device)
@@ -51,12 +54,12 @@ def run_gpu(inp: synth.Inputs, algo="auto", device="cuda"):
         sq = None if inp.seqlens_q is None else torch.from_numpy(inp.seqlens_q).to(device)
         sk = None if inp.seqlens_k is None else torch.from_numpy(inp.seqlens_k).to(device)
         attn_fwd(q, k, v, o, lse, seqlens_q=sq, seqlens_k=sk, window=inp.window,
-                 scale=inp.scale, algo=algo)
+                 scale=inp.scale, algo=algo, mask=MASK_NAMES[mask])
     else:
         cq = torch.from_numpy(inp.cu_seqlens_q).to(device)
         ck = torch.from_numpy(inp.cu_seqlens_k).to(device)
         attn_fwd_varlen(q, k, v, cq, ck, inp.Q, inp.K, o, lse, window=inp.window,
-                        scale=inp.scale, algo=algo)
+                        scale=inp.scale, algo=algo, mask=MASK_NAMES[mask])
     torch.cuda.synchronize()
     assert torch.isnan(obuf[-GUARD:].float()).all(), "write past the end of o"
     assert torch.isnan(lbuf[-GUARD:]).all(), "write past the end of lse"
@@ -65,7 +68,7 @@ def run_gpu(inp: synth.Inputs, algo="auto", device="cuda"):
     return o.float().cpu().numpy(), lse.cpu().numpy()
 
 
-def run_oracle(inp: synth.Inputs, nthreads=0):
+def run_oracle(inp: synth.Inputs, nthreads=0, mask=0):
     q = synth.exact_f32(inp.q)
     k = synth.exact_f32(inp.k)
     v = synth.exact_f32(inp.v)
@@ -73,10 +76,11 @@ def run_oracle(inp: synth.Inputs, nthreads=0):
         return oracle.attn_padded(q, k, v, B=inp.B, Hq=inp.Hq, Hkv=inp.Hkv, Q=inp.Q, K=inp.K,
                                   D=inp.D, Dv=inp.Dv, seqlens_q=inp.seqlens_q,
                                   seqlens_k=inp.seqlens_k, window=inp.window, scale=inp.scale,
-                                  nthreads=nthreads)
+                                  nthreads=nthreads, mask=mask)
     return oracle.attn_packed(q, k, v, B=inp.B, Hq=inp.Hq, Hkv=inp.Hkv, D=inp.D, Dv=inp.Dv,
                               cu_seqlens_q=inp.cu_seqlens_q, cu_seqlens_k=inp.cu_seqlens_k,
-                              window=inp.window, scale=inp.scale, nthreads=nthreads)
+                              window=inp.window, scale=inp.scale, nthreads=nthreads,
+                              mask=mask)
 
 
 def compare(dtype, o_gpu, lse_gpu, o_ref, lse_ref, what=""):
@@ -100,9 +104,9 @@ def compare(dtype, o_gpu, lse_gpu, o_ref, lse_ref, what=""):
     return eo, el
 
 
-def check(inp: synth.Inputs, algo="auto", what=""):
-    o, lse = run_gpu(inp, algo)
-    ro, rl = run_oracle(inp)
+def check(inp: synth.Inputs, algo="auto", what="", mask=0):
+    o, lse = run_gpu(inp, algo, mask=mask)
+    ro, rl = run_oracle(inp, mask=mask)
     return compare(inp.dtype, o, lse, ro, rl, what or algo)
 
 

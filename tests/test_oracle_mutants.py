@@ -11,12 +11,19 @@ from tests import oracle_pins as pins
 
 # (name, original text, mutated text)
 MUTANTS = [
-    ("causal_off_by_one", "const long diag = (long)q + Kb - Qb;",
-     "const long diag = (long)q + Kb - Qb - 1;"),
-    ("top_left_causal", "const long diag = (long)q + Kb - Qb;", "const long diag = (long)q;"),
+    ("causal_off_by_one", "mask == 1 ? (long)q : (long)q + Kb - Qb;",
+     "mask == 1 ? (long)q : (long)q + Kb - Qb - 1;"),
+    ("top_left_causal", "mask == 1 ? (long)q : (long)q + Kb - Qb;",
+     "mask == 1 ? (long)q : (long)q;"),
+    ("top_left_off_by_one", "mask == 1 ? (long)q :", "mask == 1 ? (long)q + 1 :"),
+    ("top_left_is_bottom_right", "mask == 1 ? (long)q :", "mask == 1 ? (long)q + Kb - Qb :"),
+    ("no_mask_drops_last_key", "        *hi = (long)Kb - 1;\n        return;",
+     "        *hi = (long)Kb - 2;\n        return;"),
+    ("no_mask_is_causal", "    if (mask == 2) {                                   /* no mask: every key */",
+     "    if (mask == 3) {                                   /* no mask: every key */"),
     ("head_map_modulo", "const int kh = h / G;", "const int kh = h % Hkv;"),
-    ("window_one_wider", "diag - window + 1 > lo) lo = diag - window + 1;",
-     "diag - window > lo) lo = diag - window;"),
+    ("window_one_wider", "diag - window + 1 > *lo) *lo = diag - window + 1;",
+     "diag - window > *lo) *lo = diag - window;"),
     ("scale_dropped", "const double s = scale * acc;", "const double s = acc;"),
     ("lse_without_max", "*lse_out = m + log(l);", "*lse_out = log(l);"),
     ("lse_base2", "*lse_out = m + log(l);", "*lse_out = m + log2(l);"),

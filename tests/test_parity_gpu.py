@@ -295,3 +295,48 @@ def test_tcgen05_full_size_varlen():
     every row against the oracle."""
     inp = synth.varlen_bf16_16seq_h16x4_k4096_q512_w1024()
     parity.check(inp, "auto", "varlen full size")
+
+
+# ---------------------------------------------------------------------------
+# the two masks beyond the pages' bottom-right rule: top-left causal, none
+
+MASK_SHAPES = [
+    # algo, dtype, B, Hq, Hkv, Q, K, D, Dv, window
+    ("generic", "f32", 2, 4, 2, 70, 150, 64, 48, 0),
+    ("generic", "f32", 1, 8, 2, 130, 60, 32, 32, 9),    # Q > K
+    ("tcgen05", "bf16", 2, 8, 2, 300, 500, 128, 128, 0),
+    ("tcgen05", "f16", 1, 8, 2, 500, 300, 64, 64, 0),   # Q > K
+    ("tcgen05", "bf16", 1, 8, 4, 257, 400, 128, 64, 100),
+    ("decode", "bf16", 8, 32, 8, 1, 1500, 128, 128, 0),
+    ("decode", "bf16", 4, 16, 4, 4, 900, 64, 64, 0),    # Q*G = 16
+]
+
+
+@pytest.mark.parametrize("mask", [1, 2], ids=["top_left", "none"])
+@pytest.mark.parametrize("case", MASK_SHAPES, ids=lambda c: f"{c[0]}-{c[1]}-" + "x".join(map(str, c[2:])))
+def test_masks(case, mask):
+    algo, dtype, B, Hq, Hkv, Q, K, D, Dv, window = case
+    if mask == 2:
+        window = 0
+    g = np.random.default_rng(B * 31 + K + mask)
+    sk = g.integers(0, K + 1, size=B).astype(np.int32)
+    sk[0] = K
+    inp = synth.make_padded(B, Hq, Hkv, Q, K, D, Dv, dtype, seed=51, seqlens_k=sk,
+                            window=window, pad_value=NAN)
+    parity.check(inp, algo, f"mask {mask} {case}", mask=mask)
+
+
+@pytest.mark.parametrize("mask", [1, 2], ids=["top_left", "none"])
+def test_masks_varlen_packed(mask):
+    sk = np.array([0, 5, 33, 130, 1, 640, 0, 300, 1000], np.int32)
+    sq = np.minimum(sk + 20, np.array([0, 5, 7, 64, 1, 512, 0, 100, 512]) + 20)
+    inp = synth.make_packed(sq, sk, 16, 4, 128, 128, "bf16", seed=52)
+    for algo in ("tcgen05", "generic"):
+        parity.check(inp, algo, f"mask {mask} varlen {algo}", mask=mask)
+
+
+def test_mask_none_rejects_window():
+    inp = synth.make_padded(1, 4, 2, 8, 8, 64, 64, "bf16", seed=53)
+    with pytest.raises(AttnError) as ei:
+        attn_fwd(inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), window=3, mask="none")
+    assert ei.value.status == 1
