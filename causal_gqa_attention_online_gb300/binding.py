@@ -24,7 +24,7 @@ MASKS = {"causal": 0, "causal_top_left": 1, "none": 2}
 _DTYPE_CODE = {torch.float32: ATTN_F32, torch.float16: ATTN_F16, torch.bfloat16: ATTN_BF16}
 
 EXPORTED = ("attn_fwd", "attn_fwd_varlen", "attn_fwd_algo", "attn_fwd_varlen_algo",
-            "attn_fwd_ex", "attn_fwd_varlen_ex",
+            "attn_fwd_ex", "attn_fwd_varlen_ex", "attn_fwd_paged",
             "attn_lse_combine", "attn_fwd_decode_noalloc", "attn_fwd_staged", "attn_last_error",
             "attn_device_status", "attn_kernel_launches", "attn_version")
 
@@ -66,6 +66,9 @@ def load_library(path: str | None = None):
         lib.attn_fwd_ex.argtypes = common[:-1] + [ip, ip, ip, vp]
         lib.attn_fwd_varlen_ex.argtypes = varlen[:-1] + [ip, ip, ip, vp]
         lib.attn_fwd_ex.restype = ip
+        lib.attn_fwd_paged.argtypes = [vp] * 5 + [ip] * 6 + [vp, ip, ip, ip, vp, vp, ip, fp, ip,
+                                                             ip, ip, vp]
+        lib.attn_fwd_paged.restype = ip
         lib.attn_fwd_varlen_ex.restype = ip
         lib.attn_fwd_decode_noalloc.argtypes = common + [vp]
         lib.attn_fwd_decode_noalloc.restype = ip
@@ -296,3 +299,39 @@ def attn_fwd_staged(hq, hk, hv, q, k, v, o, lse=None, ho=None, hlse=None, *, seq
                              ctypes.byref(bin_), ctypes.byref(bout), _stream_ptr(st))
     _check(rc)
     return ho, hlse, bin_.value, bout.value
+
+
+def attn_fwd_paged(q, k_pages, v_pages, block_table, seqlens_k, o=None, lse=None, *,
+                   seqlens_q=None, window=0, scale=None, algo="auto", mask="causal",
+                   stream=None, want_lse=True):
+    """Paged K/V: q [B,Q,Hq,D]; k_pages [P,page,Hkv,D], v_pages [P,page,Hkv,Dv];
+    block_table int32 [B,max_pages] (key j of sequence b: row j % page of page
+    block_table[b, j // page]); seqlens_k int32 [B].  All CUDA tensors.
+    Returns (o [B,Q,Hq,Dv], lse [B,Q,Hq] or None)."""
+    lib = load_library()
+    B, Q, Hq, D = q.shape
+    P, page, Hkv = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
+    Dv = v_pages.shape[3]
+    max_pages = block_table.shape[1]
+    dev = q.device
+    if o is None:
+        o = torch.empty((B, Q, Hq, Dv), dtype=q.dtype, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Q, Hq), dtype=torch.float32, device=dev)
+    for name, t, n in (("q", q, B * Q * Hq * D), ("k_pages", k_pages, P * page * Hkv * D),
+                       ("v_pages", v_pages, P * page * Hkv * Dv), ("o", o, B * Q * Hq * Dv)):
+        _check_tensor(name, t, q.dtype, n, dev)
+    if lse is not None:
+        _check_tensor("lse", lse, torch.float32, B * Q * Hq, dev)
+    _check_tensor("block_table", block_table, torch.int32, B * max_pages, dev)
+    _check_tensor("seqlens_k", seqlens_k, torch.int32, B, dev)
+    if seqlens_q is not None:
+        _check_tensor("seqlens_q", seqlens_q, torch.int32, B, dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = lib.attn_fwd_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(o), _ptr(lse), B, Hq, Hkv,
+                            Q, D, Dv, _ptr(block_table), max_pages, page, P, _ptr(seqlens_q),
+                            _ptr(seqlens_k), int(window), float(scale), MASKS[mask],
+                            _DTYPE_CODE[q.dtype], ALGOS[algo], _stream_ptr(stream))
+    _check(rc)
+    return o, lse

@@ -229,7 +229,9 @@ int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
                int Hkv, long long Tq, long long Tk, int Q, int K, int D, int Dv,
                const int32_t *seqlens_q,
                const int32_t *seqlens_k, const int32_t *cu_q, const int32_t *cu_k, int window,
-               float scale, int mask, int dtype, int algo, cudaStream_t stream) {
+               float scale, int mask, int dtype, int algo, cudaStream_t stream,
+               const int32_t *block_table = nullptr, int page_size = 0, int num_pages = 0,
+               int max_pages = 0) {
     g_last_error[0] = '\0';
     int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Q, K, D, Dv, dtype, algo);
     if (rc) return rc;
@@ -267,6 +269,12 @@ int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
     // (this also keeps the kernels' window arithmetic far from overflow).
     p.window = (window <= 0 || window >= K) ? 0 : window;
     p.mask = mask;
+    p.block_table = block_table;
+    p.page_size = page_size;
+    p.page_shift = 0;
+    while (page_size > 0 && (1 << p.page_shift) < page_size) ++p.page_shift;
+    p.num_pages = num_pages;
+    p.max_pages = max_pages;
     p.scale = scale;
     p.scale_log2 = scale * kLog2e;
     p.nsplit = 1;
@@ -288,6 +296,35 @@ int attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse
     return fwd_common(q, k, v, o, lse, B, Hq, Hkv, (long long)B * Q, (long long)B * K, Q, K, D, Dv,
                       seqlens_q, seqlens_k, nullptr, nullptr, window, scale, mask, dtype, algo,
                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_fwd_paged(const void *q, const void *k_pages, const void *v_pages, void *o, float *lse,
+                   int B, int Hq, int Hkv, int Q, int D, int Dv, const int32_t *block_table,
+                   int max_pages, int page_size, int num_pages, const int32_t *seqlens_q,
+                   const int32_t *seqlens_k, int window, float scale, int mask, int dtype,
+                   int algo, attn_stream_t stream) {
+    attn::g_last_error[0] = '\0';
+    if (page_size < 1 || page_size > (1 << 20) || (page_size & (page_size - 1)) != 0) {
+        set_error("page_size must be a power of two in [1, 2^20] (got %d)", page_size);
+        return ATTN_ERR_INVALID;
+    }
+    if (num_pages < 1 || max_pages < 0 ||
+        (long long)num_pages * page_size >= (1LL << 31) ||
+        (long long)max_pages * page_size >= (1LL << 31)) {
+        set_error("bad page counts (num_pages=%d max_pages=%d page_size=%d)", num_pages,
+                  max_pages, page_size);
+        return ATTN_ERR_INVALID;
+    }
+    if (B > 0 && (block_table == nullptr || seqlens_k == nullptr)) {
+        set_error("paged K/V needs block_table and seqlens_k");
+        return ATTN_ERR_INVALID;
+    }
+    const int K = max_pages * page_size;  // key capacity of a sequence
+    return fwd_common(q, k_pages, v_pages, o, lse, B, Hq, Hkv, (long long)B * Q,
+                      (long long)num_pages * page_size, Q, K, D, Dv, seqlens_q, seqlens_k, nullptr,
+                      nullptr, window, scale, mask, dtype, algo,
+                      reinterpret_cast<cudaStream_t>(stream), block_table, page_size, num_pages,
+                      max_pages);
 }
 
 int attn_fwd_algo(const void *q, const void *k, const void *v, void *o, float *lse, int B,

@@ -38,6 +38,11 @@ struct AttnParams {
     const int32_t *seqlens_k;  // padded layout, may be null
     const int32_t *cu_q;       // packed layout
     const int32_t *cu_k;       // packed layout
+    // paged K/V (block_table != null): k and v are pools of pages of
+    // page_size (a power of two) rows, [num_pages * page_size][Hkv][D or Dv];
+    // sequence b's key j lives in page block_table[b * max_pages + j / page_size]
+    const int32_t *block_table;
+    int page_size, page_shift, max_pages, num_pages;
     int window;              // <= 0: off
     int mask;                // attn_mask: 0 bottom-right causal, 1 top-left causal, 2 none
     float scale;             // multiplies Q.K
@@ -77,6 +82,16 @@ __device__ __forceinline__ SeqInfo seq_info(const AttnParams &p, int b) {
         s.Kb = p.seqlens_k ? clamp_len(__ldg(p.seqlens_k + b), p.K) : p.K;
     }
     return s;
+}
+
+// Row of key `key` of sequence b in the k / v buffers.  Page numbers outside
+// [0, num_pages) are clamped, so a bad table gives wrong keys, never a bad address.
+__device__ __forceinline__ long long kv_row(const AttnParams &p, const SeqInfo &si, int b,
+                                            int key) {
+    if (p.block_table == nullptr) return si.k_off + key;
+    int pg = __ldg(p.block_table + (long long)b * p.max_pages + (key >> p.page_shift));
+    pg = min(max(pg, 0), p.num_pages - 1);
+    return ((long long)pg << p.page_shift) + (key & (p.page_size - 1));
 }
 
 // Legal keys of query row qi: [lo, hi) (empty when hi <= lo).  Causal masks

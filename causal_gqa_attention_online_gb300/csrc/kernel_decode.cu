@@ -108,7 +108,9 @@ __device__ __forceinline__ int swz(int r, int c, int row_bytes) {
     return r * row_bytes + ((c ^ (r & 7)) << 4);
 }
 
-template <typename T, int D, int DV, int NT>
+// PAGED: K / V rows found through the block table (a separate instance, so
+// that the contiguous layout's load loop carries no paging code).
+template <typename T, int D, int DV, int NT, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p) {
     constexpr int R = NT * 8;               // query rows of a (sequence, KV head)
     constexpr int KROW = D * 2, VROW = DV * 2;
@@ -193,14 +195,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p)
         for (int i = tid; i < kTK * CK; i += kThreads) {
             const int row = i / CK, c = i % CK, key = key0 + row;
             const bool ok = key < kend;
-            const T *src = ok ? kg + ((si.k_off + key) * p.Hkv + kvh) * (long long)D + c * 8 : kg;
+            const long long kr = PAGED ? kv_row(p, si, b, key) : si.k_off + key;
+            const T *src = ok ? kg + (kr * p.Hkv + kvh) * (long long)D + c * 8 : kg;
             cp_async16(st + swz(row, c, KROW), src, ok ? 16 : 0);
         }
 #pragma unroll
         for (int i = tid; i < kTK * CV; i += kThreads) {
             const int row = i / CV, c = i % CV, key = key0 + row;
             const bool ok = key < kend;
-            const T *src = ok ? vg + ((si.k_off + key) * p.Hkv + kvh) * (long long)DV + c * 8 : vg;
+            const long long kr = PAGED ? kv_row(p, si, b, key) : si.k_off + key;
+            const T *src = ok ? vg + (kr * p.Hkv + kvh) * (long long)DV + c * 8 : vg;
             cp_async16(st + KTILE + swz(row, c, VROW), src, ok ? 16 : 0);
         }
     };
@@ -366,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p)
 template <typename T, int D, int DV, int NT>
 int launch_decode_t(const AttnParams &p, cudaStream_t stream) {
     constexpr int smem = kStages * kTK * (D + DV) * 2;
-    auto kern = decode_kernel<T, D, DV, NT>;
+    auto kern = p.block_table ? decode_kernel<T, D, DV, NT, true> : decode_kernel<T, D, DV, NT, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) {
         set_error("decode kernel: cudaFuncSetAttribute: %s", cudaGetErrorString(e));

@@ -97,12 +97,12 @@ __global__ void __launch_bounds__(128) generic_fwd_kernel(const AttnParams p) {
         for (int i = tid; i < kTK * D; i += blockDim.x) {
             const int j = i / D, d = i % D, key = t0 + j;
             ks[j * Dp + d] = key < key_hi
-                ? to_f32(kg[((si.k_off + key) * p.Hkv + kvh) * (long long)D + d]) : 0.f;
+                ? to_f32(kg[(kv_row(p, si, b, key) * p.Hkv + kvh) * (long long)D + d]) : 0.f;
         }
         for (int i = tid; i < kTK * Dv; i += blockDim.x) {
             const int j = i / Dv, c = i % Dv, key = t0 + j;
             vs[i] = key < key_hi
-                ? to_f32(vg[((si.k_off + key) * p.Hkv + kvh) * (long long)Dv + c]) : 0.f;
+                ? to_f32(vg[(kv_row(p, si, b, key) * p.Hkv + kvh) * (long long)Dv + c]) : 0.f;
         }
         __syncthreads();
 #pragma unroll

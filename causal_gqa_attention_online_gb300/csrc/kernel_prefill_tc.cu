@@ -147,6 +147,7 @@ struct UnitInfo {
     bool all_valid;      // every row of both tiles holds a real query
 };
 
+template <bool PAGED>
 __device__ __forceinline__ UnitInfo unit_info(const PrefillArgs &a, long long u64) {
     const AttnParams &p = a.p;
     // 32-bit index arithmetic (the unit count is below 2^31)
@@ -173,9 +174,11 @@ __device__ __forceinline__ UnitInfo unit_info(const PrefillArgs &a, long long u6
     legal_range(x.q0, x.si.Qb, x.si.Kb, p.window, p.mask, lo_f, hi_f);
     legal_range(q_last, x.si.Qb, x.si.Kb, p.window, p.mask, lo_l, hi_l);
     if (hi_l <= lo_f) return x;
-    x.kv_start = lo_f;
+    // paged K/V: tiles start on 128-key boundaries, so that each lies in one
+    // page (the keys before lo_f are masked)
+    x.kv_start = PAGED ? (lo_f & ~(kBN - 1)) : lo_f;
     x.hi_unit = hi_l;
-    x.n_kv = (hi_l - lo_f + kBN - 1) / kBN;
+    x.n_kv = (hi_l - x.kv_start + kBN - 1) / kBN;
     x.lo_last = lo_l;
     x.hi_first = hi_f;
     x.all_valid = x.q0 + 2 * a.QP <= x.si.Qb;
@@ -245,7 +248,8 @@ __device__ __forceinline__ void raise_abort(volatile int *abort_flag, int *statu
 
 // D, DV: the tile widths (64 or 128 columns); the real head dims p.D <= D and
 // p.Dv <= DV are multiples of 16, the rest of the tile columns zero-filled.
-template <typename T, int D, int DV>
+// PAGED: K / V tiles found through the block table (a separate instance).
+template <typename T, int D, int DV, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
@@ -327,11 +331,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (long long rnd = 0; rnd * gridDim.x < a.nunits && ok; ++rnd) {
                     const long long u = snake_unit(rnd, blockIdx.x, gridDim.x);
                     if (u >= a.nunits) continue;
-                    const UnitInfo x = unit_info(a, u);
+                    const UnitInfo x = unit_info<PAGED>(a, u);
                     if (x.n_kv == 0) continue;
                     const int qrow = (padded ? 0 : (int)x.si.q_off) + x.q0;
                     const int krow = padded ? 0 : (int)x.si.k_off;
                     const int bc = padded ? x.b : 0;
+                    // K/V tile coordinates: (row, batch) of key k0 of the unit's sequence
+                    const int kbc = PAGED ? 0 : bc;
+                    auto kv_coord = [&](int k0) -> int {
+                        return PAGED ? (int)kv_row(p, x.si, x.b, k0) : krow + k0;
+                    };
                     if (!mbar_wait(bar(B_Q_EMPTY), q_ph ^ 1u, abort_flag, kWaitLimitNs)) {
                         raise_abort(abort_flag, p.status, kStatusTimeoutQ);
                         ok = false;
@@ -351,15 +360,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // L2 prefetch: the first K/V tiles of this unit and the next unit's Q
                     auto prefetch_kv = [&](int jj) {
                         const int kk0 = x.kv_start + jj * kBN;
+                        const int kr = kv_coord(kk0);
                         for (int c = 0; c < D / 64; ++c)
-                            tma_prefetch_l2_4d(&tmK, c * 64, x.kvh, krow + kk0, bc);
+                            tma_prefetch_l2_4d(&tmK, c * 64, x.kvh, kr, kbc);
                         for (int c = 0; c < DV / 64; ++c)
-                            tma_prefetch_l2_4d(&tmV, c * 64, x.kvh, krow + kk0, bc);
+                            tma_prefetch_l2_4d(&tmV, c * 64, x.kvh, kr, kbc);
                     };
                     for (int jj = 1; jj < kPrefetchTiles && jj < x.n_kv; ++jj) prefetch_kv(jj);
                     const long long un = snake_unit(rnd + 1, blockIdx.x, gridDim.x);
                     if (un < a.nunits) {
-                        const UnitInfo nx = unit_info(a, un);
+                        const UnitInfo nx = unit_info<PAGED>(a, un);
                         if (nx.n_kv > 0) {
                             const int nq = (padded ? 0 : (int)nx.si.q_off) + nx.q0;
                             const int nbc = padded ? nx.b : 0;
@@ -369,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     for (int j = 0; j < x.n_kv && ok; ++j) {
-                        const int k0 = x.kv_start + j * kBN;
+                        const int kr = kv_coord(x.kv_start + j * kBN);
                         if (j + kPrefetchTiles < x.n_kv) prefetch_kv(j + kPrefetchTiles);
 #pragma unroll
                         for (int which = 0; which < 2; ++which) {
@@ -385,12 +395,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 mbar_arrive_expect_tx(kv_full(s), L::KTILE);
                                 for (int c = 0; c < D / 64; ++c)
                                     tma_load_4d(stage(s) + c * kChunkBytes, &tmK, kv_full(s), c * 64,
-                                                x.kvh, krow + k0, bc);
+                                                x.kvh, kr, kbc);
                             } else {
                                 mbar_arrive_expect_tx(kv_full(s), L::VTILE);
                                 for (int c = 0; c < DV / 64; ++c)
                                     tma_load_4d(stage(s) + c * kChunkBytes, &tmV, kv_full(s), c * 64,
-                                                x.kvh, krow + k0, bc);
+                                                x.kvh, kr, kbc);
                             }
                             armed |= 1u << s;
                             armed_parity = (armed_parity & ~(1u << s)) | (ph << s);
@@ -570,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (long long rnd = 0; rnd * gridDim.x < a.nunits && ok; ++rnd) {
             const long long u = snake_unit(rnd, blockIdx.x, gridDim.x);
             if (u >= a.nunits) continue;
-            const UnitInfo x = unit_info(a, u);
+            const UnitInfo x = unit_info<PAGED>(a, u);
             const int qpos = x.q0 + t * a.QP + r / a.Gp;
             const int head = x.h0 + r % a.Gp;
             const bool valid = qpos < x.si.Qb;
@@ -754,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (long long rnd = 0; rnd * gridDim.x < a.nunits && ok; ++rnd) {
             const long long u = snake_unit(rnd, blockIdx.x, gridDim.x);
             if (u >= a.nunits) continue;
-            const UnitInfo x = unit_info(a, u);
+            const UnitInfo x = unit_info<PAGED>(a, u);
             if (x.n_kv == 0) continue;  // the softmax warpgroups wrote those rows
             const int b = (int)(nunit & 1u);
             ++nunit;
@@ -906,8 +916,10 @@ int launch_t(const AttnParams &p, bool bf16, cudaStream_t stream) {
         bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const bool padded = p.cu_q == nullptr;
     const uint64_t qrows = padded ? (uint64_t)p.Q : (uint64_t)p.Tq;
-    const uint64_t krows = padded ? (uint64_t)p.K : (uint64_t)p.Tk;
+    const bool paged = p.block_table != nullptr;
+    const uint64_t krows = (padded && !paged) ? (uint64_t)p.K : (uint64_t)p.Tk;
     const uint64_t nb = padded ? (uint64_t)p.B : 1;
+    const uint64_t nbk = (padded && !paged) ? (uint64_t)p.B : 1;
     CUtensorMap tq, tk, tv, to;
     // maps over the real head dims: the columns up to the padded D / DV of the
     // tiles are zero-filled by the loads (so they add nothing to S or O) and
@@ -917,15 +929,15 @@ int launch_t(const AttnParams &p, bool bf16, cudaStream_t stream) {
     rc = make_map(&to, p.o, dt, (uint64_t)p.Dv, p.Hq, qrows, nb, a.Gp, a.QP);
     if (rc) return rc;
     if (krows > 0) {
-        rc = make_map(&tk, p.k, dt, (uint64_t)p.D, p.Hkv, krows, nb, 1, kBN);
+        rc = make_map(&tk, p.k, dt, (uint64_t)p.D, p.Hkv, krows, nbk, 1, kBN);
         if (rc) return rc;
-        rc = make_map(&tv, p.v, dt, (uint64_t)p.Dv, p.Hkv, krows, nb, 1, kBN);
+        rc = make_map(&tv, p.v, dt, (uint64_t)p.Dv, p.Hkv, krows, nbk, 1, kBN);
         if (rc) return rc;
     } else {
         tk = tq;  // never read: every unit has no key
         tv = tq;
     }
-    auto kern = prefill_tc_kernel<T, D, DV>;
+    auto kern = paged ? prefill_tc_kernel<T, D, DV, true> : prefill_tc_kernel<T, D, DV, false>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
     if (e != cudaSuccess) {
@@ -964,7 +976,9 @@ bool prefill_tc_supported(const AttnParams &p, int dtype) {
     if (p.D < 64 || p.D > 128 || p.D % 16 || p.Dv < 64 || p.Dv > 128 || p.Dv % 16) return false;
     if (p.Q < 1) return false;
     const long long rows = p.cu_q ? p.Tq : (long long)p.Q;
-    const long long keys = p.cu_q ? p.Tk : (long long)p.K;
+    const long long keys = (p.cu_q || p.block_table) ? p.Tk : (long long)p.K;
+    // paged K/V: a 128-key tile must lie in one page
+    if (p.block_table && p.page_size % kBN != 0) return false;
     // work units are indexed in 32 bits
     const int gp = pack_factor(p.G), qp = kBM / gp;
     const long long nunits = (long long)((p.Q + 2 * qp - 1) / (2 * qp)) * p.B * p.Hkv * (p.G / gp);

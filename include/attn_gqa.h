@@ -177,6 +177,27 @@ ATTN_API int attn_lse_combine(const float *o_parts, const float *lse_parts, void
                      int nsplit, long long rows, int Dv, int dtype, attn_stream_t stream);
 
 /*
+ * attn_fwd_paged -- attn_fwd with the keys and values in pages: a serving
+ * layout (the pages have no counterpart; the attention itself is unchanged).
+ *   q [B, Q, Hq, D], o [B, Q, Hq, Dv], lse [B, Q, Hq] as in attn_fwd.
+ *   k_pages [num_pages, page_size, Hkv, D], v_pages [num_pages, page_size, Hkv, Dv]:
+ *               pools of pages of page_size key rows (a power of two).
+ *   block_table int32 [B, max_pages] on the device: key j of sequence b is row
+ *               j % page_size of page block_table[b][j / page_size].  Entries
+ *               outside [0, num_pages) are clamped into it.
+ *   seqlens_k   int32 [B] on the device (required), at most max_pages * page_size.
+ *   mask, algo  as in attn_fwd_ex.  The tcgen05 prefill takes page sizes that
+ *               are multiples of 128; the decode and fp32 kernels take any.
+ * Return codes as attn_fwd.
+ */
+ATTN_API int attn_fwd_paged(const void *q, const void *k_pages, const void *v_pages, void *o,
+                            float *lse, int B, int Hq, int Hkv, int Q, int D, int Dv,
+                            const int32_t *block_table, int max_pages, int page_size,
+                            int num_pages, const int32_t *seqlens_q, const int32_t *seqlens_k,
+                            int window, float scale, int mask, int dtype, int algo,
+                            attn_stream_t stream);
+
+/*
  * attn_fwd_decode_noalloc -- attn_fwd's split-KV decode for callers that may
  * not allocate device memory while attention runs: for example a serving
  * process whose device memory is owned by another runtime's allocator or held
