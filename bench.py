@@ -277,8 +277,26 @@ def measure_decode(args, world, rank, dev, stream, flush, attn, synth):
 
     e2e_times = time_steps(decode_e2e, max(3, args.steps // 2), 3, flush, stream)
     e2e_ms = max_over_ranks(sum(e2e_times) / len(e2e_times), world)
+
+    # the same decode with the K / V cache in shuffled 64-row pages (attn_fwd_paged)
+    page = 64
+    npg = Dd["K"] // page
+    perm = torch.randperm(Dd["B"] * npg, generator=torch.Generator().manual_seed(99 + rank))
+    table = perm.view(Dd["B"], npg).to(torch.int32).to(dev)
+    kpool = torch.empty((Dd["B"] * npg, page, Dd["Hkv"], Dd["D"]), dtype=dk.dtype, device=dev)
+    vpool = torch.empty((Dd["B"] * npg, page, Dd["Hkv"], Dd["Dv"]), dtype=dv.dtype, device=dev)
+    kpool[perm.to(dev)] = dk.view(Dd["B"] * npg, page, Dd["Hkv"], Dd["D"])
+    vpool[perm.to(dev)] = dv.view(Dd["B"] * npg, page, Dd["Hkv"], Dd["Dv"])
+
+    def decode_paged():
+        attn.attn_fwd_paged(dq, kpool, vpool, table, dsk, do, dl, stream=stream)
+
+    paged_times = time_steps(decode_paged, max(3, args.steps // 2), 3, flush, stream)
+    paged_ms = max_over_ranks(sum(paged_times) / len(paged_times), world)
+    del kpool, vpool
     return dict(kv_bytes=kv_bytes, ms=ms, launches=launches, clocks=clk.summary(),
-                e2e_ms=e2e_ms, h2d=moved[0] + dsk.numel() * 4, d2h=moved[1])
+                e2e_ms=e2e_ms, h2d=moved[0] + dsk.numel() * 4, d2h=moved[1],
+                paged_ms=paged_ms, page=page)
 
 
 def run_gpu(args, world, rank, local):
@@ -333,12 +351,15 @@ def run_gpu(args, world, rank, local):
             "e2e": {"value": round(world * d["kv_bytes"] / (d["e2e_ms"] * 1e-3) / 1e9, 2),
                     "unit": "GB/s", "ms_per_step": round(d["e2e_ms"], 4),
                     "h2d_bytes_per_step": d["h2d"], "d2h_bytes_per_step": d["d2h"]},
+            "paged": {"page_size": d["page"], "layout": "K/V in shuffled pages (attn_fwd_paged)",
+                      "value": round(world * d["kv_bytes"] / (d["paged_ms"] * 1e-3) / 1e9, 2),
+                      "unit": "GB/s", "ms_per_step": round(d["paged_ms"], 5)},
         }
         if args.only == "decode":
             result.update({"value": dec["value"], "unit": "GB/s", "ms_per_step": dec["ms_per_step"],
                            "config": {"workload": DECODE_NAME}, "roofline": dec["roofline"],
                            "e2e": dec["e2e"], "gpu_launches": dec["gpu_launches"],
-                           "clocks": dec["clocks"]})
+                           "clocks": dec["clocks"], "paged": dec["paged"]})
         else:
             result["decode"] = dec
     return result, pin

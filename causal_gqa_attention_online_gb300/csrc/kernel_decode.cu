@@ -191,20 +191,27 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p)
         const int key0 = kbeg + t * kTK;
         const uint32_t st = sbase + (t % kStages) * STAGE;
         constexpr int CK = D / 8, CV = DV / 8;
+        // paged: a tile that starts on a 64-key boundary lies in one page when
+        // pages hold at least 64 rows (one table read); otherwise a read per
+        // row.  Only keys below kend are looked up.
+        long long tile_base = si.k_off + key0;
+        const bool one_page = !PAGED || (p.page_size >= kTK && (key0 & (kTK - 1)) == 0);
+        if (PAGED && one_page) tile_base = kv_row(p, si, b, key0);
+        auto row_of = [&](int key) -> long long {
+            return one_page ? tile_base + (key - key0) : kv_row(p, si, b, key);
+        };
 #pragma unroll
         for (int i = tid; i < kTK * CK; i += kThreads) {
             const int row = i / CK, c = i % CK, key = key0 + row;
             const bool ok = key < kend;
-            const long long kr = PAGED ? kv_row(p, si, b, key) : si.k_off + key;
-            const T *src = ok ? kg + (kr * p.Hkv + kvh) * (long long)D + c * 8 : kg;
+            const T *src = ok ? kg + (row_of(key) * p.Hkv + kvh) * (long long)D + c * 8 : kg;
             cp_async16(st + swz(row, c, KROW), src, ok ? 16 : 0);
         }
 #pragma unroll
         for (int i = tid; i < kTK * CV; i += kThreads) {
             const int row = i / CV, c = i % CV, key = key0 + row;
             const bool ok = key < kend;
-            const long long kr = PAGED ? kv_row(p, si, b, key) : si.k_off + key;
-            const T *src = ok ? vg + (kr * p.Hkv + kvh) * (long long)DV + c * 8 : vg;
+            const T *src = ok ? vg + (row_of(key) * p.Hkv + kvh) * (long long)DV + c * 8 : vg;
             cp_async16(st + KTILE + swz(row, c, VROW), src, ok ? 16 : 0);
         }
     };
