@@ -116,7 +116,7 @@ extern "C" int attn_fwd_decode_noalloc(const void *q, const void *k, const void 
     p.scale_log2 = scale * kLog2e;
     if (!decode_supported(p, dtype)) {
         set_error("attn_fwd_decode_noalloc: the decode kernel takes bf16/fp16, D and Dv in "
-                  "{64, 128} and Q * Hq / Hkv <= 16");
+                  "{64, 128} or both 256, and Q * Hq / Hkv <= 16");
         return ATTN_ERR_UNSUPPORTED;
     }
     int dev = 0;

@@ -403,6 +403,7 @@ int launch_decode_nt(const AttnParams &p, cudaStream_t stream) {
 template <typename T>
 int launch_decode_dims(const AttnParams &p, cudaStream_t stream) {
     if (p.D == 128 && p.Dv == 128) return launch_decode_nt<T, 128, 128>(p, stream);
+    if (p.D == 256 && p.Dv == 256) return launch_decode_nt<T, 256, 256>(p, stream);
     if (p.D == 64 && p.Dv == 64) return launch_decode_nt<T, 64, 64>(p, stream);
     if (p.D == 128 && p.Dv == 64) return launch_decode_nt<T, 128, 64>(p, stream);
     return launch_decode_nt<T, 64, 128>(p, stream);
@@ -412,7 +413,9 @@ int launch_decode_dims(const AttnParams &p, cudaStream_t stream) {
 
 bool decode_supported(const AttnParams &p, int dtype) {
     if (dtype != 1 && dtype != 2) return false;
-    if ((p.D != 64 && p.D != 128) || (p.Dv != 64 && p.Dv != 128)) return false;
+    // head dims 64 / 128 in any pair, or 256 / 256 (one block an SM: 192 KB of ring)
+    const bool small = (p.D == 64 || p.D == 128) && (p.Dv == 64 || p.Dv == 128);
+    if (!small && !(p.D == 256 && p.Dv == 256)) return false;
     if ((long long)p.Q * p.G > 16 || p.Q < 1) return false;
     return (long long)p.B * p.Hkv <= 65535;
 }

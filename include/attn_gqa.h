@@ -206,7 +206,7 @@ ATTN_API int attn_fwd_paged(const void *q, const void *k_pages, const void *v_pa
  * counterpart to this entry point; it is a deployment aid of this library.
  *
  * Same arguments, layout and result as attn_fwd, restricted to the shapes the
- * decode kernel takes (bf16/fp16, D and Dv in {64, 128}, Q * Hq / Hkv <= 16).
+ * decode kernel takes (bf16/fp16, D and Dv in {64, 128} or both 256, Q * Hq / Hkv <= 16).
  * The split-KV partials live in a fixed 32 MiB __device__ array that every
  * GPU using the library keeps until the process exits; the call makes no
  * allocation of any kind.  A problem whose partials would not fit returns

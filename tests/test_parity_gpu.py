@@ -147,6 +147,9 @@ DECODE_SHAPES = [
     (1, 16, 4, 4, 129, 128, 128),    # Q*G = 16
     (1, 8, 2, 1, 32768, 64, 64),     # long KV: many splits
     (1, 16, 4, 1, 8193, 128, 128),
+    # head dim 256 (one block an SM)
+    (4, 16, 4, 1, 1000, 256, 256),
+    (2, 16, 1, 1, 700, 256, 256),    # G = 16: two n-tiles
     # many (sequence, KV head) units, as in batched serving
     (40, 16, 1, 1, 333, 128, 64),
     (20, 8, 2, 2, 300, 128, 128),
