@@ -83,6 +83,9 @@ class OracleLib:
         lib.oracle_attn_padded_rows.argtypes = [f32p, f32p, f32p] + [ci] * 7 + [
             i32p, i32p, ci, ci, cd, i32p, i32p, i32p, cl, f64p, f64p, ci]
         lib.oracle_attn_padded_rows.restype = ci
+        lib.oracle_attn_bwd_padded.argtypes = [f32p, f32p, f32p, f32p, f64p, f64p, f64p] + [
+            ci] * 7 + [i32p, i32p, ci, ci, cd, ci]
+        lib.oracle_attn_bwd_padded.restype = ci
         lib.oracle_legal_pairs.argtypes = [ci, ci, ci, ci]
         lib.oracle_legal_pairs.restype = ctypes.c_longlong
         lib.oracle_max_threads.argtypes = []
@@ -166,6 +169,32 @@ class OracleLib:
             raise ValueError(f"oracle_attn_padded_rows failed with status {rc}")
         return o, lse
 
+    def attn_bwd_padded(self, q, k, v, dout, *, B, Hq, Hkv, Q, K, D, Dv, seqlens_q=None,
+                        seqlens_k=None, window=0, scale=None, mask=0, nthreads=0):
+        """Gradients (dq [B,Q,Hq,D], dk [B,K,Hkv,D], dv [B,K,Hkv,Dv], float64)
+        of the padded-layout attention for the output gradient ``dout``
+        [B,Q,Hq,Dv]; the forward is recomputed from its definition."""
+        if scale is None:
+            scale = 1.0 / np.sqrt(D)
+        q, qp = _f32(q)
+        k, kp = _f32(k)
+        v, vp = _f32(v)
+        g, gp = _f32(dout)
+        if (q.size != B * Q * Hq * D or k.size != B * K * Hkv * D or
+                v.size != B * K * Hkv * Dv or g.size != B * Q * Hq * Dv):
+            raise ValueError("oracle_attn_bwd_padded: array sizes do not match the dims")
+        sq, sqp = _i32(seqlens_q)
+        sk, skp = _i32(seqlens_k)
+        dq = np.empty((B, Q, Hq, D), np.float64)
+        dk = np.empty((B, K, Hkv, D), np.float64)
+        dv = np.empty((B, K, Hkv, Dv), np.float64)
+        rc = self.lib.oracle_attn_bwd_padded(qp, kp, vp, gp, _f64p(dq), _f64p(dk), _f64p(dv), B,
+                                             Hq, Hkv, Q, K, D, Dv, sqp, skp, int(window),
+                                             int(mask), float(scale), int(nthreads))
+        if rc != 0:
+            raise ValueError(f"oracle_attn_bwd_padded failed with status {rc}")
+        return dq, dk, dv
+
     def legal_pairs(self, Qb: int, Kb: int, window: int = 0, mask: int = 0) -> int:
         """Legal (query, key) pairs of one sequence and head, by enumeration."""
         return int(self.lib.oracle_legal_pairs(int(Qb), int(Kb), int(window), int(mask)))
@@ -192,6 +221,10 @@ def attn_packed(*args, **kw):
 
 def attn_padded_rows(*args, **kw):
     return _default().attn_padded_rows(*args, **kw)
+
+
+def attn_bwd_padded(*args, **kw):
+    return _default().attn_bwd_padded(*args, **kw)
 
 
 def legal_pairs(Qb: int, Kb: int, window: int = 0, mask: int = 0) -> int:

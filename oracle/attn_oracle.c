@@ -272,6 +272,96 @@ int oracle_attn_padded_rows(const float *q, const float *k, const float *v,
     return bad ? 3 : 0;
 }
 
+/* Gradients of the same attention (padded layout), for a loss whose gradient
+ * with respect to O is dO.  The pages give the forward only; the backward is
+ * the derivative of the definition above, written out per row (fp64):
+ *   P[q,k]  = exp(s_k - LSE[q]) for k in L(q), 0 otherwise (s, L, LSE as above)
+ *   Dq      = sum_j dO[q,j] * O[q,j]
+ *   dP[q,k] = sum_j dO[q,j] * V[k,j]
+ *   dS[q,k] = P[q,k] * (dP[q,k] - Dq)
+ *   dQ[q]   = scale * sum_k dS[q,k] * K[k]
+ *   dK[k]   = scale * sum over the rows q and the query heads h of KV head kh of dS[q,k] * Q[q]
+ *   dV[k]   = the same sum of P[q,k] * dO[q]
+ * O and LSE are recomputed here from the definition (nothing is taken from the
+ * device).  Rows without a legal key and padded rows contribute nothing and
+ * get dQ = 0; keys no row attends to get dK = dV = 0.
+ * dq [B,Q,Hq,D], dk [B,K,Hkv,D], dv [B,K,Hkv,Dv] are written in full. */
+int oracle_attn_bwd_padded(const float *q, const float *k, const float *v, const float *dout,
+                           double *dq, double *dk, double *dv, int B, int Hq, int Hkv, int Q,
+                           int K, int D, int Dv, const int32_t *seqlens_q,
+                           const int32_t *seqlens_k, int window, int mask, double scale,
+                           int nthreads)
+{
+    if (check_dims(B, Hq, Hkv, D, Dv) || Q < 0 || K < 0) return 1;
+    if (mask < 0 || mask > 2 || (mask == 2 && window > 0)) return 1;
+    const int G = Hq / Hkv;
+    memset(dq, 0, sizeof(double) * (size_t)B * Q * Hq * D);
+    memset(dk, 0, sizeof(double) * (size_t)B * K * Hkv * D);
+    memset(dv, 0, sizeof(double) * (size_t)B * K * Hkv * Dv);
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int bad = 0;
+    /* one (sequence, KV head) per task: it owns its dK / dV rows */
+#pragma omp parallel
+    {
+        const size_t kc = (size_t)(K > 0 ? K : 1);
+        double *s = (double *)malloc(sizeof(double) * kc);
+        double *orow = (double *)malloc(sizeof(double) * (size_t)Dv);
+        if (!s || !orow) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (long u = 0; u < (long)B * Hkv; ++u) {
+            if (!s || !orow) continue;
+            const int b = (int)(u / Hkv), kh = (int)(u % Hkv);
+            const int Qb = clamp_len(seqlens_q ? seqlens_q[b] : Q, Q);
+            const int Kb = clamp_len(seqlens_k ? seqlens_k[b] : K, K);
+            const float *kb = k + ((long)b * K * Hkv + kh) * D;      /* key row stride Hkv*D */
+            const float *vb = v + ((long)b * K * Hkv + kh) * Dv;
+            double *dkb = dk + ((long)b * K * Hkv + kh) * D;
+            double *dvb = dv + ((long)b * K * Hkv + kh) * Dv;
+            for (int h = kh * G; h < (kh + 1) * G; ++h)
+                for (int qi = 0; qi < Qb; ++qi) {
+                    const long r = ((long)b * Q + qi) * Hq + h;
+                    const float *qrow = q + r * D;
+                    const float *dorow = dout + r * Dv;
+                    double lse;
+                    oracle_row(qrow, kb, vb, (long)Hkv * D, (long)Hkv * Dv, D, Dv, qi, Qb, Kb,
+                               window, mask, scale, s, orow, &lse);
+                    if (lse == -INFINITY) continue;
+                    long lo, hi;
+                    legal_keys(qi, Qb, Kb, window, mask, &lo, &hi);
+                    double Dq = 0.0;
+                    for (int j = 0; j < Dv; ++j) Dq += (double)dorow[j] * orow[j];
+                    double *dqrow = dq + r * D;
+                    for (long kk = lo; kk <= hi; ++kk) {
+                        const float *krow = kb + kk * (long)Hkv * D;
+                        const float *vrow = vb + kk * (long)Hkv * Dv;
+                        double acc = 0.0;
+                        for (int d = 0; d < D; ++d) acc += (double)qrow[d] * (double)krow[d];
+                        const double p = exp(scale * acc - lse);
+                        double dp = 0.0;
+                        for (int j = 0; j < Dv; ++j) dp += (double)dorow[j] * (double)vrow[j];
+                        const double ds = p * (dp - Dq);
+                        for (int d = 0; d < D; ++d) {
+                            dqrow[d] += scale * ds * (double)krow[d];
+                            dkb[kk * (long)Hkv * D + d] += scale * ds * (double)qrow[d];
+                        }
+                        for (int j = 0; j < Dv; ++j)
+                            dvb[kk * (long)Hkv * Dv + j] += p * (double)dorow[j];
+                    }
+                }
+        }
+        free(s);
+        free(orow);
+    }
+    return bad ? 3 : 0;
+}
+
 /* Number of legal (query, key) pairs of one sequence, per head: the unit the
  * throughput figures count (FLOP = pairs * (2D + 2Dv) per head). */
 long long oracle_legal_pairs(int Qb, int Kb, int window, int mask)

@@ -369,5 +369,146 @@ def pin_sdpa_masks(ol):
         raise AssertionError("window accepted with no mask")
 
 
+# ---------------------------------------------------------------------------
+# backward pins: the gradients of the forward definition
+
+BWD_CASES = [
+    # B, Hq, Hkv, Q, K, D, Dv, window, seqlens_q, seqlens_k, mask
+    (2, 4, 2, 7, 11, 8, 8, 0, None, None, 0),
+    (3, 6, 2, 9, 9, 8, 12, 3, [9, 4, 0], [9, 7, 5], 0),
+    (2, 4, 1, 6, 10, 16, 8, 0, [6, 5], [10, 0], 1),
+    (2, 2, 2, 5, 8, 4, 4, 0, [5, 3], [8, 6], 2),
+    (1, 8, 2, 12, 5, 8, 8, 2, None, None, 0),
+]
+
+
+def autograd_reference(q, k, v, dout, Qb, Kb, Hq, Hkv, window, scale, mask=0):
+    """torch fp64 autograd of sum(O * dO) for one sequence, O the masked
+    softmax attention built from torch ops (softmax, matmul) and the numpy
+    mask.  Rows without a legal key are left out of the loss.  KV heads are
+    expanded with repeat_interleave, so autograd sums each KV head's
+    gradient over its query heads."""
+    G = Hq // Hkv
+    qt = torch.tensor(np.asarray(q, np.float64), requires_grad=True)
+    kt = torch.tensor(np.asarray(k, np.float64), requires_grad=True)
+    vt = torch.tensor(np.asarray(v, np.float64), requires_grad=True)
+    m = torch.from_numpy(mask_matrix(Qb, Kb, window, mask))
+    has = m.any(dim=1)
+    safe = m.clone()
+    safe[~has] = True
+    qh = qt.permute(1, 0, 2)
+    kh = kt.permute(1, 0, 2).repeat_interleave(G, 0)
+    vh = vt.permute(1, 0, 2).repeat_interleave(G, 0)
+    s = torch.matmul(qh, kh.transpose(1, 2)) * scale
+    p = torch.softmax(s.masked_fill(~safe, -math.inf), dim=-1)
+    o = torch.matmul(p, vh).permute(1, 0, 2)                          # [Qb,Hq,Dv]
+    g = torch.from_numpy(np.asarray(dout, np.float64)) * has[:, None, None]
+    (o * g).sum().backward()
+    return qt.grad.numpy(), kt.grad.numpy(), vt.grad.numpy()
+
+
+def _bwd_inputs(seed, B, Hq, Hkv, Q, K, D, Dv):
+    q, k, v = rng_inputs(seed, B, Hq, Hkv, Q, K, D, Dv)
+    g = np.random.default_rng(seed + 1)
+    dout = g.standard_normal((B, Q, Hq, Dv)).astype(np.float32)
+    return q, k, v, dout
+
+
+def pin_bwd_autograd(ol):
+    for ci, (B, Hq, Hkv, Q, K, D, Dv, w, sq, sk, mask) in enumerate(BWD_CASES):
+        q, k, v, dout = _bwd_inputs(500 + ci, B, Hq, Hkv, Q, K, D, Dv)
+        scale = 1.0 / math.sqrt(D) * (1.0 + 0.3 * ci)
+        dq, dk, dv = ol.attn_bwd_padded(q, k, v, dout, B=B, Hq=Hq, Hkv=Hkv, Q=Q, K=K, D=D,
+                                        Dv=Dv, seqlens_q=sq, seqlens_k=sk, window=w,
+                                        scale=scale, mask=mask)
+        for b in range(B):
+            Qb = Q if sq is None else sq[b]
+            Kb = K if sk is None else sk[b]
+            # padded rows and keys get no gradient
+            assert np.all(dq[b, Qb:] == 0.0) and np.all(dk[b, Kb:] == 0.0), (ci, b)
+            assert np.all(dv[b, Kb:] == 0.0), (ci, b)
+            if Qb == 0 or Kb == 0:
+                assert np.all(dq[b] == 0.0) and np.all(dk[b] == 0.0) and np.all(dv[b] == 0.0)
+                continue
+            rq, rk, rv = autograd_reference(q[b, :Qb], k[b, :Kb], v[b, :Kb], dout[b, :Qb], Qb, Kb,
+                                            Hq, Hkv, w, scale, mask)
+            for name, got, ref in (("dq", dq[b, :Qb], rq), ("dk", dk[b, :Kb], rk),
+                                   ("dv", dv[b, :Kb], rv)):
+                assert np.allclose(got, ref, atol=1e-12, rtol=1e-10), (ci, b, name)
+
+
+def pin_bwd_finite_differences(ol):
+    """Central differences of the (separately pinned) forward oracle: the
+    directional derivative of L = sum(O * dO) along a random direction of q,
+    k or v equals <grad, direction>.  The step is a power of two so that the
+    perturbed float32 inputs are exact."""
+    B, Hq, Hkv, Q, K, D, Dv = 2, 4, 2, 6, 9, 8, 6
+    sq, sk = [6, 4], [9, 6]
+    for ci, (w, mask) in enumerate(((0, 0), (3, 0), (0, 1), (0, 2))):
+        q, k, v, dout = _bwd_inputs(600 + ci, B, Hq, Hkv, Q, K, D, Dv)
+        # inputs on a 2^-16 grid: the perturbed values stay exact in float32
+        q, k, v = (np.round(t * 65536.0).astype(np.float32) / np.float32(65536.0) for t in (q, k, v))
+        kw = dict(B=B, Hq=Hq, Hkv=Hkv, Q=Q, K=K, D=D, Dv=Dv, seqlens_q=sq, seqlens_k=sk,
+                  window=w, scale=0.4, mask=mask)
+        grads = ol.attn_bwd_padded(q, k, v, dout, **kw)
+
+        def loss(q_, k_, v_):
+            o, _ = ol.attn_padded(q_, k_, v_, **kw)
+            return float((o * dout.astype(np.float64)).sum())
+
+        g = np.random.default_rng(700 + ci)
+        h = 2.0 ** -13
+        for which, grad in zip(range(3), grads):
+            args = [q, k, v]
+            # direction of small integers, masked to the sequence's valid rows
+            dirn = g.integers(-2, 3, size=args[which].shape).astype(np.float32)
+            for b in range(B):
+                dirn[b, (sq if which == 0 else sk)[b]:] = 0
+            plus, minus = list(args), list(args)
+            plus[which] = (args[which] + np.float32(h) * dirn).astype(np.float32)
+            minus[which] = (args[which] - np.float32(h) * dirn).astype(np.float32)
+            assert np.array_equal(plus[which].astype(np.float64) - args[which],
+                                  h * dirn.astype(np.float64)), "perturbation not exact"
+            fd = (loss(*plus) - loss(*minus)) / (2 * h)
+            an = float((grad * dirn.astype(np.float64)).sum())
+            assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (ci, which, fd, an)
+
+
+def pin_bwd_invariants(ol):
+    """Consequences of the softmax definition:
+    * the scores of a row shift by the same q.c when every key moves by c,
+      and softmax ignores a shift, so the keys' gradients sum to zero;
+    * the probabilities of a row sum to one, so the values' gradients of a
+      KV head sum to the sum of dO over the rows (with a key) of its query heads;
+    * identical keys give every query a zero gradient;
+    * a constant V makes O independent of the scores: dQ = dK = 0;
+    * dO = 0 gives zero gradients everywhere."""
+    B, Hq, Hkv, Q, K, D, Dv = 2, 6, 2, 7, 10, 8, 5
+    sq, sk = [7, 5], [10, 6]
+    for w, mask in ((0, 0), (4, 0), (0, 1), (0, 2)):
+        q, k, v, dout = _bwd_inputs(800 + w + mask, B, Hq, Hkv, Q, K, D, Dv)
+        kw = dict(B=B, Hq=Hq, Hkv=Hkv, Q=Q, K=K, D=D, Dv=Dv, seqlens_q=sq, seqlens_k=sk,
+                  window=w, scale=0.35, mask=mask)
+        dq, dk, dv = ol.attn_bwd_padded(q, k, v, dout, **kw)
+        G = Hq // Hkv
+        for b in range(B):
+            Qb, Kb = sq[b], sk[b]
+            has = mask_matrix(Qb, Kb, w, mask).any(axis=1)
+            assert np.allclose(dk[b].sum(axis=0), 0.0, atol=1e-12), (w, mask, b)
+            for kh in range(Hkv):
+                want = dout[b, :Qb][has][:, kh * G:(kh + 1) * G].astype(np.float64).sum(axis=(0, 1))
+                assert np.allclose(dv[b, :, kh].sum(axis=0), want, atol=1e-12), (w, mask, b, kh)
+        k_same = np.broadcast_to(k[:, :1], k.shape).copy()
+        dq2, _, _ = ol.attn_bwd_padded(q, k_same, v, dout, **kw)
+        assert np.allclose(dq2, 0.0, atol=1e-12), ("identical keys", w, mask)
+        v_const = np.broadcast_to(v[:, :1], v.shape).copy()
+        dq3, dk3, _ = ol.attn_bwd_padded(q, k, v_const, dout, **kw)
+        assert np.allclose(dq3, 0.0, atol=1e-12) and np.allclose(dk3, 0.0, atol=1e-12), \
+            ("constant V", w, mask)
+        z = ol.attn_bwd_padded(q, k, v, np.zeros_like(dout), **kw)
+        assert all(np.all(t == 0.0) for t in z), ("dO = 0", w, mask)
+
+
 ALL_PINS = [pin_golden, pin_sdpa, pin_invariants, pin_packed_matches_padded,
-            pin_rows_match_full, pin_legal_pairs, pin_sdpa_masks]
+            pin_rows_match_full, pin_legal_pairs, pin_sdpa_masks, pin_bwd_autograd,
+            pin_bwd_finite_differences, pin_bwd_invariants]

@@ -39,6 +39,22 @@ MUTANTS = [
      "const double p = exp(s_scratch[k - lo]) * 1.0000001;"),
     ("q_transposed_index", "oracle_row(q + r * D, k + ((long)b * K * Hkv + kh) * D,",
      "oracle_row(q + ((r % Hq) * Q + (r / Hq) % Q + (r / ((long)Hq * Q)) * Q * Hq) * D, k + ((long)b * K * Hkv + kh) * D,"),
+    # backward
+    ("bwd_drops_row_term", "const double ds = p * (dp - Dq);", "const double ds = p * dp;"),
+    ("bwd_ds_sign", "const double ds = p * (dp - Dq);", "const double ds = p * (Dq - dp);"),
+    ("bwd_dk_without_scale", "dkb[kk * (long)Hkv * D + d] += scale * ds * (double)qrow[d];",
+     "dkb[kk * (long)Hkv * D + d] += ds * (double)qrow[d];"),
+    ("bwd_dq_uses_query", "dqrow[d] += scale * ds * (double)krow[d];",
+     "dqrow[d] += scale * ds * (double)qrow[d];"),
+    ("bwd_dv_uses_ds", "+= p * (double)dorow[j];", "+= ds * (double)dorow[j];"),
+    ("bwd_p_unshifted", "const double p = exp(scale * acc - lse);",
+     "const double p = exp(scale * acc);"),
+    ("bwd_one_head_per_group", "for (int h = kh * G; h < (kh + 1) * G; ++h)",
+     "for (int h = kh * G; h < kh * G + 1; ++h)"),
+    ("bwd_last_key_dropped", "for (long kk = lo; kk <= hi; ++kk) {",
+     "for (long kk = lo; kk < hi; ++kk) {"),
+    ("bwd_rowterm_uses_v", "for (int j = 0; j < Dv; ++j) Dq += (double)dorow[j] * orow[j];",
+     "for (int j = 0; j < Dv; ++j) Dq += (double)dorow[j] * vb[j];"),
 ]
 
 
