@@ -18,13 +18,14 @@ from . import build_ext
 
 ATTN_F32, ATTN_F16, ATTN_BF16 = 0, 1, 2
 ATTN_ALGO_AUTO, ATTN_ALGO_GENERIC, ATTN_ALGO_TCGEN05, ATTN_ALGO_DECODE = 0, 1, 2, 3
-ALGOS = {"auto": 0, "generic": 1, "tcgen05": 2, "decode": 3}
+ATTN_ALGO_MMA = 4
+ALGOS = {"auto": 0, "generic": 1, "tcgen05": 2, "decode": 3, "mma": 4}
 # bottom-right causal (the pages' rule), top-left causal, none
 MASKS = {"causal": 0, "causal_top_left": 1, "none": 2}
 _DTYPE_CODE = {torch.float32: ATTN_F32, torch.float16: ATTN_F16, torch.bfloat16: ATTN_BF16}
 
 EXPORTED = ("attn_fwd", "attn_fwd_varlen", "attn_fwd_algo", "attn_fwd_varlen_algo",
-            "attn_fwd_ex", "attn_fwd_varlen_ex", "attn_fwd_paged",
+            "attn_fwd_ex", "attn_fwd_varlen_ex", "attn_fwd_paged", "attn_bwd", "attn_bwd_varlen",
             "attn_lse_combine", "attn_fwd_decode_noalloc", "attn_fwd_staged", "attn_last_error",
             "attn_device_status", "attn_kernel_launches", "attn_version")
 
@@ -78,6 +79,8 @@ def load_library(path: str | None = None):
         lib.attn_fwd_staged.argtypes = ([vp] * 10 + [ip] * 7 + [vp] * 4 + [ip, fp, ip, ip] +
                                         [ullp, ullp, vp])
         lib.attn_fwd_staged.restype = ip
+        lib.attn_bwd.argtypes = [vp] * 9 + [ip] * 7 + [vp, vp, ip, fp, ip, ip, ip, vp]
+        lib.attn_bwd_varlen.argtypes = [vp] * 9 + [ip] * 9 + [vp, vp, ip, fp, ip, ip, ip, vp]
         lib.attn_lse_combine.argtypes = [vp, vp, vp, vp, ip, ctypes.c_longlong, ip, ip, vp]
         lib.attn_lse_combine.restype = ip
         lib.attn_last_error.argtypes = []
@@ -197,6 +200,73 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_q, max_k, o=None, l
                                 _DTYPE_CODE[q.dtype], ALGOS[algo], _stream_ptr(stream))
     _check(rc)
     return o, lse
+
+
+def attn_bwd(q, k, v, o, lse, dout, dq=None, dk=None, dv=None, *, seqlens_q=None,
+             seqlens_k=None, window=0, scale=None, algo="auto", mask="causal", stream=None):
+    """Gradients of attn_fwd (padded layout) for the output gradient ``dout``
+    [B,Q,Hq,Dv]; ``o`` and ``lse`` are attn_fwd's outputs for q, k, v with the
+    same seqlens / window / scale / mask.  ``algo``: "auto", "generic" (CUDA
+    cores) or "mma" (mma.sync tensor cores).  Returns (dq, dk, dv)."""
+    lib = load_library()
+    B, Q, Hq, D = q.shape
+    K, Hkv = k.shape[1], k.shape[2]
+    Dv = v.shape[3]
+    dev = q.device
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t, n in (("q", q, B * Q * Hq * D), ("k", k, B * K * Hkv * D),
+                       ("v", v, B * K * Hkv * Dv), ("o", o, B * Q * Hq * Dv),
+                       ("dout", dout, B * Q * Hq * Dv), ("dq", dq, B * Q * Hq * D),
+                       ("dk", dk, B * K * Hkv * D), ("dv", dv, B * K * Hkv * Dv)):
+        _check_tensor(name, t, q.dtype, n, dev)
+    _check_tensor("lse", lse, torch.float32, B * Q * Hq, dev)
+    for name, t in (("seqlens_q", seqlens_q), ("seqlens_k", seqlens_k)):
+        if t is not None:
+            _check_tensor(name, t, torch.int32, B, dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                      _ptr(dk), _ptr(dv), B, Hq, Hkv, Q, K, D, Dv, _ptr(seqlens_q),
+                      _ptr(seqlens_k), int(window), float(scale), MASKS[mask],
+                      _DTYPE_CODE[q.dtype], ALGOS[algo], _stream_ptr(stream))
+    _check(rc)
+    return dq, dk, dv
+
+
+def attn_bwd_varlen(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_q, max_k, dq=None,
+                    dk=None, dv=None, *, window=0, scale=None, algo="auto", mask="causal",
+                    stream=None):
+    """attn_bwd on the packed layout of attn_fwd_varlen.  Returns (dq, dk, dv);
+    rows outside every sequence are left as they were (zeros when the
+    outputs are allocated here)."""
+    lib = load_library()
+    Tq, Hq, D = q.shape
+    Tk, Hkv = k.shape[0], k.shape[1]
+    Dv = v.shape[2]
+    B = cu_seqlens_q.numel() - 1
+    dev = q.device
+    dq = torch.zeros_like(q) if dq is None else dq
+    dk = torch.zeros_like(k) if dk is None else dk
+    dv = torch.zeros_like(v) if dv is None else dv
+    for name, t, n in (("q", q, Tq * Hq * D), ("k", k, Tk * Hkv * D), ("v", v, Tk * Hkv * Dv),
+                       ("o", o, Tq * Hq * Dv), ("dout", dout, Tq * Hq * Dv),
+                       ("dq", dq, Tq * Hq * D), ("dk", dk, Tk * Hkv * D),
+                       ("dv", dv, Tk * Hkv * Dv)):
+        _check_tensor(name, t, q.dtype, n, dev)
+    _check_tensor("lse", lse, torch.float32, Tq * Hq, dev)
+    _check_tensor("cu_seqlens_q", cu_seqlens_q, torch.int32, B + 1, dev)
+    _check_tensor("cu_seqlens_k", cu_seqlens_k, torch.int32, B + 1, dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = lib.attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                             _ptr(dk), _ptr(dv), B, Hq, Hkv, Tq, Tk, int(max_q), int(max_k), D,
+                             Dv, _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(window),
+                             float(scale), MASKS[mask], _DTYPE_CODE[q.dtype], ALGOS[algo],
+                             _stream_ptr(stream))
+    _check(rc)
+    return dq, dk, dv
 
 
 def attn_fwd_decode_noalloc(q, k, v, o, lse=None, *, seqlens_q=None, seqlens_k=None, window=0,

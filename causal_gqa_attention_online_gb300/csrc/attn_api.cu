@@ -282,6 +282,113 @@ int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
     return run(p, dtype, algo, stream);
 }
 
+int bwd_common(const void *q, const void *k, const void *v, const void *o, const float *lse,
+               const void *dout, void *dq, void *dk, void *dv, int B, int Hq, int Hkv,
+               long long Tq, long long Tk, int Q, int K, int D, int Dv,
+               const int32_t *seqlens_q, const int32_t *seqlens_k, const int32_t *cu_q,
+               const int32_t *cu_k, int window, float scale, int mask, int dtype, int algo,
+               cudaStream_t stream) {
+    g_last_error[0] = '\0';
+    int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Q, K, D, Dv, dtype, ATTN_ALGO_AUTO);
+    if (rc) return rc;
+    if (algo != ATTN_ALGO_AUTO && algo != ATTN_ALGO_GENERIC && algo != ATTN_ALGO_MMA) {
+        set_error("backward algo must be ATTN_ALGO_AUTO, ATTN_ALGO_GENERIC or ATTN_ALGO_MMA "
+                  "(got %d)", algo);
+        return ATTN_ERR_INVALID;
+    }
+    if (mask < ATTN_MASK_CAUSAL || mask > ATTN_MASK_NONE) {
+        set_error("unknown mask %d", mask);
+        return ATTN_ERR_INVALID;
+    }
+    if (mask == ATTN_MASK_NONE && window > 0) {
+        set_error("a window needs a causal mask (window=%d with ATTN_MASK_NONE)", window);
+        return ATTN_ERR_INVALID;
+    }
+    const bool any_q = (long long)B * Q * Hq > 0;
+    const bool any_k = (long long)B * K * Hkv > 0;
+    if ((any_q && (lse == nullptr || dout == nullptr || dq == nullptr)) ||
+        (any_k && (dk == nullptr || dv == nullptr))) {
+        set_error("lse, dout, dq, dk and dv must be non-null");
+        return ATTN_ERR_INVALID;
+    }
+    if (!ptr_aligned16(dout) || !ptr_aligned16(dq) || !ptr_aligned16(dk) || !ptr_aligned16(dv)) {
+        set_error("tensor pointers must be 16-byte aligned");
+        return ATTN_ERR_INVALID;
+    }
+    if (!any_q && !any_k) return ATTN_OK;
+    BwdParams bp;
+    memset(&bp, 0, sizeof(bp));
+    AttnParams &p = bp.f;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.o = const_cast<void *>(o);
+    p.lse = const_cast<float *>(lse);
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = Hkv > 0 ? Hq / Hkv : 1;
+    p.Q = Q;
+    p.K = K;
+    p.Tq = Tq;
+    p.Tk = Tk;
+    p.D = D;
+    p.Dv = Dv;
+    p.seqlens_q = seqlens_q;
+    p.seqlens_k = seqlens_k;
+    p.cu_q = cu_q;
+    p.cu_k = cu_k;
+    p.window = (window <= 0 || window >= K) ? 0 : window;
+    p.mask = mask;
+    p.scale = scale;
+    p.scale_log2 = scale * kLog2e;
+    p.nsplit = 1;
+    bp.dout = dout;
+    bp.dq = dq;
+    bp.dk = dk;
+    bp.dv = dv;
+    const bool mma_ok = bwd_mma_supported(p, dtype);
+    if (algo == ATTN_ALGO_MMA && !mma_ok) {
+        set_error("mma backward kernels take bf16/fp16 with D, Dv multiples of 8 up to 128");
+        return ATTN_ERR_UNSUPPORTED;
+    }
+    const bool mma = algo == ATTN_ALGO_MMA || (algo == ATTN_ALGO_AUTO && mma_ok);
+    int dev = 0;
+    rc = current_device(&dev);
+    if (rc) return rc;
+    rc = status_ptr(dev, &p.status);
+    if (rc) return rc;
+    if (!any_q) {
+        // no query rows: every key gets zero gradients
+        const size_t es = dtype == ATTN_F32 ? 4 : 2;
+        cudaError_t e = cudaMemsetAsync(dk, 0, (size_t)Tk * Hkv * D * es, stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, (size_t)Tk * Hkv * Dv * es, stream);
+        if (e != cudaSuccess) {
+            set_error("cudaMemsetAsync: %s", cudaGetErrorString(e));
+            return ATTN_ERR_CUDA;
+        }
+        return ATTN_OK;
+    }
+    cudaMemPool_t pool = nullptr;
+    rc = pool_for(dev, &pool);
+    if (rc) return rc;
+    void *ws = nullptr;
+    const size_t bytes = sizeof(float) * (size_t)(Tq * Hq);
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, bytes, pool, stream);
+    if (e != cudaSuccess) {
+        set_error("workspace cudaMallocFromPoolAsync(%zu): %s", bytes, cudaGetErrorString(e));
+        return ATTN_ERR_CUDA;
+    }
+    bp.delta = static_cast<float *>(ws);
+    rc = launch_bwd(bp, dtype, mma, stream);
+    e = cudaFreeAsync(ws, stream);
+    if (e != cudaSuccess && rc == 0) {
+        set_error("workspace cudaFreeAsync: %s", cudaGetErrorString(e));
+        rc = ATTN_ERR_CUDA;
+    }
+    return rc;
+}
+
 }  // namespace
 }  // namespace attn
 
@@ -399,6 +506,33 @@ int attn_lse_combine(const float *o_parts, const float *lse_parts, void *o, floa
     }
     return launch_combine_flat(o_parts, lse_parts, o, lse, nsplit, rows, Dv, dtype,
                                reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+             const void *dout, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int Q, int K,
+             int D, int Dv, const int32_t *seqlens_q, const int32_t *seqlens_k, int window,
+             float scale, int mask, int dtype, int algo, attn_stream_t stream) {
+    return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, (long long)B * Q,
+                      (long long)B * K, Q, K, D, Dv, seqlens_q, seqlens_k, nullptr, nullptr,
+                      window, scale, mask, dtype, algo, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_bwd_varlen(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                    const void *dout, void *dq, void *dk, void *dv, int B, int Hq, int Hkv,
+                    int total_q, int total_k, int max_Q, int max_K, int D, int Dv,
+                    const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int window,
+                    float scale, int mask, int dtype, int algo, attn_stream_t stream) {
+    if (B > 0 && (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr)) {
+        attn::set_error("cu_seqlens_q and cu_seqlens_k must be non-null");
+        return ATTN_ERR_INVALID;
+    }
+    if (total_q < 0 || total_k < 0) {
+        attn::set_error("negative size (total_q=%d total_k=%d)", total_q, total_k);
+        return ATTN_ERR_INVALID;
+    }
+    return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, total_q, total_k, max_Q,
+                      max_K, D, Dv, nullptr, nullptr, cu_seqlens_q, cu_seqlens_k, window, scale,
+                      mask, dtype, algo, reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char *attn_last_error(void) { return g_last_error; }

@@ -55,6 +55,17 @@ struct AttnParams {
     int *status;             // device status word
 };
 
+// One backward problem: the forward problem (its o and lse hold the forward's
+// outputs, read here) plus dO and the gradients.
+struct BwdParams {
+    AttnParams f;
+    const void *dout;  // [rows of q][Hq][Dv], like o
+    void *dq;          // like q
+    void *dk;          // like k
+    void *dv;          // like v
+    float *delta;      // [Tq * Hq] workspace: rowsum(dO * O)
+};
+
 struct SeqInfo {
     long long q_off;  // first query row of the sequence in q / o (row = one token)
     long long k_off;  // first key row of the sequence in k / v

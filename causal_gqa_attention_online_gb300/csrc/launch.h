@@ -28,4 +28,9 @@ int launch_decode(const AttnParams &p, int dtype, cudaStream_t stream);
 bool prefill_tc_supported(const AttnParams &p, int dtype);
 int launch_prefill_tc(const AttnParams &p, int dtype, cudaStream_t stream);
 
+// Backward: rowsum(dO * O), then dK/dV and dQ.  mma: the mma.sync kernels
+// (bf16/fp16, bwd_mma_supported); otherwise the CUDA-core kernels.
+bool bwd_mma_supported(const AttnParams &p, int dtype);
+int launch_bwd(const BwdParams &bp, int dtype, bool mma, cudaStream_t stream);
+
 }  // namespace attn

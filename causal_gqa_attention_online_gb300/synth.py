@@ -28,7 +28,7 @@ TORCH_DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat
 ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2}
 
 _CHUNK = 1 << 22
-STREAM_Q, STREAM_K, STREAM_V, STREAM_LEN = 0, 1, 2, 3
+STREAM_Q, STREAM_K, STREAM_V, STREAM_LEN, STREAM_DO = 0, 1, 2, 3, 4
 
 
 def _fill_chunk(args):
@@ -144,6 +144,27 @@ def make_packed(seqlens_q, seqlens_k, Hq, Hkv, D, Dv, dtype="bf16", seed=1234, w
     return Inputs("packed", dtype, B, Hq, Hkv, int(sq.max(initial=0)), int(sk.max(initial=0)),
                   D, Dv, int(window), float(scale), to_storage(q, dtype), to_storage(k, dtype),
                   to_storage(v, dtype), cu_seqlens_q=cq, cu_seqlens_k=ck)
+
+
+def make_dout(inp: Inputs, seed: int = 1234, pad_value=0.0) -> torch.Tensor:
+    """An output gradient dO shaped like the problem's O (padded [B,Q,Hq,Dv]
+    or packed [Tq,Hq,Dv]), N(0,1) in the storage dtype; padded rows past a
+    sequence's query length hold ``pad_value``."""
+    if inp.layout == "packed":
+        Tq = int(inp.cu_seqlens_q[-1])
+        x = normal(seed, STREAM_DO, Tq * inp.Hq * inp.Dv).reshape(Tq, inp.Hq, inp.Dv)
+        return to_storage(x, inp.dtype)
+    qb = (np.full(inp.B, inp.Q) if inp.seqlens_q is None
+          else np.clip(inp.seqlens_q, 0, inp.Q)).astype(np.int64)
+    w = inp.Hq * inp.Dv
+    out = np.full((inp.B, inp.Q, w), pad_value, np.float32)
+    vals = normal(seed, STREAM_DO, int(qb.sum()) * w)
+    off = 0
+    for b in range(inp.B):
+        n = int(qb[b])
+        out[b, :n] = vals[off:off + n * w].reshape(n, w)
+        off += n * w
+    return to_storage(out.reshape(inp.B, inp.Q, inp.Hq, inp.Dv), inp.dtype)
 
 
 # ---------------------------------------------------------------------------

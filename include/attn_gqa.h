@@ -82,7 +82,9 @@ enum attn_algo {
     ATTN_ALGO_AUTO = 0,     /* choose by dtype, head widths and query length */
     ATTN_ALGO_GENERIC = 1,  /* CUDA-core online softmax: any dtype, D, Dv <= 256 */
     ATTN_ALGO_TCGEN05 = 2,  /* tcgen05/TMEM prefill: bf16/fp16, D, Dv multiples of 16 in [64, 128] */
-    ATTN_ALGO_DECODE = 3    /* split-KV tensor-core decode: bf16/fp16, Q*G <= 16 */
+    ATTN_ALGO_DECODE = 3,   /* split-KV tensor-core decode: bf16/fp16, Q*G <= 16 */
+    ATTN_ALGO_MMA = 4       /* backward only: warp-level mma.sync tensor cores, bf16/fp16,
+                               D, Dv multiples of 8 up to 128 */
 };
 
 /* Which keys a query row may attend to (attn_fwd_ex, attn_fwd_varlen_ex). */
@@ -251,6 +253,52 @@ ATTN_API int attn_fwd_staged(const void *hq, const void *hk, const void *hv, voi
                              const int32_t *seqlens_k_host, int window, float scale, int dtype,
                              int chunks, unsigned long long *bytes_in,
                              unsigned long long *bytes_out, attn_stream_t stream);
+
+/*
+ * attn_bwd -- gradients of attn_fwd_ex (padded layout) for a loss whose
+ * gradient with respect to o is dout.  The pages define the forward only
+ * ("Online softmax" and "FlashAttention" passages: O = softmax(scale Q K^T +
+ * mask) V per row, with the row's log-sum-exp kept); this is the derivative
+ * of that definition.  With P = exp(scale q.k - LSE) over the row's legal
+ * keys and Dq = sum(dO * O) over the row:
+ *     dS = P (dO . v - Dq)
+ *     dq = scale sum_k dS k
+ *     dk = scale sum over rows of dS q
+ *     dv = sum over rows of P dO
+ * where a KV head's dk and dv sum over every query head of its group.
+ *   q, k, v       the forward's inputs, shapes as in attn_fwd
+ *   o, lse        the forward's outputs for those inputs (lse required);
+ *                 P is recomputed from lse, nothing else is stored
+ *   dout          [B, Q, Hq, Dv], same dtype as q
+ *   dq, dk, dv    outputs shaped like q, k, v (same dtype), written in full:
+ *                 rows past seqlens_q, keys past seqlens_k, rows without a
+ *                 legal key and keys no row attends to get zeros
+ *   seqlens_q, seqlens_k, window, scale, mask   as in attn_fwd_ex
+ *   algo          ATTN_ALGO_AUTO (mma.sync kernels where they apply, else the
+ *                 CUDA-core kernels), ATTN_ALGO_GENERIC or ATTN_ALGO_MMA
+ * All pointers are device memory, 16-byte aligned.  A workspace of
+ * 4 * B * Q * Hq bytes comes from the library's stream-ordered pool.  The
+ * result is deterministic (no atomics: dk/dv and dq are written by separate
+ * kernels, each element by one thread).  Returns ATTN_OK, ATTN_ERR_INVALID,
+ * ATTN_ERR_UNSUPPORTED (ATTN_ALGO_MMA on a shape it does not take) or
+ * ATTN_ERR_CUDA; asynchronous on `stream`.
+ */
+ATTN_API int attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                      const float *lse, const void *dout, void *dq, void *dk, void *dv, int B,
+                      int Hq, int Hkv, int Q, int K, int D, int Dv, const int32_t *seqlens_q,
+                      const int32_t *seqlens_k, int window, float scale, int mask, int dtype,
+                      int algo, attn_stream_t stream);
+
+/* attn_bwd on the packed layout of attn_fwd_varlen_ex: q, o, dout, dq
+ * [total_q, Hq, *], k, v, dk, dv [total_k, Hkv, *], sequences given by
+ * cu_seqlens_q / cu_seqlens_k (int32 [B + 1]).  Rows of dq, dk and dv
+ * outside every sequence are not written. */
+ATTN_API int attn_bwd_varlen(const void *q, const void *k, const void *v, const void *o,
+                             const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                             int B, int Hq, int Hkv, int total_q, int total_k, int max_Q,
+                             int max_K, int D, int Dv, const int32_t *cu_seqlens_q,
+                             const int32_t *cu_seqlens_k, int window, float scale, int mask,
+                             int dtype, int algo, attn_stream_t stream);
 
 /* Message for the calling thread's most recent failed call ("" if none). */
 ATTN_API const char *attn_last_error(void);
