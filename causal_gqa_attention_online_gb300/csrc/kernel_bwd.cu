@@ -28,6 +28,7 @@
 #include "common.cuh"
 #include "launch.h"
 #include "mma_sync.cuh"
+#include "sm100_ptx.cuh"
 
 namespace attn {
 namespace {
@@ -46,6 +47,27 @@ __device__ __forceinline__ void rows_for_keys(int k0, int k1, int Qb, int Kb, in
     qf = max(0, k0 - off);                     // hi(qi) > k0  <=>  qi + off >= k0
     qe = Qb;
     if (window > 0) qe = min(Qb, k1 + window - 1 - off);  // lo(qi) < k1
+}
+
+// 4-byte cp.async (zero-fills when src_bytes is 0, reading nothing).
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, int src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+// A 1-D grid of (tile, sequence x KV head) blocks, ordered tile rank first:
+// every (sequence, KV head)'s rank-0 tile, then every rank-1 tile, ...  The
+// kernels give rank 0 to their longest tile, so the long blocks start first
+// and the short ones fill the tail of the launch.
+__device__ __forceinline__ void block_tile(const AttnParams &p, int &rank, int &ntiles, int &b,
+                                           int &kvh) {
+    const int nbh = p.B * p.Hkv;
+    rank = blockIdx.x / nbh;
+    ntiles = gridDim.x / nbh;
+    const int bh = blockIdx.x % nbh;
+    b = bh / p.Hkv;
+    kvh = bh % p.Hkv;
 }
 
 // Legal key range of flattened row r of (sequence si, KV head); rows past the
@@ -104,12 +126,13 @@ __global__ void __launch_bounds__(128) bwd_dq_generic(const BwdParams bp) {
     float *ks = dos + kGRows * Dv;   // [kGTK][Dp]
     float *vs = ks + kGTK * Dp;      // [kGTK][Dvp]
 
-    const int b = blockIdx.y / p.Hkv, kvh = blockIdx.y % p.Hkv;
+    int rank, ntiles, b, kvh;
+    block_tile(p, rank, ntiles, b, kvh);
     const SeqInfo si = seq_info(p, b);
     const bool packed = p.cu_q != nullptr;
     const int nvalid = si.Qb * G;
     const int ncap = (packed ? si.Qb : p.Q) * G;
-    const int r0 = (gridDim.x - 1 - blockIdx.x) * kGRows;  // longest rows first
+    const int r0 = (ntiles - 1 - rank) * kGRows;  // the last rows see the most keys
     if (r0 >= ncap) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const T *qg = static_cast<const T *>(p.q), *kg = static_cast<const T *>(p.k);
@@ -221,11 +244,12 @@ __global__ void __launch_bounds__(128) bwd_dkdv_generic(const BwdParams bp) {
     float *pw = dr + 4 * Dv;        // [4][kGTK]
     float *dsw = pw + 4 * kGTK;     // [4][kGTK]
 
-    const int b = blockIdx.y / p.Hkv, kvh = blockIdx.y % p.Hkv;
+    int rank, ntiles, b, kvh;
+    block_tile(p, rank, ntiles, b, kvh);
     const SeqInfo si = seq_info(p, b);
     const bool packed = p.cu_q != nullptr;
     const int kcap = packed ? si.Kb : p.K;
-    const int k0 = blockIdx.x * kGTK;
+    const int k0 = rank * kGTK;  // the first keys are seen by the most rows
     if (k0 >= kcap) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const T *qg = static_cast<const T *>(p.q), *kg = static_cast<const T *>(p.k);
@@ -317,6 +341,7 @@ __global__ void __launch_bounds__(128) bwd_dkdv_generic(const BwdParams bp) {
 
 constexpr int kMKeys = 64;   // dK/dV: keys per block (16 per warp)
 constexpr int kMRows = 32;   // dK/dV: rows per step
+constexpr int kMStages = 3;  // dK/dV: row-tile ring depth
 constexpr int kQRows = 64;   // dQ: rows per block (16 per warp)
 constexpr int kQKeys = 64;   // dQ: keys per step
 
@@ -324,11 +349,11 @@ constexpr int kQKeys = 64;   // dQ: keys per step
 // cp.async; src(r) gives the global address of row r, or nullptr for a row
 // of zeros.  Columns at or past `cols` are zero-filled.  Zero-filled chunks
 // read nothing; they are given `base` (a valid address) all the same.
-template <typename T, int W, typename Src>
+template <typename T, int W, int NT = 128, typename Src>
 __device__ __forceinline__ void stage_rows(uint8_t *dst, int nrows, int cols, int tid,
                                            const T *base, Src src) {
     constexpr int kChunks = W / 8;
-    for (int c = tid; c < nrows * kChunks; c += 128) {
+    for (int c = tid; c < nrows * kChunks; c += NT) {
         const int r = c / kChunks, ch = c % kChunks;
         const T *g = src(r);
         const bool ok = g != nullptr && ch * 8 < cols;
@@ -336,38 +361,53 @@ __device__ __forceinline__ void stage_rows(uint8_t *dst, int nrows, int cols, in
     }
 }
 
+// dK / dV.  A block owns kMKeys keys of one (sequence, KV head) and walks,
+// kMRows at a time, the flattened rows of the group that attend to them.
+// Warps come in pairs over the same 16 keys, each pair splitting the work of
+// a step in two halves of equal MMA count:
+//   P warp  (w < 4):  S^T = K Q^T,  P^T = exp2(S^T scale_log2 - LSE_2),  dV += P^T dO
+//   dS warp (w >= 4): dP^T = V dO^T, dS^T = P^T (dP^T - Dq),            dK += dS^T Q
+// P^T goes from one to the other through shared memory in the MMA
+// accumulator layout (both warps' fragments map lane / register to the same
+// (key, row)), behind a 64-thread named barrier per pair.  Each warp keeps one
+// 16 x 128 fp32 accumulator, so two blocks of eight warps fit an SM.
 template <typename T, int DW, int DVW>
-__global__ void __launch_bounds__(128) bwd_dkdv_mma(const BwdParams bp) {
+__global__ void __launch_bounds__(256, 2) bwd_dkdv_mma(const BwdParams bp) {
+    constexpr int NT = 256;
     extern __shared__ __align__(128) uint8_t smem_b[];
     uint8_t *smem = smem_b;
     const AttnParams &p = bp.f;
     constexpr int KB = DW * 2, VB = DVW * 2;  // bytes per staged row
     uint8_t *ks = smem;                        // [kMKeys][KB]
     uint8_t *vs = ks + kMKeys * KB;            // [kMKeys][VB]
-    uint8_t *qs = vs + kMKeys * VB;            // [2][kMRows][KB]
-    uint8_t *dos = qs + 2 * kMRows * KB;       // [2][kMRows][VB]
-    float *lse_s = reinterpret_cast<float *>(dos + 2 * kMRows * VB);  // [2][kMRows], log2 units
-    float *del_s = lse_s + 2 * kMRows;                                 // [2][kMRows]
-    int *lo_s = reinterpret_cast<int *>(del_s + 2 * kMRows);           // [2][kMRows]
-    int *hi_s = lo_s + 2 * kMRows;                                     // [2][kMRows]
+    uint8_t *qs = vs + kMKeys * VB;                   // [kMStages][kMRows][KB]
+    uint8_t *dos = qs + kMStages * kMRows * KB;       // [kMStages][kMRows][VB]
+    float *pbuf = reinterpret_cast<float *>(dos + kMStages * kMRows * VB);  // [4][16][32]
+    float *lse_s = pbuf + 4 * 16 * 32;                // [kMStages][kMRows]
+    float *del_s = lse_s + kMStages * kMRows;         // [kMStages][kMRows]
+    int *lo_s = reinterpret_cast<int *>(del_s + kMStages * kMRows);
+    int *hi_s = lo_s + kMStages * kMRows;
 
-    const int b = blockIdx.y / p.Hkv, kvh = blockIdx.y % p.Hkv;
+    int rank, ntiles, b, kvh;
+    block_tile(p, rank, ntiles, b, kvh);
     const SeqInfo si = seq_info(p, b);
     const bool packed = p.cu_q != nullptr;
     const int kcap = packed ? si.Kb : p.K;
-    const int k0 = blockIdx.x * kMKeys;
+    const int k0 = rank * kMKeys;  // the first keys are seen by the most rows
     if (k0 >= kcap) return;
     const int G = p.G, D = p.D, Dv = p.Dv;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
+    const bool pwarp = warp < 4;
+    const int kw = 16 * (warp & 3);  // this pair's first key in the tile
     const T *qg = static_cast<const T *>(p.q), *kg = static_cast<const T *>(p.k);
     const T *vg = static_cast<const T *>(p.v), *dog = static_cast<const T *>(bp.dout);
 
-    stage_rows<T, DW>(ks, kMKeys, D, tid, kg, [&](int r) -> const T * {
+    stage_rows<T, DW, NT>(ks, kMKeys, D, tid, kg, [&](int r) -> const T * {
         const int key = k0 + r;
         return key < si.Kb ? kg + ((si.k_off + key) * p.Hkv + kvh) * (long long)D : nullptr;
     });
-    stage_rows<T, DVW>(vs, kMKeys, Dv, tid, vg, [&](int r) -> const T * {
+    stage_rows<T, DVW, NT>(vs, kMKeys, Dv, tid, vg, [&](int r) -> const T * {
         const int key = k0 + r;
         return key < si.Kb ? vg + ((si.k_off + key) * p.Hkv + kvh) * (long long)Dv : nullptr;
     });
@@ -385,149 +425,150 @@ __global__ void __launch_bounds__(128) bwd_dkdv_mma(const BwdParams bp) {
     auto load_rows = [&](int step, int buf) {
         const int rb = rf + step * kMRows;
         auto row_of = [&](int r) { return (si.q_off + r / G) * p.Hq + kvh * G + r % G; };
-        stage_rows<T, DW>(qs + buf * kMRows * KB, kMRows, D, tid, qg, [&](int i) -> const T * {
+        stage_rows<T, DW, NT>(qs + buf * kMRows * KB, kMRows, D, tid, qg, [&](int i) -> const T * {
             const int r = rb + i;
             return r < re ? qg + row_of(r) * D : nullptr;
         });
-        stage_rows<T, DVW>(dos + buf * kMRows * VB, kMRows, Dv, tid, dog, [&](int i) -> const T * {
-            const int r = rb + i;
-            return r < re ? dog + row_of(r) * Dv : nullptr;
-        });
+        stage_rows<T, DVW, NT>(dos + buf * kMRows * VB, kMRows, Dv, tid, dog,
+                               [&](int i) -> const T * {
+                                   const int r = rb + i;
+                                   return r < re ? dog + row_of(r) * Dv : nullptr;
+                               });
         if (tid < kMRows) {
+            // LSE and Dq travel with the tile (no thread waits on them here);
+            // rows without a legal key read nothing and are masked by [lo, hi)
             const int r = rb + tid;
             int lo = 0, hi = 0;
-            float l2 = 0.f, dl = 0.f;
-            if (r < re) {
-                row_range(p, si, r, lo, hi);
-                if (hi > lo) {
-                    l2 = p.lse[row_of(r)] * kLog2e;
-                    dl = bp.delta[row_of(r)];
-                }
-            }
-            lse_s[buf * kMRows + tid] = l2;
-            del_s[buf * kMRows + tid] = dl;
+            if (r < re) row_range(p, si, r, lo, hi);
+            const bool ok = hi > lo;
+            const long long row = ok ? row_of(r) : 0;
+            cp_async4(smem_u32(lse_s + buf * kMRows + tid), p.lse + row, ok ? 4 : 0);
+            cp_async4(smem_u32(del_s + buf * kMRows + tid), bp.delta + row, ok ? 4 : 0);
             lo_s[buf * kMRows + tid] = lo;
             hi_s[buf * kMRows + tid] = hi;
         }
     };
 
+    // a ring of three row tiles: the tile loaded during step i was last read
+    // in step i - 1, which every thread has left at step i's barrier
     if (nsteps > 0) load_rows(0, 0);
     cp_async_commit();
+    if (nsteps > 1) load_rows(1, 1);
+    cp_async_commit();
 
-    float dk[DW / 8][4], dv[DVW / 8][4];
+    // P warps accumulate dV (DVW columns), dS warps dK (DW columns)
+    constexpr int kAcc = (DW > DVW ? DW : DVW) / 8;
+    float acc[kAcc][4];
 #pragma unroll
-    for (int j = 0; j < DW / 8; ++j) dk[j][0] = dk[j][1] = dk[j][2] = dk[j][3] = 0.f;
-#pragma unroll
-    for (int j = 0; j < DVW / 8; ++j) dv[j][0] = dv[j][1] = dv[j][2] = dv[j][3] = 0.f;
+    for (int j = 0; j < kAcc; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    float *pmine = pbuf + (warp & 3) * 16 * 32;
 
     for (int step = 0; step < nsteps; ++step) {
-        if (step + 1 < nsteps) {
-            load_rows(step + 1, (step + 1) & 1);
-            cp_async_commit();
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
+        cp_async_wait<1>();  // step's tile has landed (step + 1's may be in flight)
         __syncthreads();
-        const int buf = step & 1;
+        if (step + 2 < nsteps) load_rows(step + 2, (step + 2) % kMStages);
+        cp_async_commit();
+        const int buf = step % kMStages;
         const uint8_t *qb = qs + buf * kMRows * KB;
         const uint8_t *db = dos + buf * kMRows * VB;
-        // S^T = K Q^T and dP^T = V dO^T for this warp's 16 keys x 32 rows
-        float s[4][4], dp[4][4];
+        // S^T = K Q^T (P warps) or dP^T = V dO^T (dS warps): 16 keys x 32 rows
+        float s[4][4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+        for (int j = 0; j < 4; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+        if (pwarp) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) s[j][c] = dp[j][c] = 0.f;
+            for (int kk = 0; kk < DW / 16; ++kk) {
+                uint32_t a[4];
+                ldmatrix_x4(a, smem_u32(ks + swz(kw + (lane & 15), 2 * kk + (lane >> 4), KB)));
 #pragma unroll
-        for (int kk = 0; kk < DW / 16; ++kk) {
-            uint32_t a[4];
-            ldmatrix_x4(a, smem_u32(ks + swz(16 * warp + (lane & 15), 2 * kk + (lane >> 4), KB)));
-#pragma unroll
-            for (int np = 0; np < 2; ++np) {
-                uint32_t bq[4];
-                ldmatrix_x4(bq, smem_u32(qb + swz(16 * np + (lane & 7) + ((lane >> 4) << 3),
-                                                  2 * kk + ((lane >> 3) & 1), KB)));
-                MmaOp<T>::run(s[2 * np], a, bq[0], bq[1]);
-                MmaOp<T>::run(s[2 * np + 1], a, bq[2], bq[3]);
+                for (int np = 0; np < 2; ++np) {
+                    uint32_t bq[4];
+                    ldmatrix_x4(bq, smem_u32(qb + swz(16 * np + (lane & 7) + ((lane >> 4) << 3),
+                                                      2 * kk + ((lane >> 3) & 1), KB)));
+                    MmaOp<T>::run(s[2 * np], a, bq[0], bq[1]);
+                    MmaOp<T>::run(s[2 * np + 1], a, bq[2], bq[3]);
+                }
             }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int key = k0 + kw + g + 8 * (c >> 1);
+                    const int rl = buf * kMRows + 8 * j + 2 * t + (c & 1);
+                    const bool ok = key >= lo_s[rl] && key < hi_s[rl];
+                    s[j][c] = ok ? exp2f(s[j][c] * p.scale_log2 - lse_s[rl] * kLog2e) : 0.f;
+                    pmine[(j * 4 + c) * 32 + lane] = s[j][c];
+                }
+            sm100::named_bar_arrive(1 + (warp & 3), 64);
+        } else {
+#pragma unroll
+            for (int kk = 0; kk < DVW / 16; ++kk) {
+                uint32_t a[4];
+                ldmatrix_x4(a, smem_u32(vs + swz(kw + (lane & 15), 2 * kk + (lane >> 4), VB)));
+#pragma unroll
+                for (int np = 0; np < 2; ++np) {
+                    uint32_t bq[4];
+                    ldmatrix_x4(bq, smem_u32(db + swz(16 * np + (lane & 7) + ((lane >> 4) << 3),
+                                                      2 * kk + ((lane >> 3) & 1), VB)));
+                    MmaOp<T>::run(s[2 * np], a, bq[0], bq[1]);
+                    MmaOp<T>::run(s[2 * np + 1], a, bq[2], bq[3]);
+                }
+            }
+            sm100::named_bar_sync(1 + (warp & 3), 64);  // the partner's P^T is in pmine
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int rl = buf * kMRows + 8 * j + 2 * t + (c & 1);
+                    s[j][c] = pmine[(j * 4 + c) * 32 + lane] * (s[j][c] - del_s[rl]);
+                }
         }
-#pragma unroll
-        for (int kk = 0; kk < DVW / 16; ++kk) {
-            uint32_t a[4];
-            ldmatrix_x4(a, smem_u32(vs + swz(16 * warp + (lane & 15), 2 * kk + (lane >> 4), VB)));
-#pragma unroll
-            for (int np = 0; np < 2; ++np) {
-                uint32_t bq[4];
-                ldmatrix_x4(bq, smem_u32(db + swz(16 * np + (lane & 7) + ((lane >> 4) << 3),
-                                                  2 * kk + ((lane >> 3) & 1), VB)));
-                MmaOp<T>::run(dp[2 * np], a, bq[0], bq[1]);
-                MmaOp<T>::run(dp[2 * np + 1], a, bq[2], bq[3]);
-            }
-        }
-        // P^T (in s) and dS^T (in dp)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int key = k0 + 16 * warp + g + 8 * (c >> 1);
-                const int rl = buf * kMRows + 8 * j + 2 * t + (c & 1);
-                const bool ok = key >= lo_s[rl] && key < hi_s[rl];
-                const float pr = ok ? exp2f(s[j][c] * p.scale_log2 - lse_s[rl]) : 0.f;
-                s[j][c] = pr;
-                dp[j][c] = pr * (dp[j][c] - del_s[rl]);
-            }
-        // dV += P^T dO and dK += dS^T Q, contracting over the 32 rows
+        // dV += P^T dO (P warps) or dK += dS^T Q (dS warps), over the 32 rows
+        const uint8_t *bsrc = pwarp ? db : qb;
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
-            uint32_t pa[4], da[4];
+            uint32_t pa[4];
             pa[0] = MmaOp<T>::pack(s[2 * m][0], s[2 * m][1]);
             pa[1] = MmaOp<T>::pack(s[2 * m][2], s[2 * m][3]);
             pa[2] = MmaOp<T>::pack(s[2 * m + 1][0], s[2 * m + 1][1]);
             pa[3] = MmaOp<T>::pack(s[2 * m + 1][2], s[2 * m + 1][3]);
-            da[0] = MmaOp<T>::pack(dp[2 * m][0], dp[2 * m][1]);
-            da[1] = MmaOp<T>::pack(dp[2 * m][2], dp[2 * m][3]);
-            da[2] = MmaOp<T>::pack(dp[2 * m + 1][0], dp[2 * m + 1][1]);
-            da[3] = MmaOp<T>::pack(dp[2 * m + 1][2], dp[2 * m + 1][3]);
             const int trow = 16 * m + (lane & 7) + (((lane >> 3) & 1) << 3);
+            if (pwarp) {
 #pragma unroll
-            for (int np = 0; np < DVW / 16; ++np) {
-                uint32_t bb[4];
-                ldmatrix_x4_trans(bb, smem_u32(db + swz(trow, 2 * np + (lane >> 4), VB)));
-                MmaOp<T>::run(dv[2 * np], pa, bb[0], bb[1]);
-                MmaOp<T>::run(dv[2 * np + 1], pa, bb[2], bb[3]);
-            }
+                for (int np = 0; np < DVW / 16; ++np) {
+                    uint32_t bb[4];
+                    ldmatrix_x4_trans(bb, smem_u32(bsrc + swz(trow, 2 * np + (lane >> 4), VB)));
+                    MmaOp<T>::run(acc[2 * np], pa, bb[0], bb[1]);
+                    MmaOp<T>::run(acc[2 * np + 1], pa, bb[2], bb[3]);
+                }
+            } else {
 #pragma unroll
-            for (int np = 0; np < DW / 16; ++np) {
-                uint32_t bb[4];
-                ldmatrix_x4_trans(bb, smem_u32(qb + swz(trow, 2 * np + (lane >> 4), KB)));
-                MmaOp<T>::run(dk[2 * np], da, bb[0], bb[1]);
-                MmaOp<T>::run(dk[2 * np + 1], da, bb[2], bb[3]);
+                for (int np = 0; np < DW / 16; ++np) {
+                    uint32_t bb[4];
+                    ldmatrix_x4_trans(bb, smem_u32(bsrc + swz(trow, 2 * np + (lane >> 4), KB)));
+                    MmaOp<T>::run(acc[2 * np], pa, bb[0], bb[1]);
+                    MmaOp<T>::run(acc[2 * np + 1], pa, bb[2], bb[3]);
+                }
             }
         }
-        __syncthreads();  // buffer `buf` is reloaded by the next step's prefetch
     }
     cp_async_wait<0>();
 
     // keys past the sequence (padded layout) come out as zeros: P = dS = 0 there
-    T *dkg = static_cast<T *>(bp.dk), *dvg = static_cast<T *>(bp.dv);
+    T *dst = static_cast<T *>(pwarp ? bp.dv : bp.dk);
+    const int width = pwarp ? Dv : D;
+    const float sc = pwarp ? 1.f : p.scale;
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-        const int key = k0 + 16 * warp + g + 8 * hh;
+        const int key = k0 + kw + g + 8 * hh;
         if (key >= kcap) continue;
         const long long krow = (si.k_off + key) * p.Hkv + kvh;
 #pragma unroll
-        for (int j = 0; j < DW / 8; ++j) {
+        for (int j = 0; j < kAcc; ++j) {
             const int d = 8 * j + 2 * t;
-            if (d < D)
-                *reinterpret_cast<uint32_t *>(dkg + krow * D + d) = MmaOp<T>::pack(
-                    dk[j][2 * hh] * p.scale, dk[j][2 * hh + 1] * p.scale);
-        }
-#pragma unroll
-        for (int j = 0; j < DVW / 8; ++j) {
-            const int d = 8 * j + 2 * t;
-            if (d < Dv)
-                *reinterpret_cast<uint32_t *>(dvg + krow * Dv + d) =
-                    MmaOp<T>::pack(dv[j][2 * hh], dv[j][2 * hh + 1]);
+            if (d < width)
+                *reinterpret_cast<uint32_t *>(dst + krow * width + d) =
+                    MmaOp<T>::pack(acc[j][2 * hh] * sc, acc[j][2 * hh + 1] * sc);
         }
     }
 }
@@ -543,13 +584,14 @@ __global__ void __launch_bounds__(128) bwd_dq_mma(const BwdParams bp) {
     uint8_t *ks = dos + kQRows * VB;        // [2][kQKeys][KB]
     uint8_t *vs = ks + 2 * kQKeys * KB;     // [2][kQKeys][VB]
 
-    const int b = blockIdx.y / p.Hkv, kvh = blockIdx.y % p.Hkv;
+    int rank, ntiles_q, b, kvh;
+    block_tile(p, rank, ntiles_q, b, kvh);
     const SeqInfo si = seq_info(p, b);
     const bool packed = p.cu_q != nullptr;
     const int G = p.G, D = p.D, Dv = p.Dv;
     const int nvalid = si.Qb * G;
     const int ncap = (packed ? si.Qb : p.Q) * G;
-    const int r0 = (gridDim.x - 1 - blockIdx.x) * kQRows;  // longest rows first
+    const int r0 = (ntiles_q - 1 - rank) * kQRows;  // the last rows see the most keys
     if (r0 >= ncap) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
@@ -624,29 +666,30 @@ __global__ void __launch_bounds__(128) bwd_dq_mma(const BwdParams bp) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) s[j][c] = dp[j][c] = 0.f;
 #pragma unroll
-        for (int kk = 0; kk < DW / 16; ++kk) {
-            uint32_t a[4];
-            ldmatrix_x4(a, smem_u32(qs + swz(16 * warp + (lane & 15), 2 * kk + (lane >> 4), KB)));
+        for (int kk = 0; kk < (DW > DVW ? DW : DVW) / 16; ++kk) {
+            if (kk < DW / 16) {
+                uint32_t a[4];
+                ldmatrix_x4(a, smem_u32(qs + swz(16 * warp + (lane & 15), 2 * kk + (lane >> 4), KB)));
 #pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                uint32_t bk[4];
-                ldmatrix_x4(bk, smem_u32(kb + swz(16 * np + (lane & 7) + ((lane >> 4) << 3),
-                                                  2 * kk + ((lane >> 3) & 1), KB)));
-                MmaOp<T>::run(s[2 * np], a, bk[0], bk[1]);
-                MmaOp<T>::run(s[2 * np + 1], a, bk[2], bk[3]);
+                for (int np = 0; np < 4; ++np) {
+                    uint32_t bk[4];
+                    ldmatrix_x4(bk, smem_u32(kb + swz(16 * np + (lane & 7) + ((lane >> 4) << 3),
+                                                      2 * kk + ((lane >> 3) & 1), KB)));
+                    MmaOp<T>::run(s[2 * np], a, bk[0], bk[1]);
+                    MmaOp<T>::run(s[2 * np + 1], a, bk[2], bk[3]);
+                }
             }
-        }
+            if (kk < DVW / 16) {
+                uint32_t a[4];
+                ldmatrix_x4(a, smem_u32(dos + swz(16 * warp + (lane & 15), 2 * kk + (lane >> 4), VB)));
 #pragma unroll
-        for (int kk = 0; kk < DVW / 16; ++kk) {
-            uint32_t a[4];
-            ldmatrix_x4(a, smem_u32(dos + swz(16 * warp + (lane & 15), 2 * kk + (lane >> 4), VB)));
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                uint32_t bv[4];
-                ldmatrix_x4(bv, smem_u32(vb + swz(16 * np + (lane & 7) + ((lane >> 4) << 3),
-                                                  2 * kk + ((lane >> 3) & 1), VB)));
-                MmaOp<T>::run(dp[2 * np], a, bv[0], bv[1]);
-                MmaOp<T>::run(dp[2 * np + 1], a, bv[2], bv[3]);
+                for (int np = 0; np < 4; ++np) {
+                    uint32_t bv[4];
+                    ldmatrix_x4(bv, smem_u32(vb + swz(16 * np + (lane & 7) + ((lane >> 4) << 3),
+                                                      2 * kk + ((lane >> 3) & 1), VB)));
+                    MmaOp<T>::run(dp[2 * np], a, bv[0], bv[1]);
+                    MmaOp<T>::run(dp[2 * np + 1], a, bv[2], bv[3]);
+                }
             }
         }
         // dS (in s)
@@ -722,6 +765,13 @@ int launch_k(void (*kern)(Args...), dim3 grid, int block, size_t smem, cudaStrea
     return 0;
 }
 
+// A 1-D grid of tiles x (sequence, KV head) blocks must stay below 2^31.
+bool grid_fits(long long tiles, unsigned bh) {
+    if (tiles * (long long)bh < (1LL << 31)) return true;
+    set_error("backward: %lld tiles x %u (sequence, KV head) pairs exceed one launch", tiles, bh);
+    return false;
+}
+
 int pow2_at_least(int x, int lo) {
     int v = lo;
     while (v < x) v *= 2;
@@ -736,16 +786,18 @@ int launch_generic_bwd_t(const BwdParams &bp, cudaStream_t stream) {
     const size_t s_dkdv = sizeof(float) * ((size_t)kGTK * ((D | 1) + (Dv | 1)) + 4 * (D + Dv) +
                                            8 * kGTK);
     const long long ktiles = ((long long)p.K + kGTK - 1) / kGTK;
+    if (!grid_fits(ktiles, y) || !grid_fits(((long long)p.Q * p.G + kGRows - 1) / kGRows, y))
+        return 2;
     int rc = 0;
     if (ktiles > 0) {
-        rc = launch_k(bwd_dkdv_generic<T, DL>, dim3((unsigned)ktiles, y), 128, s_dkdv, stream,
+        rc = launch_k(bwd_dkdv_generic<T, DL>, dim3((unsigned)(ktiles * y)), 128, s_dkdv, stream,
                       "bwd_dkdv_generic", bp);
         if (rc) return rc;
     }
     const size_t s_dq = sizeof(float) * ((size_t)kGRows * (D + Dv) + (size_t)kGTK * ((D | 1) + (Dv | 1)));
     const long long qtiles = ((long long)p.Q * p.G + kGRows - 1) / kGRows;
     constexpr int DQL = DL / 8;  // D <= 4 * DL = 32 * DQL
-    return launch_k(bwd_dq_generic<T, DQL>, dim3((unsigned)qtiles, y), 128, s_dq, stream,
+    return launch_k(bwd_dq_generic<T, DQL>, dim3((unsigned)(qtiles * y)), 128, s_dq, stream,
                     "bwd_dq_generic", bp);
 }
 
@@ -765,17 +817,19 @@ int launch_mma_bwd_t(const BwdParams &bp, cudaStream_t stream) {
     const AttnParams &p = bp.f;
     const unsigned y = (unsigned)p.B * p.Hkv;
     const long long ktiles = ((long long)p.K + kMKeys - 1) / kMKeys;
+    if (!grid_fits(ktiles, y) || !grid_fits(((long long)p.Q * p.G + kQRows - 1) / kQRows, y))
+        return 2;
     int rc = 0;
     if (ktiles > 0) {
-        const size_t s = (size_t)kMKeys * 2 * (DW + DVW) + (size_t)2 * kMRows * 2 * (DW + DVW) +
-                         16 * kMRows * 4;
-        rc = launch_k(bwd_dkdv_mma<T, DW, DVW>, dim3((unsigned)ktiles, y), 128, s, stream,
+        const size_t s = (size_t)kMKeys * 2 * (DW + DVW) +
+                         (size_t)kMStages * kMRows * (2 * (DW + DVW) + 16) + 4 * 16 * 32 * 4;
+        rc = launch_k(bwd_dkdv_mma<T, DW, DVW>, dim3((unsigned)(ktiles * y)), 256, s, stream,
                       "bwd_dkdv_mma", bp);
         if (rc) return rc;
     }
     const size_t s = (size_t)kQRows * 2 * (DW + DVW) + (size_t)2 * kQKeys * 2 * (DW + DVW);
     const long long qtiles = ((long long)p.Q * p.G + kQRows - 1) / kQRows;
-    return launch_k(bwd_dq_mma<T, DW, DVW>, dim3((unsigned)qtiles, y), 128, s, stream,
+    return launch_k(bwd_dq_mma<T, DW, DVW>, dim3((unsigned)(qtiles * y)), 128, s, stream,
                     "bwd_dq_mma", bp);
 }
 

@@ -126,6 +126,9 @@ __device__ __forceinline__ void bulk_wait0() {
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
     asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
 }
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t n) {
+    asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(n) : "memory");
+}
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
