@@ -387,6 +387,7 @@ __global__ void __launch_bounds__(256, 2) bwd_dkdv_mma(const BwdParams bp) {
     float *del_s = lse_s + kMStages * kMRows;         // [kMStages][kMRows]
     int *lo_s = reinterpret_cast<int *>(del_s + kMStages * kMRows);
     int *hi_s = lo_s + kMStages * kMRows;
+    int *flag_s = hi_s + kMStages * kMRows;          // [kMStages]: step needs no mask
 
     int rank, ntiles, b, kvh;
     block_tile(p, rank, ntiles, b, kvh);
@@ -422,18 +423,41 @@ __global__ void __launch_bounds__(256, 2) bwd_dkdv_mma(const BwdParams bp) {
     }
     const int nsteps = (re - rf + kMRows - 1) / kMRows;
 
+    // Row r of a tile is copied by the threads tid / kCh == r (mod NT / kCh),
+    // one 16-byte chunk each; a thread finds its rows' addresses once a step.
+    constexpr int kChQ = DW / 8, kChO = DVW / 8;
+    auto row_of = [&](int r) { return (si.q_off + r / G) * p.Hq + kvh * G + r % G; };
     auto load_rows = [&](int step, int buf) {
         const int rb = rf + step * kMRows;
-        auto row_of = [&](int r) { return (si.q_off + r / G) * p.Hq + kvh * G + r % G; };
-        stage_rows<T, DW, NT>(qs + buf * kMRows * KB, kMRows, D, tid, qg, [&](int i) -> const T * {
-            const int r = rb + i;
-            return r < re ? qg + row_of(r) * D : nullptr;
-        });
-        stage_rows<T, DVW, NT>(dos + buf * kMRows * VB, kMRows, Dv, tid, dog,
-                               [&](int i) -> const T * {
-                                   const int r = rb + i;
-                                   return r < re ? dog + row_of(r) * Dv : nullptr;
-                               });
+        uint8_t *qd = qs + buf * kMRows * KB;
+        uint8_t *od = dos + buf * kMRows * VB;
+        if constexpr (kChQ == kChO) {
+#pragma unroll
+            for (int i = tid / kChQ; i < kMRows; i += NT / kChQ) {
+                const int r = rb + i, ch = tid % kChQ;
+                const long long row = r < re ? row_of(r) : 0;
+                const bool okq = r < re && ch * 8 < D, oko = r < re && ch * 8 < Dv;
+                cp_async16(smem_u32(qd + swz(i, ch, KB)), okq ? qg + row * D + ch * 8 : qg,
+                           okq ? 16 : 0);
+                cp_async16(smem_u32(od + swz(i, ch, VB)), oko ? dog + row * Dv + ch * 8 : dog,
+                           oko ? 16 : 0);
+            }
+        } else {
+#pragma unroll
+            for (int i = tid / kChQ; i < kMRows; i += NT / kChQ) {
+                const int r = rb + i, ch = tid % kChQ;
+                const bool ok = r < re && ch * 8 < D;
+                cp_async16(smem_u32(qd + swz(i, ch, KB)), ok ? qg + row_of(r) * D + ch * 8 : qg,
+                           ok ? 16 : 0);
+            }
+#pragma unroll
+            for (int i = tid / kChO; i < kMRows; i += NT / kChO) {
+                const int r = rb + i, ch = tid % kChO;
+                const bool ok = r < re && ch * 8 < Dv;
+                cp_async16(smem_u32(od + swz(i, ch, VB)),
+                           ok ? dog + row_of(r) * Dv + ch * 8 : dog, ok ? 16 : 0);
+            }
+        }
         if (tid < kMRows) {
             // LSE and Dq travel with the tile (no thread waits on them here);
             // rows without a legal key read nothing and are masked by [lo, hi)
@@ -446,6 +470,10 @@ __global__ void __launch_bounds__(256, 2) bwd_dkdv_mma(const BwdParams bp) {
             cp_async4(smem_u32(del_s + buf * kMRows + tid), bp.delta + row, ok ? 4 : 0);
             lo_s[buf * kMRows + tid] = lo;
             hi_s[buf * kMRows + tid] = hi;
+            // the step needs no mask when every row sees all of the tile's keys
+            const bool inner = lo <= k0 && hi >= k0 + kMKeys;
+            const unsigned all = __ballot_sync(0xffffffffu, inner);
+            if (tid == 0) flag_s[buf] = all == 0xffffffffu;
         }
     };
 
@@ -489,15 +517,25 @@ __global__ void __launch_bounds__(256, 2) bwd_dkdv_mma(const BwdParams bp) {
                     MmaOp<T>::run(s[2 * np + 1], a, bq[2], bq[3]);
                 }
             }
+            const bool inner = flag_s[buf] != 0;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int key = k0 + kw + g + 8 * (c >> 1);
-                    const int rl = buf * kMRows + 8 * j + 2 * t + (c & 1);
-                    const bool ok = key >= lo_s[rl] && key < hi_s[rl];
-                    s[j][c] = ok ? exp2f(s[j][c] * p.scale_log2 - lse_s[rl] * kLog2e) : 0.f;
-                    pmine[(j * 4 + c) * 32 + lane] = s[j][c];
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int rl = buf * kMRows + 8 * j + 2 * t + cc;
+                    const float l2 = lse_s[rl] * kLog2e;
+                    int lo = INT_MIN, hi = INT_MAX;
+                    if (!inner) {
+                        lo = lo_s[rl];
+                        hi = hi_s[rl];
+                    }
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int c = 2 * hh + cc;
+                        const int key = k0 + kw + g + 8 * hh;
+                        s[j][c] = key >= lo && key < hi ? exp2f(s[j][c] * p.scale_log2 - l2) : 0.f;
+                        pmine[(j * 4 + c) * 32 + lane] = s[j][c];
+                    }
                 }
             sm100::named_bar_arrive(1 + (warp & 3), 64);
         } else {
@@ -692,17 +730,30 @@ __global__ void __launch_bounds__(128) bwd_dq_mma(const BwdParams bp) {
                 }
             }
         }
-        // dS (in s)
+        // dS (in s); no mask where all of the warp's rows see the whole tile
+        const bool inner = __all_sync(0xffffffffu, lo[0] <= kt0 && lo[1] <= kt0 &&
+                                                       hi[0] >= kt0 + kQKeys &&
+                                                       hi[1] >= kt0 + kQKeys);
+        if (inner) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
+            for (int j = 0; j < 8; ++j)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int hh = c >> 1;
-                const int key = kt0 + 8 * j + 2 * t + (c & 1);
-                const bool ok = key >= lo[hh] && key < hi[hh];
-                const float pr = ok ? exp2f(s[j][c] * p.scale_log2 - l2[hh]) : 0.f;
-                s[j][c] = pr * (dp[j][c] - dl[hh]);
-            }
+                for (int c = 0; c < 4; ++c) {
+                    const int hh = c >> 1;
+                    s[j][c] = exp2f(s[j][c] * p.scale_log2 - l2[hh]) * (dp[j][c] - dl[hh]);
+                }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int hh = c >> 1;
+                    const int key = kt0 + 8 * j + 2 * t + (c & 1);
+                    const bool ok = key >= lo[hh] && key < hi[hh];
+                    const float pr = ok ? exp2f(s[j][c] * p.scale_log2 - l2[hh]) : 0.f;
+                    s[j][c] = pr * (dp[j][c] - dl[hh]);
+                }
+        }
         // dQ += dS K, contracting over the 64 keys
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
@@ -822,7 +873,8 @@ int launch_mma_bwd_t(const BwdParams &bp, cudaStream_t stream) {
     int rc = 0;
     if (ktiles > 0) {
         const size_t s = (size_t)kMKeys * 2 * (DW + DVW) +
-                         (size_t)kMStages * kMRows * (2 * (DW + DVW) + 16) + 4 * 16 * 32 * 4;
+                         (size_t)kMStages * kMRows * (2 * (DW + DVW) + 16) + 4 * 16 * 32 * 4 +
+                         kMStages * 4;
         rc = launch_k(bwd_dkdv_mma<T, DW, DVW>, dim3((unsigned)(ktiles * y)), 256, s, stream,
                       "bwd_dkdv_mma", bp);
         if (rc) return rc;
