@@ -9,6 +9,10 @@ Second workload (the "decode" object): bf16 batched decode B=64 Hq=32 Hkv=8
 Q=1 D=Dv=128, key lengths uniform on [0, 8192] (0 included), KV padded to
 8192, KV GB/s counted over valid key rows: bytes = sum_b Kb * Hkv * (D+Dv) * 2.
 
+Third workload (the "backward" object): attn_bwd on the prefill workload for
+a seeded N(0,1) dO, FLOP = B * Hq * pairs * (6*D + 4*Dv) (the five products
+S, dP, dV, dK, dQ).
+
 Timing: W warm-up steps, then K timed steps; before every step a 512 MiB
 buffer is written to flush L2, and each step is bracketed by CUDA events on
 the launching stream (device time of the attention call only); a barrier and
@@ -299,6 +303,30 @@ def measure_decode(args, world, rank, dev, stream, flush, attn, synth):
                 paged_ms=paged_ms, page=page)
 
 
+def measure_backward(args, world, rank, dev, stream, flush, attn, synth, pin):
+    """attn_bwd on the prefill workload with a seeded N(0,1) dO: one step is
+    the three launches (rowsum(dO*O), dK/dV, dQ), O and LSE from attn_fwd."""
+    P = PREFILL
+    q, k, v = pin.q.to(dev), pin.k.to(dev), pin.v.to(dev)
+    o, lse = attn.attn_fwd(q, k, v, stream=stream)
+    g = synth.make_dout(pin, seed=4321 + rank).to(dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    # five products over the legal pairs: S, dP, dV, dK, dQ
+    flop = P["B"] * P["Hq"] * legal_pairs(P["Q"], P["K"]) * (6 * P["D"] + 4 * P["Dv"])
+
+    def bwd():
+        attn.attn_bwd(q, k, v, o, lse, g, dq, dk, dv, stream=stream)
+
+    bwd()
+    torch.cuda.synchronize()
+    n0 = attn.kernel_launches()
+    steps = max(3, args.steps // 4)
+    times = time_steps(bwd, steps, 3, flush, stream)
+    launches = (attn.kernel_launches() - n0) // (steps + 3)
+    ms = max_over_ranks(sum(times) / len(times), world)
+    return dict(flop=flop, ms=ms, launches=launches, steps=steps)
+
+
 def run_gpu(args, world, rank, local):
     import causal_gqa_attention_online_gb300 as attn
     from causal_gqa_attention_online_gb300 import build_ext, synth
@@ -337,6 +365,27 @@ def run_gpu(args, world, rank, local):
             "gpu_launches": int(r["launches"] * args.steps),
             "clocks": r["clocks"],
         })
+    if args.only in ("all", "backward"):
+        if pin is None:
+            pin = synth.prefill_bf16_b4_h32x8_s4096_d128(seed=1234 + rank)
+        bw = measure_backward(args, world, rank, dev, stream, flush, attn, synth, pin)
+        tfb = bw["flop"] / (bw["ms"] * 1e-3) / 1e12
+        bwd = {"workload": PREFILL_NAME + ", backward (dQ, dK, dV) for N(0,1) dO",
+               "value": round(world * tfb, 3), "unit": "TFLOP/s",
+               "ms_per_step": round(bw["ms"], 5), "steps": bw["steps"],
+               "flop_per_step": bw["flop"], "gpu_launches": int(bw["launches"] * bw["steps"]),
+               "kernels": "mma.sync m16n8k16 (warp-level tensor cores)",
+               "roofline": {"bound": "tensor", "achieved": round(tfb, 3), "peak": tf_peak,
+                            "unit": "TFLOP/s", "frac": round(tfb / tf_peak, 4),
+                            "traffic": traffic.get("backward"),
+                            "peak_source": f"{peak_src} bf16 dense (cuBLAS burst)"}}
+        if args.only == "backward":
+            result.update({"value": bwd["value"], "unit": "TFLOP/s",
+                           "ms_per_step": bwd["ms_per_step"],
+                           "config": {"workload": bwd["workload"]}, "roofline": bwd["roofline"],
+                           "gpu_launches": bwd["gpu_launches"]})
+        else:
+            result["backward"] = bwd
     if args.only in ("all", "decode"):
         d = measure_decode(args, world, rank, dev, stream, flush, attn, synth)
         gbs = d["kv_bytes"] / (d["ms"] * 1e-3) / 1e9
@@ -368,6 +417,7 @@ def run_gpu(args, world, rank, local):
 KERNEL_SOURCES = {
     "prefill": "causal_gqa_attention_online_gb300/csrc/kernel_prefill_tc.cu",
     "decode": "causal_gqa_attention_online_gb300/csrc/kernel_decode.cu",
+    "backward": "causal_gqa_attention_online_gb300/csrc/kernel_bwd.cu",
 }
 
 
@@ -459,7 +509,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seconds", type=float, default=60.0,
                     help="--impl reference: total seconds of oracle work over all steps")
-    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode"],
+    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "backward"],
                     help="profiling aid: run one workload (the JSON line then lacks the other)")
     args = ap.parse_args()
     if args.warmup < 3:
