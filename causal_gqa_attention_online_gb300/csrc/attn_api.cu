@@ -126,7 +126,7 @@ int validate(const void *q, const void *k, const void *v, const void *o, const f
         set_error("unknown dtype %d", dtype);
         return ATTN_ERR_INVALID;
     }
-    if (algo < ATTN_ALGO_AUTO || algo > ATTN_ALGO_DECODE) {
+    if (algo < ATTN_ALGO_AUTO || algo > ATTN_ALGO_MMA) {
         set_error("unknown algo %d", algo);
         return ATTN_ERR_INVALID;
     }
@@ -164,6 +164,8 @@ int run(AttnParams &p, int dtype, int algo, cudaStream_t stream) {
                 chosen = ATTN_ALGO_DECODE;
             else if (prefill_tc_supported(p, dtype))
                 chosen = ATTN_ALGO_TCGEN05;
+            else if (fwd_mma_supported(p, dtype))
+                chosen = ATTN_ALGO_MMA;
         }
     } else if (algo == ATTN_ALGO_DECODE && !decode_supported(p, dtype)) {
         set_error("decode kernel does not take this shape/dtype");
@@ -171,9 +173,13 @@ int run(AttnParams &p, int dtype, int algo, cudaStream_t stream) {
     } else if (algo == ATTN_ALGO_TCGEN05 && !prefill_tc_supported(p, dtype)) {
         set_error("tcgen05 prefill kernel does not take this shape/dtype");
         return ATTN_ERR_UNSUPPORTED;
+    } else if (algo == ATTN_ALGO_MMA && !fwd_mma_supported(p, dtype)) {
+        set_error("mma forward kernel takes bf16/fp16 with D, Dv multiples of 8 up to 256");
+        return ATTN_ERR_UNSUPPORTED;
     }
 
     if (chosen == ATTN_ALGO_TCGEN05) return launch_prefill_tc(p, dtype, stream);
+    if (chosen == ATTN_ALGO_MMA) return launch_fwd_mma(p, dtype, stream);
 
     // Split the key axis when the (sequence, KV head, row-block) units alone
     // would leave SMs idle.  A row whose legal keys fall in one split is

@@ -28,6 +28,11 @@ int launch_decode(const AttnParams &p, int dtype, cudaStream_t stream);
 bool prefill_tc_supported(const AttnParams &p, int dtype);
 int launch_prefill_tc(const AttnParams &p, int dtype, cudaStream_t stream);
 
+// mma.sync forward (bf16/fp16, D and Dv multiples of 8 up to 256): the
+// tensor-core path for head widths the tcgen05 prefill kernel does not take.
+bool fwd_mma_supported(const AttnParams &p, int dtype);
+int launch_fwd_mma(const AttnParams &p, int dtype, cudaStream_t stream);
+
 // Backward: rowsum(dO * O), then dK/dV and dQ.  mma: the mma.sync kernels
 // (bf16/fp16, bwd_mma_supported); otherwise the CUDA-core kernels.
 bool bwd_mma_supported(const AttnParams &p, int dtype);

@@ -343,3 +343,59 @@ def test_mask_none_rejects_window():
     with pytest.raises(AttnError) as ei:
         attn_fwd(inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), window=3, mask="none")
     assert ei.value.status == 1
+
+
+# mma.sync forward: head widths above the tcgen05 kernel's (up to 256), and
+# the narrower widths it also takes when chosen explicitly
+MMA_SHAPES = [
+    # B, Hq, Hkv, Q, K, D, Dv
+    (2, 8, 2, 200, 200, 256, 256),
+    (1, 8, 2, 130, 330, 256, 256),    # Q < K: bottom-right offset
+    (1, 4, 2, 300, 40, 256, 256),     # Q > K: leading rows without keys
+    (1, 16, 2, 100, 357, 192, 160),   # G = 8, padded tile columns
+    (1, 4, 4, 77, 200, 136, 256),     # MHA, D just above 128
+    (2, 6, 2, 90, 150, 256, 64),
+    (1, 8, 2, 3, 67, 256, 256),       # short query chunk
+    (2, 8, 2, 150, 150, 128, 128),
+    (1, 4, 1, 65, 131, 64, 64),
+    (1, 8, 4, 1, 700, 256, 256),      # one query row
+]
+
+
+@pytest.mark.parametrize("shape", MMA_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_mma_forward_shapes(shape, dtype):
+    B, Hq, Hkv, Q, K, D, Dv = shape
+    g = np.random.default_rng(Q + K)
+    sk = g.integers(0, K + 1, size=B).astype(np.int32)
+    sk[0] = K
+    inp = synth.make_padded(B, Hq, Hkv, Q, K, D, Dv, dtype, seed=37, seqlens_k=sk, pad_value=NAN)
+    parity.check(inp, "mma", f"mma {dtype} {shape}")
+
+
+@pytest.mark.parametrize("window", [1, 50, 129])
+@pytest.mark.parametrize("mask", [0, 1, 2])
+def test_mma_forward_window_and_masks(window, mask):
+    if mask == 2:
+        window = 0
+    inp = synth.make_padded(2, 8, 2, 180, 260, 256, 256, "bf16", seed=38, window=window)
+    parity.check(inp, "mma", f"mma window {window} mask {mask}", mask=mask)
+
+
+def test_mma_forward_varlen_packed_and_auto_choice():
+    sk = np.array([0, 5, 33, 130, 1, 640, 0, 300], np.int32)
+    sq = np.minimum(sk, np.array([0, 5, 7, 64, 1, 512, 0, 100]))
+    for w in (0, 100):
+        inp = synth.make_packed(sq, sk, 16, 4, 256, 256, "bf16", seed=39, window=w)
+        parity.check(inp, "auto", f"auto (mma) varlen w={w}")
+
+
+def test_mma_forward_rejects_fp32_and_wide_heads():
+    inp = synth.make_padded(1, 2, 1, 8, 8, 64, 64, "f32", seed=40)
+    with pytest.raises(AttnError) as ei:
+        parity.run_gpu(inp, "mma")
+    assert ei.value.status == 2
+    inp = synth.make_padded(1, 2, 1, 8, 8, 256, 250, "bf16", seed=40)
+    with pytest.raises(AttnError) as ei:
+        parity.run_gpu(inp, "mma")
+    assert ei.value.status == 2
