@@ -118,8 +118,8 @@ int validate(const void *q, const void *k, const void *v, const void *o, const f
         set_error("Hq (%d) must be a positive multiple of Hkv (%d)", Hq, Hkv);
         return ATTN_ERR_INVALID;
     }
-    if (D < 1 || D > 256 || Dv < 1 || Dv > 256) {
-        set_error("head widths must be in [1, 256] (D=%d Dv=%d)", D, Dv);
+    if (D < 1 || D > 512 || Dv < 1 || Dv > 512) {
+        set_error("head widths must be in [1, 512] (D=%d Dv=%d)", D, Dv);
         return ATTN_ERR_INVALID;
     }
     if (dtype < ATTN_F32 || dtype > ATTN_BF16) {
@@ -297,6 +297,10 @@ int bwd_common(const void *q, const void *k, const void *v, const void *o, const
     g_last_error[0] = '\0';
     int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Q, K, D, Dv, dtype, ATTN_ALGO_AUTO);
     if (rc) return rc;
+    if (D > 256 || Dv > 256) {
+        set_error("the backward takes head widths up to 256 (D=%d Dv=%d)", D, Dv);
+        return ATTN_ERR_UNSUPPORTED;
+    }
     if (algo != ATTN_ALGO_AUTO && algo != ATTN_ALGO_GENERIC && algo != ATTN_ALGO_MMA) {
         set_error("backward algo must be ATTN_ALGO_AUTO, ATTN_ALGO_GENERIC or ATTN_ALGO_MMA "
                   "(got %d)", algo);

@@ -1,5 +1,5 @@
 // kernel_generic.cu -- CUDA-core online-softmax attention forward (any storage
-// dtype, head widths up to 256) and the split-KV combine kernels.
+// dtype, head widths up to 512) and the split-KV combine kernels.
 //
 // This is the fp32 path ("Accelerating PyTorch on AMD GPUs with FlyDSL",
 // section on FMHA through AOTriton: that attention kernel family has no FP32
@@ -331,7 +331,8 @@ int launch_generic_dtype(const AttnParams &p, cudaStream_t stream) {
     if (p.Dv <= 32) return launch_generic_t<T, 1>(p, stream);
     if (p.Dv <= 64) return launch_generic_t<T, 2>(p, stream);
     if (p.Dv <= 128) return launch_generic_t<T, 4>(p, stream);
-    return launch_generic_t<T, 8>(p, stream);
+    if (p.Dv <= 256) return launch_generic_t<T, 8>(p, stream);
+    return launch_generic_t<T, 16>(p, stream);
 }
 
 }  // namespace

@@ -13,7 +13,7 @@ void set_error(const char *fmt, ...);
 void count_launch();  // one successful kernel launch
 int sm_count(int device);
 
-// CUDA-core online softmax (any dtype; D, Dv <= 256).  Honours p.nsplit.
+// CUDA-core online softmax (any dtype; D, Dv <= 512).  Honours p.nsplit.
 int launch_generic(const AttnParams &p, int dtype, cudaStream_t stream);
 // Split-KV partial merge, driven by the problem's layout.
 int launch_combine_rows(const AttnParams &p, int dtype, cudaStream_t stream);

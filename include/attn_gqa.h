@@ -80,7 +80,7 @@ enum attn_status {
 /* Kernel selection for the *_algo entry points. */
 enum attn_algo {
     ATTN_ALGO_AUTO = 0,     /* choose by dtype, head widths and query length */
-    ATTN_ALGO_GENERIC = 1,  /* CUDA-core online softmax: any dtype, D, Dv <= 256 */
+    ATTN_ALGO_GENERIC = 1,  /* CUDA-core online softmax: any dtype, D, Dv <= 512 */
     ATTN_ALGO_TCGEN05 = 2,  /* tcgen05/TMEM prefill: bf16/fp16, D, Dv multiples of 16 in [64, 128] */
     ATTN_ALGO_DECODE = 3,   /* split-KV tensor-core decode: bf16/fp16, Q*G <= 16 */
     ATTN_ALGO_MMA = 4       /* warp-level mma.sync tensor cores, bf16/fp16: the forward for
@@ -109,7 +109,7 @@ enum attn_mask {
  *   scale       multiplies Q.K (pass 1/sqrt(D) for the usual scaling).
  *   dtype       attn_dtype of q, k, v and o.
  * Returns ATTN_OK, ATTN_ERR_INVALID (bad pointer or size, Hq % Hkv != 0,
- * D or Dv outside [1, 256]), ATTN_ERR_UNSUPPORTED or ATTN_ERR_CUDA.
+ * D or Dv outside [1, 512]), ATTN_ERR_UNSUPPORTED or ATTN_ERR_CUDA.
  * B = 0, Q = 0 or Hq = 0 work is a successful no-op.
  */
 ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
@@ -278,6 +278,7 @@ ATTN_API int attn_fwd_staged(const void *hq, const void *hk, const void *hv, voi
  *   seqlens_q, seqlens_k, window, scale, mask   as in attn_fwd_ex
  *   algo          ATTN_ALGO_AUTO (mma.sync kernels where they apply, else the
  *                 CUDA-core kernels), ATTN_ALGO_GENERIC or ATTN_ALGO_MMA
+ * Head widths up to 256 (wider ones return ATTN_ERR_UNSUPPORTED).
  * All pointers are device memory, 16-byte aligned.  A workspace of
  * 4 * B * Q * Hq bytes comes from the library's stream-ordered pool.  The
  * result is deterministic (no atomics: dk/dv and dq are written by separate

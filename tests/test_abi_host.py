@@ -52,7 +52,7 @@ def _call_fwd(lib, q=1 << 20, k=1 << 21, v=1 << 22, o=1 << 23, lse=None, B=1, Hq
     (dict(Hq=6, Hkv=4), "multiple"),
     (dict(Hkv=0), "multiple"),
     (dict(D=0), "head widths"),
-    (dict(Dv=257), "head widths"),
+    (dict(Dv=513), "head widths"),
     (dict(dtype=7), "dtype"),
     (dict(algo=9), "algo"),
     (dict(q=0), "non-null"),
@@ -91,3 +91,25 @@ def test_binding_has_no_cpu_path():
         if f.endswith(".py"):
             text = open(os.path.join(ROOT, "causal_gqa_attention_online_gb300", f)).read()
             assert "import oracle" not in text and "from oracle" not in text, f
+
+
+def _call_bwd(lib, lse=1 << 24, dout=1 << 25, dq=1 << 26, D=64, Dv=64, algo=0, mask=0,
+              window=0, dtype=2):
+    vp = ctypes.c_void_p
+    return lib.attn_bwd(vp(1 << 20), vp(1 << 21), vp(1 << 22), vp(1 << 23), vp(lse), vp(dout),
+                        vp(dq), vp(1 << 27), vp(1 << 28), 1, 4, 2, 8, 8, D, Dv, None, None,
+                        window, 0.125, mask, dtype, algo, None)
+
+
+@pytest.mark.parametrize("kw,rc,needle", [
+    (dict(lse=0), 1, "non-null"),
+    (dict(dout=0), 1, "non-null"),
+    (dict(dq=(1 << 26) + 4), 1, "aligned"),
+    (dict(algo=2), 1, "backward algo"),
+    (dict(mask=5), 1, "mask"),
+    (dict(mask=2, window=3), 1, "window"),
+    (dict(D=320), 2, "up to 256"),
+])
+def test_bwd_invalid_arguments_rejected_on_host(lib, kw, rc, needle):
+    assert _call_bwd(lib, **kw) == rc
+    assert needle in lib.attn_last_error().decode()

@@ -399,3 +399,27 @@ def test_mma_forward_rejects_fp32_and_wide_heads():
     with pytest.raises(AttnError) as ei:
         parity.run_gpu(inp, "mma")
     assert ei.value.status == 2
+
+
+# head widths above 256 (up to 512) run on the CUDA-core kernel
+@pytest.mark.parametrize("dtype,dims", [("f32", (512, 512)), ("bf16", (320, 512)),
+                                        ("f16", (512, 264))])
+def test_wide_heads_cuda_cores(dtype, dims):
+    D, Dv = dims
+    sk = np.array([90, 0, 33], np.int32)
+    inp = synth.make_padded(3, 4, 2, 70, 90, D, Dv, dtype, seed=41, seqlens_k=sk, pad_value=NAN)
+    parity.check(inp, "auto", f"wide heads {dtype} {dims}")
+    inp = synth.make_padded(1, 8, 2, 1, 3000, D, Dv, dtype, seed=42, window=700)
+    parity.check(inp, "auto", f"wide heads decode {dtype} {dims}")
+
+
+def test_wide_heads_rejected_above_512_and_by_tensor_kernels():
+    inp = synth.make_padded(1, 2, 1, 8, 8, 520, 64, "bf16", seed=43)
+    with pytest.raises(AttnError) as ei:
+        parity.run_gpu(inp, "auto")
+    assert ei.value.status == 1
+    inp = synth.make_padded(1, 2, 1, 8, 8, 512, 512, "bf16", seed=43)
+    for algo in ("mma", "tcgen05", "decode"):
+        with pytest.raises(AttnError) as ei:
+            parity.run_gpu(inp, algo)
+        assert ei.value.status == 2
