@@ -174,7 +174,7 @@ int run(AttnParams &p, int dtype, int algo, cudaStream_t stream) {
         set_error("tcgen05 prefill kernel does not take this shape/dtype");
         return ATTN_ERR_UNSUPPORTED;
     } else if (algo == ATTN_ALGO_MMA && !fwd_mma_supported(p, dtype)) {
-        set_error("mma forward kernel takes bf16/fp16 with D, Dv multiples of 8 up to 256");
+        set_error("mma forward kernel takes bf16/fp16 with D, Dv multiples of 8 up to 512");
         return ATTN_ERR_UNSUPPORTED;
     }
 

@@ -28,7 +28,7 @@ int launch_decode(const AttnParams &p, int dtype, cudaStream_t stream);
 bool prefill_tc_supported(const AttnParams &p, int dtype);
 int launch_prefill_tc(const AttnParams &p, int dtype, cudaStream_t stream);
 
-// mma.sync forward (bf16/fp16, D and Dv multiples of 8 up to 256): the
+// mma.sync forward (bf16/fp16, D and Dv multiples of 8 up to 512): the
 // tensor-core path for head widths the tcgen05 prefill kernel does not take.
 bool fwd_mma_supported(const AttnParams &p, int dtype);
 int launch_fwd_mma(const AttnParams &p, int dtype, cudaStream_t stream);

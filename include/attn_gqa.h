@@ -84,7 +84,7 @@ enum attn_algo {
     ATTN_ALGO_TCGEN05 = 2,  /* tcgen05/TMEM prefill: bf16/fp16, D, Dv multiples of 16 in [64, 128] */
     ATTN_ALGO_DECODE = 3,   /* split-KV tensor-core decode: bf16/fp16, Q*G <= 16 */
     ATTN_ALGO_MMA = 4       /* warp-level mma.sync tensor cores, bf16/fp16: the forward for
-                               D, Dv multiples of 8 up to 256 (chosen by AUTO where the
+                               D, Dv multiples of 8 up to 512 (chosen by AUTO where the
                                tcgen05 and decode kernels do not apply), the backward for
                                D, Dv multiples of 8 up to 128 */
 };

@@ -359,6 +359,12 @@ MMA_SHAPES = [
     (2, 8, 2, 150, 150, 128, 128),
     (1, 4, 1, 65, 131, 64, 64),
     (1, 8, 4, 1, 700, 256, 256),      # one query row
+    # wide heads: warp pairs split the width
+    (1, 8, 2, 130, 200, 512, 512),
+    (2, 4, 2, 90, 150, 320, 512),
+    (1, 4, 1, 70, 70, 512, 64),
+    (1, 8, 2, 100, 300, 128, 512),
+    (1, 6, 2, 40, 100, 264, 200),
 ]
 
 
@@ -375,11 +381,12 @@ def test_mma_forward_shapes(shape, dtype):
 
 @pytest.mark.parametrize("window", [1, 50, 129])
 @pytest.mark.parametrize("mask", [0, 1, 2])
-def test_mma_forward_window_and_masks(window, mask):
+@pytest.mark.parametrize("width", [256, 512])
+def test_mma_forward_window_and_masks(window, mask, width):
     if mask == 2:
         window = 0
-    inp = synth.make_padded(2, 8, 2, 180, 260, 256, 256, "bf16", seed=38, window=window)
-    parity.check(inp, "mma", f"mma window {window} mask {mask}", mask=mask)
+    inp = synth.make_padded(2, 8, 2, 180, 260, width, width, "bf16", seed=38, window=window)
+    parity.check(inp, "mma", f"mma window {window} mask {mask} width {width}", mask=mask)
 
 
 def test_mma_forward_varlen_packed_and_auto_choice():
@@ -401,16 +408,19 @@ def test_mma_forward_rejects_fp32_and_wide_heads():
     assert ei.value.status == 2
 
 
-# head widths above 256 (up to 512) run on the CUDA-core kernel
+# head widths above 256 (up to 512): the CUDA-core kernel (every dtype) and
+# the mma.sync kernel (bf16 / fp16, the automatic choice)
 @pytest.mark.parametrize("dtype,dims", [("f32", (512, 512)), ("bf16", (320, 512)),
                                         ("f16", (512, 264))])
 def test_wide_heads_cuda_cores(dtype, dims):
     D, Dv = dims
     sk = np.array([90, 0, 33], np.int32)
     inp = synth.make_padded(3, 4, 2, 70, 90, D, Dv, dtype, seed=41, seqlens_k=sk, pad_value=NAN)
-    parity.check(inp, "auto", f"wide heads {dtype} {dims}")
+    parity.check(inp, "generic", f"wide heads {dtype} {dims}")
     inp = synth.make_padded(1, 8, 2, 1, 3000, D, Dv, dtype, seed=42, window=700)
-    parity.check(inp, "auto", f"wide heads decode {dtype} {dims}")
+    parity.check(inp, "generic", f"wide heads decode {dtype} {dims}")
+    if dtype != "f32":
+        parity.check(inp, "auto", f"wide heads decode, auto (mma) {dtype} {dims}")
 
 
 def test_wide_heads_rejected_above_512_and_by_tensor_kernels():
@@ -419,7 +429,7 @@ def test_wide_heads_rejected_above_512_and_by_tensor_kernels():
         parity.run_gpu(inp, "auto")
     assert ei.value.status == 1
     inp = synth.make_padded(1, 2, 1, 8, 8, 512, 512, "bf16", seed=43)
-    for algo in ("mma", "tcgen05", "decode"):
+    for algo in ("tcgen05", "decode"):
         with pytest.raises(AttnError) as ei:
             parity.run_gpu(inp, algo)
         assert ei.value.status == 2
