@@ -9,6 +9,8 @@ Second workload (the "decode" object): bf16 batched decode B=64 Hq=32 Hkv=8
 Q=1 D=Dv=128, key lengths uniform on [0, 8192] (0 included), KV padded to
 8192, KV GB/s counted over valid key rows: bytes = sum_b Kb * Hkv * (D+Dv) * 2.
 
+The "wide_heads" list: bf16 causal prefill with D = Dv = 256 (B=2 Hq=16
+Hkv=4 Q=K=4096) and 512 (B=1), TFLOP/s over legal pairs as above.
 Third workload (the "backward" object): attn_bwd on the prefill workload for
 a seeded N(0,1) dO, FLOP = B * Hq * pairs * (6*D + 4*Dv) (the five products
 S, dP, dV, dK, dQ).
@@ -327,6 +329,32 @@ def measure_backward(args, world, rank, dev, stream, flush, attn, synth, pin):
     return dict(flop=flop, ms=ms, launches=launches, steps=steps)
 
 
+WIDE = [dict(B=2, Hq=16, Hkv=4, Q=4096, K=4096, D=256, Dv=256),
+        dict(B=1, Hq=16, Hkv=4, Q=4096, K=4096, D=512, Dv=512)]
+
+
+def measure_wide(args, world, rank, dev, stream, flush, attn, synth):
+    """bf16 causal prefill with head widths 256 and 512 (the mma.sync kernels
+    attn_fwd chooses for widths the tcgen05 kernel does not take)."""
+    out = []
+    for W in WIDE:
+        inp = synth.make_padded(W["B"], W["Hq"], W["Hkv"], W["Q"], W["K"], W["D"], W["Dv"],
+                                "bf16", seed=777 + rank)
+        q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+        o, lse = attn.attn_fwd(q, k, v, stream=stream)
+        flop = W["B"] * W["Hq"] * legal_pairs(W["Q"], W["K"]) * (2 * W["D"] + 2 * W["Dv"])
+
+        def fwd():
+            attn.attn_fwd(q, k, v, o, lse, stream=stream)
+
+        steps = max(3, args.steps // 4)
+        times = time_steps(fwd, steps, 3, flush, stream)
+        ms = max_over_ranks(sum(times) / len(times), world)
+        out.append((W, flop, ms, steps))
+        del q, k, v, o, lse
+    return out
+
+
 def run_gpu(args, world, rank, local):
     import causal_gqa_attention_online_gb300 as attn
     from causal_gqa_attention_online_gb300 import build_ext, synth
@@ -386,6 +414,23 @@ def run_gpu(args, world, rank, local):
                            "gpu_launches": bwd["gpu_launches"]})
         else:
             result["backward"] = bwd
+    if args.only == "all":
+        wide = []
+        for W, flop, ms, steps in measure_wide(args, world, rank, dev, stream, flush, attn,
+                                               synth):
+            tfw = flop / (ms * 1e-3) / 1e12
+            wide.append({
+                "workload": (f"bf16 causal prefill B={W['B']} Hq={W['Hq']} Hkv={W['Hkv']} "
+                             f"Q=K={W['Q']} D=Dv={W['D']}"),
+                "value": round(world * tfw, 3), "unit": "TFLOP/s", "ms_per_step": round(ms, 5),
+                "steps": steps, "flop_per_step": flop,
+                "kernel": "mma.sync m16n8k16" + (" (warp pairs split the width)"
+                                                 if W["D"] > 256 else ""),
+                "roofline": {"bound": "tensor", "achieved": round(tfw, 3), "peak": tf_peak,
+                             "unit": "TFLOP/s", "frac": round(tfw / tf_peak, 4),
+                             "traffic": None,
+                             "peak_source": f"{peak_src} bf16 dense (cuBLAS burst)"}})
+        result["wide_heads"] = wide
     if args.only in ("all", "decode"):
         d = measure_decode(args, world, rank, dev, stream, flush, attn, synth)
         gbs = d["kv_bytes"] / (d["ms"] * 1e-3) / 1e9
