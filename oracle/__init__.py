@@ -86,6 +86,9 @@ class OracleLib:
         lib.oracle_attn_bwd_padded.argtypes = [f32p, f32p, f32p, f32p, f64p, f64p, f64p] + [
             ci] * 7 + [i32p, i32p, ci, ci, cd, ci]
         lib.oracle_attn_bwd_padded.restype = ci
+        lib.oracle_attn_bwd_sampled.argtypes = [f32p, f32p, f32p, f32p] + [ci] * 7 + [
+            i32p, i32p, ci, ci, cd, i32p, ctypes.c_long, f64p, ci, ci, ci, ci, f64p, f64p, ci]
+        lib.oracle_attn_bwd_sampled.restype = ci
         lib.oracle_legal_pairs.argtypes = [ci, ci, ci, ci]
         lib.oracle_legal_pairs.restype = ctypes.c_longlong
         lib.oracle_max_threads.argtypes = []
@@ -195,6 +198,37 @@ class OracleLib:
             raise ValueError(f"oracle_attn_bwd_padded failed with status {rc}")
         return dq, dk, dv
 
+    def attn_bwd_sampled(self, q, k, v, dout, *, B, Hq, Hkv, Q, K, D, Dv, rows=None,
+                         key_block=None, seqlens_q=None, seqlens_k=None, window=0, scale=None,
+                         mask=0, nthreads=0):
+        """Parts of the padded-layout gradients: dq of ``rows`` (int [n,3] of
+        (b, q, h)) and dk, dv of ``key_block`` = (b, kh, k0, k1).  Returns
+        (dq [n,D], dk [k1-k0,D], dv [k1-k0,Dv]) float64."""
+        if scale is None:
+            scale = 1.0 / np.sqrt(D)
+        q, qp = _f32(q)
+        k, kp = _f32(k)
+        v, vp = _f32(v)
+        g, gp = _f32(dout)
+        if (q.size != B * Q * Hq * D or k.size != B * K * Hkv * D or
+                v.size != B * K * Hkv * Dv or g.size != B * Q * Hq * Dv):
+            raise ValueError("oracle_attn_bwd_sampled: array sizes do not match the dims")
+        sq, sqp = _i32(seqlens_q)
+        sk, skp = _i32(seqlens_k)
+        rows = np.zeros((0, 3), np.int32) if rows is None else np.ascontiguousarray(rows, np.int32)
+        rp = rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+        kb, kh, k0, k1 = key_block if key_block is not None else (0, 0, 0, 0)
+        dq = np.zeros((rows.shape[0], D), np.float64)
+        dk = np.zeros((max(k1 - k0, 0), D), np.float64)
+        dv = np.zeros((max(k1 - k0, 0), Dv), np.float64)
+        rc = self.lib.oracle_attn_bwd_sampled(qp, kp, vp, gp, B, Hq, Hkv, Q, K, D, Dv, sqp, skp,
+                                              int(window), int(mask), float(scale), rp,
+                                              rows.shape[0], _f64p(dq), kb, kh, k0, k1,
+                                              _f64p(dk), _f64p(dv), int(nthreads))
+        if rc != 0:
+            raise ValueError(f"oracle_attn_bwd_sampled failed with status {rc}")
+        return dq, dk, dv
+
     def legal_pairs(self, Qb: int, Kb: int, window: int = 0, mask: int = 0) -> int:
         """Legal (query, key) pairs of one sequence and head, by enumeration."""
         return int(self.lib.oracle_legal_pairs(int(Qb), int(Kb), int(window), int(mask)))
@@ -225,6 +259,10 @@ def attn_padded_rows(*args, **kw):
 
 def attn_bwd_padded(*args, **kw):
     return _default().attn_bwd_padded(*args, **kw)
+
+
+def attn_bwd_sampled(*args, **kw):
+    return _default().attn_bwd_sampled(*args, **kw)
 
 
 def legal_pairs(Qb: int, Kb: int, window: int = 0, mask: int = 0) -> int:

@@ -362,6 +362,148 @@ int oracle_attn_bwd_padded(const float *q, const float *k, const float *v, const
     return bad ? 3 : 0;
 }
 
+/* The same gradients for parts of a large problem (padded layout), each
+ * output row computed on its own with the arithmetic of
+ * oracle_attn_bwd_padded (O, LSE and Dq of a row are recomputed from the
+ * definition wherever the row is needed):
+ *   rows [nrows][3] = (b, q, h):  dq_out [nrows][D] (zeros for a padded row
+ *                                 or a row without a legal key);
+ *   keys [k0, k1) of sequence b, KV head kh:  dk_out [k1-k0][D], dv_out
+ *                                 [k1-k0][Dv], summed over every row of every
+ *                                 query head of the group that attends to them.
+ * Either part may be empty (nrows = 0, or k1 <= k0). */
+int oracle_attn_bwd_sampled(const float *q, const float *k, const float *v, const float *dout,
+                            int B, int Hq, int Hkv, int Q, int K, int D, int Dv,
+                            const int32_t *seqlens_q, const int32_t *seqlens_k, int window,
+                            int mask, double scale, const int32_t *rows, long nrows,
+                            double *dq_out, int kb, int kkh, int k0, int k1, double *dk_out,
+                            double *dv_out, int nthreads)
+{
+    if (check_dims(B, Hq, Hkv, D, Dv) || Q < 0 || K < 0) return 1;
+    if (mask < 0 || mask > 2 || (mask == 2 && window > 0)) return 1;
+    const int G = Hq / Hkv;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int bad = 0;
+    if (nrows > 0) memset(dq_out, 0, sizeof(double) * (size_t)nrows * D);
+    if (k1 > k0) {
+        if (kb < 0 || kb >= B || kkh < 0 || kkh >= Hkv || k0 < 0 || k1 > K) return 1;
+        memset(dk_out, 0, sizeof(double) * (size_t)(k1 - k0) * D);
+        memset(dv_out, 0, sizeof(double) * (size_t)(k1 - k0) * Dv);
+    }
+    /* dQ rows */
+#pragma omp parallel
+    {
+        const size_t kc = (size_t)(K > 0 ? K : 1);
+        double *sc = (double *)malloc(sizeof(double) * kc);
+        double *orow = (double *)malloc(sizeof(double) * (size_t)Dv);
+        if (!sc || !orow) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(dynamic, 8)
+        for (long i = 0; i < nrows; ++i) {
+            if (!sc || !orow) continue;
+            const int b = rows[3 * i], qi = rows[3 * i + 1], h = rows[3 * i + 2];
+            if (b < 0 || b >= B || qi < 0 || qi >= Q || h < 0 || h >= Hq) {
+#pragma omp atomic write
+                bad = 2;
+                continue;
+            }
+            const int kh = h / G;
+            const int Qb = clamp_len(seqlens_q ? seqlens_q[b] : Q, Q);
+            const int Kb = clamp_len(seqlens_k ? seqlens_k[b] : K, K);
+            if (qi >= Qb) continue;
+            const long r = ((long)b * Q + qi) * Hq + h;
+            const float *qrow = q + r * D, *dorow = dout + r * Dv;
+            const float *kbp = k + ((long)b * K * Hkv + kh) * D;
+            const float *vbp = v + ((long)b * K * Hkv + kh) * Dv;
+            double lse;
+            oracle_row(qrow, kbp, vbp, (long)Hkv * D, (long)Hkv * Dv, D, Dv, qi, Qb, Kb, window,
+                       mask, scale, sc, orow, &lse);
+            if (lse == -INFINITY) continue;
+            long lo, hi;
+            legal_keys(qi, Qb, Kb, window, mask, &lo, &hi);
+            double Dq = 0.0;
+            for (int j = 0; j < Dv; ++j) Dq += (double)dorow[j] * orow[j];
+            double *dqrow = dq_out + i * D;
+            for (long kk = lo; kk <= hi; ++kk) {
+                const float *krow = kbp + kk * (long)Hkv * D;
+                const float *vrow = vbp + kk * (long)Hkv * Dv;
+                double acc = 0.0, dp = 0.0;
+                for (int d = 0; d < D; ++d) acc += (double)qrow[d] * (double)krow[d];
+                for (int j = 0; j < Dv; ++j) dp += (double)dorow[j] * (double)vrow[j];
+                const double ds = exp(scale * acc - lse) * (dp - Dq);
+                for (int d = 0; d < D; ++d) dqrow[d] += scale * ds * (double)krow[d];
+            }
+        }
+        free(sc);
+        free(orow);
+    }
+    if (bad || k1 <= k0) return bad ? 3 : 0;
+    /* dK / dV of keys [k0, k1): one task per (head of the group, row) */
+    const int Qb = clamp_len(seqlens_q ? seqlens_q[kb] : Q, Q);
+    const int Kb = clamp_len(seqlens_k ? seqlens_k[kb] : K, K);
+    const long ntask = (long)G * Qb;
+    const long nk = k1 - k0;
+#pragma omp parallel
+    {
+        const size_t kc = (size_t)(K > 0 ? K : 1);
+        double *sc = (double *)malloc(sizeof(double) * kc);
+        double *orow = (double *)malloc(sizeof(double) * (size_t)Dv);
+        double *gk = (double *)calloc((size_t)nk * D, sizeof(double));
+        double *gv = (double *)calloc((size_t)nk * Dv, sizeof(double));
+        if (!sc || !orow || !gk || !gv) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(dynamic, 4)
+        for (long t = 0; t < ntask; ++t) {
+            if (!sc || !orow || !gk || !gv) continue;
+            const int h = kkh * G + (int)(t / Qb), qi = (int)(t % Qb);
+            long lo, hi;
+            legal_keys(qi, Qb, Kb, window, mask, &lo, &hi);
+            if (hi < lo || hi < k0 || lo >= k1) continue;
+            const long r = ((long)kb * Q + qi) * Hq + h;
+            const float *qrow = q + r * D, *dorow = dout + r * Dv;
+            const float *kbp = k + ((long)kb * K * Hkv + kkh) * D;
+            const float *vbp = v + ((long)kb * K * Hkv + kkh) * Dv;
+            double lse;
+            oracle_row(qrow, kbp, vbp, (long)Hkv * D, (long)Hkv * Dv, D, Dv, qi, Qb, Kb, window,
+                       mask, scale, sc, orow, &lse);
+            double Dq = 0.0;
+            for (int j = 0; j < Dv; ++j) Dq += (double)dorow[j] * orow[j];
+            const long a = lo > k0 ? lo : k0, e = hi < k1 - 1 ? hi : k1 - 1;
+            for (long kk = a; kk <= e; ++kk) {
+                const float *krow = kbp + kk * (long)Hkv * D;
+                const float *vrow = vbp + kk * (long)Hkv * Dv;
+                double acc = 0.0, dp = 0.0;
+                for (int d = 0; d < D; ++d) acc += (double)qrow[d] * (double)krow[d];
+                for (int j = 0; j < Dv; ++j) dp += (double)dorow[j] * (double)vrow[j];
+                const double p = exp(scale * acc - lse);
+                const double ds = p * (dp - Dq);
+                for (int d = 0; d < D; ++d) gk[(kk - k0) * D + d] += scale * ds * (double)qrow[d];
+                for (int j = 0; j < Dv; ++j) gv[(kk - k0) * Dv + j] += p * (double)dorow[j];
+            }
+        }
+#pragma omp critical
+        {
+            if (gk && gv) {
+                for (long x = 0; x < nk * D; ++x) dk_out[x] += gk[x];
+                for (long x = 0; x < nk * Dv; ++x) dv_out[x] += gv[x];
+            }
+        }
+        free(sc);
+        free(orow);
+        free(gk);
+        free(gv);
+    }
+    return bad ? 3 : 0;
+}
+
 /* Number of legal (query, key) pairs of one sequence, per head: the unit the
  * throughput figures count (FLOP = pairs * (2D + 2Dv) per head). */
 long long oracle_legal_pairs(int Qb, int Kb, int window, int mask)

@@ -509,6 +509,27 @@ def pin_bwd_invariants(ol):
         assert all(np.all(t == 0.0) for t in z), ("dO = 0", w, mask)
 
 
+def pin_bwd_sampled_matches_full(ol):
+    """The sampled backward (rows of dQ, key blocks of dK / dV, for checks of
+    large problems) gives the pinned full backward's values."""
+    for ci, (B, Hq, Hkv, Q, K, D, Dv, w, sq, sk, mask) in enumerate(BWD_CASES):
+        q, k, v, dout = _bwd_inputs(900 + ci, B, Hq, Hkv, Q, K, D, Dv)
+        kw = dict(B=B, Hq=Hq, Hkv=Hkv, Q=Q, K=K, D=D, Dv=Dv, seqlens_q=sq, seqlens_k=sk,
+                  window=w, scale=0.3, mask=mask)
+        dq, dk, dv = ol.attn_bwd_padded(q, k, v, dout, **kw)
+        rows = np.array([(b, qi, h) for b in range(B) for qi in range(Q) for h in range(Hq)],
+                        np.int32)
+        sdq, _, _ = ol.attn_bwd_sampled(q, k, v, dout, rows=rows, **kw)
+        assert np.array_equal(sdq, dq.reshape(-1, D)), ci
+        for b in range(B):
+            for kh in range(Hkv):
+                for k0, k1 in ((0, K), (K // 2, K), (1, 2)):
+                    _, sdk, sdv = ol.attn_bwd_sampled(q, k, v, dout, key_block=(b, kh, k0, k1),
+                                                      **kw)
+                    assert np.allclose(sdk, dk[b, k0:k1, kh], rtol=1e-12, atol=1e-14), (ci, b)
+                    assert np.allclose(sdv, dv[b, k0:k1, kh], rtol=1e-12, atol=1e-14), (ci, b)
+
+
 ALL_PINS = [pin_golden, pin_sdpa, pin_invariants, pin_packed_matches_padded,
             pin_rows_match_full, pin_legal_pairs, pin_sdpa_masks, pin_bwd_autograd,
-            pin_bwd_finite_differences, pin_bwd_invariants]
+            pin_bwd_finite_differences, pin_bwd_invariants, pin_bwd_sampled_matches_full]

@@ -55,6 +55,11 @@ MUTANTS = [
      "for (long kk = lo; kk < hi; ++kk) {"),
     ("bwd_rowterm_uses_v", "for (int j = 0; j < Dv; ++j) Dq += (double)dorow[j] * orow[j];",
      "for (int j = 0; j < Dv; ++j) Dq += (double)dorow[j] * vb[j];"),
+    # sampled backward (rows of dQ, key blocks of dK / dV)
+    ("bwd_sampled_key_head", "const int h = kkh * G + (int)(t / Qb), qi = (int)(t % Qb);",
+     "const int h = kkh + (int)(t / Qb), qi = (int)(t % Qb);"),
+    ("bwd_sampled_row_term", "const double ds = exp(scale * acc - lse) * (dp - Dq);",
+     "const double ds = exp(scale * acc - lse) * dp;"),
 ]
 
 
