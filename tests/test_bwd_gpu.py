@@ -86,6 +86,19 @@ def compare(dtype, got, ref, what, zeros=None):
                 f"{what} {name}: l2 err {np.linalg.norm(a - r):.3e} vs {np.linalg.norm(r):.3e}"
 
 
+def compare_one(dtype, got, ref, what):
+    """One tensor under the bar of compare()."""
+    mx, l2 = BTOL[dtype]
+    got = np.asarray(got, np.float64)
+    assert np.isfinite(got).all(), f"{what}: non-finite values"
+    err = np.abs(got - ref)
+    scale = max(1.0, float(np.abs(ref).max(initial=0.0)))
+    assert err.max(initial=0.0) <= mx * scale, f"{what}: max err {err.max():.3e}"
+    if l2 is not None and ref.size:
+        assert np.linalg.norm(got - ref) <= l2 * max(np.linalg.norm(ref), 1e-30), \
+            f"{what}: l2 err {np.linalg.norm(got - ref):.3e} vs {np.linalg.norm(ref):.3e}"
+
+
 CASES = [
     # dtype, algo, B, Hq, Hkv, Q, K, D, Dv, window, mask, ragged
     ("bf16", "mma", 2, 8, 2, 200, 200, 128, 128, 0, 0, True),
@@ -193,3 +206,44 @@ def test_bwd_no_query_rows_zeroes_key_gradients():
     attn_bwd(q, k, v, o, lse, o, None, dk, dv)
     torch.cuda.synchronize()
     assert bool((dk == 0).all()) and bool((dv == 0).all())
+
+
+def test_bwd_full_size_sampled():
+    """attn_bwd on the benchmark's launch (bf16 causal B=4 Hq=32 Hkv=8
+    Q=K=4096 D=Dv=128, dO ~ N(0,1)): dQ of sampled rows and dK / dV of the
+    last 64 keys of two (sequence, KV head) pairs against the oracle, and
+    over every key the sum the definition fixes (a KV head's value gradients
+    sum to its rows' dO)."""
+    inp = synth.prefill_bf16_b4_h32x8_s4096_d128()
+    dout = synth.make_dout(inp, seed=4321)
+    dev = torch.device("cuda")
+    q, k, v, g = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev), dout.to(dev)
+    o, lse = attn_fwd(q, k, v)
+    dq, dk, dv = attn_bwd(q, k, v, o, lse, g)
+    torch.cuda.synchronize()
+    B, Hq, Hkv, S, D = inp.B, inp.Hq, inp.Hkv, inp.Q, inp.D
+    G = Hq // Hkv
+    kw = dict(B=B, Hq=Hq, Hkv=Hkv, Q=S, K=S, D=D, Dv=D, scale=inp.scale)
+    qf, kf, vf, gf = (synth.exact_f32(t) for t in (inp.q, inp.k, inp.v, dout))
+    rng = np.random.default_rng(5)
+    rows = np.stack([rng.integers(0, B, 1200), rng.integers(0, S, 1200),
+                     rng.integers(0, Hq, 1200)], axis=1).astype(np.int32)
+    rows = np.concatenate([rows, [[0, 0, 0], [B - 1, S - 1, Hq - 1], [1, S - 1, 5]]]).astype(np.int32)
+    ref_q, _, _ = oracle.attn_bwd_sampled(qf, kf, vf, gf, rows=rows, **kw)
+    got_q = dq.float().cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]]
+    compare_one("bf16", got_q, ref_q, "full-size dq rows")
+    dkc, dvc = dk.float().cpu().numpy(), dv.float().cpu().numpy()
+    for b, kh in ((0, 0), (B - 1, Hkv - 1)):
+        _, ref_k, ref_v = oracle.attn_bwd_sampled(qf, kf, vf, gf, key_block=(b, kh, S - 64, S), **kw)
+        compare_one("bf16", dkc[b, S - 64:, kh], ref_k, f"full-size dk keys b={b} kh={kh}")
+        compare_one("bf16", dvc[b, S - 64:, kh], ref_v, f"full-size dv keys b={b} kh={kh}")
+    # every (sequence, KV head): the value gradients sum to the dO of the
+    # group's rows (each row's probabilities sum to one).  Rounding P to bf16
+    # moves a row's sum by at most u = 2^-8 of its |dO|, rounding dV by u of
+    # each |dV|: the bound is twice that.
+    u = 2.0 ** -8
+    sum_dv = dv.double().sum(dim=1)                                  # [B, Hkv, Dv]
+    gg = g.double().view(B, S, Hkv, G, D)
+    want_dv = gg.sum(dim=(1, 3))
+    bound = 2 * u * (dv.double().abs().sum(dim=1) + gg.abs().sum(dim=(1, 3))) + 1e-3
+    assert bool(((sum_dv - want_dv).abs() <= bound).all()), "value gradients do not sum to dO"
