@@ -114,6 +114,9 @@ CASES = [
     ("f32", "auto", 2, 4, 2, 64, 128, 64, 64, 0, 0, True),
     ("f32", "auto", 1, 8, 2, 33, 90, 80, 96, 9, 0, False),
     ("f32", "generic", 2, 6, 3, 40, 40, 32, 16, 0, 2, True),
+    ("bf16", "mma", 1, 16, 2, 90, 140, 128, 128, 0, 0, True),    # G = 8
+    ("f16", "mma", 1, 32, 2, 40, 70, 64, 64, 30, 0, False),      # G = 16, window
+    ("bf16", "mma", 2, 8, 2, 300, 300, 128, 128, 0, 0, False),   # several row tiles of a key tile
 ]
 
 
@@ -139,6 +142,12 @@ def test_bwd_parity(case):
             structural_zeros(B, Q, K, sq, sk, window, mask))
 
 
+def test_bwd_negative_scale():
+    inp = synth.make_padded(1, 8, 2, 100, 150, 128, 128, "bf16", seed=85, scale=-0.15)
+    dout = synth.make_dout(inp, seed=86)
+    compare("bf16", gpu_bwd(inp, dout, "mma"), oracle_bwd(inp, dout), "negative scale")
+
+
 def test_bwd_deterministic_and_algos_agree():
     inp = synth.make_padded(2, 8, 2, 190, 260, 128, 128, "bf16", seed=81)
     dout = synth.make_dout(inp, seed=82)
@@ -152,17 +161,18 @@ def test_bwd_deterministic_and_algos_agree():
     compare("bf16", a, ref, "mma")
 
 
-def test_bwd_varlen_matches_padded():
+@pytest.mark.parametrize("window", [0, 45])
+def test_bwd_varlen_matches_padded(window):
     sq = np.array([0, 130, 64, 1, 200], np.int32)
     sk = np.array([50, 200, 64, 300, 200], np.int32)
-    pk = synth.make_packed(sq, sk, 8, 2, 128, 128, "bf16", seed=91, window=0)
+    pk = synth.make_packed(sq, sk, 8, 2, 128, 128, "bf16", seed=91, window=window)
     dev = torch.device("cuda")
     q, k, v = pk.q.to(dev), pk.k.to(dev), pk.v.to(dev)
     cq = torch.from_numpy(pk.cu_seqlens_q).to(dev)
     ck = torch.from_numpy(pk.cu_seqlens_k).to(dev)
-    o, lse = attn_fwd_varlen(q, k, v, cq, ck, pk.Q, pk.K)
+    o, lse = attn_fwd_varlen(q, k, v, cq, ck, pk.Q, pk.K, window=window)
     dout = synth.make_dout(pk, seed=92).to(dev)
-    dq, dk, dv = attn_bwd_varlen(q, k, v, o, lse, dout, cq, ck, pk.Q, pk.K)
+    dq, dk, dv = attn_bwd_varlen(q, k, v, o, lse, dout, cq, ck, pk.Q, pk.K, window=window)
     torch.cuda.synchronize()
     # the same problem in the padded layout, through the oracle
     B, Qm, Km = pk.B, pk.Q, pk.K
@@ -177,7 +187,8 @@ def test_bwd_varlen_matches_padded():
     ref = oracle.attn_bwd_padded(pad(synth.exact_f32(pk.q), cqn, Qm), pad(synth.exact_f32(pk.k), ckn, Km),
                                  pad(synth.exact_f32(pk.v), ckn, Km),
                                  pad(dout.float().cpu().numpy(), cqn, Qm), B=B, Hq=8, Hkv=2, Q=Qm,
-                                 K=Km, D=128, Dv=128, seqlens_q=sq, seqlens_k=sk, scale=pk.scale)
+                                 K=Km, D=128, Dv=128, seqlens_q=sq, seqlens_k=sk, scale=pk.scale,
+                                 window=window)
     got = (pad(dq.float().cpu().numpy(), cqn, Qm), pad(dk.float().cpu().numpy(), ckn, Km),
            pad(dv.float().cpu().numpy(), ckn, Km))
     compare("bf16", got, ref, "varlen")

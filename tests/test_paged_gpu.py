@@ -55,6 +55,8 @@ CASES = [
     ("tcgen05", "bf16", 2, 8, 2, 300, 300, 128, 128, 128, 0, 0),
     ("tcgen05", "bf16", 2, 8, 2, 200, 700, 128, 128, 256, 150, 0),
     ("tcgen05", "f16", 1, 8, 4, 260, 400, 64, 64, 128, 0, 1),
+    ("mma", "bf16", 2, 8, 2, 120, 300, 256, 256, 16, 0, 0),
+    ("mma", "f16", 1, 4, 2, 70, 200, 512, 512, 64, 40, 0),
     ("generic", "f32", 2, 4, 2, 50, 90, 64, 48, 32, 0, 0),
     ("generic", "f32", 2, 4, 2, 50, 90, 32, 32, 8, 11, 0),
 ]
