@@ -414,7 +414,7 @@ def run_gpu(args, world, rank, local):
                            "gpu_launches": bwd["gpu_launches"]})
         else:
             result["backward"] = bwd
-    if args.only == "all":
+    if args.only in ("all", "wide"):
         wide = []
         for W, flop, ms, steps in measure_wide(args, world, rank, dev, stream, flush, attn,
                                                synth):
@@ -428,9 +428,14 @@ def run_gpu(args, world, rank, local):
                                                  if W["D"] > 256 else ""),
                 "roofline": {"bound": "tensor", "achieved": round(tfw, 3), "peak": tf_peak,
                              "unit": "TFLOP/s", "frac": round(tfw / tf_peak, 4),
-                             "traffic": None,
+                             "traffic": traffic.get(f"wide{W['D']}"),
                              "peak_source": f"{peak_src} bf16 dense (cuBLAS burst)"}})
         result["wide_heads"] = wide
+        if args.only == "wide":
+            result.update({"value": wide[0]["value"], "unit": "TFLOP/s",
+                           "ms_per_step": wide[0]["ms_per_step"],
+                           "config": {"workload": wide[0]["workload"]},
+                           "roofline": wide[0]["roofline"]})
     if args.only in ("all", "decode"):
         d = measure_decode(args, world, rank, dev, stream, flush, attn, synth)
         gbs = d["kv_bytes"] / (d["ms"] * 1e-3) / 1e9
@@ -463,6 +468,8 @@ KERNEL_SOURCES = {
     "prefill": "causal_gqa_attention_online_gb300/csrc/kernel_prefill_tc.cu",
     "decode": "causal_gqa_attention_online_gb300/csrc/kernel_decode.cu",
     "backward": "causal_gqa_attention_online_gb300/csrc/kernel_bwd.cu",
+    "wide256": "causal_gqa_attention_online_gb300/csrc/kernel_fwd_mma.cu",
+    "wide512": "causal_gqa_attention_online_gb300/csrc/kernel_fwd_mma.cu",
 }
 
 
@@ -554,7 +561,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seconds", type=float, default=60.0,
                     help="--impl reference: total seconds of oracle work over all steps")
-    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "backward"],
+    ap.add_argument("--only", default="all",
+                    choices=["all", "prefill", "decode", "backward", "wide"],
                     help="profiling aid: run one workload (the JSON line then lacks the other)")
     args = ap.parse_args()
     if args.warmup < 3:
