@@ -329,6 +329,46 @@ def measure_backward(args, world, rank, dev, stream, flush, attn, synth, pin):
     return dict(flop=flop, ms=ms, launches=launches, steps=steps)
 
 
+def measure_small_configs(args, world, rank, dev, stream, flush, attn, synth):
+    """The other named workloads, each through attn_fwd / attn_fwd_varlen as
+    a caller runs it: fp32 prefill B=1 Hq=4 Hkv=2 Q=64 K=128 D=Dv=64, fp32
+    decode B=1 Hq=8 Hkv=2 Q=1 K=2053 D=80 Dv=96, and the bf16 varlen chunked
+    prefill (16 packed sequences, Hq=16 Hkv=4, window 1024).  Returns
+    [(name, inputs, FLOP, KV bytes, ms)]."""
+    out = []
+    named = [("fp32 prefill B=1 Hq=4 Hkv=2 Q=64 K=128 D=Dv=64",
+              synth.prefill_f32_b1_h4x2_q64_k128_d64(seed=1234 + rank)),
+             ("fp32 decode B=1 Hq=8 Hkv=2 Q=1 K=2053 D=80 Dv=96",
+              synth.decode_f32_b1_h8x2_k2053_d80x96(seed=1234 + rank)),
+             ("bf16 varlen chunked prefill: 16 packed sequences, Kb U[0,4096] incl. empty, "
+              "Qb = min(512, Kb), Hq=16 Hkv=4 D=Dv=128, window 1024",
+              synth.varlen_bf16_16seq_h16x4_k4096_q512_w1024(seed=1234 + rank))]
+    for name, inp in named:
+        q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+        es = inp.q.element_size()
+        if inp.layout == "padded":
+            Qb = np.full(inp.B, inp.Q) if inp.seqlens_q is None else inp.seqlens_q
+            Kb = np.full(inp.B, inp.K) if inp.seqlens_k is None else inp.seqlens_k
+
+            def run():
+                attn.attn_fwd(q, k, v, scale=inp.scale, window=inp.window, stream=stream)
+        else:
+            cq = torch.from_numpy(inp.cu_seqlens_q).to(dev)
+            ck = torch.from_numpy(inp.cu_seqlens_k).to(dev)
+            Qb = np.diff(inp.cu_seqlens_q)
+            Kb = np.diff(inp.cu_seqlens_k)
+
+            def run():
+                attn.attn_fwd_varlen(q, k, v, cq, ck, inp.Q, inp.K, scale=inp.scale,
+                                     window=inp.window, stream=stream)
+        pairs = sum(legal_pairs(int(a), int(b), inp.window) for a, b in zip(Qb, Kb))
+        flop = pairs * inp.Hq * (2 * inp.D + 2 * inp.Dv)
+        kv = int(np.sum(Kb)) * inp.Hkv * (inp.D + inp.Dv) * es
+        times = time_steps(run, 20, 3, flush, stream)
+        out.append((name, inp, flop, kv, max_over_ranks(statistics.median(times), world)))
+    return out
+
+
 WIDE = [dict(B=2, Hq=16, Hkv=4, Q=4096, K=4096, D=256, Dv=256),
         dict(B=1, Hq=16, Hkv=4, Q=4096, K=4096, D=512, Dv=512)]
 
@@ -414,6 +454,17 @@ def run_gpu(args, world, rank, local):
                            "gpu_launches": bwd["gpu_launches"]})
         else:
             result["backward"] = bwd
+    small = None
+    if args.only == "all":
+        small = measure_small_configs(args, world, rank, dev, stream, flush, attn, synth)
+        result["configs"] = [
+            {"workload": name, "ms_per_step": round(ms, 5), "us_per_step": round(ms * 1e3, 2),
+             "TFLOP/s": round(world * flop / (ms * 1e-3) / 1e12, 4),
+             "KV GB/s": round(world * kv / (ms * 1e-3) / 1e9, 2), "flop_per_step": flop,
+             "kv_bytes_per_step": kv,
+             "timing": ("median of 20 steps, L2 flushed before each; CUDA events around one "
+                        "call, so the binding's host time (~10 us) is included")}
+            for name, _, flop, kv, ms in small]
     if args.only in ("all", "wide"):
         wide = []
         for W, flop, ms, steps in measure_wide(args, world, rank, dev, stream, flush, attn,
@@ -461,7 +512,7 @@ def run_gpu(args, world, rank, local):
                            "clocks": dec["clocks"], "paged": dec["paged"]})
         else:
             result["decode"] = dec
-    return result, pin
+    return result, (pin, small)
 
 
 KERNEL_SOURCES = {
@@ -523,6 +574,33 @@ def oracle_sample_rate(inp, rows_budget_s=12.0, nthreads=0, seed=0):
     return total_flop / total_s / 1e12, nrows, total_s, threads
 
 
+def oracle_small_configs(small):
+    """The oracle on the two fp32 workloads in full: median wall time of 5
+    runs on one thread and on every host core."""
+    import oracle
+    cores = oracle.max_threads()  # before any call sets a thread count
+    out = []
+    for name, inp, flop, kv, _ in small:
+        q32, k32, v32 = (synth_exact(t) for t in (inp.q, inp.k, inp.v))
+        row = {"workload": name}
+        for label, nt in (("all_cores", cores), ("1_thread", 1)):
+            ts = []
+            for _ in range(5):
+                t0 = time.perf_counter()
+                oracle.attn_padded(q32, k32, v32, B=inp.B, Hq=inp.Hq, Hkv=inp.Hkv, Q=inp.Q,
+                                   K=inp.K, D=inp.D, Dv=inp.Dv, window=inp.window,
+                                   scale=inp.scale, nthreads=nt)
+                ts.append(time.perf_counter() - t0)
+            row[f"us_{label}"] = round(statistics.median(ts) * 1e6, 1)
+        row["cores"] = cores
+        out.append(row)
+    return out
+
+
+def synth_exact(t):
+    return t.detach().to("cpu").float().numpy()
+
+
 def run_reference(args, world, rank):
     from causal_gqa_attention_online_gb300 import synth
     if rank != 0:
@@ -573,13 +651,15 @@ def main():
         if res is not None:
             print(json.dumps(res))
         return
-    res, pin = run_gpu(args, world, rank, local)
+    res, (pin, small) = run_gpu(args, world, rank, local)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline and pin is not None:
             r, nrows, secs, threads = oracle_sample_rate(pin, 12.0)
             res["cpu_baseline"] = {
                 "value": r, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                 "sample": f"{nrows} random (b, q, h) rows of the prefill workload, {secs:.1f} s"}
+            if small:
+                res["cpu_baseline"]["configs"] = oracle_small_configs(small[:2])
         print(json.dumps(res))
     if world > 1:
         import torch.distributed as dist

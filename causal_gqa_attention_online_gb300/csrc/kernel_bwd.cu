@@ -49,13 +49,6 @@ __device__ __forceinline__ void rows_for_keys(int k0, int k1, int Qb, int Kb, in
     if (window > 0) qe = min(Qb, k1 + window - 1 - off);  // lo(qi) < k1
 }
 
-// 4-byte cp.async (zero-fills when src_bytes is 0, reading nothing).
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, int src_bytes) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
-
 // A 1-D grid of (tile, sequence x KV head) blocks, ordered tile rank first:
 // every (sequence, KV head)'s rank-0 tile, then every rank-1 tile, ...  The
 // kernels give rank 0 to their longest tile, so the long blocks start first

@@ -18,19 +18,22 @@
 // the combine kernel (the legal (max, sum, acc) merge of section 5).
 #include <climits>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "launch.h"
+#include "mma_sync.cuh"
 
 namespace attn {
 namespace {
 
 constexpr int kRows = 32;            // flattened rows per block
 constexpr int kTK = 32;              // keys per tile (one per lane)
-constexpr int kWarps = 4;
+constexpr int kWarps = 8;
 constexpr int kRPW = kRows / kWarps;  // rows per warp
 
 template <typename T, int DVL>
-__global__ void __launch_bounds__(128) generic_fwd_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kWarps * 32, 1) generic_fwd_kernel(const AttnParams p) {
     extern __shared__ float smem[];
     const int D = p.D, Dv = p.Dv, G = p.G;
     const int Dp = D | 1;  // odd row pitch: lane-per-key reads hit distinct banks
@@ -51,14 +54,28 @@ __global__ void __launch_bounds__(128) generic_fwd_kernel(const AttnParams p) {
     const T *kg = static_cast<const T *>(p.k);
     const T *vg = static_cast<const T *>(p.v);
 
-    for (int i = tid; i < kRows * D; i += blockDim.x) {
-        const int r = r0 + i / D, d = i % D;
-        float x = 0.f;
-        if (r < nvalid) {
-            const int qi = r / G, h = kvh * G + r % G;
-            x = to_f32(qg[((si.q_off + qi) * p.Hq + h) * (long long)D + d]) * p.scale_log2;
+    // fp32: every element of a tile is copied by cp.async, so a thread has
+    // all of its loads in flight at once (the kernel is latency-bound on
+    // small problems); other storage types convert through registers
+    constexpr bool kAsync = std::is_same<T, float>::value;
+    // a warp per row, lanes along the row
+    for (int rr = warp; rr < kRows; rr += kWarps) {
+        const int r = r0 + rr;
+        const bool ok = r < nvalid;
+        const T *src = ok ? qg + ((si.q_off + r / G) * p.Hq + kvh * G + r % G) * (long long)D : qg;
+        for (int d = lane; d < D; d += 32) {
+            if constexpr (kAsync) {
+                cp_async4(smem_u32(qs + rr * D + d), ok ? src + d : qg, ok ? 4 : 0);
+            } else {
+                qs[rr * D + d] = ok ? to_f32(src[d]) * p.scale_log2 : 0.f;
+            }
         }
-        qs[i] = x;
+    }
+    if constexpr (kAsync) {
+        cp_async_commit();
+        cp_async_wait<0>();
+        for (int rr = warp; rr < kRows; rr += kWarps)  // this thread's own copies
+            for (int d = lane; d < D; d += 32) qs[rr * D + d] *= p.scale_log2;
     }
 
     // Key range of the block: legal ranges are monotone in the query index.
@@ -94,48 +111,83 @@ __global__ void __launch_bounds__(128) generic_fwd_kernel(const AttnParams p) {
 
     for (int t0 = key_lo; t0 < key_hi; t0 += kTK) {
         __syncthreads();  // previous tile consumed; q staged
-        for (int i = tid; i < kTK * D; i += blockDim.x) {
-            const int j = i / D, d = i % D, key = t0 + j;
-            ks[j * Dp + d] = key < key_hi
-                ? to_f32(kg[(kv_row(p, si, b, key) * p.Hkv + kvh) * (long long)D + d]) : 0.f;
-        }
-        for (int i = tid; i < kTK * Dv; i += blockDim.x) {
-            const int j = i / Dv, c = i % Dv, key = t0 + j;
-            vs[i] = key < key_hi
-                ? to_f32(vg[(kv_row(p, si, b, key) * p.Hkv + kvh) * (long long)Dv + c]) : 0.f;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int i = 0; i < kRPW; ++i) {
-            // warp-uniform: the row's legal range misses this tile (or is empty:
-            // with the top-left mask and a window, lo can pass the last key)
-            if (rhi[i] <= rlo[i] || rhi[i] <= t0 || rlo[i] >= t0 + kTK) continue;
-            const int rr = warp + kWarps * i;
-            const int key = t0 + lane;
-            float s = -INFINITY;
-            if (key >= rlo[i] && key < rhi[i]) {
-                const float *qr = qs + rr * D;
-                const float *kr = ks + lane * Dp;
-                float a = 0.f;
-                for (int d = 0; d < D; ++d) a = fmaf(qr[d], kr[d], a);
-                s = a;
-            }
-            const float mnew = fmaxf(m[i], warp_max(s));  // finite: a legal key is in the tile
-            const float pj = exp2f(s - mnew);
-            const float alpha = exp2f(m[i] - mnew);
-            l[i] = l[i] * alpha + warp_sum(pj);
-#pragma unroll
-            for (int c = 0; c < DVL; ++c) acc[i][c] *= alpha;
-            for (int j = 0; j < kTK; ++j) {
-                const float pb = __shfl_sync(0xffffffffu, pj, j);
-                const float *vr = vs + j * Dv;
-#pragma unroll
-                for (int c = 0; c < DVL; ++c) {
-                    const int col = lane + 32 * c;
-                    if (col < Dv) acc[i][c] = fmaf(pb, vr[col], acc[i][c]);
+        // a warp per key row (one row lookup), lanes along the row
+        for (int j = warp; j < kTK; j += kWarps) {
+            const int key = t0 + j;
+            const bool ok = key < key_hi;
+            const long long row = ok ? kv_row(p, si, b, key) * p.Hkv + kvh : 0;
+            const T *ksrc = kg + row * D, *vsrc = vg + row * Dv;
+            for (int d = lane; d < D; d += 32) {
+                if constexpr (kAsync) {
+                    cp_async4(smem_u32(ks + j * Dp + d), ok ? ksrc + d : kg, ok ? 4 : 0);
+                } else {
+                    ks[j * Dp + d] = ok ? to_f32(ksrc[d]) : 0.f;
                 }
             }
+            for (int c = lane; c < Dv; c += 32) {
+                if constexpr (kAsync) {
+                    cp_async4(smem_u32(vs + j * Dv + c), ok ? vsrc + c : vg, ok ? 4 : 0);
+                } else {
+                    vs[j * Dv + c] = ok ? to_f32(vsrc[c]) : 0.f;
+                }
+            }
+        }
+        if constexpr (kAsync) {
+            cp_async_commit();
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        // The warp's kRPW rows go together (the kernel is latency-bound on
+        // small problems): each K element a lane reads feeds kRPW independent
+        // dot products, and each V element kRPW accumulators.  Rows whose
+        // legal keys miss the tile see only masked scores (p = 0, alpha = 1).
+        bool any = false;
+#pragma unroll
+        for (int i = 0; i < kRPW; ++i)
+            any |= rhi[i] > rlo[i] && rhi[i] > t0 && rlo[i] < t0 + kTK;
+        if (!any) continue;  // warp-uniform
+        const int key = t0 + lane;
+        float s[kRPW];
+#pragma unroll
+        for (int i = 0; i < kRPW; ++i) s[i] = 0.f;
+        {
+            const float *kr = ks + lane * Dp;
+            const float *qw = qs + warp * D;  // row warp + kWarps * i starts at i * kWarps * D
+#pragma unroll 4
+            for (int d = 0; d < D; ++d) {
+                const float kd = kr[d];
+#pragma unroll
+                for (int i = 0; i < kRPW; ++i) s[i] = fmaf(qw[i * kWarps * D + d], kd, s[i]);
+            }
+        }
+        float pj[kRPW];
+#pragma unroll
+        for (int i = 0; i < kRPW; ++i) {
+            const float si = key >= rlo[i] && key < rhi[i] ? s[i] : -INFINITY;
+            const float mnew = fmaxf(m[i], warp_max(si));
+            // a row with no legal key so far keeps a finite reference: p = 0
+            const float ref = mnew == -INFINITY ? 0.f : mnew;
+            pj[i] = exp2f(si - ref);
+            const float alpha = exp2f(m[i] - ref);
+            l[i] = l[i] * alpha + warp_sum(pj[i]);
+#pragma unroll
+            for (int c = 0; c < DVL; ++c) acc[i][c] *= alpha;
             m[i] = mnew;
+        }
+        for (int j = 0; j < kTK; ++j) {
+            const float *vr = vs + j * Dv;
+            float vv[DVL];
+#pragma unroll
+            for (int c = 0; c < DVL; ++c) {
+                const int col = lane + 32 * c;
+                vv[c] = col < Dv ? vr[col] : 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < kRPW; ++i) {
+                const float pb = __shfl_sync(0xffffffffu, pj[i], j);
+#pragma unroll
+                for (int c = 0; c < DVL; ++c) acc[i][c] = fmaf(pb, vv[c], acc[i][c]);
+            }
         }
     }
 
@@ -316,7 +368,7 @@ int launch_generic_t(const AttnParams &p, cudaStream_t stream) {
     const long long rows = (long long)p.Q * p.G;
     dim3 grid((unsigned)((rows + kRows - 1) / kRows), (unsigned)(p.B * p.Hkv),
               (unsigned)p.nsplit);
-    kern<<<grid, 128, smem, stream>>>(p);
+    kern<<<grid, kWarps * 32, smem, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("generic kernel launch: %s", cudaGetErrorString(e));

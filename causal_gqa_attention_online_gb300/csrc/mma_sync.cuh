@@ -1,5 +1,5 @@
-// mma_sync.cuh -- warp-level tensor-core helpers shared by the decode and
-// backward kernels: cp.async staging, ldmatrix / movmatrix, the m16n8k16
+// mma_sync.cuh -- warp-level tensor-core helpers shared by the decode,
+// forward-mma, backward and CUDA-core kernels: cp.async staging, ldmatrix / movmatrix, the m16n8k16
 // MMA with fp32 accumulation for bf16 and fp16, and the XOR-swizzled tile
 // layout that keeps ldmatrix free of bank conflicts.
 #pragma once
@@ -14,6 +14,12 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+// 4-byte cp.async (zero-fills when src_bytes is 0, reading nothing).
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, int src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src),
                  "r"(src_bytes)
                  : "memory");
 }
