@@ -455,7 +455,7 @@ def run_gpu(args, world, rank, local):
         else:
             result["backward"] = bwd
     small = None
-    if args.only == "all":
+    if args.only in ("all", "configs"):
         small = measure_small_configs(args, world, rank, dev, stream, flush, attn, synth)
         result["configs"] = [
             {"workload": name, "ms_per_step": round(ms, 5), "us_per_step": round(ms * 1e3, 2),
@@ -465,6 +465,10 @@ def run_gpu(args, world, rank, local):
              "timing": ("median of 20 steps, L2 flushed before each; CUDA events around one "
                         "call, so the binding's host time (~10 us) is included")}
             for name, _, flop, kv, ms in small]
+        if args.only == "configs":
+            c0 = result["configs"][0]
+            result.update({"value": c0["TFLOP/s"], "unit": "TFLOP/s",
+                           "ms_per_step": c0["ms_per_step"], "config": {"workload": c0["workload"]}})
     if args.only in ("all", "wide"):
         wide = []
         for W, flop, ms, steps in measure_wide(args, world, rank, dev, stream, flush, attn,
@@ -640,7 +644,7 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=60.0,
                     help="--impl reference: total seconds of oracle work over all steps")
     ap.add_argument("--only", default="all",
-                    choices=["all", "prefill", "decode", "backward", "wide"],
+                    choices=["all", "prefill", "decode", "backward", "wide", "configs"],
                     help="profiling aid: run one workload (the JSON line then lacks the other)")
     args = ap.parse_args()
     if args.warmup < 3:
