@@ -1,9 +1,12 @@
 // kernel_bwd.cu -- backward of the attention: dQ, dK, dV from dO, the
 // forward's O and LSE, recomputing the probabilities.
 //
-// The pages give the forward only ("Online softmax" / "FlashAttention"
-// passages: O = softmax(scale Q K^T + mask) V with the row LSE kept).  The
-// backward is the derivative of that definition, per legal (row, key):
+// "Accelerating PyTorch on AMD GPUs with FlyDSL", section on FMHA through
+// AOTriton, describes the backward's structure (separate dQ and dK/dV
+// kernels, dK/dV as the forward loop transposed with K and V resident and Q
+// and dO streamed, dQ's products matching the forward's) but prints no
+// arithmetic.  The arithmetic is the derivative of the forward definition
+// (O = softmax(scale Q K^T + mask) V with the row LSE kept), per legal (row, key):
 //
 //     P   = exp(scale q.k - LSE)          (recomputed, no stored P)
 //     Dq  = sum_j dO[j] O[j]              (one number per row: bwd_delta_kernel)

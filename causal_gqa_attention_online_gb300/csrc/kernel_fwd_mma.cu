@@ -239,7 +239,10 @@ __global__ void __launch_bounds__(128) fwd_mma_kernel(const AttnParams p) {
 
 // Wide heads (D or Dv above 256, up to 512): one 16 x 512 fp32 accumulator
 // per warp would not fit in registers, so warps work in pairs on the same 16
-// rows.  Warp w (< 4) and warp w + 4 each contract half of the head width
+// rows, each accumulating half of the output columns -- the across-wave split
+// of the wide-head body in "Accelerating PyTorch on AMD GPUs with FlyDSL"
+// (section on FMHA through AOTriton, figure 13), where both waves compute
+// the same scores.  Here the score contraction is split too.  Warp w (< 4) and warp w + 4 each contract half of the head width
 // for S (columns [0, DW/2) and [DW/2, DW)), swap their partial scores
 // through shared memory behind a 64-thread named barrier and add them (in
 // the same order, so both hold the same bits), run the same online softmax,

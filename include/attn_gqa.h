@@ -258,10 +258,12 @@ ATTN_API int attn_fwd_staged(const void *hq, const void *hk, const void *hv, voi
 
 /*
  * attn_bwd -- gradients of attn_fwd_ex (padded layout) for a loss whose
- * gradient with respect to o is dout.  The pages define the forward only
- * ("Online softmax" and "FlashAttention" passages: O = softmax(scale Q K^T +
- * mask) V per row, with the row's log-sum-exp kept); this is the derivative
- * of that definition.  With P = exp(scale q.k - LSE) over the row's legal
+ * gradient with respect to o is dout.  "Accelerating PyTorch on AMD GPUs
+ * with FlyDSL", section on FMHA through AOTriton, describes such a backward
+ * as separate dQ and dK/dV kernels reusing the forward's building blocks,
+ * without its arithmetic; the arithmetic here is the derivative of the
+ * forward definition (O = softmax(scale Q K^T + mask) V per row, with the
+ * row's log-sum-exp kept).  With P = exp(scale q.k - LSE) over the row's legal
  * keys and Dq = sum(dO * O) over the row:
  *     dS = P (dO . v - Dq)
  *     dq = scale sum_k dS k

@@ -273,7 +273,8 @@ int oracle_attn_padded_rows(const float *q, const float *k, const float *v,
 }
 
 /* Gradients of the same attention (padded layout), for a loss whose gradient
- * with respect to O is dO.  The pages give the forward only; the backward is
+ * with respect to O is dO.  The pages print no backward arithmetic (the FlyDSL
+ * page, section on FMHA through AOTriton, only names its kernels); it is
  * the derivative of the definition above, written out per row (fp64):
  *   P[q,k]  = exp(s_k - LSE[q]) for k in L(q), 0 otherwise (s, L, LSE as above)
  *   Dq      = sum_j dO[q,j] * O[q,j]
