@@ -301,9 +301,10 @@ int bwd_common(const void *q, const void *k, const void *v, const void *o, const
         set_error("the backward takes head widths up to 256 (D=%d Dv=%d)", D, Dv);
         return ATTN_ERR_UNSUPPORTED;
     }
-    if (algo != ATTN_ALGO_AUTO && algo != ATTN_ALGO_GENERIC && algo != ATTN_ALGO_MMA) {
-        set_error("backward algo must be ATTN_ALGO_AUTO, ATTN_ALGO_GENERIC or ATTN_ALGO_MMA "
-                  "(got %d)", algo);
+    if (algo != ATTN_ALGO_AUTO && algo != ATTN_ALGO_GENERIC && algo != ATTN_ALGO_MMA &&
+        algo != ATTN_ALGO_TCGEN05) {
+        set_error("backward algo must be ATTN_ALGO_AUTO, ATTN_ALGO_GENERIC, ATTN_ALGO_MMA or "
+                  "ATTN_ALGO_TCGEN05 (got %d)", algo);
         return ATTN_ERR_INVALID;
     }
     if (mask < ATTN_MASK_CAUSAL || mask > ATTN_MASK_NONE) {
@@ -358,11 +359,19 @@ int bwd_common(const void *q, const void *k, const void *v, const void *o, const
     bp.dk = dk;
     bp.dv = dv;
     const bool mma_ok = bwd_mma_supported(p, dtype);
+    const bool tc_ok = mma_ok && bwd_dq_tc_supported(p, dtype);
     if (algo == ATTN_ALGO_MMA && !mma_ok) {
         set_error("mma backward kernels take bf16/fp16 with D, Dv multiples of 8 up to 128");
         return ATTN_ERR_UNSUPPORTED;
     }
-    const bool mma = algo == ATTN_ALGO_MMA || (algo == ATTN_ALGO_AUTO && mma_ok);
+    if (algo == ATTN_ALGO_TCGEN05 && !tc_ok) {
+        set_error("the tcgen05 backward takes bf16/fp16 with D, Dv multiples of 16 in [64, 128]");
+        return ATTN_ERR_UNSUPPORTED;
+    }
+    int mode = 0;  // CUDA cores
+    if (algo == ATTN_ALGO_MMA) mode = 1;
+    else if (algo == ATTN_ALGO_TCGEN05) mode = 2;
+    else if (algo == ATTN_ALGO_AUTO) mode = tc_ok ? 2 : (mma_ok ? 1 : 0);
     int dev = 0;
     rc = current_device(&dev);
     if (rc) return rc;
@@ -390,7 +399,7 @@ int bwd_common(const void *q, const void *k, const void *v, const void *o, const
         return ATTN_ERR_CUDA;
     }
     bp.delta = static_cast<float *>(ws);
-    rc = launch_bwd(bp, dtype, mma, stream);
+    rc = launch_bwd(bp, dtype, mode, stream);
     e = cudaFreeAsync(ws, stream);
     if (e != cudaSuccess && rc == 0) {
         set_error("workspace cudaFreeAsync: %s", cudaGetErrorString(e));

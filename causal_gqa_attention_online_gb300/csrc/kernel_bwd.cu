@@ -860,7 +860,7 @@ int launch_generic_bwd(const BwdParams &bp, cudaStream_t stream) {
 }
 
 template <typename T, int DW, int DVW>
-int launch_mma_bwd_t(const BwdParams &bp, cudaStream_t stream) {
+int launch_mma_bwd_t(const BwdParams &bp, bool tc_dq, cudaStream_t stream) {
     const AttnParams &p = bp.f;
     const unsigned y = (unsigned)p.B * p.Hkv;
     const long long ktiles = ((long long)p.K + kMKeys - 1) / kMKeys;
@@ -875,6 +875,7 @@ int launch_mma_bwd_t(const BwdParams &bp, cudaStream_t stream) {
                       "bwd_dkdv_mma", bp);
         if (rc) return rc;
     }
+    if (tc_dq) return launch_bwd_dq_tc(bp, std::is_same<T, __half>::value ? 1 : 2, stream);
     const size_t s = (size_t)kQRows * 2 * (DW + DVW) + (size_t)2 * kQKeys * 2 * (DW + DVW);
     const long long qtiles = ((long long)p.Q * p.G + kQRows - 1) / kQRows;
     return launch_k(bwd_dq_mma<T, DW, DVW>, dim3((unsigned)(qtiles * y)), 128, s, stream,
@@ -882,22 +883,22 @@ int launch_mma_bwd_t(const BwdParams &bp, cudaStream_t stream) {
 }
 
 template <typename T>
-int launch_mma_bwd(const BwdParams &bp, cudaStream_t stream) {
+int launch_mma_bwd(const BwdParams &bp, bool tc_dq, cudaStream_t stream) {
     const bool wd = bp.f.D > 64, wv = bp.f.Dv > 64;
-    if (wd && wv) return launch_mma_bwd_t<T, 128, 128>(bp, stream);
-    if (wd) return launch_mma_bwd_t<T, 128, 64>(bp, stream);
-    if (wv) return launch_mma_bwd_t<T, 64, 128>(bp, stream);
-    return launch_mma_bwd_t<T, 64, 64>(bp, stream);
+    if (wd && wv) return launch_mma_bwd_t<T, 128, 128>(bp, tc_dq, stream);
+    if (wd) return launch_mma_bwd_t<T, 128, 64>(bp, tc_dq, stream);
+    if (wv) return launch_mma_bwd_t<T, 64, 128>(bp, tc_dq, stream);
+    return launch_mma_bwd_t<T, 64, 64>(bp, tc_dq, stream);
 }
 
 template <typename T>
-int launch_bwd_t(const BwdParams &bp, bool mma, cudaStream_t stream) {
+int launch_bwd_t(const BwdParams &bp, int mode, cudaStream_t stream) {
     const long long rows = bp.f.Tq * bp.f.Hq;
     int rc = launch_k(bwd_delta_kernel<T>, dim3((unsigned)((rows + 7) / 8)), 256, 0, stream,
                       "bwd_delta", bp, rows);
     if (rc) return rc;
     if constexpr (!std::is_same<T, float>::value) {
-        if (mma) return launch_mma_bwd<T>(bp, stream);
+        if (mode != 0) return launch_mma_bwd<T>(bp, mode == 2, stream);
     }
     return launch_generic_bwd<T>(bp, stream);
 }
@@ -908,12 +909,12 @@ bool bwd_mma_supported(const AttnParams &p, int dtype) {
     return dtype != 0 && p.D % 8 == 0 && p.Dv % 8 == 0 && p.D <= 128 && p.Dv <= 128;
 }
 
-int launch_bwd(const BwdParams &bp, int dtype, bool mma, cudaStream_t stream) {
+int launch_bwd(const BwdParams &bp, int dtype, int mode, cudaStream_t stream) {
     if (bp.f.Tq * bp.f.Hq == 0) return 0;
     switch (dtype) {
-        case 0: return launch_bwd_t<float>(bp, false, stream);
-        case 1: return launch_bwd_t<__half>(bp, mma, stream);
-        default: return launch_bwd_t<__nv_bfloat16>(bp, mma, stream);
+        case 0: return launch_bwd_t<float>(bp, 0, stream);
+        case 1: return launch_bwd_t<__half>(bp, mode, stream);
+        default: return launch_bwd_t<__nv_bfloat16>(bp, mode, stream);
     }
 }
 

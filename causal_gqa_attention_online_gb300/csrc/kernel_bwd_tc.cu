@@ -1,0 +1,462 @@
+// kernel_bwd_tc.cu -- the dQ half of the attention backward on the 5th-
+// generation tensor cores (tcgen05, TMEM accumulators, TMA-fed shared memory).
+//
+// dQ[q] = scale * sum_k dS[q,k] K[k],  dS = P (dP - Dq),  P = exp2(S c - LSE_2),
+// S = Q K^T, dP = dO V^T over each row's legal keys (the derivative of the
+// forward definition; Dq = rowsum(dO * O) comes from bwd_delta_kernel).  The
+// structure is the dQ kernel of "Accelerating PyTorch on AMD GPUs with
+// FlyDSL", section on FMHA through AOTriton: its three products match the
+// forward's (S like the forward's S, dP likewise, dQ += dS K like O += P V),
+// and the K tile is staged once and read in both orientations -- K-major as
+// the B operand of S, MN-major as the B operand of dQ.
+//
+// A CTA owns 128 query rows of one head (TMEM lane = row) and walks their
+// legal keys 64 at a time:
+//   warp 4 (one thread): TMA loads of the Q and dO tiles and a ring of K/V
+//     tiles;
+//   warp 5 (one thread): S_b = Q K^T and dP_b = dO V^T into TMEM buffer b =
+//     tile & 1, then, once the elementwise warps have turned the previous
+//     tile into dS, dQ += dS K with dS read from TMEM (it overwrites S_b);
+//   warps 0-3: per tile, P and dS from S_b and dP_b in registers, dS stored
+//     to TMEM as 16-bit pairs; at the end dQ out of TMEM, scaled, to memory.
+// The double buffer lets the tensor core compute tile j+1's S and dP while
+// the elementwise warps work on tile j.  TMEM: S0 S1 | dP0 dP1 | dQ.
+// Every mbarrier wait is bounded; a wait that runs out records a status and
+// raises an abort flag, and the CTA drains its copies and frees TMEM.
+#include <cuda.h>
+
+#include <climits>
+
+#include "common.cuh"
+#include "launch.h"
+#include "sm100_ptx.cuh"
+
+namespace attn {
+namespace {
+
+using namespace sm100;
+
+constexpr int kRowsT = 128;  // query rows per CTA (MMA M)
+constexpr int kKeysT = 64;   // keys per tile (N of S and dP, contraction of dQ)
+constexpr int kStagesT = 4;  // K/V ring depth
+constexpr int kThreadsT = 192;
+constexpr int kLoadWarpT = 4;
+constexpr int kMmaWarpT = 5;
+constexpr uint64_t kWaitNsT = 2000000000ull;  // 2 s
+constexpr int kStatusTimeoutBwdTc = 0x301;
+
+struct DqArgs {
+    BwdParams bp;
+    int nqt;            // 128-row query tiles per (sequence, head)
+    float c2;           // scale * log2(e)
+    uint32_t idesc_s;   // M128 N64, both operands K-major
+    uint32_t idesc_dq;  // M128 N=D, B MN-major
+};
+
+template <int D, int DV> struct DqLayout {
+    static constexpr int QCH = kRowsT * 128;  // one 64-column chunk of a 128-row tile
+    static constexpr int KCH = kKeysT * 128;  // one 64-column chunk of a 64-key tile
+    static constexpr int QTILE = (D / 64) * QCH;
+    static constexpr int OTILE = (DV / 64) * QCH;
+    static constexpr int KTILE = (D / 64) * KCH;
+    static constexpr int VTILE = (DV / 64) * KCH;
+    static constexpr int STAGE = KTILE + VTILE;
+    static constexpr int Q_OFF = 0;
+    static constexpr int DO_OFF = QTILE;
+    static constexpr int KV_OFF = QTILE + OTILE;
+    static constexpr int BAR_OFF = KV_OFF + kStagesT * STAGE;
+    static constexpr int SMEM = 1024 + BAR_OFF + 256;
+    static constexpr int S_COL = 0, DP_COL = 128, DQ_COL = 256;  // TMEM columns
+    static_assert(DQ_COL + D <= 512, "TMEM budget");
+    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+};
+
+// barrier slots (8 bytes each)
+enum : int {
+    T_QD_FULL = 0,
+    T_S_FULL = 1,     // [2]
+    T_DS_READY = 3,   // [2]
+    T_DQ_FULL = 5,
+    T_TEARDOWN = 6,
+    T_KV_FULL = 7,    // [kStagesT] full, then [kStagesT] empty
+    T_NBARS = 7 + 2 * kStagesT,
+};
+
+__device__ __forceinline__ float ex2f(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(r) : "f"(x));
+    return r;
+}
+
+template <typename T> __device__ __forceinline__ uint32_t pack16(float lo, float hi);
+template <> __device__ __forceinline__ uint32_t pack16<__nv_bfloat16>(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+template <> __device__ __forceinline__ uint32_t pack16<__half>(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ bool warp_wait_t(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    const bool ok = mbar_wait(bar, parity, abort_flag, kWaitNsT);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void raise_abort_t(volatile int *abort_flag, int *status) {
+    *abort_flag = 1;
+    report_status(status, kStatusTimeoutBwdTc);
+}
+
+template <typename T, int D, int DV>
+__global__ void __launch_bounds__(kThreadsT, 1)
+    bwd_dq_tc_kernel(const __grid_constant__ DqArgs a, const __grid_constant__ CUtensorMap tmQ,
+                     const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV) {
+    using L = DqLayout<D, DV>;
+    extern __shared__ uint8_t smem_t[];
+    const BwdParams &bp = a.bp;
+    const AttnParams &p = bp.f;
+
+    // work: (query tile rank, sequence, head); the last query tiles see the
+    // most keys and start first
+    const int nbh = p.B * p.Hq;
+    const int rank = blockIdx.x / nbh;
+    const int b = (blockIdx.x % nbh) / p.Hq, h = (blockIdx.x % nbh) % p.Hq;
+    const int kvh = h / p.G;
+    const SeqInfo si = seq_info(p, b);
+    const bool padded = p.cu_q == nullptr;
+    const int q0 = (a.nqt - 1 - rank) * kRowsT;
+    const int qcap = padded ? p.Q : si.Qb;  // rows this CTA may write
+    if (q0 >= qcap) return;                 // uniform: before any barrier
+
+    const uint32_t raw = smem_addr(smem_t);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_t + (base - raw);
+    const uint32_t bars = base + L::BAR_OFF;
+    auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + L::BAR_OFF + 8 * T_NBARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    auto kv_full = [&](int s) { return bar(T_KV_FULL + s); };
+    auto kv_empty = [&](int s) { return bar(T_KV_FULL + kStagesT + s); };
+    auto stage = [&](int s) { return base + L::KV_OFF + (uint32_t)s * L::STAGE; };
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // legal keys of the CTA's rows: the union of the rows' ranges, which grow
+    // with the row
+    const int qlast = min(q0 + kRowsT, si.Qb) - 1;
+    int klo = 0, khi = 0;
+    if (qlast >= q0) {
+        int a0, a1;
+        legal_range(q0, si.Qb, si.Kb, p.window, p.mask, klo, a0);
+        legal_range(qlast, si.Qb, si.Kb, p.window, p.mask, a1, khi);
+    }
+    const int tfirst = klo / kKeysT * kKeysT;
+    const int ntiles = khi > klo ? (khi - tfirst + kKeysT - 1) / kKeysT : 0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(T_QD_FULL), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(T_S_FULL + i), 1);
+            mbar_init(bar(T_DS_READY + i), 128);
+        }
+        mbar_init(bar(T_DQ_FULL), 1);
+        mbar_init(bar(T_TEARDOWN), 1);
+        for (int s = 0; s < kStagesT; ++s) {
+            mbar_init(kv_full(s), 1);
+            mbar_init(kv_empty(s), 1);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarpT) {
+        tmem_alloc(smem_addr(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kLoadWarpT) {
+        // ---------------------------------------------------------- TMA producer
+        if (lane == 0 && ntiles > 0) {
+            const int qrow = (padded ? 0 : (int)si.q_off) + q0;
+            const int krow = padded ? 0 : (int)si.k_off;
+            const int bc = padded ? b : 0;
+            bool ok = true;
+            uint32_t armed = 0, armed_ph = 0;
+            mbar_arrive_expect_tx(bar(T_QD_FULL), L::QTILE + L::OTILE);
+            for (int c = 0; c < D / 64; ++c)
+                tma_load_4d(base + L::Q_OFF + c * L::QCH, &tmQ, bar(T_QD_FULL), c * 64, h, qrow, bc);
+            for (int c = 0; c < DV / 64; ++c)
+                tma_load_4d(base + L::DO_OFF + c * L::QCH, &tmO, bar(T_QD_FULL), c * 64, h, qrow, bc);
+            for (int j = 0; j < ntiles; ++j) {
+                const int s = j % kStagesT;
+                const uint32_t ph = (uint32_t)(j / kStagesT) & 1u;
+                if (!mbar_wait(kv_empty(s), ph ^ 1u, abort_flag, kWaitNsT)) {
+                    raise_abort_t(abort_flag, p.status);
+                    ok = false;
+                    break;
+                }
+                const int kr = krow + tfirst + j * kKeysT;
+                mbar_arrive_expect_tx(kv_full(s), L::STAGE);
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_4d(stage(s) + c * L::KCH, &tmK, kv_full(s), c * 64, kvh, kr, bc);
+                for (int c = 0; c < DV / 64; ++c)
+                    tma_load_4d(stage(s) + L::KTILE + c * L::KCH, &tmV, kv_full(s), c * 64, kvh,
+                                kr, bc);
+                armed |= 1u << s;
+                armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+            }
+            (void)ok;
+            // drain: every copy issued has landed before the CTA exits
+            mbar_wait(bar(T_QD_FULL), 0, abort_flag, kWaitNsT);
+            for (int s = 0; s < kStagesT; ++s)
+                if (armed & (1u << s))
+                    mbar_wait(kv_full(s), (armed_ph >> s) & 1u, abort_flag, kWaitNsT);
+        }
+    } else if (warp == kMmaWarpT) {
+        // ------------------------------------------------------------ MMA issuer
+        bool ok = ntiles == 0 || warp_wait_t(bar(T_QD_FULL), 0, abort_flag);
+        const uint64_t qd = sw128_desc(base + L::Q_OFF, 16, 1024);
+        const uint64_t od = sw128_desc(base + L::DO_OFF, 16, 1024);
+        const uint32_t dq_tm = tmem + L::DQ_COL;
+        for (int j = 0; j <= ntiles && ok; ++j) {
+            if (j < ntiles) {
+                const int s = j % kStagesT, bf = j & 1;
+                if (!warp_wait_t(kv_full(s), (uint32_t)(j / kStagesT) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    // S_bf was last read by the dQ MMA of tile j - 2, issued
+                    // earlier by this thread (tcgen05.mma runs in issue order)
+                    const uint64_t kd = sw128_desc(stage(s), 16, 1024);
+                    const uint64_t vd = sw128_desc(stage(s) + L::KTILE, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + L::S_COL + bf * kKeysT,
+                               qd + (((kk / 4) * L::QCH + (kk % 4) * 32) >> 4),
+                               kd + (((kk / 4) * L::KCH + (kk % 4) * 32) >> 4), a.idesc_s, kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < DV / 16; ++kk)
+                        mma_ss(tmem + L::DP_COL + bf * kKeysT,
+                               od + (((kk / 4) * L::QCH + (kk % 4) * 32) >> 4),
+                               vd + (((kk / 4) * L::KCH + (kk % 4) * 32) >> 4), a.idesc_s, kk > 0);
+                    mma_commit(bar(T_S_FULL + bf));
+                }
+                __syncwarp();
+            }
+            if (j >= 1) {
+                // dQ += dS K for tile jj = j - 1, once its dS is in TMEM
+                const int jj = j - 1, bf = jj & 1, s = jj % kStagesT;
+                if (!warp_wait_t(bar(T_DS_READY + bf), (uint32_t)(jj >> 1) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // Keys past the last one in use (last tile only) are left out 16
+                // at a time; the K rows of the last 16-key step past it may hold
+                // anything (NaN included), so they are zeroed: 0 * K must stay 0.
+                // S of this tile has completed (the elementwise warps read it).
+                const int nvalid = min(kKeysT, khi - (tfirst + jj * kKeysT));
+                const int ksteps = (nvalid + 15) / 16;
+                const int nzero = ksteps * 16 - nvalid;
+                if (nzero > 0) {
+                    uint8_t *kt = gbase + (stage(s) - base) + nvalid * 128;
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c)
+                        for (int i = lane; i < nzero * 8; i += 32)
+                            *reinterpret_cast<uint4 *>(kt + c * L::KCH + i * 16) =
+                                make_uint4(0, 0, 0, 0);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                if (lane == 0) {
+                    // K as the MN-major B operand: 64-column chunks L::KCH apart
+                    const uint64_t kmn = sw128_desc(stage(s), L::KCH, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < kKeysT / 16; ++kk)
+                        if (kk < ksteps)
+                            mma_ts(dq_tm, tmem + L::S_COL + bf * kKeysT + kk * 8,
+                                   kmn + ((kk * 2048) >> 4), a.idesc_dq, (jj > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(kv_empty(s));
+                    if (jj == ntiles - 1) mma_commit(bar(T_DQ_FULL));
+                }
+                __syncwarp();
+            }
+        }
+        if (!ok && lane == 0) raise_abort_t(abort_flag, p.status);
+        // every MMA issued completes before TMEM is released
+        if (lane == 0) {
+            mma_commit(bar(T_TEARDOWN));
+            mbar_wait(bar(T_TEARDOWN), 0, abort_flag, kWaitNsT);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------- elementwise warps, epilogue
+        const int r = warp * 32 + lane;  // row of the tile = TMEM lane
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const int qpos = q0 + r;
+        const bool valid = qpos < si.Qb;
+        int lo = 0, hi = 0;
+        if (valid) legal_range(qpos, si.Qb, si.Kb, p.window, p.mask, lo, hi);
+        const long long row = (si.q_off + qpos) * p.Hq + h;
+        float lse2 = 0.f, dl = 0.f;
+        if (hi > lo) {
+            lse2 = p.lse[row] * kLog2e;
+            dl = bp.delta[row];
+        }
+        bool ok = true;
+        for (int j = 0; j < ntiles && ok; ++j) {
+            const int bf = j & 1;
+            if (!warp_wait_t(bar(T_S_FULL + bf), (uint32_t)(j >> 1) & 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t tS = tmem + lane_off + L::S_COL + bf * kKeysT;
+            const uint32_t tP = tmem + lane_off + L::DP_COL + bf * kKeysT;
+            uint32_t sv[2][32], pv[2][32];
+            tmem_ld32(tS, sv[0]);
+            tmem_ld32(tS + 32, sv[1]);
+            tmem_ld32(tP, pv[0]);
+            tmem_ld32(tP + 32, pv[1]);
+            tmem_ld_wait();
+            const int k0 = tfirst + j * kKeysT;
+            const bool inner = __all_sync(0xffffffffu, lo <= k0 && hi >= k0 + kKeysT);
+            uint32_t pk[32];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    float ds[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int key = k0 + hf * 32 + i + e;
+                        const bool legal = inner || (key >= lo && key < hi);
+                        const float pr = ex2f(__uint_as_float(sv[hf][i + e]) * a.c2 - lse2);
+                        ds[e] = legal ? pr * (__uint_as_float(pv[hf][i + e]) - dl) : 0.f;
+                    }
+                    pk[hf * 16 + i / 2] = pack16<T>(ds[0], ds[1]);
+                }
+            tmem_st32(tS, pk);  // dS over the first half of S_bf
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar(T_DS_READY + bf));
+        }
+        if (!ok && lane == 0) raise_abort_t(abort_flag, p.status);
+        // epilogue: dQ * scale to memory (zeros where no key contributed)
+        const bool writes = qpos < qcap;
+        if (ok && ntiles > 0) {
+            ok = warp_wait_t(bar(T_DQ_FULL), 0, abort_flag);
+            if (!ok && lane == 0) raise_abort_t(abort_flag, p.status);
+            tc_fence_after();
+        }
+        T *dqg = static_cast<T *>(bp.dq);
+        const int Dr = p.D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            if (ok && ntiles > 0) {
+                tmem_ld32(tmem + lane_off + L::DQ_COL + c * 32, v);
+                tmem_ld_wait();
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0u;
+            }
+            if (writes) {
+                T *dst = dqg + row * Dr + c * 32;
+#pragma unroll
+                for (int i = 0; i < 32; i += 2)
+                    if (c * 32 + i < Dr)
+                        *reinterpret_cast<uint32_t *>(dst + i) =
+                            pack16<T>(valid ? __uint_as_float(v[i]) * p.scale : 0.f,
+                                      valid ? __uint_as_float(v[i + 1]) * p.scale : 0.f);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarpT) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <typename T, int D, int DV>
+int launch_t(const BwdParams &bp, bool bf16, cudaStream_t stream) {
+    using L = DqLayout<D, DV>;
+    const AttnParams &p = bp.f;
+    DqArgs a;
+    a.bp = bp;
+    a.nqt = (p.Q + kRowsT - 1) / kRowsT;
+    a.c2 = p.scale * kLog2e;
+    a.idesc_s = idesc_f16(bf16, kRowsT, kKeysT, false, false);
+    a.idesc_dq = idesc_f16(bf16, kRowsT, D, true, false);
+    const long long grid = (long long)a.nqt * p.B * p.Hq;
+    if (grid == 0) return 0;
+    if (grid >= (1LL << 31)) {
+        set_error("tcgen05 dQ: %lld blocks exceed one launch", grid);
+        return 2;
+    }
+    const bool padded = p.cu_q == nullptr;
+    const uint64_t qrows = padded ? (uint64_t)p.Q : (uint64_t)p.Tq;
+    const uint64_t krows = padded ? (uint64_t)p.K : (uint64_t)p.Tk;
+    const uint64_t nb = padded ? (uint64_t)p.B : 1;
+    CUtensorMap tq, to, tk, tv;
+    int rc = make_tma_map_4d(&tq, p.q, bf16, (uint64_t)p.D, p.Hq, qrows, nb, 1, kRowsT);
+    if (!rc) rc = make_tma_map_4d(&to, bp.dout, bf16, (uint64_t)p.Dv, p.Hq, qrows, nb, 1, kRowsT);
+    if (!rc && krows > 0) {
+        rc = make_tma_map_4d(&tk, p.k, bf16, (uint64_t)p.D, p.Hkv, krows, nb, 1, kKeysT);
+        if (!rc) rc = make_tma_map_4d(&tv, p.v, bf16, (uint64_t)p.Dv, p.Hkv, krows, nb, 1, kKeysT);
+    } else {
+        tk = tq;  // never read: no CTA has a key tile
+        tv = tq;
+    }
+    if (rc) return rc;
+    auto kern = bwd_dq_tc_kernel<T, D, DV>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+    if (e != cudaSuccess) {
+        set_error("tcgen05 dQ: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        return 3;
+    }
+    kern<<<(unsigned)grid, kThreadsT, L::SMEM, stream>>>(a, tq, to, tk, tv);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("tcgen05 dQ launch: %s", cudaGetErrorString(e));
+        return 3;
+    }
+    count_launch();
+    return 0;
+}
+
+template <typename T>
+int launch_dtype(const BwdParams &bp, bool bf16, cudaStream_t stream) {
+    const bool d128 = bp.f.D > 64, dv128 = bp.f.Dv > 64;
+    if (d128 && dv128) return launch_t<T, 128, 128>(bp, bf16, stream);
+    if (!d128 && !dv128) return launch_t<T, 64, 64>(bp, bf16, stream);
+    if (d128) return launch_t<T, 128, 64>(bp, bf16, stream);
+    return launch_t<T, 64, 128>(bp, bf16, stream);
+}
+
+}  // namespace
+
+bool bwd_dq_tc_supported(const AttnParams &p, int dtype) {
+    if (dtype != 1 && dtype != 2) return false;
+    if (p.D < 64 || p.D > 128 || p.D % 16 || p.Dv < 64 || p.Dv > 128 || p.Dv % 16) return false;
+    if (p.block_table != nullptr) return false;
+    const long long rows = p.cu_q ? p.Tq : (long long)p.Q;
+    const long long keys = p.cu_q ? p.Tk : (long long)p.K;
+    return rows < (1LL << 31) && keys < (1LL << 31);
+}
+
+int launch_bwd_dq_tc(const BwdParams &bp, int dtype, cudaStream_t stream) {
+    if (dtype == 2) return launch_dtype<__nv_bfloat16>(bp, true, stream);
+    return launch_dtype<__half>(bp, false, stream);
+}
+
+}  // namespace attn

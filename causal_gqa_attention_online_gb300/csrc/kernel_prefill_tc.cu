@@ -985,6 +985,13 @@ bool prefill_tc_supported(const AttnParams &p, int dtype) {
     return rows < (1LL << 31) && keys < (1LL << 31) && nunits < (1LL << 31);
 }
 
+int make_tma_map_4d(CUtensorMap *map, const void *ptr, bool bf16, uint64_t d0, uint64_t d1,
+                    uint64_t d2, uint64_t d3, uint32_t b1, uint32_t b2) {
+    return make_map(map, ptr,
+                    bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, d0,
+                    d1, d2, d3, b1, b2);
+}
+
 int launch_prefill_tc(const AttnParams &p, int dtype, cudaStream_t stream) {
     if (dtype == 2) return launch_dtype<__nv_bfloat16>(p, true, stream);
     return launch_dtype<__half>(p, false, stream);

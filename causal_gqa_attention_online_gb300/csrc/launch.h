@@ -3,6 +3,7 @@
 // message through set_error().
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -33,9 +34,20 @@ int launch_prefill_tc(const AttnParams &p, int dtype, cudaStream_t stream);
 bool fwd_mma_supported(const AttnParams &p, int dtype);
 int launch_fwd_mma(const AttnParams &p, int dtype, cudaStream_t stream);
 
-// Backward: rowsum(dO * O), then dK/dV and dQ.  mma: the mma.sync kernels
-// (bf16/fp16, bwd_mma_supported); otherwise the CUDA-core kernels.
+// 4-D TMA map over 16-bit elements [d3][d2][d1][d0] (d0 innermost), box
+// {64, b1, b2, 1}, 128-byte swizzle; returns 0 or an attn_status code.
+int make_tma_map_4d(CUtensorMap *map, const void *ptr, bool bf16, uint64_t d0, uint64_t d1,
+                    uint64_t d2, uint64_t d3, uint32_t b1, uint32_t b2);
+
+// tcgen05 dQ kernel of the backward (bf16/fp16, D and Dv multiples of 16 in
+// [64, 128], not paged); bp.delta must already hold rowsum(dO * O).
+bool bwd_dq_tc_supported(const AttnParams &p, int dtype);
+int launch_bwd_dq_tc(const BwdParams &bp, int dtype, cudaStream_t stream);
+
+// Backward: rowsum(dO * O), then dK/dV and dQ.  mode 0: the CUDA-core
+// kernels; 1: the mma.sync kernels (bf16/fp16, bwd_mma_supported); 2: mma.sync
+// dK/dV and the tcgen05 dQ kernel (also bwd_dq_tc_supported).
 bool bwd_mma_supported(const AttnParams &p, int dtype);
-int launch_bwd(const BwdParams &bp, int dtype, bool mma, cudaStream_t stream);
+int launch_bwd(const BwdParams &bp, int dtype, int mode, cudaStream_t stream);
 
 }  // namespace attn

@@ -105,7 +105,7 @@ def _call_bwd(lib, lse=1 << 24, dout=1 << 25, dq=1 << 26, D=64, Dv=64, algo=0, m
     (dict(lse=0), 1, "non-null"),
     (dict(dout=0), 1, "non-null"),
     (dict(dq=(1 << 26) + 4), 1, "aligned"),
-    (dict(algo=2), 1, "backward algo"),
+    (dict(algo=3), 1, "backward algo"),
     (dict(mask=5), 1, "mask"),
     (dict(mask=2, window=3), 1, "window"),
     (dict(D=320), 2, "up to 256"),

@@ -117,6 +117,16 @@ CASES = [
     ("bf16", "mma", 1, 16, 2, 90, 140, 128, 128, 0, 0, True),    # G = 8
     ("f16", "mma", 1, 32, 2, 40, 70, 64, 64, 30, 0, False),      # G = 16, window
     ("bf16", "mma", 2, 8, 2, 300, 300, 128, 128, 0, 0, False),   # several row tiles of a key tile
+    # tcgen05 dQ (with mma.sync dK/dV)
+    ("bf16", "tcgen05", 2, 8, 2, 200, 200, 128, 128, 0, 0, True),
+    ("bf16", "tcgen05", 1, 8, 2, 130, 330, 128, 128, 0, 0, False),
+    ("f16", "tcgen05", 2, 4, 2, 150, 300, 64, 64, 70, 0, True),
+    ("bf16", "tcgen05", 2, 4, 1, 97, 180, 80, 112, 0, 0, True),
+    ("bf16", "tcgen05", 1, 6, 6, 120, 120, 64, 128, 0, 1, False),
+    ("bf16", "tcgen05", 2, 8, 4, 70, 90, 128, 64, 0, 2, True),
+    ("bf16", "tcgen05", 3, 32, 8, 1, 700, 128, 128, 0, 0, True),
+    ("f16", "tcgen05", 1, 32, 2, 40, 70, 64, 64, 30, 0, False),
+    ("bf16", "tcgen05", 1, 4, 2, 300, 40, 128, 128, 0, 0, False),  # Q > K: rows without keys
 ]
 
 
@@ -142,10 +152,11 @@ def test_bwd_parity(case):
             structural_zeros(B, Q, K, sq, sk, window, mask))
 
 
-def test_bwd_negative_scale():
+@pytest.mark.parametrize("algo", ["mma", "tcgen05"])
+def test_bwd_negative_scale(algo):
     inp = synth.make_padded(1, 8, 2, 100, 150, 128, 128, "bf16", seed=85, scale=-0.15)
     dout = synth.make_dout(inp, seed=86)
-    compare("bf16", gpu_bwd(inp, dout, "mma"), oracle_bwd(inp, dout), "negative scale")
+    compare("bf16", gpu_bwd(inp, dout, algo), oracle_bwd(inp, dout), f"negative scale {algo}")
 
 
 def test_bwd_deterministic_and_algos_agree():
@@ -156,9 +167,16 @@ def test_bwd_deterministic_and_algos_agree():
     for x, y in zip(a, b):
         assert np.array_equal(x, y), "two runs differ"
     c = gpu_bwd(inp, dout, "generic")
+    t1 = gpu_bwd(inp, dout, "tcgen05")
+    t2 = gpu_bwd(inp, dout, "tcgen05")
+    for x, y in zip(t1, t2):
+        assert np.array_equal(x, y), "two tcgen05 runs differ"
+    # the tcgen05 path shares the dK/dV kernel
+    assert np.array_equal(t1[1], a[1]) and np.array_equal(t1[2], a[2])
     ref = oracle_bwd(inp, dout)
     compare("bf16", c, ref, "generic")
     compare("bf16", a, ref, "mma")
+    compare("bf16", t1, ref, "tcgen05")
 
 
 @pytest.mark.parametrize("window", [0, 45])
@@ -194,7 +212,7 @@ def test_bwd_varlen_matches_padded(window):
     compare("bf16", got, ref, "varlen")
 
 
-def test_bwd_rejects_mma_on_fp32_and_bad_algo():
+def test_bwd_rejects_tensor_kernels_on_fp32_and_bad_algo():
     inp = synth.make_padded(1, 2, 1, 8, 8, 64, 64, "f32", seed=93)
     dout = synth.make_dout(inp, seed=94)
     with pytest.raises(AttnError) as ei:
@@ -202,6 +220,9 @@ def test_bwd_rejects_mma_on_fp32_and_bad_algo():
     assert ei.value.status == 2
     with pytest.raises(AttnError) as ei:
         gpu_bwd(inp, dout, "tcgen05")
+    assert ei.value.status == 2
+    with pytest.raises(AttnError) as ei:
+        gpu_bwd(inp, dout, "decode")
     assert ei.value.status == 1
 
 
