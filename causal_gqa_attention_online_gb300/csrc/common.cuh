@@ -122,6 +122,22 @@ __device__ __forceinline__ void legal_range(int qi, int Qb, int Kb, int window, 
     if (window > 0) lo = max(0, diag - window + 1);
 }
 
+// Query positions [qf, qe) of a sequence that have a legal key in [k0, k1)
+// (k0 < k1 <= Kb); empty when qe <= qf.  The causal masks' ranges
+// [lo(qi), hi(qi)) both grow with qi, so the set is an interval.
+__device__ __forceinline__ void rows_for_keys(int k0, int k1, int Qb, int Kb, int window,
+                                              int mask, int &qf, int &qe) {
+    if (mask == 2) {
+        qf = 0;
+        qe = Qb;
+        return;
+    }
+    const int off = mask == 1 ? 0 : Kb - Qb;  // diagonal key of row qi is qi + off
+    qf = max(0, k0 - off);                     // hi(qi) > k0  <=>  qi + off >= k0
+    qe = Qb;
+    if (window > 0) qe = min(Qb, k1 + window - 1 - off);  // lo(qi) < k1
+}
+
 // Split-KV ownership of one row with legal keys [lo, hi).  The key axis is cut
 // into splits of `len` keys.  A row whose legal keys lie in one split (or that
 // has none) is "direct": the block of split `first` writes its final O / LSE.

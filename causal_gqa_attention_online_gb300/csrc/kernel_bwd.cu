@@ -36,22 +36,6 @@
 namespace attn {
 namespace {
 
-// Query positions [qf, qe) of a sequence that have a legal key in [k0, k1)
-// (k0 < k1 <= Kb); empty when qe <= qf.  The causal masks' ranges
-// [lo(qi), hi(qi)) both grow with qi, so the set is an interval.
-__device__ __forceinline__ void rows_for_keys(int k0, int k1, int Qb, int Kb, int window,
-                                              int mask, int &qf, int &qe) {
-    if (mask == 2) {
-        qf = 0;
-        qe = Qb;
-        return;
-    }
-    const int off = mask == 1 ? 0 : Kb - Qb;  // diagonal key of row qi is qi + off
-    qf = max(0, k0 - off);                     // hi(qi) > k0  <=>  qi + off >= k0
-    qe = Qb;
-    if (window > 0) qe = min(Qb, k1 + window - 1 - off);  // lo(qi) < k1
-}
-
 // A 1-D grid of (tile, sequence x KV head) blocks, ordered tile rank first:
 // every (sequence, KV head)'s rank-0 tile, then every rank-1 tile, ...  The
 // kernels give rank 0 to their longest tile, so the long blocks start first
@@ -867,7 +851,10 @@ int launch_mma_bwd_t(const BwdParams &bp, bool tc_dq, cudaStream_t stream) {
     if (!grid_fits(ktiles, y) || !grid_fits(((long long)p.Q * p.G + kQRows - 1) / kQRows, y))
         return 2;
     int rc = 0;
-    if (ktiles > 0) {
+    if (ktiles > 0 && tc_dq && bwd_dkdv_tc_supported(p, std::is_same<T, __half>::value ? 1 : 2)) {
+        rc = launch_bwd_dkdv_tc(bp, std::is_same<T, __half>::value ? 1 : 2, stream);
+        if (rc) return rc;
+    } else if (ktiles > 0) {
         const size_t s = (size_t)kMKeys * 2 * (DW + DVW) +
                          (size_t)kMStages * kMRows * (2 * (DW + DVW) + 16) + 4 * 16 * 32 * 4 +
                          kMStages * 4;

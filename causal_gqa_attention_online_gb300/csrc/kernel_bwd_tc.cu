@@ -1,5 +1,6 @@
-// kernel_bwd_tc.cu -- the dQ half of the attention backward on the 5th-
-// generation tensor cores (tcgen05, TMEM accumulators, TMA-fed shared memory).
+// kernel_bwd_tc.cu -- the attention backward on the 5th-generation tensor
+// cores (tcgen05, TMEM accumulators, TMA-fed shared memory): a dQ kernel and
+// a dK/dV kernel (further down).
 //
 // dQ[q] = scale * sum_k dS[q,k] K[k],  dS = P (dP - Dq),  P = exp2(S c - LSE_2),
 // S = Q K^T, dP = dO V^T over each row's legal keys (the derivative of the
@@ -387,6 +388,431 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// dK / dV.  A CTA owns 128 keys of one (sequence, KV head) -- TMEM lane = key
+// -- with K and V resident in shared memory, and streams the rows that attend
+// to them: 64 rows a tile of the flattened (query position, head-in-group)
+// space, all heads of the group, one TMA box {64 columns, G heads, 64 / G
+// positions} per 64 columns (the forward loop transposed, keys resident and
+// rows streamed, as the FlyDSL page describes its dK/dV kernel):
+//   S^T = K Q^T and dP^T = V dO^T into TMEM buffer b (M = 128 keys, N = 64
+//   rows); the elementwise warps turn them into P^T and dS^T (16-bit pairs
+//   over the first halves of S^T_b and dP^T_b); then dV += P^T dO and
+//   dK += dS^T Q with dO and Q read MN-major from the same row tile.
+// TMEM: S^T0 S^T1 | dP^T0 dP^T1 | dV | dK.  Per-row LSE, Dq and legal key
+// range ride with each row tile (written by the loader warp, published by
+// the tile's full barrier).
+constexpr int kKeysK = 128;  // keys per CTA (MMA M)
+constexpr int kRowsK = 64;   // rows per tile (N of S^T and dP^T, contraction of dV and dK)
+constexpr int kStagesK = 3;
+
+template <int D, int DV> struct KvLayout {
+    static constexpr int KCH = kKeysK * 128;  // a 64-column chunk of the 128-key tile
+    static constexpr int RCH = kRowsK * 128;  // a 64-column chunk of a 64-row tile
+    static constexpr int KTILE = (D / 64) * KCH;
+    static constexpr int VTILE = (DV / 64) * KCH;
+    static constexpr int QTILE = (D / 64) * RCH;
+    static constexpr int OTILE = (DV / 64) * RCH;
+    static constexpr int STAGE = QTILE + OTILE;
+    static constexpr int STATS = kRowsK * 16;  // per row: LSE (log2 units), Dq, lo, hi
+    static constexpr int K_OFF = 0;
+    static constexpr int V_OFF = KTILE;
+    static constexpr int R_OFF = KTILE + VTILE;
+    static constexpr int ST_OFF = R_OFF + kStagesK * STAGE;
+    static constexpr int FLAG_OFF = ST_OFF + kStagesK * STATS;  // [kStagesK] ints: interior tile
+    static constexpr int BAR_OFF = FLAG_OFF + 64;
+    static constexpr int SMEM = 1024 + BAR_OFF + 256;
+    static constexpr int ST_COL = 0, DPT_COL = 128, DV_COL = 256, DK_COL = 256 + DV;
+    static_assert(DK_COL + D <= 512, "TMEM budget");
+    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+};
+
+enum : int {
+    K_KV_FULL = 0,
+    K_S_FULL = 1,     // [2]
+    K_DS_READY = 3,   // [2]
+    K_ACC_FULL = 5,
+    K_TEARDOWN = 6,
+    K_ROW_FULL = 7,   // [kStagesK] full, then [kStagesK] empty
+    K_NBARS = 7 + 2 * kStagesK,
+};
+
+struct KvArgs {
+    BwdParams bp;
+    int nkt;           // 128-key tiles per (sequence, KV head)
+    float c2;          // scale * log2(e)
+    uint32_t idesc_s;  // M128 N64, both K-major
+    uint32_t idesc_v;  // M128 N=DV, B MN-major
+    uint32_t idesc_k;  // M128 N=D, B MN-major
+};
+
+template <typename T, int D, int DV>
+__global__ void __launch_bounds__(kThreadsT, 1)
+    bwd_dkdv_tc_kernel(const __grid_constant__ KvArgs a, const __grid_constant__ CUtensorMap tmQ,
+                       const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV) {
+    using L = KvLayout<D, DV>;
+    extern __shared__ uint8_t smem_k[];
+    const BwdParams &bp = a.bp;
+    const AttnParams &p = bp.f;
+    const int G = p.G;
+    const int PP = kRowsK / G;  // query positions per row tile
+
+    const int nbh = p.B * p.Hkv;
+    const int rank = blockIdx.x / nbh;  // the first keys are seen by the most rows: rank 0 first
+    const int b = (blockIdx.x % nbh) / p.Hkv, kvh = (blockIdx.x % nbh) % p.Hkv;
+    const SeqInfo si = seq_info(p, b);
+    const bool padded = p.cu_q == nullptr;
+    const int k0 = rank * kKeysK;
+    const int kcap = padded ? p.K : si.Kb;  // keys this CTA may write
+    if (k0 >= kcap) return;                 // uniform: before any barrier
+
+    const uint32_t raw = smem_addr(smem_k);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_k + (base - raw);
+    const uint32_t bars = base + L::BAR_OFF;
+    auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + L::BAR_OFF + 8 * K_NBARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    auto row_full = [&](int s) { return bar(K_ROW_FULL + s); };
+    auto row_empty = [&](int s) { return bar(K_ROW_FULL + kStagesK + s); };
+    auto rstage = [&](int s) { return base + L::R_OFF + (uint32_t)s * L::STAGE; };
+    float *stats = reinterpret_cast<float *>(gbase + L::ST_OFF);  // [stage][4][kRowsK]
+    int *flags = reinterpret_cast<int *>(gbase + L::FLAG_OFF);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // the query positions that attend to any of the CTA's keys: an interval
+    int qf = 0, qe = 0;
+    if (k0 < si.Kb) rows_for_keys(k0, min(k0 + kKeysK, si.Kb), si.Qb, si.Kb, p.window, p.mask, qf, qe);
+    const int ntiles = qe > qf ? (qe - qf + PP - 1) / PP : 0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(K_KV_FULL), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(K_S_FULL + i), 1);
+            mbar_init(bar(K_DS_READY + i), 128);
+        }
+        mbar_init(bar(K_ACC_FULL), 1);
+        mbar_init(bar(K_TEARDOWN), 1);
+        for (int s = 0; s < kStagesK; ++s) {
+            mbar_init(row_full(s), 1);
+            mbar_init(row_empty(s), 1);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarpT) {
+        tmem_alloc(smem_addr(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kLoadWarpT) {
+        // ------------------------------------------------ TMA producer + row stats
+        const int qrow = padded ? 0 : (int)si.q_off;
+        const int krow = padded ? 0 : (int)si.k_off;
+        const int bc = padded ? b : 0;
+        bool ok = true;
+        uint32_t armed = 0, armed_ph = 0;
+        if (ntiles > 0 && lane == 0) {
+            mbar_arrive_expect_tx(bar(K_KV_FULL), L::KTILE + L::VTILE);
+            for (int c = 0; c < D / 64; ++c)
+                tma_load_4d(base + L::K_OFF + c * L::KCH, &tmK, bar(K_KV_FULL), c * 64, kvh,
+                            krow + k0, bc);
+            for (int c = 0; c < DV / 64; ++c)
+                tma_load_4d(base + L::V_OFF + c * L::KCH, &tmV, bar(K_KV_FULL), c * 64, kvh,
+                            krow + k0, bc);
+        }
+        for (int t = 0; t < ntiles && ok; ++t) {
+            const int s = t % kStagesK;
+            const uint32_t ph = (uint32_t)(t / kStagesK) & 1u;
+            ok = warp_wait_t(row_empty(s), ph ^ 1u, abort_flag);
+            if (!ok) break;
+            // per-row statistics of the tile, two rows a lane
+            float *st = stats + s * 4 * kRowsK;
+            bool inner = true;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int i = lane + 32 * e;  // row of the tile = smem row
+                const int pos = qf + t * PP + i / G;
+                const int hh = kvh * G + i % G;
+                int lo = 0, hi = 0;
+                if (pos < si.Qb) legal_range(pos, si.Qb, si.Kb, p.window, p.mask, lo, hi);
+                float l2 = 0.f, dl = 0.f;
+                if (hi > lo) {
+                    const long long row = (si.q_off + pos) * p.Hq + hh;
+                    l2 = p.lse[row] * kLog2e;
+                    dl = bp.delta[row];
+                }
+                st[i] = l2;
+                st[kRowsK + i] = dl;
+                reinterpret_cast<int *>(st)[2 * kRowsK + i] = lo;
+                reinterpret_cast<int *>(st)[3 * kRowsK + i] = hi;
+                inner = inner && lo <= k0 && hi >= k0 + kKeysK;
+            }
+            inner = __all_sync(0xffffffffu, inner);
+            if (lane == 0) flags[s] = inner ? 1 : 0;
+            __syncwarp();
+            if (lane == 0) {
+                const int r0 = qrow + qf + t * PP;
+                mbar_arrive_expect_tx(row_full(s), L::STAGE);
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_4d(rstage(s) + c * L::RCH, &tmQ, row_full(s), c * 64, kvh * G, r0, bc);
+                for (int c = 0; c < DV / 64; ++c)
+                    tma_load_4d(rstage(s) + L::QTILE + c * L::RCH, &tmO, row_full(s), c * 64,
+                                kvh * G, r0, bc);
+                armed |= 1u << s;
+                armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+            }
+        }
+        if (!ok && lane == 0) raise_abort_t(abort_flag, p.status);
+        if (lane == 0) {
+            // drain: every copy issued has landed before the CTA exits
+            if (ntiles > 0) mbar_wait(bar(K_KV_FULL), 0, abort_flag, kWaitNsT);
+            for (int s = 0; s < kStagesK; ++s)
+                if (armed & (1u << s))
+                    mbar_wait(row_full(s), (armed_ph >> s) & 1u, abort_flag, kWaitNsT);
+        }
+    } else if (warp == kMmaWarpT) {
+        // ------------------------------------------------------------ MMA issuer
+        bool ok = ntiles == 0 || warp_wait_t(bar(K_KV_FULL), 0, abort_flag);
+        const uint64_t kd = sw128_desc(base + L::K_OFF, 16, 1024);
+        const uint64_t vd = sw128_desc(base + L::V_OFF, 16, 1024);
+        for (int t = 0; t <= ntiles && ok; ++t) {
+            if (t < ntiles) {
+                const int s = t % kStagesK, bf = t & 1;
+                if (!warp_wait_t(row_full(s), (uint32_t)(t / kStagesK) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    // buffer bf was last read by the dV / dK MMAs of tile t - 2,
+                    // issued earlier by this thread
+                    const uint64_t qd = sw128_desc(rstage(s), 16, 1024);
+                    const uint64_t od = sw128_desc(rstage(s) + L::QTILE, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + L::ST_COL + bf * kRowsK,
+                               kd + (((kk / 4) * L::KCH + (kk % 4) * 32) >> 4),
+                               qd + (((kk / 4) * L::RCH + (kk % 4) * 32) >> 4), a.idesc_s, kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < DV / 16; ++kk)
+                        mma_ss(tmem + L::DPT_COL + bf * kRowsK,
+                               vd + (((kk / 4) * L::KCH + (kk % 4) * 32) >> 4),
+                               od + (((kk / 4) * L::RCH + (kk % 4) * 32) >> 4), a.idesc_s, kk > 0);
+                    mma_commit(bar(K_S_FULL + bf));
+                }
+                __syncwarp();
+            }
+            if (t >= 1) {
+                const int tt = t - 1, bf = tt & 1, s = tt % kStagesK;
+                if (!warp_wait_t(bar(K_DS_READY + bf), (uint32_t)(tt >> 1) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // rows of the tile past the sequence's queries may hold anything
+                // (NaN included): their P and dS are 0, and the Q and dO rows are
+                // zeroed so that 0 * row stays 0 (S^T and dP^T of the tile have
+                // completed: the elementwise warps read them)
+                const int pos0 = qf + tt * PP;
+                const int nreal = min(kRowsK, max(0, (si.Qb - pos0) * G));
+                if (nreal < kRowsK) {
+                    uint8_t *rt = gbase + (rstage(s) - base);
+                    const int nzero = kRowsK - nreal;
+                    for (int c = 0; c < D / 64 + DV / 64; ++c)
+                        for (int i = lane; i < nzero * 8; i += 32)
+                            *reinterpret_cast<uint4 *>(rt + c * L::RCH + nreal * 128 + i * 16) =
+                                make_uint4(0, 0, 0, 0);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                if (lane == 0) {
+                    const uint64_t qmn = sw128_desc(rstage(s), L::RCH, 1024);
+                    const uint64_t omn = sw128_desc(rstage(s) + L::QTILE, L::RCH, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < kRowsK / 16; ++kk)
+                        mma_ts(tmem + L::DV_COL, tmem + L::ST_COL + bf * kRowsK + kk * 8,
+                               omn + ((kk * 2048) >> 4), a.idesc_v, (tt > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < kRowsK / 16; ++kk)
+                        mma_ts(tmem + L::DK_COL, tmem + L::DPT_COL + bf * kRowsK + kk * 8,
+                               qmn + ((kk * 2048) >> 4), a.idesc_k, (tt > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(row_empty(s));
+                    if (tt == ntiles - 1) mma_commit(bar(K_ACC_FULL));
+                }
+                __syncwarp();
+            }
+        }
+        if (!ok && lane == 0) raise_abort_t(abort_flag, p.status);
+        if (lane == 0) {
+            mma_commit(bar(K_TEARDOWN));
+            mbar_wait(bar(K_TEARDOWN), 0, abort_flag, kWaitNsT);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------- elementwise warps, epilogue
+        const int r = warp * 32 + lane;  // key of the tile = TMEM lane
+        const int key = k0 + r;
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        bool ok = true;
+        for (int t = 0; t < ntiles && ok; ++t) {
+            const int bf = t & 1, s = t % kStagesK;
+            if (!warp_wait_t(bar(K_S_FULL + bf), (uint32_t)(t >> 1) & 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            // the tile's row statistics: published with its row_full phase (the
+            // stage is not refilled before this tile's dV / dK MMAs, which wait
+            // for this warpgroup)
+            if (!warp_wait_t(row_full(s), (uint32_t)(t / kStagesK) & 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t tS = tmem + lane_off + L::ST_COL + bf * kRowsK;
+            const uint32_t tP = tmem + lane_off + L::DPT_COL + bf * kRowsK;
+            uint32_t sv[2][32], pv[2][32];
+            tmem_ld32(tS, sv[0]);
+            tmem_ld32(tS + 32, sv[1]);
+            tmem_ld32(tP, pv[0]);
+            tmem_ld32(tP + 32, pv[1]);
+            tmem_ld_wait();
+            const float *st = stats + s * 4 * kRowsK;
+            const int *sti = reinterpret_cast<const int *>(st);
+            const bool inner = flags[s] != 0;
+            uint32_t pk[32], dk[32];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    float pp[2], dd[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int row = hf * 32 + i + e;
+                        const bool legal =
+                            inner || (key >= sti[2 * kRowsK + row] && key < sti[3 * kRowsK + row]);
+                        const float pr = ex2f(__uint_as_float(sv[hf][i + e]) * a.c2 - st[row]);
+                        pp[e] = legal ? pr : 0.f;
+                        dd[e] = legal ? pr * (__uint_as_float(pv[hf][i + e]) - st[kRowsK + row]) : 0.f;
+                    }
+                    pk[hf * 16 + i / 2] = pack16<T>(pp[0], pp[1]);
+                    dk[hf * 16 + i / 2] = pack16<T>(dd[0], dd[1]);
+                }
+            tmem_st32(tS, pk);  // P^T over the first half of S^T_bf
+            tmem_st32(tP, dk);  // dS^T over the first half of dP^T_bf
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar(K_DS_READY + bf));
+        }
+        if (!ok && lane == 0) raise_abort_t(abort_flag, p.status);
+        // epilogue: dV and dK * scale to memory (zeros for keys no row sees)
+        if (ok && ntiles > 0) {
+            ok = warp_wait_t(bar(K_ACC_FULL), 0, abort_flag);
+            if (!ok && lane == 0) raise_abort_t(abort_flag, p.status);
+            tc_fence_after();
+        }
+        const bool writes = key < kcap;
+        const bool has = ok && ntiles > 0;
+        const long long krow = (si.k_off + key) * p.Hkv + kvh;
+        T *dvg = static_cast<T *>(bp.dv), *dkg = static_cast<T *>(bp.dk);
+#pragma unroll
+        for (int c = 0; c < DV / 32; ++c) {
+            uint32_t v[32];
+            if (has) {
+                tmem_ld32(tmem + lane_off + L::DV_COL + c * 32, v);
+                tmem_ld_wait();
+            }
+            if (writes)
+#pragma unroll
+                for (int i = 0; i < 32; i += 2)
+                    if (c * 32 + i < p.Dv)
+                        *reinterpret_cast<uint32_t *>(dvg + krow * p.Dv + c * 32 + i) =
+                            pack16<T>(has ? __uint_as_float(v[i]) : 0.f,
+                                      has ? __uint_as_float(v[i + 1]) : 0.f);
+        }
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            if (has) {
+                tmem_ld32(tmem + lane_off + L::DK_COL + c * 32, v);
+                tmem_ld_wait();
+            }
+            if (writes)
+#pragma unroll
+                for (int i = 0; i < 32; i += 2)
+                    if (c * 32 + i < p.D)
+                        *reinterpret_cast<uint32_t *>(dkg + krow * p.D + c * 32 + i) =
+                            pack16<T>(has ? __uint_as_float(v[i]) * p.scale : 0.f,
+                                      has ? __uint_as_float(v[i + 1]) * p.scale : 0.f);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarpT) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <typename T, int D, int DV>
+int launch_kv_t(const BwdParams &bp, bool bf16, cudaStream_t stream) {
+    using L = KvLayout<D, DV>;
+    const AttnParams &p = bp.f;
+    KvArgs a;
+    a.bp = bp;
+    a.nkt = (p.K + kKeysK - 1) / kKeysK;
+    a.c2 = p.scale * kLog2e;
+    a.idesc_s = idesc_f16(bf16, kKeysK, kRowsK, false, false);
+    a.idesc_v = idesc_f16(bf16, kKeysK, DV, true, false);
+    a.idesc_k = idesc_f16(bf16, kKeysK, D, true, false);
+    const long long grid = (long long)a.nkt * p.B * p.Hkv;
+    if (grid == 0) return 0;
+    if (grid >= (1LL << 31)) {
+        set_error("tcgen05 dK/dV: %lld blocks exceed one launch", grid);
+        return 2;
+    }
+    const bool padded = p.cu_q == nullptr;
+    const uint64_t qrows = padded ? (uint64_t)p.Q : (uint64_t)p.Tq;
+    const uint64_t krows = padded ? (uint64_t)p.K : (uint64_t)p.Tk;
+    const uint64_t nb = padded ? (uint64_t)p.B : 1;
+    const uint32_t pp = (uint32_t)(kRowsK / p.G);
+    CUtensorMap tq, to, tk, tv;
+    int rc = make_tma_map_4d(&tq, p.q, bf16, (uint64_t)p.D, p.Hq, qrows, nb, (uint32_t)p.G, pp);
+    if (!rc) rc = make_tma_map_4d(&to, bp.dout, bf16, (uint64_t)p.Dv, p.Hq, qrows, nb, (uint32_t)p.G, pp);
+    if (!rc) rc = make_tma_map_4d(&tk, p.k, bf16, (uint64_t)p.D, p.Hkv, krows, nb, 1, kKeysK);
+    if (!rc) rc = make_tma_map_4d(&tv, p.v, bf16, (uint64_t)p.Dv, p.Hkv, krows, nb, 1, kKeysK);
+    if (rc) return rc;
+    auto kern = bwd_dkdv_tc_kernel<T, D, DV>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+    if (e != cudaSuccess) {
+        set_error("tcgen05 dK/dV: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        return 3;
+    }
+    kern<<<(unsigned)grid, kThreadsT, L::SMEM, stream>>>(a, tq, to, tk, tv);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("tcgen05 dK/dV launch: %s", cudaGetErrorString(e));
+        return 3;
+    }
+    count_launch();
+    return 0;
+}
+
+template <typename T>
+int launch_kv_dtype(const BwdParams &bp, bool bf16, cudaStream_t stream) {
+    const bool d128 = bp.f.D > 64, dv128 = bp.f.Dv > 64;
+    if (d128 && dv128) return launch_kv_t<T, 128, 128>(bp, bf16, stream);
+    if (!d128 && !dv128) return launch_kv_t<T, 64, 64>(bp, bf16, stream);
+    if (d128) return launch_kv_t<T, 128, 64>(bp, bf16, stream);
+    return launch_kv_t<T, 64, 128>(bp, bf16, stream);
+}
+
 template <typename T, int D, int DV>
 int launch_t(const BwdParams &bp, bool bf16, cudaStream_t stream) {
     using L = DqLayout<D, DV>;
@@ -452,6 +878,16 @@ bool bwd_dq_tc_supported(const AttnParams &p, int dtype) {
     const long long rows = p.cu_q ? p.Tq : (long long)p.Q;
     const long long keys = p.cu_q ? p.Tk : (long long)p.K;
     return rows < (1LL << 31) && keys < (1LL << 31);
+}
+
+bool bwd_dkdv_tc_supported(const AttnParams &p, int dtype) {
+    // the rows of a tile are (position, head) pairs of one KV group: 64 / G positions
+    return bwd_dq_tc_supported(p, dtype) && p.G >= 1 && p.G <= kRowsK && kRowsK % p.G == 0;
+}
+
+int launch_bwd_dkdv_tc(const BwdParams &bp, int dtype, cudaStream_t stream) {
+    if (dtype == 2) return launch_kv_dtype<__nv_bfloat16>(bp, true, stream);
+    return launch_kv_dtype<__half>(bp, false, stream);
 }
 
 int launch_bwd_dq_tc(const BwdParams &bp, int dtype, cudaStream_t stream) {

@@ -43,10 +43,14 @@ int make_tma_map_4d(CUtensorMap *map, const void *ptr, bool bf16, uint64_t d0, u
 // [64, 128], not paged); bp.delta must already hold rowsum(dO * O).
 bool bwd_dq_tc_supported(const AttnParams &p, int dtype);
 int launch_bwd_dq_tc(const BwdParams &bp, int dtype, cudaStream_t stream);
+// tcgen05 dK/dV kernel: as bwd_dq_tc_supported, and Hq / Hkv divides 64.
+bool bwd_dkdv_tc_supported(const AttnParams &p, int dtype);
+int launch_bwd_dkdv_tc(const BwdParams &bp, int dtype, cudaStream_t stream);
 
 // Backward: rowsum(dO * O), then dK/dV and dQ.  mode 0: the CUDA-core
-// kernels; 1: the mma.sync kernels (bf16/fp16, bwd_mma_supported); 2: mma.sync
-// dK/dV and the tcgen05 dQ kernel (also bwd_dq_tc_supported).
+// kernels; 1: the mma.sync kernels (bf16/fp16, bwd_mma_supported); 2: the
+// tcgen05 dQ kernel (bwd_dq_tc_supported) and the tcgen05 dK/dV kernel where
+// it applies (bwd_dkdv_tc_supported), the mma.sync one otherwise.
 bool bwd_mma_supported(const AttnParams &p, int dtype);
 int launch_bwd(const BwdParams &bp, int dtype, int mode, cudaStream_t stream);
 
