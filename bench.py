@@ -442,7 +442,7 @@ def run_gpu(args, world, rank, local):
                "value": round(world * tfb, 3), "unit": "TFLOP/s",
                "ms_per_step": round(bw["ms"], 5), "steps": bw["steps"],
                "flop_per_step": bw["flop"], "gpu_launches": int(bw["launches"] * bw["steps"]),
-               "kernels": "mma.sync m16n8k16 (warp-level tensor cores)",
+               "kernels": "tcgen05 dK/dV and dQ (TMEM accumulators, TMA-fed)",
                "roofline": {"bound": "tensor", "achieved": round(tfb, 3), "peak": tf_peak,
                             "unit": "TFLOP/s", "frac": round(tfb / tf_peak, 4),
                             "traffic": traffic.get("backward"),
@@ -522,16 +522,21 @@ def run_gpu(args, world, rank, local):
 KERNEL_SOURCES = {
     "prefill": "causal_gqa_attention_online_gb300/csrc/kernel_prefill_tc.cu",
     "decode": "causal_gqa_attention_online_gb300/csrc/kernel_decode.cu",
-    "backward": "causal_gqa_attention_online_gb300/csrc/kernel_bwd.cu",
+    "backward": ("causal_gqa_attention_online_gb300/csrc/kernel_bwd.cu",
+                 "causal_gqa_attention_online_gb300/csrc/kernel_bwd_tc.cu"),
     "wide256": "causal_gqa_attention_online_gb300/csrc/kernel_fwd_mma.cu",
     "wide512": "causal_gqa_attention_online_gb300/csrc/kernel_fwd_mma.cu",
 }
 
 
-def source_sha(rel: str) -> str:
+def source_sha(rel) -> str:
+    """sha256[:16] of a kernel source file (or of several, concatenated)."""
     import hashlib
-    with open(os.path.join(ROOT, rel), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for r in ((rel,) if isinstance(rel, str) else rel):
+        with open(os.path.join(ROOT, r), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def load_traffic():
