@@ -207,8 +207,8 @@ def attn_bwd(q, k, v, o, lse, dout, dq=None, dk=None, dv=None, *, seqlens_q=None
     """Gradients of attn_fwd (padded layout) for the output gradient ``dout``
     [B,Q,Hq,Dv]; ``o`` and ``lse`` are attn_fwd's outputs for q, k, v with the
     same seqlens / window / scale / mask.  ``algo``: "auto", "generic" (CUDA
-    cores), "mma" (mma.sync tensor cores) or "tcgen05" (mma.sync dK/dV and a
-    tcgen05 dQ).  Returns (dq, dk, dv)."""
+    cores), "mma" (mma.sync tensor cores) or "tcgen05" (tcgen05 dQ and dK/dV
+    kernels).  Returns (dq, dk, dv)."""
     lib = load_library()
     B, Q, Hq, D = q.shape
     K, Hkv = k.shape[1], k.shape[2]

@@ -82,7 +82,7 @@ enum attn_algo {
     ATTN_ALGO_AUTO = 0,     /* choose by dtype, head widths and query length */
     ATTN_ALGO_GENERIC = 1,  /* CUDA-core online softmax: any dtype, D, Dv <= 512 */
     ATTN_ALGO_TCGEN05 = 2,  /* tcgen05/TMEM prefill: bf16/fp16, D, Dv multiples of 16 in
-                               [64, 128]; in the backward, the tcgen05 dQ kernel */
+                               [64, 128]; in the backward, the tcgen05 dQ and dK/dV kernels */
     ATTN_ALGO_DECODE = 3,   /* split-KV tensor-core decode: bf16/fp16, Q*G <= 16 */
     ATTN_ALGO_MMA = 4       /* warp-level mma.sync tensor cores, bf16/fp16: the forward for
                                D, Dv multiples of 8 up to 512 (chosen by AUTO where the
@@ -282,9 +282,10 @@ ATTN_API int attn_fwd_staged(const void *hq, const void *hk, const void *hv, voi
  *   algo          ATTN_ALGO_AUTO (ATTN_ALGO_TCGEN05 where it applies, else
  *                 ATTN_ALGO_MMA, else the CUDA-core kernels), ATTN_ALGO_GENERIC,
  *                 ATTN_ALGO_MMA (mma.sync dK/dV and dQ; bf16/fp16, widths
- *                 multiples of 8 up to 128) or ATTN_ALGO_TCGEN05 (mma.sync
- *                 dK/dV and a tcgen05 dQ; bf16/fp16, widths multiples of 16
- *                 in [64, 128], padded or packed layout)
+ *                 multiples of 8 up to 128) or ATTN_ALGO_TCGEN05 (tcgen05
+ *                 dQ and dK/dV kernels -- the dK/dV one when Hq / Hkv
+ *                 divides 64, else mma.sync; bf16/fp16, widths multiples of
+ *                 16 in [64, 128], padded or packed layout)
  * Head widths up to 256 (wider ones return ATTN_ERR_UNSUPPORTED).
  * All pointers are device memory, 16-byte aligned.  A workspace of
  * 4 * B * Q * Hq bytes comes from the library's stream-ordered pool.  The
