@@ -40,9 +40,11 @@ using namespace sm100;
 constexpr int kRowsT = 128;  // query rows per CTA (MMA M)
 constexpr int kKeysT = 64;   // keys per tile (N of S and dP, contraction of dQ)
 constexpr int kStagesT = 4;  // K/V ring depth
-constexpr int kThreadsT = 192;
+constexpr int kThreadsT = 192;  // dK/dV: warps 0-3 elementwise, 4 TMA, 5 MMA
+constexpr int kThreadsQ = 224;  // dQ: warps 0-3 elementwise, 4 TMA, 5 S / dP MMAs, 6 dQ MMAs
 constexpr int kLoadWarpT = 4;
 constexpr int kMmaWarpT = 5;
+constexpr int kDqWarpT = 6;
 constexpr uint64_t kWaitNsT = 2000000000ull;  // 2 s
 constexpr int kStatusTimeoutBwdTc = 0x301;
 
@@ -78,9 +80,10 @@ enum : int {
     T_S_FULL = 1,     // [2]
     T_DS_READY = 3,   // [2]
     T_DQ_FULL = 5,
-    T_TEARDOWN = 6,
-    T_KV_FULL = 7,    // [kStagesT] full, then [kStagesT] empty
-    T_NBARS = 7 + 2 * kStagesT,
+    T_TEARDOWN = 6,   // one commit from each MMA-issuing warp
+    T_S_EMPTY = 7,    // [2]: the dQ MMAs that read dS out of S_b have completed
+    T_KV_FULL = 9,    // [kStagesT] full, then [kStagesT] empty
+    T_NBARS = 9 + 2 * kStagesT,
 };
 
 __device__ __forceinline__ float ex2f(float x) {
@@ -110,7 +113,7 @@ __device__ __forceinline__ void raise_abort_t(volatile int *abort_flag, int *sta
 }
 
 template <typename T, int D, int DV>
-__global__ void __launch_bounds__(kThreadsT, 1)
+__global__ void __launch_bounds__(kThreadsQ, 1)
     bwd_dq_tc_kernel(const __grid_constant__ DqArgs a, const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV) {
@@ -162,7 +165,9 @@ __global__ void __launch_bounds__(kThreadsT, 1)
             mbar_init(bar(T_DS_READY + i), 128);
         }
         mbar_init(bar(T_DQ_FULL), 1);
-        mbar_init(bar(T_TEARDOWN), 1);
+        mbar_init(bar(T_TEARDOWN), 2);
+        mbar_init(bar(T_S_EMPTY), 1);
+        mbar_init(bar(T_S_EMPTY + 1), 1);
         for (int s = 0; s < kStagesT; ++s) {
             mbar_init(kv_full(s), 1);
             mbar_init(kv_empty(s), 1);
@@ -218,79 +223,94 @@ __global__ void __launch_bounds__(kThreadsT, 1)
                     mbar_wait(kv_full(s), (armed_ph >> s) & 1u, abort_flag, kWaitNsT);
         }
     } else if (warp == kMmaWarpT) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------ S / dP MMA issuer
+        // Two issuing warps: one thread issuing every MMA of a tile spends more
+        // time issuing than the tensor core spends on them (the products of a
+        // 64-key tile are small), so the dQ products have a warp of their own.
         bool ok = ntiles == 0 || warp_wait_t(bar(T_QD_FULL), 0, abort_flag);
         const uint64_t qd = sw128_desc(base + L::Q_OFF, 16, 1024);
         const uint64_t od = sw128_desc(base + L::DO_OFF, 16, 1024);
-        const uint32_t dq_tm = tmem + L::DQ_COL;
-        for (int j = 0; j <= ntiles && ok; ++j) {
-            if (j < ntiles) {
-                const int s = j % kStagesT, bf = j & 1;
-                if (!warp_wait_t(kv_full(s), (uint32_t)(j / kStagesT) & 1u, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (lane == 0) {
-                    // S_bf was last read by the dQ MMA of tile j - 2, issued
-                    // earlier by this thread (tcgen05.mma runs in issue order)
-                    const uint64_t kd = sw128_desc(stage(s), 16, 1024);
-                    const uint64_t vd = sw128_desc(stage(s) + L::KTILE, 16, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + L::S_COL + bf * kKeysT,
-                               qd + (((kk / 4) * L::QCH + (kk % 4) * 32) >> 4),
-                               kd + (((kk / 4) * L::KCH + (kk % 4) * 32) >> 4), a.idesc_s, kk > 0);
-#pragma unroll
-                    for (int kk = 0; kk < DV / 16; ++kk)
-                        mma_ss(tmem + L::DP_COL + bf * kKeysT,
-                               od + (((kk / 4) * L::QCH + (kk % 4) * 32) >> 4),
-                               vd + (((kk / 4) * L::KCH + (kk % 4) * 32) >> 4), a.idesc_s, kk > 0);
-                    mma_commit(bar(T_S_FULL + bf));
-                }
-                __syncwarp();
+        for (int j = 0; j < ntiles && ok; ++j) {
+            const int s = j % kStagesT, bf = j & 1;
+            if (!warp_wait_t(kv_full(s), (uint32_t)(j / kStagesT) & 1u, abort_flag)) {
+                ok = false;
+                break;
             }
-            if (j >= 1) {
-                // dQ += dS K for tile jj = j - 1, once its dS is in TMEM
-                const int jj = j - 1, bf = jj & 1, s = jj % kStagesT;
-                if (!warp_wait_t(bar(T_DS_READY + bf), (uint32_t)(jj >> 1) & 1u, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                // Keys past the last one in use (last tile only) are left out 16
-                // at a time; the K rows of the last 16-key step past it may hold
-                // anything (NaN included), so they are zeroed: 0 * K must stay 0.
-                // S of this tile has completed (the elementwise warps read it).
-                const int nvalid = min(kKeysT, khi - (tfirst + jj * kKeysT));
-                const int ksteps = (nvalid + 15) / 16;
-                const int nzero = ksteps * 16 - nvalid;
-                if (nzero > 0) {
-                    uint8_t *kt = gbase + (stage(s) - base) + nvalid * 128;
-#pragma unroll
-                    for (int c = 0; c < D / 64; ++c)
-                        for (int i = lane; i < nzero * 8; i += 32)
-                            *reinterpret_cast<uint4 *>(kt + c * L::KCH + i * 16) =
-                                make_uint4(0, 0, 0, 0);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                }
-                if (lane == 0) {
-                    // K as the MN-major B operand: 64-column chunks L::KCH apart
-                    const uint64_t kmn = sw128_desc(stage(s), L::KCH, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < kKeysT / 16; ++kk)
-                        if (kk < ksteps)
-                            mma_ts(dq_tm, tmem + L::S_COL + bf * kKeysT + kk * 8,
-                                   kmn + ((kk * 2048) >> 4), a.idesc_dq, (jj > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(kv_empty(s));
-                    if (jj == ntiles - 1) mma_commit(bar(T_DQ_FULL));
-                }
-                __syncwarp();
+            // S_bf and dP_bf were last read for tile j - 2: dP by the elementwise
+            // warps, S (as dS) by its dQ MMAs, which have completed
+            if (j >= 2 && !warp_wait_t(bar(T_S_EMPTY + bf), (uint32_t)((j - 2) >> 1) & 1u, abort_flag)) {
+                ok = false;
+                break;
             }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint64_t kd = sw128_desc(stage(s), 16, 1024);
+                const uint64_t vd = sw128_desc(stage(s) + L::KTILE, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + L::S_COL + bf * kKeysT,
+                           qd + (((kk / 4) * L::QCH + (kk % 4) * 32) >> 4),
+                           kd + (((kk / 4) * L::KCH + (kk % 4) * 32) >> 4), a.idesc_s, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < DV / 16; ++kk)
+                    mma_ss(tmem + L::DP_COL + bf * kKeysT,
+                           od + (((kk / 4) * L::QCH + (kk % 4) * 32) >> 4),
+                           vd + (((kk / 4) * L::KCH + (kk % 4) * 32) >> 4), a.idesc_s, kk > 0);
+                mma_commit(bar(T_S_FULL + bf));
+            }
+            __syncwarp();
         }
         if (!ok && lane == 0) raise_abort_t(abort_flag, p.status);
         // every MMA issued completes before TMEM is released
+        if (lane == 0) {
+            mma_commit(bar(T_TEARDOWN));
+            mbar_wait(bar(T_TEARDOWN), 0, abort_flag, kWaitNsT);
+        }
+        __syncwarp();
+    } else if (warp == kDqWarpT) {
+        // ----------------------------------------------------- dQ MMA issuer
+        bool ok = true;
+        const uint32_t dq_tm = tmem + L::DQ_COL;
+        for (int jj = 0; jj < ntiles && ok; ++jj) {
+            // dQ += dS K for tile jj, once its dS is in TMEM
+            const int bf = jj & 1, s = jj % kStagesT;
+            if (!warp_wait_t(bar(T_DS_READY + bf), (uint32_t)(jj >> 1) & 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            // Keys past the last one in use (last tile only) are left out 16
+            // at a time; the K rows of the last 16-key step past it may hold
+            // anything (NaN included), so they are zeroed: 0 * K must stay 0.
+            // S of this tile has completed (the elementwise warps read it).
+            const int nvalid = min(kKeysT, khi - (tfirst + jj * kKeysT));
+            const int ksteps = (nvalid + 15) / 16;
+            const int nzero = ksteps * 16 - nvalid;
+            if (nzero > 0) {
+                uint8_t *kt = gbase + (stage(s) - base) + nvalid * 128;
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    for (int i = lane; i < nzero * 8; i += 32)
+                        *reinterpret_cast<uint4 *>(kt + c * L::KCH + i * 16) =
+                            make_uint4(0, 0, 0, 0);
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            if (lane == 0) {
+                // K as the MN-major B operand: 64-column chunks L::KCH apart
+                const uint64_t kmn = sw128_desc(stage(s), L::KCH, 1024);
+#pragma unroll
+                for (int kk = 0; kk < kKeysT / 16; ++kk)
+                    if (kk < ksteps)
+                        mma_ts(dq_tm, tmem + L::S_COL + bf * kKeysT + kk * 8,
+                               kmn + ((kk * 2048) >> 4), a.idesc_dq, (jj > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(kv_empty(s));
+                mma_commit(bar(T_S_EMPTY + bf));
+                if (jj == ntiles - 1) mma_commit(bar(T_DQ_FULL));
+            }
+            __syncwarp();
+        }
+        if (!ok && lane == 0) raise_abort_t(abort_flag, p.status);
         if (lane == 0) {
             mma_commit(bar(T_TEARDOWN));
             mbar_wait(bar(T_TEARDOWN), 0, abort_flag, kWaitNsT);
@@ -850,7 +870,7 @@ int launch_t(const BwdParams &bp, bool bf16, cudaStream_t stream) {
         set_error("tcgen05 dQ: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         return 3;
     }
-    kern<<<(unsigned)grid, kThreadsT, L::SMEM, stream>>>(a, tq, to, tk, tv);
+    kern<<<(unsigned)grid, kThreadsQ, L::SMEM, stream>>>(a, tq, to, tk, tv);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("tcgen05 dQ launch: %s", cudaGetErrorString(e));
