@@ -16,8 +16,9 @@
 //   warp 4 (one thread): TMA loads of the Q and dO tiles and a ring of K/V
 //     tiles;
 //   warp 5 (one thread): S_b = Q K^T and dP_b = dO V^T into TMEM buffer b =
-//     tile & 1, then, once the elementwise warps have turned the previous
-//     tile into dS, dQ += dS K with dS read from TMEM (it overwrites S_b);
+//     tile & 1, once the dQ products of tile - 2 have released S_b;
+//   warp 6 (one thread): once the elementwise warps have turned a tile into
+//     dS, dQ += dS K with dS read from TMEM (it overwrites S_b);
 //   warps 0-3: per tile, P and dS from S_b and dP_b in registers, dS stored
 //     to TMEM as 16-bit pairs; at the end dQ out of TMEM, scaled, to memory.
 // The double buffer lets the tensor core compute tile j+1's S and dP while
