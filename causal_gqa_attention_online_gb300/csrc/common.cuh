@@ -72,7 +72,7 @@ struct SeqInfo {
     int Qb, Kb;
 };
 
-__device__ __forceinline__ int clamp_len(int n, int cap) {
+__host__ __device__ __forceinline__ int clamp_len(int n, int cap) {
     return n < 0 ? 0 : (n > cap ? cap : n);
 }
 
@@ -109,8 +109,8 @@ __device__ __forceinline__ long long kv_row(const AttnParams &p, const SeqInfo &
 // keep the keys up to the row's diagonal -- aligned to the end of the keys
 // (bottom-right, the default) or to their start (top-left) -- and a window
 // keeps the last `window` of those; no mask keeps every key of the sequence.
-__device__ __forceinline__ void legal_range(int qi, int Qb, int Kb, int window, int mask, int &lo,
-                                            int &hi) {
+__host__ __device__ __forceinline__ void legal_range(int qi, int Qb, int Kb, int window,
+                                                     int mask, int &lo, int &hi) {
     if (mask == 2) {
         lo = 0;
         hi = Kb;
@@ -125,8 +125,8 @@ __device__ __forceinline__ void legal_range(int qi, int Qb, int Kb, int window, 
 // Query positions [qf, qe) of a sequence that have a legal key in [k0, k1)
 // (k0 < k1 <= Kb); empty when qe <= qf.  The causal masks' ranges
 // [lo(qi), hi(qi)) both grow with qi, so the set is an interval.
-__device__ __forceinline__ void rows_for_keys(int k0, int k1, int Qb, int Kb, int window,
-                                              int mask, int &qf, int &qe) {
+__host__ __device__ __forceinline__ void rows_for_keys(int k0, int k1, int Qb, int Kb,
+                                                       int window, int mask, int &qf, int &qe) {
     if (mask == 2) {
         qf = 0;
         qe = Qb;
@@ -148,7 +148,7 @@ struct SplitSpan {
     bool direct;
 };
 
-__device__ __forceinline__ SplitSpan split_span(int lo, int hi, int len) {
+__host__ __device__ __forceinline__ SplitSpan split_span(int lo, int hi, int len) {
     SplitSpan s;
     if (hi <= lo) {
         s.first = s.last = 0;
