@@ -54,6 +54,21 @@ DECODE_NAME = ("bf16 batched decode B=64 Hq=32 Hkv=8 Q=1 D=Dv=128, key lengths U
 FLUSH_BYTES = 512 << 20
 
 
+def prefill_flop() -> int:
+    P = PREFILL
+    return P["B"] * P["Hq"] * legal_pairs(P["Q"], P["K"]) * (2 * P["D"] + 2 * P["Dv"])
+
+
+def prefill_config(world: int) -> dict:
+    """The headline workload's config object (the same for both arms)."""
+    P = PREFILL
+    return {"workload": PREFILL_NAME, "B": P["B"], "Hq": P["Hq"], "Hkv": P["Hkv"],
+            "seq_len": P["Q"], "D": P["D"], "Dv": P["Dv"], "global_batch": P["B"] * world,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "512 MiB buffer written before every timed step",
+            "flop_per_step": prefill_flop()}
+
+
 def legal_pairs(Qb: int, Kb: int, window: int = 0) -> int:
     """Legal (query, key) pairs of one sequence and head (closed form)."""
     total = 0
@@ -302,7 +317,9 @@ def measure_decode(args, world, rank, dev, stream, flush, attn, synth):
     del kpool, vpool
     return dict(kv_bytes=kv_bytes, ms=ms, launches=launches, clocks=clk.summary(),
                 e2e_ms=e2e_ms, h2d=moved[0] + dsk.numel() * 4, d2h=moved[1],
-                paged_ms=paged_ms, page=page)
+                paged_ms=paged_ms, page=page, inp=din,
+                flop=int(din.seqlens_k.astype(np.int64).sum()) * Dd["Hq"] * 2 * (
+                    Dd["D"] + Dd["Dv"]))
 
 
 def measure_backward(args, world, rank, dev, stream, flush, attn, synth, pin):
@@ -411,18 +428,14 @@ def run_gpu(args, world, rank, local):
               "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
               "data": "synthetic: N(0,1) seeded (PCG64), bf16 round-to-nearest"}
     pin = None
+    dec_in = None
     if args.only in ("all", "prefill"):
         r = measure_prefill(args, world, rank, dev, stream, flush, attn, synth)
         pin = r["pin"]
         tf = r["flop"] / (r["ms"] * 1e-3) / 1e12
         result.update({
             "value": round(world * tf, 3), "unit": "TFLOP/s", "ms_per_step": round(r["ms"], 5),
-            "config": {"workload": PREFILL_NAME, "B": P["B"], "Hq": P["Hq"], "Hkv": P["Hkv"],
-                       "seq_len": P["Q"], "D": P["D"], "Dv": P["Dv"],
-                       "global_batch": P["B"] * world,
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": "512 MiB buffer written before every timed step",
-                       "flop_per_step": r["flop"]},
+            "config": prefill_config(world),
             "roofline": {"bound": "tensor", "achieved": round(tf, 3), "peak": tf_peak,
                          "unit": "TFLOP/s", "frac": round(tf / tf_peak, 4),
                          "traffic": traffic.get("prefill"),
@@ -457,14 +470,26 @@ def run_gpu(args, world, rank, local):
     small = None
     if args.only in ("all", "configs"):
         small = measure_small_configs(args, world, rank, dev, stream, flush, attn, synth)
-        result["configs"] = [
-            {"workload": name, "ms_per_step": round(ms, 5), "us_per_step": round(ms * 1e3, 2),
-             "TFLOP/s": round(world * flop / (ms * 1e-3) / 1e12, 4),
-             "KV GB/s": round(world * kv / (ms * 1e-3) / 1e9, 2), "flop_per_step": flop,
-             "kv_bytes_per_step": kv,
-             "timing": ("median of 20 steps, L2 flushed before each; CUDA events around one "
-                        "call, so the binding's host time (~10 us) is included")}
-            for name, _, flop, kv, ms in small]
+        result["configs"] = []
+        for name, inp, flop, kv, ms in small:
+            entry = {"workload": name, "ms_per_step": round(ms, 5),
+                     "us_per_step": round(ms * 1e3, 2),
+                     "TFLOP/s": round(world * flop / (ms * 1e-3) / 1e12, 4),
+                     "KV GB/s": round(world * kv / (ms * 1e-3) / 1e9, 2), "flop_per_step": flop,
+                     "kv_bytes_per_step": kv,
+                     "timing": ("median of 20 steps, L2 flushed before each; CUDA events on "
+                                "the launching stream around one call")}
+            if inp.dtype != "f32":
+                tfv = flop / (ms * 1e-3) / 1e12
+                entry["kernel"] = "prefill_tc_kernel (tcgen05, packed layout)"
+                entry["roofline"] = {
+                    "bound": "tensor", "achieved": round(tfv, 3), "peak": tf_peak,
+                    "unit": "TFLOP/s", "frac": round(tfv / tf_peak, 4),
+                    "traffic": traffic.get("varlen"),
+                    "peak_source": f"{peak_src} bf16 dense (cuBLAS burst)"}
+            else:
+                entry["bound"] = "latency (a few MFLOP: launch and one wave of small blocks)"
+            result["configs"].append(entry)
         if args.only == "configs":
             c0 = result["configs"][0]
             result.update({"value": c0["TFLOP/s"], "unit": "TFLOP/s",
@@ -493,6 +518,7 @@ def run_gpu(args, world, rank, local):
                            "roofline": wide[0]["roofline"]})
     if args.only in ("all", "decode"):
         d = measure_decode(args, world, rank, dev, stream, flush, attn, synth)
+        dec_in = (DECODE_NAME, d["inp"], d["flop"], d["kv_bytes"])
         gbs = d["kv_bytes"] / (d["ms"] * 1e-3) / 1e9
         dec = {
             "workload": DECODE_NAME, "metric": "KV GB/s", "value": round(world * gbs, 2),
@@ -516,11 +542,12 @@ def run_gpu(args, world, rank, local):
                            "clocks": dec["clocks"], "paged": dec["paged"]})
         else:
             result["decode"] = dec
-    return result, (pin, small)
+    return result, (pin, small, dec_in)
 
 
 KERNEL_SOURCES = {
     "prefill": "causal_gqa_attention_online_gb300/csrc/kernel_prefill_tc.cu",
+    "varlen": "causal_gqa_attention_online_gb300/csrc/kernel_prefill_tc.cu",
     "decode": "causal_gqa_attention_online_gb300/csrc/kernel_decode.cu",
     "backward": ("causal_gqa_attention_online_gb300/csrc/kernel_bwd.cu",
                  "causal_gqa_attention_online_gb300/csrc/kernel_bwd_tc.cu"),
@@ -556,15 +583,19 @@ def load_traffic():
     return out
 
 
-def oracle_sample_rate(inp, rows_budget_s=12.0, nthreads=0, seed=0):
-    """Time the CPU oracle on random query rows of the prefill workload until
-    about ``rows_budget_s`` seconds of work; returns (TFLOP/s, rows, secs, threads)."""
-    import oracle
+def oracle_inputs(inp):
+    """The prefill workload's inputs as the exact float32 values the oracle takes."""
     from causal_gqa_attention_online_gb300 import synth
+    return synth.exact_f32(inp.q), synth.exact_f32(inp.k), synth.exact_f32(inp.v)
 
-    q32 = synth.exact_f32(inp.q)
-    k32 = synth.exact_f32(inp.k)
-    v32 = synth.exact_f32(inp.v)
+
+def oracle_sample_rate(qkv, rows_budget_s=12.0, nthreads=0, seed=0):
+    """Time the CPU oracle on random query rows of the prefill workload (its
+    inputs ``qkv`` from oracle_inputs) until about ``rows_budget_s`` seconds of
+    work; returns (TFLOP/s, rows, secs, threads)."""
+    import oracle
+
+    q32, k32, v32 = qkv
     g = np.random.default_rng(seed)
     P = PREFILL
     total_flop, total_s, nrows = 0, 0.0, 0
@@ -583,25 +614,38 @@ def oracle_sample_rate(inp, rows_budget_s=12.0, nthreads=0, seed=0):
     return total_flop / total_s / 1e12, nrows, total_s, threads
 
 
-def oracle_small_configs(small):
-    """The oracle on the two fp32 workloads in full: median wall time of 5
-    runs on one thread and on every host core."""
+def oracle_small_configs(workloads):
+    """The oracle in full on the other named workloads (the two fp32 ones, the
+    bf16 varlen chunked prefill and the bf16 batched decode): median wall time
+    of a few runs on every host core, and on one thread for the fp32 ones;
+    each with the throughput in the workload's own unit."""
     import oracle
     cores = oracle.max_threads()  # before any call sets a thread count
     out = []
-    for name, inp, flop, kv, _ in small:
+    for name, inp, flop, kv in workloads:
         q32, k32, v32 = (synth_exact(t) for t in (inp.q, inp.k, inp.v))
-        row = {"workload": name}
-        for label, nt in (("all_cores", cores), ("1_thread", 1)):
+        row = {"workload": name, "cores": cores}
+        runs = (("all_cores", cores), ("1_thread", 1)) if inp.dtype == "f32" else (
+            ("all_cores", cores),)
+        for label, nt in runs:
             ts = []
-            for _ in range(5):
+            for _ in range(5 if inp.dtype == "f32" else 3):
                 t0 = time.perf_counter()
-                oracle.attn_padded(q32, k32, v32, B=inp.B, Hq=inp.Hq, Hkv=inp.Hkv, Q=inp.Q,
-                                   K=inp.K, D=inp.D, Dv=inp.Dv, window=inp.window,
-                                   scale=inp.scale, nthreads=nt)
+                if inp.layout == "padded":
+                    oracle.attn_padded(q32, k32, v32, B=inp.B, Hq=inp.Hq, Hkv=inp.Hkv, Q=inp.Q,
+                                       K=inp.K, D=inp.D, Dv=inp.Dv, seqlens_q=inp.seqlens_q,
+                                       seqlens_k=inp.seqlens_k, window=inp.window,
+                                       scale=inp.scale, nthreads=nt)
+                else:
+                    oracle.attn_packed(q32, k32, v32, B=inp.B, Hq=inp.Hq, Hkv=inp.Hkv, D=inp.D,
+                                       Dv=inp.Dv, cu_seqlens_q=inp.cu_seqlens_q,
+                                       cu_seqlens_k=inp.cu_seqlens_k, window=inp.window,
+                                       scale=inp.scale, nthreads=nt)
                 ts.append(time.perf_counter() - t0)
-            row[f"us_{label}"] = round(statistics.median(ts) * 1e6, 1)
-        row["cores"] = cores
+            sec = statistics.median(ts)
+            row[f"us_{label}"] = round(sec * 1e6, 1)
+            row[f"TFLOP/s_{label}"] = round(flop / sec / 1e12, 5)
+            row[f"KV GB/s_{label}"] = round(kv / sec / 1e9, 3)
         out.append(row)
     return out
 
@@ -611,27 +655,37 @@ def synth_exact(t):
 
 
 def run_reference(args, world, rank):
+    """The reference arm: the fp64 CPU oracle on every host core, on the
+    headline workload's inputs.  Each step is a bounded sample of the
+    workload (random (b, q, h) output rows, about ``ref_seconds / (steps +
+    warmup)`` seconds of oracle work) whose wall time is measured: ms_per_step
+    is that measured time, value the sampled rows' legal-pair FLOP over it."""
     from causal_gqa_attention_online_gb300 import synth
     if rank != 0:
         return None
-    inp = synth.prefill_bf16_b4_h32x8_s4096_d128(seed=1234)
-    P = PREFILL
+    qkv = oracle_inputs(synth.prefill_bf16_b4_h32x8_s4096_d128(seed=1234))
     per_step_s = max(0.05, args.ref_seconds / max(1, args.steps + args.warmup))
-    rates = []
+    step_s, step_flop, step_rows = [], [], []
+    threads = None
     for i in range(args.warmup + args.steps):
-        r, nrows, secs, threads = oracle_sample_rate(inp, per_step_s, seed=i)
+        t0 = time.perf_counter()
+        r, nrows, secs, threads = oracle_sample_rate(qkv, per_step_s, seed=i)
+        wall = time.perf_counter() - t0
         if i >= args.warmup:
-            rates.append(r)
-    value = statistics.mean(rates)
-    flop = P["B"] * P["Hq"] * legal_pairs(P["Q"], P["K"]) * (2 * P["D"] + 2 * P["Dv"])
-    sample = (f"random (b, q, h) rows of the prefill workload, batches of 2048 rows, "
-              f"~{per_step_s:.1f} s of oracle work per step")
+            step_s.append(wall)
+            step_flop.append(r * 1e12 * secs)
+            step_rows.append(nrows)
+    value = sum(step_flop) / sum(step_s) / 1e12
+    ms = sum(step_s) / len(step_s) * 1e3
+    sample = (f"{int(statistics.mean(step_rows))} random (b, q, h) output rows of the prefill "
+              f"workload per step (batches of 2048 rows, ~{per_step_s:.1f} s of oracle work); "
+              f"value = their legal-pair FLOP / measured wall time")
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": flop / (value * 1e12) * 1e3, "higher_is_better": True,
+        "ms_per_step": round(ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": PREFILL_NAME},
+        "config": prefill_config(world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -660,15 +714,18 @@ def main():
         if res is not None:
             print(json.dumps(res))
         return
-    res, (pin, small) = run_gpu(args, world, rank, local)
+    res, (pin, small, dec_in) = run_gpu(args, world, rank, local)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline and pin is not None:
-            r, nrows, secs, threads = oracle_sample_rate(pin, 12.0)
+            r, nrows, secs, threads = oracle_sample_rate(oracle_inputs(pin), 12.0)
             res["cpu_baseline"] = {
                 "value": r, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                 "sample": f"{nrows} random (b, q, h) rows of the prefill workload, {secs:.1f} s"}
-            if small:
-                res["cpu_baseline"]["configs"] = oracle_small_configs(small[:2])
+            more = [(name, inp, flop, kv) for name, inp, flop, kv, _ in (small or [])]
+            if dec_in is not None:
+                more.append(dec_in)
+            if more:
+                res["cpu_baseline"]["configs"] = oracle_small_configs(more)
         print(json.dumps(res))
     if world > 1:
         import torch.distributed as dist

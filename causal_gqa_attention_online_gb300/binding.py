@@ -27,7 +27,7 @@ _DTYPE_CODE = {torch.float32: ATTN_F32, torch.float16: ATTN_F16, torch.bfloat16:
 EXPORTED = ("attn_fwd", "attn_fwd_varlen", "attn_fwd_algo", "attn_fwd_varlen_algo",
             "attn_fwd_ex", "attn_fwd_varlen_ex", "attn_fwd_paged", "attn_bwd", "attn_bwd_varlen",
             "attn_lse_combine", "attn_fwd_decode_noalloc", "attn_fwd_staged", "attn_last_error",
-            "attn_device_status", "attn_kernel_launches", "attn_version")
+            "attn_device_status", "attn_set_wait_limit", "attn_kernel_launches", "attn_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -87,6 +87,8 @@ def load_library(path: str | None = None):
         lib.attn_last_error.restype = ctypes.c_char_p
         lib.attn_device_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
         lib.attn_device_status.restype = ip
+        lib.attn_set_wait_limit.argtypes = [ctypes.c_ulonglong]
+        lib.attn_set_wait_limit.restype = ctypes.c_ulonglong
         lib.attn_kernel_launches.argtypes = []
         lib.attn_kernel_launches.restype = ctypes.c_ulonglong
         lib.attn_version.argtypes = []
@@ -109,6 +111,13 @@ def device_status() -> tuple[int, int]:
     d = ctypes.c_int(0)
     st = load_library().attn_device_status(ctypes.byref(d))
     return st, d.value
+
+
+def set_wait_limit(ns: int) -> int:
+    """Limit (ns) of the tcgen05 kernels' mbarrier waits for later launches;
+    0 restores the default (2 s).  Returns the previous limit.  A diagnostic
+    aid: a short limit makes a launch time out, reported by device_status()."""
+    return int(load_library().attn_set_wait_limit(int(ns)))
 
 
 def _ptr(t):

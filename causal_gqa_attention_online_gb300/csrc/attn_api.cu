@@ -25,11 +25,17 @@ int g_sm_count[kMaxDevices] = {};
 }  // namespace
 
 std::atomic<unsigned long long> g_launches{0};
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+unsigned long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+
 // The device status word (one per device, in this module's device image).
 __device__ int g_device_status;
+
+void clear_error() { g_last_error[0] = '\0'; }
 
 void set_error(const char *fmt, ...) {
     va_list ap;
@@ -107,6 +113,8 @@ int pool_for(int dev, cudaMemPool_t *out) {
 
 bool ptr_aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+}  // namespace
+
 // Host-side validation shared by both layouts.
 int validate(const void *q, const void *k, const void *v, const void *o, const float *lse,
              int B, int Hq, int Hkv, int Q, int K, int D, int Dv, int dtype, int algo) {
@@ -147,6 +155,53 @@ int validate(const void *q, const void *k, const void *v, const void *o, const f
     return ATTN_OK;
 }
 
+int plan_splits(AttnParams &p, int chosen, int nsm) {
+    if (nsm < 1) {
+        set_error("the device reports no multiprocessors");
+        return ATTN_ERR_CUDA;
+    }
+    if (chosen == ATTN_ALGO_DECODE) {
+        p.split_len = decode_split_len(p, nsm);
+    } else {
+        p.split_len = p.K > 0 ? p.K : 1;
+        const long long units = (long long)p.B * p.Hkv * (((long long)p.Q * p.G + 31) / 32);
+        const int min_split = 128;
+        if (p.K > 2 * min_split && units < 2LL * nsm) {
+            const long long want = (2LL * nsm + units - 1) / units;
+            const long long most = (p.K + min_split - 1) / min_split;
+            const long long ns = want < most ? want : most;
+            if (ns > 1) {
+                long long len = (p.K + ns - 1) / ns;
+                p.split_len = (int)((len + 63) / 64 * 64);
+            }
+        }
+    }
+    if (p.split_len < 1) p.split_len = 1;
+    p.nsplit = p.K > 0 ? (int)(((long long)p.K + p.split_len - 1) / p.split_len) : 1;
+    return ATTN_OK;
+}
+
+unsigned long long split_workspace_bytes(const AttnParams &p) {
+    if (p.nsplit <= 1) return 0;
+    const unsigned long long rows = (unsigned long long)p.nsplit * p.B * p.Q * p.Hq;
+    return sizeof(float) * rows * (unsigned long long)(p.Dv + 1);
+}
+
+void set_split_workspace(AttnParams &p, void *ws) {
+    const long long rows = (long long)p.nsplit * p.B * p.Q * p.Hq;
+    p.part_o = static_cast<float *>(ws);
+    p.part_lse = p.part_o + rows * p.Dv;
+}
+
+int launch_split_kv(const AttnParams &p, int chosen, int dtype, cudaStream_t stream) {
+    int rc = chosen == ATTN_ALGO_DECODE ? launch_decode(p, dtype, stream)
+                                        : launch_generic(p, dtype, stream);
+    if (rc == 0 && p.nsplit > 1) rc = launch_combine_rows(p, dtype, stream);
+    return rc;
+}
+
+namespace {
+
 int run(AttnParams &p, int dtype, int algo, cudaStream_t stream) {
     int dev = 0;
     int rc = current_device(&dev);
@@ -184,29 +239,12 @@ int run(AttnParams &p, int dtype, int algo, cudaStream_t stream) {
     // Split the key axis when the (sequence, KV head, row-block) units alone
     // would leave SMs idle.  A row whose legal keys fall in one split is
     // written directly; the others are merged by the combine kernel.
-    if (chosen == ATTN_ALGO_DECODE) {
-        p.split_len = decode_split_len(p, nsm);
-    } else {
-        p.split_len = p.K > 0 ? p.K : 1;
-        const long long units = (long long)p.B * p.Hkv * (((long long)p.Q * p.G + 31) / 32);
-        const int min_split = 128;
-        if (p.K > 2 * min_split && units < 2LL * nsm) {
-            const long long want = (2LL * nsm + units - 1) / units;
-            const long long most = (p.K + min_split - 1) / min_split;
-            const long long ns = want < most ? want : most;
-            if (ns > 1) {
-                long long len = (p.K + ns - 1) / ns;
-                p.split_len = (int)((len + 63) / 64 * 64);
-            }
-        }
-    }
-    if (p.split_len < 1) p.split_len = 1;
-    p.nsplit = p.K > 0 ? (int)(((long long)p.K + p.split_len - 1) / p.split_len) : 1;
+    rc = plan_splits(p, chosen, nsm);
+    if (rc) return rc;
 
     void *ws = nullptr;
     if (p.nsplit > 1) {
-        const long long rows = (long long)p.nsplit * p.B * p.Q * p.Hq;
-        const size_t bytes = sizeof(float) * (size_t)rows * (size_t)(p.Dv + 1);
+        const size_t bytes = (size_t)split_workspace_bytes(p);
         cudaMemPool_t pool = nullptr;
         rc = pool_for(dev, &pool);
         if (rc) return rc;
@@ -215,12 +253,9 @@ int run(AttnParams &p, int dtype, int algo, cudaStream_t stream) {
             set_error("workspace cudaMallocFromPoolAsync(%zu): %s", bytes, cudaGetErrorString(e));
             return ATTN_ERR_CUDA;
         }
-        p.part_o = static_cast<float *>(ws);
-        p.part_lse = p.part_o + rows * p.Dv;
+        set_split_workspace(p, ws);
     }
-    rc = chosen == ATTN_ALGO_DECODE ? launch_decode(p, dtype, stream)
-                                    : launch_generic(p, dtype, stream);
-    if (rc == 0 && p.nsplit > 1) rc = launch_combine_rows(p, dtype, stream);
+    rc = launch_split_kv(p, chosen, dtype, stream);
     if (ws != nullptr) {
         const cudaError_t e = cudaFreeAsync(ws, stream);
         if (e != cudaSuccess && rc == 0) {
@@ -238,7 +273,7 @@ int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
                float scale, int mask, int dtype, int algo, cudaStream_t stream,
                const int32_t *block_table = nullptr, int page_size = 0, int num_pages = 0,
                int max_pages = 0) {
-    g_last_error[0] = '\0';
+    clear_error();
     int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Q, K, D, Dv, dtype, algo);
     if (rc) return rc;
     if (mask < ATTN_MASK_CAUSAL || mask > ATTN_MASK_NONE) {
@@ -285,6 +320,7 @@ int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
     p.scale_log2 = scale * kLog2e;
     p.nsplit = 1;
     p.split_len = K > 0 ? K : 1;
+    p.wait_ns = wait_limit_ns();
     return run(p, dtype, algo, stream);
 }
 
@@ -294,7 +330,7 @@ int bwd_common(const void *q, const void *k, const void *v, const void *o, const
                const int32_t *seqlens_q, const int32_t *seqlens_k, const int32_t *cu_q,
                const int32_t *cu_k, int window, float scale, int mask, int dtype, int algo,
                cudaStream_t stream) {
-    g_last_error[0] = '\0';
+    clear_error();
     int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Q, K, D, Dv, dtype, ATTN_ALGO_AUTO);
     if (rc) return rc;
     if (D > 256 || Dv > 256) {
@@ -354,6 +390,7 @@ int bwd_common(const void *q, const void *k, const void *v, const void *o, const
     p.scale = scale;
     p.scale_log2 = scale * kLog2e;
     p.nsplit = 1;
+    p.wait_ns = wait_limit_ns();
     bp.dout = dout;
     bp.dq = dq;
     bp.dk = dk;
@@ -429,7 +466,7 @@ int attn_fwd_paged(const void *q, const void *k_pages, const void *v_pages, void
                    int max_pages, int page_size, int num_pages, const int32_t *seqlens_q,
                    const int32_t *seqlens_k, int window, float scale, int mask, int dtype,
                    int algo, attn_stream_t stream) {
-    attn::g_last_error[0] = '\0';
+    attn::clear_error();
     if (page_size < 1 || page_size > (1 << 20) || (page_size & (page_size - 1)) != 0) {
         set_error("page_size must be a power of two in [1, 2^20] (got %d)", page_size);
         return ATTN_ERR_INVALID;
@@ -509,7 +546,7 @@ int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float 
 
 int attn_lse_combine(const float *o_parts, const float *lse_parts, void *o, float *lse,
                      int nsplit, long long rows, int Dv, int dtype, attn_stream_t stream) {
-    g_last_error[0] = '\0';
+    clear_error();
     if (nsplit < 1 || rows < 0 || Dv < 1 || Dv > 4096 || dtype < ATTN_F32 || dtype > ATTN_BF16) {
         attn::set_error("attn_lse_combine: bad size or dtype (nsplit=%d rows=%lld Dv=%d)",
                         nsplit, rows, Dv);
@@ -586,6 +623,10 @@ unsigned long long attn_kernel_launches(void) {
     return g_launches.load(std::memory_order_relaxed);
 }
 
-const char *attn_version(void) { return "0.1.0"; }
+unsigned long long attn_set_wait_limit(unsigned long long ns) {
+    return g_wait_ns.exchange(ns == 0 ? kDefaultWaitNs : ns, std::memory_order_relaxed);
+}
+
+const char *attn_version(void) { return "0.2.0"; }
 
 }  // extern "C"

@@ -39,18 +39,13 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 std::mutex g_noalloc_mutex;
 void *g_noalloc_ptr[kNoAllocMaxDevices] = {};
 
-// Device address of the scratch array on the current device (looked up once).
-int noalloc_scratch(void **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) {
-        set_error("attn_fwd_decode_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
-        return ATTN_ERR_CUDA;
-    }
+// Device address of the scratch array on `dev`, the current device (looked
+// up once per device).
+int noalloc_scratch(int dev, void **out) {
     std::lock_guard<std::mutex> lk(g_noalloc_mutex);
     if (g_noalloc_ptr[dev] == nullptr) {
         void *ptr = nullptr;
-        e = cudaGetSymbolAddress((void **)&ptr, g_noalloc_scratch);
+        const cudaError_t e = cudaGetSymbolAddress((void **)&ptr, g_noalloc_scratch);
         if (e != cudaSuccess || ptr == nullptr) {
             set_error("attn_fwd_decode_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
             return ATTN_ERR_CUDA;
@@ -70,27 +65,10 @@ extern "C" int attn_fwd_decode_noalloc(const void *q, const void *k, const void 
                                        const int32_t *seqlens_k, int window, float scale,
                                        int dtype, attn_stream_t stream) {
     using namespace attn;
-    if (B < 0 || Hq < 0 || Hkv < 0 || Q < 0 || K < 0) {
-        set_error("attn_fwd_decode_noalloc: negative size");
-        return ATTN_ERR_INVALID;
-    }
-    if (Hq > 0 && (Hkv == 0 || Hq % Hkv != 0)) {
-        set_error("attn_fwd_decode_noalloc: Hq (%d) must be a positive multiple of Hkv (%d)", Hq,
-                  Hkv);
-        return ATTN_ERR_INVALID;
-    }
+    clear_error();
+    int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Q, K, D, Dv, dtype, ATTN_ALGO_DECODE);
+    if (rc) return rc;
     if ((long long)B * Q * Hq == 0) return ATTN_OK;
-    if (q == nullptr || o == nullptr || (K > 0 && (k == nullptr || v == nullptr))) {
-        set_error("attn_fwd_decode_noalloc: null tensor pointer");
-        return ATTN_ERR_INVALID;
-    }
-    const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-                          reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o) |
-                          reinterpret_cast<uintptr_t>(lse);
-    if (mis & 15u) {
-        set_error("attn_fwd_decode_noalloc: tensor pointers must be 16-byte aligned");
-        return ATTN_ERR_INVALID;
-    }
     AttnParams p;
     memset(&p, 0, sizeof(p));
     p.q = q;
@@ -114,37 +92,35 @@ extern "C" int attn_fwd_decode_noalloc(const void *q, const void *k, const void 
     p.mask = 0;  // bottom-right causal, as attn_fwd
     p.scale = scale;
     p.scale_log2 = scale * kLog2e;
+    p.wait_ns = wait_limit_ns();
     if (!decode_supported(p, dtype)) {
         set_error("attn_fwd_decode_noalloc: the decode kernel takes bf16/fp16, D and Dv in "
                   "{64, 128} or both 256, and Q * Hq / Hkv <= 16");
         return ATTN_ERR_UNSUPPORTED;
     }
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        set_error("attn_fwd_decode_noalloc: cudaGetDevice failed");
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) {
+        set_error("attn_fwd_decode_noalloc: cudaGetDevice: %s (device %d)", cudaGetErrorString(e),
+                  dev);
         return ATTN_ERR_CUDA;
     }
-    // the same split of the key axis as attn_fwd, so both give the same result
-    p.split_len = decode_split_len(p, sm_count(dev));
-    if (p.split_len < 1) p.split_len = 1;
-    p.nsplit = K > 0 ? (int)(((long long)K + p.split_len - 1) / p.split_len) : 1;
-    if (p.nsplit > 1) {
-        const long long rows = (long long)p.nsplit * B * Q * Hq;
-        const unsigned long long need = 4ull * (unsigned long long)rows * (unsigned long long)(Dv + 1);
-        if (need > kNoAllocScratchBytes) {
-            set_error("attn_fwd_decode_noalloc: this problem needs %llu bytes of split-KV "
-                      "scratch; the fixed scratch array holds %llu bytes (use attn_fwd)",
-                      need, (unsigned long long)kNoAllocScratchBytes);
-            return ATTN_ERR_UNSUPPORTED;
-        }
-        void *scratch = nullptr;
-        const int rc = noalloc_scratch(&scratch);
-        if (rc) return rc;
-        p.part_o = static_cast<float *>(scratch);
-        p.part_lse = p.part_o + rows * Dv;
+    // the split of the key axis that attn_fwd plans (the same helper), so both
+    // entry points run the same launches
+    rc = plan_splits(p, ATTN_ALGO_DECODE, sm_count(dev));
+    if (rc) return rc;
+    const unsigned long long need = split_workspace_bytes(p);
+    if (need > kNoAllocScratchBytes) {
+        set_error("attn_fwd_decode_noalloc: this problem needs %llu bytes of split-KV "
+                  "scratch; the fixed scratch array holds %llu bytes (use attn_fwd)",
+                  need, (unsigned long long)kNoAllocScratchBytes);
+        return ATTN_ERR_UNSUPPORTED;
     }
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    int rc = launch_decode(p, dtype, s);
-    if (rc == 0 && p.nsplit > 1) rc = launch_combine_rows(p, dtype, s);
-    return rc;
+    if (need > 0) {
+        void *scratch = nullptr;
+        rc = noalloc_scratch(dev, &scratch);
+        if (rc) return rc;
+        set_split_workspace(p, scratch);
+    }
+    return launch_split_kv(p, ATTN_ALGO_DECODE, dtype, reinterpret_cast<cudaStream_t>(stream));
 }

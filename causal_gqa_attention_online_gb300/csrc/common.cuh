@@ -53,6 +53,7 @@ struct AttnParams {
     float *part_o;           // [nsplit][B][Q][Hq][Dv] fp32
     float *part_lse;         // [nsplit][B][Q][Hq] fp32, natural log
     int *status;             // device status word
+    unsigned long long wait_ns;  // limit of the tcgen05 kernels' mbarrier waits (ns)
 };
 
 // One backward problem: the forward problem (its o and lse hold the forward's

@@ -46,7 +46,6 @@ constexpr int kThreadsQ = 224;  // dQ: warps 0-3 elementwise, 4 TMA, 5 S / dP MM
 constexpr int kLoadWarpT = 4;
 constexpr int kMmaWarpT = 5;
 constexpr int kDqWarpT = 6;
-constexpr uint64_t kWaitNsT = 2000000000ull;  // 2 s
 constexpr int kStatusTimeoutBwdTc = 0x301;
 
 struct DqArgs {
@@ -103,8 +102,9 @@ template <> __device__ __forceinline__ uint32_t pack16<__half>(float lo, float h
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-__device__ __forceinline__ bool warp_wait_t(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
-    const bool ok = mbar_wait(bar, parity, abort_flag, kWaitNsT);
+__device__ __forceinline__ bool warp_wait_t(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                            uint64_t limit_ns) {
+    const bool ok = mbar_wait(bar, parity, abort_flag, limit_ns);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -122,6 +122,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
     extern __shared__ uint8_t smem_t[];
     const BwdParams &bp = a.bp;
     const AttnParams &p = bp.f;
+    const uint64_t wl = p.wait_ns;  // limit of every wait but the drains
 
     // work: (query tile rank, sequence, head); the last query tiles see the
     // most keys and start first
@@ -201,7 +202,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
             for (int j = 0; j < ntiles; ++j) {
                 const int s = j % kStagesT;
                 const uint32_t ph = (uint32_t)(j / kStagesT) & 1u;
-                if (!mbar_wait(kv_empty(s), ph ^ 1u, abort_flag, kWaitNsT)) {
+                if (!mbar_wait(kv_empty(s), ph ^ 1u, abort_flag, wl)) {
                     raise_abort_t(abort_flag, p.status);
                     ok = false;
                     break;
@@ -217,29 +218,29 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
                 armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
             }
             (void)ok;
-            // drain: every copy issued has landed before the CTA exits
-            mbar_wait(bar(T_QD_FULL), 0, abort_flag, kWaitNsT);
+            // drain: every copy issued has landed before the CTA exits (these
+            // waits ignore the abort flag: the copies always land)
+            mbar_wait_drain(bar(T_QD_FULL), 0);
             for (int s = 0; s < kStagesT; ++s)
-                if (armed & (1u << s))
-                    mbar_wait(kv_full(s), (armed_ph >> s) & 1u, abort_flag, kWaitNsT);
+                if (armed & (1u << s)) mbar_wait_drain(kv_full(s), (armed_ph >> s) & 1u);
         }
     } else if (warp == kMmaWarpT) {
         // ------------------------------------------------ S / dP MMA issuer
         // Two issuing warps: one thread issuing every MMA of a tile spends more
         // time issuing than the tensor core spends on them (the products of a
         // 64-key tile are small), so the dQ products have a warp of their own.
-        bool ok = ntiles == 0 || warp_wait_t(bar(T_QD_FULL), 0, abort_flag);
+        bool ok = ntiles == 0 || warp_wait_t(bar(T_QD_FULL), 0, abort_flag, wl);
         const uint64_t qd = sw128_desc(base + L::Q_OFF, 16, 1024);
         const uint64_t od = sw128_desc(base + L::DO_OFF, 16, 1024);
         for (int j = 0; j < ntiles && ok; ++j) {
             const int s = j % kStagesT, bf = j & 1;
-            if (!warp_wait_t(kv_full(s), (uint32_t)(j / kStagesT) & 1u, abort_flag)) {
+            if (!warp_wait_t(kv_full(s), (uint32_t)(j / kStagesT) & 1u, abort_flag, wl)) {
                 ok = false;
                 break;
             }
             // S_bf and dP_bf were last read for tile j - 2: dP by the elementwise
             // warps, S (as dS) by its dQ MMAs, which have completed
-            if (j >= 2 && !warp_wait_t(bar(T_S_EMPTY + bf), (uint32_t)((j - 2) >> 1) & 1u, abort_flag)) {
+            if (j >= 2 && !warp_wait_t(bar(T_S_EMPTY + bf), (uint32_t)((j - 2) >> 1) & 1u, abort_flag, wl)) {
                 ok = false;
                 break;
             }
@@ -265,7 +266,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         // every MMA issued completes before TMEM is released
         if (lane == 0) {
             mma_commit(bar(T_TEARDOWN));
-            mbar_wait(bar(T_TEARDOWN), 0, abort_flag, kWaitNsT);
+            mbar_wait_drain(bar(T_TEARDOWN), 0);  // ignores the abort flag
         }
         __syncwarp();
     } else if (warp == kDqWarpT) {
@@ -275,7 +276,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         for (int jj = 0; jj < ntiles && ok; ++jj) {
             // dQ += dS K for tile jj, once its dS is in TMEM
             const int bf = jj & 1, s = jj % kStagesT;
-            if (!warp_wait_t(bar(T_DS_READY + bf), (uint32_t)(jj >> 1) & 1u, abort_flag)) {
+            if (!warp_wait_t(bar(T_DS_READY + bf), (uint32_t)(jj >> 1) & 1u, abort_flag, wl)) {
                 ok = false;
                 break;
             }
@@ -314,7 +315,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         if (!ok && lane == 0) raise_abort_t(abort_flag, p.status);
         if (lane == 0) {
             mma_commit(bar(T_TEARDOWN));
-            mbar_wait(bar(T_TEARDOWN), 0, abort_flag, kWaitNsT);
+            mbar_wait_drain(bar(T_TEARDOWN), 0);  // ignores the abort flag
         }
         __syncwarp();
     } else {
@@ -334,7 +335,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         bool ok = true;
         for (int j = 0; j < ntiles && ok; ++j) {
             const int bf = j & 1;
-            if (!warp_wait_t(bar(T_S_FULL + bf), (uint32_t)(j >> 1) & 1u, abort_flag)) {
+            if (!warp_wait_t(bar(T_S_FULL + bf), (uint32_t)(j >> 1) & 1u, abort_flag, wl)) {
                 ok = false;
                 break;
             }
@@ -373,7 +374,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         // epilogue: dQ * scale to memory (zeros where no key contributed)
         const bool writes = qpos < qcap;
         if (ok && ntiles > 0) {
-            ok = warp_wait_t(bar(T_DQ_FULL), 0, abort_flag);
+            ok = warp_wait_t(bar(T_DQ_FULL), 0, abort_flag, wl);
             if (!ok && lane == 0) raise_abort_t(abort_flag, p.status);
             tc_fence_after();
         }
@@ -476,6 +477,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     extern __shared__ uint8_t smem_k[];
     const BwdParams &bp = a.bp;
     const AttnParams &p = bp.f;
+    const uint64_t wl = p.wait_ns;  // limit of every wait but the drains
     const int G = p.G;
     const int PP = kRowsK / G;  // query positions per row tile
 
@@ -550,7 +552,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         for (int t = 0; t < ntiles && ok; ++t) {
             const int s = t % kStagesK;
             const uint32_t ph = (uint32_t)(t / kStagesK) & 1u;
-            ok = warp_wait_t(row_empty(s), ph ^ 1u, abort_flag);
+            ok = warp_wait_t(row_empty(s), ph ^ 1u, abort_flag, wl);
             if (!ok) break;
             // per-row statistics of the tile, two rows a lane
             float *st = stats + s * 4 * kRowsK;
@@ -591,21 +593,21 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         }
         if (!ok && lane == 0) raise_abort_t(abort_flag, p.status);
         if (lane == 0) {
-            // drain: every copy issued has landed before the CTA exits
-            if (ntiles > 0) mbar_wait(bar(K_KV_FULL), 0, abort_flag, kWaitNsT);
+            // drain: every copy issued has landed before the CTA exits (these
+            // waits ignore the abort flag: the copies always land)
+            if (ntiles > 0) mbar_wait_drain(bar(K_KV_FULL), 0);
             for (int s = 0; s < kStagesK; ++s)
-                if (armed & (1u << s))
-                    mbar_wait(row_full(s), (armed_ph >> s) & 1u, abort_flag, kWaitNsT);
+                if (armed & (1u << s)) mbar_wait_drain(row_full(s), (armed_ph >> s) & 1u);
         }
     } else if (warp == kMmaWarpT) {
         // ------------------------------------------------------------ MMA issuer
-        bool ok = ntiles == 0 || warp_wait_t(bar(K_KV_FULL), 0, abort_flag);
+        bool ok = ntiles == 0 || warp_wait_t(bar(K_KV_FULL), 0, abort_flag, wl);
         const uint64_t kd = sw128_desc(base + L::K_OFF, 16, 1024);
         const uint64_t vd = sw128_desc(base + L::V_OFF, 16, 1024);
         for (int t = 0; t <= ntiles && ok; ++t) {
             if (t < ntiles) {
                 const int s = t % kStagesK, bf = t & 1;
-                if (!warp_wait_t(row_full(s), (uint32_t)(t / kStagesK) & 1u, abort_flag)) {
+                if (!warp_wait_t(row_full(s), (uint32_t)(t / kStagesK) & 1u, abort_flag, wl)) {
                     ok = false;
                     break;
                 }
@@ -631,7 +633,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
             }
             if (t >= 1) {
                 const int tt = t - 1, bf = tt & 1, s = tt % kStagesK;
-                if (!warp_wait_t(bar(K_DS_READY + bf), (uint32_t)(tt >> 1) & 1u, abort_flag)) {
+                if (!warp_wait_t(bar(K_DS_READY + bf), (uint32_t)(tt >> 1) & 1u, abort_flag, wl)) {
                     ok = false;
                     break;
                 }
@@ -672,7 +674,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         if (!ok && lane == 0) raise_abort_t(abort_flag, p.status);
         if (lane == 0) {
             mma_commit(bar(K_TEARDOWN));
-            mbar_wait(bar(K_TEARDOWN), 0, abort_flag, kWaitNsT);
+            mbar_wait_drain(bar(K_TEARDOWN), 0);  // ignores the abort flag
         }
         __syncwarp();
     } else {
@@ -683,14 +685,14 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         bool ok = true;
         for (int t = 0; t < ntiles && ok; ++t) {
             const int bf = t & 1, s = t % kStagesK;
-            if (!warp_wait_t(bar(K_S_FULL + bf), (uint32_t)(t >> 1) & 1u, abort_flag)) {
+            if (!warp_wait_t(bar(K_S_FULL + bf), (uint32_t)(t >> 1) & 1u, abort_flag, wl)) {
                 ok = false;
                 break;
             }
             // the tile's row statistics: published with its row_full phase (the
             // stage is not refilled before this tile's dV / dK MMAs, which wait
             // for this warpgroup)
-            if (!warp_wait_t(row_full(s), (uint32_t)(t / kStagesK) & 1u, abort_flag)) {
+            if (!warp_wait_t(row_full(s), (uint32_t)(t / kStagesK) & 1u, abort_flag, wl)) {
                 ok = false;
                 break;
             }
@@ -733,7 +735,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         if (!ok && lane == 0) raise_abort_t(abort_flag, p.status);
         // epilogue: dV and dK * scale to memory (zeros for keys no row sees)
         if (ok && ntiles > 0) {
-            ok = warp_wait_t(bar(K_ACC_FULL), 0, abort_flag);
+            ok = warp_wait_t(bar(K_ACC_FULL), 0, abort_flag, wl);
             if (!ok && lane == 0) raise_abort_t(abort_flag, p.status);
             tc_fence_after();
         }

@@ -355,6 +355,7 @@ bool decode_supported(const AttnParams &p, int dtype) {
 int decode_split_len(const AttnParams &p, int nsm) {
     // Small splits balance sequences of very different lengths; fewer, longer
     // splits when the (sequence, KV head) units already fill the SMs.
+    if (nsm < 1) nsm = 1;  // a failed device query must not divide by zero
     const long long units = (long long)p.B * p.Hkv;
     long long len = ((long long)p.K * units + 4LL * nsm - 1) / (4LL * nsm);
     len = (len + kTK - 1) / kTK * kTK;

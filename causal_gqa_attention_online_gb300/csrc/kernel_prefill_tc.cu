@@ -72,7 +72,6 @@ constexpr uint32_t kRegsEpi = 72;    // epilogue warpgroup
 static_assert(256 * kRegsSoftmax + 128 * (kRegsOther + kRegsEpi) <= kThreads * kRegsLaunch,
               "register split");
 static_assert(2 * kRegsSoftmax + kRegsOther + kRegsEpi <= 512, "register split per sub-partition");
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kChunkBytes = 128 * 128;       // one 128-row x 128-byte swizzled chunk
 constexpr int kPrefetchTiles = 4;                 // K/V tiles pulled into L2 ahead of use
 // Where the two softmax warpgroups take turns: 0 = never, 1 = the whole
@@ -236,8 +235,9 @@ __device__ __forceinline__ float ex2(float x) {
     return r;
 }
 
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
-    const bool ok = mbar_wait(bar, parity, abort_flag, kWaitLimitNs);
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          uint64_t limit_ns) {
+    const bool ok = mbar_wait(bar, parity, abort_flag, limit_ns);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -273,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int *unit_desc = reinterpret_cast<int *>(tmem_slot + 2);
 
     const AttnParams &p = a.p;
+    const uint64_t wl = p.wait_ns;  // limit of every wait but the drains
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -341,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     auto kv_coord = [&](int k0) -> int {
                         return PAGED ? (int)kv_row(p, x.si, x.b, k0) : krow + k0;
                     };
-                    if (!mbar_wait(bar(B_Q_EMPTY), q_ph ^ 1u, abort_flag, kWaitLimitNs)) {
+                    if (!mbar_wait(bar(B_Q_EMPTY), q_ph ^ 1u, abort_flag, wl)) {
                         raise_abort(abort_flag, p.status, kStatusTimeoutQ);
                         ok = false;
                         break;
@@ -386,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint32_t it = kv_it++;
                             const int s = (int)(it % NS);
                             const uint32_t ph = (it / NS) & 1u;
-                            if (!mbar_wait(kv_empty(s), ph ^ 1u, abort_flag, kWaitLimitNs)) {
+                            if (!mbar_wait(kv_empty(s), ph ^ 1u, abort_flag, wl)) {
                                 raise_abort(abort_flag, p.status, kStatusTimeoutKvEmpty);
                                 ok = false;
                                 break;
@@ -410,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // End marker for the MMA warps, once the last Q tile has been
                 // consumed (so no Q load is left in flight either).
                 if (ok) {
-                    if (mbar_wait(bar(B_Q_EMPTY), q_ph ^ 1u, abort_flag, kWaitLimitNs)) {
+                    if (mbar_wait(bar(B_Q_EMPTY), q_ph ^ 1u, abort_flag, wl)) {
                         unit_desc[q_ph * 4] = 0;
                         mbar_arrive(bar(B_Q_FULL));
                         last_q_parity = -1;
@@ -419,11 +420,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 // Drain: every copy this thread issued has landed before the CTA exits.
-                if (last_q_parity >= 0)
-                    mbar_wait(bar(B_Q_FULL), (uint32_t)last_q_parity, abort_flag, kWaitLimitNs);
+                // (these waits ignore the abort flag: the copies always land)
+                if (last_q_parity >= 0) mbar_wait_drain(bar(B_Q_FULL), (uint32_t)last_q_parity);
                 for (int s = 0; s < NS; ++s)
-                    if (armed & (1u << s))
-                        mbar_wait(kv_full(s), (armed_parity >> s) & 1u, abort_flag, kWaitLimitNs);
+                    if (armed & (1u << s)) mbar_wait_drain(kv_full(s), (armed_parity >> s) & 1u);
             }
         } else if (warp == kMmaWarp0 || warp == kMmaWarp1) {
             // -------------------------------------- MMA issuers, one per Q tile
@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // The units come from the TMA warp with each Q tile: no index
             // arithmetic on this warp's path from one unit to the next.
             while (ok) {
-                if (!warp_wait(bar(B_Q_FULL), q_ph, abort_flag)) {
+                if (!warp_wait(bar(B_Q_FULL), q_ph, abort_flag, wl)) {
                     ok = false;
                     break;
                 }
@@ -458,10 +458,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 // O_t (+)= P_t V_jj, then release V_jj
                 auto issue_pv = [&](int jj) -> bool {
-                    if (!warp_wait(bar(B_P_READY + t), p_ph, abort_flag)) return false;
+                    if (!warp_wait(bar(B_P_READY + t), p_ph, abort_flag, wl)) return false;
                     p_ph ^= 1u;
                     if (jj == 0) {  // the previous unit's epilogue has read O_t
-                        if (!warp_wait(bar(B_O_EMPTY + t), oe_ph ^ 1u, abort_flag)) return false;
+                        if (!warp_wait(bar(B_O_EMPTY + t), oe_ph ^ 1u, abort_flag, wl)) return false;
                         oe_ph ^= 1u;
                     }
                     const uint32_t it = kb + 2u * (uint32_t)jj + 1u;
@@ -474,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int ksteps = (nvalid + 15) / 16;
                     const int nzero = ksteps * 16 - nvalid;
                     if (t == 0 || nzero == 0) {
-                        if (!warp_wait(kv_full(vslot), (it / NS) & 1u, abort_flag)) return false;
+                        if (!warp_wait(kv_full(vslot), (it / NS) & 1u, abort_flag, wl)) return false;
                     }
                     if (nzero > 0) {
                         if (t == 0) {
@@ -490,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             __syncwarp();
                             if (lane == 0) mbar_arrive(v_tail(vslot));
                         } else {
-                            if (!warp_wait(v_tail(vslot), (vt_ph >> vslot) & 1u, abort_flag))
+                            if (!warp_wait(v_tail(vslot), (vt_ph >> vslot) & 1u, abort_flag, wl))
                                 return false;
                             vt_ph ^= 1u << vslot;
                         }
@@ -518,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint32_t it = kb + 2u * (uint32_t)j;
                     const int kslot = (int)(it % NS);
-                    if (!warp_wait(kv_full(kslot), (it / NS) & 1u, abort_flag)) {
+                    if (!warp_wait(kv_full(kslot), (it / NS) & 1u, abort_flag, wl)) {
                         ok = false;
                         break;
                     }
@@ -554,9 +554,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok && lane == 0) raise_abort(abort_flag, p.status, kStatusTimeoutMma);
             // all MMAs issued by this warp complete before TMEM is released
+            // (also after an abort: this wait ignores the abort flag)
             if (lane == 0) {
                 mma_commit(bar(B_TEARDOWN + t));
-                mbar_wait(bar(B_TEARDOWN + t), 0, abort_flag, kWaitLimitNs);
+                mbar_wait_drain(bar(B_TEARDOWN + t), 0);
             }
             __syncwarp();
         }
@@ -611,14 +612,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int tb = kTurnMode == 3 ? B_TURN : B_P_READY;
                     bool w = true;
                     if (t == 1)
-                        w = warp_wait(bar(tb + 0), ntile & 1u, abort_flag);
+                        w = warp_wait(bar(tb + 0), ntile & 1u, abort_flag, wl);
                     else if (ntile > 0)
-                        w = warp_wait(bar(tb + 1), (ntile - 1) & 1u, abort_flag);
+                        w = warp_wait(bar(tb + 1), (ntile - 1) & 1u, abort_flag, wl);
                     ++ntile;
                     return w;
                 };
                 if ((kTurnMode == 1 || kTurnMode == 3) && !take_turn()) return false;
-                if (!warp_wait(bar(B_S_FULL + t), s_ph, abort_flag)) return false;
+                if (!warp_wait(bar(B_S_FULL + t), s_ph, abort_flag, wl)) return false;
                 s_ph ^= 1u;
                 tc_fence_after();
                 if (!interior) {
@@ -770,8 +771,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++nunit;
             for (int t = 0; t < 2; ++t) {
                 const int sb = 2 * t + b;
-                if (!warp_wait(bar(B_O_FULL + t), (o_ph >> t) & 1u, abort_flag) ||
-                    !warp_wait(bar(B_STATS + sb), (st_ph >> sb) & 1u, abort_flag)) {
+                const bool got = warp_wait(bar(B_O_FULL + t), (o_ph >> t) & 1u, abort_flag, wl) &&
+                                 warp_wait(bar(B_STATS + sb), (st_ph >> sb) & 1u, abort_flag, wl);
+                // The four warps go on or give up together: a warp that went on
+                // alone would wait forever at the named barriers below.
+                if (!bar_red_and(2, 128, got)) {
                     ok = false;
                     break;
                 }

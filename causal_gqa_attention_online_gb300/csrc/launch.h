@@ -11,8 +11,25 @@
 namespace attn {
 
 void set_error(const char *fmt, ...);
+void clear_error();   // the calling thread's message becomes ""
 void count_launch();  // one successful kernel launch
-int sm_count(int device);
+int sm_count(int device);  // 0 if the device index or the query is bad
+unsigned long long wait_limit_ns();  // limit of the tcgen05 kernels' mbarrier waits
+
+// Host-side argument checks shared by the entry points (dtype, algo, sizes,
+// pointers, 16-byte alignment); 0 or an attn_status code with a message.
+int validate(const void *q, const void *k, const void *v, const void *o, const float *lse,
+             int B, int Hq, int Hkv, int Q, int K, int D, int Dv, int dtype, int algo);
+
+// Split-KV plan of a decode (chosen = ATTN_ALGO_DECODE) or CUDA-core problem:
+// sets p.split_len and p.nsplit.  The partials need split_workspace_bytes(p)
+// bytes (0 when nsplit == 1) at a 16-byte aligned address handed over with
+// set_split_workspace; launch_split_kv then runs the kernel and, for
+// nsplit > 1, the combine.
+int plan_splits(AttnParams &p, int chosen, int nsm);
+unsigned long long split_workspace_bytes(const AttnParams &p);
+void set_split_workspace(AttnParams &p, void *ws);
+int launch_split_kv(const AttnParams &p, int chosen, int dtype, cudaStream_t stream);
 
 // CUDA-core online softmax (any dtype; D, Dv <= 512).  Honours p.nsplit.
 int launch_generic(const AttnParams &p, int dtype, cudaStream_t stream);

@@ -34,13 +34,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// How long one try_wait may suspend the thread before it returns "not yet"
+// (it returns at once when the phase completes).  Without an explicit hint the
+// suspension is system-dependent and was measured to exceed a microsecond, so
+// a bound checked between calls would be coarse and unpredictable.
+constexpr uint32_t kSuspendHintNs = 1000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(done)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return done != 0;
 }
@@ -51,20 +57,48 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
-// A wait that gives up: after `limit_ns` of waiting, or as soon as another
-// thread of the CTA has raised *abort, it returns false (the caller then
-// records a status and unwinds).  A correct kernel never reaches the limit.
+// A wait that gives up: once `limit_ns` has passed since it started, or as
+// soon as another thread of the CTA has raised *abort, it returns false (the
+// caller then records a status and unwinds).  Both are checked after every
+// try_wait that returned "not yet", so the bound holds to within about
+// kSuspendHintNs.  A correct kernel never reaches the default limit.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           volatile int *abort_flag, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 1;; ++i) {
+    for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > limit_ns) return false;
-        }
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
+}
+
+// The wait of a CTA that is unwinding: for its own TMA copies to land and its
+// own issued MMAs to complete before shared memory and TMEM are given up.
+// Those operations always finish, so this ignores the abort flag and gives up
+// only after `limit_ns` (a fixed bound independent of the kernel's wait limit).
+constexpr uint64_t kDrainLimitNs = 2000000000ull;  // 2 s
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity,
+                                                uint64_t limit_ns = kDrainLimitNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// AND of `pred` over the n threads (a multiple of 32) of named barrier `id`;
+// every one of them gets the same result.
+__device__ __forceinline__ bool bar_red_and(uint32_t id, uint32_t n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+        " bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
 }
 
 // Warpgroup-wide register re-split (every warp of the warpgroup executes it).

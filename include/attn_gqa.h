@@ -320,6 +320,22 @@ ATTN_API const char *attn_last_error(void);
  * kernel-specific detail code. */
 ATTN_API int attn_device_status(int *detail);
 
+/*
+ * Sets the time limit of the mbarrier waits inside the tcgen05 kernels
+ * (prefill, backward) for launches made after the call, in nanoseconds, for
+ * every thread and device of the process; 0 restores the default of 2 s.
+ * Returns the previous limit.  A wait that runs out records ATTN_ERR_TIMEOUT
+ * and a detail code in the device status word (attn_device_status), and the
+ * launch unwinds: its blocks wait (up to 2 s, whatever this limit) for their
+ * own copies and tensor-core operations in flight, free their tensor memory
+ * and return, leaving the outputs incomplete and the context usable.  A
+ * diagnostic aid: a limit shorter than the kernel's run makes a correct launch
+ * time out on purpose, which is how the timeout path is tested.  The pages
+ * have no counterpart ("Attention execution mapping" records a submission
+ * stall, section 21.9, which is why the waits are bounded at all).
+ */
+ATTN_API unsigned long long attn_set_wait_limit(unsigned long long ns);
+
 /* Number of kernels this library has launched in the process so far (all
  * devices, all threads).  A measurement aid: the difference around a region
  * counts the library's launches inside it. */

@@ -113,3 +113,37 @@ def _call_bwd(lib, lse=1 << 24, dout=1 << 25, dq=1 << 26, D=64, Dv=64, algo=0, m
 def test_bwd_invalid_arguments_rejected_on_host(lib, kw, rc, needle):
     assert _call_bwd(lib, **kw) == rc
     assert needle in lib.attn_last_error().decode()
+
+
+def test_wait_limit_setter_round_trip(lib):
+    # host-side state only: the limit the next tcgen05 launches will carry
+    prev = lib.attn_set_wait_limit(12345)
+    assert lib.attn_set_wait_limit(0) == 12345
+    assert lib.attn_set_wait_limit(prev) == 2_000_000_000
+
+
+def _call_noalloc(lib, dtype=2, D=128, Dv=128, B=2, Hq=32, Hkv=8, Q=1, K=64, q=1 << 20):
+    vp = ctypes.c_void_p
+    return lib.attn_fwd_decode_noalloc(vp(q), vp(1 << 21), vp(1 << 22), vp(1 << 23), None, B, Hq,
+                                       Hkv, Q, K, D, Dv, None, None, 0, 0.088, dtype, None)
+
+
+@pytest.mark.parametrize("kw,rc,needle", [
+    (dict(B=-1), 1, "negative"),
+    (dict(Hq=30), 1, "multiple"),
+    (dict(D=0), 1, "head widths"),
+    (dict(q=(1 << 20) + 8), 1, "aligned"),
+    (dict(dtype=0), 2, "decode kernel takes"),      # fp32: not the decode kernel's
+    (dict(D=96, Dv=96), 2, "decode kernel takes"),
+    (dict(Q=3, Hq=64), 2, "decode kernel takes"),  # Q * G = 24 > 16 rows
+])
+def test_noalloc_rejects_on_host(lib, kw, rc, needle):
+    assert _call_noalloc(lib, **kw) == rc
+    assert needle in lib.attn_last_error().decode()
+
+
+def test_noalloc_clears_the_last_error(lib):
+    assert _call_noalloc(lib, dtype=0) == 2
+    assert lib.attn_last_error().decode() != ""
+    assert _call_noalloc(lib, B=0) == 0  # nothing to do: no CUDA call
+    assert lib.attn_last_error().decode() == ""

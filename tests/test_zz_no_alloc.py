@@ -4,11 +4,15 @@ owned by another runtime's allocator or held under a hard cap, or a
 latency-critical decode loop).  Its partial results live in the library's
 fixed device array instead of coming from an allocator.
 
-The test calls the entry point through the C ABI twice in a row, on two
-different problems, and checks each result against attn_fwd (the allocating
-entry point) within the tolerances of the other parity tests; the second call
-must not change the device's free memory.  It sits in a file of its own that
-pytest collects last and needs nothing from the other tests."""
+Calls go through the C ABI, several in a row on different problems, and each
+result is checked twice within the tolerances of the other parity tests:
+against the fp64 CPU oracle on the same inputs, and against attn_fwd (the
+allocating entry point).  Between two checked calls a larger problem fills the
+array with unrelated partials, so a result that read stale scratch would show.
+The checked calls must not change the device's free memory.  The cases cover
+bf16 and fp16, a sliding window, empty and full sequences, NaN in the padding,
+and a short problem that needs no scratch at all (one split).  The file is
+collected last and needs nothing from the other tests."""
 import ctypes
 
 import numpy as np
@@ -21,6 +25,8 @@ from tests import parity
 
 pytestmark = pytest.mark.gpu
 
+DT = {"bf16": attn.ATTN_BF16, "f16": attn.ATTN_F16}
+
 
 @pytest.fixture(scope="module")
 def lib():
@@ -28,55 +34,75 @@ def lib():
     return attn.load_library()
 
 
-def _problem(seed, B, K):
+def _problem(seed, B, K, dtype="bf16", window=0):
     g = np.random.default_rng(seed)
     sk = g.integers(0, K + 1, size=B).astype(np.int32)
     sk[0] = K
     sk[1] = 0
-    return synth.make_padded(B, 32, 8, 1, K, 128, 128, "bf16", seed=seed, seqlens_k=sk,
-                             pad_value=float("nan"))
+    return synth.make_padded(B, 32, 8, 1, K, 128, 128, dtype, seed=seed, seqlens_k=sk,
+                             window=window, pad_value=float("nan"))
 
 
-def _call_noalloc(lib, q, k, v, o, lse, sk, inp):
+class Staged:
+    """Device copies of a problem, NaN-filled outputs, and attn_fwd's result."""
+
+    def __init__(self, inp):
+        dev = torch.device("cuda")
+        self.inp = inp
+        self.q, self.k, self.v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+        self.sk = torch.from_numpy(inp.seqlens_k).to(dev)
+        self.ref_o, self.ref_lse = attn.attn_fwd(self.q, self.k, self.v, seqlens_k=self.sk,
+                                                 window=inp.window, scale=inp.scale)
+        self.o = torch.full_like(self.ref_o, float("nan"))
+        self.lse = torch.full_like(self.ref_lse, float("nan"))
+
+
+def _call_noalloc(lib, s: Staged):
     vp = ctypes.c_void_p
+    inp = s.inp
     rc = lib.attn_fwd_decode_noalloc(
-        vp(q.data_ptr()), vp(k.data_ptr()), vp(v.data_ptr()), vp(o.data_ptr()),
-        vp(lse.data_ptr()), inp.B, inp.Hq, inp.Hkv, inp.Q, inp.K, inp.D, inp.Dv, None,
-        vp(sk.data_ptr()), inp.window, inp.scale, attn.ATTN_BF16,
+        vp(s.q.data_ptr()), vp(s.k.data_ptr()), vp(s.v.data_ptr()), vp(s.o.data_ptr()),
+        vp(s.lse.data_ptr()), inp.B, inp.Hq, inp.Hkv, inp.Q, inp.K, inp.D, inp.Dv, None,
+        vp(s.sk.data_ptr()), inp.window, inp.scale, DT[inp.dtype],
         vp(torch.cuda.current_stream().cuda_stream))
     assert rc == 0, lib.attn_last_error().decode()
 
 
-def test_noalloc_matches_allocating_entry_point_twice(lib):
-    problems = [_problem(71, 16, 4096), _problem(72, 24, 3000)]
-    dev = torch.device("cuda")
-    staged, refs = [], []
-    for inp in problems:
-        q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
-        sk = torch.from_numpy(inp.seqlens_k).to(dev)
-        ro, rl = attn.attn_fwd(q, k, v, seqlens_k=sk, window=inp.window, scale=inp.scale)
-        o = torch.full_like(ro, float("nan"))
-        lse = torch.full_like(rl, float("nan"))
-        staged.append((q, k, v, o, lse, sk))
-        refs.append((ro, rl))
+def _check(s: Staged, what):
+    o = s.o.float().cpu().numpy()
+    lse = s.lse.cpu().numpy()
+    ro, rl = parity.run_oracle(s.inp)
+    parity.compare(s.inp.dtype, o, lse, ro, rl, f"{what}: noalloc vs oracle")
+    parity.compare(s.inp.dtype, o, lse, s.ref_o.float().cpu().numpy(),
+                   s.ref_lse.cpu().numpy().astype(np.float64), f"{what}: noalloc vs attn_fwd")
+
+
+def test_noalloc_matches_oracle_and_allocating_entry_point(lib):
+    first = Staged(_problem(71, 16, 4096))
+    filler = Staged(_problem(75, 64, 8192))        # more partials than the checked calls
+    second = Staged(_problem(72, 24, 3000, "f16", window=700))
+    single = Staged(_problem(73, 4, 100))          # one split: no scratch at all
     torch.cuda.synchronize()
 
-    # first call (looks up the array's address), then a second, different one
-    _call_noalloc(lib, *staged[0], problems[0])
+    # the first call on the device looks up the array's address
+    _call_noalloc(lib, first)
+    torch.cuda.synchronize()
+    _call_noalloc(lib, filler)                     # leaves unrelated partials behind
     torch.cuda.synchronize()
     free_before = torch.cuda.mem_get_info()[0]
-    _call_noalloc(lib, *staged[1], problems[1])
+    _call_noalloc(lib, second)
+    _call_noalloc(lib, single)
     torch.cuda.synchronize()
-    assert torch.cuda.mem_get_info()[0] == free_before, "the call changed free device memory"
+    assert torch.cuda.mem_get_info()[0] == free_before, "a call changed free device memory"
 
-    for inp, (q, k, v, o, lse, sk), (ro, rl) in zip(problems, staged, refs):
-        parity.compare("bf16", o.float().cpu().numpy(), lse.cpu().numpy(),
-                       ro.float().cpu().numpy(), rl.cpu().numpy().astype(np.float64),
-                       "noalloc vs attn_fwd")
+    _check(first, "bf16 B=16 K=4096")
+    _check(second, "fp16 B=24 K=3000 window 700")
+    _check(single, "bf16 B=4 K=100 (one split)")
+    _check(filler, "bf16 B=64 K=8192")
 
 
 def test_noalloc_rejects_problems_beyond_the_array(lib):
-    # 512 sequences x 32 heads x 16 splits of fp32 partials exceed 32 MiB
+    # 512 sequences x 32 heads x 8 splits of fp32 partials (68 MB) exceed 32 MiB
     B, K = 512, 8192
     dev = torch.device("cuda")
     q = torch.zeros((B, 1, 32, 128), dtype=torch.bfloat16, device=dev)
