@@ -233,7 +233,27 @@ int run(AttnParams &p, int dtype, int algo, cudaStream_t stream) {
         return ATTN_ERR_UNSUPPORTED;
     }
 
-    if (chosen == ATTN_ALGO_TCGEN05) return launch_prefill_tc(p, dtype, stream);
+    if (chosen == ATTN_ALGO_TCGEN05) {
+        const long long n = prefill_tc_order_len(p);
+        if (n == 0) return launch_prefill_tc(p, dtype, stream, nullptr);
+        void *ws = nullptr;
+        cudaMemPool_t pool = nullptr;
+        rc = pool_for(dev, &pool);
+        if (rc) return rc;
+        const size_t bytes = sizeof(int) * (size_t)n;
+        cudaError_t e = cudaMallocFromPoolAsync(&ws, bytes, pool, stream);
+        if (e != cudaSuccess) {
+            set_error("workspace cudaMallocFromPoolAsync(%zu): %s", bytes, cudaGetErrorString(e));
+            return ATTN_ERR_CUDA;
+        }
+        rc = launch_prefill_tc(p, dtype, stream, static_cast<int *>(ws));
+        e = cudaFreeAsync(ws, stream);
+        if (e != cudaSuccess && rc == 0) {
+            set_error("workspace cudaFreeAsync: %s", cudaGetErrorString(e));
+            rc = ATTN_ERR_CUDA;
+        }
+        return rc;
+    }
     if (chosen == ATTN_ALGO_MMA) return launch_fwd_mma(p, dtype, stream);
 
     // Split the key axis when the (sequence, KV head, row-block) units alone

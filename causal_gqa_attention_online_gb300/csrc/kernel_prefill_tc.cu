@@ -92,6 +92,10 @@ struct PrefillArgs {
     float c_scale;     // |scale| * log2(e)  (> 0)
     uint32_t idesc_s;  // S = Q K^T
     uint32_t idesc_o;  // O += P V
+    // Ragged problems: the unit indices ordered by their KV tile count, most
+    // first (written by unit_order_kernel); null: the natural order, which is
+    // longest-first already when every sequence has the same lengths.
+    const int *order;
 };
 
 template <int D, int DV> struct Layout {
@@ -150,7 +154,7 @@ template <bool PAGED>
 __device__ __forceinline__ UnitInfo unit_info(const PrefillArgs &a, long long u64) {
     const AttnParams &p = a.p;
     // 32-bit index arithmetic (the unit count is below 2^31)
-    const uint32_t u = (uint32_t)u64;
+    const uint32_t u = a.order != nullptr ? (uint32_t)__ldg(a.order + u64) : (uint32_t)u64;
     const uint32_t qi = u / a.per, rest = u - qi * a.per;
     const uint32_t b = rest / a.hs, r2 = rest - b * a.hs;
     const uint32_t kvh = r2 / (uint32_t)a.nsub, sub = r2 - kvh * (uint32_t)a.nsub;
@@ -311,6 +315,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // launched as a programmatic dependent of unit_order_kernel: the unit
+    // order is complete and visible once this returns
+    if (a.order != nullptr) asm volatile("griddepcontrol.wait;\n" ::: "memory");
     const uint32_t tmem = *tmem_slot;
     auto kv_full = [&](int s) { return bar(B_KV_FULL + s); };
     auto kv_empty = [&](int s) { return bar(B_KV_FULL + NS + s); };
@@ -431,6 +438,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // of its own tile; two issuing warps keep the tensor core fed while
             // either one waits.  P_t aliases S_t in TMEM, so S_t(j+1) is issued
             // after PV_t(j) by the same thread (tcgen05.mma executes in order).
+            // Only the wait for P_t(j) is left between the softmax and the two
+            // MMA batches: V_j, K_{j+1} and O_t's release are waited for while
+            // the softmax still runs (each mbarrier wait costs a few hundred
+            // cycles here even when its phase is long complete: 494 -> 421 us
+            // on the 4096^2 bf16 prefill).
             const int t = warp - kMmaWarp0;
             uint32_t kv_it = 0, q_ph = 0, p_ph = 0, oe_ph = 0;
             uint32_t vt_ph = 0;  // per ring slot: parity of its next v_tail phase (bit s)
@@ -456,72 +468,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (x.n_kv == 0) break;  // end marker
                 const uint32_t kb = kv_it;
 
-                // O_t (+)= P_t V_jj, then release V_jj
-                auto issue_pv = [&](int jj) -> bool {
-                    if (!warp_wait(bar(B_P_READY + t), p_ph, abort_flag, wl)) return false;
-                    p_ph ^= 1u;
-                    if (jj == 0) {  // the previous unit's epilogue has read O_t
-                        if (!warp_wait(bar(B_O_EMPTY + t), oe_ph ^ 1u, abort_flag, wl)) return false;
-                        oe_ph ^= 1u;
-                    }
-                    const uint32_t it = kb + 2u * (uint32_t)jj + 1u;
-                    const int vslot = (int)(it % NS);
-                    // Keys past the last one any row of the unit uses (only in the
-                    // last tile) are left out 16 at a time; the V rows of the
-                    // last 16-key step that lie past it may hold anything (NaN
-                    // included), so they are zeroed to keep 0 * V at 0.
-                    const int nvalid = min(kBN, x.hi_unit - (x.kv_start + jj * kBN));
-                    const int ksteps = (nvalid + 15) / 16;
-                    const int nzero = ksteps * 16 - nvalid;
-                    if (t == 0 || nzero == 0) {
-                        if (!warp_wait(kv_full(vslot), (it / NS) & 1u, abort_flag, wl)) return false;
-                    }
-                    if (nzero > 0) {
-                        if (t == 0) {
-                            // zero the rows (whole 128-byte rows: the swizzle does not
-                            // matter), then hand the tile to the other MMA warp
-                            uint8_t *vt = gbase + (stage(vslot) - base) + nvalid * 128;
-#pragma unroll
-                            for (int c = 0; c < DV / 64; ++c)
-                                for (int i = lane; i < nzero * 8; i += 32)
-                                    *reinterpret_cast<uint4 *>(vt + c * kChunkBytes + i * 16) =
-                                        make_uint4(0, 0, 0, 0);
-                            fence_proxy_async_smem();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(v_tail(vslot));
-                        } else {
-                            if (!warp_wait(v_tail(vslot), (vt_ph >> vslot) & 1u, abort_flag, wl))
-                                return false;
-                            vt_ph ^= 1u << vslot;
-                        }
-                    }
-                    tc_fence_after();
-                    if (lane == 0) {
-                        const uint64_t vd = sw128_desc(stage(vslot), kChunkBytes, 1024);
-                        // unrolled with a guard: a loop with a run-time trip count
-                        // issues markedly slower
-#pragma unroll
-                        for (int kk = 0; kk < kBN / 16; ++kk)
-                            if (kk < ksteps)
-                                mma_ts(o_tm, s_tm + kk * 8, vd + (kk * 2048 >> 4), a.idesc_o,
-                                       (jj > 0 || kk > 0) ? 1u : 0u);
-                        mma_commit(kv_empty(vslot));
-                    }
-                    __syncwarp();
-                    return true;
-                };
-
-                for (int j = 0; j < x.n_kv && ok; ++j) {
-                    if (j > 0 && !issue_pv(j - 1)) {
-                        ok = false;
-                        break;
-                    }
+                // S_t(j) = Q_t K_j^T into TMEM (K_j has landed), then release K_j
+                auto issue_s = [&](int j) {
                     const uint32_t it = kb + 2u * (uint32_t)j;
                     const int kslot = (int)(it % NS);
-                    if (!warp_wait(kv_full(kslot), (it / NS) & 1u, abort_flag, wl)) {
-                        ok = false;
-                        break;
-                    }
                     tc_fence_after();
                     if (lane == 0) {
                         // the start-address field is the low 14 bits (address >> 4)
@@ -542,12 +492,94 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (j == x.n_kv - 1) mma_commit(bar(B_Q_EMPTY));
                     }
                     __syncwarp();
-                }
-                if (!ok) break;
-                if (!issue_pv(x.n_kv - 1)) {
+                };
+                auto wait_k = [&](int j) -> bool {
+                    const uint32_t it = kb + 2u * (uint32_t)j;
+                    return warp_wait(kv_full((int)(it % NS)), (it / NS) & 1u, abort_flag, wl);
+                };
+
+                if (!wait_k(0)) {
                     ok = false;
                     break;
                 }
+                issue_s(0);
+                for (int jj = 0; jj < x.n_kv && ok; ++jj) {
+                    // Everything PV_t(jj) and S_t(jj + 1) need apart from P_t(jj) is
+                    // waited for first, while the softmax still runs: V_jj (zeroed
+                    // past the unit's last key), K_{jj+1}, and for the first tile the
+                    // previous unit's O_t read out by the epilogue.
+                    const uint32_t it = kb + 2u * (uint32_t)jj + 1u;
+                    const int vslot = (int)(it % NS);
+                    // Keys past the last one any row of the unit uses (only in the
+                    // last tile) are left out 16 at a time; the V rows of the
+                    // last 16-key step that lie past it may hold anything (NaN
+                    // included), so they are zeroed to keep 0 * V at 0.
+                    const int nvalid = min(kBN, x.hi_unit - (x.kv_start + jj * kBN));
+                    const int ksteps = (nvalid + 15) / 16;
+                    const int nzero = ksteps * 16 - nvalid;
+                    if (t == 0 || nzero == 0) {
+                        if (!warp_wait(kv_full(vslot), (it / NS) & 1u, abort_flag, wl)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (nzero > 0) {
+                        if (t == 0) {
+                            // zero the rows (whole 128-byte rows: the swizzle does not
+                            // matter), then hand the tile to the other MMA warp
+                            uint8_t *vt = gbase + (stage(vslot) - base) + nvalid * 128;
+#pragma unroll
+                            for (int c = 0; c < DV / 64; ++c)
+                                for (int i = lane; i < nzero * 8; i += 32)
+                                    *reinterpret_cast<uint4 *>(vt + c * kChunkBytes + i * 16) =
+                                        make_uint4(0, 0, 0, 0);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(v_tail(vslot));
+                        } else {
+                            if (!warp_wait(v_tail(vslot), (vt_ph >> vslot) & 1u, abort_flag, wl)) {
+                                ok = false;
+                                break;
+                            }
+                            vt_ph ^= 1u << vslot;
+                        }
+                    }
+                    const bool more = jj + 1 < x.n_kv;
+                    if (more && !wait_k(jj + 1)) {
+                        ok = false;
+                        break;
+                    }
+                    if (jj == 0) {  // the previous unit's epilogue has read O_t
+                        if (!warp_wait(bar(B_O_EMPTY + t), oe_ph ^ 1u, abort_flag, wl)) {
+                            ok = false;
+                            break;
+                        }
+                        oe_ph ^= 1u;
+                    }
+                    if (!warp_wait(bar(B_P_READY + t), p_ph, abort_flag, wl)) {
+                        ok = false;
+                        break;
+                    }
+                    p_ph ^= 1u;
+                    // O_t (+)= P_t V_jj, then release V_jj
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint64_t vd = sw128_desc(stage(vslot), kChunkBytes, 1024);
+                        // unrolled with a guard: a loop with a run-time trip count
+                        // issues markedly slower
+#pragma unroll
+                        for (int kk = 0; kk < kBN / 16; ++kk)
+                            if (kk < ksteps)
+                                mma_ts(o_tm, s_tm + kk * 8, vd + (kk * 2048 >> 4), a.idesc_o,
+                                       (jj > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(kv_empty(vslot));
+                    }
+                    __syncwarp();
+                    // S_t(jj + 1) overwrites P_t(jj): issued after PV_t(jj) by the same
+                    // thread (tcgen05.mma executes in order)
+                    if (more) issue_s(jj + 1);
+                }
+                if (!ok) break;
                 if (lane == 0) mma_commit(bar(B_O_FULL + t));
                 __syncwarp();
                 kv_it += 2u * (uint32_t)x.n_kv;
@@ -854,6 +886,70 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// Longest-first order of the units of a ragged problem (one block): a
+// counting sort of the unit indices by KV tile count, descending, so that the
+// persistent CTAs' alternating rounds deal the long units out first and the
+// short ones even out the ends (the natural order is longest-first only when
+// all sequences have the same lengths).  Units in the same bin keep no fixed
+// order; each unit still writes only its own rows, so the result does not
+// depend on it.
+constexpr int kOrderThreads = 1024;
+constexpr int kOrderBins = 2048;  // tile counts at or above the last bin share it
+
+template <bool PAGED>
+__global__ void __launch_bounds__(kOrderThreads) unit_order_kernel(const PrefillArgs a,
+                                                                   int *order) {
+    __shared__ int hist[kOrderBins];
+    __shared__ int warp_sum[kOrderThreads / 32];
+    // the prefill grid (a programmatic dependent launch) may be scheduled now:
+    // its blocks set up and then wait in griddepcontrol.wait for this order
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n = (int)a.nunits;
+    auto bin_of = [&](int u) {
+        const int c = unit_info<PAGED>(a, u).n_kv;  // a.order is null here
+        return kOrderBins - 1 - min(c, kOrderBins - 1);  // bin 0: the most tiles
+    };
+    for (int i = tid; i < kOrderBins; i += kOrderThreads) hist[i] = 0;
+    __syncthreads();
+    for (int u = tid; u < n; u += kOrderThreads) atomicAdd(&hist[bin_of(u)], 1);
+    __syncthreads();
+    // exclusive scan of the histogram: two bins a thread, then warps, then block
+    constexpr int PER = kOrderBins / kOrderThreads;
+    int v[PER], local = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        v[i] = hist[tid * PER + i];
+        local += v[i];
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_sum[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        warp_sum[lane] = w;  // inclusive
+    }
+    __syncthreads();
+    int run = incl - local + (warp > 0 ? warp_sum[warp - 1] : 0);
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        hist[tid * PER + i] = run;
+        run += v[i];
+    }
+    __syncthreads();
+    for (int u = tid; u < n; u += kOrderThreads) order[atomicAdd(&hist[bin_of(u)], 1)] = u;
+}
+
 // ------------------------------------------------------------------ host
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -899,10 +995,11 @@ int pack_factor(int G) {
 }
 
 template <typename T, int D, int DV>
-int launch_t(const AttnParams &p, bool bf16, cudaStream_t stream) {
+int launch_t(const AttnParams &p, bool bf16, cudaStream_t stream, int *order_ws) {
     using L = Layout<D, DV>;
     PrefillArgs a;
     a.p = p;
+    a.order = nullptr;
     a.Gp = pack_factor(p.G);
     a.QP = kBM / a.Gp;
     a.nsub = p.G / a.Gp;
@@ -941,9 +1038,20 @@ int launch_t(const AttnParams &p, bool bf16, cudaStream_t stream) {
         tk = tq;  // never read: every unit has no key
         tv = tq;
     }
+    cudaError_t e;
+    if (order_ws != nullptr) {
+        auto ok = paged ? unit_order_kernel<true> : unit_order_kernel<false>;
+        ok<<<1, kOrderThreads, 0, stream>>>(a, order_ws);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) {
+            set_error("unit order kernel launch: %s", cudaGetErrorString(e));
+            return 3;
+        }
+        count_launch();
+        a.order = order_ws;
+    }
     auto kern = paged ? prefill_tc_kernel<T, D, DV, true> : prefill_tc_kernel<T, D, DV, false>;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
     if (e != cudaSuccess) {
         set_error("prefill kernel: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         return 3;
@@ -952,8 +1060,18 @@ int launch_t(const AttnParams &p, bool bf16, cudaStream_t stream) {
     cudaGetDevice(&dev);
     const int nsm = sm_count(dev);
     const long long grid = a.nunits < nsm ? a.nunits : nsm;
-    kern<<<(unsigned)grid, kThreads, L::SMEM, stream>>>(a, tq, tk, tv, to);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.order != nullptr ? 1 : 0;  // after the order kernel: overlap its run
+    e = cudaLaunchKernelEx(&cfg, kern, a, tq, tk, tv, to);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("prefill kernel launch: %s", cudaGetErrorString(e));
         return 3;
@@ -963,13 +1081,18 @@ int launch_t(const AttnParams &p, bool bf16, cudaStream_t stream) {
 }
 
 template <typename T>
-int launch_dtype(const AttnParams &p, bool bf16, cudaStream_t stream) {
+int launch_dtype(const AttnParams &p, bool bf16, cudaStream_t stream, int *order_ws) {
     // tiles padded to 64 or 128 columns
     const bool d128 = p.D > 64, dv128 = p.Dv > 64;
-    if (d128 && dv128) return launch_t<T, 128, 128>(p, bf16, stream);
-    if (!d128 && !dv128) return launch_t<T, 64, 64>(p, bf16, stream);
-    if (d128) return launch_t<T, 128, 64>(p, bf16, stream);
-    return launch_t<T, 64, 128>(p, bf16, stream);
+    if (d128 && dv128) return launch_t<T, 128, 128>(p, bf16, stream, order_ws);
+    if (!d128 && !dv128) return launch_t<T, 64, 64>(p, bf16, stream, order_ws);
+    if (d128) return launch_t<T, 128, 64>(p, bf16, stream, order_ws);
+    return launch_t<T, 64, 128>(p, bf16, stream, order_ws);
+}
+
+long long unit_count(const AttnParams &p) {
+    const int gp = pack_factor(p.G), qp = kBM / gp;
+    return (long long)((p.Q + 2 * qp - 1) / (2 * qp)) * p.B * p.Hkv * (p.G / gp);
 }
 
 }  // namespace
@@ -984,9 +1107,15 @@ bool prefill_tc_supported(const AttnParams &p, int dtype) {
     // paged K/V: a 128-key tile must lie in one page
     if (p.block_table && p.page_size % kBN != 0) return false;
     // work units are indexed in 32 bits
-    const int gp = pack_factor(p.G), qp = kBM / gp;
-    const long long nunits = (long long)((p.Q + 2 * qp - 1) / (2 * qp)) * p.B * p.Hkv * (p.G / gp);
-    return rows < (1LL << 31) && keys < (1LL << 31) && nunits < (1LL << 31);
+    return rows < (1LL << 31) && keys < (1LL << 31) && unit_count(p) < (1LL << 31);
+}
+
+long long prefill_tc_order_len(const AttnParams &p) {
+    // ragged problems (packed, or padded with per-sequence lengths) of a size
+    // the one-block sort handles in a few microseconds
+    const bool ragged = p.cu_q != nullptr || p.seqlens_q != nullptr || p.seqlens_k != nullptr;
+    const long long n = unit_count(p);
+    return (ragged && n > 1 && n <= (1LL << 16)) ? n : 0;
 }
 
 int make_tma_map_4d(CUtensorMap *map, const void *ptr, bool bf16, uint64_t d0, uint64_t d1,
@@ -996,9 +1125,9 @@ int make_tma_map_4d(CUtensorMap *map, const void *ptr, bool bf16, uint64_t d0, u
                     d1, d2, d3, b1, b2);
 }
 
-int launch_prefill_tc(const AttnParams &p, int dtype, cudaStream_t stream) {
-    if (dtype == 2) return launch_dtype<__nv_bfloat16>(p, true, stream);
-    return launch_dtype<__half>(p, false, stream);
+int launch_prefill_tc(const AttnParams &p, int dtype, cudaStream_t stream, int *order_ws) {
+    if (dtype == 2) return launch_dtype<__nv_bfloat16>(p, true, stream, order_ws);
+    return launch_dtype<__half>(p, false, stream, order_ws);
 }
 
 }  // namespace attn

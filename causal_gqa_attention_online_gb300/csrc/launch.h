@@ -44,7 +44,10 @@ int decode_split_len(const AttnParams &p, int nsm);
 int launch_decode(const AttnParams &p, int dtype, cudaStream_t stream);
 // tcgen05/TMEM prefill (bf16/fp16, D and Dv multiples of 16 in [64, 128]).
 bool prefill_tc_supported(const AttnParams &p, int dtype);
-int launch_prefill_tc(const AttnParams &p, int dtype, cudaStream_t stream);
+// Ints of workspace the launch wants for its longest-first unit order (0: the
+// natural order is used); order_ws holds that many, or is null.
+long long prefill_tc_order_len(const AttnParams &p);
+int launch_prefill_tc(const AttnParams &p, int dtype, cudaStream_t stream, int *order_ws);
 
 // mma.sync forward (bf16/fp16, D and Dv multiples of 8 up to 512): the
 // tensor-core path for head widths the tcgen05 prefill kernel does not take.
