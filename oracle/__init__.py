@@ -89,6 +89,10 @@ class OracleLib:
         lib.oracle_attn_bwd_sampled.argtypes = [f32p, f32p, f32p, f32p] + [ci] * 7 + [
             i32p, i32p, ci, ci, cd, i32p, ctypes.c_long, f64p, ci, ci, ci, ci, f64p, f64p, ci]
         lib.oracle_attn_bwd_sampled.restype = ci
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        lib.oracle_attn_padded_allow.argtypes = [f32p, f32p, f32p, f64p, f64p] + [ci] * 7 + [
+            i32p, i32p, u8p, ci, ci, ci, cd, ci]
+        lib.oracle_attn_padded_allow.restype = ci
         lib.oracle_legal_pairs.argtypes = [ci, ci, ci, ci]
         lib.oracle_legal_pairs.restype = ctypes.c_longlong
         lib.oracle_max_threads.argtypes = []
@@ -142,6 +146,34 @@ class OracleLib:
                                          int(nthreads))
         if rc != 0:
             raise ValueError(f"oracle_attn_packed failed with status {rc}")
+        return o, lse
+
+    def attn_padded_allow(self, q, k, v, allow, *, B, Hq, Hkv, Q, K, D, Dv, seqlens_q=None,
+                          seqlens_k=None, window=0, scale=None, nthreads=0, mask=0):
+        """Padded layout with an arbitrary boolean mask ``allow`` [B, Hm, Q, K]
+        (Hm = 1: one mask for every head; Hm = Hq: one per query head), ANDed
+        with the ``mask`` mode and the window.  Returns (o, lse) float64."""
+        if scale is None:
+            scale = 1.0 / np.sqrt(D)
+        q, qp = _f32(q)
+        k, kp = _f32(k)
+        v, vp = _f32(v)
+        allow = np.ascontiguousarray(allow, dtype=bool).astype(np.uint8)
+        if allow.ndim != 4 or allow.shape[0] != B or allow.shape[2:] != (Q, K):
+            raise ValueError("oracle_attn_padded_allow: allow must be [B, Hm, Q, K]")
+        Hm = allow.shape[1]
+        if q.size != B * Q * Hq * D or k.size != B * K * Hkv * D or v.size != B * K * Hkv * Dv:
+            raise ValueError("oracle_attn_padded_allow: array sizes do not match the dims")
+        sq, sqp = _i32(seqlens_q)
+        sk, skp = _i32(seqlens_k)
+        o = np.empty((B, Q, Hq, Dv), np.float64)
+        lse = np.empty((B, Q, Hq), np.float64)
+        ap = allow.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8))
+        rc = self.lib.oracle_attn_padded_allow(qp, kp, vp, _f64p(o), _f64p(lse), B, Hq, Hkv, Q,
+                                               K, D, Dv, sqp, skp, ap, int(Hm), int(window),
+                                               int(mask), float(scale), int(nthreads))
+        if rc != 0:
+            raise ValueError(f"oracle_attn_padded_allow failed with status {rc}")
         return o, lse
 
     def attn_padded_rows(self, q, k, v, rows, *, B, Hq, Hkv, Q, K, D, Dv, seqlens_q=None,
@@ -255,6 +287,10 @@ def attn_packed(*args, **kw):
 
 def attn_padded_rows(*args, **kw):
     return _default().attn_padded_rows(*args, **kw)
+
+
+def attn_padded_allow(*args, **kw):
+    return _default().attn_padded_allow(*args, **kw)
 
 
 def attn_bwd_padded(*args, **kw):

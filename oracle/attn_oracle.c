@@ -505,6 +505,107 @@ int oracle_attn_bwd_sampled(const float *q, const float *k, const float *v, cons
     return bad ? 3 : 0;
 }
 
+/*
+ * An arbitrary boolean mask on top of the masks above -- an extension of this
+ * library ("Attention execution mapping" (LuisaCompute), section 7, names
+ * arbitrary masks as a semantic extension that needs an independent oracle).
+ * allow[((b * Hm + hm) * Q + q) * K + k] != 0 lets query row q of sequence b
+ * attend to key k, for query head h with hm = h when Hm == Hq and hm = 0 when
+ * Hm == 1 (one mask shared by every head).  The legal set is the set of the
+ * chosen mask mode intersected with it:
+ *     L = { k in [lo, hi] of legal_keys(q) : allow[b, hm, q, k] != 0 }
+ * and the definition is otherwise the one at the top of this file: the keys of
+ * L are listed explicitly, pass 1 takes their maximum score, pass 2 the
+ * normaliser and the weighted sum of V rows; an empty L gives +0 / -inf.
+ */
+static void oracle_row_allow(const float *qrow, const float *kbase, const float *vbase,
+                             long kstride, long vstride, int D, int Dv, int q, int Qb,
+                             int Kb, int window, int mask, const uint8_t *allow_row,
+                             double scale, long *keys, double *s_scratch, double *orow,
+                             double *lse_out)
+{
+    long lo, hi;                                       /* inclusive bounds */
+    legal_keys(q, Qb, Kb, window, mask, &lo, &hi);
+    long n = 0;
+    for (long k = lo; k <= hi; ++k)
+        if (allow_row[k] != 0) keys[n++] = k;
+    for (int j = 0; j < Dv; ++j) orow[j] = 0.0;
+    if (n == 0) { *lse_out = -INFINITY; return; }
+    double m = -INFINITY;
+    for (long i = 0; i < n; ++i) {
+        const float *krow = kbase + keys[i] * kstride;
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d) acc += (double)qrow[d] * (double)krow[d];
+        s_scratch[i] = scale * acc;
+        if (s_scratch[i] > m) m = s_scratch[i];
+    }
+    double l = 0.0;
+    for (long i = 0; i < n; ++i) {
+        const double p = exp(s_scratch[i] - m);
+        l += p;
+        const float *vrow = vbase + keys[i] * vstride;
+        for (int j = 0; j < Dv; ++j) orow[j] += p * (double)vrow[j];
+    }
+    for (int j = 0; j < Dv; ++j) orow[j] /= l;
+    *lse_out = m + log(l);
+}
+
+/* Padded layout with the boolean mask `allow` [B, Hm, Q, K] (Hm = 1 or Hq);
+ * other arguments as oracle_attn_padded. */
+int oracle_attn_padded_allow(const float *q, const float *k, const float *v, double *o,
+                             double *lse, int B, int Hq, int Hkv, int Q, int K, int D, int Dv,
+                             const int32_t *seqlens_q, const int32_t *seqlens_k,
+                             const uint8_t *allow, int Hm, int window, int mask, double scale,
+                             int nthreads)
+{
+    if (check_dims(B, Hq, Hkv, D, Dv) || Q < 0 || K < 0 || !allow) return 1;
+    if (mask < 0 || mask > 2 || (mask == 2 && window > 0)) return 1;
+    if (Hm != 1 && Hm != Hq) return 1;
+    const int G = Hq / Hkv;
+    const long nrows = (long)B * Q * Hq;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int bad = 0;
+#pragma omp parallel
+    {
+        const size_t kn = (size_t)(K > 0 ? K : 1);
+        double *s = (double *)malloc(sizeof(double) * kn);
+        long *keys = (long *)malloc(sizeof(long) * kn);
+        if (!s || !keys) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (long r = 0; r < nrows; ++r) {
+            if (!s || !keys) continue;
+            const int h = (int)(r % Hq);
+            const int qi = (int)((r / Hq) % Q);
+            const int b = (int)(r / ((long)Hq * Q));
+            const int Qb = clamp_len(seqlens_q ? seqlens_q[b] : Q, Q);
+            const int Kb = clamp_len(seqlens_k ? seqlens_k[b] : K, K);
+            double *orow = o + r * Dv;
+            if (qi >= Qb) {
+                for (int j = 0; j < Dv; ++j) orow[j] = 0.0;
+                lse[r] = -INFINITY;
+                continue;
+            }
+            const int kh = h / G;
+            const int hm = Hm == 1 ? 0 : h;
+            const uint8_t *arow = allow + (((long)b * Hm + hm) * Q + qi) * (long)K;
+            oracle_row_allow(q + r * D, k + ((long)b * K * Hkv + kh) * D,
+                             v + ((long)b * K * Hkv + kh) * Dv, (long)Hkv * D, (long)Hkv * Dv,
+                             D, Dv, qi, Qb, Kb, window, mask, arow, scale, keys, s, orow,
+                             &lse[r]);
+        }
+        free(s);
+        free(keys);
+    }
+    return bad ? 3 : 0;
+}
+
 /* Number of legal (query, key) pairs of one sequence, per head: the unit the
  * throughput figures count (FLOP = pairs * (2D + 2Dv) per head). */
 long long oracle_legal_pairs(int Qb, int Kb, int window, int mask)

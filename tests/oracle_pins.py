@@ -530,6 +530,104 @@ def pin_bwd_sampled_matches_full(ol):
                     assert np.allclose(sdv, dv[b, k0:k1, kh], rtol=1e-12, atol=1e-14), (ci, b)
 
 
+# ---------------------------------------------------------------------------
+# the arbitrary (boolean) mask extension
+
+def sdpa_reference_allow(q, k, v, Qb, Kb, Hq, Hkv, window, scale, mask, allow):
+    """fp64 torch SDPA for one sequence with a per-head boolean mask: the
+    numpy-triangle mask of ``mask``/``window`` ANDed with ``allow`` [Hm,Qb,Kb]
+    (Hm = 1 broadcasts over the heads).  Returns (o [Qb,Hq,Dv], lse [Qb,Hq],
+    has [Qb,Hq])."""
+    G = Hq // Hkv
+    qt = torch.from_numpy(np.asarray(q, np.float64)).permute(1, 0, 2)       # [Hq,Qb,D]
+    kt = torch.from_numpy(np.asarray(k, np.float64)).permute(1, 0, 2).repeat_interleave(G, 0)
+    vt = torch.from_numpy(np.asarray(v, np.float64)).permute(1, 0, 2).repeat_interleave(G, 0)
+    m = mask_matrix(Qb, Kb, window, mask)[None] & np.broadcast_to(allow, (Hq, Qb, Kb))
+    has = m.any(axis=2)                                                     # [Hq,Qb]
+    mt = torch.from_numpy(np.ascontiguousarray(m))
+    safe = mt.clone()
+    safe[~torch.from_numpy(has)] = True
+    o = torch.nn.functional.scaled_dot_product_attention(
+        qt.unsqueeze(0), kt.unsqueeze(0), vt.unsqueeze(0), attn_mask=safe.unsqueeze(0),
+        scale=scale)[0]
+    sc = torch.matmul(qt, kt.transpose(1, 2)) * scale
+    sc = sc.masked_fill(~mt, -math.inf)
+    lse = torch.logsumexp(sc, dim=-1)
+    return o.permute(1, 0, 2).numpy(), lse.permute(1, 0).numpy(), has.T
+
+
+ALLOW_CASES = [
+    # B, Hq, Hkv, Q, K, D, Dv, window, mask, Hm, density, seqlens_q, seqlens_k
+    (2, 4, 2, 10, 23, 8, 6, 0, 2, 1, 0.5, None, None),       # a pure arbitrary mask, shared
+    (1, 6, 3, 12, 12, 5, 7, 0, 0, 6, 0.3, None, None),       # causal AND a per-head mask
+    (2, 4, 1, 9, 31, 8, 8, 4, 0, 4, 0.7, [9, 5], [31, 12]),  # window, per-head, ragged
+    (1, 4, 2, 14, 20, 6, 6, 3, 1, 1, 0.6, None, None),       # top-left causal + window
+]
+
+
+def pin_allow_sdpa(ol):
+    for ci, (B, Hq, Hkv, Q, K, D, Dv, w, mode, Hm, dens, sq, sk) in enumerate(ALLOW_CASES):
+        q, k, v = rng_inputs(300 + ci, B, Hq, Hkv, Q, K, D, Dv)
+        allow = np.random.default_rng(400 + ci).random((B, Hm, Q, K)) < dens
+        allow[:, :, 1, :] = False          # a row with no allowed key in every case
+        scale = 1.0 / math.sqrt(D) * (1.0 + 0.3 * ci)
+        o, lse = ol.attn_padded_allow(q, k, v, allow, B=B, Hq=Hq, Hkv=Hkv, Q=Q, K=K, D=D, Dv=Dv,
+                                      seqlens_q=sq, seqlens_k=sk, window=w, scale=scale,
+                                      mask=mode)
+        for b in range(B):
+            Qb = Q if sq is None else sq[b]
+            Kb = K if sk is None else sk[b]
+            assert np.all(o[b, Qb:] == 0.0) and np.all(lse[b, Qb:] == -math.inf), (ci, b)
+            if Qb == 0:
+                continue
+            ro, rl, has = sdpa_reference_allow(q[b, :Qb], k[b, :Kb], v[b, :Kb], Qb, Kb, Hq, Hkv,
+                                               w, scale, mode, allow[b, :, :Qb, :Kb])
+            ob, lb = o[b, :Qb], lse[b, :Qb]
+            assert has.any() and not has.all(), ("case mixes empty and non-empty rows", ci)
+            assert np.allclose(ob[has], ro[has], atol=1e-12, rtol=1e-10), (ci, b)
+            assert np.allclose(lb[has], rl[has], atol=1e-12, rtol=1e-12), (ci, b)
+            assert np.all(ob[~has] == 0.0) and not np.any(np.signbit(ob[~has])), (ci, b)
+            assert np.all(lb[~has] == -math.inf), (ci, b)
+
+
+def pin_allow_invariants(ol):
+    B, Hq, Hkv, Q, K, D, Dv = 2, 4, 2, 11, 17, 8, 5
+    q, k, v = rng_inputs(31, B, Hq, Hkv, Q, K, D, Dv)
+    kw = dict(B=B, Hq=Hq, Hkv=Hkv, Q=Q, K=K, D=D, Dv=Dv)
+    G = Hq // Hkv
+    # every key allowed: the plain masks, bit for bit
+    for mode, w in ((0, 0), (0, 5), (1, 3), (2, 0)):
+        ones = np.ones((B, 1, Q, K), bool)
+        oa, la = ol.attn_padded_allow(q, k, v, ones, window=w, mask=mode, **kw)
+        op, lp = ol.attn_padded(q, k, v, window=w, mask=mode, **kw)
+        assert np.array_equal(oa, op) and np.array_equal(la, lp), ("all allowed", mode, w)
+    # the bottom-right triangle as an arbitrary mask with no mask mode = the causal rule
+    tri = np.broadcast_to(np.tril(np.ones((Q, K), bool), k=K - Q), (B, Hq, Q, K))
+    oa, la = ol.attn_padded_allow(q, k, v, tri, mask=2, **kw)
+    op, lp = ol.attn_padded(q, k, v, mask=0, **kw)
+    assert np.array_equal(oa, op) and np.array_equal(la, lp), "triangle == causal"
+    # nothing allowed: +0 and -inf on every row
+    oz, lz = ol.attn_padded_allow(q, k, v, np.zeros((B, Hq, Q, K), bool), mask=2, **kw)
+    assert np.all(oz == 0.0) and not np.any(np.signbit(oz)) and np.all(lz == -math.inf)
+    # one allowed key per (row, head): its V row, and its score as the LSE
+    g = np.random.default_rng(32)
+    one = np.zeros((B, Hq, Q, K), bool)
+    pick = g.integers(0, K, size=(B, Hq, Q))
+    for b in range(B):
+        for h in range(Hq):
+            one[b, h, np.arange(Q), pick[b, h]] = True
+    o1, l1 = ol.attn_padded_allow(q, k, v, one, mask=2, **kw)
+    scale = 1.0 / math.sqrt(D)
+    for b in range(B):
+        for h in range(Hq):
+            for i in range(Q):
+                kk = pick[b, h, i]
+                assert np.allclose(o1[b, i, h], v[b, kk, h // G], atol=1e-14), "one key"
+                s = scale * float(np.dot(q[b, i, h].astype(np.float64), k[b, kk, h // G]))
+                assert abs(l1[b, i, h] - s) < 1e-12, "one key lse"
+
+
 ALL_PINS = [pin_golden, pin_sdpa, pin_invariants, pin_packed_matches_padded,
             pin_rows_match_full, pin_legal_pairs, pin_sdpa_masks, pin_bwd_autograd,
-            pin_bwd_finite_differences, pin_bwd_invariants, pin_bwd_sampled_matches_full]
+            pin_bwd_finite_differences, pin_bwd_invariants, pin_bwd_sampled_matches_full,
+            pin_allow_sdpa, pin_allow_invariants]

@@ -60,6 +60,16 @@ MUTANTS = [
      "const int h = kkh + (int)(t / Qb), qi = (int)(t % Qb);"),
     ("bwd_sampled_row_term", "const double ds = exp(scale * acc - lse) * (dp - Dq);",
      "const double ds = exp(scale * acc - lse) * dp;"),
+    # the arbitrary (boolean) mask
+    ("allow_ignored", "if (allow_row[k] != 0) keys[n++] = k;", "keys[n++] = k;"),
+    ("allow_inverted", "if (allow_row[k] != 0) keys[n++] = k;", "if (allow_row[k] == 0) keys[n++] = k;"),
+    ("allow_kv_head", "const int hm = Hm == 1 ? 0 : h;", "const int hm = Hm == 1 ? 0 : kh;"),
+    ("allow_batch_dropped", "allow + (((long)b * Hm + hm) * Q + qi) * (long)K;",
+     "allow + (((long)0 * Hm + hm) * Q + qi) * (long)K;"),
+    ("allow_row_shifted", "allow + (((long)b * Hm + hm) * Q + qi) * (long)K;",
+     "allow + (((long)b * Hm + hm) * Q + (qi + 1 < Qb ? qi + 1 : qi)) * (long)K;"),
+    ("allow_ignores_range", "    legal_keys(q, Qb, Kb, window, mask, &lo, &hi);\n    long n = 0;",
+     "    legal_keys(q, Qb, Kb, window, mask, &lo, &hi);\n    lo = 0;\n    hi = (long)Kb - 1;\n    long n = 0;"),
 ]
 
 
