@@ -8,13 +8,13 @@ seeded synthetic-input generators (``synth``).  Build the library with
 from .binding import (ALGOS, MASKS, ATTN_ALGO_AUTO, ATTN_ALGO_DECODE, ATTN_ALGO_GENERIC,
                       ATTN_ALGO_TCGEN05, ATTN_BF16, ATTN_F16, ATTN_F32, EXPORTED, AttnError,
                       attn_bwd, attn_bwd_varlen, attn_fwd, attn_fwd_decode_noalloc,
-                      attn_fwd_paged, attn_fwd_staged, attn_fwd_varlen, attn_lse_combine,
-                      device_status, kernel_launches, last_error, library_path, load_library,
-                      set_wait_limit)
+                      attn_fwd_masked, attn_fwd_paged, attn_fwd_staged, attn_fwd_varlen,
+                      attn_lse_combine, device_status, kernel_launches, last_error,
+                      library_path, load_library, pack_mask, set_wait_limit)
 
 __all__ = ["ALGOS", "MASKS", "ATTN_ALGO_AUTO", "ATTN_ALGO_DECODE", "ATTN_ALGO_GENERIC",
            "ATTN_ALGO_TCGEN05", "ATTN_BF16", "ATTN_F16", "ATTN_F32", "EXPORTED", "AttnError",
            "attn_bwd", "attn_bwd_varlen", "attn_fwd", "attn_fwd_decode_noalloc",
-           "attn_fwd_paged", "attn_fwd_staged", "attn_fwd_varlen", "attn_lse_combine",
-           "device_status", "kernel_launches", "last_error", "library_path", "load_library",
-           "set_wait_limit"]
+           "attn_fwd_masked", "attn_fwd_paged", "attn_fwd_staged", "attn_fwd_varlen",
+           "attn_lse_combine", "device_status", "kernel_launches", "last_error",
+           "library_path", "load_library", "pack_mask", "set_wait_limit"]

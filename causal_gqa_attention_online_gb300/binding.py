@@ -25,7 +25,8 @@ MASKS = {"causal": 0, "causal_top_left": 1, "none": 2}
 _DTYPE_CODE = {torch.float32: ATTN_F32, torch.float16: ATTN_F16, torch.bfloat16: ATTN_BF16}
 
 EXPORTED = ("attn_fwd", "attn_fwd_varlen", "attn_fwd_algo", "attn_fwd_varlen_algo",
-            "attn_fwd_ex", "attn_fwd_varlen_ex", "attn_fwd_paged", "attn_bwd", "attn_bwd_varlen",
+            "attn_fwd_ex", "attn_fwd_varlen_ex", "attn_fwd_paged", "attn_fwd_masked", "attn_bwd",
+            "attn_bwd_varlen",
             "attn_lse_combine", "attn_fwd_decode_noalloc", "attn_fwd_staged", "attn_last_error",
             "attn_device_status", "attn_set_wait_limit", "attn_kernel_launches", "attn_version")
 
@@ -70,6 +71,9 @@ def load_library(path: str | None = None):
         lib.attn_fwd_paged.argtypes = [vp] * 5 + [ip] * 6 + [vp, ip, ip, ip, vp, vp, ip, fp, ip,
                                                              ip, ip, vp]
         lib.attn_fwd_paged.restype = ip
+        lib.attn_fwd_masked.argtypes = [vp] * 5 + [ip] * 7 + [vp, vp, vp, ip, ip, ip, fp, ip, ip,
+                                                             ip, vp]
+        lib.attn_fwd_masked.restype = ip
         lib.attn_fwd_varlen_ex.restype = ip
         lib.attn_fwd_decode_noalloc.argtypes = common + [vp]
         lib.attn_fwd_decode_noalloc.restype = ip
@@ -379,6 +383,58 @@ def attn_fwd_staged(hq, hk, hv, q, k, v, o, lse=None, ho=None, hlse=None, *, seq
                              ctypes.byref(bin_), ctypes.byref(bout), _stream_ptr(st))
     _check(rc)
     return ho, hlse, bin_.value, bout.value
+
+
+def pack_mask(allow: torch.Tensor) -> torch.Tensor:
+    """Bit-pack a boolean mask [B, Hm, Q, K] into the int32 words attn_fwd_masked
+    reads: bit k % 32 of word k / 32 of a row is key k, rows padded to a
+    multiple of 128 keys.  Returns [B, Hm, Q, 4 * ceil(K / 128)] int32 on the
+    mask's device."""
+    B, Hm, Q, K = allow.shape
+    kp = (K + 127) // 128 * 128
+    bits = torch.zeros((B, Hm, Q, kp), dtype=torch.int64, device=allow.device)
+    bits[..., :K] = allow.to(torch.int64)
+    bits = bits.view(B, Hm, Q, kp // 32, 32)
+    weights = torch.ones(32, dtype=torch.int64, device=allow.device) << torch.arange(
+        32, device=allow.device)
+    words = (bits * weights).sum(dim=-1)
+    words = torch.where(words >= 2**31, words - 2**32, words)
+    return words.to(torch.int32).contiguous()
+
+
+def attn_fwd_masked(q, k, v, mask_words, o=None, lse=None, *, seqlens_q=None, seqlens_k=None,
+                    window=0, scale=None, algo="auto", mask="none", stream=None, want_lse=True):
+    """Padded layout with an arbitrary mask: ``mask_words`` int32 [B, Hm, Q, W]
+    (``pack_mask`` of a boolean [B, Hm, Q, K]; Hm = 1 or Hq), ANDed with
+    ``mask`` ("none" by default, or a causal mode) and ``window``.
+    Returns (o, lse)."""
+    lib = load_library()
+    B, Q, Hq, D = q.shape
+    K, Hkv = k.shape[1], k.shape[2]
+    Dv = v.shape[3]
+    dev = q.device
+    Hm, W = mask_words.shape[1], mask_words.shape[3]
+    if o is None:
+        o = torch.empty((B, Q, Hq, Dv), dtype=q.dtype, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Q, Hq), dtype=torch.float32, device=dev)
+    for name, t, n in (("q", q, B * Q * Hq * D), ("k", k, B * K * Hkv * D),
+                       ("v", v, B * K * Hkv * Dv), ("o", o, B * Q * Hq * Dv)):
+        _check_tensor(name, t, q.dtype, n, dev)
+    if lse is not None:
+        _check_tensor("lse", lse, torch.float32, B * Q * Hq, dev)
+    _check_tensor("mask_words", mask_words, torch.int32, B * Hm * Q * W, dev)
+    for name, t in (("seqlens_q", seqlens_q), ("seqlens_k", seqlens_k)):
+        if t is not None:
+            _check_tensor(name, t, torch.int32, B, dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = lib.attn_fwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Q, K, D,
+                             Dv, _ptr(seqlens_q), _ptr(seqlens_k), _ptr(mask_words), W, Hm,
+                             int(window), float(scale), MASKS[mask], _DTYPE_CODE[q.dtype],
+                             ALGOS[algo], _stream_ptr(stream))
+    _check(rc)
+    return o, lse
 
 
 def attn_fwd_paged(q, k_pages, v_pages, block_table, seqlens_k, o=None, lse=None, *,

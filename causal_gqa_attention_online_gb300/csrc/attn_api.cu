@@ -210,16 +210,22 @@ int run(AttnParams &p, int dtype, int algo, cudaStream_t stream) {
     if (rc) return rc;
     const int nsm = sm_count(dev);
 
-    // Kernel choice.
+    // Kernel choice.  An arbitrary mask runs on the tcgen05 prefill or the
+    // CUDA-core kernel only.
+    const bool masked = p.mask_bits != nullptr;
+    if (masked && (algo == ATTN_ALGO_DECODE || algo == ATTN_ALGO_MMA)) {
+        set_error("an arbitrary mask runs on the tcgen05 or the generic kernel only");
+        return ATTN_ERR_UNSUPPORTED;
+    }
     int chosen = algo;
     if (algo == ATTN_ALGO_AUTO) {
         chosen = ATTN_ALGO_GENERIC;
         if (dtype != ATTN_F32) {
-            if (decode_supported(p, dtype))
+            if (!masked && decode_supported(p, dtype))
                 chosen = ATTN_ALGO_DECODE;
             else if (prefill_tc_supported(p, dtype))
                 chosen = ATTN_ALGO_TCGEN05;
-            else if (fwd_mma_supported(p, dtype))
+            else if (!masked && fwd_mma_supported(p, dtype))
                 chosen = ATTN_ALGO_MMA;
         }
     } else if (algo == ATTN_ALGO_DECODE && !decode_supported(p, dtype)) {
@@ -234,19 +240,22 @@ int run(AttnParams &p, int dtype, int algo, cudaStream_t stream) {
     }
 
     if (chosen == ATTN_ALGO_TCGEN05) {
-        const long long n = prefill_tc_order_len(p);
-        if (n == 0) return launch_prefill_tc(p, dtype, stream, nullptr);
+        // workspace: the unit order (ints), then the live-tile flags of a mask
+        const long long n = prefill_tc_order_len(p), nlive = prefill_tc_live_len(p);
+        if (n == 0 && nlive == 0) return launch_prefill_tc(p, dtype, stream, nullptr, nullptr);
         void *ws = nullptr;
         cudaMemPool_t pool = nullptr;
         rc = pool_for(dev, &pool);
         if (rc) return rc;
-        const size_t bytes = sizeof(int) * (size_t)n;
+        const size_t order_bytes = (sizeof(int) * (size_t)n + 255) / 256 * 256;
+        const size_t bytes = order_bytes + (size_t)nlive;
         cudaError_t e = cudaMallocFromPoolAsync(&ws, bytes, pool, stream);
         if (e != cudaSuccess) {
             set_error("workspace cudaMallocFromPoolAsync(%zu): %s", bytes, cudaGetErrorString(e));
             return ATTN_ERR_CUDA;
         }
-        rc = launch_prefill_tc(p, dtype, stream, static_cast<int *>(ws));
+        rc = launch_prefill_tc(p, dtype, stream, n > 0 ? static_cast<int *>(ws) : nullptr,
+                               nlive > 0 ? static_cast<uint8_t *>(ws) + order_bytes : nullptr);
         e = cudaFreeAsync(ws, stream);
         if (e != cudaSuccess && rc == 0) {
             set_error("workspace cudaFreeAsync: %s", cudaGetErrorString(e));
@@ -292,7 +301,8 @@ int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
                const int32_t *seqlens_k, const int32_t *cu_q, const int32_t *cu_k, int window,
                float scale, int mask, int dtype, int algo, cudaStream_t stream,
                const int32_t *block_table = nullptr, int page_size = 0, int num_pages = 0,
-               int max_pages = 0) {
+               int max_pages = 0, const uint32_t *mask_bits = nullptr, int mask_words = 0,
+               int mask_heads = 0) {
     clear_error();
     int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Q, K, D, Dv, dtype, algo);
     if (rc) return rc;
@@ -336,6 +346,9 @@ int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse,
     while (page_size > 0 && (1 << p.page_shift) < page_size) ++p.page_shift;
     p.num_pages = num_pages;
     p.max_pages = max_pages;
+    p.mask_bits = K > 0 ? mask_bits : nullptr;  // no key: nothing to mask
+    p.mask_words = mask_words;
+    p.mask_heads = mask_heads;
     p.scale = scale;
     p.scale_log2 = scale * kLog2e;
     p.nsplit = 1;
@@ -508,6 +521,39 @@ int attn_fwd_paged(const void *q, const void *k_pages, const void *v_pages, void
                       nullptr, window, scale, mask, dtype, algo,
                       reinterpret_cast<cudaStream_t>(stream), block_table, page_size, num_pages,
                       max_pages);
+}
+
+int attn_fwd_masked(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                    int Hq, int Hkv, int Q, int K, int D, int Dv, const int32_t *seqlens_q,
+                    const int32_t *seqlens_k, const uint32_t *mask_bits, int mask_words,
+                    int mask_heads, int window, float scale, int mask, int dtype, int algo,
+                    attn_stream_t stream) {
+    attn::clear_error();
+    if ((long long)B * Q * Hq > 0 && K > 0) {
+        if (mask_bits == nullptr) {
+            set_error("attn_fwd_masked: mask_bits must be non-null");
+            return ATTN_ERR_INVALID;
+        }
+        if ((reinterpret_cast<uintptr_t>(mask_bits) & 15u) != 0) {
+            set_error("attn_fwd_masked: mask_bits must be 16-byte aligned");
+            return ATTN_ERR_INVALID;
+        }
+        const long long need = 4LL * (((long long)K + 127) / 128);
+        if (mask_words < need || mask_words % 4 != 0) {
+            set_error("attn_fwd_masked: mask_words (%d) must be a multiple of 4 and at least "
+                      "4 * ceil(K / 128) = %lld",
+                      mask_words, need);
+            return ATTN_ERR_INVALID;
+        }
+        if (mask_heads != 1 && mask_heads != Hq) {
+            set_error("attn_fwd_masked: mask_heads (%d) must be 1 or Hq (%d)", mask_heads, Hq);
+            return ATTN_ERR_INVALID;
+        }
+    }
+    return fwd_common(q, k, v, o, lse, B, Hq, Hkv, (long long)B * Q, (long long)B * K, Q, K, D, Dv,
+                      seqlens_q, seqlens_k, nullptr, nullptr, window, scale, mask, dtype, algo,
+                      reinterpret_cast<cudaStream_t>(stream), nullptr, 0, 0, 0, mask_bits,
+                      mask_words, mask_heads);
 }
 
 int attn_fwd_algo(const void *q, const void *k, const void *v, void *o, float *lse, int B,

@@ -54,6 +54,12 @@ struct AttnParams {
     float *part_lse;         // [nsplit][B][Q][Hq] fp32, natural log
     int *status;             // device status word
     unsigned long long wait_ns;  // limit of the tcgen05 kernels' mbarrier waits (ns)
+    // arbitrary mask (padded layout; null: none): key k of query row q of
+    // sequence b and query head h is legal only if bit k % 32 of word k / 32 of
+    // mask row ((b * mask_heads + hm) * Q + q) is set, hm = h when
+    // mask_heads == Hq and 0 when mask_heads == 1; rows are mask_words apart
+    const uint32_t *mask_bits;
+    int mask_words, mask_heads;
 };
 
 // One backward problem: the forward problem (its o and lse hold the forward's
@@ -104,6 +110,12 @@ __device__ __forceinline__ long long kv_row(const AttnParams &p, const SeqInfo &
     int pg = __ldg(p.block_table + (long long)b * p.max_pages + (key >> p.page_shift));
     pg = min(max(pg, 0), p.num_pages - 1);
     return ((long long)pg << p.page_shift) + (key & (p.page_size - 1));
+}
+
+// Row of the arbitrary mask for query row qi of sequence b and query head h.
+__device__ __forceinline__ const uint32_t *mask_row(const AttnParams &p, int b, int h, int qi) {
+    const int hm = p.mask_heads == 1 ? 0 : h;
+    return p.mask_bits + (((long long)b * p.mask_heads + hm) * p.Q + qi) * (long long)p.mask_words;
 }
 
 // Legal keys of query row qi: [lo, hi) (empty when hi <= lo).  Causal masks

@@ -94,12 +94,17 @@ __global__ void __launch_bounds__(kWarps * 32, 1) generic_fwd_kernel(const AttnP
     float m[kRPW], l[kRPW], acc[kRPW][DVL];
     int rlo[kRPW], rhi[kRPW];
     SplitSpan span[kRPW];
+    const uint32_t *mrow[kRPW];  // arbitrary mask rows (null: no mask or no real query)
 #pragma unroll
     for (int i = 0; i < kRPW; ++i) {
         const int r = r0 + warp + kWarps * i;
         rlo[i] = 0;
         rhi[i] = 0;
-        if (r < nvalid) legal_range(r / G, si.Qb, si.Kb, p.window, p.mask, rlo[i], rhi[i]);
+        mrow[i] = nullptr;
+        if (r < nvalid) {
+            legal_range(r / G, si.Qb, si.Kb, p.window, p.mask, rlo[i], rhi[i]);
+            if (p.mask_bits != nullptr) mrow[i] = mask_row(p, b, kvh * G + r % G, r / G);
+        }
         span[i] = split_span(rlo[i], rhi[i], p.split_len);
         rlo[i] = max(rlo[i], key_lo);
         rhi[i] = min(rhi[i], key_hi);
@@ -163,7 +168,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) generic_fwd_kernel(const AttnP
         float pj[kRPW];
 #pragma unroll
         for (int i = 0; i < kRPW; ++i) {
-            const float si = key >= rlo[i] && key < rhi[i] ? s[i] : -INFINITY;
+            bool legal = key >= rlo[i] && key < rhi[i];
+            // (a key in the row's range is below Kb <= K: its word is in the row)
+            if (legal && mrow[i] != nullptr) legal = (__ldg(mrow[i] + (key >> 5)) >> (key & 31)) & 1u;
+            const float si = legal ? s[i] : -INFINITY;
             const float mnew = fmaxf(m[i], warp_max(si));
             // a row with no legal key so far keeps a finite reference: p = 0
             const float ref = mnew == -INFINITY ? 0.f : mnew;

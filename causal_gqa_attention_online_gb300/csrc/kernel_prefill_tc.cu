@@ -96,6 +96,14 @@ struct PrefillArgs {
     // first (written by unit_order_kernel); null: the natural order, which is
     // longest-first already when every sequence has the same lengths.
     const int *order;
+    // Arbitrary mask: live[row * live_tiles + T] != 0 when 128-key tile T has
+    // a key that some row of the unit may attend to (written by
+    // mask_summary_kernel); a row is one (sequence, query block) when the mask
+    // is shared by all heads, else one unit (its natural index).  Dead tiles
+    // are neither loaded nor multiplied.
+    const uint8_t *live;
+    int live_tiles;   // ceil(K / 128)
+    int live_shared;  // 1: the mask is shared by all heads
 };
 
 template <int D, int DV> struct Layout {
@@ -148,9 +156,11 @@ struct UnitInfo {
     int lo_last, hi_first;  // interior test: all rows legal on [lo_last, hi_first)
     int hi_unit;         // one past the last key any row uses
     bool all_valid;      // every row of both tiles holds a real query
+    uint32_t u;          // natural unit index
 };
 
-template <bool PAGED>
+// Kernel modes: 0 the plain layouts, 1 paged K/V, 2 an arbitrary mask.
+template <int MODE>
 __device__ __forceinline__ UnitInfo unit_info(const PrefillArgs &a, long long u64) {
     const AttnParams &p = a.p;
     // 32-bit index arithmetic (the unit count is below 2^31)
@@ -160,6 +170,7 @@ __device__ __forceinline__ UnitInfo unit_info(const PrefillArgs &a, long long u6
     const uint32_t kvh = r2 / (uint32_t)a.nsub, sub = r2 - kvh * (uint32_t)a.nsub;
     const int qblk = a.nqblk - 1 - (int)qi;
     UnitInfo x;
+    x.u = u;
     x.b = (int)b;
     x.kvh = (int)kvh;
     x.h0 = x.kvh * p.G + (int)sub * a.Gp;
@@ -177,9 +188,10 @@ __device__ __forceinline__ UnitInfo unit_info(const PrefillArgs &a, long long u6
     legal_range(x.q0, x.si.Qb, x.si.Kb, p.window, p.mask, lo_f, hi_f);
     legal_range(q_last, x.si.Qb, x.si.Kb, p.window, p.mask, lo_l, hi_l);
     if (hi_l <= lo_f) return x;
-    // paged K/V: tiles start on 128-key boundaries, so that each lies in one
-    // page (the keys before lo_f are masked)
-    x.kv_start = PAGED ? (lo_f & ~(kBN - 1)) : lo_f;
+    // paged K/V and an arbitrary mask: tiles start on 128-key boundaries, so
+    // that each lies in one page, or covers four whole words of a mask row
+    // (the keys before lo_f are masked)
+    x.kv_start = MODE != 0 ? (lo_f & ~(kBN - 1)) : lo_f;
     x.hi_unit = hi_l;
     x.n_kv = (hi_l - x.kv_start + kBN - 1) / kBN;
     x.lo_last = lo_l;
@@ -194,6 +206,24 @@ __device__ __forceinline__ UnitInfo unit_info(const PrefillArgs &a, long long u6
 // round).
 __device__ __forceinline__ long long snake_unit(long long r, int c, int G) {
     return r * G + ((r & 1) ? (G - 1 - c) : c);
+}
+
+// Arbitrary mask: the live flags of the unit's tiles (tile j of the unit is
+// entry j), and how many are live (*last: the last live one).
+__device__ __forceinline__ const uint8_t *live_row(const PrefillArgs &a, const UnitInfo &x) {
+    const long long row =
+        a.live_shared ? (long long)x.b * a.nqblk + x.q0 / (2 * a.QP) : (long long)x.u;
+    return a.live + row * a.live_tiles + x.kv_start / kBN;
+}
+__device__ __forceinline__ int count_live(const uint8_t *lv, int n_kv, int *last) {
+    int n = 0;
+    *last = -1;
+    for (int j = 0; j < n_kv; ++j)
+        if (lv[j] != 0) {
+            ++n;
+            *last = j;
+        }
+    return n;
 }
 
 template <typename T> __device__ __forceinline__ uint32_t pack2(float lo, float hi);
@@ -252,8 +282,10 @@ __device__ __forceinline__ void raise_abort(volatile int *abort_flag, int *statu
 
 // D, DV: the tile widths (64 or 128 columns); the real head dims p.D <= D and
 // p.Dv <= DV are multiples of 16, the rest of the tile columns zero-filled.
-// PAGED: K / V tiles found through the block table (a separate instance).
-template <typename T, int D, int DV, bool PAGED>
+// MODE: 0 the plain layouts; 1 K / V tiles found through the block table; 2 an
+// arbitrary mask (dead tiles skipped, live ones masked bit by bit).  Separate
+// instances, so that the plain one carries none of the others' code.
+template <typename T, int D, int DV, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
@@ -261,6 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmO) {
     using L = Layout<D, DV>;
     constexpr int NS = L::NS;
+    constexpr bool PAGED = MODE == 1;
+    constexpr bool MASKED = MODE == 2;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte-swizzle atoms
     const uint32_t raw = smem_addr(smem_raw);
@@ -317,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     // launched as a programmatic dependent of unit_order_kernel: the unit
     // order is complete and visible once this returns
-    if (a.order != nullptr) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    if (a.order != nullptr || a.live != nullptr) asm volatile("griddepcontrol.wait;\n" ::: "memory");
     const uint32_t tmem = *tmem_slot;
     auto kv_full = [&](int s) { return bar(B_KV_FULL + s); };
     auto kv_empty = [&](int s) { return bar(B_KV_FULL + NS + s); };
@@ -339,8 +373,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (long long rnd = 0; rnd * gridDim.x < a.nunits && ok; ++rnd) {
                     const long long u = snake_unit(rnd, blockIdx.x, gridDim.x);
                     if (u >= a.nunits) continue;
-                    const UnitInfo x = unit_info<PAGED>(a, u);
+                    const UnitInfo x = unit_info<MODE>(a, u);
                     if (x.n_kv == 0) continue;
+                    // an arbitrary mask: only the live tiles are loaded and multiplied;
+                    // the MMA warps see n_use tiles and a first key placed so that
+                    // the last one they process starts at the last live tile
+                    const uint8_t *lv = MASKED ? live_row(a, x) : nullptr;
+                    int n_use = x.n_kv, j_last = x.n_kv - 1;
+                    if (MASKED) {
+                        n_use = count_live(lv, x.n_kv, &j_last);
+                        if (n_use == 0) continue;
+                    }
                     const int qrow = (padded ? 0 : (int)x.si.q_off) + x.q0;
                     const int krow = padded ? 0 : (int)x.si.k_off;
                     const int bc = padded ? x.b : 0;
@@ -355,8 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     int *d = unit_desc + q_ph * 4;  // slot by the parity of this Q_FULL phase
-                    d[0] = x.n_kv;
-                    d[1] = x.kv_start;
+                    d[0] = n_use;
+                    d[1] = x.kv_start + (j_last - (n_use - 1)) * kBN;
                     d[2] = x.hi_unit;
                     mbar_arrive_expect_tx(bar(B_Q_FULL), 2 * L::QTILE);
                     last_q_parity = (int)q_ph;
@@ -374,10 +417,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int c = 0; c < DV / 64; ++c)
                             tma_prefetch_l2_4d(&tmV, c * 64, x.kvh, kr, kbc);
                     };
-                    for (int jj = 1; jj < kPrefetchTiles && jj < x.n_kv; ++jj) prefetch_kv(jj);
+                    for (int jj = 1; jj < kPrefetchTiles && jj < x.n_kv; ++jj)
+                        if (!MASKED || lv[jj] != 0) prefetch_kv(jj);
                     const long long un = snake_unit(rnd + 1, blockIdx.x, gridDim.x);
                     if (un < a.nunits) {
-                        const UnitInfo nx = unit_info<PAGED>(a, un);
+                        const UnitInfo nx = unit_info<MODE>(a, un);
                         if (nx.n_kv > 0) {
                             const int nq = (padded ? 0 : (int)nx.si.q_off) + nx.q0;
                             const int nbc = padded ? nx.b : 0;
@@ -387,8 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     for (int j = 0; j < x.n_kv && ok; ++j) {
+                        if (MASKED && lv[j] == 0) continue;
                         const int kr = kv_coord(x.kv_start + j * kBN);
-                        if (j + kPrefetchTiles < x.n_kv) prefetch_kv(j + kPrefetchTiles);
+                        if (j + kPrefetchTiles < x.n_kv && (!MASKED || lv[j + kPrefetchTiles] != 0))
+                            prefetch_kv(j + kPrefetchTiles);
 #pragma unroll
                         for (int which = 0; which < 2; ++which) {
                             const uint32_t it = kv_it++;
@@ -613,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (long long rnd = 0; rnd * gridDim.x < a.nunits && ok; ++rnd) {
             const long long u = snake_unit(rnd, blockIdx.x, gridDim.x);
             if (u >= a.nunits) continue;
-            const UnitInfo x = unit_info<PAGED>(a, u);
+            const UnitInfo x = unit_info<MODE>(a, u);
             const int qpos = x.q0 + t * a.QP + r / a.Gp;
             const int head = x.h0 + r % a.Gp;
             const bool valid = qpos < x.si.Qb;
@@ -621,8 +667,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             int lo = 0, hi = 0;
             if (valid) legal_range(qpos, x.si.Qb, x.si.Kb, p.window, p.mask, lo, hi);
             const long long orow = (x.si.q_off + qpos) * p.Hq + head;
+            const uint8_t *lv = nullptr;
+            int n_use = x.n_kv;
+            const uint32_t *mrow = nullptr;  // arbitrary mask: this row's words
+            if (MASKED && x.n_kv > 0) {
+                int j_last;
+                lv = live_row(a, x);
+                n_use = count_live(lv, x.n_kv, &j_last);
+                if (valid) mrow = mask_row(p, x.b, head, qpos);
+            }
 
-            if (x.n_kv == 0) {  // nothing to attend: +0 and -inf
+            if (n_use == 0) {  // nothing to attend: +0 and -inf
                 if (writes) {
                     uint4 *dst = reinterpret_cast<uint4 *>(og + orow * p.Dv);
                     for (int i = 0; i < p.Dv * 2 / 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
@@ -634,6 +689,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m_run = -INFINITY, l_run = 0.f;
             // One KV tile of this warpgroup's softmax.
             auto tile_step = [&](int j, bool interior) -> bool {
+                // an arbitrary mask: this row's 128 bits of the tile (k0 is a multiple
+                // of 128, the row a multiple of four words), fetched before the waits
+                uint4 mw = make_uint4(~0u, ~0u, ~0u, ~0u);
+                if (MASKED) {
+                    mw = make_uint4(0u, 0u, 0u, 0u);
+                    if (mrow != nullptr)
+                        mw = __ldg(reinterpret_cast<const uint4 *>(mrow + (x.kv_start + j * kBN) / 32));
+                }
                 // The two warpgroups take turns (tile k of group 0, tile k of
                 // group 1, tile k+1 of group 0, ...): while one runs its softmax
                 // the tensor core works on the other's tile.  Left free, the two
@@ -668,7 +731,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int b0 = min(max(hi - k0 - cc * 32, 0), 32);
                         const uint32_t below_b = b0 >= 32 ? 0xffffffffu : (1u << b0) - 1u;
                         const uint32_t below_a = a0 >= 32 ? 0xffffffffu : (1u << a0) - 1u;
-                        const uint32_t keep = below_b & ~below_a;
+                        uint32_t keep = below_b & ~below_a;
+                        if (MASKED) keep &= cc == 0 ? mw.x : cc == 1 ? mw.y : cc == 2 ? mw.z : mw.w;
                         if (__all_sync(0xffffffffu, keep == 0xffffffffu)) continue;
                         uint32_t v[32];
                         tmem_ld32(tS + cc * 32, v);
@@ -757,8 +821,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             for (int j = 0; j < x.n_kv && ok; ++j) {
+                if (MASKED && lv[j] == 0) continue;  // a dead tile: not computed
                 const int k0 = x.kv_start + j * kBN;
-                const bool interior = x.all_valid && k0 >= x.lo_last && k0 + kBN <= x.hi_first;
+                const bool interior =
+                    !MASKED && x.all_valid && k0 >= x.lo_last && k0 + kBN <= x.hi_first;
                 ok = tile_step(j, interior);
             }
             if (!ok) break;
@@ -797,8 +863,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (long long rnd = 0; rnd * gridDim.x < a.nunits && ok; ++rnd) {
             const long long u = snake_unit(rnd, blockIdx.x, gridDim.x);
             if (u >= a.nunits) continue;
-            const UnitInfo x = unit_info<PAGED>(a, u);
+            const UnitInfo x = unit_info<MODE>(a, u);
             if (x.n_kv == 0) continue;  // the softmax warpgroups wrote those rows
+            if (MASKED) {
+                int j_last;
+                if (count_live(live_row(a, x), x.n_kv, &j_last) == 0) continue;  // likewise
+            }
             const int b = (int)(nunit & 1u);
             ++nunit;
             for (int t = 0; t < 2; ++t) {
@@ -896,7 +966,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 constexpr int kOrderThreads = 1024;
 constexpr int kOrderBins = 2048;  // tile counts at or above the last bin share it
 
-template <bool PAGED>
+template <int MODE>
 __global__ void __launch_bounds__(kOrderThreads) unit_order_kernel(const PrefillArgs a,
                                                                    int *order) {
     __shared__ int hist[kOrderBins];
@@ -907,7 +977,12 @@ __global__ void __launch_bounds__(kOrderThreads) unit_order_kernel(const Prefill
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n = (int)a.nunits;
     auto bin_of = [&](int u) {
-        const int c = unit_info<PAGED>(a, u).n_kv;  // a.order is null here
+        const UnitInfo x = unit_info<MODE>(a, u);  // a.order is null here
+        int c = x.n_kv;
+        if (MODE == 2 && c > 0) {  // an arbitrary mask: the live tiles only
+            int j_last;
+            c = count_live(live_row(a, x), c, &j_last);
+        }
         return kOrderBins - 1 - min(c, kOrderBins - 1);  // bin 0: the most tiles
     };
     for (int i = tid; i < kOrderBins; i += kOrderThreads) hist[i] = 0;
@@ -948,6 +1023,51 @@ __global__ void __launch_bounds__(kOrderThreads) unit_order_kernel(const Prefill
     }
     __syncthreads();
     for (int u = tid; u < n; u += kOrderThreads) order[atomicAdd(&hist[bin_of(u)], 1)] = u;
+}
+
+// Arbitrary mask: which 128-key tiles have a key some row of a unit may attend
+// to.  One warp per (summary row, tile): a summary row is one (sequence, query
+// block) when the mask is shared by all heads (its rows are the block's query
+// positions) and one unit otherwise (the block's positions x the unit's
+// heads); each lane ORs the tile's four words of its rows.  Rows past the
+// sequence's queries are not read.
+constexpr int kSummaryWarps = 8;
+
+template <int MODE>
+__global__ void __launch_bounds__(kSummaryWarps * 32) mask_summary_kernel(const PrefillArgs a,
+                                                                          uint8_t *live) {
+    // the next launch (a programmatic dependent) may set up meanwhile
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    const AttnParams &p = a.p;
+    const int lane = threadIdx.x & 31;
+    const long long w = (long long)blockIdx.x * kSummaryWarps + (threadIdx.x >> 5);
+    const long long nrow = a.live_shared ? (long long)p.B * a.nqblk : a.nunits;
+    if (w >= nrow * a.live_tiles) return;
+    const long long row = w / a.live_tiles;
+    const int tile = (int)(w - row * a.live_tiles);
+    int b, q0, h0, nh;
+    if (a.live_shared) {
+        b = (int)(row / a.nqblk);
+        q0 = (int)(row - (long long)b * a.nqblk) * 2 * a.QP;
+        h0 = 0;
+        nh = 1;
+    } else {
+        const UnitInfo x = unit_info<MODE>(a, row);  // a.order is null here
+        b = x.b;
+        q0 = x.q0;
+        h0 = x.h0;
+        nh = a.Gp;
+    }
+    const int Qb = seq_info(p, b).Qb;
+    uint32_t any = 0;
+    for (int r = lane; r < 2 * a.QP * nh; r += 32) {
+        const int pos = q0 + r / nh;
+        if (pos >= Qb) continue;
+        const uint4 m = __ldg(reinterpret_cast<const uint4 *>(mask_row(p, b, h0 + r % nh, pos)) + tile);
+        any |= m.x | m.y | m.z | m.w;
+    }
+    any = __any_sync(0xffffffffu, any != 0);
+    if (lane == 0) live[w] = any ? 1 : 0;
 }
 
 // ------------------------------------------------------------------ host
@@ -995,11 +1115,15 @@ int pack_factor(int G) {
 }
 
 template <typename T, int D, int DV>
-int launch_t(const AttnParams &p, bool bf16, cudaStream_t stream, int *order_ws) {
+int launch_t(const AttnParams &p, bool bf16, cudaStream_t stream, int *order_ws,
+             uint8_t *live_ws) {
     using L = Layout<D, DV>;
     PrefillArgs a;
     a.p = p;
     a.order = nullptr;
+    a.live = nullptr;
+    a.live_tiles = (p.K + kBN - 1) / kBN;
+    a.live_shared = p.mask_heads == 1 ? 1 : 0;
     a.Gp = pack_factor(p.G);
     a.QP = kBM / a.Gp;
     a.nsub = p.G / a.Gp;
@@ -1038,9 +1162,31 @@ int launch_t(const AttnParams &p, bool bf16, cudaStream_t stream, int *order_ws)
         tk = tq;  // never read: every unit has no key
         tv = tq;
     }
+    const bool masked = p.mask_bits != nullptr;
     cudaError_t e;
+    if (masked) {
+        if (live_ws == nullptr) {
+            set_error("prefill kernel: the masked launch needs its tile workspace");
+            return 1;
+        }
+        const long long nrow = a.live_shared ? (long long)p.B * a.nqblk : a.nunits;
+        const long long warps = nrow * a.live_tiles;
+        const long long blocks = (warps + kSummaryWarps - 1) / kSummaryWarps;
+        if (blocks >= (1LL << 31)) {
+            set_error("prefill kernel: too many mask tiles");
+            return 2;
+        }
+        mask_summary_kernel<2><<<(unsigned)blocks, kSummaryWarps * 32, 0, stream>>>(a, live_ws);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) {
+            set_error("mask summary kernel launch: %s", cudaGetErrorString(e));
+            return 3;
+        }
+        count_launch();
+        a.live = live_ws;
+    }
     if (order_ws != nullptr) {
-        auto ok = paged ? unit_order_kernel<true> : unit_order_kernel<false>;
+        auto ok = masked ? unit_order_kernel<2> : paged ? unit_order_kernel<1> : unit_order_kernel<0>;
         ok<<<1, kOrderThreads, 0, stream>>>(a, order_ws);
         e = cudaGetLastError();
         if (e != cudaSuccess) {
@@ -1050,7 +1196,8 @@ int launch_t(const AttnParams &p, bool bf16, cudaStream_t stream, int *order_ws)
         count_launch();
         a.order = order_ws;
     }
-    auto kern = paged ? prefill_tc_kernel<T, D, DV, true> : prefill_tc_kernel<T, D, DV, false>;
+    auto kern = masked ? prefill_tc_kernel<T, D, DV, 2>
+                       : paged ? prefill_tc_kernel<T, D, DV, 1> : prefill_tc_kernel<T, D, DV, 0>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
     if (e != cudaSuccess) {
         set_error("prefill kernel: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
@@ -1069,7 +1216,8 @@ int launch_t(const AttnParams &p, bool bf16, cudaStream_t stream, int *order_ws)
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = a.order != nullptr ? 1 : 0;  // after the order kernel: overlap its run
+    // after the order / mask summary kernel: overlap their run
+    cfg.numAttrs = (a.order != nullptr || a.live != nullptr) ? 1 : 0;
     e = cudaLaunchKernelEx(&cfg, kern, a, tq, tk, tv, to);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
@@ -1081,13 +1229,14 @@ int launch_t(const AttnParams &p, bool bf16, cudaStream_t stream, int *order_ws)
 }
 
 template <typename T>
-int launch_dtype(const AttnParams &p, bool bf16, cudaStream_t stream, int *order_ws) {
+int launch_dtype(const AttnParams &p, bool bf16, cudaStream_t stream, int *order_ws,
+                 uint8_t *live_ws) {
     // tiles padded to 64 or 128 columns
     const bool d128 = p.D > 64, dv128 = p.Dv > 64;
-    if (d128 && dv128) return launch_t<T, 128, 128>(p, bf16, stream, order_ws);
-    if (!d128 && !dv128) return launch_t<T, 64, 64>(p, bf16, stream, order_ws);
-    if (d128) return launch_t<T, 128, 64>(p, bf16, stream, order_ws);
-    return launch_t<T, 64, 128>(p, bf16, stream, order_ws);
+    if (d128 && dv128) return launch_t<T, 128, 128>(p, bf16, stream, order_ws, live_ws);
+    if (!d128 && !dv128) return launch_t<T, 64, 64>(p, bf16, stream, order_ws, live_ws);
+    if (d128) return launch_t<T, 128, 64>(p, bf16, stream, order_ws, live_ws);
+    return launch_t<T, 64, 128>(p, bf16, stream, order_ws, live_ws);
 }
 
 long long unit_count(const AttnParams &p) {
@@ -1106,16 +1255,27 @@ bool prefill_tc_supported(const AttnParams &p, int dtype) {
     const long long keys = (p.cu_q || p.block_table) ? p.Tk : (long long)p.K;
     // paged K/V: a 128-key tile must lie in one page
     if (p.block_table && p.page_size % kBN != 0) return false;
+    // an arbitrary mask: padded layout, contiguous K/V
+    if (p.mask_bits && (p.block_table || p.cu_q)) return false;
     // work units are indexed in 32 bits
     return rows < (1LL << 31) && keys < (1LL << 31) && unit_count(p) < (1LL << 31);
 }
 
 long long prefill_tc_order_len(const AttnParams &p) {
-    // ragged problems (packed, or padded with per-sequence lengths) of a size
-    // the one-block sort handles in a few microseconds
-    const bool ragged = p.cu_q != nullptr || p.seqlens_q != nullptr || p.seqlens_k != nullptr;
+    // ragged problems (packed, or padded with per-sequence lengths, or an
+    // arbitrary mask) of a size the one-block sort handles in a few microseconds
+    const bool ragged = p.cu_q != nullptr || p.seqlens_q != nullptr || p.seqlens_k != nullptr ||
+                        p.mask_bits != nullptr;
     const long long n = unit_count(p);
     return (ragged && n > 1 && n <= (1LL << 16)) ? n : 0;
+}
+
+long long prefill_tc_live_len(const AttnParams &p) {
+    if (p.mask_bits == nullptr) return 0;
+    const int gp = pack_factor(p.G), qp = kBM / gp;
+    const long long nqblk = (p.Q + 2 * qp - 1) / (2 * qp);
+    const long long rows = p.mask_heads == 1 ? (long long)p.B * nqblk : unit_count(p);
+    return rows * ((p.K + kBN - 1) / kBN);
 }
 
 int make_tma_map_4d(CUtensorMap *map, const void *ptr, bool bf16, uint64_t d0, uint64_t d1,
@@ -1125,9 +1285,10 @@ int make_tma_map_4d(CUtensorMap *map, const void *ptr, bool bf16, uint64_t d0, u
                     d1, d2, d3, b1, b2);
 }
 
-int launch_prefill_tc(const AttnParams &p, int dtype, cudaStream_t stream, int *order_ws) {
-    if (dtype == 2) return launch_dtype<__nv_bfloat16>(p, true, stream, order_ws);
-    return launch_dtype<__half>(p, false, stream, order_ws);
+int launch_prefill_tc(const AttnParams &p, int dtype, cudaStream_t stream, int *order_ws,
+                      uint8_t *live_ws) {
+    if (dtype == 2) return launch_dtype<__nv_bfloat16>(p, true, stream, order_ws, live_ws);
+    return launch_dtype<__half>(p, false, stream, order_ws, live_ws);
 }
 
 }  // namespace attn

@@ -45,9 +45,12 @@ int launch_decode(const AttnParams &p, int dtype, cudaStream_t stream);
 // tcgen05/TMEM prefill (bf16/fp16, D and Dv multiples of 16 in [64, 128]).
 bool prefill_tc_supported(const AttnParams &p, int dtype);
 // Ints of workspace the launch wants for its longest-first unit order (0: the
-// natural order is used); order_ws holds that many, or is null.
+// natural order is used), and bytes for the live-tile flags of an arbitrary
+// mask (0: no mask); order_ws / live_ws hold that many, or are null.
 long long prefill_tc_order_len(const AttnParams &p);
-int launch_prefill_tc(const AttnParams &p, int dtype, cudaStream_t stream, int *order_ws);
+long long prefill_tc_live_len(const AttnParams &p);
+int launch_prefill_tc(const AttnParams &p, int dtype, cudaStream_t stream, int *order_ws,
+                      uint8_t *live_ws);
 
 // mma.sync forward (bf16/fp16, D and Dv multiples of 8 up to 512): the
 // tensor-core path for head widths the tcgen05 prefill kernel does not take.

@@ -203,6 +203,35 @@ ATTN_API int attn_fwd_paged(const void *q, const void *k_pages, const void *v_pa
                             attn_stream_t stream);
 
 /*
+ * attn_fwd_masked -- attn_fwd_ex with an arbitrary boolean mask on top of the
+ * mask mode and the window: key k is legal for query row q of sequence b and
+ * query head h only if it is legal under `mask` / `window` and bit k % 32 of
+ * word k / 32 of mask row ((b * mask_heads + hm) * Q + q) is set, where hm = h
+ * when mask_heads == Hq and hm = 0 when mask_heads == 1 (one mask shared by
+ * every head).  ATTN_MASK_NONE with this mask gives a purely arbitrary mask.
+ * "Attention execution mapping" (LuisaCompute), section 7, names arbitrary
+ * masks as a semantic extension beyond the pages' bottom-right rule; the rest
+ * of the definition (the online softmax over the legal keys, +0 / -inf for a
+ * row without one) is unchanged.
+ *   mask_bits   uint32 [B, mask_heads, Q, mask_words] on the device, 16-byte
+ *               aligned; bits of keys at or past a sequence's length are ignored
+ *   mask_words  words per row: a multiple of 4, at least 4 * ceil(K / 128)
+ *   mask_heads  1 or Hq
+ * Padded layout only; other arguments as attn_fwd_ex.  The tcgen05 prefill
+ * (ATTN_ALGO_AUTO's choice for bf16/fp16 widths 64..128) skips 128-key tiles in
+ * which no row of a work unit has an allowed key, without loading them; the
+ * CUDA-core kernel (ATTN_ALGO_GENERIC, and AUTO otherwise) tests every key.
+ * ATTN_ALGO_DECODE and ATTN_ALGO_MMA return ATTN_ERR_UNSUPPORTED.  Extra
+ * workspace from the library's pool: ceil(K / 128) bytes per query block and
+ * head group.  Return codes as attn_fwd.
+ */
+ATTN_API int attn_fwd_masked(const void *q, const void *k, const void *v, void *o, float *lse,
+                             int B, int Hq, int Hkv, int Q, int K, int D, int Dv,
+                             const int32_t *seqlens_q, const int32_t *seqlens_k,
+                             const uint32_t *mask_bits, int mask_words, int mask_heads, int window,
+                             float scale, int mask, int dtype, int algo, attn_stream_t stream);
+
+/*
  * attn_fwd_decode_noalloc -- attn_fwd's split-KV decode for callers that may
  * not allocate device memory while attention runs: for example a serving
  * process whose device memory is owned by another runtime's allocator or held

@@ -147,3 +147,36 @@ def test_noalloc_clears_the_last_error(lib):
     assert lib.attn_last_error().decode() != ""
     assert _call_noalloc(lib, B=0) == 0  # nothing to do: no CUDA call
     assert lib.attn_last_error().decode() == ""
+
+
+def _call_masked(lib, mask_bits=1 << 24, mask_words=4, mask_heads=1, K=100, Hq=4):
+    vp = ctypes.c_void_p
+    return lib.attn_fwd_masked(vp(1 << 20), vp(1 << 21), vp(1 << 22), vp(1 << 23), None, 1, Hq,
+                               2, 8, K, 64, 64, None, None, vp(mask_bits), mask_words,
+                               mask_heads, 0, 0.125, 2, 2, 0, None)
+
+
+@pytest.mark.parametrize("kw,needle", [
+    (dict(mask_bits=0), "non-null"),
+    (dict(mask_bits=(1 << 24) + 4), "aligned"),
+    (dict(mask_words=3), "multiple of 4"),
+    (dict(mask_words=4, K=200), "at least"),
+    (dict(mask_heads=2), "mask_heads"),
+])
+def test_masked_rejects_on_host(lib, kw, needle):
+    assert _call_masked(lib, **kw) == 1
+    assert needle in lib.attn_last_error().decode()
+
+
+def test_pack_mask_bit_layout():
+    # bit k % 32 of word k // 32 of a row is key k; rows padded to 128 keys
+    import torch
+    g = torch.Generator().manual_seed(5)
+    allow = torch.rand((2, 3, 5, 130), generator=g) < 0.4
+    words = attn.pack_mask(allow)
+    assert words.shape == (2, 3, 5, 8) and words.dtype == torch.int32
+    w = words.to(torch.int64) & 0xFFFFFFFF
+    k = torch.arange(130)
+    bits = (w[..., k // 32] >> (k % 32)) & 1
+    assert torch.equal(bits.bool(), allow)
+    assert torch.all(w[..., 5:] == 0) and torch.all((w[..., 4] >> 2) == 0)
