@@ -386,6 +386,41 @@ def measure_small_configs(args, world, rank, dev, stream, flush, attn, synth):
     return out
 
 
+MASKED = dict(B=4, Hq=32, Hkv=8, Q=4096, K=4096, D=128, Dv=128, qblock=64, density=0.5)
+MASKED_NAME = ("bf16 causal prefill B=4 Hq=32 Hkv=8 Q=K=4096 D=Dv=128 AND a block-sparse mask "
+               "shared by the heads (64 x 128 blocks, each allowed with probability 0.5)")
+
+
+def measure_masked(args, world, rank, dev, stream, flush, attn, synth, pin):
+    """attn_fwd_masked on the prefill workload with a seeded block-sparse mask:
+    TFLOP/s over the legal pairs (causal AND the mask), FLOP = pairs x (2D + 2Dv)."""
+    M = MASKED
+    q, k, v = pin.q.to(dev), pin.k.to(dev), pin.v.to(dev)
+    g = np.random.default_rng(555 + rank)
+    nq, nk = M["Q"] // M["qblock"], M["K"] // 128
+    blocks = g.random((M["B"], 1, nq, nk)) < M["density"]
+    allow = np.repeat(np.repeat(blocks, M["qblock"], axis=2), 128, axis=3)
+    causal = np.tril(np.ones((M["Q"], M["K"]), bool), k=M["K"] - M["Q"])
+    pairs = int(np.logical_and(allow[:, 0], causal[None]).sum()) * M["Hq"]
+    flop = pairs * (2 * M["D"] + 2 * M["Dv"])
+    words = attn.pack_mask(torch.from_numpy(allow)).to(dev)
+    o = torch.empty((M["B"], M["Q"], M["Hq"], M["Dv"]), dtype=q.dtype, device=dev)
+    lse = torch.empty((M["B"], M["Q"], M["Hq"]), dtype=torch.float32, device=dev)
+
+    def run():
+        attn.attn_fwd_masked(q, k, v, words, o, lse, mask="causal", stream=stream)
+
+    run()
+    torch.cuda.synchronize()
+    n0 = attn.kernel_launches()
+    steps = max(3, args.steps // 4)
+    times = time_steps(run, steps, 3, flush, stream)
+    launches = (attn.kernel_launches() - n0) // (steps + 3)
+    ms = max_over_ranks(sum(times) / len(times), world)
+    return dict(flop=flop, ms=ms, steps=steps, launches=launches,
+                density=float(blocks.mean()))
+
+
 WIDE = [dict(B=2, Hq=16, Hkv=4, Q=4096, K=4096, D=256, Dv=256),
         dict(B=1, Hq=16, Hkv=4, Q=4096, K=4096, D=512, Dv=512)]
 
@@ -467,6 +502,25 @@ def run_gpu(args, world, rank, local):
                            "gpu_launches": bwd["gpu_launches"]})
         else:
             result["backward"] = bwd
+    if args.only in ("all", "masked"):
+        if pin is None:
+            pin = synth.prefill_bf16_b4_h32x8_s4096_d128(seed=1234 + rank)
+        mk = measure_masked(args, world, rank, dev, stream, flush, attn, synth, pin)
+        tfm = mk["flop"] / (mk["ms"] * 1e-3) / 1e12
+        result["masked"] = {
+            "workload": MASKED_NAME, "value": round(world * tfm, 3), "unit": "TFLOP/s",
+            "ms_per_step": round(mk["ms"], 5), "steps": mk["steps"], "flop_per_step": mk["flop"],
+            "block_density": round(mk["density"], 4), "gpu_launches": int(mk["launches"] * mk["steps"]),
+            "kernels": "mask_summary_kernel + unit_order_kernel + prefill_tc_kernel (dead tiles skipped)",
+            "roofline": {"bound": "tensor", "achieved": round(tfm, 3), "peak": tf_peak,
+                         "unit": "TFLOP/s", "frac": round(tfm / tf_peak, 4),
+                         "traffic": traffic.get("masked"),
+                         "peak_source": f"{peak_src} bf16 dense (cuBLAS burst)"}}
+        if args.only == "masked":
+            result.update({"value": result["masked"]["value"], "unit": "TFLOP/s",
+                           "ms_per_step": result["masked"]["ms_per_step"],
+                           "config": {"workload": MASKED_NAME},
+                           "roofline": result["masked"]["roofline"]})
     small = None
     if args.only in ("all", "configs"):
         small = measure_small_configs(args, world, rank, dev, stream, flush, attn, synth)
@@ -548,6 +602,7 @@ def run_gpu(args, world, rank, local):
 KERNEL_SOURCES = {
     "prefill": "causal_gqa_attention_online_gb300/csrc/kernel_prefill_tc.cu",
     "varlen": "causal_gqa_attention_online_gb300/csrc/kernel_prefill_tc.cu",
+    "masked": "causal_gqa_attention_online_gb300/csrc/kernel_prefill_tc.cu",
     "decode": "causal_gqa_attention_online_gb300/csrc/kernel_decode.cu",
     "backward": ("causal_gqa_attention_online_gb300/csrc/kernel_bwd.cu",
                  "causal_gqa_attention_online_gb300/csrc/kernel_bwd_tc.cu"),
@@ -703,7 +758,7 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=60.0,
                     help="--impl reference: total seconds of oracle work over all steps")
     ap.add_argument("--only", default="all",
-                    choices=["all", "prefill", "decode", "backward", "wide", "configs"],
+                    choices=["all", "prefill", "decode", "backward", "wide", "configs", "masked"],
                     help="profiling aid: run one workload (the JSON line then lacks the other)")
     args = ap.parse_args()
     if args.warmup < 3:

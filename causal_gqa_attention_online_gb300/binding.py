@@ -25,9 +25,9 @@ MASKS = {"causal": 0, "causal_top_left": 1, "none": 2}
 _DTYPE_CODE = {torch.float32: ATTN_F32, torch.float16: ATTN_F16, torch.bfloat16: ATTN_BF16}
 
 EXPORTED = ("attn_fwd", "attn_fwd_varlen", "attn_fwd_algo", "attn_fwd_varlen_algo",
-            "attn_fwd_ex", "attn_fwd_varlen_ex", "attn_fwd_paged", "attn_fwd_masked", "attn_bwd",
-            "attn_bwd_varlen",
-            "attn_lse_combine", "attn_fwd_decode_noalloc", "attn_fwd_staged", "attn_last_error",
+            "attn_fwd_ex", "attn_fwd_varlen_ex", "attn_fwd_paged", "attn_fwd_masked",
+            "attn_bwd", "attn_bwd_varlen", "attn_lse_combine", "attn_lse_combine_ex",
+            "attn_fwd_decode_noalloc", "attn_fwd_staged", "attn_last_error",
             "attn_device_status", "attn_set_wait_limit", "attn_kernel_launches", "attn_version")
 
 _lock = threading.Lock()
@@ -87,6 +87,8 @@ def load_library(path: str | None = None):
         lib.attn_bwd_varlen.argtypes = [vp] * 9 + [ip] * 9 + [vp, vp, ip, fp, ip, ip, ip, vp]
         lib.attn_lse_combine.argtypes = [vp, vp, vp, vp, ip, ctypes.c_longlong, ip, ip, vp]
         lib.attn_lse_combine.restype = ip
+        lib.attn_lse_combine_ex.argtypes = [vp, vp, vp, vp, ip, ctypes.c_longlong, ip, ip, ip, vp]
+        lib.attn_lse_combine_ex.restype = ip
         lib.attn_last_error.argtypes = []
         lib.attn_last_error.restype = ctypes.c_char_p
         lib.attn_device_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
@@ -325,6 +327,26 @@ def attn_lse_combine(o_parts, lse_parts, o=None, lse=None, *, dtype=torch.float3
     _check_tensor("o", o, o.dtype, rows * Dv, dev)
     rc = lib.attn_lse_combine(_ptr(o_parts), _ptr(lse_parts), _ptr(o), _ptr(lse), S, rows, Dv,
                               _DTYPE_CODE[o.dtype], _stream_ptr(stream))
+    _check(rc)
+    return o, lse
+
+
+def attn_lse_combine_parts(o_parts, lse_parts, o=None, lse=None, *, stream=None):
+    """Merge partials [S, rows, Dv] in their storage dtype (fp32, fp16 or bf16;
+    as attn_fwd wrote them) by their LSE [S, rows]; o is in that dtype."""
+    lib = load_library()
+    S, rows, Dv = o_parts.shape
+    dev = o_parts.device
+    if o is None:
+        o = torch.empty((rows, Dv), dtype=o_parts.dtype, device=dev)
+    if lse is None:
+        lse = torch.empty((rows,), dtype=torch.float32, device=dev)
+    _check_tensor("o_parts", o_parts, o_parts.dtype, S * rows * Dv, dev)
+    _check_tensor("lse_parts", lse_parts, torch.float32, S * rows, dev)
+    _check_tensor("o", o, o_parts.dtype, rows * Dv, dev)
+    code = _DTYPE_CODE[o_parts.dtype]
+    rc = lib.attn_lse_combine_ex(_ptr(o_parts), _ptr(lse_parts), _ptr(o), _ptr(lse), S, rows, Dv,
+                                 code, code, _stream_ptr(stream))
     _check(rc)
     return o, lse
 

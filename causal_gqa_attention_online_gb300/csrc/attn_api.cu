@@ -630,6 +630,31 @@ int attn_lse_combine(const float *o_parts, const float *lse_parts, void *o, floa
                                reinterpret_cast<cudaStream_t>(stream));
 }
 
+int attn_lse_combine_ex(const void *o_parts, const float *lse_parts, void *o, float *lse,
+                        int nsplit, long long rows, int Dv, int parts_dtype, int dtype,
+                        attn_stream_t stream) {
+    clear_error();
+    if (parts_dtype == ATTN_F32)
+        return attn_lse_combine(static_cast<const float *>(o_parts), lse_parts, o, lse, nsplit,
+                                rows, Dv, dtype, stream);
+    if (nsplit < 1 || rows < 0 || Dv < 1 || Dv > 4096 || parts_dtype < ATTN_F32 ||
+        parts_dtype > ATTN_BF16 || dtype < ATTN_F32 || dtype > ATTN_BF16) {
+        attn::set_error("attn_lse_combine_ex: bad size or dtype (nsplit=%d rows=%lld Dv=%d)",
+                        nsplit, rows, Dv);
+        return ATTN_ERR_INVALID;
+    }
+    if (rows > 0 && (o_parts == nullptr || lse_parts == nullptr || o == nullptr)) {
+        attn::set_error("attn_lse_combine_ex: null pointer");
+        return ATTN_ERR_INVALID;
+    }
+    if (rows > (1LL << 40)) {
+        attn::set_error("attn_lse_combine_ex: too many rows");
+        return ATTN_ERR_UNSUPPORTED;
+    }
+    return launch_combine_parts(o_parts, parts_dtype, lse_parts, o, lse, nsplit, rows, Dv, dtype,
+                                reinterpret_cast<cudaStream_t>(stream));
+}
+
 int attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
              const void *dout, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int Q, int K,
              int D, int Dv, const int32_t *seqlens_q, const int32_t *seqlens_k, int window,

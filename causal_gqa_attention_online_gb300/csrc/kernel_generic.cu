@@ -447,6 +447,67 @@ int launch_combine_rows(const AttnParams &p, int dtype, cudaStream_t stream) {
     return 0;
 }
 
+// One warp per row, partials in a 16-bit storage type P (the merge of the
+// key shards of several ranks, exchanged as they were written).
+template <typename P, typename T>
+__global__ void __launch_bounds__(128) combine_parts_kernel(const P *o_parts,
+                                                            const float *lse_parts, T *o,
+                                                            float *lse, int nsplit,
+                                                            long long rows, int Dv) {
+    const int lane = threadIdx.x & 31;
+    const long long row = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    float mx = -INFINITY;
+    for (int s = lane; s < nsplit; s += 32) mx = fmaxf(mx, lse_parts[s * rows + row]);
+    mx = warp_max(mx);
+    T *orow = o + row * Dv;
+    if (mx == -INFINITY) {
+        for (int c = lane; c < Dv; c += 32) orow[c] = from_f32<T>(0.f);
+        if (lane == 0 && lse) lse[row] = -INFINITY;
+        return;
+    }
+    float wsum = 0.f;
+    for (int s = lane; s < nsplit; s += 32) wsum += exp2f((lse_parts[s * rows + row] - mx) * kLog2e);
+    wsum = warp_sum(wsum);
+    const float inv = 1.f / wsum;
+    for (int c = lane; c < Dv; c += 32) {
+        float a = 0.f;
+        for (int s = 0; s < nsplit; ++s) {
+            const float w = exp2f((lse_parts[s * rows + row] - mx) * kLog2e);
+            a = fmaf(w, to_f32(o_parts[(s * rows + row) * Dv + c]), a);
+        }
+        orow[c] = from_f32<T>(a * inv);
+    }
+    if (lane == 0 && lse) lse[row] = mx + __logf(wsum);
+}
+
+int launch_combine_parts(const void *o_parts, int parts_dtype, const float *lse_parts, void *o,
+                         float *lse, int nsplit, long long rows, int Dv, int dtype,
+                         cudaStream_t stream) {
+    if (rows == 0) return 0;
+    const unsigned blocks = (unsigned)((rows + 3) / 4);
+    if (parts_dtype == 1 && dtype == 1)
+        combine_parts_kernel<__half, __half><<<blocks, 128, 0, stream>>>(
+            static_cast<const __half *>(o_parts), lse_parts, static_cast<__half *>(o), lse,
+            nsplit, rows, Dv);
+    else if (parts_dtype == 2 && dtype == 2)
+        combine_parts_kernel<__nv_bfloat16, __nv_bfloat16><<<blocks, 128, 0, stream>>>(
+            static_cast<const __nv_bfloat16 *>(o_parts), lse_parts,
+            static_cast<__nv_bfloat16 *>(o), lse, nsplit, rows, Dv);
+    else {
+        set_error("combine: 16-bit partials combine into the same dtype (parts %d, out %d)",
+                  parts_dtype, dtype);
+        return 2;
+    }
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("combine kernel launch: %s", cudaGetErrorString(e));
+        return 3;
+    }
+    count_launch();
+    return 0;
+}
+
 int launch_combine_flat(const float *o_parts, const float *lse_parts, void *o, float *lse,
                         int nsplit, long long rows, int Dv, int dtype, cudaStream_t stream) {
     if (rows == 0) return 0;

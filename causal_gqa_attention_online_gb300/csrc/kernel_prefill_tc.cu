@@ -96,11 +96,12 @@ struct PrefillArgs {
     // first (written by unit_order_kernel); null: the natural order, which is
     // longest-first already when every sequence has the same lengths.
     const int *order;
-    // Arbitrary mask: live[row * live_tiles + T] != 0 when 128-key tile T has
-    // a key that some row of the unit may attend to (written by
-    // mask_summary_kernel); a row is one (sequence, query block) when the mask
-    // is shared by all heads, else one unit (its natural index).  Dead tiles
-    // are neither loaded nor multiplied.
+    // Arbitrary mask: live[row * live_tiles + T] is 0 when no row of the unit
+    // may attend to a key of 128-key tile T (a dead tile: neither loaded nor
+    // multiplied), 2 when every real row may attend to all of its keys (the
+    // mask bits need not be read), 1 otherwise (written by mask_summary_kernel);
+    // a row is one (sequence, query block) when the mask is shared by all
+    // heads, else one unit (its natural index).
     const uint8_t *live;
     int live_tiles;   // ceil(K / 128)
     int live_shared;  // 1: the mask is shared by all heads
@@ -692,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // an arbitrary mask: this row's 128 bits of the tile (k0 is a multiple
                 // of 128, the row a multiple of four words), fetched before the waits
                 uint4 mw = make_uint4(~0u, ~0u, ~0u, ~0u);
-                if (MASKED) {
+                if (MASKED && lv[j] != 2) {
                     mw = make_uint4(0u, 0u, 0u, 0u);
                     if (mrow != nullptr)
                         mw = __ldg(reinterpret_cast<const uint4 *>(mrow + (x.kv_start + j * kBN) / 32));
@@ -823,8 +824,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < x.n_kv && ok; ++j) {
                 if (MASKED && lv[j] == 0) continue;  // a dead tile: not computed
                 const int k0 = x.kv_start + j * kBN;
-                const bool interior =
-                    !MASKED && x.all_valid && k0 >= x.lo_last && k0 + kBN <= x.hi_first;
+                // (a live tile every row may attend to whole is masked as unmasked)
+                const bool interior = (!MASKED || lv[j] == 2) && x.all_valid && k0 >= x.lo_last &&
+                                      k0 + kBN <= x.hi_first;
                 ok = tile_step(j, interior);
             }
             if (!ok) break;
@@ -1059,15 +1061,17 @@ __global__ void __launch_bounds__(kSummaryWarps * 32) mask_summary_kernel(const 
         nh = a.Gp;
     }
     const int Qb = seq_info(p, b).Qb;
-    uint32_t any = 0;
+    uint32_t any = 0, all = 0xffffffffu;
     for (int r = lane; r < 2 * a.QP * nh; r += 32) {
         const int pos = q0 + r / nh;
         if (pos >= Qb) continue;
         const uint4 m = __ldg(reinterpret_cast<const uint4 *>(mask_row(p, b, h0 + r % nh, pos)) + tile);
         any |= m.x | m.y | m.z | m.w;
+        all &= m.x & m.y & m.z & m.w;
     }
-    any = __any_sync(0xffffffffu, any != 0);
-    if (lane == 0) live[w] = any ? 1 : 0;
+    const bool some = __any_sync(0xffffffffu, any != 0);
+    const bool full = __all_sync(0xffffffffu, all == 0xffffffffu);
+    if (lane == 0) live[w] = some ? (full ? 2 : 1) : 0;
 }
 
 // ------------------------------------------------------------------ host

@@ -38,6 +38,10 @@ int launch_combine_rows(const AttnParams &p, int dtype, cudaStream_t stream);
 // Plain [nsplit, rows, Dv] merge for attn_lse_combine.
 int launch_combine_flat(const float *o_parts, const float *lse_parts, void *o, float *lse,
                         int nsplit, long long rows, int Dv, int dtype, cudaStream_t stream);
+// The same merge with fp16 / bf16 partials (parts_dtype == dtype).
+int launch_combine_parts(const void *o_parts, int parts_dtype, const float *lse_parts, void *o,
+                         float *lse, int nsplit, long long rows, int Dv, int dtype,
+                         cudaStream_t stream);
 // Tensor-core split-KV decode (bf16/fp16, Q*G <= 16).  Honours p.nsplit.
 bool decode_supported(const AttnParams &p, int dtype);
 int decode_split_len(const AttnParams &p, int nsm);

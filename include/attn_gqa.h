@@ -182,6 +182,19 @@ ATTN_API int attn_lse_combine(const float *o_parts, const float *lse_parts, void
                      int nsplit, long long rows, int Dv, int dtype, attn_stream_t stream);
 
 /*
+ * attn_lse_combine_ex -- attn_lse_combine with the partials in any storage
+ * dtype: parts_dtype ATTN_F32 is attn_lse_combine; ATTN_F16 / ATTN_BF16 take
+ * o_parts [nsplit, rows, Dv] in that dtype (as attn_fwd wrote them, each
+ * normalised by its own sum) and need dtype == parts_dtype.  This merges the
+ * outputs of one sequence's key shards computed on several GPUs and exchanged
+ * as they are (the sharded decode of the Python package).  Accumulation is in
+ * fp32; return codes as attn_lse_combine.
+ */
+ATTN_API int attn_lse_combine_ex(const void *o_parts, const float *lse_parts, void *o, float *lse,
+                                 int nsplit, long long rows, int Dv, int parts_dtype, int dtype,
+                                 attn_stream_t stream);
+
+/*
  * attn_fwd_paged -- attn_fwd with the keys and values in pages: a serving
  * layout (the pages have no counterpart; the attention itself is unchanged).
  *   q [B, Q, Hq, D], o [B, Q, Hq, Dv], lse [B, Q, Hq] as in attn_fwd.
