@@ -223,7 +223,7 @@ int run(AttnParams &p, int dtype, int algo, cudaStream_t stream) {
         if (dtype != ATTN_F32) {
             if (!masked && decode_supported(p, dtype))
                 chosen = ATTN_ALGO_DECODE;
-            else if (prefill_tc_supported(p, dtype))
+            else if (prefill_tc_supported(p, dtype) || prefill_wide_tc_supported(p, dtype))
                 chosen = ATTN_ALGO_TCGEN05;
             else if (!masked && fwd_mma_supported(p, dtype))
                 chosen = ATTN_ALGO_MMA;
@@ -231,7 +231,8 @@ int run(AttnParams &p, int dtype, int algo, cudaStream_t stream) {
     } else if (algo == ATTN_ALGO_DECODE && !decode_supported(p, dtype)) {
         set_error("decode kernel does not take this shape/dtype");
         return ATTN_ERR_UNSUPPORTED;
-    } else if (algo == ATTN_ALGO_TCGEN05 && !prefill_tc_supported(p, dtype)) {
+    } else if (algo == ATTN_ALGO_TCGEN05 && !prefill_tc_supported(p, dtype) &&
+               !prefill_wide_tc_supported(p, dtype)) {
         set_error("tcgen05 prefill kernel does not take this shape/dtype");
         return ATTN_ERR_UNSUPPORTED;
     } else if (algo == ATTN_ALGO_MMA && !fwd_mma_supported(p, dtype)) {
@@ -239,6 +240,8 @@ int run(AttnParams &p, int dtype, int algo, cudaStream_t stream) {
         return ATTN_ERR_UNSUPPORTED;
     }
 
+    if (chosen == ATTN_ALGO_TCGEN05 && !prefill_tc_supported(p, dtype))
+        return launch_prefill_wide_tc(p, dtype, stream);
     if (chosen == ATTN_ALGO_TCGEN05) {
         // workspace: the unit order (ints), then the live-tile flags of a mask
         const long long n = prefill_tc_order_len(p), nlive = prefill_tc_live_len(p);

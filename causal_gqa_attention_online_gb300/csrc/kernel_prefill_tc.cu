@@ -46,11 +46,13 @@
 #include "common.cuh"
 #include "launch.h"
 #include "sm100_ptx.cuh"
+#include "tc_softmax.cuh"
 
 namespace attn {
 namespace {
 
 using namespace sm100;
+using namespace tcfwd;
 
 constexpr int kBM = 128;  // rows per Q tile (MMA M)
 constexpr int kBN = 128;  // keys per KV tile
@@ -225,60 +227,6 @@ __device__ __forceinline__ int count_live(const uint8_t *lv, int n_kv, int *last
             *last = j;
         }
     return n;
-}
-
-template <typename T> __device__ __forceinline__ uint32_t pack2(float lo, float hi);
-template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-template <> __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
-    __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-    float r;
-    asm("max.f32 %0, %1, %2, %3;\n" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-    return r;
-}
-
-// Packed fp32 pairs (two lanes of work per instruction on sm_100+).
-__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};\n" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void f2unpack(uint64_t v, float &lo, float &hi) {
-    asm("mov.b64 {%0, %1}, %2;\n" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("add.rn.f32x2 %0, %1, %2;\n" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-
-// 2^x on the MUFU unit (flushes subnormal results to zero; 2^-inf = +0)
-__device__ __forceinline__ float ex2(float x) {
-    float r;
-    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(r) : "f"(x));
-    return r;
-}
-
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          uint64_t limit_ns) {
-    const bool ok = mbar_wait(bar, parity, abort_flag, limit_ns);
-    return __all_sync(0xffffffffu, ok);
-}
-
-__device__ __forceinline__ void raise_abort(volatile int *abort_flag, int *status, int code) {
-    *abort_flag = 1;
-    report_status(status, code);
 }
 
 // D, DV: the tile widths (64 or 128 columns); the real head dims p.D <= D and

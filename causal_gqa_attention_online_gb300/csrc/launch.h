@@ -56,6 +56,11 @@ long long prefill_tc_live_len(const AttnParams &p);
 int launch_prefill_tc(const AttnParams &p, int dtype, cudaStream_t stream, int *order_ws,
                       uint8_t *live_ws);
 
+// tcgen05/TMEM prefill for head widths above 128 (bf16/fp16, D and Dv multiples
+// of 16 in [64, 256], at least one above 128; not paged, no arbitrary mask).
+bool prefill_wide_tc_supported(const AttnParams &p, int dtype);
+int launch_prefill_wide_tc(const AttnParams &p, int dtype, cudaStream_t stream);
+
 // mma.sync forward (bf16/fp16, D and Dv multiples of 8 up to 512): the
 // tensor-core path for head widths the tcgen05 prefill kernel does not take.
 bool fwd_mma_supported(const AttnParams &p, int dtype);

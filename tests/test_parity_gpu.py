@@ -401,7 +401,7 @@ def test_mma_forward_varlen_packed_and_auto_choice():
     sq = np.minimum(sk, np.array([0, 5, 7, 64, 1, 512, 0, 100]))
     for w in (0, 100):
         inp = synth.make_packed(sq, sk, 16, 4, 256, 256, "bf16", seed=39, window=w)
-        parity.check(inp, "auto", f"auto (mma) varlen w={w}")
+        parity.check(inp, "auto", f"auto (tcgen05 wide) varlen w={w}")
 
 
 def test_mma_forward_rejects_fp32_and_wide_heads():
