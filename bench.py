@@ -427,7 +427,8 @@ WIDE = [dict(B=2, Hq=16, Hkv=4, Q=4096, K=4096, D=256, Dv=256),
 
 def measure_wide(args, world, rank, dev, stream, flush, attn, synth):
     """bf16 causal prefill with head widths 256 (the tcgen05 wide-head kernel)
-    and 512 (the mma.sync warp-pair kernel), as attn_fwd chooses them."""
+    and 512 (the tcgen05 kernel with the output columns in halves), as
+    attn_fwd chooses them."""
     out = []
     for W in WIDE:
         inp = synth.make_padded(W["B"], W["Hq"], W["Hkv"], W["Q"], W["K"], W["D"], W["Dv"],
@@ -558,7 +559,8 @@ def run_gpu(args, world, rank, local):
                              f"Q=K={W['Q']} D=Dv={W['D']}"),
                 "value": round(world * tfw, 3), "unit": "TFLOP/s", "ms_per_step": round(ms, 5),
                 "steps": steps, "flop_per_step": flop,
-                "kernel": ("mma.sync m16n8k16 (warp pairs split the width)" if W["D"] > 256
+                "kernel": ("prefill_wide512_tc_kernel (tcgen05, output columns in halves of "
+                           "256, K / V streamed in 16 KB chunks)" if W["D"] > 256
                            else "prefill_wide_tc_kernel (tcgen05, one Q tile, S double-buffered)"),
                 "roofline": {"bound": "tensor", "achieved": round(tfw, 3), "peak": tf_peak,
                              "unit": "TFLOP/s", "frac": round(tfw / tf_peak, 4),
@@ -606,8 +608,10 @@ KERNEL_SOURCES = {
     "decode": "causal_gqa_attention_online_gb300/csrc/kernel_decode.cu",
     "backward": ("causal_gqa_attention_online_gb300/csrc/kernel_bwd.cu",
                  "causal_gqa_attention_online_gb300/csrc/kernel_bwd_tc.cu"),
-    "wide256": "causal_gqa_attention_online_gb300/csrc/kernel_prefill_wide_tc.cu",
-    "wide512": "causal_gqa_attention_online_gb300/csrc/kernel_fwd_mma.cu",
+    "wide256": ("causal_gqa_attention_online_gb300/csrc/kernel_prefill_wide_tc.cu",
+                "causal_gqa_attention_online_gb300/csrc/wide_common.cuh"),
+    "wide512": ("causal_gqa_attention_online_gb300/csrc/kernel_prefill_wide512_tc.cu",
+                "causal_gqa_attention_online_gb300/csrc/wide_common.cuh"),
 }
 
 

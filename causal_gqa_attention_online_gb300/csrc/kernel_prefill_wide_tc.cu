@@ -36,12 +36,14 @@
 #include "launch.h"
 #include "sm100_ptx.cuh"
 #include "tc_softmax.cuh"
+#include "wide_common.cuh"
 
 namespace attn {
 namespace {
 
 using namespace sm100;
 using namespace tcfwd;
+using namespace tcwide;
 
 constexpr int kBM = 128;  // rows per Q tile
 constexpr int kBN = 128;  // keys per KV tile
@@ -106,49 +108,8 @@ enum : int {
     W_NBARS = 16,
 };
 
-struct WideUnit {
-    int b, kvh, h0, q0;
-    SeqInfo si;
-    int n_kv, kv_start, lo_last, hi_first, hi_unit;
-    bool all_valid;
-};
-
-__device__ __forceinline__ WideUnit wide_unit(const WideArgs &a, long long u64) {
-    const AttnParams &p = a.p;
-    const uint32_t u = (uint32_t)u64;
-    const uint32_t qi = u / a.per, rest = u - qi * a.per;
-    const uint32_t b = rest / a.hs, r2 = rest - b * a.hs;
-    const uint32_t kvh = r2 / (uint32_t)a.nsub, sub = r2 - kvh * (uint32_t)a.nsub;
-    const int qblk = a.nqblk - 1 - (int)qi;  // longest first
-    WideUnit x;
-    x.b = (int)b;
-    x.kvh = (int)kvh;
-    x.h0 = x.kvh * p.G + (int)sub * a.Gp;
-    x.q0 = qblk * a.QP;
-    x.si = seq_info(p, x.b);
-    x.n_kv = 0;
-    x.kv_start = 0;
-    x.lo_last = INT_MAX;
-    x.hi_first = INT_MIN;
-    x.hi_unit = 0;
-    x.all_valid = false;
-    if (x.q0 >= x.si.Qb) return x;
-    const int q_last = min(x.q0 + a.QP, x.si.Qb) - 1;
-    int lo_f, hi_f, lo_l, hi_l;
-    legal_range(x.q0, x.si.Qb, x.si.Kb, p.window, p.mask, lo_f, hi_f);
-    legal_range(q_last, x.si.Qb, x.si.Kb, p.window, p.mask, lo_l, hi_l);
-    if (hi_l <= lo_f) return x;
-    x.kv_start = lo_f;
-    x.hi_unit = hi_l;
-    x.n_kv = (hi_l - lo_f + kBN - 1) / kBN;
-    x.lo_last = lo_l;
-    x.hi_first = hi_f;
-    x.all_valid = x.q0 + a.QP <= x.si.Qb;
-    return x;
-}
-
-__device__ __forceinline__ long long snake(long long r, int c, int G) {
-    return r * G + ((r & 1) ? (G - 1 - c) : c);
+__device__ __forceinline__ QTileUnit wide_unit(const WideArgs &a, long long u64) {
+    return qtile_unit(a.p, a.per, a.hs, a.nsub, a.Gp, a.QP, a.nqblk, (uint32_t)u64);
 }
 
 // Ring positions (relative to the unit's first element) of K_j and V_j in
@@ -232,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (long long rnd = 0; rnd * gridDim.x < a.nunits && ok; ++rnd) {
                     const long long u = snake(rnd, blockIdx.x, gridDim.x);
                     if (u >= a.nunits) continue;
-                    const WideUnit x = wide_unit(a, u);
+                    const QTileUnit x = wide_unit(a, u);
                     if (x.n_kv == 0) continue;
                     const int qrow = (padded ? 0 : (int)x.si.q_off) + x.q0;
                     const int krow = padded ? 0 : (int)x.si.k_off;
@@ -441,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (long long rnd = 0; rnd * gridDim.x < a.nunits && ok; ++rnd) {
             const long long u = snake(rnd, blockIdx.x, gridDim.x);
             if (u >= a.nunits) continue;
-            const WideUnit x = wide_unit(a, u);
+            const QTileUnit x = wide_unit(a, u);
             const int qpos = x.q0 + r / a.Gp;
             const int head = x.h0 + r % a.Gp;
             const bool valid = qpos < x.si.Qb;
@@ -470,101 +431,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t tS = tmem + lane_off + sb * 128u;
                 const int k0 = x.kv_start + j * kBN;
                 const bool interior = x.all_valid && k0 >= x.lo_last && k0 + kBN <= x.hi_first;
-                if (!interior) {
-                    // keys outside [lo, hi) of this row to -inf in TMEM, 32 at a time
-#pragma unroll 1
-                    for (int cc = 0; cc < 4; ++cc) {
-                        const int a0 = min(max(lo - k0 - cc * 32, 0), 32);
-                        const int b0 = min(max(hi - k0 - cc * 32, 0), 32);
-                        const uint32_t below_b = b0 >= 32 ? 0xffffffffu : (1u << b0) - 1u;
-                        const uint32_t below_a = a0 >= 32 ? 0xffffffffu : (1u << a0) - 1u;
-                        const uint32_t keep = below_b & ~below_a;
-                        if (__all_sync(0xffffffffu, keep == 0xffffffffu)) continue;
-                        uint32_t v[32];
-                        tmem_ld32(tS + cc * 32, v);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            v[i] = ((keep >> i) & 1u) ? v[i] : 0xff800000u;
-                        tmem_st32(tS + cc * 32, v);
-                    }
-                    tmem_st_wait();
+                // a rescale first waits for PV(j - 1): its phase of W_PV_DONE
+                if (!softmax_tile<T, DV>(tS, tO, k0, interior, lo, hi, c, m_run, l_run,
+                                         bar(W_PV_DONE), (gt - 2u) & 1u, abort_flag, wl)) {
+                    ok = false;
+                    break;
                 }
-                uint32_t sr[4][32];
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + cc * 32, sr[cc]);
-                tmem_ld_wait();
-                float mc[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mc[i] = -INFINITY;
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        mc[i & 7] = fmax3(mc[i & 7], __uint_as_float(sr[cc][2 * i]),
-                                          __uint_as_float(sr[cc][2 * i + 1]));
-                const float mx = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]),
-                                       fmaxf(mc[6], mc[7]));
-                const float m_tile = mx * c;
-                float alpha = 1.f;
-                bool rescale = false;
-                if (m_run == -INFINITY) {
-                    m_run = m_tile;
-                } else if (m_tile > m_run + 8.f) {
-                    alpha = ex2(m_run - m_tile);
-                    m_run = m_tile;
-                    rescale = true;
-                }
-                const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
-                if (__any_sync(0xffffffffu, rescale)) {
-                    // S(j) was issued before PV(j - 1), so O may still be taking
-                    // PV(j - 1): wait for that tile's phase of W_PV_DONE (PV(j) is
-                    // issued only after this step, so the barrier cannot be two
-                    // phases ahead).  j >= 1 here: the first tile of a unit sets
-                    // the reference max without a rescale.
-                    if (!warp_wait(bar(W_PV_DONE), (gt - 2u) & 1u, abort_flag, wl)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-#pragma unroll
-                    for (int cc = 0; cc < DV / 16; ++cc) {
-                        uint32_t ov[16];
-                        tmem_ld16(tO + cc * 16, ov);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                        tmem_st16(tO + cc * 16, ov);
-                    }
-                }
-                const uint64_t c2 = f2pack(c, c), nm2 = f2pack(neg_m, neg_m);
-                uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int cc = 2 * half; cc < 2 * half + 2; ++cc)
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const uint64_t x2 = ffma2(f2pack(__uint_as_float(sr[cc][2 * i]),
-                                                             __uint_as_float(sr[cc][2 * i + 1])),
-                                                      c2, nm2);
-                            float x0, x1;
-                            f2unpack(x2, x0, x1);
-                            const float p0 = ex2(x0), p1 = ex2(x1);
-                            acc2[i & 3] = fadd2(acc2[i & 3], f2pack(p0, p1));
-                            pk[(cc & 1) * 16 + i] = pack2<T>(p0, p1);
-                        }
-                    tmem_st32(tS + 32 * half, pk);
-                }
-                float sa[8];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) f2unpack(acc2[i], sa[2 * i], sa[2 * i + 1]);
-                const float sum =
-                    ((sa[0] + sa[1]) + (sa[2] + sa[3])) + ((sa[4] + sa[5]) + (sa[6] + sa[7]));
-                l_run = l_run * alpha + sum;
-                tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(bar(W_P_READY + (int)sb));
             }
@@ -593,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (long long rnd = 0; rnd * gridDim.x < a.nunits && ok; ++rnd) {
             const long long u = snake(rnd, blockIdx.x, gridDim.x);
             if (u >= a.nunits) continue;
-            const WideUnit x = wide_unit(a, u);
+            const QTileUnit x = wide_unit(a, u);
             if (x.n_kv == 0) continue;  // the softmax warps wrote those rows
             const int b = (int)(nunit & 1u);
             ++nunit;
@@ -743,6 +615,7 @@ int launch_wide_dtype(const AttnParams &p, bool bf16, cudaStream_t stream) {
 }  // namespace
 
 bool prefill_wide_tc_supported(const AttnParams &p, int dtype) {
+    if (p.D > 256 || p.Dv > 256) return prefill_wide512_tc_supported(p, dtype);
     if (dtype != 1 && dtype != 2) return false;
     if (p.D < 64 || p.D > 256 || p.D % 16 || p.Dv < 64 || p.Dv > 256 || p.Dv % 16) return false;
     if (p.D <= 128 && p.Dv <= 128) return false;  // the two-tile kernel's widths
@@ -755,6 +628,7 @@ bool prefill_wide_tc_supported(const AttnParams &p, int dtype) {
 }
 
 int launch_prefill_wide_tc(const AttnParams &p, int dtype, cudaStream_t stream) {
+    if (p.D > 256 || p.Dv > 256) return launch_prefill_wide512_tc(p, dtype, stream);
     if (dtype == 2) return launch_wide_dtype<__nv_bfloat16>(p, true, stream);
     return launch_wide_dtype<__half>(p, false, stream);
 }

@@ -57,9 +57,12 @@ int launch_prefill_tc(const AttnParams &p, int dtype, cudaStream_t stream, int *
                       uint8_t *live_ws);
 
 // tcgen05/TMEM prefill for head widths above 128 (bf16/fp16, D and Dv multiples
-// of 16 in [64, 256], at least one above 128; not paged, no arbitrary mask).
+// of 16 in [64, 512], at least one above 128; not paged, no arbitrary mask).
+// Widths above 256 go to the 512-wide kernel (output columns in halves).
 bool prefill_wide_tc_supported(const AttnParams &p, int dtype);
 int launch_prefill_wide_tc(const AttnParams &p, int dtype, cudaStream_t stream);
+bool prefill_wide512_tc_supported(const AttnParams &p, int dtype);
+int launch_prefill_wide512_tc(const AttnParams &p, int dtype, cudaStream_t stream);
 
 // mma.sync forward (bf16/fp16, D and Dv multiples of 8 up to 512): the
 // tensor-core path for head widths the tcgen05 prefill kernel does not take.
