@@ -82,7 +82,8 @@ enum attn_algo {
     ATTN_ALGO_AUTO = 0,     /* choose by dtype, head widths and query length */
     ATTN_ALGO_GENERIC = 1,  /* CUDA-core online softmax: any dtype, D, Dv <= 512 */
     ATTN_ALGO_TCGEN05 = 2,  /* tcgen05/TMEM prefill: bf16/fp16, D, Dv multiples of 16 in
-                               [64, 128]; in the backward, the tcgen05 dQ and dK/dV kernels */
+                               [64, 512], not paged above 128; in the backward, the
+                               tcgen05 dQ and dK/dV kernels (D, Dv in [64, 128]) */
     ATTN_ALGO_DECODE = 3,   /* split-KV tensor-core decode: bf16/fp16, Q*G <= 16 */
     ATTN_ALGO_MMA = 4       /* warp-level mma.sync tensor cores, bf16/fp16: the forward for
                                D, Dv multiples of 8 up to 512 (chosen by AUTO where the
