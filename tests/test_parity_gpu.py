@@ -435,8 +435,10 @@ def test_wide_heads_rejected_above_512_and_by_tensor_kernels():
     with pytest.raises(AttnError) as ei:
         parity.run_gpu(inp, "auto")
     assert ei.value.status == 1
-    inp = synth.make_padded(1, 2, 1, 8, 8, 512, 512, "bf16", seed=43)
-    for algo in ("tcgen05", "decode"):
+    # tcgen05 takes widths that are multiples of 16 up to 512; the decode
+    # kernel D = Dv in {64, 128, 256}
+    for shape, algo in (((504, 504), "tcgen05"), ((512, 512), "decode")):
+        inp = synth.make_padded(1, 2, 1, 8, 8, *shape, "bf16", seed=43)
         with pytest.raises(AttnError) as ei:
             parity.run_gpu(inp, algo)
         assert ei.value.status == 2
