@@ -28,6 +28,7 @@
 #include <cuda.h>
 
 #include <climits>
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
@@ -226,26 +227,29 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         }
     } else if (warp == kMmaWarpT) {
         // ------------------------------------------------ S / dP MMA issuer
-        // Two issuing warps: one thread issuing every MMA of a tile spends more
-        // time issuing than the tensor core spends on them (the products of a
-        // 64-key tile are small), so the dQ products have a warp of their own.
-        bool ok = ntiles == 0 || warp_wait_t(bar(T_QD_FULL), 0, abort_flag, wl);
-        const uint64_t qd = sw128_desc(base + L::Q_OFF, 16, 1024);
-        const uint64_t od = sw128_desc(base + L::DO_OFF, 16, 1024);
-        for (int j = 0; j < ntiles && ok; ++j) {
-            const int s = j % kStagesT, bf = j & 1;
-            if (!warp_wait_t(kv_full(s), (uint32_t)(j / kStagesT) & 1u, abort_flag, wl)) {
-                ok = false;
-                break;
-            }
-            // S_bf and dP_bf were last read for tile j - 2: dP by the elementwise
-            // warps, S (as dS) by its dQ MMAs, which have completed
-            if (j >= 2 && !warp_wait_t(bar(T_S_EMPTY + bf), (uint32_t)((j - 2) >> 1) & 1u, abort_flag, wl)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            if (lane == 0) {
+        // Two issuing warps, one thread each: one thread issuing every MMA of
+        // a tile spends more time issuing than the tensor core spends on them
+        // (the products of a 64-key tile are small), so the dQ products have
+        // a warp of their own; a warp-wide wait per tile costs more than the
+        // wait of one thread.
+        if (lane == 0) {
+            bool ok = ntiles == 0 || mbar_wait(bar(T_QD_FULL), 0, abort_flag, wl);
+            const uint64_t qd = sw128_desc(base + L::Q_OFF, 16, 1024);
+            const uint64_t od = sw128_desc(base + L::DO_OFF, 16, 1024);
+            for (int j = 0; j < ntiles && ok; ++j) {
+                const int s = j % kStagesT, bf = j & 1;
+                if (!mbar_wait(kv_full(s), (uint32_t)(j / kStagesT) & 1u, abort_flag, wl)) {
+                    ok = false;
+                    break;
+                }
+                // S_bf and dP_bf were last read for tile j - 2: dP by the
+                // elementwise warps, S (as dS) by its dQ MMAs, which have completed
+                if (j >= 2 &&
+                    !mbar_wait(bar(T_S_EMPTY + bf), (uint32_t)((j - 2) >> 1) & 1u, abort_flag, wl)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
                 const uint64_t kd = sw128_desc(stage(s), 16, 1024);
                 const uint64_t vd = sw128_desc(stage(s) + L::KTILE, 16, 1024);
 #pragma unroll
@@ -260,45 +264,40 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
                            vd + (((kk / 4) * L::KCH + (kk % 4) * 32) >> 4), a.idesc_s, kk > 0);
                 mma_commit(bar(T_S_FULL + bf));
             }
-            __syncwarp();
-        }
-        if (!ok && lane == 0) raise_abort_t(abort_flag, p.status);
-        // every MMA issued completes before TMEM is released
-        if (lane == 0) {
+            if (!ok) raise_abort_t(abort_flag, p.status);
+            // every MMA issued completes before TMEM is released
             mma_commit(bar(T_TEARDOWN));
             mbar_wait_drain(bar(T_TEARDOWN), 0);  // ignores the abort flag
         }
         __syncwarp();
     } else if (warp == kDqWarpT) {
         // ----------------------------------------------------- dQ MMA issuer
-        bool ok = true;
-        const uint32_t dq_tm = tmem + L::DQ_COL;
-        for (int jj = 0; jj < ntiles && ok; ++jj) {
-            // dQ += dS K for tile jj, once its dS is in TMEM
-            const int bf = jj & 1, s = jj % kStagesT;
-            if (!warp_wait_t(bar(T_DS_READY + bf), (uint32_t)(jj >> 1) & 1u, abort_flag, wl)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            // Keys past the last one in use (last tile only) are left out 16
-            // at a time; the K rows of the last 16-key step past it may hold
-            // anything (NaN included), so they are zeroed: 0 * K must stay 0.
-            // S of this tile has completed (the elementwise warps read it).
-            const int nvalid = min(kKeysT, khi - (tfirst + jj * kKeysT));
-            const int ksteps = (nvalid + 15) / 16;
-            const int nzero = ksteps * 16 - nvalid;
-            if (nzero > 0) {
-                uint8_t *kt = gbase + (stage(s) - base) + nvalid * 128;
+        if (lane == 0) {
+            bool ok = true;
+            const uint32_t dq_tm = tmem + L::DQ_COL;
+            for (int jj = 0; jj < ntiles && ok; ++jj) {
+                const int bf = jj & 1, s = jj % kStagesT;
+                if (!mbar_wait(bar(T_DS_READY + bf), (uint32_t)(jj >> 1) & 1u, abort_flag, wl)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // Keys past the last one in use (last tile only) are left out 16
+                // at a time; the K rows of the last 16-key step past it may hold
+                // anything (NaN included), so they are zeroed: 0 * K must stay 0.
+                // S of this tile has completed (the elementwise warps read it).
+                const int nvalid = min(kKeysT, khi - (tfirst + jj * kKeysT));
+                const int ksteps = (nvalid + 15) / 16;
+                const int nzero = ksteps * 16 - nvalid;
+                if (nzero > 0) {
+                    uint8_t *kt = gbase + (stage(s) - base) + nvalid * 128;
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c)
-                    for (int i = lane; i < nzero * 8; i += 32)
-                        *reinterpret_cast<uint4 *>(kt + c * L::KCH + i * 16) =
-                            make_uint4(0, 0, 0, 0);
-                fence_proxy_async_smem();
-                __syncwarp();
-            }
-            if (lane == 0) {
+                    for (int c = 0; c < D / 64; ++c)
+                        for (int i = 0; i < nzero * 8; ++i)
+                            *reinterpret_cast<uint4 *>(kt + c * L::KCH + i * 16) =
+                                make_uint4(0, 0, 0, 0);
+                    fence_proxy_async_smem();
+                }
                 // K as the MN-major B operand: 64-column chunks L::KCH apart
                 const uint64_t kmn = sw128_desc(stage(s), L::KCH, 1024);
 #pragma unroll
@@ -310,10 +309,8 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
                 mma_commit(bar(T_S_EMPTY + bf));
                 if (jj == ntiles - 1) mma_commit(bar(T_DQ_FULL));
             }
-            __syncwarp();
-        }
-        if (!ok && lane == 0) raise_abort_t(abort_flag, p.status);
-        if (lane == 0) {
+            if (!ok) raise_abort_t(abort_flag, p.status);
+            // every MMA issued completes before TMEM is released
             mma_commit(bar(T_TEARDOWN));
             mbar_wait_drain(bar(T_TEARDOWN), 0);  // ignores the abort flag
         }
@@ -349,7 +346,18 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
             tmem_ld32(tP + 32, pv[1]);
             tmem_ld_wait();
             const int k0 = tfirst + j * kKeysT;
-            const bool inner = __all_sync(0xffffffffu, lo <= k0 && hi >= k0 + kKeysT);
+            // bit i of keep[hf]: key k0 + 32 hf + i lies in the row's [lo, hi).
+            // Tested against a compile-time bit below: a per-key comparison
+            // there compiled to branches and cost ~3x the rest of the step.
+            uint32_t keep[2];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int a0 = min(max(lo - k0 - hf * 32, 0), 32);
+                const int b0 = min(max(hi - k0 - hf * 32, 0), 32);
+                const uint32_t below_b = b0 >= 32 ? 0xffffffffu : (1u << b0) - 1u;
+                const uint32_t below_a = a0 >= 32 ? 0xffffffffu : (1u << a0) - 1u;
+                keep[hf] = below_b & ~below_a;
+            }
             uint32_t pk[32];
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf)
@@ -358,10 +366,10 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
                     float ds[2];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const int key = k0 + hf * 32 + i + e;
-                        const bool legal = inner || (key >= lo && key < hi);
                         const float pr = ex2f(__uint_as_float(sv[hf][i + e]) * a.c2 - lse2);
-                        ds[e] = legal ? pr * (__uint_as_float(pv[hf][i + e]) - dl) : 0.f;
+                        ds[e] = ((keep[hf] >> (i + e)) & 1u)
+                                    ? pr * (__uint_as_float(pv[hf][i + e]) - dl)
+                                    : 0.f;
                     }
                     pk[hf * 16 + i / 2] = pack16<T>(ds[0], ds[1]);
                 }
@@ -391,13 +399,15 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
                 for (int i = 0; i < 32; ++i) v[i] = 0u;
             }
             if (writes) {
+                // 16-byte stores (D is a multiple of 16, so rows are 32-byte aligned)
                 T *dst = dqg + row * Dr + c * 32;
+                auto f = [&](int i) { return valid ? __uint_as_float(v[i]) * p.scale : 0.f; };
 #pragma unroll
-                for (int i = 0; i < 32; i += 2)
+                for (int i = 0; i < 32; i += 8)
                     if (c * 32 + i < Dr)
-                        *reinterpret_cast<uint32_t *>(dst + i) =
-                            pack16<T>(valid ? __uint_as_float(v[i]) * p.scale : 0.f,
-                                      valid ? __uint_as_float(v[i + 1]) * p.scale : 0.f);
+                        *reinterpret_cast<uint4 *>(dst + i) =
+                            make_uint4(pack16<T>(f(i), f(i + 1)), pack16<T>(f(i + 2), f(i + 3)),
+                                       pack16<T>(f(i + 4), f(i + 5)), pack16<T>(f(i + 6), f(i + 7)));
             }
         }
     }
@@ -601,18 +611,19 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         }
     } else if (warp == kMmaWarpT) {
         // ------------------------------------------------------------ MMA issuer
-        bool ok = ntiles == 0 || warp_wait_t(bar(K_KV_FULL), 0, abort_flag, wl);
-        const uint64_t kd = sw128_desc(base + L::K_OFF, 16, 1024);
-        const uint64_t vd = sw128_desc(base + L::V_OFF, 16, 1024);
-        for (int t = 0; t <= ntiles && ok; ++t) {
-            if (t < ntiles) {
-                const int s = t % kStagesK, bf = t & 1;
-                if (!warp_wait_t(row_full(s), (uint32_t)(t / kStagesK) & 1u, abort_flag, wl)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (lane == 0) {
+        // (one thread: a warp-wide wait per tile costs more than its own)
+        if (lane == 0) {
+            bool ok = ntiles == 0 || mbar_wait(bar(K_KV_FULL), 0, abort_flag, wl);
+            const uint64_t kd = sw128_desc(base + L::K_OFF, 16, 1024);
+            const uint64_t vd = sw128_desc(base + L::V_OFF, 16, 1024);
+            for (int t = 0; t <= ntiles && ok; ++t) {
+                if (t < ntiles) {
+                    const int s = t % kStagesK, bf = t & 1;
+                    if (!mbar_wait(row_full(s), (uint32_t)(t / kStagesK) & 1u, abort_flag, wl)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
                     // buffer bf was last read by the dV / dK MMAs of tile t - 2,
                     // issued earlier by this thread
                     const uint64_t qd = sw128_desc(rstage(s), 16, 1024);
@@ -629,32 +640,28 @@ __global__ void __launch_bounds__(kThreadsT, 1)
                                od + (((kk / 4) * L::RCH + (kk % 4) * 32) >> 4), a.idesc_s, kk > 0);
                     mma_commit(bar(K_S_FULL + bf));
                 }
-                __syncwarp();
-            }
-            if (t >= 1) {
-                const int tt = t - 1, bf = tt & 1, s = tt % kStagesK;
-                if (!warp_wait_t(bar(K_DS_READY + bf), (uint32_t)(tt >> 1) & 1u, abort_flag, wl)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                // rows of the tile past the sequence's queries may hold anything
-                // (NaN included): their P and dS are 0, and the Q and dO rows are
-                // zeroed so that 0 * row stays 0 (S^T and dP^T of the tile have
-                // completed: the elementwise warps read them)
-                const int pos0 = qf + tt * PP;
-                const int nreal = min(kRowsK, max(0, (si.Qb - pos0) * G));
-                if (nreal < kRowsK) {
-                    uint8_t *rt = gbase + (rstage(s) - base);
-                    const int nzero = kRowsK - nreal;
-                    for (int c = 0; c < D / 64 + DV / 64; ++c)
-                        for (int i = lane; i < nzero * 8; i += 32)
-                            *reinterpret_cast<uint4 *>(rt + c * L::RCH + nreal * 128 + i * 16) =
-                                make_uint4(0, 0, 0, 0);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                }
-                if (lane == 0) {
+                if (t >= 1) {
+                    const int tt = t - 1, bf = tt & 1, s = tt % kStagesK;
+                    if (!mbar_wait(bar(K_DS_READY + bf), (uint32_t)(tt >> 1) & 1u, abort_flag, wl)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // rows of the tile past the sequence's queries may hold
+                    // anything (NaN included): their P and dS are 0, and the Q and
+                    // dO rows are zeroed so that 0 * row stays 0 (S^T and dP^T of
+                    // the tile have completed: the elementwise warps read them)
+                    const int pos0 = qf + tt * PP;
+                    const int nreal = min(kRowsK, max(0, (si.Qb - pos0) * G));
+                    if (nreal < kRowsK) {
+                        uint8_t *rt = gbase + (rstage(s) - base);
+                        const int nzero = kRowsK - nreal;
+                        for (int c = 0; c < D / 64 + DV / 64; ++c)
+                            for (int i = 0; i < nzero * 8; ++i)
+                                *reinterpret_cast<uint4 *>(rt + c * L::RCH + nreal * 128 + i * 16) =
+                                    make_uint4(0, 0, 0, 0);
+                        fence_proxy_async_smem();
+                    }
                     const uint64_t qmn = sw128_desc(rstage(s), L::RCH, 1024);
                     const uint64_t omn = sw128_desc(rstage(s) + L::QTILE, L::RCH, 1024);
 #pragma unroll
@@ -668,11 +675,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
                     mma_commit(row_empty(s));
                     if (tt == ntiles - 1) mma_commit(bar(K_ACC_FULL));
                 }
-                __syncwarp();
             }
-        }
-        if (!ok && lane == 0) raise_abort_t(abort_flag, p.status);
-        if (lane == 0) {
+            if (!ok) raise_abort_t(abort_flag, p.status);
             mma_commit(bar(K_TEARDOWN));
             mbar_wait_drain(bar(K_TEARDOWN), 0);  // ignores the abort flag
         }
@@ -707,25 +711,43 @@ __global__ void __launch_bounds__(kThreadsT, 1)
             tmem_ld_wait();
             const float *st = stats + s * 4 * kRowsK;
             const int *sti = reinterpret_cast<const int *>(st);
-            const bool inner = flags[s] != 0;
+            const bool inner = flags[s] != 0;  // the same for every thread
             uint32_t pk[32], dk[32];
+            // P^T and dS^T of the tile; rows that may not see this key give 0.
+            // Interior tiles (every row sees every key of the CTA) skip the
+            // row bounds; elsewhere they are combined without short-circuit
+            // (a per-key || / && compiled to branches, ~3x the step's cost).
+            auto body = [&](auto masked) {
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf)
+                for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    float pp[2], dd[2];
+                    for (int i = 0; i < 32; i += 2) {
+                        float pp[2], dd[2];
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int row = hf * 32 + i + e;
-                        const bool legal =
-                            inner || (key >= sti[2 * kRowsK + row] && key < sti[3 * kRowsK + row]);
-                        const float pr = ex2f(__uint_as_float(sv[hf][i + e]) * a.c2 - st[row]);
-                        pp[e] = legal ? pr : 0.f;
-                        dd[e] = legal ? pr * (__uint_as_float(pv[hf][i + e]) - st[kRowsK + row]) : 0.f;
+                        for (int e = 0; e < 2; ++e) {
+                            const int row = hf * 32 + i + e;
+                            const float pr =
+                                ex2f(__uint_as_float(sv[hf][i + e]) * a.c2 - st[row]);
+                            const float d =
+                                pr * (__uint_as_float(pv[hf][i + e]) - st[kRowsK + row]);
+                            if (decltype(masked)::value) {
+                                const bool legal = (key >= sti[2 * kRowsK + row]) &
+                                                   (key < sti[3 * kRowsK + row]);
+                                pp[e] = legal ? pr : 0.f;
+                                dd[e] = legal ? d : 0.f;
+                            } else {
+                                pp[e] = pr;
+                                dd[e] = d;
+                            }
+                        }
+                        pk[hf * 16 + i / 2] = pack16<T>(pp[0], pp[1]);
+                        dk[hf * 16 + i / 2] = pack16<T>(dd[0], dd[1]);
                     }
-                    pk[hf * 16 + i / 2] = pack16<T>(pp[0], pp[1]);
-                    dk[hf * 16 + i / 2] = pack16<T>(dd[0], dd[1]);
-                }
+            };
+            if (inner)
+                body(std::false_type{});
+            else
+                body(std::true_type{});
             tmem_st32(tS, pk);  // P^T over the first half of S^T_bf
             tmem_st32(tP, dk);  // dS^T over the first half of dP^T_bf
             tmem_st_wait();
@@ -750,13 +772,15 @@ __global__ void __launch_bounds__(kThreadsT, 1)
                 tmem_ld32(tmem + lane_off + L::DV_COL + c * 32, v);
                 tmem_ld_wait();
             }
-            if (writes)
+            if (writes) {
+                auto f = [&](int i) { return has ? __uint_as_float(v[i]) : 0.f; };
 #pragma unroll
-                for (int i = 0; i < 32; i += 2)
+                for (int i = 0; i < 32; i += 8)
                     if (c * 32 + i < p.Dv)
-                        *reinterpret_cast<uint32_t *>(dvg + krow * p.Dv + c * 32 + i) =
-                            pack16<T>(has ? __uint_as_float(v[i]) : 0.f,
-                                      has ? __uint_as_float(v[i + 1]) : 0.f);
+                        *reinterpret_cast<uint4 *>(dvg + krow * p.Dv + c * 32 + i) =
+                            make_uint4(pack16<T>(f(i), f(i + 1)), pack16<T>(f(i + 2), f(i + 3)),
+                                       pack16<T>(f(i + 4), f(i + 5)), pack16<T>(f(i + 6), f(i + 7)));
+            }
         }
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -765,13 +789,15 @@ __global__ void __launch_bounds__(kThreadsT, 1)
                 tmem_ld32(tmem + lane_off + L::DK_COL + c * 32, v);
                 tmem_ld_wait();
             }
-            if (writes)
+            if (writes) {
+                auto f = [&](int i) { return has ? __uint_as_float(v[i]) * p.scale : 0.f; };
 #pragma unroll
-                for (int i = 0; i < 32; i += 2)
+                for (int i = 0; i < 32; i += 8)
                     if (c * 32 + i < p.D)
-                        *reinterpret_cast<uint32_t *>(dkg + krow * p.D + c * 32 + i) =
-                            pack16<T>(has ? __uint_as_float(v[i]) * p.scale : 0.f,
-                                      has ? __uint_as_float(v[i + 1]) * p.scale : 0.f);
+                        *reinterpret_cast<uint4 *>(dkg + krow * p.D + c * 32 + i) =
+                            make_uint4(pack16<T>(f(i), f(i + 1)), pack16<T>(f(i + 2), f(i + 3)),
+                                       pack16<T>(f(i + 4), f(i + 5)), pack16<T>(f(i + 6), f(i + 7)));
+            }
         }
     }
 

@@ -227,6 +227,31 @@ def test_bwd_rejects_tensor_kernels_on_fp32_and_bad_algo():
     assert ei.value.status == 1
 
 
+def test_bwd_misaligned_gradients_rejected():
+    """Gradient buffers 8 bytes past a 16-byte boundary are refused before any
+    launch (the kernels store 16 bytes at a time), for every kernel choice,
+    and the buffers are left untouched."""
+    inp = synth.make_padded(1, 8, 2, 150, 200, 128, 128, "bf16", seed=95)
+    dout = synth.make_dout(inp, seed=96)
+    dev = torch.device("cuda")
+    q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+    o, lse = attn_fwd(q, k, v, scale=inp.scale)
+    g = dout.to(dev)
+
+    def shifted(t):
+        buf = torch.full((t.numel() + 4,), NAN, dtype=t.dtype, device=dev)
+        return buf[4:].view(t.shape)  # 4 bf16 elements = 8 bytes in
+
+    dq, dk, dv = shifted(q), shifted(k), shifted(v)
+    assert dq.data_ptr() % 16 == 8
+    for algo in ("auto", "tcgen05", "mma", "generic"):
+        with pytest.raises(AttnError) as ei:
+            attn_bwd(q, k, v, o, lse, g, dq, dk, dv, scale=inp.scale, algo=algo)
+        assert ei.value.status == 1, algo
+    torch.cuda.synchronize()
+    assert all(torch.isnan(t.float()).all() for t in (dq, dk, dv))
+
+
 def test_bwd_no_query_rows_zeroes_key_gradients():
     dev = torch.device("cuda")
     q = torch.zeros((2, 0, 4, 64), dtype=torch.bfloat16, device=dev)
