@@ -33,16 +33,21 @@
 #include "common.cuh"
 #include "launch.h"
 #include "sm100_ptx.cuh"
+#include "tc_softmax.cuh"
 
 namespace attn {
 namespace {
 
 using namespace sm100;
+using tcfwd::f2pack;
+using tcfwd::f2unpack;
+using tcfwd::ffma2;
+using tcfwd::fadd2;
+using tcfwd::fmul2;
 
 constexpr int kRowsT = 128;  // query rows per CTA (MMA M)
 constexpr int kKeysT = 64;   // keys per tile (N of S and dP, contraction of dQ)
 constexpr int kStagesT = 4;  // K/V ring depth
-constexpr int kThreadsT = 192;  // dK/dV: warps 0-3 elementwise, 4 TMA, 5 MMA
 constexpr int kThreadsQ = 224;  // dQ: warps 0-3 elementwise, 4 TMA, 5 S / dP MMAs, 6 dQ MMAs
 constexpr int kLoadWarpT = 4;
 constexpr int kMmaWarpT = 5;
@@ -358,21 +363,37 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
                 const uint32_t below_a = a0 >= 32 ? 0xffffffffu : (1u << a0) - 1u;
                 keep[hf] = below_b & ~below_a;
             }
+            // pairs of keys share packed f32x2 arithmetic; warps whose rows all
+            // see the whole tile skip the test
+            const bool all_in = __all_sync(0xffffffffu, (keep[0] & keep[1]) == 0xffffffffu);
+            const uint64_t c2 = f2pack(a.c2, a.c2), nl2 = f2pack(-lse2, -lse2),
+                           nd2 = f2pack(-dl, -dl);
             uint32_t pk[32];
+            auto body = [&](auto masked) {
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf)
+                for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    float ds[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float pr = ex2f(__uint_as_float(sv[hf][i + e]) * a.c2 - lse2);
-                        ds[e] = ((keep[hf] >> (i + e)) & 1u)
-                                    ? pr * (__uint_as_float(pv[hf][i + e]) - dl)
-                                    : 0.f;
+                    for (int i = 0; i < 32; i += 2) {
+                        const uint64_t x2 = ffma2(
+                            f2pack(__uint_as_float(sv[hf][i]), __uint_as_float(sv[hf][i + 1])), c2, nl2);
+                        float x0, x1;
+                        f2unpack(x2, x0, x1);
+                        const uint64_t y2 = fmul2(
+                            fadd2(f2pack(__uint_as_float(pv[hf][i]), __uint_as_float(pv[hf][i + 1])), nd2),
+                            f2pack(ex2f(x0), ex2f(x1)));
+                        float d0, d1;
+                        f2unpack(y2, d0, d1);
+                        if (decltype(masked)::value) {
+                            d0 = ((keep[hf] >> i) & 1u) ? d0 : 0.f;
+                            d1 = ((keep[hf] >> (i + 1)) & 1u) ? d1 : 0.f;
+                        }
+                        pk[hf * 16 + i / 2] = pack16<T>(d0, d1);
                     }
-                    pk[hf * 16 + i / 2] = pack16<T>(ds[0], ds[1]);
-                }
+            };
+            if (all_in)
+                body(std::false_type{});
+            else
+                body(std::true_type{});
             tmem_st32(tS, pk);  // dS over the first half of S_bf
             tmem_st_wait();
             tc_fence_before();
@@ -423,24 +444,43 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
 // ---------------------------------------------------------------------------
 // dK / dV.  A CTA owns 128 keys of one (sequence, KV head) -- TMEM lane = key
 // -- with K and V resident in shared memory, and streams the rows that attend
-// to them: 64 rows a tile of the flattened (query position, head-in-group)
-// space, all heads of the group, one TMA box {64 columns, G heads, 64 / G
+// to them: 128 rows a tile of the flattened (query position, head-in-group)
+// space, all heads of the group, one TMA box {64 columns, G heads, 128 / G
 // positions} per 64 columns (the forward loop transposed, keys resident and
-// rows streamed, as the FlyDSL page describes its dK/dV kernel):
-//   S^T = K Q^T and dP^T = V dO^T into TMEM buffer b (M = 128 keys, N = 64
-//   rows); the elementwise warps turn them into P^T and dS^T (16-bit pairs
-//   over the first halves of S^T_b and dP^T_b); then dV += P^T dO and
-//   dK += dS^T Q with dO and Q read MN-major from the same row tile.
-// TMEM: S^T0 S^T1 | dP^T0 dP^T1 | dV | dK.  Per-row LSE, Dq and legal key
-// range ride with each row tile (written by the loader warp, published by
-// the tile's full barrier).
-constexpr int kKeysK = 128;  // keys per CTA (MMA M)
-constexpr int kRowsK = 64;   // rows per tile (N of S^T and dP^T, contraction of dV and dK)
-constexpr int kStagesK = 3;
+// rows streamed, as the FlyDSL page describes its dK/dV kernel).  Per tile:
+//   S^T = K Q^T and dP^T = V dO^T into TMEM (M = 128 keys, N = 128 rows);
+//   two elementwise warpgroups, one per 64-row half, turn S^T into P^T as
+//   soon as S^T is in (while dP^T is still computed), then dP^T into dS^T,
+//   16-bit pairs over the first halves of their columns;
+//   dV += P^T dO for a half as soon as its P^T is in, dK += dS^T Q once its
+//   dS^T is, with dO and Q read MN-major from the same row tile.
+// At N = 128 every product takes 64 tensor cycles an MMA; 64-row tiles made
+// S^T and dP^T N = 64 products, bound by shared-memory operand reads and by
+// issue.  S^T and dP^T are single-buffered: the next tile's S^T, issued after
+// this tile's dK by the same thread (tcgen05.mma executes in order), writes
+// TMEM only after the dV products have read P^T.
+// TMEM: S^T | dP^T | dV | dK.  Per-row LSE, Dq and legal key range ride with
+// each row tile (written by the loader warp, published by the tile's full
+// barrier).
+constexpr int kKeysK = 128;     // keys per CTA (MMA M)
+constexpr int kRowsK = 128;     // rows per tile (N of S^T and dP^T, contraction of dV and dK)
+constexpr int kHalfK = 64;      // rows per elementwise warpgroup
+constexpr int kStagesK = 2;     // row-tile ring
+constexpr int kThreadsK = 384;  // warps 0-7 elementwise (two warpgroups), 8 TMA, 9 MMA, 10-11 idle
+constexpr int kLoadWarpK = 8;
+constexpr int kMmaWarpK = 9;
+// Three warps share each SM sub-partition, so a thread may hold 168 registers
+// at launch; the elementwise warps keep 64 fp32 P values across the wait for
+// dP^T and take more from the loader, MMA and idle warps (whole warpgroups).
+constexpr uint32_t kRegsLaunchK = 168;
+constexpr uint32_t kRegsElemK = 208;
+constexpr uint32_t kRegsOtherK = 80;
+static_assert(256 * kRegsElemK + 128 * kRegsOtherK <= kThreadsK * kRegsLaunchK, "register split");
+static_assert(2 * kRegsElemK + kRegsOtherK <= 512, "register split per sub-partition");
 
 template <int D, int DV> struct KvLayout {
     static constexpr int KCH = kKeysK * 128;  // a 64-column chunk of the 128-key tile
-    static constexpr int RCH = kRowsK * 128;  // a 64-column chunk of a 64-row tile
+    static constexpr int RCH = kRowsK * 128;  // a 64-column chunk of a 128-row tile
     static constexpr int KTILE = (D / 64) * KCH;
     static constexpr int VTILE = (DV / 64) * KCH;
     static constexpr int QTILE = (D / 64) * RCH;
@@ -461,25 +501,27 @@ template <int D, int DV> struct KvLayout {
 
 enum : int {
     K_KV_FULL = 0,
-    K_S_FULL = 1,     // [2]
-    K_DS_READY = 3,   // [2]
-    K_ACC_FULL = 5,
-    K_TEARDOWN = 6,
-    K_ROW_FULL = 7,   // [kStagesK] full, then [kStagesK] empty
-    K_NBARS = 7 + 2 * kStagesK,
+    K_S_FULL = 1,     // S^T of the tile has completed
+    K_DP_FULL = 2,    // dP^T of the tile has completed
+    K_P_READY = 3,    // [2] by half: its P^T is in TMEM
+    K_DS_READY = 5,   // [2] by half: its dS^T is in TMEM
+    K_ACC_FULL = 7,
+    K_TEARDOWN = 8,
+    K_ROW_FULL = 9,   // [kStagesK] full, then [kStagesK] empty
+    K_NBARS = 9 + 2 * kStagesK,
 };
 
 struct KvArgs {
     BwdParams bp;
     int nkt;           // 128-key tiles per (sequence, KV head)
     float c2;          // scale * log2(e)
-    uint32_t idesc_s;  // M128 N64, both K-major
+    uint32_t idesc_s;  // M128 N128, both K-major
     uint32_t idesc_v;  // M128 N=DV, B MN-major
     uint32_t idesc_k;  // M128 N=D, B MN-major
 };
 
 template <typename T, int D, int DV>
-__global__ void __launch_bounds__(kThreadsT, 1)
+__global__ void __launch_bounds__(kThreadsK, 1)
     bwd_dkdv_tc_kernel(const __grid_constant__ KvArgs a, const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV) {
@@ -510,7 +552,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     auto row_full = [&](int s) { return bar(K_ROW_FULL + s); };
     auto row_empty = [&](int s) { return bar(K_ROW_FULL + kStagesK + s); };
     auto rstage = [&](int s) { return base + L::R_OFF + (uint32_t)s * L::STAGE; };
-    float *stats = reinterpret_cast<float *>(gbase + L::ST_OFF);  // [stage][4][kRowsK]
+    // [stage][4][kRowsK]: -LSE (log2 units), -Dq, lo, hi
+    float *stats = reinterpret_cast<float *>(gbase + L::ST_OFF);
     int *flags = reinterpret_cast<int *>(gbase + L::FLAG_OFF);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -521,9 +564,11 @@ __global__ void __launch_bounds__(kThreadsT, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(K_KV_FULL), 1);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(K_S_FULL + i), 1);
-            mbar_init(bar(K_DS_READY + i), 128);
+        mbar_init(bar(K_S_FULL), 1);
+        mbar_init(bar(K_DP_FULL), 1);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(bar(K_P_READY + h), 128);
+            mbar_init(bar(K_DS_READY + h), 128);
         }
         mbar_init(bar(K_ACC_FULL), 1);
         mbar_init(bar(K_TEARDOWN), 1);
@@ -534,7 +579,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == kMmaWarpT) {
+    if (warp == kMmaWarpK) {
         tmem_alloc(smem_addr(tmem_slot), 512);
         tmem_relinquish();
     }
@@ -543,7 +588,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == kLoadWarpT) {
+    if (warp >= kLoadWarpK) regs_decrease<kRegsOtherK>();
+    if (warp == kLoadWarpK) {
         // ------------------------------------------------ TMA producer + row stats
         const int qrow = padded ? 0 : (int)si.q_off;
         const int krow = padded ? 0 : (int)si.k_off;
@@ -559,16 +605,27 @@ __global__ void __launch_bounds__(kThreadsT, 1)
                 tma_load_4d(base + L::V_OFF + c * L::KCH, &tmV, bar(K_KV_FULL), c * 64, kvh,
                             krow + k0, bc);
         }
+        // The rows of tile t + kStagesK are prefetched into L2 when tile t is
+        // loaded, and each tile's row statistics (global LSE and Dq loads) are
+        // gathered before waiting for its stage: the stage is free only once
+        // the previous occupant's products have completed, and a load started
+        // then from DRAM stalled the MMA thread.
+        auto prefetch_rows = [&](int tt) {
+            const int r0 = qrow + qf + tt * PP;
+            for (int c = 0; c < D / 64; ++c) tma_prefetch_l2_4d(&tmQ, c * 64, kvh * G, r0, bc);
+            for (int c = 0; c < DV / 64; ++c) tma_prefetch_l2_4d(&tmO, c * 64, kvh * G, r0, bc);
+        };
+        if (lane == 0)
+            for (int tt = 0; tt < kStagesK && tt < ntiles; ++tt) prefetch_rows(tt);
         for (int t = 0; t < ntiles && ok; ++t) {
             const int s = t % kStagesK;
             const uint32_t ph = (uint32_t)(t / kStagesK) & 1u;
-            ok = warp_wait_t(row_empty(s), ph ^ 1u, abort_flag, wl);
-            if (!ok) break;
-            // per-row statistics of the tile, two rows a lane
-            float *st = stats + s * 4 * kRowsK;
+            // per-row statistics of the tile, four rows a lane
+            float nl2[kRowsK / 32], ndl[kRowsK / 32];
+            int rlo[kRowsK / 32], rhi[kRowsK / 32];
             bool inner = true;
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
+            for (int e = 0; e < kRowsK / 32; ++e) {
                 const int i = lane + 32 * e;  // row of the tile = smem row
                 const int pos = qf + t * PP + i / G;
                 const int hh = kvh * G + i % G;
@@ -580,13 +637,24 @@ __global__ void __launch_bounds__(kThreadsT, 1)
                     l2 = p.lse[row] * kLog2e;
                     dl = bp.delta[row];
                 }
-                st[i] = l2;
-                st[kRowsK + i] = dl;
-                reinterpret_cast<int *>(st)[2 * kRowsK + i] = lo;
-                reinterpret_cast<int *>(st)[3 * kRowsK + i] = hi;
+                nl2[e] = -l2;  // stored negated: one packed FMA / add a pair of rows
+                ndl[e] = -dl;
+                rlo[e] = lo;
+                rhi[e] = hi;
                 inner = inner && lo <= k0 && hi >= k0 + kKeysK;
             }
             inner = __all_sync(0xffffffffu, inner);
+            ok = warp_wait_t(row_empty(s), ph ^ 1u, abort_flag, wl);
+            if (!ok) break;
+            float *st = stats + s * 4 * kRowsK;
+#pragma unroll
+            for (int e = 0; e < kRowsK / 32; ++e) {
+                const int i = lane + 32 * e;
+                st[i] = nl2[e];
+                st[kRowsK + i] = ndl[e];
+                reinterpret_cast<int *>(st)[2 * kRowsK + i] = rlo[e];
+                reinterpret_cast<int *>(st)[3 * kRowsK + i] = rhi[e];
+            }
             if (lane == 0) flags[s] = inner ? 1 : 0;
             __syncwarp();
             if (lane == 0) {
@@ -599,6 +667,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
                                 kvh * G, r0, bc);
                 armed |= 1u << s;
                 armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+                if (t + kStagesK < ntiles) prefetch_rows(t + kStagesK);
             }
         }
         if (!ok && lane == 0) raise_abort_t(abort_flag, p.status);
@@ -609,153 +678,230 @@ __global__ void __launch_bounds__(kThreadsT, 1)
             for (int s = 0; s < kStagesK; ++s)
                 if (armed & (1u << s)) mbar_wait_drain(row_full(s), (armed_ph >> s) & 1u);
         }
-    } else if (warp == kMmaWarpT) {
+    } else if (warp == kMmaWarpK) {
         // ------------------------------------------------------------ MMA issuer
-        // (one thread: a warp-wide wait per tile costs more than its own)
+        // (one thread: a warp-wide wait costs more than the wait of one thread)
         if (lane == 0) {
             bool ok = ntiles == 0 || mbar_wait(bar(K_KV_FULL), 0, abort_flag, wl);
             const uint64_t kd = sw128_desc(base + L::K_OFF, 16, 1024);
             const uint64_t vd = sw128_desc(base + L::V_OFF, 16, 1024);
-            for (int t = 0; t <= ntiles && ok; ++t) {
-                if (t < ntiles) {
-                    const int s = t % kStagesK, bf = t & 1;
-                    if (!mbar_wait(row_full(s), (uint32_t)(t / kStagesK) & 1u, abort_flag, wl)) {
+            for (int t = 0; t < ntiles && ok; ++t) {
+                const int s = t % kStagesK;
+                const uint32_t tp = (uint32_t)t & 1u;  // parity of this tile's phases
+                if (!mbar_wait(row_full(s), (uint32_t)(t / kStagesK) & 1u, abort_flag, wl)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                // S^T and dP^T overwrite the previous tile's P^T / dS^T: issued
+                // after its dV / dK products by this thread
+                const uint64_t qd = sw128_desc(rstage(s), 16, 1024);
+                const uint64_t od = sw128_desc(rstage(s) + L::QTILE, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + L::ST_COL, kd + (((kk / 4) * L::KCH + (kk % 4) * 32) >> 4),
+                           qd + (((kk / 4) * L::RCH + (kk % 4) * 32) >> 4), a.idesc_s, kk > 0);
+                mma_commit(bar(K_S_FULL));
+#pragma unroll
+                for (int kk = 0; kk < DV / 16; ++kk)
+                    mma_ss(tmem + L::DPT_COL, vd + (((kk / 4) * L::KCH + (kk % 4) * 32) >> 4),
+                           od + (((kk / 4) * L::RCH + (kk % 4) * 32) >> 4), a.idesc_s, kk > 0);
+                mma_commit(bar(K_DP_FULL));
+                // rows of the tile past the sequence's queries may hold anything
+                // (NaN included): their P and dS are 0, and their Q and dO rows
+                // are zeroed so that 0 * row stays 0 -- once S^T and dP^T, which
+                // read them, have completed
+                const int pos0 = qf + t * PP;
+                const int nreal = min(kRowsK, max(0, (si.Qb - pos0) * G));
+                if (nreal < kRowsK) {
+                    if (!mbar_wait(bar(K_DP_FULL), tp, abort_flag, wl)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *rt = gbase + (rstage(s) - base);
+                    const int nzero = kRowsK - nreal;
+                    for (int c = 0; c < D / 64 + DV / 64; ++c)
+                        for (int i = 0; i < nzero * 8; ++i)
+                            *reinterpret_cast<uint4 *>(rt + c * L::RCH + nreal * 128 + i * 16) =
+                                make_uint4(0, 0, 0, 0);
+                    fence_proxy_async_smem();
+                }
+                // dV += P^T dO, half by half as the warpgroups deliver P^T
+                const uint64_t omn = sw128_desc(rstage(s) + L::QTILE, L::RCH, 1024);
+                for (int h = 0; h < 2 && ok; ++h) {
+                    if (!mbar_wait(bar(K_P_READY + h), tp, abort_flag, wl)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    // buffer bf was last read by the dV / dK MMAs of tile t - 2,
-                    // issued earlier by this thread
-                    const uint64_t qd = sw128_desc(rstage(s), 16, 1024);
-                    const uint64_t od = sw128_desc(rstage(s) + L::QTILE, 16, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + L::ST_COL + bf * kRowsK,
-                               kd + (((kk / 4) * L::KCH + (kk % 4) * 32) >> 4),
-                               qd + (((kk / 4) * L::RCH + (kk % 4) * 32) >> 4), a.idesc_s, kk > 0);
-#pragma unroll
-                    for (int kk = 0; kk < DV / 16; ++kk)
-                        mma_ss(tmem + L::DPT_COL + bf * kRowsK,
-                               vd + (((kk / 4) * L::KCH + (kk % 4) * 32) >> 4),
-                               od + (((kk / 4) * L::RCH + (kk % 4) * 32) >> 4), a.idesc_s, kk > 0);
-                    mma_commit(bar(K_S_FULL + bf));
+                    for (int kk = 0; kk < kHalfK / 16; ++kk)
+                        mma_ts(tmem + L::DV_COL, tmem + L::ST_COL + h * kHalfK + kk * 8,
+                               omn + (((h * kHalfK + kk * 16) * 128) >> 4), a.idesc_v,
+                               (t > 0 || h > 0 || kk > 0) ? 1u : 0u);
                 }
-                if (t >= 1) {
-                    const int tt = t - 1, bf = tt & 1, s = tt % kStagesK;
-                    if (!mbar_wait(bar(K_DS_READY + bf), (uint32_t)(tt >> 1) & 1u, abort_flag, wl)) {
+                if (!ok) break;
+                // dK += dS^T Q, likewise
+                const uint64_t qmn = sw128_desc(rstage(s), L::RCH, 1024);
+                for (int h = 0; h < 2 && ok; ++h) {
+                    if (!mbar_wait(bar(K_DS_READY + h), tp, abort_flag, wl)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    // rows of the tile past the sequence's queries may hold
-                    // anything (NaN included): their P and dS are 0, and the Q and
-                    // dO rows are zeroed so that 0 * row stays 0 (S^T and dP^T of
-                    // the tile have completed: the elementwise warps read them)
-                    const int pos0 = qf + tt * PP;
-                    const int nreal = min(kRowsK, max(0, (si.Qb - pos0) * G));
-                    if (nreal < kRowsK) {
-                        uint8_t *rt = gbase + (rstage(s) - base);
-                        const int nzero = kRowsK - nreal;
-                        for (int c = 0; c < D / 64 + DV / 64; ++c)
-                            for (int i = 0; i < nzero * 8; ++i)
-                                *reinterpret_cast<uint4 *>(rt + c * L::RCH + nreal * 128 + i * 16) =
-                                    make_uint4(0, 0, 0, 0);
-                        fence_proxy_async_smem();
-                    }
-                    const uint64_t qmn = sw128_desc(rstage(s), L::RCH, 1024);
-                    const uint64_t omn = sw128_desc(rstage(s) + L::QTILE, L::RCH, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < kRowsK / 16; ++kk)
-                        mma_ts(tmem + L::DV_COL, tmem + L::ST_COL + bf * kRowsK + kk * 8,
-                               omn + ((kk * 2048) >> 4), a.idesc_v, (tt > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                    for (int kk = 0; kk < kRowsK / 16; ++kk)
-                        mma_ts(tmem + L::DK_COL, tmem + L::DPT_COL + bf * kRowsK + kk * 8,
-                               qmn + ((kk * 2048) >> 4), a.idesc_k, (tt > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(row_empty(s));
-                    if (tt == ntiles - 1) mma_commit(bar(K_ACC_FULL));
+                    for (int kk = 0; kk < kHalfK / 16; ++kk)
+                        mma_ts(tmem + L::DK_COL, tmem + L::DPT_COL + h * kHalfK + kk * 8,
+                               qmn + (((h * kHalfK + kk * 16) * 128) >> 4), a.idesc_k,
+                               (t > 0 || h > 0 || kk > 0) ? 1u : 0u);
                 }
+                if (!ok) break;
+                mma_commit(row_empty(s));
+                if (t == ntiles - 1) mma_commit(bar(K_ACC_FULL));
             }
             if (!ok) raise_abort_t(abort_flag, p.status);
             mma_commit(bar(K_TEARDOWN));
             mbar_wait_drain(bar(K_TEARDOWN), 0);  // ignores the abort flag
         }
         __syncwarp();
-    } else {
+    } else if (warp < kLoadWarpK) {
         // ------------------------------------------- elementwise warps, epilogue
-        const int r = warp * 32 + lane;  // key of the tile = TMEM lane
+        regs_increase<kRegsElemK>();
+        const int hg = warp >> 2;  // warpgroup = half of the tile's rows
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;  // key of the CTA = TMEM lane
         const int key = k0 + r;
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tS = tmem + lane_off + L::ST_COL + hg * kHalfK;
+        const uint32_t tP = tmem + lane_off + L::DPT_COL + hg * kHalfK;
         bool ok = true;
         for (int t = 0; t < ntiles && ok; ++t) {
-            const int bf = t & 1, s = t % kStagesK;
-            if (!warp_wait_t(bar(K_S_FULL + bf), (uint32_t)(t >> 1) & 1u, abort_flag, wl)) {
+            const int s = t % kStagesK;
+            const uint32_t tp = (uint32_t)t & 1u;
+            if (!warp_wait_t(bar(K_S_FULL), tp, abort_flag, wl)) {
                 ok = false;
                 break;
             }
             // the tile's row statistics: published with its row_full phase (the
             // stage is not refilled before this tile's dV / dK MMAs, which wait
-            // for this warpgroup)
+            // for both warpgroups)
             if (!warp_wait_t(row_full(s), (uint32_t)(t / kStagesK) & 1u, abort_flag, wl)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t tS = tmem + lane_off + L::ST_COL + bf * kRowsK;
-            const uint32_t tP = tmem + lane_off + L::DPT_COL + bf * kRowsK;
-            uint32_t sv[2][32], pv[2][32];
-            tmem_ld32(tS, sv[0]);
-            tmem_ld32(tS + 32, sv[1]);
-            tmem_ld32(tP, pv[0]);
-            tmem_ld32(tP + 32, pv[1]);
-            tmem_ld_wait();
-            const float *st = stats + s * 4 * kRowsK;
-            const int *sti = reinterpret_cast<const int *>(st);
-            const bool inner = flags[s] != 0;  // the same for every thread
-            uint32_t pk[32], dk[32];
-            // P^T and dS^T of the tile; rows that may not see this key give 0.
-            // Interior tiles (every row sees every key of the CTA) skip the
-            // row bounds; elsewhere they are combined without short-circuit
-            // (a per-key || / && compiled to branches, ~3x the step's cost).
-            auto body = [&](auto masked) {
+            const float *st = stats + s * 4 * kRowsK + hg * kHalfK;
+            const int *sti = reinterpret_cast<const int *>(stats + s * 4 * kRowsK) + hg * kHalfK;
+            // Rows that may not see this key give P = dS = 0.  Interior tiles
+            // (every row sees every key of the CTA; the flag is the same for
+            // every thread) take a path without the test; elsewhere bit `row`
+            // of keep[row / 32], built once a tile, is tested against
+            // compile-time bits (a per-key || / && compiled to branches, ~3x
+            // the step's cost).  Pairs of rows share packed f32x2 arithmetic:
+            // with eight elementwise warps the step is bound by issue.
+            const bool inner = flags[s] != 0;
+            uint32_t keep[2] = {0xffffffffu, 0xffffffffu};
+            if (!inner) {
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        float pp[2], dd[2];
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int row = hf * 32 + i + e;
-                            const float pr =
-                                ex2f(__uint_as_float(sv[hf][i + e]) * a.c2 - st[row]);
-                            const float d =
-                                pr * (__uint_as_float(pv[hf][i + e]) - st[kRowsK + row]);
-                            if (decltype(masked)::value) {
-                                const bool legal = (key >= sti[2 * kRowsK + row]) &
-                                                   (key < sti[3 * kRowsK + row]);
-                                pp[e] = legal ? pr : 0.f;
-                                dd[e] = legal ? d : 0.f;
-                            } else {
-                                pp[e] = pr;
-                                dd[e] = d;
-                            }
-                        }
-                        pk[hf * 16 + i / 2] = pack16<T>(pp[0], pp[1]);
-                        dk[hf * 16 + i / 2] = pack16<T>(dd[0], dd[1]);
+                for (int w = 0; w < 2; ++w) {
+                    uint32_t m = 0;
+#pragma unroll 8
+                    for (int i = 0; i < 32; ++i) {
+                        const int row = w * 32 + i;
+                        const bool in = (key >= sti[2 * kRowsK + row]) & (key < sti[3 * kRowsK + row]);
+                        m |= (in ? 1u : 0u) << i;
                     }
+                    keep[w] = m;
+                }
+            }
+            const uint64_t c2 = f2pack(a.c2, a.c2);
+            float pr[kHalfK];
+            // P^T: 2^(S c - LSE), then 16-bit pairs over the first half of this
+            // half's S^T columns
+            auto p_phase = [&](auto masked) {
+#pragma unroll
+                for (int c = 0; c < kHalfK / 32; ++c) {
+                    uint32_t sv[32];
+                    tmem_ld32(tS + c * 32, sv);
+                    tmem_ld_wait();
+                    const float4 *l4 = reinterpret_cast<const float4 *>(st + c * 32);
+#pragma unroll
+                    for (int i4 = 0; i4 < 8; ++i4) {
+                        const float4 nl = l4[i4];  // -LSE of four rows
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            const int i = 4 * i4 + 2 * h2;
+                            const uint64_t x2 = ffma2(
+                                f2pack(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), c2,
+                                h2 == 0 ? f2pack(nl.x, nl.y) : f2pack(nl.z, nl.w));
+                            float x0, x1;
+                            f2unpack(x2, x0, x1);
+                            float e0 = ex2f(x0), e1 = ex2f(x1);
+                            if (decltype(masked)::value) {
+                                e0 = ((keep[c] >> i) & 1u) ? e0 : 0.f;
+                                e1 = ((keep[c] >> (i + 1)) & 1u) ? e1 : 0.f;
+                            }
+                            pr[c * 32 + i] = e0;
+                            pr[c * 32 + i + 1] = e1;
+                            sv[i / 2] = pack16<T>(e0, e1);  // over the consumed sv[i / 2]
+                        }
+                    }
+                    tmem_st16(tS + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(sv));
+                }
+            };
+            // dS^T: P (dP - Dq), likewise over dP^T
+            auto ds_phase = [&](auto masked) {
+#pragma unroll
+                for (int c = 0; c < kHalfK / 32; ++c) {
+                    uint32_t pv[32];
+                    tmem_ld32(tP + c * 32, pv);
+                    tmem_ld_wait();
+                    const float4 *d4 = reinterpret_cast<const float4 *>(st + kRowsK + c * 32);
+#pragma unroll
+                    for (int i4 = 0; i4 < 8; ++i4) {
+                        const float4 nd = d4[i4];  // -Dq of four rows
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            const int i = 4 * i4 + 2 * h2;
+                            const uint64_t y2 = fmul2(
+                                fadd2(f2pack(__uint_as_float(pv[i]), __uint_as_float(pv[i + 1])),
+                                      h2 == 0 ? f2pack(nd.x, nd.y) : f2pack(nd.z, nd.w)),
+                                f2pack(pr[c * 32 + i], pr[c * 32 + i + 1]));
+                            float d0, d1;
+                            f2unpack(y2, d0, d1);
+                            if (decltype(masked)::value) {
+                                d0 = ((keep[c] >> i) & 1u) ? d0 : 0.f;
+                                d1 = ((keep[c] >> (i + 1)) & 1u) ? d1 : 0.f;
+                            }
+                            pv[i / 2] = pack16<T>(d0, d1);  // over the consumed pv[i / 2]
+                        }
+                    }
+                    tmem_st16(tP + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(pv));
+                }
             };
             if (inner)
-                body(std::false_type{});
+                p_phase(std::false_type{});
             else
-                body(std::true_type{});
-            tmem_st32(tS, pk);  // P^T over the first half of S^T_bf
-            tmem_st32(tP, dk);  // dS^T over the first half of dP^T_bf
+                p_phase(std::true_type{});
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(bar(K_DS_READY + bf));
+            mbar_arrive(bar(K_P_READY + hg));
+            if (!warp_wait_t(bar(K_DP_FULL), tp, abort_flag, wl)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (inner)
+                ds_phase(std::false_type{});
+            else
+                ds_phase(std::true_type{});
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar(K_DS_READY + hg));
         }
         if (!ok && lane == 0) raise_abort_t(abort_flag, p.status);
-        // epilogue: dV and dK * scale to memory (zeros for keys no row sees)
+        // epilogue: warpgroup 0 writes dV, warpgroup 1 dK * scale (zeros for
+        // keys no row sees)
         if (ok && ntiles > 0) {
             ok = warp_wait_t(bar(K_ACC_FULL), 0, abort_flag, wl);
             if (!ok && lane == 0) raise_abort_t(abort_flag, p.status);
@@ -764,46 +910,35 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         const bool writes = key < kcap;
         const bool has = ok && ntiles > 0;
         const long long krow = (si.k_off + key) * p.Hkv + kvh;
-        T *dvg = static_cast<T *>(bp.dv), *dkg = static_cast<T *>(bp.dk);
+        const int W = hg == 0 ? p.Dv : p.D;
+        const int WT = hg == 0 ? DV : D;
+        const float sc = hg == 0 ? 1.f : p.scale;
+        T *dst = static_cast<T *>(hg == 0 ? bp.dv : bp.dk) + krow * W;
+        const uint32_t col0 = hg == 0 ? L::DV_COL : L::DK_COL;
 #pragma unroll
-        for (int c = 0; c < DV / 32; ++c) {
-            uint32_t v[32];
-            if (has) {
-                tmem_ld32(tmem + lane_off + L::DV_COL + c * 32, v);
-                tmem_ld_wait();
-            }
-            if (writes) {
-                auto f = [&](int i) { return has ? __uint_as_float(v[i]) : 0.f; };
+        for (int c = 0; c < 4; ++c) {
+            if (c * 32 < WT) {
+                uint32_t v[32];
+                if (has) {
+                    tmem_ld32(tmem + lane_off + col0 + c * 32, v);
+                    tmem_ld_wait();
+                }
+                if (writes) {
+                    auto f = [&](int i) { return has ? __uint_as_float(v[i]) * sc : 0.f; };
 #pragma unroll
-                for (int i = 0; i < 32; i += 8)
-                    if (c * 32 + i < p.Dv)
-                        *reinterpret_cast<uint4 *>(dvg + krow * p.Dv + c * 32 + i) =
-                            make_uint4(pack16<T>(f(i), f(i + 1)), pack16<T>(f(i + 2), f(i + 3)),
-                                       pack16<T>(f(i + 4), f(i + 5)), pack16<T>(f(i + 6), f(i + 7)));
-            }
-        }
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-            uint32_t v[32];
-            if (has) {
-                tmem_ld32(tmem + lane_off + L::DK_COL + c * 32, v);
-                tmem_ld_wait();
-            }
-            if (writes) {
-                auto f = [&](int i) { return has ? __uint_as_float(v[i]) * p.scale : 0.f; };
-#pragma unroll
-                for (int i = 0; i < 32; i += 8)
-                    if (c * 32 + i < p.D)
-                        *reinterpret_cast<uint4 *>(dkg + krow * p.D + c * 32 + i) =
-                            make_uint4(pack16<T>(f(i), f(i + 1)), pack16<T>(f(i + 2), f(i + 3)),
-                                       pack16<T>(f(i + 4), f(i + 5)), pack16<T>(f(i + 6), f(i + 7)));
+                    for (int i = 0; i < 32; i += 8)
+                        if (c * 32 + i < W)
+                            *reinterpret_cast<uint4 *>(dst + c * 32 + i) = make_uint4(
+                                pack16<T>(f(i), f(i + 1)), pack16<T>(f(i + 2), f(i + 3)),
+                                pack16<T>(f(i + 4), f(i + 5)), pack16<T>(f(i + 6), f(i + 7)));
+                }
             }
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == kMmaWarpT) {
+    if (warp == kMmaWarpK) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -843,7 +978,7 @@ int launch_kv_t(const BwdParams &bp, bool bf16, cudaStream_t stream) {
         set_error("tcgen05 dK/dV: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         return 3;
     }
-    kern<<<(unsigned)grid, kThreadsT, L::SMEM, stream>>>(a, tq, to, tk, tv);
+    kern<<<(unsigned)grid, kThreadsK, L::SMEM, stream>>>(a, tq, to, tk, tv);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("tcgen05 dK/dV launch: %s", cudaGetErrorString(e));
@@ -930,7 +1065,7 @@ bool bwd_dq_tc_supported(const AttnParams &p, int dtype) {
 }
 
 bool bwd_dkdv_tc_supported(const AttnParams &p, int dtype) {
-    // the rows of a tile are (position, head) pairs of one KV group: 64 / G positions
+    // the rows of a tile are (position, head) pairs of one KV group: 128 / G positions
     return bwd_dq_tc_supported(p, dtype) && p.G >= 1 && p.G <= kRowsK && kRowsK % p.G == 0;
 }
 
