@@ -78,7 +78,7 @@ int make_tma_map_4d(CUtensorMap *map, const void *ptr, bool bf16, uint64_t d0, u
 // [64, 128], not paged); bp.delta must already hold rowsum(dO * O).
 bool bwd_dq_tc_supported(const AttnParams &p, int dtype);
 int launch_bwd_dq_tc(const BwdParams &bp, int dtype, cudaStream_t stream);
-// tcgen05 dK/dV kernel: as bwd_dq_tc_supported, and Hq / Hkv divides 64.
+// tcgen05 dK/dV kernel: as bwd_dq_tc_supported, and Hq / Hkv divides 128.
 bool bwd_dkdv_tc_supported(const AttnParams &p, int dtype);
 int launch_bwd_dkdv_tc(const BwdParams &bp, int dtype, cudaStream_t stream);
 

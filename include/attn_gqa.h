@@ -327,7 +327,7 @@ ATTN_API int attn_fwd_staged(const void *hq, const void *hk, const void *hv, voi
  *                 ATTN_ALGO_MMA (mma.sync dK/dV and dQ; bf16/fp16, widths
  *                 multiples of 8 up to 128) or ATTN_ALGO_TCGEN05 (tcgen05
  *                 dQ and dK/dV kernels -- the dK/dV one when Hq / Hkv
- *                 divides 64, else mma.sync; bf16/fp16, widths multiples of
+ *                 divides 128, else mma.sync; bf16/fp16, widths multiples of
  *                 16 in [64, 128], padded or packed layout)
  * Head widths up to 256 (wider ones return ATTN_ERR_UNSUPPORTED).
  * All pointers are device memory, 16-byte aligned.  A workspace of

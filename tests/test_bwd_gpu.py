@@ -117,7 +117,7 @@ CASES = [
     ("bf16", "mma", 1, 16, 2, 90, 140, 128, 128, 0, 0, True),    # G = 8
     ("f16", "mma", 1, 32, 2, 40, 70, 64, 64, 30, 0, False),      # G = 16, window
     ("bf16", "mma", 2, 8, 2, 300, 300, 128, 128, 0, 0, False),   # several row tiles of a key tile
-    # tcgen05 dQ (with mma.sync dK/dV)
+    # tcgen05 dQ and dK/dV (mma.sync dK/dV where Hq / Hkv does not divide 128)
     ("bf16", "tcgen05", 2, 8, 2, 200, 200, 128, 128, 0, 0, True),
     ("bf16", "tcgen05", 1, 8, 2, 130, 330, 128, 128, 0, 0, False),
     ("f16", "tcgen05", 2, 4, 2, 150, 300, 64, 64, 70, 0, True),
@@ -130,6 +130,9 @@ CASES = [
     ("bf16", "tcgen05", 1, 6, 2, 90, 150, 128, 128, 0, 0, True),   # G = 3: mma.sync dK/dV
     ("bf16", "tcgen05", 1, 16, 1, 70, 300, 128, 128, 50, 0, True),  # G = 16, window
     ("f16", "tcgen05", 2, 8, 8, 260, 260, 96, 80, 0, 1, True),     # MHA, padded widths
+    ("bf16", "tcgen05", 1, 64, 2, 50, 120, 64, 64, 0, 0, True),    # G = 32: 4 positions a row tile
+    ("bf16", "tcgen05", 1, 64, 1, 33, 90, 128, 128, 0, 0, True),   # G = 64
+    ("f16", "tcgen05", 1, 128, 1, 21, 60, 64, 64, 0, 1, False),    # G = 128: one position a tile
 ]
 
 
