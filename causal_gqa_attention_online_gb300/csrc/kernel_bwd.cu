@@ -851,9 +851,37 @@ int launch_mma_bwd_t(const BwdParams &bp, bool tc_dq, cudaStream_t stream) {
     if (!grid_fits(ktiles, y) || !grid_fits(((long long)p.Q * p.G + kQRows - 1) / kQRows, y))
         return 2;
     int rc = 0;
-    if (ktiles > 0 && tc_dq && bwd_dkdv_tc_supported(p, std::is_same<T, __half>::value ? 1 : 2)) {
-        rc = launch_bwd_dkdv_tc(bp, std::is_same<T, __half>::value ? 1 : 2, stream);
+    const int dt = std::is_same<T, __half>::value ? 1 : 2;
+    if (ktiles > 0 && tc_dq && bwd_dkdv_tc_supported(p, dt)) {
+        // The dQ kernel does not read what the dK/dV kernel writes (both read
+        // only the inputs and Dq), so it runs on a second stream beside it
+        // and fills the SMs the dK/dV kernel's last, longest CTAs leave idle:
+        // fork after Dq, join before returning.
+        cudaStream_t side = nullptr;
+        rc = side_stream(&side);
         if (rc) return rc;
+        cudaEvent_t fork = nullptr, join = nullptr;
+        cudaError_t e = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&join, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventRecord(fork, stream);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(side, fork, 0);
+        if (e != cudaSuccess) {
+            set_error("backward fork: %s", cudaGetErrorString(e));
+            if (fork) cudaEventDestroy(fork);
+            if (join) cudaEventDestroy(join);
+            return 3;
+        }
+        rc = launch_bwd_dkdv_tc(bp, dt, stream);
+        const int rq = launch_bwd_dq_tc(bp, dt, side);
+        e = cudaEventRecord(join, side);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, join, 0);
+        cudaEventDestroy(fork);  // released once the recorded work completes
+        cudaEventDestroy(join);
+        if (e != cudaSuccess) {
+            set_error("backward join: %s", cudaGetErrorString(e));
+            return 3;
+        }
+        return rc ? rc : rq;
     } else if (ktiles > 0) {
         const size_t s = (size_t)kMKeys * 2 * (DW + DVW) +
                          (size_t)kMStages * kMRows * (2 * (DW + DVW) + 16) + 4 * 16 * 32 * 4 +
@@ -862,7 +890,7 @@ int launch_mma_bwd_t(const BwdParams &bp, bool tc_dq, cudaStream_t stream) {
                       "bwd_dkdv_mma", bp);
         if (rc) return rc;
     }
-    if (tc_dq) return launch_bwd_dq_tc(bp, std::is_same<T, __half>::value ? 1 : 2, stream);
+    if (tc_dq) return launch_bwd_dq_tc(bp, dt, stream);
     const size_t s = (size_t)kQRows * 2 * (DW + DVW) + (size_t)2 * kQKeys * 2 * (DW + DVW);
     const long long qtiles = ((long long)p.Q * p.G + kQRows - 1) / kQRows;
     return launch_k(bwd_dq_mma<T, DW, DVW>, dim3((unsigned)(qtiles * y)), 128, s, stream,

@@ -82,6 +82,9 @@ int launch_bwd_dq_tc(const BwdParams &bp, int dtype, cudaStream_t stream);
 bool bwd_dkdv_tc_supported(const AttnParams &p, int dtype);
 int launch_bwd_dkdv_tc(const BwdParams &bp, int dtype, cudaStream_t stream);
 
+// A second, library-owned stream of the current device (created once).
+int side_stream(cudaStream_t *out);
+
 // Backward: rowsum(dO * O), then dK/dV and dQ.  mode 0: the CUDA-core
 // kernels; 1: the mma.sync kernels (bf16/fp16, bwd_mma_supported); 2: the
 // tcgen05 dQ kernel (bwd_dq_tc_supported) and the tcgen05 dK/dV kernel where
