@@ -61,30 +61,65 @@ __device__ __forceinline__ void row_range(const AttnParams &p, const SeqInfo &si
 // ---------------------------------------------------------------------------
 // Dq = rowsum(dO * O), one warp per (token, head) row.
 
+// Dq = rowsum(dO * O), one float a row.  A warp covers kDeltaRows rows: a
+// row is split over L lanes of 16-byte loads (L = Dv / 8 rounded up to a power
+// of two, at most 32), 32 / L rows a pass, and every load of the warp is
+// issued before any arithmetic, so enough bytes are in flight to run at the
+// HBM rate (one 256-byte row a warp left it at half of it).
+constexpr int kDeltaRows = 8;     // rows per warp
+constexpr int kDeltaWarps = 8;    // warps per block
+
 template <typename T>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const BwdParams bp, long long rows) {
-    const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (row >= rows) return;
+    const long long row0 = ((long long)blockIdx.x * kDeltaWarps + (threadIdx.x >> 5)) * kDeltaRows;
+    if (row0 >= rows) return;
     const int Dv = bp.f.Dv;
-    const T *o = static_cast<const T *>(bp.f.o) + row * Dv;
-    const T *g = static_cast<const T *>(bp.dout) + row * Dv;
-    float acc = 0.f;
+    const T *ob = static_cast<const T *>(bp.f.o);
+    const T *gb = static_cast<const T *>(bp.dout);
     constexpr int kVec = 16 / sizeof(T);
-    if (Dv % kVec == 0) {
-        for (int j = lane * kVec; j < Dv; j += 32 * kVec) {
-            const uint4 ov = *reinterpret_cast<const uint4 *>(o + j);
-            const uint4 gv = *reinterpret_cast<const uint4 *>(g + j);
-            const T *oe = reinterpret_cast<const T *>(&ov);
-            const T *ge = reinterpret_cast<const T *>(&gv);
+    const int nchunk = Dv / kVec;
+    if (Dv % kVec == 0 && nchunk <= 32) {
+        int L = 1;
+        while (L < nchunk) L *= 2;
+        const int rpp = 32 / L;  // rows a pass
+        const int sub = lane / L, c = lane % L;
+        const bool active = c < nchunk;
+        constexpr int kMaxPass = kDeltaRows;  // L = 1 .. 32: passes = 8 / rpp <= 8
+        uint4 ov[kMaxPass], gv[kMaxPass];
+        const int npass = (kDeltaRows + rpp - 1) / rpp;
+#pragma unroll
+        for (int ps = 0; ps < kMaxPass; ++ps) {
+            ov[ps] = gv[ps] = make_uint4(0, 0, 0, 0);
+            const long long row = row0 + (long long)ps * rpp + sub;
+            if (ps < npass && active && ps * rpp + sub < kDeltaRows && row < rows) {
+                ov[ps] = *reinterpret_cast<const uint4 *>(ob + row * Dv + c * kVec);
+                gv[ps] = *reinterpret_cast<const uint4 *>(gb + row * Dv + c * kVec);
+            }
+        }
+#pragma unroll
+        for (int ps = 0; ps < kMaxPass; ++ps) {
+            if (ps >= npass) break;  // uniform
+            const T *oe = reinterpret_cast<const T *>(&ov[ps]);
+            const T *ge = reinterpret_cast<const T *>(&gv[ps]);
+            float acc = 0.f;
 #pragma unroll
             for (int e = 0; e < kVec; ++e) acc += to_f32(oe[e]) * to_f32(ge[e]);
+            for (int off = L / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            const long long row = row0 + (long long)ps * rpp + sub;
+            if (c == 0 && ps * rpp + sub < kDeltaRows && row < rows) bp.delta[row] = acc;
         }
     } else {
-        for (int j = lane; j < Dv; j += 32) acc += to_f32(o[j]) * to_f32(g[j]);
+        for (int r = 0; r < kDeltaRows; ++r) {
+            const long long row = row0 + r;
+            if (row >= rows) break;
+            float acc = 0.f;
+            for (int j = lane; j < Dv; j += 32)
+                acc += to_f32(ob[row * Dv + j]) * to_f32(gb[row * Dv + j]);
+            acc = warp_sum(acc);
+            if (lane == 0) bp.delta[row] = acc;
+        }
     }
-    acc = warp_sum(acc);
-    if (lane == 0) bp.delta[row] = acc;
 }
 
 // ---------------------------------------------------------------------------
@@ -909,8 +944,9 @@ int launch_mma_bwd(const BwdParams &bp, bool tc_dq, cudaStream_t stream) {
 template <typename T>
 int launch_bwd_t(const BwdParams &bp, int mode, cudaStream_t stream) {
     const long long rows = bp.f.Tq * bp.f.Hq;
-    int rc = launch_k(bwd_delta_kernel<T>, dim3((unsigned)((rows + 7) / 8)), 256, 0, stream,
-                      "bwd_delta", bp, rows);
+    const long long per_block = (long long)kDeltaWarps * kDeltaRows;
+    int rc = launch_k(bwd_delta_kernel<T>, dim3((unsigned)((rows + per_block - 1) / per_block)), 256,
+                      0, stream, "bwd_delta", bp, rows);
     if (rc) return rc;
     if constexpr (!std::is_same<T, float>::value) {
         if (mode != 0) return launch_mma_bwd<T>(bp, mode == 2, stream);
