@@ -308,3 +308,33 @@ def test_bwd_full_size_sampled():
     want_dv = gg.sum(dim=(1, 3))
     bound = 2 * u * (dv.double().abs().sum(dim=1) + gg.abs().sum(dim=(1, 3))) + 1e-3
     assert bool(((sum_dv - want_dv).abs() <= bound).all()), "value gradients do not sum to dO"
+
+
+def test_sdpa_example_shape_forward_and_backward():
+    """The SDPA usage example of "Accelerating PyTorch on AMD GPUs with FlyDSL"
+    (q, k, v of shape (4, 16, 4096, 128) bf16, is_causal=True, then the
+    backward), as a synthetic shape: MHA (G = 1), so the dK/dV kernel's row
+    tiles hold 128 positions of one head.  Forward: every row against the
+    oracle; backward: sampled dQ rows and the last 64 keys of two heads."""
+    inp = synth.make_padded(4, 16, 16, 4096, 4096, 128, 128, "bf16", seed=1166)
+    parity.check(inp, "auto", "SDPA example forward")
+    dout = synth.make_dout(inp, seed=1167)
+    dev = torch.device("cuda")
+    q, k, v, g = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev), dout.to(dev)
+    o, lse = attn_fwd(q, k, v)
+    dq, dk, dv = attn_bwd(q, k, v, o, lse, g)
+    torch.cuda.synchronize()
+    B, H, S, D = 4, 16, 4096, 128
+    kw = dict(B=B, Hq=H, Hkv=H, Q=S, K=S, D=D, Dv=D, scale=inp.scale)
+    qf, kf, vf, gf = (synth.exact_f32(t) for t in (inp.q, inp.k, inp.v, dout))
+    rng = np.random.default_rng(1168)
+    rows = np.stack([rng.integers(0, B, 600), rng.integers(0, S, 600),
+                     rng.integers(0, H, 600)], axis=1).astype(np.int32)
+    ref_q, _, _ = oracle.attn_bwd_sampled(qf, kf, vf, gf, rows=rows, **kw)
+    compare_one("bf16", dq.float().cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]], ref_q,
+                "SDPA example dq rows")
+    dkc, dvc = dk.float().cpu().numpy(), dv.float().cpu().numpy()
+    for b, kh in ((0, 3), (B - 1, H - 1)):
+        _, ref_k, ref_v = oracle.attn_bwd_sampled(qf, kf, vf, gf, key_block=(b, kh, S - 64, S), **kw)
+        compare_one("bf16", dkc[b, S - 64:, kh], ref_k, f"SDPA example dk b={b} h={kh}")
+        compare_one("bf16", dvc[b, S - 64:, kh], ref_v, f"SDPA example dv b={b} h={kh}")
