@@ -27,11 +27,17 @@
 // are merged through shared memory at the end, and rows spanning several
 // splits are merged by the combine kernel (the legal (max, sum, acc) merge of
 // section 5).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <climits>
+#include <cstring>
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
 #include "mma_sync.cuh"
+#include "sm100_ptx.cuh"
 
 namespace attn {
 namespace {
@@ -40,10 +46,28 @@ constexpr int kTK = 64;      // keys per tile (4 warps x 16)
 constexpr int kStages = 3;
 constexpr int kThreads = 128;
 
-// PAGED: K / V rows found through the block table (a separate instance, so
-// that the contiguous layout's load loop carries no paging code).
-template <typename T, int D, int DV, int NT, bool PAGED>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p) {
+// How K / V tiles come in.  kLoadTma: one thread issues TMA copies of 64-row
+// boxes (one per 64 columns) onto the stage's mbarrier -- the contiguous layout,
+// and paged K / V with pages of at least 64 rows (a 64-key tile is then one
+// page).  kLoadAsync / kLoadAsyncPaged: every thread issues 16-byte cp.async
+// copies, the latter finding each row through the block table (pages of fewer
+// than 64 rows).
+enum : int { kLoadAsync = 0, kLoadAsyncPaged = 1, kLoadTma = 2 };
+
+// Byte offset of 16-byte chunk c of row r in a TMA-loaded tile: 64-column
+// boxes of 64 rows x 128 bytes, 8 KB apart, in the 128-byte swizzle (chunk
+// c % 8 of a row stored at c % 8 ^ r % 8), which keeps ldmatrix free of bank
+// conflicts.
+__device__ __forceinline__ int swz_box(int r, int c) {
+    return (c >> 3) * (kTK * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
+
+template <typename T, int D, int DV, int NT, int LOAD>
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV) {
+    constexpr bool PAGED = LOAD == kLoadAsyncPaged;
+    constexpr bool TMA = LOAD == kLoadTma;
     constexpr int R = NT * 8;               // query rows of a (sequence, KV head)
     constexpr int KROW = D * 2, VROW = DV * 2;
     constexpr int KTILE = kTK * KROW, VTILE = kTK * VROW;
@@ -77,7 +101,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p)
     // while this grid's last blocks run; it waits for our completion itself
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     if (!mine) return;
-    const int kbeg = max(lo_min, split * p.split_len);
+    // TMA tiles start on a 64-key boundary, so a tile is one page of a paged
+    // layout; the keys this adds before the first legal one are masked
+    const int kbeg0 = max(lo_min, split * p.split_len);
+    const int kbeg = TMA ? (kbeg0 & ~(kTK - 1)) : kbeg0;
     const int kend = min(hi_max, (split + 1) * p.split_len);
     const int ntiles = kend > kbeg ? (kend - kbeg + kTK - 1) / kTK : 0;
 
@@ -87,6 +114,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p)
     const T *kg = static_cast<const T *>(p.k);
     const T *vg = static_cast<const T *>(p.v);
     const uint32_t sbase = smem_u32(smem);
+    const uint32_t fbar = sbase + kStages * STAGE;  // TMA: one full barrier a stage
+    if (TMA) {
+        if (tid == 0) {
+            for (int s = 0; s < kStages; ++s) sm100::mbar_init(fbar + 8u * s, 1);
+            sm100::fence_mbar_init();
+        }
+        __syncthreads();
+    }
 
     // Q^T fragments (B operand of S^T = K Q^T): column n = query row g.
     uint32_t qf[D / 16][NT][2];
@@ -119,9 +154,27 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p)
             rhi[nt][e] = min(hi, kend);
         }
 
+    uint32_t armed = 0, armed_ph = 0;  // TMA: stages with a copy in flight, its phase
     auto load_tile = [&](int t) {
         const int key0 = kbeg + t * kTK;
         const uint32_t st = sbase + (t % kStages) * STAGE;
+        if constexpr (TMA) {
+            if (tid == 0) {
+                const int row = (int)kv_row(p, si, b, key0);
+                const uint32_t fb = fbar + 8u * (t % kStages);
+                sm100::mbar_arrive_expect_tx(fb, KTILE + VTILE);
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    sm100::tma_load_4d(st + c * kTK * 128, &tmK, fb, c * 64, kvh, row, 0);
+#pragma unroll
+                for (int c = 0; c < DV / 64; ++c)
+                    sm100::tma_load_4d(st + KTILE + c * kTK * 128, &tmV, fb, c * 64, kvh, row, 0);
+                armed |= 1u << (t % kStages);
+                armed_ph = (armed_ph & ~(1u << (t % kStages))) |
+                           (((uint32_t)(t / kStages) & 1u) << (t % kStages));
+            }
+            return;
+        }
         constexpr int CK = D / 8, CV = DV / 8;
         // paged: a tile that starts on a 64-key boundary lies in one page when
         // pages hold at least 64 rows (one table read); otherwise a read per
@@ -163,14 +216,42 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p)
 #pragma unroll
     for (int s = 0; s < kStages - 1; ++s) {
         if (s < ntiles) load_tile(s);
-        cp_async_commit();
+        if (!TMA) cp_async_commit();
     }
 
+    bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
-        cp_async_wait<kStages - 2>();
-        __syncthreads();  // tile t visible to all; tile t-1's stage is free
-        if (t + kStages - 1 < ntiles) load_tile(t + kStages - 1);
-        cp_async_commit();
+        if constexpr (TMA) {
+            // tile t has landed (a bounded wait: a copy that never lands records
+            // a status, and the block stops with its outputs unwritten)
+            const bool got = sm100::mbar_wait_drain(fbar + 8u * (t % kStages),
+                                             (uint32_t)(t / kStages) & 1u, p.wait_ns);
+            if (!__syncthreads_and(got)) {
+                ok = false;
+                break;
+            }
+            armed &= ~(1u << (t % kStages));
+            // V rows past the split's last key may hold anything (NaN included):
+            // their P is 0, and 0 * NaN must not reach O
+            const int nreal = kend - (kbeg + t * kTK);
+            if (nreal < kTK) {
+                uint8_t *vt = smem + (t % kStages) * STAGE + KTILE;
+                const int nz = (kTK - nreal) * 8;  // 16-byte chunks a box
+                for (int i = tid; i < nz * (DV / 64); i += kThreads) {
+                    const int bx = i / nz, j = i % nz;
+                    *reinterpret_cast<uint4 *>(vt + bx * kTK * 128 + nreal * 128 + j * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+                sm100::fence_proxy_async_smem();
+            }
+            __syncthreads();  // tile t visible to all; tile t-1's stage is free
+            if (t + kStages - 1 < ntiles) load_tile(t + kStages - 1);
+        } else {
+            cp_async_wait<kStages - 2>();
+            __syncthreads();  // tile t visible to all; tile t-1's stage is free
+            if (t + kStages - 1 < ntiles) load_tile(t + kStages - 1);
+            cp_async_commit();
+        }
 
         const uint32_t ks = sbase + (t % kStages) * STAGE;
         const uint32_t vs = ks + KTILE;
@@ -187,7 +268,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p)
         for (int kk = 0; kk < D / 16; ++kk) {
             uint32_t a[4];
             const int row = kw0 + (lane & 15);
-            ldmatrix_x4(a, ks + swz(row, kk * 2 + (lane >> 4), KROW));
+            ldmatrix_x4(a, ks + (TMA ? swz_box(row, kk * 2 + (lane >> 4))
+                                     : swz(row, kk * 2 + (lane >> 4), KROW)));
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) MmaOp<T>::run(sacc[nt], a, qf[kk][nt][0], qf[kk][nt][1]);
         }
@@ -231,12 +313,23 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p)
             uint32_t a[4];
             const int mi = lane >> 3;
             const int key = kw0 + (mi >> 1) * 8 + (lane & 7);
-            ldmatrix_x4_trans(a, vs + swz(key, mt * 2 + (mi & 1), VROW));
+            ldmatrix_x4_trans(a, vs + (TMA ? swz_box(key, mt * 2 + (mi & 1))
+                                           : swz(key, mt * 2 + (mi & 1), VROW)));
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) MmaOp<T>::run(oacc[mt][nt], a, pb[nt][0], pb[nt][1]);
         }
     }
-    cp_async_wait<0>();
+    if (TMA && !ok) {
+        // copies still in flight land before the block exits (a wait that
+        // ignores the abort: they always land); the outputs stay unwritten
+        if (tid == 0) {
+            report_status(p.status, kStatusTimeoutDecode);
+            for (int s2 = 0; s2 < kStages; ++s2)
+                if (armed & (1u << s2)) sm100::mbar_wait_drain(fbar + 8u * s2, (armed_ph >> s2) & 1u);
+        }
+        return;
+    }
+    if (!TMA) cp_async_wait<0>();
     __syncthreads();  // ring drained: reuse it as the merge buffer
 
     // Merge the four warps' states: buffer [warp][row][dv] + per-warp (m, l).
@@ -308,15 +401,32 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const AttnParams p)
 
 template <typename T, int D, int DV, int NT>
 int launch_decode_t(const AttnParams &p, cudaStream_t stream) {
-    constexpr int smem = kStages * kTK * (D + DV) * 2;
-    auto kern = p.block_table ? decode_kernel<T, D, DV, NT, true> : decode_kernel<T, D, DV, NT, false>;
+    constexpr int smem = kStages * kTK * (D + DV) * 2 + 64;  // ring + TMA barriers
+    // K / V by TMA as flat [rows][Hkv][D] arrays (rows: B * K padded, Tk
+    // packed, the page pool when paged); cp.async where pages hold fewer
+    // than 64 rows or a tensor map cannot be made
+    const bool bf16 = std::is_same<T, __nv_bfloat16>::value;
+    const long long rows = p.block_table ? (long long)p.num_pages * p.page_size
+                                         : (p.cu_q ? p.Tk : (long long)p.B * p.K);
+    CUtensorMap tk, tv;
+    memset(&tk, 0, sizeof(tk));
+    memset(&tv, 0, sizeof(tv));
+    bool tma = (!p.block_table || p.page_size >= kTK) && rows > 0 && rows < (1LL << 31);
+    if (tma) {
+        tma = make_tma_map_4d(&tk, p.k, bf16, (uint64_t)D, p.Hkv, (uint64_t)rows, 1, 1, kTK) == 0 &&
+              make_tma_map_4d(&tv, p.v, bf16, (uint64_t)DV, p.Hkv, (uint64_t)rows, 1, 1, kTK) == 0;
+        if (!tma) clear_error();
+    }
+    auto kern = tma ? decode_kernel<T, D, DV, NT, kLoadTma>
+                    : (p.block_table ? decode_kernel<T, D, DV, NT, kLoadAsyncPaged>
+                                     : decode_kernel<T, D, DV, NT, kLoadAsync>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) {
         set_error("decode kernel: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         return 3;
     }
     dim3 grid((unsigned)p.nsplit, (unsigned)(p.B * p.Hkv));
-    kern<<<grid, kThreads, smem, stream>>>(p);
+    kern<<<grid, kThreads, smem, stream>>>(p, tk, tv);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("decode kernel launch: %s", cudaGetErrorString(e));
