@@ -20,7 +20,6 @@ thread_local char g_last_error[512] = "";
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mutex;
 cudaMemPool_t g_pools[kMaxDevices] = {};
-cudaStream_t g_side[kMaxDevices] = {};  // second stream for concurrent backward kernels
 int *g_status_ptr[kMaxDevices] = {};
 int g_sm_count[kMaxDevices] = {};
 }  // namespace
@@ -55,29 +54,6 @@ int sm_count(int device) {
         g_sm_count[device] = n;
     }
     return g_sm_count[device];
-}
-
-// A second, library-owned stream of the current device (non-blocking, created
-// once): the backward runs its dQ kernel there, beside the dK/dV kernel.
-int side_stream(cudaStream_t *out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        set_error("cudaGetDevice: %s", cudaGetErrorString(e));
-        return ATTN_ERR_CUDA;
-    }
-    std::lock_guard<std::mutex> lk(g_dev_mutex);
-    if (g_side[dev] == nullptr) {
-        cudaStream_t st = nullptr;
-        e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
-        if (e != cudaSuccess) {
-            set_error("cudaStreamCreateWithFlags: %s", cudaGetErrorString(e));
-            return ATTN_ERR_CUDA;
-        }
-        g_side[dev] = st;
-    }
-    *out = g_side[dev];
-    return ATTN_OK;
 }
 
 namespace {

@@ -9,7 +9,8 @@
 // (O = softmax(scale Q K^T + mask) V with the row LSE kept), per legal (row, key):
 //
 //     P   = exp(scale q.k - LSE)          (recomputed, no stored P)
-//     Dq  = sum_j dO[j] O[j]              (one number per row: bwd_delta_kernel)
+//     Dq  = sum_j dO[j] O[j]              (one number per row: bwd_delta_kernel,
+//                                          or the tcgen05 dQ kernel for its rows)
 //     dP  = dO . v
 //     dS  = P (dP - Dq)
 //     dQ  = scale sum_k dS k      dK = scale sum_rows dS q      dV = sum_rows P dO
@@ -878,6 +879,9 @@ int launch_generic_bwd(const BwdParams &bp, cudaStream_t stream) {
     }
 }
 
+template <typename T>
+int launch_delta(const BwdParams &bp, cudaStream_t stream);
+
 template <typename T, int DW, int DVW>
 int launch_mma_bwd_t(const BwdParams &bp, bool tc_dq, cudaStream_t stream) {
     const AttnParams &p = bp.f;
@@ -888,36 +892,18 @@ int launch_mma_bwd_t(const BwdParams &bp, bool tc_dq, cudaStream_t stream) {
     int rc = 0;
     const int dt = std::is_same<T, __half>::value ? 1 : 2;
     if (ktiles > 0 && tc_dq && bwd_dkdv_tc_supported(p, dt)) {
-        // The dQ kernel does not read what the dK/dV kernel writes (both read
-        // only the inputs and Dq), so it runs on a second stream beside it
-        // and fills the SMs the dK/dV kernel's last, longest CTAs leave idle:
-        // fork after Dq, join before returning.
-        cudaStream_t side = nullptr;
-        rc = side_stream(&side);
+        // The dQ kernel computes Dq = rowsum(dO * O) of its rows itself (from
+        // the dO tile it stages anyway and O's tile, staged in ring slots before
+        // their first K / V tile) and writes it; the dK/dV kernel, launched as
+        // its programmatic dependent, sets up on the SMs the dQ kernel's last
+        // CTAs free and waits for that grid before reading Dq.  No Dq launch.
+        rc = launch_bwd_dq_tc(bp, dt, stream, 2);
         if (rc) return rc;
-        cudaEvent_t fork = nullptr, join = nullptr;
-        cudaError_t e = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&join, cudaEventDisableTiming);
-        if (e == cudaSuccess) e = cudaEventRecord(fork, stream);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(side, fork, 0);
-        if (e != cudaSuccess) {
-            set_error("backward fork: %s", cudaGetErrorString(e));
-            if (fork) cudaEventDestroy(fork);
-            if (join) cudaEventDestroy(join);
-            return 3;
-        }
-        rc = launch_bwd_dkdv_tc(bp, dt, stream);
-        const int rq = launch_bwd_dq_tc(bp, dt, side);
-        e = cudaEventRecord(join, side);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, join, 0);
-        cudaEventDestroy(fork);  // released once the recorded work completes
-        cudaEventDestroy(join);
-        if (e != cudaSuccess) {
-            set_error("backward join: %s", cudaGetErrorString(e));
-            return 3;
-        }
-        return rc ? rc : rq;
-    } else if (ktiles > 0) {
+        return launch_bwd_dkdv_tc(bp, dt, stream, true);
+    }
+    rc = launch_delta<T>(bp, stream);
+    if (rc) return rc;
+    if (ktiles > 0) {
         const size_t s = (size_t)kMKeys * 2 * (DW + DVW) +
                          (size_t)kMStages * kMRows * (2 * (DW + DVW) + 16) + 4 * 16 * 32 * 4 +
                          kMStages * 4;
@@ -925,7 +911,7 @@ int launch_mma_bwd_t(const BwdParams &bp, bool tc_dq, cudaStream_t stream) {
                       "bwd_dkdv_mma", bp);
         if (rc) return rc;
     }
-    if (tc_dq) return launch_bwd_dq_tc(bp, dt, stream);
+    if (tc_dq) return launch_bwd_dq_tc(bp, dt, stream, 0);
     const size_t s = (size_t)kQRows * 2 * (DW + DVW) + (size_t)2 * kQKeys * 2 * (DW + DVW);
     const long long qtiles = ((long long)p.Q * p.G + kQRows - 1) / kQRows;
     return launch_k(bwd_dq_mma<T, DW, DVW>, dim3((unsigned)(qtiles * y)), 128, s, stream,
@@ -942,15 +928,20 @@ int launch_mma_bwd(const BwdParams &bp, bool tc_dq, cudaStream_t stream) {
 }
 
 template <typename T>
-int launch_bwd_t(const BwdParams &bp, int mode, cudaStream_t stream) {
+int launch_delta(const BwdParams &bp, cudaStream_t stream) {
     const long long rows = bp.f.Tq * bp.f.Hq;
     const long long per_block = (long long)kDeltaWarps * kDeltaRows;
-    int rc = launch_k(bwd_delta_kernel<T>, dim3((unsigned)((rows + per_block - 1) / per_block)), 256,
-                      0, stream, "bwd_delta", bp, rows);
-    if (rc) return rc;
+    return launch_k(bwd_delta_kernel<T>, dim3((unsigned)((rows + per_block - 1) / per_block)), 256,
+                    0, stream, "bwd_delta", bp, rows);
+}
+
+template <typename T>
+int launch_bwd_t(const BwdParams &bp, int mode, cudaStream_t stream) {
     if constexpr (!std::is_same<T, float>::value) {
         if (mode != 0) return launch_mma_bwd<T>(bp, mode == 2, stream);
     }
+    const int rc = launch_delta<T>(bp, stream);
+    if (rc) return rc;
     return launch_generic_bwd<T>(bp, stream);
 }
 

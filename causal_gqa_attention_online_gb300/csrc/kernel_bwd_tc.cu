@@ -4,7 +4,8 @@
 //
 // dQ[q] = scale * sum_k dS[q,k] K[k],  dS = P (dP - Dq),  P = exp2(S c - LSE_2),
 // S = Q K^T, dP = dO V^T over each row's legal keys (the derivative of the
-// forward definition; Dq = rowsum(dO * O) comes from bwd_delta_kernel).  The
+// forward definition; Dq = rowsum(dO * O) is computed here for the CTA's rows
+// and written for the dK/dV kernel that follows, or read from memory).  The
 // structure is the dQ kernel of "Accelerating PyTorch on AMD GPUs with
 // FlyDSL", section on FMHA through AOTriton: its three products match the
 // forward's (S like the forward's S, dP likewise, dQ += dS K like O += P V),
@@ -13,14 +14,16 @@
 //
 // A CTA owns 128 query rows of one head (TMEM lane = row) and walks their
 // legal keys 64 at a time:
-//   warp 4 (one thread): TMA loads of the Q and dO tiles and a ring of K/V
-//     tiles;
+//   warp 4 (one thread): TMA loads of the Q and dO tiles, of O's tile (into
+//     the last ring slot(s), which take K/V tiles once Dq is computed) and a
+//     ring of K/V tiles;
 //   warp 5 (one thread): S_b = Q K^T and dP_b = dO V^T into TMEM buffer b =
 //     tile & 1, once the dQ products of tile - 2 have released S_b;
 //   warp 6 (one thread): once the elementwise warps have turned a tile into
 //     dS, dQ += dS K with dS read from TMEM (it overwrites S_b);
-//   warps 0-3: per tile, P and dS from S_b and dP_b in registers, dS stored
-//     to TMEM as 16-bit pairs; at the end dQ out of TMEM, scaled, to memory.
+//   warps 0-3: first Dq of their row from the dO and O tiles; per tile, P
+//     and dS from S_b and dP_b in registers, dS stored to TMEM as 16-bit
+//     pairs; at the end dQ out of TMEM, scaled, to memory.
 // The double buffer lets the tensor core compute tile j+1's S and dP while
 // the elementwise warps work on tile j.  TMEM: S0 S1 | dP0 dP1 | dQ.
 // Every mbarrier wait is bounded; a wait that runs out records a status and
@@ -61,6 +64,10 @@ struct DqArgs {
     float c2;           // scale * log2(e)
     uint32_t idesc_s;   // M128 N64, both operands K-major
     uint32_t idesc_dq;  // M128 N=D, B MN-major
+    // 0: Dq of each row from bp.delta; 1: computed here, rowsum(dO * O) with
+    // dO from the staged tile; 2: as 1, and written to bp.delta for a dK/dV
+    // launch that follows
+    int self_delta;
 };
 
 template <int D, int DV> struct DqLayout {
@@ -76,6 +83,11 @@ template <int D, int DV> struct DqLayout {
     static constexpr int KV_OFF = QTILE + OTILE;
     static constexpr int BAR_OFF = KV_OFF + kStagesT * STAGE;
     static constexpr int SMEM = 1024 + BAR_OFF + 256;
+    // O's tile (for Dq = rowsum(dO * O) computed in the kernel) is staged in
+    // the last O_STAGES ring slots before their first K / V tile
+    static constexpr int O_STAGES = (OTILE + STAGE - 1) / STAGE;
+    static constexpr int O_OFF = KV_OFF + (kStagesT - O_STAGES) * STAGE;
+    static_assert(O_STAGES < kStagesT, "O tile in the ring");
     static constexpr int S_COL = 0, DP_COL = 128, DQ_COL = 256;  // TMEM columns
     static_assert(DQ_COL + D <= 512, "TMEM budget");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
@@ -90,7 +102,9 @@ enum : int {
     T_TEARDOWN = 6,   // one commit from each MMA-issuing warp
     T_S_EMPTY = 7,    // [2]: the dQ MMAs that read dS out of S_b have completed
     T_KV_FULL = 9,    // [kStagesT] full, then [kStagesT] empty
-    T_NBARS = 9 + 2 * kStagesT,
+    T_O_FULL = 9 + 2 * kStagesT,  // O's tile has landed
+    T_O_FREE = 10 + 2 * kStagesT, // Dq is computed: O's ring slots may take K / V
+    T_NBARS = 11 + 2 * kStagesT,
 };
 
 __device__ __forceinline__ float ex2f(float x) {
@@ -109,6 +123,19 @@ template <> __device__ __forceinline__ uint32_t pack16<__half>(float lo, float h
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// a + the dot product of two 16-bit pairs, in fp32
+template <typename T> __device__ __forceinline__ float dot2_acc(uint32_t x, uint32_t y, float a);
+template <>
+__device__ __forceinline__ float dot2_acc<__nv_bfloat16>(uint32_t x, uint32_t y, float a) {
+    a = fmaf(__uint_as_float(x << 16), __uint_as_float(y << 16), a);
+    return fmaf(__uint_as_float(x & 0xffff0000u), __uint_as_float(y & 0xffff0000u), a);
+}
+template <> __device__ __forceinline__ float dot2_acc<__half>(uint32_t x, uint32_t y, float a) {
+    const float2 fx = __half22float2(*reinterpret_cast<const __half2 *>(&x));
+    const float2 fy = __half22float2(*reinterpret_cast<const __half2 *>(&y));
+    return fmaf(fx.y, fy.y, fmaf(fx.x, fy.x, a));
+}
+
 __device__ __forceinline__ bool warp_wait_t(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                             uint64_t limit_ns) {
     const bool ok = mbar_wait(bar, parity, abort_flag, limit_ns);
@@ -124,9 +151,14 @@ template <typename T, int D, int DV>
 __global__ void __launch_bounds__(kThreadsQ, 1)
     bwd_dq_tc_kernel(const __grid_constant__ DqArgs a, const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV) {
+                     const __grid_constant__ CUtensorMap tmV,
+                     const __grid_constant__ CUtensorMap tmOut) {
     using L = DqLayout<D, DV>;
     extern __shared__ uint8_t smem_t[];
+    // a dK/dV launch that depends on this one (programmatic) may be scheduled
+    // once every CTA has started: it sets up on the SMs the last ones free and
+    // waits for this grid's Dq before reading it
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     const BwdParams &bp = a.bp;
     const AttnParams &p = bp.f;
     const uint64_t wl = p.wait_ns;  // limit of every wait but the drains
@@ -177,6 +209,8 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         mbar_init(bar(T_TEARDOWN), 2);
         mbar_init(bar(T_S_EMPTY), 1);
         mbar_init(bar(T_S_EMPTY + 1), 1);
+        mbar_init(bar(T_O_FULL), 1);
+        mbar_init(bar(T_O_FREE), 128);
         for (int s = 0; s < kStagesT; ++s) {
             mbar_init(kv_full(s), 1);
             mbar_init(kv_empty(s), 1);
@@ -206,9 +240,22 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
                 tma_load_4d(base + L::Q_OFF + c * L::QCH, &tmQ, bar(T_QD_FULL), c * 64, h, qrow, bc);
             for (int c = 0; c < DV / 64; ++c)
                 tma_load_4d(base + L::DO_OFF + c * L::QCH, &tmO, bar(T_QD_FULL), c * 64, h, qrow, bc);
+            if (a.self_delta) {
+                mbar_arrive_expect_tx(bar(T_O_FULL), L::OTILE);
+                for (int c = 0; c < DV / 64; ++c)
+                    tma_load_4d(base + L::O_OFF + c * L::QCH, &tmOut, bar(T_O_FULL), c * 64, h, qrow,
+                                bc);
+            }
             for (int j = 0; j < ntiles; ++j) {
                 const int s = j % kStagesT;
                 const uint32_t ph = (uint32_t)(j / kStagesT) & 1u;
+                // the first K / V tile of a slot O's tile occupies waits for Dq
+                if (a.self_delta && j == kStagesT - L::O_STAGES &&
+                    !mbar_wait(bar(T_O_FREE), 0, abort_flag, wl)) {
+                    raise_abort_t(abort_flag, p.status);
+                    ok = false;
+                    break;
+                }
                 if (!mbar_wait(kv_empty(s), ph ^ 1u, abort_flag, wl)) {
                     raise_abort_t(abort_flag, p.status);
                     ok = false;
@@ -228,6 +275,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
             // drain: every copy issued has landed before the CTA exits (these
             // waits ignore the abort flag: the copies always land)
             mbar_wait_drain(bar(T_QD_FULL), 0);
+            if (a.self_delta) mbar_wait_drain(bar(T_O_FULL), 0);
             for (int s = 0; s < kStagesT; ++s)
                 if (armed & (1u << s)) mbar_wait_drain(kv_full(s), (armed_ph >> s) & 1u);
         }
@@ -331,11 +379,45 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         if (valid) legal_range(qpos, si.Qb, si.Kb, p.window, p.mask, lo, hi);
         const long long row = (si.q_off + qpos) * p.Hq + h;
         float lse2 = 0.f, dl = 0.f;
-        if (hi > lo) {
-            lse2 = p.lse[row] * kLog2e;
+        if (hi > lo) lse2 = p.lse[row] * kLog2e;
+        bool ok = true;
+        if (a.self_delta) {
+            // Dq = rowsum(dO * O) of this row from the staged dO and O tiles (from
+            // memory when the CTA has no key tile and so stages nothing); rows
+            // past the sequence's queries: none
+            float acc = 0.f;
+            auto dot = [&](const uint4 &x, const uint4 &y) {
+                acc = dot2_acc<T>(x.x, y.x, acc);
+                acc = dot2_acc<T>(x.y, y.y, acc);
+                acc = dot2_acc<T>(x.z, y.z, acc);
+                acc = dot2_acc<T>(x.w, y.w, acc);
+            };
+            if (ntiles > 0) {
+                ok = warp_wait_t(bar(T_QD_FULL), 0, abort_flag, wl) &&
+                     warp_wait_t(bar(T_O_FULL), 0, abort_flag, wl);
+                if (!ok && lane == 0) raise_abort_t(abort_flag, p.status);
+                if (valid && ok) {
+#pragma unroll
+                    for (int i = 0; i < DV / 8; ++i) {
+                        // 128-byte swizzled rows, 64 columns a chunk
+                        const int off = (i / 8) * L::QCH + r * 128 + (((i % 8) ^ (r & 7)) << 4);
+                        dot(*reinterpret_cast<const uint4 *>(gbase + L::O_OFF + off),
+                            *reinterpret_cast<const uint4 *>(gbase + L::DO_OFF + off));
+                    }
+                }
+                mbar_arrive(bar(T_O_FREE));
+            } else if (valid) {
+                const T *orow = static_cast<const T *>(p.o) + row * (long long)p.Dv;
+                const T *grow = static_cast<const T *>(bp.dout) + row * (long long)p.Dv;
+                for (int i = 0; i * 8 < p.Dv; ++i)
+                    dot(*reinterpret_cast<const uint4 *>(orow + i * 8),
+                        *reinterpret_cast<const uint4 *>(grow + i * 8));
+            }
+            if (a.self_delta == 2 && valid && ok) bp.delta[row] = acc;
+            dl = acc;
+        } else if (hi > lo) {
             dl = bp.delta[row];
         }
-        bool ok = true;
         for (int j = 0; j < ntiles && ok; ++j) {
             const int bf = j & 1;
             if (!warp_wait_t(bar(T_S_FULL + bf), (uint32_t)(j >> 1) & 1u, abort_flag, wl)) {
@@ -630,6 +712,9 @@ __global__ void __launch_bounds__(kThreadsK, 1)
         };
         if (lane == 0)
             for (int tt = 0; tt < kStagesK && tt < ntiles; ++tt) prefetch_rows(tt);
+        // launched as a programmatic dependent of the dQ kernel (which writes
+        // Dq): Dq is complete and visible once this returns (a no-op otherwise)
+        asm volatile("griddepcontrol.wait;\n" ::: "memory");
         for (int t = 0; t < ntiles && ok; ++t) {
             const int s = t % kStagesK;
             const uint32_t ph = (uint32_t)(t / kStagesK) & 1u;
@@ -958,7 +1043,7 @@ __global__ void __launch_bounds__(kThreadsK, 1)
 }
 
 template <typename T, int D, int DV>
-int launch_kv_t(const BwdParams &bp, bool bf16, cudaStream_t stream) {
+int launch_kv_t(const BwdParams &bp, bool bf16, cudaStream_t stream, bool pdl) {
     using L = KvLayout<D, DV>;
     const AttnParams &p = bp.f;
     KvArgs a;
@@ -1001,8 +1086,18 @@ int launch_kv_t(const BwdParams &bp, bool bf16, cudaStream_t stream) {
         set_error("tcgen05 dK/dV: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         return 3;
     }
-    kern<<<(unsigned)grid, kThreadsK, L::SMEM, stream>>>(a, tq, to, tk, tv);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreadsK);
+    cfg.dynamicSmemBytes = L::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, kern, a, tq, to, tk, tv);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("tcgen05 dK/dV launch: %s", cudaGetErrorString(e));
         return 3;
@@ -1012,20 +1107,21 @@ int launch_kv_t(const BwdParams &bp, bool bf16, cudaStream_t stream) {
 }
 
 template <typename T>
-int launch_kv_dtype(const BwdParams &bp, bool bf16, cudaStream_t stream) {
+int launch_kv_dtype(const BwdParams &bp, bool bf16, cudaStream_t stream, bool pdl) {
     const bool d128 = bp.f.D > 64, dv128 = bp.f.Dv > 64;
-    if (d128 && dv128) return launch_kv_t<T, 128, 128>(bp, bf16, stream);
-    if (!d128 && !dv128) return launch_kv_t<T, 64, 64>(bp, bf16, stream);
-    if (d128) return launch_kv_t<T, 128, 64>(bp, bf16, stream);
-    return launch_kv_t<T, 64, 128>(bp, bf16, stream);
+    if (d128 && dv128) return launch_kv_t<T, 128, 128>(bp, bf16, stream, pdl);
+    if (!d128 && !dv128) return launch_kv_t<T, 64, 64>(bp, bf16, stream, pdl);
+    if (d128) return launch_kv_t<T, 128, 64>(bp, bf16, stream, pdl);
+    return launch_kv_t<T, 64, 128>(bp, bf16, stream, pdl);
 }
 
 template <typename T, int D, int DV>
-int launch_t(const BwdParams &bp, bool bf16, cudaStream_t stream) {
+int launch_t(const BwdParams &bp, bool bf16, cudaStream_t stream, int self_delta) {
     using L = DqLayout<D, DV>;
     const AttnParams &p = bp.f;
     DqArgs a;
     a.bp = bp;
+    a.self_delta = self_delta;
     a.nqt = (p.Q + kRowsT - 1) / kRowsT;
     a.c2 = p.scale * kLog2e;
     a.idesc_s = idesc_f16(bf16, kRowsT, kKeysT, false, false);
@@ -1040,9 +1136,13 @@ int launch_t(const BwdParams &bp, bool bf16, cudaStream_t stream) {
     const uint64_t qrows = padded ? (uint64_t)p.Q : (uint64_t)p.Tq;
     const uint64_t krows = padded ? (uint64_t)p.K : (uint64_t)p.Tk;
     const uint64_t nb = padded ? (uint64_t)p.B : 1;
-    CUtensorMap tq, to, tk, tv;
+    CUtensorMap tq, to, tk, tv, tout;
     int rc = make_tma_map_4d(&tq, p.q, bf16, (uint64_t)p.D, p.Hq, qrows, nb, 1, kRowsT);
     if (!rc) rc = make_tma_map_4d(&to, bp.dout, bf16, (uint64_t)p.Dv, p.Hq, qrows, nb, 1, kRowsT);
+    if (!rc && self_delta)
+        rc = make_tma_map_4d(&tout, p.o, bf16, (uint64_t)p.Dv, p.Hq, qrows, nb, 1, kRowsT);
+    else
+        tout = tq;  // never read
     if (!rc && krows > 0) {
         rc = make_tma_map_4d(&tk, p.k, bf16, (uint64_t)p.D, p.Hkv, krows, nb, 1, kKeysT);
         if (!rc) rc = make_tma_map_4d(&tv, p.v, bf16, (uint64_t)p.Dv, p.Hkv, krows, nb, 1, kKeysT);
@@ -1057,7 +1157,7 @@ int launch_t(const BwdParams &bp, bool bf16, cudaStream_t stream) {
         set_error("tcgen05 dQ: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         return 3;
     }
-    kern<<<(unsigned)grid, kThreadsQ, L::SMEM, stream>>>(a, tq, to, tk, tv);
+    kern<<<(unsigned)grid, kThreadsQ, L::SMEM, stream>>>(a, tq, to, tk, tv, tout);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error("tcgen05 dQ launch: %s", cudaGetErrorString(e));
@@ -1068,12 +1168,12 @@ int launch_t(const BwdParams &bp, bool bf16, cudaStream_t stream) {
 }
 
 template <typename T>
-int launch_dtype(const BwdParams &bp, bool bf16, cudaStream_t stream) {
+int launch_dtype(const BwdParams &bp, bool bf16, cudaStream_t stream, int self_delta) {
     const bool d128 = bp.f.D > 64, dv128 = bp.f.Dv > 64;
-    if (d128 && dv128) return launch_t<T, 128, 128>(bp, bf16, stream);
-    if (!d128 && !dv128) return launch_t<T, 64, 64>(bp, bf16, stream);
-    if (d128) return launch_t<T, 128, 64>(bp, bf16, stream);
-    return launch_t<T, 64, 128>(bp, bf16, stream);
+    if (d128 && dv128) return launch_t<T, 128, 128>(bp, bf16, stream, self_delta);
+    if (!d128 && !dv128) return launch_t<T, 64, 64>(bp, bf16, stream, self_delta);
+    if (d128) return launch_t<T, 128, 64>(bp, bf16, stream, self_delta);
+    return launch_t<T, 64, 128>(bp, bf16, stream, self_delta);
 }
 
 }  // namespace
@@ -1092,14 +1192,14 @@ bool bwd_dkdv_tc_supported(const AttnParams &p, int dtype) {
     return bwd_dq_tc_supported(p, dtype) && p.G >= 1 && p.G <= kRowsK && kRowsK % p.G == 0;
 }
 
-int launch_bwd_dkdv_tc(const BwdParams &bp, int dtype, cudaStream_t stream) {
-    if (dtype == 2) return launch_kv_dtype<__nv_bfloat16>(bp, true, stream);
-    return launch_kv_dtype<__half>(bp, false, stream);
+int launch_bwd_dkdv_tc(const BwdParams &bp, int dtype, cudaStream_t stream, bool after_dq) {
+    if (dtype == 2) return launch_kv_dtype<__nv_bfloat16>(bp, true, stream, after_dq);
+    return launch_kv_dtype<__half>(bp, false, stream, after_dq);
 }
 
-int launch_bwd_dq_tc(const BwdParams &bp, int dtype, cudaStream_t stream) {
-    if (dtype == 2) return launch_dtype<__nv_bfloat16>(bp, true, stream);
-    return launch_dtype<__half>(bp, false, stream);
+int launch_bwd_dq_tc(const BwdParams &bp, int dtype, cudaStream_t stream, int self_delta) {
+    if (dtype == 2) return launch_dtype<__nv_bfloat16>(bp, true, stream, self_delta);
+    return launch_dtype<__half>(bp, false, stream, self_delta);
 }
 
 }  // namespace attn

@@ -75,20 +75,22 @@ int make_tma_map_4d(CUtensorMap *map, const void *ptr, bool bf16, uint64_t d0, u
                     uint64_t d2, uint64_t d3, uint32_t b1, uint32_t b2);
 
 // tcgen05 dQ kernel of the backward (bf16/fp16, D and Dv multiples of 16 in
-// [64, 128], not paged); bp.delta must already hold rowsum(dO * O).
+// [64, 128], not paged).  self_delta 0: bp.delta must already hold
+// rowsum(dO * O); 1: the kernel computes it for its rows; 2: and writes it to
+// bp.delta.
 bool bwd_dq_tc_supported(const AttnParams &p, int dtype);
-int launch_bwd_dq_tc(const BwdParams &bp, int dtype, cudaStream_t stream);
+int launch_bwd_dq_tc(const BwdParams &bp, int dtype, cudaStream_t stream, int self_delta);
 // tcgen05 dK/dV kernel: as bwd_dq_tc_supported, and Hq / Hkv divides 128.
+// after_dq: launched as a programmatic dependent of the dQ launch just before
+// it on the same stream (which writes bp.delta).
 bool bwd_dkdv_tc_supported(const AttnParams &p, int dtype);
-int launch_bwd_dkdv_tc(const BwdParams &bp, int dtype, cudaStream_t stream);
-
-// A second, library-owned stream of the current device (created once).
-int side_stream(cudaStream_t *out);
+int launch_bwd_dkdv_tc(const BwdParams &bp, int dtype, cudaStream_t stream, bool after_dq);
 
 // Backward: rowsum(dO * O), then dK/dV and dQ.  mode 0: the CUDA-core
 // kernels; 1: the mma.sync kernels (bf16/fp16, bwd_mma_supported); 2: the
 // tcgen05 dQ kernel (bwd_dq_tc_supported) and the tcgen05 dK/dV kernel where
-// it applies (bwd_dkdv_tc_supported), the mma.sync one otherwise.
+// it applies (bwd_dkdv_tc_supported; then the dQ kernel computes rowsum(dO * O)
+// and runs first), the mma.sync one otherwise.
 bool bwd_mma_supported(const AttnParams &p, int dtype);
 int launch_bwd(const BwdParams &bp, int dtype, int mode, cudaStream_t stream);
 
