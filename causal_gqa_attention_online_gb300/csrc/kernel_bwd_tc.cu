@@ -222,6 +222,14 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
         tmem_alloc(smem_addr(tmem_slot), 512);
         tmem_relinquish();
     }
+    if (warp == kLoadWarpT && lane == 0 && ntiles > 0) {
+        // the tensor maps' descriptors on their way while the CTA sets up
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmO);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        if (a.self_delta) tma_prefetch_desc(&tmOut);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -677,6 +685,13 @@ __global__ void __launch_bounds__(kThreadsK, 1)
     if (warp == kMmaWarpK) {
         tmem_alloc(smem_addr(tmem_slot), 512);
         tmem_relinquish();
+    }
+    if (warp == kLoadWarpK && lane == 0 && ntiles > 0) {
+        // the tensor maps' descriptors on their way while the CTA sets up
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmO);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
     }
     tc_fence_before();
     __syncthreads();
