@@ -17,8 +17,9 @@
 //   warp 4 (one thread): TMA loads of the Q and dO tiles, of O's tile (into
 //     the last ring slot(s), which take K/V tiles once Dq is computed) and a
 //     ring of K/V tiles;
-//   warp 5 (one thread): S_b = Q K^T and dP_b = dO V^T into TMEM buffer b =
-//     tile mod 3, once the dQ products of tile - 3 have released S_b;
+//   warps 5 and 7 (one thread each): S_b = Q K^T and dP_b = dO V^T into TMEM
+//     buffer b = tile mod 3, once the dQ products of tile - 3 have released
+//     S_b;
 //   warp 6 (one thread): once the elementwise warps have turned a tile into
 //     dS, dQ += dS K with dS read from TMEM (it overwrites S_b);
 //   warps 0-3: first Dq of their row from the dO and O tiles; per tile, P
@@ -55,10 +56,11 @@ constexpr int kRowsT = 128;  // query rows per CTA (MMA M)
 constexpr int kKeysT = 64;   // keys per tile (N of S and dP, contraction of dQ)
 constexpr int kStagesT = 4;  // K/V ring depth
 constexpr int kSBufT = 3;    // S / dP buffers in TMEM
-constexpr int kThreadsQ = 224;  // dQ: warps 0-3 elementwise, 4 TMA, 5 S / dP MMAs, 6 dQ MMAs
+constexpr int kThreadsQ = 256;  // dQ: warps 0-3 elementwise, 4 TMA, 5 S, 6 dQ, 7 dP MMAs
 constexpr int kLoadWarpT = 4;
-constexpr int kMmaWarpT = 5;
+constexpr int kMmaWarpT = 5;  // S MMAs; owns the TMEM allocation
 constexpr int kDqWarpT = 6;
+constexpr int kDpWarpT = 7;
 constexpr int kStatusTimeoutBwdTc = 0x301;
 
 struct DqArgs {
@@ -103,7 +105,7 @@ enum : int {
     T_S_FULL = 1,                   // [kSBufT]
     T_DS_READY = 1 + kSBufT,        // [kSBufT]
     T_DQ_FULL = 1 + 2 * kSBufT,
-    T_TEARDOWN = 2 + 2 * kSBufT,    // one commit from each MMA-issuing warp
+    T_TEARDOWN = 2 + 2 * kSBufT,    // one commit from each of the three MMA-issuing warps
     T_S_EMPTY = 3 + 2 * kSBufT,     // [kSBufT]: the dQ MMAs that read dS out of S_b have completed
     T_KV_FULL = 3 + 3 * kSBufT,     // [kStagesT] full, then [kStagesT] empty
     T_O_FULL = T_KV_FULL + 2 * kStagesT,  // O's tile has landed
@@ -206,12 +208,12 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
     if (threadIdx.x == 0) {
         mbar_init(bar(T_QD_FULL), 1);
         for (int i = 0; i < kSBufT; ++i) {
-            mbar_init(bar(T_S_FULL + i), 1);
+            mbar_init(bar(T_S_FULL + i), 2);  // S and dP commits
             mbar_init(bar(T_DS_READY + i), 128);
             mbar_init(bar(T_S_EMPTY + i), 1);
         }
         mbar_init(bar(T_DQ_FULL), 1);
-        mbar_init(bar(T_TEARDOWN), 2);
+        mbar_init(bar(T_TEARDOWN), 3);
         mbar_init(bar(T_O_FULL), 1);
         mbar_init(bar(T_O_FREE), 128);
         for (int s = 0; s < kStagesT; ++s) {
@@ -290,17 +292,17 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
             for (int s = 0; s < kStagesT; ++s)
                 if (armed & (1u << s)) mbar_wait_drain(kv_full(s), (armed_ph >> s) & 1u);
         }
-    } else if (warp == kMmaWarpT) {
-        // ------------------------------------------------ S / dP MMA issuer
-        // Two issuing warps, one thread each: one thread issuing every MMA of
-        // a tile spends more time issuing than the tensor core spends on them
-        // (the products of a 64-key tile are small), so the dQ products have
-        // a warp of their own; a warp-wide wait per tile costs more than the
-        // wait of one thread.
+    } else if (warp == kMmaWarpT || warp == kDpWarpT) {
+        // ------------------------------------------- S and dP MMA issuers
+        // Three issuing warps, one thread each (S, dP, dQ): one thread issuing
+        // the sixteen N = 64 products of S and dP took ~1550 cycles a tile at
+        // ~100 cycles an issue, three times their tensor time, and a second
+        // thread had already taken the dQ products off it; a warp-wide wait per
+        // tile costs more than the wait of one thread.
         if (lane == 0) {
+            const bool is_s = warp == kMmaWarpT;
             bool ok = ntiles == 0 || mbar_wait(bar(T_QD_FULL), 0, abort_flag, wl);
-            const uint64_t qd = sw128_desc(base + L::Q_OFF, 16, 1024);
-            const uint64_t od = sw128_desc(base + L::DO_OFF, 16, 1024);
+            const uint64_t ad = sw128_desc(base + (is_s ? L::Q_OFF : L::DO_OFF), 16, 1024);
             for (int j = 0; j < ntiles && ok; ++j) {
                 const int s = j % kStagesT, bf = j % kSBufT;
                 if (!mbar_wait(kv_full(s), (uint32_t)(j / kStagesT) & 1u, abort_flag, wl)) {
@@ -315,18 +317,21 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint64_t kd = sw128_desc(stage(s), 16, 1024);
-                const uint64_t vd = sw128_desc(stage(s) + L::KTILE, 16, 1024);
+                if (is_s) {
+                    const uint64_t kd = sw128_desc(stage(s), 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + L::S_COL + bf * kKeysT,
-                           qd + (((kk / 4) * L::QCH + (kk % 4) * 32) >> 4),
-                           kd + (((kk / 4) * L::KCH + (kk % 4) * 32) >> 4), a.idesc_s, kk > 0);
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + L::S_COL + bf * kKeysT,
+                               ad + (((kk / 4) * L::QCH + (kk % 4) * 32) >> 4),
+                               kd + (((kk / 4) * L::KCH + (kk % 4) * 32) >> 4), a.idesc_s, kk > 0);
+                } else {
+                    const uint64_t vd = sw128_desc(stage(s) + L::KTILE, 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < DV / 16; ++kk)
-                    mma_ss(tmem + L::DP_COL + bf * kKeysT,
-                           od + (((kk / 4) * L::QCH + (kk % 4) * 32) >> 4),
-                           vd + (((kk / 4) * L::KCH + (kk % 4) * 32) >> 4), a.idesc_s, kk > 0);
+                    for (int kk = 0; kk < DV / 16; ++kk)
+                        mma_ss(tmem + L::DP_COL + bf * kKeysT,
+                               ad + (((kk / 4) * L::QCH + (kk % 4) * 32) >> 4),
+                               vd + (((kk / 4) * L::KCH + (kk % 4) * 32) >> 4), a.idesc_s, kk > 0);
+                }
                 mma_commit(bar(T_S_FULL + bf));
             }
             if (!ok) raise_abort_t(abort_flag, p.status);
