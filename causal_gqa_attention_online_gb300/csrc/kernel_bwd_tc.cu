@@ -555,9 +555,10 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
 //   dS^T is, with dO and Q read MN-major from the same row tile.
 // At N = 128 every product takes 64 tensor cycles an MMA; 64-row tiles made
 // S^T and dP^T N = 64 products, bound by shared-memory operand reads and by
-// issue.  S^T and dP^T are single-buffered: the next tile's S^T, issued after
-// this tile's dK by the same thread (tcgen05.mma executes in order), writes
-// TMEM only after the dV products have read P^T.
+// issue.  Two threads issue the products (S^T and dP^T in warp 9, dV and dK
+// in warp 10).  S^T and dP^T are single-buffered: the next tile's S^T waits
+// for this tile's dV products to complete (they read P^T over S^T), its dP^T
+// for the dK products (dS^T over dP^T).
 // TMEM: S^T | dP^T | dV | dK.  Per-row LSE, Dq and legal key range ride with
 // each row tile (written by the loader warp, published by the tile's full
 // barrier).
@@ -565,9 +566,12 @@ constexpr int kKeysK = 128;     // keys per CTA (MMA M)
 constexpr int kRowsK = 128;     // rows per tile (N of S^T and dP^T, contraction of dV and dK)
 constexpr int kHalfK = 64;      // rows per elementwise warpgroup
 constexpr int kStagesK = 2;     // row-tile ring
-constexpr int kThreadsK = 384;  // warps 0-7 elementwise (two warpgroups), 8 TMA, 9 MMA, 10-11 idle
+// warps 0-7 elementwise (two warpgroups), 8 TMA, 9 S^T / dP^T MMAs, 10 dV / dK
+// MMAs, 11 idle
+constexpr int kThreadsK = 384;
 constexpr int kLoadWarpK = 8;
 constexpr int kMmaWarpK = 9;
+constexpr int kAccWarpK = 10;
 // Three warps share each SM sub-partition, so a thread may hold 168 registers
 // at launch; the elementwise warps keep 64 fp32 P values across the wait for
 // dP^T and take more from the loader, MMA and idle warps (whole warpgroups).
@@ -607,7 +611,10 @@ enum : int {
     K_ACC_FULL = 7,
     K_TEARDOWN = 8,
     K_ROW_FULL = 9,   // [kStagesK] full, then [kStagesK] empty
-    K_NBARS = 9 + 2 * kStagesK,
+    K_DV_DONE = 9 + 2 * kStagesK,  // the tile's dV products have completed (P^T read)
+    K_DK_DONE = 10 + 2 * kStagesK, // the tile's dK products have completed (dS^T read)
+    K_ROWS_READY = 11 + 2 * kStagesK,  // a tile's rows past the queries are zeroed
+    K_NBARS = 12 + 2 * kStagesK,
 };
 
 struct KvArgs {
@@ -682,7 +689,10 @@ __global__ void __launch_bounds__(kThreadsK, 1)
             mbar_init(bar(K_DS_READY + h), 128);
         }
         mbar_init(bar(K_ACC_FULL), 1);
-        mbar_init(bar(K_TEARDOWN), 1);
+        mbar_init(bar(K_TEARDOWN), 2);  // one commit from each MMA-issuing thread
+        mbar_init(bar(K_DV_DONE), 1);
+        mbar_init(bar(K_DK_DONE), 1);
+        mbar_init(bar(K_ROWS_READY), 1);
         for (int s = 0; s < kStagesK; ++s) {
             mbar_init(row_full(s), 1);
             mbar_init(row_empty(s), 1);
@@ -727,7 +737,7 @@ __global__ void __launch_bounds__(kThreadsK, 1)
         // loaded, and each tile's row statistics (global LSE and Dq loads) are
         // gathered before waiting for its stage: the stage is free only once
         // the previous occupant's products have completed, and a load started
-        // then from DRAM stalled the MMA thread.
+        // then from DRAM stalled the MMA threads.
         auto prefetch_rows = [&](int tt) {
             const int r0 = qrow + qf + tt * PP;
             for (int c = 0; c < D / 64; ++c) tma_prefetch_l2_4d(&tmQ, c * 64, kvh * G, r0, bc);
@@ -800,8 +810,13 @@ __global__ void __launch_bounds__(kThreadsK, 1)
                 if (armed & (1u << s)) mbar_wait_drain(row_full(s), (armed_ph >> s) & 1u);
         }
     } else if (warp == kMmaWarpK) {
-        // ------------------------------------------------------------ MMA issuer
-        // (one thread: a warp-wide wait costs more than the wait of one thread)
+        // ---------------------------------------------- S^T / dP^T MMA issuer
+        // Two issuing threads (S^T and dP^T here, dV and dK in warp 10): one
+        // thread issuing the 32 products of a tile spent more cycles issuing
+        // than the tensor core spent on them.  S^T and dP^T overwrite the
+        // previous tile's P^T / dS^T, so they wait for its dV / dK products to
+        // complete (the other thread's commits).  A warp-wide wait costs more
+        // than the wait of one thread.
         if (lane == 0) {
             bool ok = ntiles == 0 || mbar_wait(bar(K_KV_FULL), 0, abort_flag, wl);
             const uint64_t kd = sw128_desc(base + L::K_OFF, 16, 1024);
@@ -813,9 +828,11 @@ __global__ void __launch_bounds__(kThreadsK, 1)
                     ok = false;
                     break;
                 }
+                if (t > 0 && !mbar_wait(bar(K_DV_DONE), tp ^ 1u, abort_flag, wl)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
-                // S^T and dP^T overwrite the previous tile's P^T / dS^T: issued
-                // after its dV / dK products by this thread
                 const uint64_t qd = sw128_desc(rstage(s), 16, 1024);
                 const uint64_t od = sw128_desc(rstage(s) + L::QTILE, 16, 1024);
 #pragma unroll
@@ -823,6 +840,11 @@ __global__ void __launch_bounds__(kThreadsK, 1)
                     mma_ss(tmem + L::ST_COL, kd + (((kk / 4) * L::KCH + (kk % 4) * 32) >> 4),
                            qd + (((kk / 4) * L::RCH + (kk % 4) * 32) >> 4), a.idesc_s, kk > 0);
                 mma_commit(bar(K_S_FULL));
+                if (t > 0 && !mbar_wait(bar(K_DK_DONE), tp ^ 1u, abort_flag, wl)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < DV / 16; ++kk)
                     mma_ss(tmem + L::DPT_COL, vd + (((kk / 4) * L::KCH + (kk % 4) * 32) >> 4),
@@ -831,7 +853,8 @@ __global__ void __launch_bounds__(kThreadsK, 1)
                 // rows of the tile past the sequence's queries may hold anything
                 // (NaN included): their P and dS are 0, and their Q and dO rows
                 // are zeroed so that 0 * row stays 0 -- once S^T and dP^T, which
-                // read them, have completed
+                // read them, have completed, and before the dV / dK products
+                // (the other thread waits for K_ROWS_READY on such tiles)
                 const int pos0 = qf + t * PP;
                 const int nreal = min(kRowsK, max(0, (si.Qb - pos0) * G));
                 if (nreal < kRowsK) {
@@ -846,6 +869,34 @@ __global__ void __launch_bounds__(kThreadsK, 1)
                             *reinterpret_cast<uint4 *>(rt + c * L::RCH + nreal * 128 + i * 16) =
                                 make_uint4(0, 0, 0, 0);
                     fence_proxy_async_smem();
+                    mbar_arrive(bar(K_ROWS_READY));
+                }
+            }
+            if (!ok) raise_abort_t(abort_flag, p.status);
+            mma_commit(bar(K_TEARDOWN));
+            mbar_wait_drain(bar(K_TEARDOWN), 0);  // ignores the abort flag
+        }
+        __syncwarp();
+    } else if (warp == kAccWarpK) {
+        // --------------------------------------------------- dV / dK MMA issuer
+        if (lane == 0) {
+            bool ok = true;
+            uint32_t nz = 0;  // tiles with zeroed rows so far (K_ROWS_READY phases)
+            for (int t = 0; t < ntiles && ok; ++t) {
+                const int s = t % kStagesK;
+                const uint32_t tp = (uint32_t)t & 1u;
+                if (!mbar_wait(row_full(s), (uint32_t)(t / kStagesK) & 1u, abort_flag, wl)) {
+                    ok = false;
+                    break;
+                }
+                const int pos0 = qf + t * PP;
+                const int nreal = min(kRowsK, max(0, (si.Qb - pos0) * G));
+                if (nreal < kRowsK) {
+                    if (!mbar_wait(bar(K_ROWS_READY), nz & 1u, abort_flag, wl)) {
+                        ok = false;
+                        break;
+                    }
+                    ++nz;
                 }
                 // dV += P^T dO, half by half as the warpgroups deliver P^T
                 const uint64_t omn = sw128_desc(rstage(s) + L::QTILE, L::RCH, 1024);
@@ -862,6 +913,7 @@ __global__ void __launch_bounds__(kThreadsK, 1)
                                (t > 0 || h > 0 || kk > 0) ? 1u : 0u);
                 }
                 if (!ok) break;
+                mma_commit(bar(K_DV_DONE));
                 // dK += dS^T Q, likewise
                 const uint64_t qmn = sw128_desc(rstage(s), L::RCH, 1024);
                 for (int h = 0; h < 2 && ok; ++h) {
@@ -877,6 +929,9 @@ __global__ void __launch_bounds__(kThreadsK, 1)
                                (t > 0 || h > 0 || kk > 0) ? 1u : 0u);
                 }
                 if (!ok) break;
+                mma_commit(bar(K_DK_DONE));
+                // the stage's S^T / dP^T products completed before its dS^T was
+                // written, so this commit covers every read of the stage
                 mma_commit(row_empty(s));
                 if (t == ntiles - 1) mma_commit(bar(K_ACC_FULL));
             }
