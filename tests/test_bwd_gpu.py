@@ -338,3 +338,35 @@ def test_sdpa_example_shape_forward_and_backward():
         _, ref_k, ref_v = oracle.attn_bwd_sampled(qf, kf, vf, gf, key_block=(b, kh, S - 64, S), **kw)
         compare_one("bf16", dkc[b, S - 64:, kh], ref_k, f"SDPA example dk b={b} h={kh}")
         compare_one("bf16", dvc[b, S - 64:, kh], ref_v, f"SDPA example dv b={b} h={kh}")
+
+
+@pytest.mark.parametrize("Hq,Hkv,launches", [(8, 2, 2), (6, 2, 3)])
+def test_bwd_tcgen05_launch_sequence(Hq, Hkv, launches):
+    """The tcgen05 backward's launches: with the tcgen05 dK/dV kernel (G =
+    Hq / Hkv divides 128) two, the dQ kernel -- which computes each of its
+    rows' Dq = rowsum(dO * O) from the O tile it stages and writes it -- then
+    the dK/dV kernel as its programmatic dependent; with the mma.sync dK/dV
+    kernel (G = 3) three, the Dq launch first.  Gradients against the oracle
+    in both cases, padded rows with NaN."""
+    from causal_gqa_attention_online_gb300 import binding
+    g = np.random.default_rng(Hq)
+    sq = g.integers(1, 261, size=2).astype(np.int32)
+    sk = np.maximum(sq, g.integers(1, 301, size=2)).astype(np.int32)
+    inp = synth.make_padded(2, Hq, Hkv, 260, 300, 128, 128, "bf16", seed=81, seqlens_q=sq,
+                            seqlens_k=sk, pad_value=NAN)
+    dout = synth.make_dout(inp, seed=82, pad_value=NAN)
+    dev = torch.device("cuda")
+    q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+    tsq, tsk = torch.from_numpy(sq).to(dev), torch.from_numpy(sk).to(dev)
+    o, lse = attn_fwd(q, k, v, seqlens_q=tsq, seqlens_k=tsk, scale=inp.scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    torch.cuda.synchronize()
+    n0 = binding.kernel_launches()
+    attn_bwd(q, k, v, o, lse, dout.to(dev), dq, dk, dv, seqlens_q=tsq, seqlens_k=tsk,
+             scale=inp.scale, algo="tcgen05")
+    torch.cuda.synchronize()
+    assert binding.kernel_launches() - n0 == launches
+    got = tuple(t.float().cpu().numpy() for t in (dq, dk, dv))
+    ref = oracle_bwd(inp, dout)
+    compare("bf16", got, ref, f"launch sequence Hq={Hq} Hkv={Hkv}",
+            structural_zeros(2, 260, 300, sq, sk, 0, 0))
